@@ -1,0 +1,159 @@
+"""Thin ctypes binding to libpnq.so: argument marshalling only, same names as the C ABI.
+
+Every computation runs in the library's CUDA kernels. There is no fallback: if the
+library is missing or fails to load, the first call raises ``PnqError``.
+"""
+from __future__ import annotations
+
+import ctypes
+import enum
+import os
+
+PN3T, PN4T, NVFP4 = 124, 125, 1004
+BLOCK_WEIGHTS = {PN3T: 80, PN4T: 64}
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "libpnq.so")
+
+
+class Status(enum.IntEnum):
+    OK = 0
+    ERR_TYPE = -1
+    ERR_SHAPE = -2
+    ERR_NULL = -3
+    ERR_ALIGN = -4
+    ERR_CUDA = -5
+    ERR_DEVICE = -6
+
+
+class PnqError(RuntimeError):
+    def __init__(self, what: str, status: int | None = None):
+        self.status = status
+        super().__init__(what if status is None else f"{what}: {Status(status).name} ({status})")
+
+
+class pnq_nvfp4_weights(ctypes.Structure):
+    _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p), ("global_scale", ctypes.c_float)]
+
+
+_lib = None
+
+
+def lib_path() -> str:
+    return _LIB_PATH
+
+
+def lib() -> ctypes.CDLL:
+    """Load libpnq.so (built by ``__graft_entry__.build()``); raise if it is not there."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise PnqError(f"{_LIB_PATH} is not built; run `python -c 'import __graft_entry__ as g; g.build()'`")
+        try:
+            L = ctypes.CDLL(_LIB_PATH)
+        except OSError as e:
+            raise PnqError(f"cannot load {_LIB_PATH}: {e}") from e
+        P, I64, I = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+        L.pnq_gemv.restype = I
+        L.pnq_gemv.argtypes = [I, P, I64, I64, P, I, P, P]
+        L.pnq_dequantize_row.restype = I
+        L.pnq_dequantize_row.argtypes = [I, P, I64, I64, P, P]
+        L.pnq_validate_row.restype = I
+        L.pnq_validate_row.argtypes = [I, P, I64, I64, P, P]
+        L.pnq_device_error.restype = I
+        L.pnq_device_error.argtypes = [ctypes.POINTER(ctypes.c_int32)]
+        L.pnq_version.restype = ctypes.c_char_p
+        L.pnq_version.argtypes = []
+        _lib = L
+    return _lib
+
+
+def _check(rc: int, what: str) -> None:
+    if rc != 0:
+        raise PnqError(what, rc)
+
+
+def nvfp4_weights(codes_ptr: int, scales_ptr: int, global_scale: float) -> pnq_nvfp4_weights:
+    return pnq_nvfp4_weights(codes_ptr, scales_ptr, float(global_scale))
+
+
+def _w_arg(type_: int, W):
+    """PN: W is a device address (int). NVFP4: W is a pnq_nvfp4_weights (passed by host pointer)."""
+    if type_ == NVFP4:
+        if not isinstance(W, pnq_nvfp4_weights):
+            raise TypeError("NVFP4 weights must be a pnq_nvfp4_weights descriptor")
+        return ctypes.byref(W)
+    return ctypes.c_void_p(W)
+
+
+# ---- raw entry points (integer addresses; stream as an integer handle) ----------------
+
+def gemv_ptr(type_: int, W, N: int, K: int, X: int, M: int, Y: int, stream: int = 0) -> int:
+    return lib().pnq_gemv(type_, _w_arg(type_, W), N, K, ctypes.c_void_p(X), M, ctypes.c_void_p(Y),
+                          ctypes.c_void_p(stream))
+
+
+def dequantize_row_ptr(type_: int, W, n_rows: int, K: int, out: int, stream: int = 0) -> int:
+    return lib().pnq_dequantize_row(type_, _w_arg(type_, W), n_rows, K, ctypes.c_void_p(out),
+                                    ctypes.c_void_p(stream))
+
+
+def validate_row_ptr(type_: int, W, n_rows: int, K: int, flags: int, stream: int = 0) -> int:
+    return lib().pnq_validate_row(type_, _w_arg(type_, W), n_rows, K, ctypes.c_void_p(flags),
+                                  ctypes.c_void_p(stream))
+
+
+def device_error() -> int:
+    code = ctypes.c_int32(0)
+    rc = lib().pnq_device_error(ctypes.byref(code))
+    if rc not in (0, int(Status.ERR_DEVICE)):
+        raise PnqError("pnq_device_error", rc)
+    return int(code.value)
+
+
+# ---- torch tensor wrappers (marshalling only) ----------------------------------------------
+
+def _stream_handle(stream) -> int:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream)
+
+
+def _weights(type_: int, W):
+    if type_ == NVFP4:
+        codes, scales, g = W
+        return nvfp4_weights(codes.data_ptr(), scales.data_ptr(), g)
+    return W.data_ptr()
+
+
+def gemv(type_: int, W, X, N: int, K: int, Y=None, stream=None):
+    """Y[m][n] = sum_k W[n][k] X[m][k]. W: uint8 CUDA tensor of PN blocks, or (codes, scales, g)
+    for NVFP4. X: CUDA [M][K] fp32 (PN) or bf16 (NVFP4). Returns Y (CUDA fp32 [M][N])."""
+    import torch
+    M = X.shape[0] if X.dim() == 2 else 1
+    if Y is None:
+        Y = torch.empty((M, N), dtype=torch.float32, device=X.device)
+    _check(gemv_ptr(type_, _weights(type_, W), N, K, X.data_ptr(), M, Y.data_ptr(), _stream_handle(stream)),
+           "pnq_gemv")
+    return Y
+
+
+def dequantize_row(type_: int, W, n_rows: int, K: int, out=None, stream=None):
+    import torch
+    if out is None:
+        dev = W[0].device if type_ == NVFP4 else W.device
+        out = torch.empty((n_rows, K), dtype=torch.float32, device=dev)
+    _check(dequantize_row_ptr(type_, _weights(type_, W), n_rows, K, out.data_ptr(), _stream_handle(stream)),
+           "pnq_dequantize_row")
+    return out
+
+
+def validate_row(type_: int, W, n_rows: int, K: int, flags=None, stream=None):
+    import torch
+    if flags is None:
+        dev = W[0].device if type_ == NVFP4 else W.device
+        flags = torch.empty((n_rows,), dtype=torch.int32, device=dev)
+    _check(validate_row_ptr(type_, _weights(type_, W), n_rows, K, flags.data_ptr(), _stream_handle(stream)),
+           "pnq_validate_row")
+    return flags

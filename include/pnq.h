@@ -1,0 +1,125 @@
+/*
+ * pnq.h -- C ABI of libpnq: decode-time products straight from block-quantized
+ * weights (pn3t, pn4t, NVFP4 W4A16) on sm_103a (GB300).
+ *
+ * Conventions shared by every entry point
+ *   - Returns PNQ_OK (0) or a negative pnq_status. Nothing aborts; no kernel traps.
+ *   - Device pointers are plain CUDA device addresses owned by the caller. The library
+ *     allocates no device memory and keeps no per-call state.
+ *   - Calls are asynchronous and ordered on `stream` (0 = the legacy default stream).
+ *     Argument errors are reported before anything is launched; a launch failure is
+ *     reported as PNQ_ERR_CUDA. Results are valid once the stream reaches the call.
+ *   - Matrices are row-major with the ggml row convention: weight row n holds the K
+ *     weights that multiply x[m][0..K), so Y[m][n] = sum_k W[n][k] * X[m][k].
+ *   - Y / out / flags are overwritten, never accumulated into.
+ *
+ * Weight formats (citations name the page and its section)
+ *   PNQ_PN3T (124), PNQ_PN4T (125): "PN weight format" (tensorless docs, reference/pn-format),
+ *     sections Types, Block layout and Value. A row of K weights is K/BLK consecutive
+ *     34-byte blocks (BLK = 80 for pn3t, 64 for pn4t); rows are back to back, so row n
+ *     starts at byte n * (K/BLK) * 34. A block is d (fp16, little-endian, signed) at bytes
+ *     0..1 and eight little-endian u32 words at bytes 2..33; element e is in word
+ *     e / CPW (CPW = 10 or 8) at shift BITS*(t>>1) + 16*(t&1), t = e mod CPW, and
+ *     decodes to w = d * (n - z), z = 4 (pn3t) or 8 (pn4t). W needs only 2-byte
+ *     alignment: odd blocks' words are not 4-byte aligned.
+ *   PNQ_NVFP4 (1004, a library id; the pages assign none): TandemLLM "Quantisation and
+ *     profiles", section NVFP4, and NInfer "tensor-formats.md" section 3.3. Weight
+ *     w[n][k] = e2m1(code[n][k]) * e4m3fn(scale[n][k/16]) * global_scale, with codes
+ *     packed two per byte, low nibble = even k, [N][K/2] row-major, and scales one
+ *     E4M3FN byte per 16 weights along K, [N][K/16] row-major. global_scale is a
+ *     multiplier (the TandemLLM reading).
+ *
+ * Fast paths (taken automatically, never required)
+ *   PN: W 16-byte aligned and (K/BLK) % 8 == 0.  NVFP4: codes and scales 16-byte
+ *   aligned and K % 256 == 0. Other layouts run a slower path with identical results.
+ */
+#ifndef PNQ_H
+#define PNQ_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum pnq_type { PNQ_PN3T = 124, PNQ_PN4T = 125, PNQ_NVFP4 = 1004 };
+
+enum pnq_status {
+    PNQ_OK = 0,
+    PNQ_ERR_TYPE = -1,   /* unknown type id */
+    PNQ_ERR_SHAPE = -2,  /* K not a positive multiple of BLK (PN) or 16 (NVFP4); N < 0;
+                            M outside [1, 16]; size overflow */
+    PNQ_ERR_NULL = -3,   /* a required pointer is NULL */
+    PNQ_ERR_ALIGN = -4,  /* a pointer misses its minimum alignment (see each call) */
+    PNQ_ERR_CUDA = -5,   /* a CUDA call failed (launch error, no device, bad stream) */
+    PNQ_ERR_DEVICE = -6  /* a kernel gave up on an internal wait (see pnq_device_error) */
+};
+
+/* NVFP4 weight descriptor, passed by HOST pointer as the W argument when type ==
+ * PNQ_NVFP4. codes and scales are device pointers (1-byte alignment suffices). */
+typedef struct pnq_nvfp4_weights {
+    const uint8_t* codes;   /* device, [N][K/2] E2M1 pairs, low nibble = even k */
+    const uint8_t* scales;  /* device, [N][K/16] E4M3FN */
+    float global_scale;     /* host value, multiplies every weight */
+} pnq_nvfp4_weights;
+
+/*
+ * pnq_gemv -- Y[m][n] = sum_k W[n][k] * X[m][k] for m < M, n < N, fp32 accumulation.
+ * The decode-step product of the pages ("PN weight format", section "Where PN runs":
+ * PN tensors use their own GEMV kernels; TandemLLM "Quantisation and profiles",
+ * section NVFP4: the W4A16 kernel unpacks codes in registers before the multiply).
+ *   type  PNQ_PN3T, PNQ_PN4T or PNQ_NVFP4.
+ *   W     PN: device pointer to N*(K/BLK)*34 bytes, >= 2-byte aligned (else PNQ_ERR_ALIGN).
+ *         NVFP4: host pointer to a pnq_nvfp4_weights.
+ *   N     output rows (>= 0; N == 0 launches nothing).  K: inner dimension.
+ *   X     device, [M][K] row-major: fp32 for PN (4-byte aligned), bf16 for NVFP4
+ *         (2-byte aligned). Finite values; any magnitude is accepted.
+ *   M     1..16 activation rows (1..4 per matrix-vector pass, 5..16 small batch).
+ *   Y     device, [M][N] fp32, 4-byte aligned; must not overlap W or X.
+ * Accuracy: |Y - Y_exact| <= 1e-5 * sum_k |W[n][k] X[m][k]| + 1e-6 for finite inputs,
+ * where Y_exact is the fp64 sum over the exactly decoded weights. Weights that fail
+ * pnq_validate_row give unspecified (but memory-safe) results.
+ */
+int pnq_gemv(int type, const void* W, int64_t N, int64_t K, const void* X, int M, float* Y,
+             cudaStream_t stream);
+
+/*
+ * pnq_dequantize_row -- out[r][k] = the fp32 weight, bit-exact:
+ *   PN: fp32(d) * fp32(n - z), exact ("PN weight format", section Value: both steps exact
+ *   in fp32; code z with negative d gives -0.0). NVFP4: e2m1 * e4m3 (exact) times the
+ *   global scale, rounded once to nearest-even fp32. A non-finite d or a NaN scale gives
+ *   NaN/inf of the IEEE product (bit patterns of NaNs are not specified).
+ *   W      as for pnq_gemv (n_rows rows).   out: device fp32 [n_rows][K], 4-byte aligned.
+ */
+int pnq_dequantize_row(int type, const void* W, int64_t n_rows, int64_t K, float* out,
+                       cudaStream_t stream);
+
+/*
+ * pnq_validate_row -- flags[r] = 1 if row r is invalid, else 0.
+ *   PN ("PN weight format", section Validation): any block's d is an fp16 NaN or infinity,
+ *   or (pn3t) bit 15 or bit 31 of any word is set.
+ *   NVFP4 ("tensor-formats.md" section 3.3): any scale byte has its sign bit set (negative
+ *   or -0) or is NaN (0x7F / 0xFF), or global_scale is not finite and > 0 (then every row).
+ *   W as for pnq_gemv.   flags: device int32 [n_rows], 4-byte aligned.
+ */
+int pnq_validate_row(int type, const void* W, int64_t n_rows, int64_t K, int32_t* flags,
+                     cudaStream_t stream);
+
+/*
+ * pnq_device_error -- reads and clears the library's device error word on the current
+ * device (synchronous: waits for the device). *code = 0 when no kernel has given up on a
+ * bounded internal wait since the last call; otherwise the nonzero site code of the first
+ * one (1: a consumer's wait for data, 2: the producer's wait for a free stage, 3: the final
+ * wait for copies in flight), and the call returns PNQ_ERR_DEVICE. Other returns: PNQ_OK,
+ * PNQ_ERR_NULL, PNQ_ERR_CUDA. (Library plumbing; the pages define no such call.)
+ */
+int pnq_device_error(int32_t* code);
+
+/* Library version string (static storage). */
+const char* pnq_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PNQ_H */
