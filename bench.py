@@ -1,0 +1,396 @@
+#!/usr/bin/env python3
+"""Decode-step benchmark for libpnq on GB300.
+
+Workload: a Qwen-27B-shaped decode step, 64 layers x 7 projections, every projection a
+separate pnq_gemv call (pn3t gate/up [17408x5120], q [12288x5120]; pn4t k/v [1024x5120],
+o [5120x6144], down [5120x17408]); 11.0 GB of weights generated on the device from a seed
+(codes uniform, d = fp16(+-|N(0, 0.003)|), pn3t reserved bits clear); x ~ N(0, 1) fp32;
+M = 1 by default. One step = all 448 GEMVs, captured once in a CUDA graph and replayed.
+The weights are 85x the L2, so every replay reads them from HBM (no flush needed).
+
+Reported (one JSON line from rank 0): weight GB/s over the step (value), us per step,
+fraction of the measured HBM copy bandwidth, an end-to-end figure through the C ABI with
+the step's activations copied from pinned host memory and the last output copied back,
+the dominant kernel's roofline measured with CUDA events, SM clocks sampled during the
+timed region, and the CPU oracle on a bounded sample of the same workload.
+
+--impl reference times the CPU oracle (oracle/) on the same workload, one sampled layer
+per step. With N > 1 (torchrun), every rank runs an independent replica of the step
+(the GEMV has no exchange step) and value is the bytes of all ranks over the slowest rank.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+PN3T, PN4T = 124, 125
+BLK = {PN3T: 80, PN4T: 64}
+# name, type, N, K
+PROJECTIONS = [("attn_q", PN3T, 12288, 5120), ("attn_k", PN4T, 1024, 5120), ("attn_v", PN4T, 1024, 5120),
+               ("attn_o", PN4T, 5120, 6144), ("ffn_gate", PN3T, 17408, 5120), ("ffn_up", PN3T, 17408, 5120),
+               ("ffn_down", PN4T, 5120, 17408)]
+METRIC = "GEMV weight GB/s and % of GB300 HBM peak at M=1; us per 27B-shaped decode step"
+SEED = 20261202
+
+
+def row_bytes(t, K):
+    return K // BLK[t] * 34
+
+
+def layer_bytes():
+    return sum(N * row_bytes(t, K) for _, t, N, K in PROJECTIONS)
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# ---------------------------------------------------------------------------- helpers
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(prefix="pnq_clocks_", suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                                          "-i", str(self.gpu), "-lms", "100"], stdout=self.fh,
+                                         stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        loaded = [s for s in sm if mx and s > 0.5 * max(mx)] or sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+def kernel_source_digest():
+    h = hashlib.sha256()
+    for fn in ("pnq_gemv_mma.cu", "pnq_device.cuh"):
+        with open(os.path.join(ROOT, "block_quantized_weight_pn3t_gb300", "csrc", fn), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel_tag: str):
+    """dram bytes per launch for the dominant kernel from the committed ncu summary, or None when
+    the summary is missing or was taken on a different kernel source."""
+    path = os.path.join(ROOT, "profiles", f"{kernel_tag}.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m_src = re.search(r"kernel_source_digest:\s*`?([0-9a-f]+)", text)
+    m_tr = re.search(r"traffic_bytes_per_launch:\s*`?([0-9.e+]+)", text)
+    if not m_src or not m_tr or m_src.group(1) != kernel_source_digest():
+        return None
+    return float(m_tr.group(1))
+
+
+def dist_info():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# ----------------------------------------------------------------------- CPU oracle legs
+
+def host_layer(layer: int):
+    """One layer's weights regenerated on the host (identical bytes to the device replica)."""
+    from block_quantized_weight_pn3t_gb300 import synth
+    out = []
+    for p, (name, t, N, K) in enumerate(PROJECTIONS):
+        out.append(synth.pn_random_blocks(t, N, K, seed=SEED, stream=layer * 8 + p).numpy())
+    return out
+
+
+def host_x(M):
+    from block_quantized_weight_pn3t_gb300 import synth
+    return {K: synth.activations(M, K, seed=SEED + K) for K in sorted({K for *_, K in PROJECTIONS})}
+
+
+def oracle_layer(oracle, layer_w, xs):
+    nbytes = 0
+    for (name, t, N, K), W in zip(PROJECTIONS, layer_w):
+        oracle.gemv(t, W, N, K, xs[K])
+        nbytes += W.nbytes
+    return nbytes
+
+
+def cpu_baseline(M: int, budget_s: float = 12.0):
+    """The oracle (single-threaded C, fp64) on whole sampled layers until ~budget_s of CPU time."""
+    import oracle
+    oracle.lib()
+    xs = host_x(M)
+    nbytes, elapsed, layers = 0, 0.0, 0
+    while elapsed < budget_s and layers < 64:
+        w = host_layer(layers)
+        t0 = time.perf_counter()
+        nbytes += oracle_layer(oracle, w, xs)
+        elapsed += time.perf_counter() - t0
+        layers += 1
+    return {"value": round(nbytes / elapsed / 1e9, 5), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"layers 0..{layers - 1} of 64 (all 7 projections, {nbytes / 1e6:.0f} MB of weights), M={M}, "
+                      f"{elapsed:.1f} s of single-thread fp64 CPU work"}
+
+
+def run_reference(args):
+    world, rank, _ = dist_info()
+    if rank != 0:
+        return
+    import oracle
+    oracle.lib()
+    xs = host_x(args.m)
+    w = host_layer(0)
+    for _ in range(args.warmup):
+        oracle_layer(oracle, w, xs)
+    t0 = time.perf_counter()
+    nbytes = 0
+    for _ in range(args.steps):
+        nbytes += oracle_layer(oracle, w, xs)
+    dt = time.perf_counter() - t0
+    value = nbytes / dt / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 5), "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "qwen27b-decode-step-64x7", "M": args.m,
+                       "sample": "one of the 64 layers (all 7 projections) per step"},
+            "cpu_baseline": {"value": round(value, 5), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": f"layer 0 of 64 (all 7 projections, {layer_bytes() / 1e6:.0f} MB), "
+                                       f"M={args.m}, {args.steps} steps"},
+            "e2e": {"value": round(value, 5), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------------------- GPU arm
+
+def run_ours(args):
+    import block_quantized_weight_pn3t_gb300 as pnq
+    from block_quantized_weight_pn3t_gb300 import synth
+
+    world, rank, local = dist_info()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU for the libpnq arm")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+    pnq.lib()
+    M, L = args.m, args.layers
+
+    # ---- inputs resident in HBM: weights, activations, outputs
+    weights = []  # [layer][proj] -> uint8 tensor
+    for layer in range(L):
+        weights.append([synth.pn_random_blocks(t, N, K, seed=SEED, stream=layer * 8 + p, device=dev)
+                        for p, (_, t, N, K) in enumerate(PROJECTIONS)])
+    step_bytes = L * layer_bytes()
+    xs_host = host_x(M)
+    xs = {K: torch.from_numpy(v).to(dev) for K, v in xs_host.items()}
+    ys = [torch.empty((M, N), dtype=torch.float32, device=dev) for (_, _, N, _) in PROJECTIONS]
+    torch.cuda.synchronize()
+
+    stream = torch.cuda.Stream(device=dev)
+    calls = []
+    for layer in range(L):
+        for p, (_, t, N, K) in enumerate(PROJECTIONS):
+            calls.append((t, weights[layer][p].data_ptr(), N, K, xs[K].data_ptr(), ys[p].data_ptr()))
+
+    def step(s):
+        h = s.cuda_stream
+        for t, w, N, K, x, y in calls:
+            rc = pnq.gemv_ptr(t, w, N, K, x, M, y, h)
+            if rc != 0:
+                raise pnq.PnqError("pnq_gemv", rc)
+
+    # eager warm-up (sets kernel attributes once), then capture one step in a graph
+    with torch.cuda.stream(stream):
+        step(stream)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        step(torch.cuda.current_stream())
+    torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+
+    # ---- timed region: K graph replays, events on the replay stream
+    sampler = ClockSampler(local)
+    sampler.start()
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(args.steps):
+            graph.replay()
+        ev1.record(stream)
+    torch.cuda.synchronize()
+    if pg:
+        pg.barrier()
+    ms = ev0.elapsed_time(ev1) / args.steps
+    clocks = sampler.stop()
+
+    # ---- end to end through the C ABI: activations from pinned host memory, last output back
+    xs_pinned = {K: torch.from_numpy(v).pin_memory() for K, v in xs_host.items()}
+    y_last = torch.empty((M, PROJECTIONS[-1][2]), dtype=torch.float32).pin_memory()
+    h2d = sum(v.numel() * 4 for v in xs_pinned.values())
+    d2h = y_last.numel() * 4
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def e2e_step():
+        for K, v in xs_pinned.items():
+            xs[K].copy_(v, non_blocking=True)
+        graph.replay()
+        y_last.copy_(ys[-1], non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            e2e_step()
+        stream.synchronize()
+        if pg:
+            pg.barrier()
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    ms_e2e = e0.elapsed_time(e1) / args.steps
+
+    # ---- dominant kernel (pn3t, M=1 tensor-core GEMV): events around each launch, back to back
+    dom = [(t, w, N, K, x, y) for (t, w, N, K, x, y) in calls if t == PN3T]
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(2 * len(dom))]
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(50_000_000)  # keep the GPU busy while the launches are queued
+        for i, (t, w, N, K, x, y) in enumerate(dom):
+            evs[2 * i].record(stream)
+            pnq.gemv_ptr(t, w, N, K, x, M, y, stream.cuda_stream)
+            evs[2 * i + 1].record(stream)
+    torch.cuda.synchronize()
+    dur_ms = [evs[2 * i].elapsed_time(evs[2 * i + 1]) for i in range(len(dom))]
+    dom_bytes = sum(N * row_bytes(t, K) for (t, _, N, K, _, _) in dom)
+    dom_gbs = dom_bytes / (sum(dur_ms) * 1e-3) / 1e9
+    peak, peak_kind = measured_peaks()
+    traffic = profiled_traffic("pn3t_gemv_m1_decode_step") if M == 1 else None
+
+    err = pnq.device_error()
+    if err:
+        raise SystemExit(f"libpnq recorded a device error (site {err})")
+
+    # ---- aggregate over ranks (replicas): bytes of all ranks / slowest rank
+    ms_max, ms_e2e_max = ms, ms_e2e
+    if pg:
+        t = torch.tensor([ms, ms_e2e], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        ms_max, ms_e2e_max = float(t[0]), float(t[1])
+    value = world * step_bytes / (ms_max * 1e-3) / 1e9
+    e2e_value = world * step_bytes / (ms_e2e_max * 1e-3) / 1e9
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_max, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f16-mma/f32-acc", "data": "synthetic",
+            "config": {"workload": "qwen27b-decode-step-64x7", "layers": L, "M": M,
+                       "projections": {n: f"{'pn3t' if t == PN3T else 'pn4t'} {N}x{K}" for n, t, N, K in PROJECTIONS},
+                       "weight_bytes_per_step": step_bytes, "us_per_step": round(ms_max * 1e3, 2),
+                       "hbm_fraction": round(value / world / peak, 4),
+                       "l2": "inputs larger than L2 (weights 85x L2 per step); no flush",
+                       "graph": "one CUDA graph per step, 448 pnq_gemv launches", "parallelism": f"replicas x{world}"},
+            "roofline": {"bound": "hbm", "achieved": round(dom_gbs, 2), "peak": peak, "unit": "GB/s",
+                         "frac": round(dom_gbs / peak, 4), "traffic": traffic,
+                         "kernel": "gemv_mma_kernel<pn3t, M<=4>", "launches": len(dom),
+                         "algorithmic_bytes_per_launch": round(dom_bytes / len(dom)),
+                         "avg_launch_us": round(sum(dur_ms) / len(dur_ms) * 1e3, 3),
+                         "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({peak_kind})"},
+            "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": round(ms_e2e_max, 4)},
+            "gpu_launches": args.steps * len(calls),
+            "clocks": clocks,
+        }
+        if not args.no_cpu_baseline and world == 1:
+            line["cpu_baseline"] = cpu_baseline(M)
+        print(json.dumps(line), flush=True)
+    if pg:
+        pg.barrier()
+        pg.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--m", type=int, default=1, help="activation rows (1..16)")
+    ap.add_argument("--layers", type=int, default=64)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

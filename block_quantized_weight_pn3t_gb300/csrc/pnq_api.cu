@@ -1,0 +1,163 @@
+// pnq_api.cu -- the C ABI declared in include/pnq.h: argument checks, kernel choice, status codes.
+#include "pnq.h"
+#include "pnq_internal.h"
+
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+
+// Device error word: 0, or the site code of the first bounded wait that gave up (one copy per
+// device that loads the library).
+__device__ int g_pnq_error_word = 0;
+
+namespace pnq {
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+int current_device() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+    return dev;
+}
+
+int* error_word() {
+    static int* ptrs[kMaxDevices] = {};
+    const int dev = current_device();
+    if (dev < 0) return nullptr;
+    if (!ptrs[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_pnq_error_word) != cudaSuccess) return nullptr;
+        ptrs[dev] = static_cast<int*>(p);
+    }
+    return ptrs[dev];
+}
+
+// "auto" (default), "simt" (generic path only) or "mma" (fast path whenever eligible).
+int forced_kernel() {
+    static int mode = [] {
+        const char* s = std::getenv("PNQ_FORCE_KERNEL");
+        if (s && std::strcmp(s, "simt") == 0) return 1;
+        if (s && std::strcmp(s, "mma") == 0) return 2;
+        return 0;
+    }();
+    return mode;
+}
+
+int block_weights(int type) {
+    if (type == PNQ_PN3T) return 80;
+    if (type == PNQ_PN4T) return 64;
+    return 0;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int map_cuda(cudaError_t e) { return e == cudaSuccess ? PNQ_OK : PNQ_ERR_CUDA; }
+
+// Shared shape / pointer checks. On success fills the NVFP4 view (when type is NVFP4).
+int check_common(int type, const void* W, int64_t rows, int64_t K, Nvfp4View* nv) {
+    if (type != PNQ_PN3T && type != PNQ_PN4T && type != PNQ_NVFP4) return PNQ_ERR_TYPE;
+    if (rows < 0 || K <= 0) return PNQ_ERR_SHAPE;
+    if (type == PNQ_NVFP4) {
+        if (K % 16 != 0) return PNQ_ERR_SHAPE;
+        if (rows > INT64_MAX / K) return PNQ_ERR_SHAPE;
+        if (!W) return PNQ_ERR_NULL;
+        const pnq_nvfp4_weights* d = static_cast<const pnq_nvfp4_weights*>(W);
+        if (rows > 0 && (!d->codes || !d->scales)) return PNQ_ERR_NULL;
+        nv->codes = d->codes;
+        nv->scales = d->scales;
+        nv->g = d->global_scale;
+        return PNQ_OK;
+    }
+    const int blk = block_weights(type);
+    if (K % blk != 0) return PNQ_ERR_SHAPE;
+    if (rows > INT64_MAX / (K / blk * 34) || rows > INT64_MAX / K) return PNQ_ERR_SHAPE;
+    if (rows > 0 && !W) return PNQ_ERR_NULL;
+    if (!aligned(W, 2)) return PNQ_ERR_ALIGN;
+    return PNQ_OK;
+}
+
+}  // namespace
+
+int device_sm_count() {
+    static int counts[kMaxDevices] = {};
+    const int dev = current_device();
+    if (dev < 0) return 148;
+    if (!counts[dev]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+        counts[dev] = n;
+    }
+    return counts[dev];
+}
+
+}  // namespace pnq
+
+using namespace pnq;
+
+extern "C" int pnq_gemv(int type, const void* W, int64_t N, int64_t K, const void* X, int M, float* Y,
+                        cudaStream_t stream) {
+    Nvfp4View nv{};
+    int rc = check_common(type, W, N, K, &nv);
+    if (rc != PNQ_OK) return rc;
+    if (M < 1 || M > 16) return PNQ_ERR_SHAPE;
+    if (static_cast<int64_t>(M) > INT64_MAX / K) return PNQ_ERR_SHAPE;
+    if (N == 0) return PNQ_OK;
+    if (!X || !Y) return PNQ_ERR_NULL;
+    if (!aligned(Y, 4)) return PNQ_ERR_ALIGN;
+    const int mode = forced_kernel();
+    if (type == PNQ_NVFP4) {
+        if (!aligned(X, 2)) return PNQ_ERR_ALIGN;
+        const uint16_t* x = static_cast<const uint16_t*>(X);
+        if (mode != 1 && aligned(nv.codes, 16) && aligned(nv.scales, 16) && K % 256 == 0) {
+            const cudaError_t e = launch_nvfp4_gemv_mma(nv, N, K, x, M, Y, error_word(), MmaConfig{0, 0, 0, 0}, stream);
+            if (e != cudaErrorNotSupported) return map_cuda(e);
+        }
+        return map_cuda(launch_nvfp4_gemv_simt(nv, N, K, x, M, Y, stream));
+    }
+    if (!aligned(X, 4)) return PNQ_ERR_ALIGN;
+    const uint8_t* w = static_cast<const uint8_t*>(W);
+    const float* x = static_cast<const float*>(X);
+    if (mode != 1 && aligned(w, 16) && (K / block_weights(type)) % 8 == 0) {
+        const cudaError_t e = launch_pn_gemv_mma(type, w, N, K, x, M, Y, error_word(), MmaConfig{0, 0, 0, 0}, stream);
+        if (e != cudaErrorNotSupported) return map_cuda(e);
+    }
+    return map_cuda(launch_pn_gemv_simt(type, w, N, K, x, M, Y, stream));
+}
+
+extern "C" int pnq_dequantize_row(int type, const void* W, int64_t n_rows, int64_t K, float* out,
+                                  cudaStream_t stream) {
+    Nvfp4View nv{};
+    int rc = check_common(type, W, n_rows, K, &nv);
+    if (rc != PNQ_OK) return rc;
+    if (n_rows == 0) return PNQ_OK;
+    if (!out) return PNQ_ERR_NULL;
+    if (!aligned(out, 4)) return PNQ_ERR_ALIGN;
+    if (type == PNQ_NVFP4) return map_cuda(launch_nvfp4_dequant(nv, n_rows, K, out, stream));
+    return map_cuda(launch_pn_dequant(type, static_cast<const uint8_t*>(W), n_rows, K, out, stream));
+}
+
+extern "C" int pnq_validate_row(int type, const void* W, int64_t n_rows, int64_t K, int32_t* flags,
+                                cudaStream_t stream) {
+    Nvfp4View nv{};
+    int rc = check_common(type, W, n_rows, K, &nv);
+    if (rc != PNQ_OK) return rc;
+    if (n_rows == 0) return PNQ_OK;
+    if (!flags) return PNQ_ERR_NULL;
+    if (!aligned(flags, 4)) return PNQ_ERR_ALIGN;
+    if (type == PNQ_NVFP4) return map_cuda(launch_nvfp4_validate(nv, n_rows, K, flags, stream));
+    return map_cuda(launch_pn_validate(type, static_cast<const uint8_t*>(W), n_rows, K, flags, stream));
+}
+
+extern "C" int pnq_device_error(int32_t* code) {
+    if (!code) return PNQ_ERR_NULL;
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_pnq_error_word, sizeof(int)) != cudaSuccess) return PNQ_ERR_CUDA;
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_pnq_error_word, &zero, sizeof(int)) != cudaSuccess) return PNQ_ERR_CUDA;
+    *code = v;
+    return v == 0 ? PNQ_OK : PNQ_ERR_DEVICE;
+}
+
+extern "C" const char* pnq_version(void) { return "pnq 0.1.0 (sm_103a)"; }

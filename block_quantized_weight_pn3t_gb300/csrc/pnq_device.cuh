@@ -1,0 +1,237 @@
+// pnq_device.cuh -- device-side building blocks for libpnq (sm_103a).
+//
+// Format constants follow the "PN weight format" page (sections Types and Block layout):
+// 34-byte blocks, d = fp16 at bytes 0..1, eight little-endian u32 words at bytes 2..33,
+// element e in word e / CPW at shift BITS*(t>>1) + 16*(t&1), value d * (n - z).
+#pragma once
+
+#include <cstdint>
+#include <cuda_fp16.h>
+
+namespace pnq {
+
+constexpr int kBlockBytes = 34;
+constexpr int kTypePn3t = 124;
+constexpr int kTypePn4t = 125;
+constexpr int kTypeNvfp4 = 1004;
+
+template <int TYPE> struct PnFmt;
+template <> struct PnFmt<kTypePn3t> {
+    static constexpr int BLK = 80, BITS = 3, CPW = 10, Z = 4, PAIRS = 5;
+};
+template <> struct PnFmt<kTypePn4t> {
+    static constexpr int BLK = 64, BITS = 4, CPW = 8, Z = 8, PAIRS = 4;
+};
+
+// Site codes written to the device error word when a bounded wait gives up.
+enum ErrSite : int { kErrFullWait = 1, kErrEmptyWait = 2, kErrDrainWait = 3 };
+
+// The device error word lives in pnq_api.cu; kernels receive its address. It holds 0, or the
+// site code of the first bounded wait that gave up.
+__device__ __forceinline__ void record_error(int* err, int site) {
+    if (err) atomicCAS(err, 0, site);
+}
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// ---- mbarrier --------------------------------------------------------------
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_fence_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Waits for the phase with the given parity; gives up after ~limit_ns of wall time and
+// returns false (the caller records the error and skips its work).
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
+                                                  uint64_t limit_ns = 2000000000ull) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (global_timer_ns() - t0 > limit_ns) return false;
+    }
+}
+
+// ---- bulk copy (TMA, non-tensor) --------------------------------------------
+
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// 16-byte aligned global -> 16-byte aligned shared, size a multiple of 16; completion is
+// counted on `bar` in bytes.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
+                                         uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+        "[%0], [%1], %2, [%3], %4;" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+// Same copy with the default L2 policy (for data that other CTAs read again).
+__device__ __forceinline__ void bulk_g2s_plain(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+// ---- cluster ------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                     : "memory");
+}
+
+__device__ __forceinline__ float ld_dsmem_f32(uint32_t local_addr, uint32_t rank) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_addr), "r"(rank));
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+    return v;
+}
+
+// Named barrier over the first `threads` threads of the CTA (id 1; id 0 is __syncthreads).
+__device__ __forceinline__ void named_sync(uint32_t id, uint32_t threads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// ---- integer / half helpers ----------------------------------------------------
+
+// (a & b) | c in one instruction.
+__device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
+
+__device__ __forceinline__ uint32_t hadd2_u32(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("add.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+__device__ __forceinline__ uint32_t hfma2_u32(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+__device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// Two fp16 halves packed low | high << 16.
+__device__ __forceinline__ uint32_t pack_half2(__half lo, __half hi) {
+    return static_cast<uint32_t>(__half_as_ushort(lo)) |
+           (static_cast<uint32_t>(__half_as_ushort(hi)) << 16);
+}
+
+// Byte i (0..3) of w as two E2M1 codes (low nibble first) -> f16x2 with the exact values.
+template <int I>
+__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t w) {
+    uint32_t d;
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+        "mov.b32 {b0, b1, b2, b3}, %1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, b" "%2" ";\n\t}"
+        : "=r"(d)
+        : "r"(w), "n"(I));
+    return d;
+}
+
+// Two E4M3FN bytes (low 16 bits of w) -> f16x2 with the exact values (NaN stays NaN).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t w) {
+    uint32_t d;
+    asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}" : "=r"(d) : "r"(w));
+    return d;
+}
+
+// ---- mma.sync m16n8k16, fp16 x fp16 -> fp32 -----------------------------------------
+
+__device__ __forceinline__ void mma_f16_16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                              uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// ---- scalar decoders (written from the bit definitions) -----------------------------
+
+// E2M1 (NInfer "tensor-formats.md" section 3.3): sign bit 3, exponent bits 2:1, mantissa bit 0.
+__device__ __forceinline__ float e2m1_to_f32(uint32_t c) {
+    const uint32_t e = (c >> 1) & 3u, m = c & 1u;
+    float v = (e == 0) ? 0.5f * static_cast<float>(m)
+                       : __uint_as_float(((e + 126u) << 23) | (m << 22));
+    return (c & 8u) ? -v : v;
+}
+
+// E4M3FN (same section): sign bit 7, exponent bits 6:3 (bias 7), fraction 2:0;
+// e == 0 -> m * 2^-9, e == 15 && m == 7 -> NaN, no infinities.
+__device__ __forceinline__ float e4m3_to_f32(uint32_t b) {
+    const uint32_t e = (b >> 3) & 15u, m = b & 7u;
+    float v;
+    if ((b & 0x7Fu) == 0x7Fu)
+        v = __uint_as_float(0x7FC00000u);
+    else if (e == 0)
+        v = static_cast<float>(m) * 0.001953125f;
+    else
+        v = __uint_as_float(((e + 120u) << 23) | (m << 20));
+    return (b & 0x80u) ? -v : v;
+}
+
+// Power of two 2^e as fp32 for e in [-126, 127].
+__device__ __forceinline__ float exp2i(int e) { return __uint_as_float(static_cast<uint32_t>(e + 127) << 23); }
+
+}  // namespace pnq

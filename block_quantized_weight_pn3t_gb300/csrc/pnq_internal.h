@@ -1,0 +1,48 @@
+// pnq_internal.h -- host-side launchers shared by the translation units of libpnq.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace pnq {
+
+struct Nvfp4View {
+    const uint8_t* codes;   // device [N][K/2], low nibble = even k
+    const uint8_t* scales;  // device [N][K/16] E4M3FN
+    float g;                // global multiplier
+};
+
+// Tile configuration of the tensor-core GEMV (fast path).
+struct MmaConfig {
+    int rw;  // consumer ("row") warps per CTA; each owns a 16-row mma tile
+    int S;   // K split = cluster size along K (1 = no cluster)
+    int cb;  // chunk per pipeline stage: blocks (PN) or 256-weight units (NVFP4)
+    int ns;  // pipeline stages
+};
+
+int device_sm_count();
+
+cudaError_t launch_pn_dequant(int type, const uint8_t* W, int64_t n_rows, int64_t K, float* out,
+                              cudaStream_t stream);
+cudaError_t launch_nvfp4_dequant(const Nvfp4View& w, int64_t n_rows, int64_t K, float* out,
+                                 cudaStream_t stream);
+cudaError_t launch_pn_validate(int type, const uint8_t* W, int64_t n_rows, int64_t K, int32_t* flags,
+                               cudaStream_t stream);
+cudaError_t launch_nvfp4_validate(const Nvfp4View& w, int64_t n_rows, int64_t K, int32_t* flags,
+                                  cudaStream_t stream);
+
+// Generic path: any 2-byte aligned PN buffer / any NVFP4 layout, CUDA-core FMA.
+cudaError_t launch_pn_gemv_simt(int type, const uint8_t* W, int64_t N, int64_t K, const float* X, int M,
+                                float* Y, cudaStream_t stream);
+cudaError_t launch_nvfp4_gemv_simt(const Nvfp4View& w, int64_t N, int64_t K, const uint16_t* X, int M,
+                                   float* Y, cudaStream_t stream);
+
+// Fast path: 16-byte aligned weights, bulk-copy pipeline, mma.sync decode-and-multiply.
+// `cfg` fields <= 0 are chosen automatically. Returns cudaErrorNotSupported when the shape is
+// outside the fast path's range (the caller then uses the generic path).
+cudaError_t launch_pn_gemv_mma(int type, const uint8_t* W, int64_t N, int64_t K, const float* X, int M,
+                               float* Y, int* err, MmaConfig cfg, cudaStream_t stream);
+cudaError_t launch_nvfp4_gemv_mma(const Nvfp4View& w, int64_t N, int64_t K, const uint16_t* X, int M,
+                                  float* Y, int* err, MmaConfig cfg, cudaStream_t stream);
+
+}  // namespace pnq
