@@ -24,6 +24,10 @@ class Status(enum.IntEnum):
     ERR_ALIGN = -4
     ERR_CUDA = -5
     ERR_DEVICE = -6
+    ERR_FLAGS = -7
+
+
+GEMV_STATIC_WEIGHTS = 1
 
 
 class PnqError(RuntimeError):
@@ -56,6 +60,8 @@ def lib() -> ctypes.CDLL:
         P, I64, I = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
         L.pnq_gemv.restype = I
         L.pnq_gemv.argtypes = [I, P, I64, I64, P, I, P, P]
+        L.pnq_gemv_ex.restype = I
+        L.pnq_gemv_ex.argtypes = [I, P, I64, I64, P, I, P, ctypes.c_uint, P]
         L.pnq_dequantize_row.restype = I
         L.pnq_dequantize_row.argtypes = [I, P, I64, I64, P, P]
         L.pnq_validate_row.restype = I
@@ -93,6 +99,11 @@ def gemv_ptr(type_: int, W, N: int, K: int, X: int, M: int, Y: int, stream: int 
                           ctypes.c_void_p(stream))
 
 
+def gemv_ex_ptr(type_: int, W, N: int, K: int, X: int, M: int, Y: int, flags: int, stream: int = 0) -> int:
+    return lib().pnq_gemv_ex(type_, _w_arg(type_, W), N, K, ctypes.c_void_p(X), M, ctypes.c_void_p(Y),
+                             flags, ctypes.c_void_p(stream))
+
+
 def dequantize_row_ptr(type_: int, W, n_rows: int, K: int, out: int, stream: int = 0) -> int:
     return lib().pnq_dequantize_row(type_, _w_arg(type_, W), n_rows, K, ctypes.c_void_p(out),
                                     ctypes.c_void_p(stream))
@@ -127,15 +138,15 @@ def _weights(type_: int, W):
     return W.data_ptr()
 
 
-def gemv(type_: int, W, X, N: int, K: int, Y=None, stream=None):
+def gemv(type_: int, W, X, N: int, K: int, Y=None, stream=None, flags: int = 0):
     """Y[m][n] = sum_k W[n][k] X[m][k]. W: uint8 CUDA tensor of PN blocks, or (codes, scales, g)
     for NVFP4. X: CUDA [M][K] fp32 (PN) or bf16 (NVFP4). Returns Y (CUDA fp32 [M][N])."""
     import torch
     M = X.shape[0] if X.dim() == 2 else 1
     if Y is None:
         Y = torch.empty((M, N), dtype=torch.float32, device=X.device)
-    _check(gemv_ptr(type_, _weights(type_, W), N, K, X.data_ptr(), M, Y.data_ptr(), _stream_handle(stream)),
-           "pnq_gemv")
+    _check(gemv_ex_ptr(type_, _weights(type_, W), N, K, X.data_ptr(), M, Y.data_ptr(), flags,
+                       _stream_handle(stream)), "pnq_gemv_ex")
     return Y
 
 

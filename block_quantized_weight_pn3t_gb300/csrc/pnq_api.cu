@@ -96,22 +96,25 @@ int device_sm_count() {
 
 using namespace pnq;
 
-extern "C" int pnq_gemv(int type, const void* W, int64_t N, int64_t K, const void* X, int M, float* Y,
-                        cudaStream_t stream) {
+extern "C" int pnq_gemv_ex(int type, const void* W, int64_t N, int64_t K, const void* X, int M, float* Y,
+                           unsigned int flags, cudaStream_t stream) {
     Nvfp4View nv{};
     int rc = check_common(type, W, N, K, &nv);
     if (rc != PNQ_OK) return rc;
     if (M < 1 || M > 16) return PNQ_ERR_SHAPE;
     if (static_cast<int64_t>(M) > INT64_MAX / K) return PNQ_ERR_SHAPE;
+    if ((flags & ~static_cast<unsigned int>(PNQ_GEMV_STATIC_WEIGHTS)) != 0) return PNQ_ERR_FLAGS;
     if (N == 0) return PNQ_OK;
     if (!X || !Y) return PNQ_ERR_NULL;
     if (!aligned(Y, 4)) return PNQ_ERR_ALIGN;
+    const bool static_w = (flags & PNQ_GEMV_STATIC_WEIGHTS) != 0;
     const int mode = forced_kernel();
     if (type == PNQ_NVFP4) {
         if (!aligned(X, 2)) return PNQ_ERR_ALIGN;
         const uint16_t* x = static_cast<const uint16_t*>(X);
         if (mode != 1 && aligned(nv.codes, 16) && aligned(nv.scales, 16) && K % 256 == 0) {
-            const cudaError_t e = launch_nvfp4_gemv_mma(nv, N, K, x, M, Y, error_word(), MmaConfig{0, 0, 0, 0}, stream);
+            const cudaError_t e =
+                launch_nvfp4_gemv_mma(nv, N, K, x, M, Y, error_word(), MmaConfig{0, 0, 0, 0}, static_w, stream);
             if (e != cudaErrorNotSupported) return map_cuda(e);
         }
         return map_cuda(launch_nvfp4_gemv_simt(nv, N, K, x, M, Y, stream));
@@ -120,10 +123,16 @@ extern "C" int pnq_gemv(int type, const void* W, int64_t N, int64_t K, const voi
     const uint8_t* w = static_cast<const uint8_t*>(W);
     const float* x = static_cast<const float*>(X);
     if (mode != 1 && aligned(w, 16) && (K / block_weights(type)) % 8 == 0) {
-        const cudaError_t e = launch_pn_gemv_mma(type, w, N, K, x, M, Y, error_word(), MmaConfig{0, 0, 0, 0}, stream);
+        const cudaError_t e =
+            launch_pn_gemv_mma(type, w, N, K, x, M, Y, error_word(), MmaConfig{0, 0, 0, 0}, static_w, stream);
         if (e != cudaErrorNotSupported) return map_cuda(e);
     }
     return map_cuda(launch_pn_gemv_simt(type, w, N, K, x, M, Y, stream));
+}
+
+extern "C" int pnq_gemv(int type, const void* W, int64_t N, int64_t K, const void* X, int M, float* Y,
+                        cudaStream_t stream) {
+    return pnq_gemv_ex(type, W, N, K, X, M, Y, 0u, stream);
 }
 
 extern "C" int pnq_dequantize_row(int type, const void* W, int64_t n_rows, int64_t K, float* out,

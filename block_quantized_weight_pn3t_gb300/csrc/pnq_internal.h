@@ -12,12 +12,12 @@ struct Nvfp4View {
     float g;                // global multiplier
 };
 
-// Tile configuration of the tensor-core GEMV (fast path).
+// Tile configuration of the tensor-core GEMV (fast path); fields <= 0 are chosen automatically.
 struct MmaConfig {
-    int rw;  // consumer ("row") warps per CTA; each owns a 16-row mma tile
-    int S;   // K split = cluster size along K (1 = no cluster)
-    int cb;  // chunk per pipeline stage: blocks (PN) or 256-weight units (NVFP4)
-    int ns;  // pipeline stages
+    int rw;   // consumer warps per CTA (2, 4 or 8)
+    int S;    // K split = cluster size along K (1 = persistent grid, no cluster)
+    int tpw;  // unused (tiles per pass equal the consumer warps)
+    int ns;   // pipeline stages
 };
 
 int device_sm_count();
@@ -37,12 +37,13 @@ cudaError_t launch_pn_gemv_simt(int type, const uint8_t* W, int64_t N, int64_t K
 cudaError_t launch_nvfp4_gemv_simt(const Nvfp4View& w, int64_t N, int64_t K, const uint16_t* X, int M,
                                    float* Y, cudaStream_t stream);
 
-// Fast path: 16-byte aligned weights, bulk-copy pipeline, mma.sync decode-and-multiply.
-// `cfg` fields <= 0 are chosen automatically. Returns cudaErrorNotSupported when the shape is
-// outside the fast path's range (the caller then uses the generic path).
+// Fast path: 16-byte aligned weights and x, bulk-copy pipeline, mma.sync decode-and-multiply.
+// static_weights: the weights are not written by work queued earlier in the stream, so they
+// may be prefetched before the previous grid completes. Returns cudaErrorNotSupported when
+// the shape is outside the fast path's range (the caller then uses the generic path).
 cudaError_t launch_pn_gemv_mma(int type, const uint8_t* W, int64_t N, int64_t K, const float* X, int M,
-                               float* Y, int* err, MmaConfig cfg, cudaStream_t stream);
+                               float* Y, int* err, MmaConfig cfg, bool static_weights, cudaStream_t stream);
 cudaError_t launch_nvfp4_gemv_mma(const Nvfp4View& w, int64_t N, int64_t K, const uint16_t* X, int M,
-                                  float* Y, int* err, MmaConfig cfg, cudaStream_t stream);
+                                  float* Y, int* err, MmaConfig cfg, bool static_weights, cudaStream_t stream);
 
 }  // namespace pnq

@@ -53,7 +53,16 @@ enum pnq_status {
     PNQ_ERR_NULL = -3,   /* a required pointer is NULL */
     PNQ_ERR_ALIGN = -4,  /* a pointer misses its minimum alignment (see each call) */
     PNQ_ERR_CUDA = -5,   /* a CUDA call failed (launch error, no device, bad stream) */
-    PNQ_ERR_DEVICE = -6  /* a kernel gave up on an internal wait (see pnq_device_error) */
+    PNQ_ERR_DEVICE = -6, /* a kernel gave up on an internal wait (see pnq_device_error) */
+    PNQ_ERR_FLAGS = -7   /* unknown bit in a flags argument */
+};
+
+/* Flags of pnq_gemv_ex. */
+enum pnq_gemv_flags {
+    /* The weights are not written by any work queued earlier on the stream (e.g. model weights
+     * in a decode loop). The kernel may then start streaming them from HBM while the previous
+     * grid in the stream is still running; x is still read only after that grid completes. */
+    PNQ_GEMV_STATIC_WEIGHTS = 1u
 };
 
 /* NVFP4 weight descriptor, passed by HOST pointer as the W argument when type ==
@@ -83,6 +92,17 @@ typedef struct pnq_nvfp4_weights {
  */
 int pnq_gemv(int type, const void* W, int64_t N, int64_t K, const void* X, int M, float* Y,
              cudaStream_t stream);
+
+/*
+ * pnq_gemv_ex -- pnq_gemv with flags (a bitwise OR of pnq_gemv_flags; 0 = pnq_gemv).
+ * Same arguments, results and errors as pnq_gemv, plus PNQ_ERR_FLAGS for unknown bits. The
+ * pages define no such call: it exposes an overlap that only the caller can declare safe.
+ * Launches on the fast path use programmatic dependent launch: a GEMV may begin while the
+ * previous kernel on the stream finishes, and reads nothing that kernel may write (x, and
+ * the weights unless PNQ_GEMV_STATIC_WEIGHTS) before that kernel has completed.
+ */
+int pnq_gemv_ex(int type, const void* W, int64_t N, int64_t K, const void* X, int M, float* Y,
+                unsigned int flags, cudaStream_t stream);
 
 /*
  * pnq_dequantize_row -- out[r][k] = the fp32 weight, bit-exact:

@@ -74,6 +74,8 @@ def test_argument_errors(lib, call):
         assert run(pnq.PN3T, FAKE, 4, 80, X=0) == Status.ERR_NULL
         assert run(pnq.PN3T, FAKE, 4, 80, X=FAKE + 2) == Status.ERR_ALIGN  # fp32 X
         assert run(pnq.NVFP4, nv, 4, 32, X=FAKE + 1) == Status.ERR_ALIGN   # bf16 X
+        assert pnq.gemv_ex_ptr(pnq.PN3T, FAKE, 4, 80, FAKE, 1, FAKE, 2) == Status.ERR_FLAGS
+        assert pnq.gemv_ex_ptr(pnq.PN3T, FAKE, 0, 80, FAKE, 1, FAKE, pnq.GEMV_STATIC_WEIGHTS) == Status.OK
 
 
 def test_nvfp4_descriptor_null_pointer(lib):

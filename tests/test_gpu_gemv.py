@@ -181,9 +181,10 @@ out = []
 for type_, N, K, M in [(124, 200, 80*48, 1), (125, 130, 64*80, 3), (125, 64, 64*8, 16), (124, 17, 80*16, 8)]:
     W = synth.pn_random_blocks(type_, N, K, seed=N + K)
     X = synth.activations(M, K, seed=M)
-    Y = pnq.gemv(type_, W.cuda(), torch.from_numpy(X).cuda(), N, K).cpu().numpy()
-    Yr, Ar = oracle.gemv(type_, W.numpy(), N, K, X)
-    assert_within_tolerance(Y, Yr, Ar, str((type_, N, K, M)))
+    for flags in (0, pnq.GEMV_STATIC_WEIGHTS):
+        Y = pnq.gemv(type_, W.cuda(), torch.from_numpy(X).cuda(), N, K, flags=flags).cpu().numpy()
+        Yr, Ar = oracle.gemv(type_, W.numpy(), N, K, X)
+        assert_within_tolerance(Y, Yr, Ar, str((type_, N, K, M, flags)))
 for N, K, M in [(130, 256*6, 1), (33, 256*9, 5), (64, 256*2, 16)]:
     c, s, g = synth.nvfp4_random(N, K, seed=K)
     Xb = synth.activations_bf16(M, K, seed=K)
@@ -195,9 +196,9 @@ print(json.dumps({{"ok": True, "device_error": pnq.device_error()}}))
 """
 
 
-@pytest.mark.parametrize("cfg", ["2,1,8,2", "4,2,16,3", "2,5,8,4", "4,8,8,2", "2,3,24,6"])
+@pytest.mark.parametrize("cfg", ["2,1,0,2", "4,2,0,3", "2,4,0,4", "4,8,0,5", "4,1,0,8", "2,16,0,6", "4,4,0,0"])
 def test_tile_and_cluster_configs(cfg):
-    """Row warps, K-split cluster size, chunk and stage count forced through PNQ_GEMV_CFG (read
+    """Consumer warps, K-split cluster size and stage count forced through PNQ_GEMV_CFG (read
     once per process, so each configuration runs in a child process)."""
     env = dict(os.environ, PNQ_GEMV_CFG=cfg, PNQ_FORCE_KERNEL="mma")
     r = subprocess.run([sys.executable, "-c", CHILD.format(root=ROOT)], env=env, capture_output=True, text=True,
