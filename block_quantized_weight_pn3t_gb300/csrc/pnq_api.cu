@@ -34,12 +34,14 @@ int* error_word() {
     return ptrs[dev];
 }
 
-// "auto" (default), "simt" (generic path only) or "mma" (fast path whenever eligible).
+// "auto" (default), "simt" (generic path only), "mma" (mma.sync path whenever eligible) or
+// "tc" (tcgen05 path whenever eligible).
 int forced_kernel() {
     static int mode = [] {
         const char* s = std::getenv("PNQ_FORCE_KERNEL");
         if (s && std::strcmp(s, "simt") == 0) return 1;
         if (s && std::strcmp(s, "mma") == 0) return 2;
+        if (s && std::strcmp(s, "tc") == 0) return 3;
         return 0;
     }();
     return mode;
@@ -123,6 +125,10 @@ extern "C" int pnq_gemv_ex(int type, const void* W, int64_t N, int64_t K, const 
     const uint8_t* w = static_cast<const uint8_t*>(W);
     const float* x = static_cast<const float*>(X);
     if (mode != 1 && aligned(w, 16) && (K / block_weights(type)) % 8 == 0) {
+        if (mode != 2) {
+            const cudaError_t e = launch_pn_gemv_tc(type, w, N, K, x, M, Y, error_word(), static_w, stream);
+            if (e != cudaErrorNotSupported) return map_cuda(e);
+        }
         const cudaError_t e =
             launch_pn_gemv_mma(type, w, N, K, x, M, Y, error_word(), MmaConfig{0, 0, 0, 0}, static_w, stream);
         if (e != cudaErrorNotSupported) return map_cuda(e);

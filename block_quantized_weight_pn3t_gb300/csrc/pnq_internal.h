@@ -43,6 +43,11 @@ cudaError_t launch_nvfp4_gemv_simt(const Nvfp4View& w, int64_t N, int64_t K, con
 // the shape is outside the fast path's range (the caller then uses the generic path).
 cudaError_t launch_pn_gemv_mma(int type, const uint8_t* W, int64_t N, int64_t K, const float* X, int M,
                                float* Y, int* err, MmaConfig cfg, bool static_weights, cudaStream_t stream);
+// Tensor-core path (tcgen05, tensor memory): 16-byte aligned weights and x, (K / block) a
+// multiple of 8. Keeps a per-(device, stream) workspace of partial rows. Returns
+// cudaErrorNotSupported outside its range.
+cudaError_t launch_pn_gemv_tc(int type, const uint8_t* W, int64_t N, int64_t K, const float* X, int M, float* Y,
+                              int* err, bool static_weights, cudaStream_t stream);
 cudaError_t launch_nvfp4_gemv_mma(const Nvfp4View& w, int64_t N, int64_t K, const uint16_t* X, int M,
                                   float* Y, int* err, MmaConfig cfg, bool static_weights, cudaStream_t stream);
 
