@@ -2,9 +2,15 @@
 #include "pnq.h"
 #include "pnq_internal.h"
 
+#include <algorithm>
+
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
+#include <map>
+#include <mutex>
+#include <utility>
+#include <vector>
 
 // Device error word: 0, or the site code of the first bounded wait that gave up (one copy per
 // device that loads the library).
@@ -34,8 +40,9 @@ int* error_word() {
     return ptrs[dev];
 }
 
-// "auto" (default), "simt" (generic path only), "mma" (mma.sync path whenever eligible) or
-// "tc" (tcgen05 path whenever eligible).
+// "auto" (default: the mma.sync path whenever eligible), "simt" (generic path only), "mma"
+// (same as auto) or "tc" (the tcgen05 path whenever eligible; slower for M <= 16, kept as a
+// measured alternative).
 int forced_kernel() {
     static int mode = [] {
         const char* s = std::getenv("PNQ_FORCE_KERNEL");
@@ -94,6 +101,78 @@ int device_sm_count() {
     return counts[dev];
 }
 
+namespace {
+
+using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                              const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                              CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeFn tensor_map_encoder() {
+    static EncodeFn fn = [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return static_cast<EncodeFn>(nullptr);
+        return reinterpret_cast<EncodeFn>(p);
+    }();
+    return fn;
+}
+
+struct Workspace {
+    float* ws = nullptr;
+    uint32_t* cnt = nullptr;
+    size_t floats = 0, counters = 0;
+};
+
+}  // namespace
+
+bool encode_u32_map(CUtensorMap* map, const void* base, int64_t rows, int64_t row_u32, int box_x, int box_y) {
+    EncodeFn enc = tensor_map_encoder();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(row_u32), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_u32 * 4)};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_x), static_cast<cuuint32_t>(box_y)};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+cudaError_t stream_workspace(cudaStream_t stream, size_t floats, size_t counters, float** ws, uint32_t** cnt) {
+    static std::mutex mu;
+    static std::map<std::pair<int, cudaStream_t>, Workspace> table;
+    static std::vector<void*> retired;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(mu);
+    Workspace& w = table[{dev, stream}];
+    if (w.floats < floats || w.counters < counters) {
+        Workspace n;
+        n.floats = std::max(floats, w.floats);
+        n.counters = std::max(counters, w.counters);
+        cudaStreamCaptureMode mode = cudaStreamCaptureModeRelaxed;
+        cudaThreadExchangeStreamCaptureMode(&mode);
+        e = cudaMalloc(&n.ws, n.floats * sizeof(float));
+        if (e == cudaSuccess) {
+            e = cudaMalloc(&n.cnt, n.counters * sizeof(uint32_t));
+            if (e != cudaSuccess) cudaFree(n.ws);
+        }
+        cudaThreadExchangeStreamCaptureMode(&mode);
+        if (e != cudaSuccess) return e;
+        e = cudaMemsetAsync(n.cnt, 0, n.counters * sizeof(uint32_t), stream);
+        if (e != cudaSuccess) return e;
+        if (w.ws) retired.push_back(w.ws);
+        if (w.cnt) retired.push_back(w.cnt);
+        w = n;
+    }
+    *ws = w.ws;
+    *cnt = w.cnt;
+    return cudaSuccess;
+}
+
 }  // namespace pnq
 
 using namespace pnq;
@@ -125,7 +204,7 @@ extern "C" int pnq_gemv_ex(int type, const void* W, int64_t N, int64_t K, const 
     const uint8_t* w = static_cast<const uint8_t*>(W);
     const float* x = static_cast<const float*>(X);
     if (mode != 1 && aligned(w, 16) && (K / block_weights(type)) % 8 == 0) {
-        if (mode != 2) {
+        if (mode == 3) {
             const cudaError_t e = launch_pn_gemv_tc(type, w, N, K, x, M, Y, error_word(), static_w, stream);
             if (e != cudaErrorNotSupported) return map_cuda(e);
         }

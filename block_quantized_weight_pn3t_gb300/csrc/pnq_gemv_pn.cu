@@ -1,729 +1,711 @@
-// pnq_gemv_pn.cu -- tensor-core GEMV straight from pn3t / pn4t 34-byte blocks (fast path).
+// pnq_gemv_pn.cu -- PN (pn3t / pn4t) GEMV on the tensor cores with mma.sync, sm_103a (fast path).
 //
-// Computes Y[m][n] = sum_k w[n][k] x[m][k], 1 <= M <= 16, with w decoded in registers just
-// before the multiply ("PN weight format", sections Block layout and Value).
+// Computes Y[m][n] = sum_k w[n][k] x[m][k] for 1 <= M <= 16, with w = d * (n - z) decoded in
+// registers from the 34-byte blocks of the "PN weight format" page (sections Block layout and
+// Value) just before the multiply.
 //
-// Work split. Persistent grid, one wave: clusters of S CTAs (S = 1, 2, 4 or 8), one CTA per
-// SM. Weight rows are cut into 16-row tiles; each cluster owns a balanced contiguous range of
-// tiles and streams it in passes of 4 tiles (64 rows); CTA rank q owns the q-th slice of K.
+// Why mma.sync. A GEMV streams every weight once; at HBM rate an SM has to take in about 50
+// weights per cycle. The warp-level m16n8k16 MMA sustains 0.5 instructions per cycle per SM
+// (256 weights each), while a tcgen05.mma of M = 128, K = 16 occupies the tensor core for about
+// 100 cycles whatever N <= 128 is (2048 weights each) -- both measured on this part -- so for
+// the narrow N of a GEMV the warp-level MMA has the throughput and tcgen05 does not.
 //
-// Memory pipeline. One producer thread issues 2-D tensor-map copies: a stage is 16 blocks of
-// 64 rows, loaded as two 64 x 272-byte boxes (272 bytes = 8 blocks, a multiple of 16 and an odd
-// number of 16-byte lines, so a warp's 8 row groups hit distinct banks). Ragged last passes
-// use 16-row boxes. NS stages ring under mbarriers, L2 evict-first. At start the producer
-// also copies the CTA's slice of x (fp32) into the last stages of the ring.
+// Items and schedule (stream-K). The weight matrix is cut into items of 128 rows x one K unit
+// of 8 blocks (272 bytes per row). Items are numbered unit-major (item = u * T + t for row tile
+// t of T) and every CTA of a persistent grid (one per SM) takes an equal contiguous share, so
+// all SMs stream the same number of bytes and a CTA's items touch at most a few K units.
 //
-// Compute. RW consumer warps (8 for M <= 4, else 4) split every stage along K: each takes its
-// own 16/RW blocks for all four tiles, so each block's B fragments feed four independent mma
-// chains. The decode is one AND per pair of weights: a 32-bit word holds two codes at the same shift in
-// its two 16-bit halves, and with a zero fp16 exponent field the masked halves are the exact
-// fp16 subnormals n * 2^-24 * 8^j (pn3t, j = position of the pair) or n * 2^-24 * 16^j (pn4t)
-// -- an mma A register, no bias, no conversion. The 8^-j (16^-j) factor and a power of two
-// 2^sigma (chosen per CTA and activation row so that any finite x fits fp16) are folded into
-// the B operand: x is split into fp16 hi + lo parts (~22 bits), one mma column each (M rows
-// use 2M columns, NT = ceil(2M/8) n8 tiles). The zero point is applied per block as
-// d * (sum n x - z * sum x) with the per-block sums of x precomputed next to the fragments.
-// Within a block the k order is free (x is permuted the same way), which lets 2-byte aligned
-// words be read as aligned words pairing the high half of word i-1 with the low half of word i.
+// Memory pipeline. One producer thread loads one item per stage with a 2-D tensor-map copy
+// (box 272 bytes x 128 rows, L2 evict-first; rows past N read as zeros) into an NS-stage ring
+// under mbarriers; at start it also copies the CTA's slice of x (fp32) into the last stages.
+// With the static-weights flag the first stages are requested before the previous grid in the
+// stream has finished.
 //
-// Reduction. The warps' partial sums of a pass meet in shared memory; with S > 1 the
-// cluster's CTAs exchange partial rows through distributed shared memory (ready / consumed
-// mbarrier handshakes, double-buffered by pass) and sum them in rank order: deterministic,
-// no atomics, no global scratch.
+// Decode and multiply (consumer warps). Warp = TPW tiles of 16 rows x half a unit (4 blocks).
+// A 32-bit word of a block holds two codes at the same shift in its two 16-bit halves; masking
+// out one such pair leaves in each half the exact fp16 subnormal n * 2^-24 * 8^j (pn3t; 16^j
+// for pn4t, j = position of the pair): one AND per two weights gives an mma A register. Lane
+// (g, c) of the warp uses words c and c + 4 of rows g and g + 8; the k order inside a block is
+// free as long as B uses the same order, so the 2-byte aligned words of even blocks are read as
+// aligned words pairing the high half of word i-1 with the low half of word i (one PRMT).
 //
-// Launch. Programmatic dependent launch: every CTA lets the next grid in the stream begin
-// launching, and reads nothing the previous grid may write before that grid has completed
-// (with the static-weights flag only the weights, which the caller declares unchanged). All
-// mbarrier waits are bounded in time and report to the library's device error word.
+// B operand: x times 8^-j (16^-j) times 2^sigma (per CTA and activation row, so that max|x| *
+// 2^sigma lies in [2^14, 2^15)), split into fp16 hi + lo parts (~22 bits) that take mma
+// columns 2m and 2m + 1 (NT = ceil(2M / 8) n8 tiles). The fragments of the CTA's blocks are
+// built once in shared memory in register order.
+//
+// Block scale and zero point: acc += d * (c - Z) per block, Z = z * (sum over the block of B
+// times 2^-24 * 8^j), precomputed beside B in fp32.
+//
+// Reduction. At the end of an item the consumer warps leave their row sums (two halves) in
+// shared memory; a reducer warp adds them, writes the item's rows to a workspace slot and
+// counts the item on its row tile; the CTA that brings a tile's count to U sums the tile's U
+// slots in unit order (so the result does not depend on timing) and writes Y.
 #include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstdlib>
 
 #include "pnq_device.cuh"
 #include "pnq_internal.h"
 
-#include <algorithm>
-#include <cstdlib>
-#include <cstring>
-
 namespace pnq {
 namespace {
 
-constexpr int kMaxM = 16;
-constexpr int kTP = 4;                           // 16-row tiles per pass
-constexpr int kRows = 16 * kTP;                  // rows per pass
-constexpr int kColBlocks = 8;                    // blocks per tensor-map column (272 bytes of a row)
-constexpr int kColBytes = kColBlocks * kBlockBytes;
-constexpr int kColU32 = kColBytes / 4;           // 68 elements of the u32 tensor map
-constexpr int kCols = 2;                         // columns per stage: 16 blocks
-constexpr int kBoxBytes = kRows * kColBytes;     // 17408: one 64-row column box
-constexpr int kTileBoxBytes = 16 * kColBytes;    // 4352: one 16-row column box
-constexpr int kStageBytes = kCols * kBoxBytes;   // 34816
+constexpr int kTileRows = 128;                         // rows per item
+constexpr int kUnitBlocks = 8;                         // blocks per K unit
+constexpr int kUnitBytes = kUnitBlocks * kBlockBytes;  // 272 bytes of a row per unit
+constexpr int kUnitU32 = kUnitBytes / 4;               // 68
+constexpr int kStageBytes = kTileRows * kUnitBytes;    // 34816
+constexpr int kHalfBlocks = 4;                         // blocks per consumer warp and item
+constexpr int kPartPitch = 132;                        // floats per (half, buffer, m) row-sum vector
+constexpr int kMaxStages = 8;
+constexpr unsigned kStaticWeights = 1u;
+constexpr size_t kSmemLimit = 227u * 1024u;
 
-__host__ __device__ constexpr uint32_t align_up(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
+template <int TYPE, int NT, int TPW>
+struct Cfg {
+    static constexpr int STEPS = PnFmt<TYPE>::PAIRS;
+    static constexpr int TG = 8 / TPW;             // tile groups per half
+    static constexpr int CW = 2 * TG;              // consumer warps
+    static constexpr int PRODUCER = CW, REDUCER = CW + 1;
+    static constexpr int THREADS = 32 * (CW + 2);
+    static constexpr int NCT = 32 * CW;            // consumer threads
+    static constexpr int BFU = NT * 256 * STEPS;   // fragment bytes per block
+};
+
+// Item numbering. Tile-major (item = t * U + u): a CTA's share covers one or two row tiles and
+// at most U units, and it accumulates a tile over consecutive items. Unit-major (item = u * T + t):
+// a CTA's share touches at most a few units (for operands that would not fit otherwise). CTA c
+// of G takes items [c * items / G, (c + 1) * items / G).
+struct Sched {
+    long long items;
+    int T, U, G, tile_major;
+    __host__ __device__ int tile_of(long long i) const {
+        return tile_major ? static_cast<int>(i / U) : static_cast<int>(i % T);
+    }
+    __host__ __device__ int unit_of(long long i) const {
+        return tile_major ? static_cast<int>(i % U) : static_cast<int>(i / T);
+    }
+    __host__ __device__ long long item(int t, int u) const {
+        return tile_major ? static_cast<long long>(t) * U + u : static_cast<long long>(u) * T + t;
+    }
+    __host__ __device__ long long first(long long c) const { return c * items / G; }
+    __host__ __device__ long long owner(long long i) const { return ((i + 1) * G - 1) / items; }
+    // units a CTA's share touches (a cyclic range starting at unit_of(first item))
+    __host__ __device__ int span(long long i0, long long i1) const {
+        if (i1 <= i0) return 0;
+        if (tile_major) return static_cast<int>(i1 - i0 < U ? i1 - i0 : U);
+        return unit_of(i1 - 1) - unit_of(i0) + 1;
+    }
+};
 
 struct PnArgs {
-    CUtensorMap map_pass;  // weights as u32 [N][row_bytes / 4], box {68, 64}
-    CUtensorMap map_tile;  // same tensor, box {68, 16}
-    const float* X;        // [M][K]
-    float* Y;              // [M][N]
+    CUtensorMap map;  // weights as u32 [N][row_bytes / 4], box {68, 128}
+    const float* X;
+    float* Y;
+    float* ws;       // partial rows [T][U][M][128]: slot (t, u) = the share of tile t starting at unit u
+    uint32_t* cnt;   // [T] shares counted per row tile (zero between launches)
     int* err;
-    int N;
-    int K;
-    int units;             // 8-block units per row
-    int M;
-    int S;                 // cluster size along K
-    int NS;                // stages
-    int flags;             // kStaticWeights
+    Sched sc;
+    int N, K, M, NS, x_stage, xpitch;
+    unsigned flags;
+    uint32_t bar_off, misc_off, z_off, part_off, b_off, stage_off;
 };
 
-enum ArgFlags : int { kStaticWeights = 1 };
-
-// Shared-memory map (offsets from a 1024-byte aligned base), identical on host and device.
-struct PnLayout {
-    uint32_t bar_off;     // full[NS], empty[NS], x_ready, x_free, red_full[2], red_free[2]
-    uint32_t misc_off;    // maxbits[16] u32, sig_in[16] f32, sig_out[16] f32, issued u32
-    uint32_t red_off;     // [RW][kTP][NT][32 lanes][4] f32: warps' partial sums of a pass
-    uint32_t part_off;    // [2][kRows][M] f32: partial rows exchanged in the cluster (S > 1)
-    uint32_t z_off;       // [block][2M] f32: z * (sum of the block's scaled x, per mma column)
-    uint32_t bfrag_off;   // B fragments, bfrag_unit bytes per block
-    uint32_t bfrag_unit;
-    uint32_t zero_off;    // 64 zero bytes read by lanes whose mma column is unused
-    uint32_t stage_off;   // NS stages of kStageBytes
-    uint32_t x_stage;     // x is staged in stages [x_stage, NS) at start (0: does not fit)
-    uint32_t total;       // bytes from the aligned base
-};
-
-__host__ __device__ inline PnLayout make_pn_layout(int steps, int blk, int M, int NT, int RW, int units_max, int NS,
-                                                   int S) {
-    PnLayout L{};
-    const uint32_t blocks_max = 8u * units_max;
-    L.bar_off = 0;
-    L.misc_off = align_up(8u * (2 * NS + 6), 16);
-    L.red_off = L.misc_off + 256;
-    L.part_off = align_up(L.red_off + 512u * RW * kTP * NT, 16);
-    L.z_off = align_up(L.part_off + ((S > 1) ? 2u * 4u * kRows * M : 0u), 16);
-    L.bfrag_off = align_up(L.z_off + blocks_max * 8u * M, 128);
-    L.bfrag_unit = 64u * M * steps;  // 8M lanes x steps x 8 bytes
-    L.zero_off = align_up(L.bfrag_off + L.bfrag_unit * blocks_max, 128);
-    L.stage_off = align_up(L.zero_off + 64u, 1024);
-    const uint32_t xbytes = static_cast<uint32_t>(M) * blocks_max * blk * 4u;
-    const uint32_t xst = (xbytes + kStageBytes - 1) / kStageBytes;
-    L.x_stage = (xst >= static_cast<uint32_t>(NS)) ? 0u : NS - xst;
-    L.total = L.stage_off + kStageBytes * NS;
-    return L;
-}
-
-// ---- decode -----------------------------------------------------------------------------
-
-// Pair j of a (possibly re-paired) word as the f16x2 of exact subnormals (n_lo, n_hi) * 2^-24 *
-// base^jj, base = 8 (pn3t) or 16 (pn4t); jj is the pair's slot after the shift that brings it
-// below the fp16 exponent field.
-template <int TYPE, int J>
-__device__ __forceinline__ uint32_t pn_code_pair(uint32_t w) {
-    if (TYPE == kTypePn3t) {
-        constexpr int jj = (J < 3) ? J : J - 3;
-        const uint32_t src = (J < 3) ? w : (w >> 9);
-        return src & (0x00070007u << (3 * jj));
-    } else {
-        constexpr int jj = J & 1;
-        const uint32_t src = (J < 2) ? w : (w >> 8);
-        return src & (0x000F000Fu << (4 * jj));
-    }
-}
-
-// 2^-(BITS * jj) for pair j: the factor folded into step j's B operand.
+// 2^-(BITS * jj) for slice j, and its inverse.
 template <int TYPE>
-__host__ __device__ constexpr float step_scale(int j) {
+__device__ __forceinline__ float step_scale(int j) {
     return (TYPE == kTypePn3t) ? ((j % 3 == 0) ? 1.0f : (j % 3 == 1) ? 0.125f : 0.015625f)
                                : ((j & 1) ? 0.0625f : 1.0f);
 }
+template <int TYPE>
+__device__ __forceinline__ float step_scale_inv(int j) {
+    return (TYPE == kTypePn3t) ? ((j % 3 == 0) ? 1.0f : (j % 3 == 1) ? 8.0f : 64.0f) : ((j & 1) ? 16.0f : 1.0f);
+}
 
-// Element (within a block) of the low (hi_half = 0) or high code of pair j of decode word i,
-// for a block starting on a 4-byte boundary (even block) or not (odd block). Odd block: natural
-// word i. Even block: the aligned word at byte 4i holds the high half of word i-1 and the low
-// half of word i; decode word 0 pairs the low half of word 0 with the high half of word 7.
+// Masked pair J of a word (w) or of the word shifted right by 9 (pn3t) / 8 (pn4t) (s).
+template <int TYPE, int J>
+__device__ __forceinline__ uint32_t code_pair(uint32_t w, uint32_t s) {
+    if constexpr (TYPE == kTypePn3t) {
+        if constexpr (J < 3) return w & (0x00070007u << (3 * J));
+        else return s & (0x00070007u << (3 * (J - 3)));
+    } else {
+        if constexpr (J < 2) return w & (0x000F000Fu << (4 * J));
+        else return s & (0x000F000Fu << (4 * (J - 2)));
+    }
+}
+
+// Element (within a block) that the low (hi_half = 0) or high half of decode register i holds
+// for pair j. Odd blocks start 2 bytes past a 4-byte boundary: register i is word i. Even
+// blocks: register i (i >= 1) is the aligned word at byte 4i = high half of word i-1 and low
+// half of word i; register 0 pairs the low half of word 0 with the high half of word 7.
 __device__ __forceinline__ int pn_elem(int cpw, int odd_block, int i, int j, int hi_half) {
     if (odd_block) return cpw * i + 2 * j + hi_half;
     if (i == 0) return hi_half ? cpw * 7 + 2 * j + 1 : 2 * j;
     return hi_half ? cpw * i + 2 * j : cpw * (i - 1) + 2 * j + 1;
 }
 
-__device__ __forceinline__ __half split_part(float xs, int part) {
-    const __half hi = __float2half_rn(xs);
+__device__ __forceinline__ __half split_part(float v, int part) {
+    const __half hi = __float2half_rn(v);
     if (part == 0) return hi;
-    return __float2half_rn(xs - __half2float(hi));
+    return __float2half_rn(v - __half2float(hi));
 }
 
-// Per-m power-of-two scaling: sigma chosen so max|x| * 2^sigma lies in [2^14, 2^15) over the
-// CTA's slice (an all-zero or non-finite slice keeps sigma = 0). sig_out = 2^(24 - sigma)
-// undoes both sigma and the 2^-24 of the subnormal decode.
-__device__ void compute_sigma(int M, const float* xs, int klen, uint8_t* misc_p, int nct) {
-    uint32_t* maxbits = reinterpret_cast<uint32_t*>(misc_p);
-    float* sig_in = reinterpret_cast<float*>(misc_p + 64);
-    float* sig_out = reinterpret_cast<float*>(misc_p + 128);
-    const int tid = threadIdx.x;
-    const uint4* xv = reinterpret_cast<const uint4*>(xs);
-    const int nvec = klen / 4;  // klen is a multiple of 512
+__device__ __forceinline__ uint32_t lds32(const uint8_t* p) { return *reinterpret_cast<const uint32_t*>(p); }
+__device__ __forceinline__ float ld_half(const uint8_t* p) {
+    return __half2float(*reinterpret_cast<const __half*>(p));
+}
+
+// Kernel parameters the loops read, copied once into registers (parameters reached through a
+// pointer would be reloaded after every barrier).
+struct Ctx {
+    Sched sc;
+    const float* X;
+    float* Y;
+    float* ws;
+    uint32_t* cnt;
+    int* err;
+    int N, K, M, NS, x_stage, xpitch;
+    unsigned flags;
+};
+
+// Shared-memory regions (offsets from the 1024-aligned base).
+struct Smem {
+    uint8_t* base;
+    uint32_t bar0;  // shared address of barrier 0
+    int NS;
+    uint32_t misc_off, z_off, part_off, b_off, stage_off;
+    __device__ uint32_t full(int s) const { return bar0 + 8u * s; }
+    __device__ uint32_t empty(int s) const { return bar0 + 8u * (NS + s); }
+    __device__ uint32_t x_ready() const { return bar0 + 8u * (2 * NS); }
+    __device__ uint32_t x_free() const { return bar0 + 8u * (2 * NS + 1); }
+    __device__ uint32_t part_full(int b) const { return bar0 + 8u * (2 * NS + 2 + b); }
+    __device__ uint32_t part_free(int b) const { return bar0 + 8u * (2 * NS + 4 + b); }
+    __device__ uint32_t* maxbits() const { return reinterpret_cast<uint32_t*>(base + misc_off); }
+    __device__ float* sig_in() const { return reinterpret_cast<float*>(base + misc_off + 64); }
+    __device__ float* sig_out() const { return reinterpret_cast<float*>(base + misc_off + 128); }
+    __device__ float* z() const { return reinterpret_cast<float*>(base + z_off); }
+    __device__ float* part() const { return reinterpret_cast<float*>(base + part_off); }
+    __device__ uint8_t* b() const { return base + b_off; }
+    __device__ uint8_t* stage(int s) const { return base + stage_off + static_cast<uint32_t>(s) * kStageBytes; }
+};
+
+// Next item of a share: (t, u) in the share's order, without divisions.
+__device__ __forceinline__ void next_item(const Sched& sc, int& t, int& u) {
+    if (sc.tile_major) {
+        if (++u == sc.U) {
+            u = 0;
+            ++t;
+        }
+    } else if (++t == sc.T) {
+        t = 0;
+        ++u;
+    }
+}
+
+// sigma per activation row, the B fragments and the per-block zero-point sums for the CTA's
+// nblk blocks (consumer threads only).
+template <int TYPE, int NT, int TPW>
+__device__ __forceinline__ void fill_operands(const Smem& sm, const float* xs, int xpitch, int nblk, int M) {
+    using F = PnFmt<TYPE>;
+    using C = Cfg<TYPE, NT, TPW>;
+    constexpr int STEPS = F::PAIRS;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int klen = nblk * F::BLK;
+    uint32_t* maxbits = sm.maxbits();
+    float* sig_in = sm.sig_in();
+    float* sig_out = sm.sig_out();
+    // sigma: max |x| over the slice per row m (a non-negative float's bits order like its value)
     for (int m = 0; m < M; ++m) {
+        const uint4* xv = reinterpret_cast<const uint4*>(xs + m * xpitch);
         uint32_t mx = 0;
-        for (int i = tid; i < nvec; i += nct) {
-            const uint4 v = xv[m * nvec + i];
+        for (int i = tid; i < klen / 4; i += C::NCT) {
+            const uint4 v = xv[i];
             mx = max(mx, max(max(v.x & 0x7FFFFFFFu, v.y & 0x7FFFFFFFu), max(v.z & 0x7FFFFFFFu, v.w & 0x7FFFFFFFu)));
         }
         mx = __reduce_max_sync(0xffffffffu, mx);
-        if ((tid & 31) == 0) atomicMax(&maxbits[m], mx);
+        if (lane == 0) atomicMax(&maxbits[m], mx);
     }
-    named_sync(1, nct);
+    named_sync(1, C::NCT);
     if (tid < M) {
         const uint32_t bits = maxbits[tid];
         const int E = static_cast<int>(bits >> 23);
         int sg = (bits == 0 || E >= 255) ? 0 : 141 - E;  // max < 2^(E-126)
         sg = min(100, max(-100, sg));
         sig_in[tid] = exp2i(sg);
-        sig_out[tid] = exp2i(24 - sg);
+        sig_out[tid] = exp2i(24 - sg);  // undoes sigma and the 2^-24 of the subnormal codes
     }
-    named_sync(1, nct);
-}
-
-// B fragments of one block: for each n8 tile t, lanes 0..LU-1 (LU = lanes whose column is in
-// use) hold 2 registers per step; steps are grouped in pairs as 16-byte records [pair][lane],
-// an odd last step as 8-byte records [lane].
-__device__ __forceinline__ uint32_t bfrag_offset(const PnLayout& L, int M, int steps, int blk, int t, int l, int st,
-                                                 int r) {
-    const int LU = min(32, 8 * M - 32 * t);
-    uint32_t off = L.bfrag_off + blk * L.bfrag_unit + t * (256 * steps);
-    if ((steps & 1) && st == steps - 1)
-        off += (steps >> 1) * LU * 16 + l * 8 + r * 4;
-    else
-        off += (st >> 1) * LU * 16 + l * 16 + (st & 1) * 8 + r * 4;
-    return off;
-}
-
-template <int TYPE>
-__device__ void fill_fragments(int M, int nblocks, const float* xs, uint8_t* smem, const PnLayout& L, int nct) {
-    using F = PnFmt<TYPE>;
-    constexpr int STEPS = F::PAIRS;
-    const float* sig_in = reinterpret_cast<const float*>(smem + L.misc_off + 64);
-    const int klen = nblocks * F::BLK;
-    const int lanes = 8 * M;
-    // B fragments: one item per (pair of blocks, lane record); the block parity is unrolled
-    for (int idx = threadIdx.x; idx < (nblocks / 2) * lanes; idx += nct) {
-        const int bp = idx / lanes;
-        const int lr = idx - bp * lanes;
-        const int t = lr >> 5, l = lr & 31;
-        const int g = l >> 2, tig = l & 3;
-        const int col = 8 * t + g, m = col >> 1, part = col & 1;
+    named_sync(1, C::NCT);
+    // B fragments: per block, tile t, slice st and lane l the two registers b0 (decode register
+    // c = l % 4) and b1 (register c + 4) of column 8t + l / 4; paired slices share 16 bytes.
+    // Only lanes whose column is in use (l < 8M - 32t) are written: the others never read.
+    uint8_t* bbase = sm.b();
+    const int lanes = min(32, 8 * M);  // live lanes of tile 0 (and of every full tile)
+    const int items = nblk * NT * STEPS * lanes;
+    for (int it = tid; it < items; it += C::NCT) {
+        const int l = it % lanes;
+        int rest = it / lanes;
+        const int st = rest % STEPS;
+        rest /= STEPS;
+        const int t = rest % NT, blk = rest / NT;
+        const int n = 8 * t + (l >> 2), m = n >> 1, prt = n & 1;
+        if (n >= 2 * M) continue;
+        const float sc = sig_in[m] * step_scale<TYPE>(st);
+        const float* xb = xs + m * xpitch + blk * F::BLK;
+        const int odd = blk & 1;
+        uint32_t r[2];
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            const int i = (l & 3) + 4 * q;
+            r[q] = pack_half2(split_part(xb[pn_elem(F::CPW, odd, i, st, 0)] * sc, prt),
+                              split_part(xb[pn_elem(F::CPW, odd, i, st, 1)] * sc, prt));
+        }
+        const int off = blk * C::BFU + t * 256 * STEPS +
+                        (((STEPS & 1) && st == STEPS - 1) ? (STEPS / 2) * 512 + l * 8 : (st >> 1) * 512 + l * 16 + (st & 1) * 8);
+        *reinterpret_cast<uint2*>(bbase + off) = make_uint2(r[0], r[1]);
+    }
+    // Z = z * sum over the block of (2^-24 * 8^j) * (hi + lo): one warp per (block, m)
+    float* z = sm.z();
+    for (int pr = warp; pr < nblk * M; pr += C::CW) {
+        const int blk = pr / M, m = pr - blk * M;
+        const float* xb = xs + m * xpitch + blk * F::BLK;
         const float si = sig_in[m];
-#pragma unroll
-        for (int odd = 0; odd < 2; ++odd) {
-            const int b = 2 * bp + odd;  // slices start on a multiple of 8 blocks
-            const float* xb = xs + m * klen + b * F::BLK;
-#pragma unroll
-            for (int st = 0; st < STEPS; ++st) {
-                const float sc = si * step_scale<TYPE>(st);
-#pragma unroll
-                for (int r = 0; r < 2; ++r) {
-                    const int i = tig + 4 * r;
-                    const __half v0 = split_part(xb[pn_elem(F::CPW, odd, i, st, 0)] * sc, part);
-                    const __half v1 = split_part(xb[pn_elem(F::CPW, odd, i, st, 1)] * sc, part);
-                    *reinterpret_cast<uint32_t*>(smem + bfrag_offset(L, M, STEPS, b, t, l, st, r)) =
-                        pack_half2(v0, v1);
-                }
-            }
+        float s = 0.0f;
+        for (int e = lane; e < F::BLK; e += 32) {
+            const int j = (e % F::CPW) >> 1;
+            const float v = xb[e] * (si * step_scale<TYPE>(j));
+            const float hi = __half2float(__float2half_rn(v));
+            const float lo = __half2float(__float2half_rn(v - hi));
+            s = fmaf(5.9604644775390625e-08f * step_scale_inv<TYPE>(j), hi + lo, s);
         }
-    }
-    // z * sum over the block of what the decoded A multiplies (2^-24 * base^jj * B element):
-    // one warp per block, lanes over the block's elements, then a shuffle reduction
-    float* z = reinterpret_cast<float*>(smem + L.z_off);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = nct >> 5;
-    for (int b = warp; b < nblocks; b += nwarps) {
-        for (int m = 0; m < M; ++m) {
-            const float* xb = xs + m * klen + b * F::BLK;
-            const float si = sig_in[m];
-            float shi = 0.0f, slo = 0.0f;
-            for (int e = lane; e < F::BLK; e += 32) {
-                const float sc = step_scale<TYPE>((e % F::CPW) >> 1);
-                const float v = xb[e] * (si * sc);
-                const __half h = __float2half_rn(v);
-                const float hf = __half2float(h);
-                const float lf = __half2float(__float2half_rn(v - hf));
-                const float f = 5.9604644775390625e-08f / sc;  // 2^-24 * base^jj
-                shi = fmaf(f, hf, shi);
-                slo = fmaf(f, lf, slo);
-            }
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                shi += __shfl_xor_sync(0xffffffffu, shi, o);
-                slo += __shfl_xor_sync(0xffffffffu, slo, o);
-            }
-            if (lane == 0) {
-                z[b * 2 * M + 2 * m] = static_cast<float>(F::Z) * shi;
-                z[b * 2 * M + 2 * m + 1] = static_cast<float>(F::Z) * slo;
-            }
-        }
+        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+        if (lane == 0) z[blk * M + m] = static_cast<float>(F::Z) * s;
     }
+    named_sync(1, C::NCT);
 }
 
-// One block (ODD: starts 2 bytes past a 4-byte boundary) for the first `tiles` of kTP tiles:
-// rowp[tile][0] = row g, [1] = row g + 8 (stage addresses of the block's column).
-template <int TYPE, int NT, int ODD, bool FULL>
-__device__ __forceinline__ void pn_block(const uint8_t* const (&rowp)[kTP][2], int off, const uint8_t* bblk,
-                                         const float* zblk, const uint8_t* zero, int M, int lane, int tiles,
-                                         float (&acc)[kTP][NT][4]) {
+// One block B (of the unit, compile time) for the warp's TPW tiles: decode, multiply, fold
+// d * (c - Z) into acc[tile][t][row half].
+template <int TYPE, int NT, int TPW, int B>
+__device__ __forceinline__ void pn_block(const uint8_t* const (&row0)[TPW], int tig, uint32_t sel,
+                                         const uint8_t* bf, int lane, const bool (&live)[NT], const float* zb, int M,
+                                         float (&acc)[TPW][NT][2]) {
     using F = PnFmt<TYPE>;
     constexpr int STEPS = F::PAIRS;
-    const int tig = lane & 3;
-    float d[kTP][2];
-    uint32_t wa[kTP][2], wb[kTP][2];
-#pragma unroll
-    for (int tp = 0; tp < kTP; ++tp) {
-        if (FULL || tp < tiles) {
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const uint8_t* p = rowp[tp][h] + off;
-                d[tp][h] = __half2float(*reinterpret_cast<const __half*>(p));
-                if (ODD) {
-                    wa[tp][h] = *reinterpret_cast<const uint32_t*>(p + 2 + 4 * tig);
-                    wb[tp][h] = *reinterpret_cast<const uint32_t*>(p + 18 + 4 * tig);
-                } else {
-                    const uint32_t w0 = *reinterpret_cast<const uint32_t*>(p + 4 * tig);
-                    wb[tp][h] = *reinterpret_cast<const uint32_t*>(p + 16 + 4 * tig);
-                    const uint32_t x8 = *reinterpret_cast<const uint32_t*>(p + 32);
-                    const uint32_t pr = prmt(w0, x8, 0x5432u);
-                    wa[tp][h] = (tig == 0) ? pr : w0;
-                }
-            }
-        }
-    }
-    // B registers and zero-point corrections for this lane's columns (unused columns read zeros)
+    constexpr int OFF = kBlockBytes * B;
+    constexpr int SH = (TYPE == kTypePn3t) ? 9 : 8;
+    // B fragments (columns past 2M are zero and are not read)
     uint32_t b[NT][STEPS][2];
-    float zh[NT], zl[NT];
+    float zt[NT];
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
-        const int LU = min(32, 8 * M - 32 * t);
-        const bool live = lane < LU;
-        const uint8_t* base = bblk + t * (256 * STEPS);
+        const uint8_t* base = bf + t * 256 * STEPS;
 #pragma unroll
         for (int q = 0; q < STEPS / 2; ++q) {
-            const uint4 v = *reinterpret_cast<const uint4*>(live ? base + q * LU * 16 + lane * 16 : zero);
+            uint4 v = make_uint4(0u, 0u, 0u, 0u);
+            if (live[t]) v = *reinterpret_cast<const uint4*>(base + q * 512 + lane * 16);
             b[t][2 * q][0] = v.x;
             b[t][2 * q][1] = v.y;
             b[t][2 * q + 1][0] = v.z;
             b[t][2 * q + 1][1] = v.w;
         }
-        if (STEPS & 1) {
-            const uint2 v = *reinterpret_cast<const uint2*>(live ? base + (STEPS / 2) * LU * 16 + lane * 8 : zero);
+        if constexpr (STEPS & 1) {
+            uint2 v = make_uint2(0u, 0u);
+            if (live[t]) v = *reinterpret_cast<const uint2*>(base + (STEPS / 2) * 512 + lane * 8);
             b[t][STEPS - 1][0] = v.x;
             b[t][STEPS - 1][1] = v.y;
         }
         const int m = 4 * t + tig;
-        const float2 zz = *reinterpret_cast<const float2*>(m < M ? reinterpret_cast<const uint8_t*>(zblk + 2 * m) : zero);
-        zh[t] = zz.x;
-        zl[t] = zz.y;
+        zt[t] = (m < M) ? zb[m] : 0.0f;
     }
-    float c[kTP][NT][4];
-#define PNQ_STEP(J)                                                                                           \
-    {                                                                                                         \
-        _Pragma("unroll") for (int tp = 0; tp < kTP; ++tp) {                                                  \
-            if (FULL || tp < tiles) {                                                                         \
-                const uint32_t a0 = pn_code_pair<TYPE, J>(wa[tp][0]), a1 = pn_code_pair<TYPE, J>(wa[tp][1]);  \
-                const uint32_t a2 = pn_code_pair<TYPE, J>(wb[tp][0]), a3 = pn_code_pair<TYPE, J>(wb[tp][1]);  \
-                _Pragma("unroll") for (int t = 0; t < NT; ++t) {                                              \
-                    if (J == 0)                                                                               \
-                        mma_f16_16816_z(c[tp][t], a0, a1, a2, a3, b[t][J][0], b[t][J][1]);                     \
-                    else                                                                                      \
-                        mma_f16_16816(c[tp][t], a0, a1, a2, a3, b[t][J][0], b[t][J][1]);                       \
-                }                                                                                             \
-            }                                                                                                 \
-        }                                                                                                     \
-    }
-    PNQ_STEP(0)
-    PNQ_STEP(1)
-    PNQ_STEP(2)
-    PNQ_STEP(3)
-    if constexpr (STEPS == 5) PNQ_STEP(4)
-#undef PNQ_STEP
 #pragma unroll
-    for (int tp = 0; tp < kTP; ++tp) {
-        if (FULL || tp < tiles) {
+    for (int tp = 0; tp < TPW; ++tp) {
+        // rows g (h = 0) and g + 8 (h = 1): decode registers c and c + 4, block scale
+        uint32_t ra[2], rb[2];
+        float d[2];
 #pragma unroll
-            for (int t = 0; t < NT; ++t) {
-                acc[tp][t][0] = fmaf(d[tp][0], c[tp][t][0] - zh[t], acc[tp][t][0]);
-                acc[tp][t][1] = fmaf(d[tp][0], c[tp][t][1] - zl[t], acc[tp][t][1]);
-                acc[tp][t][2] = fmaf(d[tp][1], c[tp][t][2] - zh[t], acc[tp][t][2]);
-                acc[tp][t][3] = fmaf(d[tp][1], c[tp][t][3] - zl[t], acc[tp][t][3]);
+        for (int h = 0; h < 2; ++h) {
+            const uint8_t* rp = row0[tp] + h * 8 * kUnitBytes + OFF;
+            if constexpr ((B & 1) == 0) {
+                ra[h] = prmt(lds32(rp + 4 * tig), lds32(rp + 32), sel);
+                rb[h] = lds32(rp + 16 + 4 * tig);
+            } else {
+                ra[h] = lds32(rp + 2 + 4 * tig);
+                rb[h] = lds32(rp + 18 + 4 * tig);
             }
+            d[h] = ld_half(rp);
+        }
+        const uint32_t sa0 = ra[0] >> SH, sa1 = ra[1] >> SH, sb0 = rb[0] >> SH, sb1 = rb[1] >> SH;
+        float c[NT][4];
+#define PNQ_SLICE(J)                                                                                         \
+    if constexpr (J < STEPS) {                                                                               \
+        const uint32_t a0 = code_pair<TYPE, J>(ra[0], sa0), a1 = code_pair<TYPE, J>(ra[1], sa1);             \
+        const uint32_t a2 = code_pair<TYPE, J>(rb[0], sb0), a3 = code_pair<TYPE, J>(rb[1], sb1);             \
+        _Pragma("unroll") for (int t = 0; t < NT; ++t) {                                                     \
+            if constexpr (J == 0)                                                                            \
+                mma_f16_16816_z(c[t], a0, a1, a2, a3, b[t][J][0], b[t][J][1]);                               \
+            else                                                                                             \
+                mma_f16_16816(c[t], a0, a1, a2, a3, b[t][J][0], b[t][J][1]);                                 \
+        }                                                                                                    \
+    }
+        PNQ_SLICE(0)
+        PNQ_SLICE(1)
+        PNQ_SLICE(2)
+        PNQ_SLICE(3)
+        PNQ_SLICE(4)
+#undef PNQ_SLICE
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+            acc[tp][t][0] = fmaf(d[0], (c[t][0] + c[t][1]) - zt[t], acc[tp][t][0]);
+            acc[tp][t][1] = fmaf(d[1], (c[t][2] + c[t][3]) - zt[t], acc[tp][t][1]);
         }
     }
 }
 
-// ---- the kernel ---------------------------------------------------------------------------------
+template <int TYPE, int NT, int TPW, int H>
+__device__ __forceinline__ void consumer_loop(const Smem& sm, const Ctx& cx, long long i0, int n_items, int u0) {
+    using C = Cfg<TYPE, NT, TPW>;
+    const Sched& sc = cx.sc;
+    const int M = cx.M, NS = cx.NS, U = sc.U;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, tig = lane & 3;
+    const int tg = warp % C::TG;  // tile group: rows 16 * TPW * tg ..
+    const uint32_t sel = (tig == 0) ? 0x5432u : 0x3210u;  // even blocks: register 0 pairs words 0 and 7
+    bool live[NT];
+#pragma unroll
+    for (int t = 0; t < NT; ++t) live[t] = (8 * t + g) < 2 * M;
+    const float* z = sm.z();
+    const float* sig_out = sm.sig_out();
+    float* part = sm.part();
+    bool ok = true;
+    float acc[TPW][NT][2];
+#pragma unroll
+    for (int tp = 0; tp < TPW; ++tp)
+#pragma unroll
+        for (int t = 0; t < NT; ++t) acc[tp][t][0] = acc[tp][t][1] = 0.0f;
+    int e = 0;  // row sums handed to the reducer so far
+    // hand the row sums of the tile just finished to the reducer (scaled back), then clear them
+    auto emit = [&]() {
+        const int buf = e & 1;
+        if (e >= 2 && !mbar_wait_warp(sm.part_free(buf), ((e >> 1) - 1) & 1)) {
+            ok = false;
+            return;
+        }
+#pragma unroll
+        for (int tp = 0; tp < TPW; ++tp)
+#pragma unroll
+            for (int t = 0; t < NT; ++t) {
+                const int m = 4 * t + tig;
+                if (m < M) {
+                    float* dst = part + ((H * 2 + buf) * M + m) * kPartPitch + 16 * (TPW * tg + tp) + g;
+                    dst[0] = acc[tp][t][0] * sig_out[m];
+                    dst[8] = acc[tp][t][1] * sig_out[m];
+                }
+                acc[tp][t][0] = acc[tp][t][1] = 0.0f;
+            }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sm.part_full(buf));
+        ++e;
+    };
+    int t_i = sc.tile_of(i0), u_i = sc.unit_of(i0);
+    int cur_t = t_i;
+    for (int gi = 0; gi < n_items && ok; ++gi, next_item(sc, t_i, u_i)) {
+        if (t_i != cur_t) {
+            emit();
+            if (!ok) break;
+            cur_t = t_i;
+        }
+        const int slot = (u_i >= u0) ? u_i - u0 : u_i - u0 + U;
+        const int s = gi % NS;
+        if (!mbar_wait_warp(sm.full(s), (gi / NS) & 1)) {
+            ok = false;
+            break;
+        }
+        const uint8_t* stage = sm.stage(s);
+        const uint8_t* row0[TPW];
+#pragma unroll
+        for (int tp = 0; tp < TPW; ++tp) row0[tp] = stage + (16 * (TPW * tg + tp) + g) * kUnitBytes;
+        const int blk0 = slot * kUnitBlocks + kHalfBlocks * H;
+        const uint8_t* bf0 = sm.b() + blk0 * C::BFU;
+        const float* z0 = z + blk0 * M;
+        pn_block<TYPE, NT, TPW, kHalfBlocks * H + 0>(row0, tig, sel, bf0 + 0 * C::BFU, lane, live, z0 + 0 * M, M, acc);
+        pn_block<TYPE, NT, TPW, kHalfBlocks * H + 1>(row0, tig, sel, bf0 + 1 * C::BFU, lane, live, z0 + 1 * M, M, acc);
+        pn_block<TYPE, NT, TPW, kHalfBlocks * H + 2>(row0, tig, sel, bf0 + 2 * C::BFU, lane, live, z0 + 2 * M, M, acc);
+        pn_block<TYPE, NT, TPW, kHalfBlocks * H + 3>(row0, tig, sel, bf0 + 3 * C::BFU, lane, live, z0 + 3 * M, M, acc);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sm.empty(s));
+    }
+    if (ok && n_items > 0) emit();
+    if (!ok && lane == 0) record_error(cx.err, kErrFullWait);
+}
 
-template <int TYPE, int NT, int kRW>
-__global__ void __launch_bounds__(32 * (kRW + 1), 1) pn_gemv_kernel(const __grid_constant__ PnArgs a) {
+// Reducer side of one share of tile t (consecutive items of this CTA, units u_first ..
+// u_first+n-1):
+// add the two halves; a whole tile goes to Y, a part to its workspace slot, and the share that
+// completes the tile sums the tile's slots in unit order into Y.
+template <int MAXM>
+__device__ __forceinline__ void reduce_share(const Ctx& a, const Smem& sm, int buf, int t, int u_first, int n_units,
+                                             int lane) {
+    const Sched& sc = a.sc;
+    const int row = t * kTileRows + 4 * lane;
+    auto put_y = [&](int m, float4 v) {
+        float* y = a.Y + static_cast<size_t>(m) * a.N;
+        if (row + 0 < a.N) y[row + 0] = v.x;
+        if (row + 1 < a.N) y[row + 1] = v.y;
+        if (row + 2 < a.N) y[row + 2] = v.z;
+        if (row + 3 < a.N) y[row + 3] = v.w;
+    };
+    // the two halves' row sums into registers; the buffer goes back to the consumers at once
+    const float* part = sm.part();
+    float4 v[MAXM];
+#pragma unroll
+    for (int m = 0; m < MAXM; ++m) {
+        if (m < a.M) {
+            const float4 p0 = reinterpret_cast<const float4*>(part + ((0 * 2 + buf) * a.M + m) * kPartPitch)[lane];
+            const float4 p1 = reinterpret_cast<const float4*>(part + ((1 * 2 + buf) * a.M + m) * kPartPitch)[lane];
+            v[m] = make_float4(p0.x + p1.x, p0.y + p1.y, p0.z + p1.z, p0.w + p1.w);
+        }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(sm.part_free(buf));
+    if (n_units == sc.U) {
+#pragma unroll
+        for (int m = 0; m < MAXM; ++m)
+            if (m < a.M) put_y(m, v[m]);
+        return;
+    }
+    float* slot = a.ws + (static_cast<size_t>(t) * sc.U + u_first) * a.M * kTileRows;
+#pragma unroll
+    for (int m = 0; m < MAXM; ++m)
+        if (m < a.M) __stcg(reinterpret_cast<float4*>(slot + m * kTileRows) + lane, v[m]);
+    __threadfence();
+    __syncwarp();
+    // shares of tile t: a share is a run of consecutive items of one CTA, so one starts at unit
+    // 0 and wherever the previous unit is not the previous item of the same CTA
+    auto starts = [&](int c0) {
+        const int u = c0 + lane;
+        bool st = false;
+        if (u < sc.U) {
+            const long long it = sc.item(t, u);
+            st = (u == 0) || sc.item(t, u - 1) != it - 1 || sc.owner(it) != sc.owner(it - 1);
+        }
+        return __ballot_sync(0xffffffffu, st);
+    };
+    int shares = 0;
+    for (int c0 = 0; c0 < sc.U; c0 += 32) shares += __popc(starts(c0));
+    unsigned old = 0;
+    if (lane == 0) old = atomicAdd(a.cnt + t, 1u);
+    old = __shfl_sync(0xffffffffu, old, 0);
+    if (old != static_cast<unsigned>(shares - 1)) return;
+    __threadfence();
+    for (int m = 0; m < a.M; ++m) {
+        float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        for (int c0 = 0; c0 < sc.U; c0 += 32) {
+            unsigned mask = starts(c0);
+            while (mask) {
+                const int u = c0 + __ffs(mask) - 1;
+                mask &= mask - 1;
+                const float4 v = __ldcg(
+                    reinterpret_cast<const float4*>(a.ws + ((static_cast<size_t>(t) * sc.U + u) * a.M + m) * kTileRows) +
+                    lane);
+                acc.x += v.x;
+                acc.y += v.y;
+                acc.z += v.z;
+                acc.w += v.w;
+            }
+        }
+        put_y(m, acc);
+    }
+    __syncwarp();
+    if (lane == 0) a.cnt[t] = 0u;  // ready for the next launch
+}
+
+template <int TYPE, int NT, int TPW>
+__global__ void __launch_bounds__(Cfg<TYPE, NT, TPW>::THREADS, 1) pn_gemv_kernel(const __grid_constant__ PnArgs a) {
     using F = PnFmt<TYPE>;
-    constexpr int STEPS = F::PAIRS;
-    constexpr int kBlkPerWarp = kCols * kColBlocks / kRW;  // blocks of a stage per consumer warp (even)
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-
-    const uint32_t rank = (a.S > 1) ? cluster_ctarank() : 0u;
-    const int units_max = (a.units + a.S - 1) / a.S;
-    const PnLayout L = make_pn_layout(STEPS, F::BLK, a.M, NT, kRW, units_max, a.NS, a.S);
-    // this CTA's K slice, in 8-block units
-    const int u0 = static_cast<int>((static_cast<int64_t>(rank) * a.units) / a.S);
-    const int nunits = static_cast<int>((static_cast<int64_t>(rank + 1) * a.units) / a.S) - u0;
-    const int nchunks = (nunits + kCols - 1) / kCols;
+    using C = Cfg<TYPE, NT, TPW>;
+    constexpr int UK = kUnitBlocks * F::BLK;  // weights of a row per unit
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* base = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+    const Smem sm{base, smem_addr(base + a.bar_off), a.NS, a.misc_off, a.z_off, a.part_off, a.b_off, a.stage_off};
+    const Ctx cx{a.sc, a.X, a.Y, a.ws, a.cnt, a.err, a.N, a.K, a.M, a.NS, a.x_stage, a.xpitch, a.flags};
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    // this cluster's tiles: a balanced contiguous share of the 16-row tiles
-    const int T16 = (a.N + 15) / 16;
-    const int cl = blockIdx.y, ncl = gridDim.y;
-    const int t_begin = static_cast<int>((static_cast<int64_t>(cl) * T16) / ncl);
-    const int t_end = static_cast<int>((static_cast<int64_t>(cl + 1) * T16) / ncl);
-    const int npasses = (t_end - t_begin + kTP - 1) / kTP;
-    const int total_chunks = npasses * nchunks;
-
-    const uint32_t bar0 = smem_addr(smem + L.bar_off);
-    auto full_bar = [&](int s) { return bar0 + 8u * s; };
-    auto empty_bar = [&](int s) { return bar0 + 8u * (a.NS + s); };
-    const uint32_t x_ready = bar0 + 8u * (2 * a.NS);
-    const uint32_t x_free = bar0 + 8u * (2 * a.NS + 1);
-    auto red_full = [&](int b) { return bar0 + 8u * (2 * a.NS + 2 + b); };
-    auto red_free = [&](int b) { return bar0 + 8u * (2 * a.NS + 4 + b); };
-    uint32_t* misc = reinterpret_cast<uint32_t*>(smem + L.misc_off);
-    float* xs = reinterpret_cast<float*>(smem + L.stage_off + L.x_stage * kStageBytes);
+    // this CTA's share of the items, and the K units it touches (slot = (u - u0) mod U)
+    const Sched& sc = cx.sc;
+    const long long i0 = sc.first(blockIdx.x), i1 = sc.first(blockIdx.x + 1);
+    const int n_items = static_cast<int>(i1 - i0);
+    const int u0 = n_items > 0 ? sc.unit_of(i0) : 0;
+    const int span = sc.span(i0, i1);
+    const int nblk = span * kUnitBlocks;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < a.NS; ++s) {
-            mbar_init(full_bar(s), 1);
-            mbar_init(empty_bar(s), kRW);
+            mbar_init(sm.full(s), 1);
+            mbar_init(sm.empty(s), C::CW);
         }
-        mbar_init(x_ready, 1);
-        mbar_init(x_free, 1);
+        mbar_init(sm.x_ready(), 1);
+        mbar_init(sm.x_free(), 1);
         for (int b = 0; b < 2; ++b) {
-            mbar_init(red_full(b), a.S);
-            mbar_init(red_free(b), a.S);
+            mbar_init(sm.part_full(b), C::CW);
+            mbar_init(sm.part_free(b), 1);
         }
         mbar_fence_init();
         griddep_launch_dependents();
     }
-    if (threadIdx.x < 16) {
-        misc[threadIdx.x] = 0u;                                                // maxbits
-        reinterpret_cast<uint32_t*>(smem + L.zero_off)[threadIdx.x] = 0u;      // zero area
-    }
-    if (threadIdx.x == 16) misc[48] = 0u;  // issued
+    if (threadIdx.x < 16) sm.maxbits()[threadIdx.x] = 0u;
     __syncthreads();
-    if (a.S > 1) cluster_sync();  // every CTA's barriers exist before any remote arrive
 
-    if (warp == kRW) {
-        // ---------------- producer warp ----------------
-        const uint64_t pol = l2_policy_evict_first();
-        bool ok = true;
-        auto issue = [&](int gch) {
-            const int p = gch / nchunks, c = gch - p * nchunks;
-            const int s = gch % a.NS;
-            if (gch >= a.NS) {
-                if (!mbar_wait_bounded(empty_bar(s), ((gch / a.NS) - 1) & 1)) return false;
-            } else if (s >= static_cast<int>(L.x_stage)) {
-                if (!mbar_wait_bounded(x_free, 0)) return false;
-            }
-            if (lane == 0) {
-                const int t0 = t_begin + p * kTP;
-                const int tiles = min(kTP, t_end - t0);
-                const int ncol = min(kCols, nunits - c * kCols);
-                const uint32_t dst = smem_addr(smem + L.stage_off + s * kStageBytes);
-                if (tiles == kTP) {
-                    mbar_arrive_expect_tx(full_bar(s), static_cast<uint32_t>(ncol * kBoxBytes));
-                    for (int h = 0; h < ncol; ++h)
-                        tma_load_2d(dst + h * kBoxBytes, &a.map_pass, (u0 + c * kCols + h) * kColU32, 16 * t0, full_bar(s),
-                                    pol);
-                } else {
-                    mbar_arrive_expect_tx(full_bar(s), static_cast<uint32_t>(ncol * tiles * kTileBoxBytes));
-                    for (int h = 0; h < ncol; ++h)
-                        for (int t = 0; t < tiles; ++t)
-                            tma_load_2d(dst + h * kBoxBytes + t * kTileBoxBytes, &a.map_tile,
-                                        (u0 + c * kCols + h) * kColU32, 16 * (t0 + t), full_bar(s), pol);
+    if (warp == C::PRODUCER) {
+        // ---------------- producer: x slice + one tensor-map copy per item ----------------
+        if (lane == 0 && n_items > 0) {
+            const uint64_t pol = l2_policy_evict_first();
+            bool ok = true;
+            int t_n = sc.tile_of(i0), u_n = sc.unit_of(i0);  // next item to request
+            auto issue = [&](int gi) {
+                const int s = gi % cx.NS;
+                if (gi >= cx.NS) {
+                    if (!mbar_wait_bounded(sm.empty(s), ((gi / cx.NS) - 1) & 1)) return false;
+                } else if (s >= cx.x_stage) {
+                    if (!mbar_wait_bounded(sm.x_free(), 0)) return false;
                 }
+                mbar_arrive_expect_tx(sm.full(s), static_cast<uint32_t>(kStageBytes));
+                tma_load_2d(smem_addr(sm.stage(s)), &a.map, u_n * kUnitU32, t_n * kTileRows, sm.full(s), pol);
+                next_item(sc, t_n, u_n);
+                return true;
+            };
+            int gi = 0;
+            if (cx.flags & kStaticWeights) {
+                // the weights are not written by earlier work in the stream: start streaming
+                // them into the stages that will not hold x before the previous grid completes
+                for (; ok && gi < min(n_items, cx.x_stage); ++gi) ok = issue(gi);
             }
-            __syncwarp();
-            return true;
-        };
-        int gch = 0;
-        if (a.flags & kStaticWeights) {
-            // weights are declared unchanged by earlier work: stream them into the stages that do
-            // not hold x before the previous grid in the stream has finished
-            for (; ok && gch < min(total_chunks, static_cast<int>(L.x_stage)); ++gch) ok = issue(gch);
+            griddep_wait();
+            // x rows at pitch xpitch floats in slot order: units u0 .. U-1 then 0 .. (one or two
+            // bulk copies per row; 16-byte aligned: X is, units are multiples of 512 elements and
+            // the pitch is a multiple of 4)
+            const int run1 = min(span, sc.U - u0);
+            const uint32_t b1 = static_cast<uint32_t>(run1 * UK * 4), b2 = static_cast<uint32_t>((span - run1) * UK * 4);
+            mbar_arrive_expect_tx(sm.x_ready(), (b1 + b2) * cx.M);
+            for (int m = 0; m < cx.M; ++m) {
+                const uint32_t dst = smem_addr(sm.stage(cx.x_stage)) + m * cx.xpitch * 4;
+                const float* xm = cx.X + static_cast<size_t>(m) * cx.K;
+                bulk_g2s_plain(dst, xm + static_cast<size_t>(u0) * UK, b1, sm.x_ready());
+                if (b2) bulk_g2s_plain(dst + b1, xm, b2, sm.x_ready());
+            }
+            for (; ok && gi < n_items; ++gi) ok = issue(gi);
+            if (!ok) record_error(cx.err, kErrEmptyWait);
+            // every copy issued has landed before the CTA may exit
+            bool drained = mbar_wait_bounded(sm.x_ready(), 0);
+            for (int gg = max(0, gi - cx.NS); drained && gg < gi; ++gg)
+                drained = mbar_wait_bounded(sm.full(gg % cx.NS), (gg / cx.NS) & 1);
+            if (!drained) record_error(cx.err, kErrDrainWait);
         }
-        griddep_wait();
-        {
-            // the CTA's slice of x: one bulk copy per activation row (16-byte aligned: X is, and the
-            // slice starts at a multiple of 512 elements)
-            const uint32_t xbytes = static_cast<uint32_t>(nunits * kColBlocks * F::BLK * 4);
-            if (lane == 0) mbar_arrive_expect_tx(x_ready, xbytes * a.M);
-            __syncwarp();
-            const float* xsrc = a.X + static_cast<size_t>(u0) * kColBlocks * F::BLK;
-            if (lane < a.M)
-                bulk_g2s_plain(smem_addr(xs) + lane * xbytes, xsrc + static_cast<size_t>(lane) * a.K, xbytes, x_ready);
-        }
-        for (; ok && gch < total_chunks; ++gch) ok = issue(gch);
-        if (!ok && lane == 0) record_error(a.err, kErrEmptyWait);
-        if (lane == 0) misc[48] = static_cast<uint32_t>(ok ? total_chunks : gch);
-    } else {
-        // ---------------- consumer warps ----------------
-        constexpr int nct = 32 * kRW;
-        const int nblocks = nunits * kColBlocks;
-        if (!mbar_wait_bounded(x_ready, 0) && lane == 0) record_error(a.err, kErrFullWait);
-        compute_sigma(a.M, xs, nblocks * F::BLK, smem + L.misc_off, nct);
-        fill_fragments<TYPE>(a.M, nblocks, xs, smem, L, nct);
-        named_sync(1, nct);
-        if (threadIdx.x == 0) mbar_arrive(x_free);  // the x stages may now take weights
-
-        const int g = lane >> 2, tig = lane & 3;
-        const float* sig_out = reinterpret_cast<const float*>(smem + L.misc_off + 128);
-        const uint8_t* zero = smem + L.zero_off;
-        const float* zarr = reinterpret_cast<const float*>(smem + L.z_off);
-        float* red = reinterpret_cast<float*>(smem + L.red_off);
-        const uint32_t part_addr = smem_addr(smem + L.part_off);
-        const uint32_t part_stride = 4u * kRows * a.M;  // bytes per pass buffer
-        const int hcol = (warp * kBlkPerWarp) / kColBlocks;  // the stage column this warp reads
-        const int cblk = (warp * kBlkPerWarp) % kColBlocks;  // its first block within the column
-        bool ok = true;
-        int p = 0;
-        for (; p < npasses && ok; ++p) {
-            const int t0 = t_begin + p * kTP;
-            const int tiles = min(kTP, t_end - t0);
-            const int rbase = 16 * t0;
-            float acc[kTP][NT][4];
-#pragma unroll
-            for (int tp = 0; tp < kTP; ++tp)
-#pragma unroll
-                for (int t = 0; t < NT; ++t) acc[tp][t][0] = acc[tp][t][1] = acc[tp][t][2] = acc[tp][t][3] = 0.0f;
-            for (int c = 0; c < nchunks; ++c) {
-                const int gch = p * nchunks + c;
-                const int s = gch % a.NS;
-                if (!mbar_wait_bounded(full_bar(s), (gch / a.NS) & 1)) {
-                    if (lane == 0) record_error(a.err, kErrFullWait);
+        __syncwarp();
+    } else if (warp == C::REDUCER) {
+        // ---------------- reducer: row sums -> Y or workspace ----------------
+        if (n_items > 0) {
+            griddep_wait();  // the workspace, the counters and Y belong to earlier grids until now
+            bool ok = true;
+            int e = 0;
+            int t_i = sc.tile_of(i0), u_i = sc.unit_of(i0);
+            int u_first = u_i, n_run = 0;  // the current share: first unit, items so far
+            for (int gi = 0; gi < n_items && ok; ++gi) {
+                const int t_cur = t_i;
+                ++n_run;
+                next_item(sc, t_i, u_i);
+                if (gi + 1 < n_items && t_i == t_cur) continue;
+                const int buf = e & 1;
+                if (!mbar_wait_warp(sm.part_full(buf), (e >> 1) & 1)) {
                     ok = false;
                     break;
                 }
-                if (c * kCols + hcol < nunits) {
-                    const uint8_t* colp = smem + L.stage_off + s * kStageBytes + hcol * kBoxBytes;
-                    const uint8_t* rowp[kTP][2];
-#pragma unroll
-                    for (int tp = 0; tp < kTP; ++tp) {
-                        rowp[tp][0] = colp + (16 * tp + g) * kColBytes;
-                        rowp[tp][1] = rowp[tp][0] + 8 * kColBytes;
-                    }
-#pragma unroll
-                    for (int j = 0; j < kBlkPerWarp; j += 2) {
-                        const int blk = (c * kCols + hcol) * kColBlocks + cblk + j;  // block index in the slice
-                        const uint8_t* b0 = smem + L.bfrag_off + blk * L.bfrag_unit;
-                        const float* z0 = zarr + blk * 2 * a.M;
-                        const int off = kBlockBytes * (cblk + j);
-                        if (tiles == kTP) {
-                            pn_block<TYPE, NT, 0, true>(rowp, off, b0, z0, zero, a.M, lane, tiles, acc);
-                            pn_block<TYPE, NT, 1, true>(rowp, off + kBlockBytes, b0 + L.bfrag_unit, z0 + 2 * a.M, zero,
-                                                        a.M, lane, tiles, acc);
-                        } else {
-                            pn_block<TYPE, NT, 0, false>(rowp, off, b0, z0, zero, a.M, lane, tiles, acc);
-                            pn_block<TYPE, NT, 1, false>(rowp, off + kBlockBytes, b0 + L.bfrag_unit, z0 + 2 * a.M, zero,
-                                                         a.M, lane, tiles, acc);
-                        }
-                    }
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(empty_bar(s));
+                reduce_share<4 * NT>(cx, sm, buf, t_cur, u_first, n_run, lane);
+                ++e;
+                u_first = u_i;
+                n_run = 0;
             }
-            if (!ok) break;
-
-            // ---- reduce the warps' K shares, then (S > 1) the cluster's K slices
-            const int b = p & 1;
-#pragma unroll
-            for (int tp = 0; tp < kTP; ++tp)
-                if (tp < tiles)
-#pragma unroll
-                    for (int t = 0; t < NT; ++t)
-                        *reinterpret_cast<float4*>(red + ((((warp * kTP + tp) * NT + t) * 32 + lane) * 4)) =
-                            make_float4(acc[tp][t][0], acc[tp][t][1], acc[tp][t][2], acc[tp][t][3]);
-            if (a.S > 1 && p >= 2 && !mbar_wait_cluster_bounded(red_free(b), ((p - 2) >> 1) & 1)) {
-                if (lane == 0) record_error(a.err, kErrReduceWait);
-                ok = false;
-            }
-            named_sync(1, nct);
-            if (warp < tiles) {
-                float sum[NT][4];
-#pragma unroll
-                for (int t = 0; t < NT; ++t) sum[t][0] = sum[t][1] = sum[t][2] = sum[t][3] = 0.0f;
-#pragma unroll
-                for (int w = 0; w < kRW; ++w)
-#pragma unroll
-                    for (int t = 0; t < NT; ++t) {
-                        const float4 v = *reinterpret_cast<const float4*>(red + ((((w * kTP + warp) * NT + t) * 32 + lane) * 4));
-                        sum[t][0] += v.x;
-                        sum[t][1] += v.y;
-                        sum[t][2] += v.z;
-                        sum[t][3] += v.w;
-                    }
-#pragma unroll
-                for (int t = 0; t < NT; ++t) {
-                    const int m = 4 * t + tig;
-                    if (m < a.M) {
-                        const float so = sig_out[m];
-                        const float y0 = (sum[t][0] + sum[t][1]) * so;
-                        const float y1 = (sum[t][2] + sum[t][3]) * so;
-                        const int ra = 16 * warp + g, rb = ra + 8;
-                        if (a.S == 1) {
-                            if (rbase + ra < a.N) a.Y[static_cast<size_t>(m) * a.N + rbase + ra] = y0;
-                            if (rbase + rb < a.N) a.Y[static_cast<size_t>(m) * a.N + rbase + rb] = y1;
-                        } else {
-                            float* part = reinterpret_cast<float*>(smem + L.part_off + b * part_stride);
-                            part[ra * a.M + m] = y0;
-                            part[rb * a.M + m] = y1;
-                        }
-                    }
-                }
-            }
-            named_sync(1, nct);
-            if (a.S > 1) {
-                // this CTA's partial rows of the pass are complete: tell every rank
-                if (threadIdx.x == 0) {
-                    fence_acq_rel_cluster();
-                    for (int q = 0; q < a.S; ++q) mbar_arrive_remote(mapa_shared(red_full(b), q));
-                }
-                if (!mbar_wait_cluster_bounded(red_full(b), (p >> 1) & 1)) {
-                    if (lane == 0) record_error(a.err, kErrReduceWait);
-                    ok = false;
-                }
-                // rank r finishes the tiles t with t % S == r: sum the S partials in rank order
-                const uint32_t pb = part_addr + b * part_stride;
-                for (int idx = threadIdx.x; idx < tiles * 16 * a.M; idx += nct) {
-                    const int rr = idx / a.M, m = idx - rr * a.M;
-                    if (((rr >> 4) % a.S) != static_cast<int>(rank) || rbase + rr >= a.N) continue;
-                    float sum = 0.0f;
-                    for (int q = 0; q < a.S; ++q) sum += ld_dsmem_f32_at(mapa_shared(pb + 4u * idx, q));
-                    a.Y[static_cast<size_t>(m) * a.N + rbase + rr] = sum;
-                }
-                named_sync(1, nct);
-                if (threadIdx.x == 0) {
-                    fence_acq_rel_cluster();
-                    for (int q = 0; q < a.S; ++q) mbar_arrive_remote(mapa_shared(red_free(b), q));
-                }
+            if (!ok && lane == 0) record_error(cx.err, kErrReduceWait);
+        }
+    } else {
+        // ---------------- consumer warps ----------------
+        if (n_items > 0) {
+            if (named_sync_and(1, C::NCT, mbar_wait_bounded(sm.x_ready(), 0))) {
+                const float* xs = reinterpret_cast<const float*>(sm.stage(cx.x_stage));
+                fill_operands<TYPE, NT, TPW>(sm, xs, cx.xpitch, nblk, cx.M);
+                if (threadIdx.x == 0) mbar_arrive(sm.x_free());  // the x stages may now take weights
+                if (warp < C::TG)
+                    consumer_loop<TYPE, NT, TPW, 0>(sm, cx, i0, n_items, u0);
+                else
+                    consumer_loop<TYPE, NT, TPW, 1>(sm, cx, i0, n_items, u0);
+            } else if (threadIdx.x == 0) {
+                record_error(cx.err, kErrFullWait);
             }
         }
-        if (a.S > 1) {
-            // every rank has finished reading this CTA's last partial buffers
-            for (int q = max(0, p - 2); q < p; ++q)
-                if (!mbar_wait_cluster_bounded(red_free(q & 1), (q >> 1) & 1) && lane == 0)
-                    record_error(a.err, kErrReduceWait);
-        }
     }
-
-    __syncthreads();
-    // Drain: no CTA leaves while a copy it issued may still be writing its shared memory.
-    if (warp == kRW && lane == 0) {
-        if (!mbar_wait_bounded(x_ready, 0)) record_error(a.err, kErrDrainWait);
-        const int issued = static_cast<int>(misc[48]);
-        for (int c = max(0, issued - a.NS); c < issued; ++c)
-            if (!mbar_wait_bounded(full_bar(c % a.NS), (c / a.NS) & 1)) record_error(a.err, kErrDrainWait);
-    }
-    if (a.S > 1) cluster_sync();  // no CTA leaves while a peer may still address its shared memory
 }
 
 // ---- host side --------------------------------------------------------------------------------------
 
-using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                              const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                              CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+uint32_t align_up(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
 
-EncodeFn tensor_map_encoder() {
-    static EncodeFn fn = [] {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q{};
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
-                cudaSuccess ||
-            q != cudaDriverEntryPointSuccess)
-            return static_cast<EncodeFn>(nullptr);
-        return reinterpret_cast<EncodeFn>(p);
-    }();
-    return fn;
-}
+struct Plan {
+    Sched sc{};
+    int NS = 0, x_stage = 0, span_max = 0, xpitch = 0;
+    uint32_t bar_off = 0, misc_off = 0, z_off = 0, part_off = 0, b_off = 0, stage_off = 0, total = 0;
+};
 
-// Weights viewed as u32 [N][row_bytes / 4]; box {68, rows}. Rows past N read as zeros.
-bool encode_weight_map(CUtensorMap* map, const uint8_t* W, int64_t N, int64_t row_bytes, int box_rows) {
-    EncodeFn enc = tensor_map_encoder();
-    if (!enc) return false;
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(row_bytes / 4), static_cast<cuuint64_t>(N)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_bytes)};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kColU32), static_cast<cuuint32_t>(box_rows)};
-    const cuuint32_t estr[2] = {1, 1};
-    return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint8_t*>(W), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-template <int TYPE, int NT, int kRW>
-cudaError_t prepare_kernel(int S, size_t smem_bytes) {
-    auto kern = pn_gemv_kernel<TYPE, NT, kRW>;
-    // raised once per device and size (so never while a stream is being captured after the first
-    // eager call)
-    static size_t opted[64] = {};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (opted[dev] < smem_bytes) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_bytes));
-        if (e != cudaSuccess) return e;
-        opted[dev] = smem_bytes;
-    }
-    (void)S;
-    return cudaSuccess;
-}
-
-// Co-resident clusters of S CTAs with this shared-memory size (cached per device, S, size).
-template <int TYPE, int NT, int kRW>
-int resident_clusters(int S, size_t smem_bytes) {
-    struct Entry { int dev, S; size_t smem; int n; };
-    static Entry cache[64];
-    static int used = 0;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-    for (int i = 0; i < used; ++i)
-        if (cache[i].dev == dev && cache[i].S == S && cache[i].smem == smem_bytes) return cache[i].n;
-    if (prepare_kernel<TYPE, NT, kRW>(S, smem_bytes) != cudaSuccess) return 0;
-    auto kern = pn_gemv_kernel<TYPE, NT, kRW>;
-    int n = 0;
-    if (S == 1) {
-        int per_sm = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 32 * (kRW + 1), smem_bytes) != cudaSuccess)
-            return 0;
-        n = per_sm * device_sm_count();
-    } else {
-        cudaLaunchConfig_t cfg{};
-        cfg.gridDim = dim3(S, 1024, 1);
-        cfg.blockDim = dim3(32 * (kRW + 1), 1, 1);
-        cfg.dynamicSmemBytes = smem_bytes;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = S;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
-            cudaGetLastError();
-            return 0;
+// Shared-memory layout and stage count for one item order; false when it does not fit.
+bool layout(int blk_weights, int bfu, int M, int ns_req, Plan& p) {
+    p.span_max = 0;
+    for (long long c = 0; c < p.sc.G; ++c)
+        p.span_max = std::max(p.span_max, p.sc.span(p.sc.first(c), p.sc.first(c + 1)));
+    const uint32_t nblk = static_cast<uint32_t>(p.span_max) * kUnitBlocks;
+    p.xpitch = static_cast<int>(nblk) * blk_weights + 4;
+    p.bar_off = 0;
+    p.misc_off = 8u * (2 * kMaxStages + 6);
+    p.z_off = align_up(p.misc_off + 192u, 16);
+    p.part_off = align_up(p.z_off + nblk * M * 4u, 16);
+    p.b_off = align_up(p.part_off + 4u * M * kPartPitch * 4u, 128);
+    p.stage_off = align_up(p.b_off + nblk * static_cast<uint32_t>(bfu), 1024);
+    const uint64_t xbytes = static_cast<uint64_t>(M) * p.xpitch * 4u;
+    const int x_stages = static_cast<int>((xbytes + kStageBytes - 1) / kStageBytes);
+    for (int ns = kMaxStages; ns >= 2; --ns) {
+        if (ns_req > 0 && ns != ns_req) continue;
+        const uint64_t total = p.stage_off + static_cast<uint64_t>(ns) * kStageBytes;
+        // at least three stages unless forced, and one stage free of x when the ring allows it
+        if (total + 1024u <= kSmemLimit && ns >= x_stages && (ns_req > 0 || ns >= 3)) {
+            p.NS = ns;
+            p.x_stage = ns - x_stages;
+            p.total = static_cast<uint32_t>(total);
+            return true;
         }
     }
-    if (used < 64) cache[used++] = Entry{dev, S, smem_bytes, n};
-    return n;
+    return false;
 }
 
-// Environment override "rw,S,_,ns" (fields 0 = automatic; rw is ignored here), read once.
+// Grid, item order, stage count and layout: tile-major when the operands of a share fit.
+bool make_plan(int blk_weights, int bfu, int M, int64_t T, int64_t U, int grid_cap, int ns_req, Plan& p) {
+    const int64_t items = T * U;
+    p.sc.items = items;
+    p.sc.T = static_cast<int>(T);
+    p.sc.U = static_cast<int>(U);
+    p.sc.G = static_cast<int>(std::min<int64_t>(grid_cap, items));
+    p.sc.tile_major = 1;
+    if (layout(blk_weights, bfu, M, ns_req, p)) return true;
+    p.sc.tile_major = 0;
+    return layout(blk_weights, bfu, M, ns_req, p);
+}
+
+// Environment override PNQ_PN_CFG="tpw,grid,_,ns" (fields 0 = automatic), read once.
 MmaConfig env_config() {
     static MmaConfig cfg = [] {
         MmaConfig c{0, 0, 0, 0};
-        if (const char* s = std::getenv("PNQ_GEMV_CFG")) {
+        if (const char* s = std::getenv("PNQ_PN_CFG")) {
             int v[4] = {0, 0, 0, 0};
             int n = 0;
             const char* p = s;
@@ -738,85 +720,64 @@ MmaConfig env_config() {
     return cfg;
 }
 
-template <int TYPE, int NT, int kRW>
-cudaError_t plan_and_launch(PnArgs& a, const MmaConfig& cfg, cudaStream_t stream) {
+template <int TYPE, int NT, int TPW>
+cudaError_t launch_cfg(PnArgs& a, const MmaConfig& cfg, bool static_weights, cudaStream_t stream) {
     using F = PnFmt<TYPE>;
-    const int U = a.units;
-    const int T16 = (a.N + 15) / 16;
-    auto layout_for = [&](int S, int ns) {
-        return make_pn_layout(F::PAIRS, F::BLK, a.M, NT, kRW, (U + S - 1) / S, ns, S);
-    };
-    auto fits = [&](const PnLayout& L) { return L.total + 1024u <= 227u * 1024u && L.x_stage >= 1; };
-    auto stages_for = [&](int S) {
-        if (cfg.ns > 0) return fits(layout_for(S, cfg.ns)) ? cfg.ns : 0;
-        for (int ns = 4; ns >= 3; --ns)
-            if (fits(layout_for(S, ns))) return ns;
-        for (int ns = 5; ns <= 6; ++ns)  // x may need more stages than the default
-            if (fits(layout_for(S, ns))) return ns;
-        return 0;
-    };
-    const int s_list[] = {1, 2, 4, 8};
-    int s_forced = 0;  // a requested cluster size, rounded down to the list and to U
-    if (cfg.S > 0)
-        for (int S : s_list)
-            if (S <= std::min(cfg.S, U)) s_forced = S;
-    int best_S = 0, best_ns = 0, best_clusters = 0;
-    int64_t best_cost = INT64_MAX;
-    for (int S : s_list) {
-        if (S > U) break;
-        if (s_forced > 0 && S != s_forced) continue;
-        const int ns = stages_for(S);
-        if (ns == 0) continue;
-        const int resident = resident_clusters<TYPE, NT, kRW>(S, layout_for(S, ns).total + 1024u);
-        if (resident < 1) continue;
-        const int clusters = std::min(resident, T16);
-        // makespan of the busiest CTA in (16-row tile x 8-block unit) items, plus per-pass costs
-        const int64_t tiles = (T16 + clusters - 1) / clusters;
-        const int64_t units = (U + S - 1) / S;
-        const int64_t cost = tiles * units * 8 + ((tiles + kTP - 1) / kTP) * (S > 1 ? 40 : 16) + units * 4;
-        if (cost < best_cost) {
-            best_cost = cost;
-            best_S = S;
-            best_ns = ns;
-            best_clusters = clusters;
-        }
-    }
-    if (best_S == 0) return cudaErrorNotSupported;
-    a.S = best_S;
-    a.NS = best_ns;
-    const size_t smem_bytes = layout_for(best_S, best_ns).total + 1024u;
-    cudaError_t e = prepare_kernel<TYPE, NT, kRW>(a.S, smem_bytes);
+    using C = Cfg<TYPE, NT, TPW>;
+    Plan p;
+    const int cap = cfg.S > 0 ? std::min(cfg.S, device_sm_count()) : device_sm_count();
+    if (!make_plan(F::BLK, C::BFU, a.M, a.sc.T, a.sc.U, cap, cfg.ns, p)) return cudaErrorNotSupported;
+    auto kern = pn_gemv_kernel<TYPE, NT, TPW>;
+    static bool opted[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    cudaLaunchConfig_t lc{};
-    lc.gridDim = dim3(a.S, best_clusters, 1);
-    lc.blockDim = dim3(32 * (kRW + 1), 1, 1);
-    lc.dynamicSmemBytes = smem_bytes;
-    lc.stream = stream;
-    cudaLaunchAttribute attr[2];
-    int n = 0;
-    if (a.S > 1) {
-        attr[n].id = cudaLaunchAttributeClusterDimension;
-        attr[n].val.clusterDim.x = a.S;
-        attr[n].val.clusterDim.y = 1;
-        attr[n].val.clusterDim.z = 1;
-        ++n;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!opted[dev]) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmemLimit));
+        if (e != cudaSuccess) return e;
+        opted[dev] = true;
     }
+    e = stream_workspace(stream, static_cast<size_t>(a.sc.T) * a.sc.U * a.M * kTileRows, static_cast<size_t>(a.sc.T),
+                         &a.ws, &a.cnt);
+    if (e != cudaSuccess) return e;
+    a.sc = p.sc;
+    a.NS = p.NS;
+    a.x_stage = p.x_stage;
+    a.xpitch = p.xpitch;
+    a.flags = static_weights ? kStaticWeights : 0u;
+    a.bar_off = p.bar_off;
+    a.misc_off = p.misc_off;
+    a.z_off = p.z_off;
+    a.part_off = p.part_off;
+    a.b_off = p.b_off;
+    a.stage_off = p.stage_off;
+    cudaLaunchConfig_t lc{};
+    lc.gridDim = dim3(p.sc.G, 1, 1);
+    lc.blockDim = dim3(C::THREADS, 1, 1);
+    lc.dynamicSmemBytes = p.total + 1024u;
+    lc.stream = stream;
+    cudaLaunchAttribute attr[1];
     // may begin while the previous grid in the stream finishes (see griddep_wait in the kernel)
-    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[n].val.programmaticStreamSerializationAllowed = 1;
-    ++n;
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
     lc.attrs = attr;
-    lc.numAttrs = n;
-    return cudaLaunchKernelEx(&lc, pn_gemv_kernel<TYPE, NT, kRW>, a);
+    lc.numAttrs = 1;
+    return cudaLaunchKernelEx(&lc, kern, a);
 }
 
 template <int TYPE>
-cudaError_t launch_typed(PnArgs& a, const MmaConfig& cfg, cudaStream_t stream) {
+cudaError_t launch_typed(PnArgs& a, const MmaConfig& cfg, bool static_weights, cudaStream_t stream) {
     const int nt = (2 * a.M + 7) / 8;
-    // eight consumer warps while the registers allow it (one tile of n8 columns), four otherwise
-    if (nt <= 1) return plan_and_launch<TYPE, 1, 8>(a, cfg, stream);
-    if (nt <= 2) return plan_and_launch<TYPE, 2, 4>(a, cfg, stream);
-    return plan_and_launch<TYPE, 4, 4>(a, cfg, stream);
+    // one tile per warp (16 consumer warps) for the matrix-vector range; two tiles per warp
+    // (8 consumer warps, B fragments reused across the tiles) for wider batches
+    const int tpw = cfg.rw > 0 ? cfg.rw : (nt == 1 ? 1 : 2);
+    if (nt == 1) return tpw == 1 ? launch_cfg<TYPE, 1, 1>(a, cfg, static_weights, stream)
+                                 : launch_cfg<TYPE, 1, 2>(a, cfg, static_weights, stream);
+    if (nt == 2) return tpw == 1 ? launch_cfg<TYPE, 2, 1>(a, cfg, static_weights, stream)
+                                 : launch_cfg<TYPE, 2, 2>(a, cfg, static_weights, stream);
+    return tpw == 1 ? launch_cfg<TYPE, 4, 1>(a, cfg, static_weights, stream)
+                    : launch_cfg<TYPE, 4, 2>(a, cfg, static_weights, stream);
 }
 
 }  // namespace
@@ -826,27 +787,26 @@ cudaError_t launch_pn_gemv_mma(int type, const uint8_t* W, int64_t N, int64_t K,
     if (N == 0) return cudaSuccess;
     const int blk = (type == kTypePn3t) ? 80 : 64;
     const int64_t nb = K / blk;
-    if (N > INT32_MAX || nb % 8 != 0 || nb / 8 > INT32_MAX / 2 || M < 1 || M > kMaxM) return cudaErrorNotSupported;
+    if (nb % kUnitBlocks != 0 || M < 1 || M > 16) return cudaErrorNotSupported;
+    const int64_t U = nb / kUnitBlocks, T = (N + kTileRows - 1) / kTileRows;
+    if (N > INT32_MAX || K > INT32_MAX || U * kUnitU32 > INT32_MAX || T * kTileRows > INT32_MAX)
+        return cudaErrorNotSupported;
     if (reinterpret_cast<uintptr_t>(W) % 16 != 0 || reinterpret_cast<uintptr_t>(X) % 16 != 0)
         return cudaErrorNotSupported;
-    const MmaConfig env = env_config();
-    if (cfg.S <= 0) cfg.S = env.S;
-    if (cfg.ns <= 0) cfg.ns = env.ns;
-    if (cfg.ns != 0 && (cfg.ns < 2 || cfg.ns > 16)) return cudaErrorInvalidValue;
     PnArgs a{};
-    const int64_t row_bytes = nb * kBlockBytes;
-    if (!encode_weight_map(&a.map_pass, W, N, row_bytes, kRows) || !encode_weight_map(&a.map_tile, W, N, row_bytes, 16))
-        return cudaErrorNotSupported;
+    if (!encode_u32_map(&a.map, W, N, nb * kBlockBytes / 4, kUnitU32, kTileRows)) return cudaErrorNotSupported;
     a.X = X;
     a.Y = Y;
     a.err = err;
     a.N = static_cast<int>(N);
     a.K = static_cast<int>(K);
-    a.units = static_cast<int>(nb / 8);
     a.M = M;
-    a.flags = static_weights ? kStaticWeights : 0;
-    if (type == kTypePn3t) return launch_typed<kTypePn3t>(a, cfg, stream);
-    return launch_typed<kTypePn4t>(a, cfg, stream);
+    a.sc.T = static_cast<int>(T);
+    a.sc.U = static_cast<int>(U);
+    a.sc.items = T * U;
+    const MmaConfig c = (cfg.rw > 0 || cfg.S > 0 || cfg.ns > 0) ? cfg : env_config();
+    return (type == kTypePn3t) ? launch_typed<kTypePn3t>(a, c, static_weights, stream)
+                               : launch_typed<kTypePn4t>(a, c, static_weights, stream);
 }
 
 }  // namespace pnq

@@ -45,11 +45,8 @@
 
 #include <algorithm>
 #include <cstdint>
-#include <map>
-#include <mutex>
 #include <type_traits>
 #include <utility>
-#include <vector>
 
 #include "pnq_device.cuh"
 #include "pnq_internal.h"
@@ -613,36 +610,6 @@ __global__ void __launch_bounds__(kThreads, 1) pn_tc_gemv_kernel(const __grid_co
 
 // ---- host side --------------------------------------------------------------------------------------
 
-using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                              const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                              CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeFn tensor_map_encoder() {
-    static EncodeFn fn = [] {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q{};
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
-                cudaSuccess ||
-            q != cudaDriverEntryPointSuccess)
-            return static_cast<EncodeFn>(nullptr);
-        return reinterpret_cast<EncodeFn>(p);
-    }();
-    return fn;
-}
-
-// Weights viewed as u32 [N][row_bytes / 4]; box {68, 128}. Rows past N read as zeros.
-bool encode_weight_map(CUtensorMap* map, const uint8_t* W, int64_t N, int64_t row_bytes) {
-    EncodeFn enc = tensor_map_encoder();
-    if (!enc) return false;
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(row_bytes / 4), static_cast<cuuint64_t>(N)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_bytes)};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kUnitU32), static_cast<cuuint32_t>(kTileRows)};
-    const cuuint32_t estr[2] = {1, 1};
-    return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint8_t*>(W), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 uint32_t align_up(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
 
 struct Plan {
@@ -680,50 +647,6 @@ bool make_plan(int blk_weights, int steps, int parts, int M, int64_t T, int64_t 
     return false;
 }
 
-// Per (device, stream) workspace: partial rows and tile counters. Grows on demand; outgrown
-// buffers stay allocated (a captured graph may still refer to them).
-struct Workspace {
-    float* ws = nullptr;
-    uint32_t* cnt = nullptr;
-    size_t ws_floats = 0, cnt_n = 0;
-};
-
-cudaError_t get_workspace(cudaStream_t stream, size_t ws_floats, size_t cnt_n, Workspace& out) {
-    static std::mutex mu;
-    static std::map<std::pair<int, cudaStream_t>, Workspace> table;
-    static std::vector<void*> retired;
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    std::lock_guard<std::mutex> lock(mu);
-    Workspace& w = table[{dev, stream}];
-    if (w.ws_floats >= ws_floats && w.cnt_n >= cnt_n) {
-        out = w;
-        return cudaSuccess;
-    }
-    // allocation is allowed while the stream is being captured
-    cudaStreamCaptureMode mode = cudaStreamCaptureModeRelaxed;
-    cudaThreadExchangeStreamCaptureMode(&mode);
-    Workspace n;
-    n.ws_floats = std::max(ws_floats, w.ws_floats);
-    n.cnt_n = std::max(cnt_n, w.cnt_n);
-    e = cudaMalloc(&n.ws, n.ws_floats * sizeof(float));
-    if (e == cudaSuccess) {
-        e = cudaMalloc(&n.cnt, n.cnt_n * sizeof(uint32_t));
-        if (e != cudaSuccess) cudaFree(n.ws);
-    }
-    cudaThreadExchangeStreamCaptureMode(&mode);
-    if (e != cudaSuccess) return e;
-    // counters start at zero (a memset node when captured: re-zeroing is harmless)
-    e = cudaMemsetAsync(n.cnt, 0, n.cnt_n * sizeof(uint32_t), stream);
-    if (e != cudaSuccess) return e;
-    if (w.ws) retired.push_back(w.ws);
-    if (w.cnt) retired.push_back(w.cnt);
-    w = n;
-    out = n;
-    return cudaSuccess;
-}
-
 template <int TYPE, int MC>
 cudaError_t launch_mc(TcArgs& a, bool static_weights, cudaStream_t stream) {
     using F = PnFmt<TYPE>;
@@ -741,11 +664,9 @@ cudaError_t launch_mc(TcArgs& a, bool static_weights, cudaStream_t stream) {
         if (e != cudaSuccess) return e;
         opted[dev] = true;
     }
-    Workspace w;
-    e = get_workspace(stream, static_cast<size_t>(a.T) * a.U * a.M * kTileRows, static_cast<size_t>(a.T), w);
+    e = stream_workspace(stream, static_cast<size_t>(a.T) * a.U * a.M * kTileRows, static_cast<size_t>(a.T), &a.ws,
+                         &a.cnt);
     if (e != cudaSuccess) return e;
-    a.ws = w.ws;
-    a.cnt = w.cnt;
     a.NS = p.NS;
     a.x_stage = p.x_stage;
     a.flags = static_weights ? kStaticWeights : 0u;
@@ -791,7 +712,7 @@ cudaError_t launch_pn_gemv_tc(int type, const uint8_t* W, int64_t N, int64_t K, 
     if (reinterpret_cast<uintptr_t>(W) % 16 != 0 || reinterpret_cast<uintptr_t>(X) % 16 != 0)
         return cudaErrorNotSupported;
     TcArgs a{};
-    if (!encode_weight_map(&a.map, W, N, nb * kBlockBytes)) return cudaErrorNotSupported;
+    if (!encode_u32_map(&a.map, W, N, nb * kBlockBytes / 4, kUnitU32, kTileRows)) return cudaErrorNotSupported;
     a.X = X;
     a.Y = Y;
     a.err = err;

@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace pnq {
@@ -21,6 +22,17 @@ struct MmaConfig {
 };
 
 int device_sm_count();
+
+// 2-D tensor map over a row-major u32 matrix [rows][row_u32] (row pitch a multiple of 16
+// bytes) with box {box_x, box_y}; rows past the end read as zeros. False when the driver entry
+// point is missing or the encoder rejects the arguments.
+bool encode_u32_map(CUtensorMap* map, const void* base, int64_t rows, int64_t row_u32, int box_x, int box_y);
+
+// Workspace of the stream-K GEMV kernels, one per (device, stream): `floats` partial sums and
+// `counters` tile counters (zero between launches). Grows on demand; outgrown buffers stay
+// allocated because a captured graph may still refer to them. Allocation is allowed while the
+// stream is being captured (the counters are then cleared by a captured memset node).
+cudaError_t stream_workspace(cudaStream_t stream, size_t floats, size_t counters, float** ws, uint32_t** cnt);
 
 cudaError_t launch_pn_dequant(int type, const uint8_t* W, int64_t n_rows, int64_t K, float* out,
                               cudaStream_t stream);

@@ -3,7 +3,8 @@
 Covers both paths (tensor-core fast path for aligned weights with (K/BLK) % 8 == 0 or
 NVFP4 K % 256 == 0; generic path otherwise), every M from the matrix-vector (1..4) and
 small-batch (5..16) ranges, ragged N, alignment offsets, the workload sizes (sampled rows),
-exact closed forms, canaries past the output, determinism, and cluster split configurations.
+exact closed forms, canaries past the output, determinism, and forced tile / grid / stage
+configurations.
 """
 import json
 import os
@@ -196,11 +197,14 @@ print(json.dumps({{"ok": True, "device_error": pnq.device_error()}}))
 """
 
 
-@pytest.mark.parametrize("cfg", ["2,1,0,2", "4,2,0,3", "2,4,0,4", "4,8,0,5", "4,1,0,8", "2,16,0,6", "4,4,0,0"])
-def test_tile_and_cluster_configs(cfg):
-    """Consumer warps, K-split cluster size and stage count forced through PNQ_GEMV_CFG (read
-    once per process, so each configuration runs in a child process)."""
-    env = dict(os.environ, PNQ_GEMV_CFG=cfg, PNQ_FORCE_KERNEL="mma")
+@pytest.mark.parametrize("pn_cfg,nv_cfg", [("1,0,0,0", "2,1,0,2"), ("2,0,0,0", "4,2,0,3"), ("1,7,0,2", "2,4,0,4"),
+                                            ("2,13,0,3", "4,8,0,5"), ("1,152,0,8", "4,1,0,8"),
+                                            ("2,3,0,5", "2,16,0,6"), ("1,40,0,4", "4,4,0,0")])
+def test_tile_and_grid_configs(pn_cfg, nv_cfg):
+    """Forced configurations, read once per process (so each runs in a child): PN path through
+    PNQ_PN_CFG "tiles per warp, grid size, _, stages" (small grids make CTAs span several K
+    units); NVFP4 path through PNQ_GEMV_CFG "consumer warps, cluster size, _, stages"."""
+    env = dict(os.environ, PNQ_PN_CFG=pn_cfg, PNQ_GEMV_CFG=nv_cfg, PNQ_FORCE_KERNEL="mma")
     r = subprocess.run([sys.executable, "-c", CHILD.format(root=ROOT)], env=env, capture_output=True, text=True,
                        timeout=600)
     assert r.returncode == 0, r.stderr[-3000:]
