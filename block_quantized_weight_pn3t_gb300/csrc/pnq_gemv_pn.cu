@@ -94,6 +94,15 @@ struct Sched {
     }
     __host__ __device__ long long first(long long c) const { return c * items / G; }
     __host__ __device__ long long owner(long long i) const { return ((i + 1) * G - 1) / items; }
+    // A share is a run of consecutive items of one CTA within a tile. Tile-major (or T = 1):
+    // the items of tile t are consecutive, a share starts at unit 0 and at the first item of
+    // every CTA that begins inside the tile. Unit-major: every unit is a share of its own.
+    __host__ __device__ bool consecutive() const { return tile_major || T == 1; }
+    __host__ __device__ int shares(int t) const {
+        if (!consecutive()) return U;
+        const long long a0 = item(t, 0);
+        return static_cast<int>(owner(a0 + U - 1) - owner(a0)) + 1;
+    }
     // units a CTA's share touches (a cyclic range starting at unit_of(first item))
     __host__ __device__ int span(long long i0, long long i1) const {
         if (i1 <= i0) return 0;
@@ -112,7 +121,8 @@ struct PnArgs {
     Sched sc;
     int N, K, M, NS, x_stage, xpitch;
     unsigned flags;
-    uint32_t bar_off, misc_off, z_off, part_off, b_off, stage_off;
+    uint32_t bar_off, misc_off, z_off, part_off, b_off, stage_off, list_off;
+    int list_cap;
 };
 
 // 2^-(BITS * jj) for slice j, and its inverse.
@@ -177,7 +187,7 @@ struct Smem {
     uint8_t* base;
     uint32_t bar0;  // shared address of barrier 0
     int NS;
-    uint32_t misc_off, z_off, part_off, b_off, stage_off;
+    uint32_t misc_off, z_off, part_off, b_off, stage_off, list_off;
     __device__ uint32_t full(int s) const { return bar0 + 8u * s; }
     __device__ uint32_t empty(int s) const { return bar0 + 8u * (NS + s); }
     __device__ uint32_t x_ready() const { return bar0 + 8u * (2 * NS); }
@@ -191,6 +201,12 @@ struct Smem {
     __device__ float* part() const { return reinterpret_cast<float*>(base + part_off); }
     __device__ uint8_t* b() const { return base + b_off; }
     __device__ uint8_t* stage(int s) const { return base + stage_off + static_cast<uint32_t>(s) * kStageBytes; }
+    // tiles whose partial shares wait to be counted, tiles this CTA completes (list_cap entries
+    // each, list_cap >= the items of any CTA), and the number of the latter
+    int list_cap;
+    __device__ int* n_finish() const { return reinterpret_cast<int*>(base + list_off); }
+    __device__ int* pending() const { return reinterpret_cast<int*>(base + list_off) + 4; }
+    __device__ int* finish() const { return reinterpret_cast<int*>(base + list_off) + 4 + list_cap; }
 };
 
 // Next item of a share: (t, u) in the share's order, without divisions.
@@ -203,6 +219,41 @@ __device__ __forceinline__ void next_item(const Sched& sc, int& t, int& u) {
     } else if (++t == sc.T) {
         t = 0;
         ++u;
+    }
+}
+
+// A register (two halves) holding code 1 at slice j's position: the fp16 subnormal
+// 2^-24 * 8^j (pn3t) or 2^-24 * 16^j (pn4t) in both halves.
+template <int TYPE>
+__device__ __forceinline__ uint32_t code_one(int j) {
+    const int jj = (TYPE == kTypePn3t) ? (j < 3 ? j : j - 3) : (j & 1);
+    return 0x00010001u << (PnFmt<TYPE>::BITS * jj);
+}
+
+// B fragments of one block for every n8 tile: lanes whose column is in use load their records,
+// the others hold zeros.
+template <int TYPE, int NT>
+__device__ __forceinline__ void load_bfrag(const uint8_t* bf, int lane, const bool (&live)[NT],
+                                           uint32_t (&b)[NT][PnFmt<TYPE>::PAIRS][2]) {
+    constexpr int STEPS = PnFmt<TYPE>::PAIRS;
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+        const uint8_t* base = bf + t * 256 * STEPS;
+#pragma unroll
+        for (int q = 0; q < STEPS / 2; ++q) {
+            uint4 v = make_uint4(0u, 0u, 0u, 0u);
+            if (live[t]) v = *reinterpret_cast<const uint4*>(base + q * 512 + lane * 16);
+            b[t][2 * q][0] = v.x;
+            b[t][2 * q][1] = v.y;
+            b[t][2 * q + 1][0] = v.z;
+            b[t][2 * q + 1][1] = v.w;
+        }
+        if constexpr (STEPS & 1) {
+            uint2 v = make_uint2(0u, 0u);
+            if (live[t]) v = *reinterpret_cast<const uint2*>(base + (STEPS / 2) * 512 + lane * 8);
+            b[t][STEPS - 1][0] = v.x;
+            b[t][STEPS - 1][1] = v.y;
+        }
     }
 }
 
@@ -239,51 +290,58 @@ __device__ __forceinline__ void fill_operands(const Smem& sm, const float* xs, i
         sig_out[tid] = exp2i(24 - sg);  // undoes sigma and the 2^-24 of the subnormal codes
     }
     named_sync(1, C::NCT);
-    // B fragments: per block, tile t, slice st and lane l the two registers b0 (decode register
-    // c = l % 4) and b1 (register c + 4) of column 8t + l / 4; paired slices share 16 bytes.
-    // Only lanes whose column is in use (l < 8M - 32t) are written: the others never read.
+    // B fragments: one item per (block, slice st, decode register i, row m). The two x values
+    // register i holds for slice st, scaled, go split into the hi part to the lane of column 2m
+    // and the lo part to the lane of column 2m + 1 (lane = 4 * (column % 8) + i % 4, register
+    // b0 for i < 4, b1 otherwise; records of paired slices share 16 bytes).
     uint8_t* bbase = sm.b();
-    const int lanes = min(32, 8 * M);  // live lanes of tile 0 (and of every full tile)
-    const int items = nblk * NT * STEPS * lanes;
+    const int items = nblk * STEPS * 8 * M;
     for (int it = tid; it < items; it += C::NCT) {
-        const int l = it % lanes;
-        int rest = it / lanes;
-        const int st = rest % STEPS;
-        rest /= STEPS;
-        const int t = rest % NT, blk = rest / NT;
-        const int n = 8 * t + (l >> 2), m = n >> 1, prt = n & 1;
-        if (n >= 2 * M) continue;
+        const int rest = it / M;
+        const int m = it - rest * M;
+        const int i = rest & 7, bs = rest >> 3;
+        const int st = bs % STEPS, blk = bs / STEPS;
         const float sc = sig_in[m] * step_scale<TYPE>(st);
         const float* xb = xs + m * xpitch + blk * F::BLK;
         const int odd = blk & 1;
-        uint32_t r[2];
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-            const int i = (l & 3) + 4 * q;
-            r[q] = pack_half2(split_part(xb[pn_elem(F::CPW, odd, i, st, 0)] * sc, prt),
-                              split_part(xb[pn_elem(F::CPW, odd, i, st, 1)] * sc, prt));
-        }
-        const int off = blk * C::BFU + t * 256 * STEPS +
-                        (((STEPS & 1) && st == STEPS - 1) ? (STEPS / 2) * 512 + l * 8 : (st >> 1) * 512 + l * 16 + (st & 1) * 8);
-        *reinterpret_cast<uint2*>(bbase + off) = make_uint2(r[0], r[1]);
+        const float v0 = xb[pn_elem(F::CPW, odd, i, st, 0)] * sc;
+        const float v1 = xb[pn_elem(F::CPW, odd, i, st, 1)] * sc;
+        const __half h0 = __float2half_rn(v0), h1 = __float2half_rn(v1);
+        const __half l0 = __float2half_rn(v0 - __half2float(h0)), l1 = __float2half_rn(v1 - __half2float(h1));
+        const int n = 2 * m, tile = n >> 3, tig = i & 3, reg = i >> 2;
+        const bool last_odd = (STEPS & 1) && st == STEPS - 1;
+        const int rec = last_odd ? 8 : 16;  // bytes per lane record
+        uint8_t* p = bbase + blk * C::BFU + tile * 256 * STEPS +
+                     (last_odd ? (STEPS / 2) * 512 : (st >> 1) * 512 + (st & 1) * 8) + reg * 4;
+        *reinterpret_cast<uint32_t*>(p + ((((n & 7) << 2) | tig) * rec)) = pack_half2(h0, h1);
+        *reinterpret_cast<uint32_t*>(p + (((((n + 1) & 7) << 2) | tig) * rec)) = pack_half2(l0, l1);
     }
-    // Z = z * sum over the block of (2^-24 * 8^j) * (hi + lo): one warp per (block, m)
+    named_sync(1, C::NCT);
+    // Z = z * sum over the block of (2^-24 * 8^j) * B, on the tensor core: an A operand with code
+    // 1 at slice j's position in every row and k (the subnormal 2^-24 * 8^j) sums B the same way
+    // the main loop's mma sums n * 2^-24 * 8^j * B. One warp per block.
     float* z = sm.z();
-    for (int pr = warp; pr < nblk * M; pr += C::CW) {
-        const int blk = pr / M, m = pr - blk * M;
-        const float* xb = xs + m * xpitch + blk * F::BLK;
-        const float si = sig_in[m];
-        float s = 0.0f;
-        for (int e = lane; e < F::BLK; e += 32) {
-            const int j = (e % F::CPW) >> 1;
-            const float v = xb[e] * (si * step_scale<TYPE>(j));
-            const float hi = __half2float(__float2half_rn(v));
-            const float lo = __half2float(__float2half_rn(v - hi));
-            s = fmaf(5.9604644775390625e-08f * step_scale_inv<TYPE>(j), hi + lo, s);
-        }
+    const int g = lane >> 2, tig = lane & 3;
+    bool live[NT];
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-        if (lane == 0) z[blk * M + m] = static_cast<float>(F::Z) * s;
+    for (int t = 0; t < NT; ++t) live[t] = (8 * t + g) < 2 * M;
+    for (int blk = warp; blk < nblk; blk += C::CW) {
+        uint32_t b[NT][STEPS][2];
+        load_bfrag<TYPE, NT>(bbase + blk * C::BFU, lane, live, b);
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+            float c[4];
+#pragma unroll
+            for (int j = 0; j < STEPS; ++j) {
+                const uint32_t one = code_one<TYPE>(j);
+                if (j == 0)
+                    mma_f16_16816_z(c, one, one, one, one, b[t][j][0], b[t][j][1]);
+                else
+                    mma_f16_16816(c, one, one, one, one, b[t][j][0], b[t][j][1]);
+            }
+            const int m = 4 * t + tig;
+            if (g == 0 && m < M) z[blk * M + m] = static_cast<float>(F::Z) * (c[0] + c[1]);
+        }
     }
     named_sync(1, C::NCT);
 }
@@ -300,25 +358,10 @@ __device__ __forceinline__ void pn_block(const uint8_t* const (&row0)[TPW], int 
     constexpr int SH = (TYPE == kTypePn3t) ? 9 : 8;
     // B fragments (columns past 2M are zero and are not read)
     uint32_t b[NT][STEPS][2];
+    load_bfrag<TYPE, NT>(bf, lane, live, b);
     float zt[NT];
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
-        const uint8_t* base = bf + t * 256 * STEPS;
-#pragma unroll
-        for (int q = 0; q < STEPS / 2; ++q) {
-            uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            if (live[t]) v = *reinterpret_cast<const uint4*>(base + q * 512 + lane * 16);
-            b[t][2 * q][0] = v.x;
-            b[t][2 * q][1] = v.y;
-            b[t][2 * q + 1][0] = v.z;
-            b[t][2 * q + 1][1] = v.w;
-        }
-        if constexpr (STEPS & 1) {
-            uint2 v = make_uint2(0u, 0u);
-            if (live[t]) v = *reinterpret_cast<const uint2*>(base + (STEPS / 2) * 512 + lane * 8);
-            b[t][STEPS - 1][0] = v.x;
-            b[t][STEPS - 1][1] = v.y;
-        }
         const int m = 4 * t + tig;
         zt[t] = (m < M) ? zb[m] : 0.0f;
     }
@@ -443,22 +486,23 @@ __device__ __forceinline__ void consumer_loop(const Smem& sm, const Ctx& cx, lon
     if (!ok && lane == 0) record_error(cx.err, kErrFullWait);
 }
 
+// Y rows t*128 + 4*lane .. + 3 of activation row m.
+__device__ __forceinline__ void put_y(const Ctx& a, int t, int m, int lane, float4 v) {
+    const int row = t * kTileRows + 4 * lane;
+    float* y = a.Y + static_cast<size_t>(m) * a.N;
+    if (row + 0 < a.N) y[row + 0] = v.x;
+    if (row + 1 < a.N) y[row + 1] = v.y;
+    if (row + 2 < a.N) y[row + 2] = v.z;
+    if (row + 3 < a.N) y[row + 3] = v.w;
+}
+
 // Reducer side of one share of tile t (consecutive items of this CTA, units u_first ..
-// u_first+n-1):
-// add the two halves; a whole tile goes to Y, a part to its workspace slot, and the share that
-// completes the tile sums the tile's slots in unit order into Y.
+// u_first+n-1): add the two halves; a whole tile goes to Y, a part to its workspace slot (it is
+// counted later). Returns true for a part.
 template <int MAXM>
-__device__ __forceinline__ void reduce_share(const Ctx& a, const Smem& sm, int buf, int t, int u_first, int n_units,
+__device__ __forceinline__ bool reduce_share(const Ctx& a, const Smem& sm, int buf, int t, int u_first, int n_units,
                                              int lane) {
     const Sched& sc = a.sc;
-    const int row = t * kTileRows + 4 * lane;
-    auto put_y = [&](int m, float4 v) {
-        float* y = a.Y + static_cast<size_t>(m) * a.N;
-        if (row + 0 < a.N) y[row + 0] = v.x;
-        if (row + 1 < a.N) y[row + 1] = v.y;
-        if (row + 2 < a.N) y[row + 2] = v.z;
-        if (row + 3 < a.N) y[row + 3] = v.w;
-    };
     // the two halves' row sums into registers; the buffer goes back to the consumers at once
     const float* part = sm.part();
     float4 v[MAXM];
@@ -475,50 +519,63 @@ __device__ __forceinline__ void reduce_share(const Ctx& a, const Smem& sm, int b
     if (n_units == sc.U) {
 #pragma unroll
         for (int m = 0; m < MAXM; ++m)
-            if (m < a.M) put_y(m, v[m]);
-        return;
+            if (m < a.M) put_y(a, t, m, lane, v[m]);
+        return false;
     }
     float* slot = a.ws + (static_cast<size_t>(t) * sc.U + u_first) * a.M * kTileRows;
 #pragma unroll
     for (int m = 0; m < MAXM; ++m)
         if (m < a.M) __stcg(reinterpret_cast<float4*>(slot + m * kTileRows) + lane, v[m]);
-    __threadfence();
+    return true;
+}
+
+// Count the np partial shares of this CTA (tiles in pending[]) after their slots were stored:
+// the ones that complete their tile are appended to finish[] (n_finish[0] entries). One warp.
+__device__ __forceinline__ void count_shares(const Ctx& a, const Smem& sm, int np, int lane) {
+    __threadfence();  // the slots are visible before they are counted
     __syncwarp();
-    // shares of tile t: a share is a run of consecutive items of one CTA, so one starts at unit
-    // 0 and wherever the previous unit is not the previous item of the same CTA
-    auto starts = [&](int c0) {
-        const int u = c0 + lane;
-        bool st = false;
-        if (u < sc.U) {
-            const long long it = sc.item(t, u);
-            st = (u == 0) || sc.item(t, u - 1) != it - 1 || sc.owner(it) != sc.owner(it - 1);
+    int* pend = sm.pending();
+    int* fin = sm.finish();
+    for (int k0 = 0; k0 < np; k0 += 32) {
+        const int k = k0 + lane;
+        bool last = false;
+        int t = 0;
+        if (k < np) {
+            t = pend[k];
+            last = atomicAdd(a.cnt + t, 1u) == static_cast<unsigned>(a.sc.shares(t) - 1);
         }
-        return __ballot_sync(0xffffffffu, st);
-    };
-    int shares = 0;
-    for (int c0 = 0; c0 < sc.U; c0 += 32) shares += __popc(starts(c0));
-    unsigned old = 0;
-    if (lane == 0) old = atomicAdd(a.cnt + t, 1u);
-    old = __shfl_sync(0xffffffffu, old, 0);
-    if (old != static_cast<unsigned>(shares - 1)) return;
-    __threadfence();
+        const unsigned mask = __ballot_sync(0xffffffffu, last);
+        const int base = *sm.n_finish();
+        if (last) fin[base + __popc(mask & ((1u << lane) - 1u))] = t;
+        __syncwarp();
+        if (lane == 0) *sm.n_finish() = base + __popc(mask);
+        __syncwarp();
+    }
+    __threadfence();  // what the other CTAs stored before counting is seen by the finishers
+}
+
+// Sum the shares of tile t in unit order into Y and clear its counter (one warp).
+__device__ __forceinline__ void finish_tile(const Ctx& a, int t, int lane) {
+    const Sched& sc = a.sc;
     for (int m = 0; m < a.M; ++m) {
         float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-        for (int c0 = 0; c0 < sc.U; c0 += 32) {
-            unsigned mask = starts(c0);
-            while (mask) {
-                const int u = c0 + __ffs(mask) - 1;
-                mask &= mask - 1;
-                const float4 v = __ldcg(
-                    reinterpret_cast<const float4*>(a.ws + ((static_cast<size_t>(t) * sc.U + u) * a.M + m) * kTileRows) +
-                    lane);
-                acc.x += v.x;
-                acc.y += v.y;
-                acc.z += v.z;
-                acc.w += v.w;
-            }
+        auto add_slot = [&](int u) {
+            const float* slot = a.ws + ((static_cast<size_t>(t) * sc.U + u) * a.M + m) * kTileRows;
+            const float4 v = __ldcg(reinterpret_cast<const float4*>(slot) + lane);
+            acc.x += v.x;
+            acc.y += v.y;
+            acc.z += v.z;
+            acc.w += v.w;
+        };
+        if (sc.consecutive()) {
+            const long long a0 = sc.item(t, 0);
+            add_slot(0);
+            for (long long c = sc.owner(a0) + 1; c <= sc.owner(a0 + sc.U - 1); ++c)
+                add_slot(static_cast<int>(sc.first(c) - a0));
+        } else {
+            for (int u = 0; u < sc.U; ++u) add_slot(u);
         }
-        put_y(m, acc);
+        put_y(a, t, m, lane, acc);
     }
     __syncwarp();
     if (lane == 0) a.cnt[t] = 0u;  // ready for the next launch
@@ -531,7 +588,8 @@ __global__ void __launch_bounds__(Cfg<TYPE, NT, TPW>::THREADS, 1) pn_gemv_kernel
     constexpr int UK = kUnitBlocks * F::BLK;  // weights of a row per unit
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* base = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
-    const Smem sm{base, smem_addr(base + a.bar_off), a.NS, a.misc_off, a.z_off, a.part_off, a.b_off, a.stage_off};
+    const Smem sm{base,        smem_addr(base + a.bar_off), a.NS,       a.misc_off, a.z_off, a.part_off,
+                  a.b_off,     a.stage_off,                 a.list_off, a.list_cap};
     const Ctx cx{a.sc, a.X, a.Y, a.ws, a.cnt, a.err, a.N, a.K, a.M, a.NS, a.x_stage, a.xpitch, a.flags};
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -558,6 +616,7 @@ __global__ void __launch_bounds__(Cfg<TYPE, NT, TPW>::THREADS, 1) pn_gemv_kernel
         griddep_launch_dependents();
     }
     if (threadIdx.x < 16) sm.maxbits()[threadIdx.x] = 0u;
+    if (threadIdx.x == 0) *sm.n_finish() = 0;
     __syncthreads();
 
     if (warp == C::PRODUCER) {
@@ -611,7 +670,7 @@ __global__ void __launch_bounds__(Cfg<TYPE, NT, TPW>::THREADS, 1) pn_gemv_kernel
         if (n_items > 0) {
             griddep_wait();  // the workspace, the counters and Y belong to earlier grids until now
             bool ok = true;
-            int e = 0;
+            int e = 0, np = 0;
             int t_i = sc.tile_of(i0), u_i = sc.unit_of(i0);
             int u_first = u_i, n_run = 0;  // the current share: first unit, items so far
             for (int gi = 0; gi < n_items && ok; ++gi) {
@@ -624,11 +683,15 @@ __global__ void __launch_bounds__(Cfg<TYPE, NT, TPW>::THREADS, 1) pn_gemv_kernel
                     ok = false;
                     break;
                 }
-                reduce_share<4 * NT>(cx, sm, buf, t_cur, u_first, n_run, lane);
+                if (reduce_share<4 * NT>(cx, sm, buf, t_cur, u_first, n_run, lane)) {
+                    if (lane == 0) sm.pending()[np] = t_cur;
+                    ++np;
+                }
                 ++e;
                 u_first = u_i;
                 n_run = 0;
             }
+            if (np > 0) count_shares(cx, sm, np, lane);
             if (!ok && lane == 0) record_error(cx.err, kErrReduceWait);
         }
     } else {
@@ -647,6 +710,10 @@ __global__ void __launch_bounds__(Cfg<TYPE, NT, TPW>::THREADS, 1) pn_gemv_kernel
             }
         }
     }
+    // the tiles this CTA completed: every warp sums some of them
+    __syncthreads();
+    const int nf = *sm.n_finish();
+    for (int k = warp; k < nf; k += C::THREADS / 32) finish_tile(cx, sm.finish()[k], lane);
 }
 
 // ---- host side --------------------------------------------------------------------------------------
@@ -655,8 +722,8 @@ uint32_t align_up(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
 
 struct Plan {
     Sched sc{};
-    int NS = 0, x_stage = 0, span_max = 0, xpitch = 0;
-    uint32_t bar_off = 0, misc_off = 0, z_off = 0, part_off = 0, b_off = 0, stage_off = 0, total = 0;
+    int NS = 0, x_stage = 0, span_max = 0, xpitch = 0, list_cap = 0;
+    uint32_t bar_off = 0, misc_off = 0, list_off = 0, z_off = 0, part_off = 0, b_off = 0, stage_off = 0, total = 0;
 };
 
 // Shared-memory layout and stage count for one item order; false when it does not fit.
@@ -668,7 +735,9 @@ bool layout(int blk_weights, int bfu, int M, int ns_req, Plan& p) {
     p.xpitch = static_cast<int>(nblk) * blk_weights + 4;
     p.bar_off = 0;
     p.misc_off = 8u * (2 * kMaxStages + 6);
-    p.z_off = align_up(p.misc_off + 192u, 16);
+    p.list_cap = static_cast<int>((p.sc.items + p.sc.G - 1) / p.sc.G);
+    p.list_off = align_up(p.misc_off + 192u, 16);
+    p.z_off = align_up(p.list_off + (2u * p.list_cap + 4u) * 4u, 16);
     p.part_off = align_up(p.z_off + nblk * M * 4u, 16);
     p.b_off = align_up(p.part_off + 4u * M * kPartPitch * 4u, 128);
     p.stage_off = align_up(p.b_off + nblk * static_cast<uint32_t>(bfu), 1024);
@@ -688,17 +757,39 @@ bool layout(int blk_weights, int bfu, int M, int ns_req, Plan& p) {
     return false;
 }
 
-// Grid, item order, stage count and layout: tile-major when the operands of a share fit.
-bool make_plan(int blk_weights, int bfu, int M, int64_t T, int64_t U, int grid_cap, int ns_req, Plan& p) {
+// Grid, item order, stage count and layout. Candidates: one CTA per SM (stream-K), and one CTA
+// per row tile when there are fewer tiles than SMs (every tile whole, nothing to reduce across
+// CTAs). Tile-major when the operands of a share fit, else unit-major. Picks the smallest
+// estimate of (items of the busiest CTA) x (time per item) + (cross-CTA reduction tail).
+bool make_plan(int blk_weights, int bfu, int M, int64_t T, int64_t U, int sms, bool grid_forced, int ns_req, Plan& p) {
     const int64_t items = T * U;
-    p.sc.items = items;
-    p.sc.T = static_cast<int>(T);
-    p.sc.U = static_cast<int>(U);
-    p.sc.G = static_cast<int>(std::min<int64_t>(grid_cap, items));
-    p.sc.tile_major = 1;
-    if (layout(blk_weights, bfu, M, ns_req, p)) return true;
-    p.sc.tile_major = 0;
-    return layout(blk_weights, bfu, M, ns_req, p);
+    int64_t cands[2] = {std::min<int64_t>(sms, items), 0};
+    if (!grid_forced && T < sms) cands[1] = T;
+    bool found = false;
+    double best = 0.0;
+    for (int64_t G : cands) {
+        if (G <= 0) continue;
+        for (int tm = 1; tm >= 0; --tm) {
+            Plan q;
+            q.sc.items = items;
+            q.sc.T = static_cast<int>(T);
+            q.sc.U = static_cast<int>(U);
+            q.sc.G = static_cast<int>(G);
+            q.sc.tile_major = tm;
+            if (!layout(blk_weights, bfu, M, ns_req, q)) continue;
+            bool publish = false;
+            for (int64_t c = 1; c < G && !publish; ++c) publish = q.sc.tile_of(q.sc.first(c)) == q.sc.tile_of(q.sc.first(c) - 1);
+            if (!tm && U > 1) publish = true;
+            const double cost = static_cast<double>((items + G - 1) / G) + (publish ? 2.5 : 0.0);
+            if (!found || cost < best) {
+                best = cost;
+                p = q;
+                found = true;
+            }
+            break;  // unit-major only when tile-major does not fit
+        }
+    }
+    return found;
 }
 
 // Environment override PNQ_PN_CFG="tpw,grid,_,ns" (fields 0 = automatic), read once.
@@ -726,7 +817,7 @@ cudaError_t launch_cfg(PnArgs& a, const MmaConfig& cfg, bool static_weights, cud
     using C = Cfg<TYPE, NT, TPW>;
     Plan p;
     const int cap = cfg.S > 0 ? std::min(cfg.S, device_sm_count()) : device_sm_count();
-    if (!make_plan(F::BLK, C::BFU, a.M, a.sc.T, a.sc.U, cap, cfg.ns, p)) return cudaErrorNotSupported;
+    if (!make_plan(F::BLK, C::BFU, a.M, a.sc.T, a.sc.U, cap, cfg.S > 0, cfg.ns, p)) return cudaErrorNotSupported;
     auto kern = pn_gemv_kernel<TYPE, NT, TPW>;
     static bool opted[64] = {};
     int dev = 0;
@@ -748,6 +839,8 @@ cudaError_t launch_cfg(PnArgs& a, const MmaConfig& cfg, bool static_weights, cud
     a.flags = static_weights ? kStaticWeights : 0u;
     a.bar_off = p.bar_off;
     a.misc_off = p.misc_off;
+    a.list_off = p.list_off;
+    a.list_cap = p.list_cap;
     a.z_off = p.z_off;
     a.part_off = p.part_off;
     a.b_off = p.b_off;
