@@ -158,12 +158,6 @@ __device__ __forceinline__ int pn_elem(int cpw, int odd_block, int i, int j, int
     return hi_half ? cpw * i + 2 * j : cpw * (i - 1) + 2 * j + 1;
 }
 
-__device__ __forceinline__ __half split_part(float v, int part) {
-    const __half hi = __float2half_rn(v);
-    if (part == 0) return hi;
-    return __float2half_rn(v - __half2float(hi));
-}
-
 __device__ __forceinline__ uint32_t lds32(const uint8_t* p) { return *reinterpret_cast<const uint32_t*>(p); }
 __device__ __forceinline__ float ld_half(const uint8_t* p) {
     return __half2float(*reinterpret_cast<const __half*>(p));
@@ -190,7 +184,6 @@ struct Smem {
     uint32_t misc_off, z_off, part_off, b_off, stage_off, list_off;
     __device__ uint32_t full(int s) const { return bar0 + 8u * s; }
     __device__ uint32_t empty(int s) const { return bar0 + 8u * (NS + s); }
-    __device__ uint32_t x_ready() const { return bar0 + 8u * (2 * NS); }
     __device__ uint32_t x_free() const { return bar0 + 8u * (2 * NS + 1); }
     __device__ uint32_t part_full(int b) const { return bar0 + 8u * (2 * NS + 2 + b); }
     __device__ uint32_t part_free(int b) const { return bar0 + 8u * (2 * NS + 4 + b); }
@@ -260,26 +253,40 @@ __device__ __forceinline__ void load_bfrag(const uint8_t* bf, int lane, const bo
 // sigma per activation row, the B fragments and the per-block zero-point sums for the CTA's
 // nblk blocks (consumer threads only).
 template <int TYPE, int NT, int TPW>
-__device__ __forceinline__ void fill_operands(const Smem& sm, const float* xs, int xpitch, int nblk, int M) {
+__device__ __forceinline__ void fill_operands(const Smem& sm, const float* X, int K, int U, int u0, int span,
+                                              float* xs, int xpitch, int M) {
     using F = PnFmt<TYPE>;
     using C = Cfg<TYPE, NT, TPW>;
     constexpr int STEPS = F::PAIRS;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int klen = nblk * F::BLK;
+    const int nblk = span * kUnitBlocks;
     uint32_t* maxbits = sm.maxbits();
     float* sig_in = sm.sig_in();
     float* sig_out = sm.sig_out();
-    // sigma: max |x| over the slice per row m (a non-negative float's bits order like its value)
+    // x: the CTA's K units (slots 0..span-1 = units u0, u0+1, .. mod U) of every row, straight
+    // from global memory (L2 only: X may have been written by the previous grid), into shared
+    // memory at pitch xpitch; max |x| per row on the way (a non-negative float's bits order like
+    // its value)
+    constexpr int UK = kUnitBlocks * F::BLK;
+    const int vec = span * (UK / 4);
     for (int m = 0; m < M; ++m) {
-        const uint4* xv = reinterpret_cast<const uint4*>(xs + m * xpitch);
+        const float* xg = X + static_cast<size_t>(m) * K;
+        float* xd = xs + m * xpitch;
         uint32_t mx = 0;
-        for (int i = tid; i < klen / 4; i += C::NCT) {
-            const uint4 v = xv[i];
-            mx = max(mx, max(max(v.x & 0x7FFFFFFFu, v.y & 0x7FFFFFFFu), max(v.z & 0x7FFFFFFFu, v.w & 0x7FFFFFFFu)));
+        for (int q = tid; q < vec; q += C::NCT) {
+            const int sl = q / (UK / 4);
+            int u = u0 + sl;
+            if (u >= U) u -= U;
+            const int off = 4 * q - sl * UK;
+            const float4 v = __ldcg(reinterpret_cast<const float4*>(xg + static_cast<size_t>(u) * UK + off));
+            *reinterpret_cast<float4*>(xd + sl * UK + off) = v;
+            mx = max(mx, max(max(__float_as_uint(v.x) & 0x7FFFFFFFu, __float_as_uint(v.y) & 0x7FFFFFFFu),
+                             max(__float_as_uint(v.z) & 0x7FFFFFFFu, __float_as_uint(v.w) & 0x7FFFFFFFu)));
         }
         mx = __reduce_max_sync(0xffffffffu, mx);
         if (lane == 0) atomicMax(&maxbits[m], mx);
     }
+    fence_proxy_async_smem();  // these bytes are later overwritten by tensor-map copies
     named_sync(1, C::NCT);
     if (tid < M) {
         const uint32_t bits = maxbits[tid];
@@ -290,31 +297,33 @@ __device__ __forceinline__ void fill_operands(const Smem& sm, const float* xs, i
         sig_out[tid] = exp2i(24 - sg);  // undoes sigma and the 2^-24 of the subnormal codes
     }
     named_sync(1, C::NCT);
-    // B fragments: one item per (block, slice st, decode register i, row m). The two x values
-    // register i holds for slice st, scaled, go split into the hi part to the lane of column 2m
-    // and the lo part to the lane of column 2m + 1 (lane = 4 * (column % 8) + i % 4, register
-    // b0 for i < 4, b1 otherwise; records of paired slices share 16 bytes).
+    // B fragments: one item per (block, slice st, decode register i), rows m inside. The two x
+    // values register i holds for slice st, scaled, go split into the hi part to the lane of
+    // column 2m and the lo part to the lane of column 2m + 1 (lane = 4 * (column % 8) + i % 4,
+    // register b0 for i < 4, b1 otherwise; records of paired slices share 16 bytes).
     uint8_t* bbase = sm.b();
-    const int items = nblk * STEPS * 8 * M;
+    const int items = nblk * STEPS * 8;
     for (int it = tid; it < items; it += C::NCT) {
-        const int rest = it / M;
-        const int m = it - rest * M;
-        const int i = rest & 7, bs = rest >> 3;
+        const int i = it & 7, bs = it >> 3;
         const int st = bs % STEPS, blk = bs / STEPS;
-        const float sc = sig_in[m] * step_scale<TYPE>(st);
-        const float* xb = xs + m * xpitch + blk * F::BLK;
         const int odd = blk & 1;
-        const float v0 = xb[pn_elem(F::CPW, odd, i, st, 0)] * sc;
-        const float v1 = xb[pn_elem(F::CPW, odd, i, st, 1)] * sc;
-        const __half h0 = __float2half_rn(v0), h1 = __float2half_rn(v1);
-        const __half l0 = __float2half_rn(v0 - __half2float(h0)), l1 = __float2half_rn(v1 - __half2float(h1));
-        const int n = 2 * m, tile = n >> 3, tig = i & 3, reg = i >> 2;
+        const int e0 = pn_elem(F::CPW, odd, i, st, 0), e1 = pn_elem(F::CPW, odd, i, st, 1);
+        const int tig = i & 3, reg = i >> 2;
         const bool last_odd = (STEPS & 1) && st == STEPS - 1;
         const int rec = last_odd ? 8 : 16;  // bytes per lane record
-        uint8_t* p = bbase + blk * C::BFU + tile * 256 * STEPS +
-                     (last_odd ? (STEPS / 2) * 512 : (st >> 1) * 512 + (st & 1) * 8) + reg * 4;
-        *reinterpret_cast<uint32_t*>(p + ((((n & 7) << 2) | tig) * rec)) = pack_half2(h0, h1);
-        *reinterpret_cast<uint32_t*>(p + (((((n + 1) & 7) << 2) | tig) * rec)) = pack_half2(l0, l1);
+        uint8_t* p0 = bbase + blk * C::BFU + (last_odd ? (STEPS / 2) * 512 : (st >> 1) * 512 + (st & 1) * 8) + reg * 4;
+        const float stc = step_scale<TYPE>(st);
+        for (int m = 0; m < M; ++m) {
+            const float sc = sig_in[m] * stc;
+            const float* xb = xs + m * xpitch + blk * F::BLK;
+            const float v0 = xb[e0] * sc, v1 = xb[e1] * sc;
+            const __half h0 = __float2half_rn(v0), h1 = __float2half_rn(v1);
+            const __half l0 = __float2half_rn(v0 - __half2float(h0)), l1 = __float2half_rn(v1 - __half2float(h1));
+            const int n = 2 * m;  // hi column; the lo column n + 1 is in the same n8 tile
+            uint8_t* p = p0 + (n >> 3) * 256 * STEPS;
+            *reinterpret_cast<uint32_t*>(p + ((((n & 7) << 2) | tig) * rec)) = pack_half2(h0, h1);
+            *reinterpret_cast<uint32_t*>(p + (((((n + 1) & 7) << 2) | tig) * rec)) = pack_half2(l0, l1);
+        }
     }
     named_sync(1, C::NCT);
     // Z = z * sum over the block of (2^-24 * 8^j) * B, on the tensor core: an A operand with code
@@ -599,14 +608,12 @@ __global__ void __launch_bounds__(Cfg<TYPE, NT, TPW>::THREADS, 1) pn_gemv_kernel
     const int n_items = static_cast<int>(i1 - i0);
     const int u0 = n_items > 0 ? sc.unit_of(i0) : 0;
     const int span = sc.span(i0, i1);
-    const int nblk = span * kUnitBlocks;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < a.NS; ++s) {
             mbar_init(sm.full(s), 1);
             mbar_init(sm.empty(s), C::CW);
         }
-        mbar_init(sm.x_ready(), 1);
         mbar_init(sm.x_free(), 1);
         for (int b = 0; b < 2; ++b) {
             mbar_init(sm.part_full(b), C::CW);
@@ -643,23 +650,11 @@ __global__ void __launch_bounds__(Cfg<TYPE, NT, TPW>::THREADS, 1) pn_gemv_kernel
                 // them into the stages that will not hold x before the previous grid completes
                 for (; ok && gi < min(n_items, cx.x_stage); ++gi) ok = issue(gi);
             }
-            griddep_wait();
-            // x rows at pitch xpitch floats in slot order: units u0 .. U-1 then 0 .. (one or two
-            // bulk copies per row; 16-byte aligned: X is, units are multiples of 512 elements and
-            // the pitch is a multiple of 4)
-            const int run1 = min(span, sc.U - u0);
-            const uint32_t b1 = static_cast<uint32_t>(run1 * UK * 4), b2 = static_cast<uint32_t>((span - run1) * UK * 4);
-            mbar_arrive_expect_tx(sm.x_ready(), (b1 + b2) * cx.M);
-            for (int m = 0; m < cx.M; ++m) {
-                const uint32_t dst = smem_addr(sm.stage(cx.x_stage)) + m * cx.xpitch * 4;
-                const float* xm = cx.X + static_cast<size_t>(m) * cx.K;
-                bulk_g2s_plain(dst, xm + static_cast<size_t>(u0) * UK, b1, sm.x_ready());
-                if (b2) bulk_g2s_plain(dst + b1, xm, b2, sm.x_ready());
-            }
+            griddep_wait();  // without the static-weights flag W may be written by the previous grid
             for (; ok && gi < n_items; ++gi) ok = issue(gi);
             if (!ok) record_error(cx.err, kErrEmptyWait);
             // every copy issued has landed before the CTA may exit
-            bool drained = mbar_wait_bounded(sm.x_ready(), 0);
+            bool drained = true;
             for (int gg = max(0, gi - cx.NS); drained && gg < gi; ++gg)
                 drained = mbar_wait_bounded(sm.full(gg % cx.NS), (gg / cx.NS) & 1);
             if (!drained) record_error(cx.err, kErrDrainWait);
@@ -697,17 +692,14 @@ __global__ void __launch_bounds__(Cfg<TYPE, NT, TPW>::THREADS, 1) pn_gemv_kernel
     } else {
         // ---------------- consumer warps ----------------
         if (n_items > 0) {
-            if (named_sync_and(1, C::NCT, mbar_wait_bounded(sm.x_ready(), 0))) {
-                const float* xs = reinterpret_cast<const float*>(sm.stage(cx.x_stage));
-                fill_operands<TYPE, NT, TPW>(sm, xs, cx.xpitch, nblk, cx.M);
-                if (threadIdx.x == 0) mbar_arrive(sm.x_free());  // the x stages may now take weights
-                if (warp < C::TG)
-                    consumer_loop<TYPE, NT, TPW, 0>(sm, cx, i0, n_items, u0);
-                else
-                    consumer_loop<TYPE, NT, TPW, 1>(sm, cx, i0, n_items, u0);
-            } else if (threadIdx.x == 0) {
-                record_error(cx.err, kErrFullWait);
-            }
+            griddep_wait();  // X belongs to the previous grid until now
+            float* xs = reinterpret_cast<float*>(sm.stage(cx.x_stage));
+            fill_operands<TYPE, NT, TPW>(sm, cx.X, cx.K, sc.U, u0, span, xs, cx.xpitch, cx.M);
+            if (threadIdx.x == 0) mbar_arrive(sm.x_free());  // the x stages may now take weights
+            if (warp < C::TG)
+                consumer_loop<TYPE, NT, TPW, 0>(sm, cx, i0, n_items, u0);
+            else
+                consumer_loop<TYPE, NT, TPW, 1>(sm, cx, i0, n_items, u0);
         }
     }
     // the tiles this CTA completed: every warp sums some of them
