@@ -81,32 +81,28 @@ struct Cfg {
 // a CTA's share touches at most a few units (for operands that would not fit otherwise). CTA c
 // of G takes items [c * items / G, (c + 1) * items / G).
 struct Sched {
-    long long items;
+    int items;  // T * U < 2^31 (checked by the host)
     int T, U, G, tile_major;
-    __host__ __device__ int tile_of(long long i) const {
-        return tile_major ? static_cast<int>(i / U) : static_cast<int>(i % T);
+    __host__ __device__ int tile_of(int i) const { return tile_major ? i / U : i % T; }
+    __host__ __device__ int unit_of(int i) const { return tile_major ? i % U : i / T; }
+    __host__ __device__ int item(int t, int u) const { return tile_major ? t * U + u : u * T + t; }
+    __host__ __device__ int first(int c) const { return static_cast<int>(static_cast<long long>(c) * items / G); }
+    __host__ __device__ int owner(int i) const {
+        return static_cast<int>((static_cast<long long>(i + 1) * G - 1) / items);
     }
-    __host__ __device__ int unit_of(long long i) const {
-        return tile_major ? static_cast<int>(i % U) : static_cast<int>(i / T);
-    }
-    __host__ __device__ long long item(int t, int u) const {
-        return tile_major ? static_cast<long long>(t) * U + u : static_cast<long long>(u) * T + t;
-    }
-    __host__ __device__ long long first(long long c) const { return c * items / G; }
-    __host__ __device__ long long owner(long long i) const { return ((i + 1) * G - 1) / items; }
     // A share is a run of consecutive items of one CTA within a tile. Tile-major (or T = 1):
     // the items of tile t are consecutive, a share starts at unit 0 and at the first item of
     // every CTA that begins inside the tile. Unit-major: every unit is a share of its own.
     __host__ __device__ bool consecutive() const { return tile_major || T == 1; }
     __host__ __device__ int shares(int t) const {
         if (!consecutive()) return U;
-        const long long a0 = item(t, 0);
-        return static_cast<int>(owner(a0 + U - 1) - owner(a0)) + 1;
+        const int a0 = item(t, 0);
+        return owner(a0 + U - 1) - owner(a0) + 1;
     }
     // units a CTA's share touches (a cyclic range starting at unit_of(first item))
-    __host__ __device__ int span(long long i0, long long i1) const {
+    __host__ __device__ int span(int i0, int i1) const {
         if (i1 <= i0) return 0;
-        if (tile_major) return static_cast<int>(i1 - i0 < U ? i1 - i0 : U);
+        if (tile_major) return i1 - i0 < U ? i1 - i0 : U;
         return unit_of(i1 - 1) - unit_of(i0) + 1;
     }
 };
@@ -297,32 +293,43 @@ __device__ __forceinline__ void fill_operands(const Smem& sm, const float* X, in
         sig_out[tid] = exp2i(24 - sg);  // undoes sigma and the 2^-24 of the subnormal codes
     }
     named_sync(1, C::NCT);
-    // B fragments: one item per (block, slice st, decode register i), rows m inside. The two x
-    // values register i holds for slice st, scaled, go split into the hi part to the lane of
-    // column 2m and the lo part to the lane of column 2m + 1 (lane = 4 * (column % 8) + i % 4,
-    // register b0 for i < 4, b1 otherwise; records of paired slices share 16 bytes).
+    // B fragments: one item per (block, pair of slices, lane column c), rows m inside. For slices
+    // 2p and 2p + 1 the item builds the registers b0 (decode register c) and b1 (register c + 4)
+    // of row m's hi column 2m and lo column 2m + 1 and stores them as the two 16-byte lane
+    // records (lane = 4 * (column % 8) + c; an odd last slice has 8-byte records).
     uint8_t* bbase = sm.b();
-    const int items = nblk * STEPS * 8;
+    constexpr int PAIRS = (STEPS + 1) / 2;
+    const int items = nblk * PAIRS * 4;
     for (int it = tid; it < items; it += C::NCT) {
-        const int i = it & 7, bs = it >> 3;
-        const int st = bs % STEPS, blk = bs / STEPS;
+        const int c = it & 3, rest = it >> 2;
+        const int pr = rest % PAIRS, blk = rest / PAIRS;
         const int odd = blk & 1;
-        const int e0 = pn_elem(F::CPW, odd, i, st, 0), e1 = pn_elem(F::CPW, odd, i, st, 1);
-        const int tig = i & 3, reg = i >> 2;
-        const bool last_odd = (STEPS & 1) && st == STEPS - 1;
-        const int rec = last_odd ? 8 : 16;  // bytes per lane record
-        uint8_t* p0 = bbase + blk * C::BFU + (last_odd ? (STEPS / 2) * 512 : (st >> 1) * 512 + (st & 1) * 8) + reg * 4;
-        const float stc = step_scale<TYPE>(st);
+        const bool single = (STEPS & 1) && pr == PAIRS - 1;  // the odd last slice alone
         for (int m = 0; m < M; ++m) {
-            const float sc = sig_in[m] * stc;
             const float* xb = xs + m * xpitch + blk * F::BLK;
-            const float v0 = xb[e0] * sc, v1 = xb[e1] * sc;
-            const __half h0 = __float2half_rn(v0), h1 = __float2half_rn(v1);
-            const __half l0 = __float2half_rn(v0 - __half2float(h0)), l1 = __float2half_rn(v1 - __half2float(h1));
+            uint32_t hi[4] = {0u, 0u, 0u, 0u}, lo[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {  // q = 2 * (slice - 2pr) + register
+                const int st = 2 * pr + (q >> 1), i = c + 4 * (q & 1);
+                if (st < STEPS) {
+                    const float sc = sig_in[m] * step_scale<TYPE>(st);
+                    const float v0 = xb[pn_elem(F::CPW, odd, i, st, 0)] * sc;
+                    const float v1 = xb[pn_elem(F::CPW, odd, i, st, 1)] * sc;
+                    const __half h0 = __float2half_rn(v0), h1 = __float2half_rn(v1);
+                    hi[q] = pack_half2(h0, h1);
+                    lo[q] = pack_half2(__float2half_rn(v0 - __half2float(h0)), __float2half_rn(v1 - __half2float(h1)));
+                }
+            }
             const int n = 2 * m;  // hi column; the lo column n + 1 is in the same n8 tile
-            uint8_t* p = p0 + (n >> 3) * 256 * STEPS;
-            *reinterpret_cast<uint32_t*>(p + ((((n & 7) << 2) | tig) * rec)) = pack_half2(h0, h1);
-            *reinterpret_cast<uint32_t*>(p + (((((n + 1) & 7) << 2) | tig) * rec)) = pack_half2(l0, l1);
+            uint8_t* tb = bbase + blk * C::BFU + (n >> 3) * 256 * STEPS + pr * 512;
+            const int lh = ((n & 7) << 2) | c, ll = (((n + 1) & 7) << 2) | c;
+            if (single) {
+                *reinterpret_cast<uint2*>(tb + lh * 8) = make_uint2(hi[0], hi[1]);
+                *reinterpret_cast<uint2*>(tb + ll * 8) = make_uint2(lo[0], lo[1]);
+            } else {
+                *reinterpret_cast<uint4*>(tb + lh * 16) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                *reinterpret_cast<uint4*>(tb + ll * 16) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            }
         }
     }
     named_sync(1, C::NCT);
@@ -419,7 +426,7 @@ __device__ __forceinline__ void pn_block(const uint8_t* const (&row0)[TPW], int 
 }
 
 template <int TYPE, int NT, int TPW, int H>
-__device__ __forceinline__ void consumer_loop(const Smem& sm, const Ctx& cx, long long i0, int n_items, int u0) {
+__device__ __forceinline__ void consumer_loop(const Smem& sm, const Ctx& cx, int i0, int n_items, int u0) {
     using C = Cfg<TYPE, NT, TPW>;
     const Sched& sc = cx.sc;
     const int M = cx.M, NS = cx.NS, U = sc.U;
@@ -577,10 +584,9 @@ __device__ __forceinline__ void finish_tile(const Ctx& a, int t, int lane) {
             acc.w += v.w;
         };
         if (sc.consecutive()) {
-            const long long a0 = sc.item(t, 0);
+            const int a0 = sc.item(t, 0);
             add_slot(0);
-            for (long long c = sc.owner(a0) + 1; c <= sc.owner(a0 + sc.U - 1); ++c)
-                add_slot(static_cast<int>(sc.first(c) - a0));
+            for (int c = sc.owner(a0) + 1; c <= sc.owner(a0 + sc.U - 1); ++c) add_slot(sc.first(c) - a0);
         } else {
             for (int u = 0; u < sc.U; ++u) add_slot(u);
         }
@@ -604,7 +610,7 @@ __global__ void __launch_bounds__(Cfg<TYPE, NT, TPW>::THREADS, 1) pn_gemv_kernel
 
     // this CTA's share of the items, and the K units it touches (slot = (u - u0) mod U)
     const Sched& sc = cx.sc;
-    const long long i0 = sc.first(blockIdx.x), i1 = sc.first(blockIdx.x + 1);
+    const int i0 = sc.first(blockIdx.x), i1 = sc.first(blockIdx.x + 1);
     const int n_items = static_cast<int>(i1 - i0);
     const int u0 = n_items > 0 ? sc.unit_of(i0) : 0;
     const int span = sc.span(i0, i1);
@@ -721,13 +727,12 @@ struct Plan {
 // Shared-memory layout and stage count for one item order; false when it does not fit.
 bool layout(int blk_weights, int bfu, int M, int ns_req, Plan& p) {
     p.span_max = 0;
-    for (long long c = 0; c < p.sc.G; ++c)
-        p.span_max = std::max(p.span_max, p.sc.span(p.sc.first(c), p.sc.first(c + 1)));
+    for (int c = 0; c < p.sc.G; ++c) p.span_max = std::max(p.span_max, p.sc.span(p.sc.first(c), p.sc.first(c + 1)));
     const uint32_t nblk = static_cast<uint32_t>(p.span_max) * kUnitBlocks;
     p.xpitch = static_cast<int>(nblk) * blk_weights + 4;
     p.bar_off = 0;
     p.misc_off = 8u * (2 * kMaxStages + 6);
-    p.list_cap = static_cast<int>((p.sc.items + p.sc.G - 1) / p.sc.G);
+    p.list_cap = (p.sc.items + p.sc.G - 1) / p.sc.G;
     p.list_off = align_up(p.misc_off + 192u, 16);
     p.z_off = align_up(p.list_off + (2u * p.list_cap + 4u) * 4u, 16);
     p.part_off = align_up(p.z_off + nblk * M * 4u, 16);
@@ -770,7 +775,7 @@ bool make_plan(int blk_weights, int bfu, int M, int64_t T, int64_t U, int sms, b
             q.sc.tile_major = tm;
             if (!layout(blk_weights, bfu, M, ns_req, q)) continue;
             bool publish = false;
-            for (int64_t c = 1; c < G && !publish; ++c) publish = q.sc.tile_of(q.sc.first(c)) == q.sc.tile_of(q.sc.first(c) - 1);
+            for (int c = 1; c < G && !publish; ++c) publish = q.sc.tile_of(q.sc.first(c)) == q.sc.tile_of(q.sc.first(c) - 1);
             if (!tm && U > 1) publish = true;
             const double cost = static_cast<double>((items + G - 1) / G) + (publish ? 2.5 : 0.0);
             if (!found || cost < best) {
@@ -874,7 +879,8 @@ cudaError_t launch_pn_gemv_mma(int type, const uint8_t* W, int64_t N, int64_t K,
     const int64_t nb = K / blk;
     if (nb % kUnitBlocks != 0 || M < 1 || M > 16) return cudaErrorNotSupported;
     const int64_t U = nb / kUnitBlocks, T = (N + kTileRows - 1) / kTileRows;
-    if (N > INT32_MAX || K > INT32_MAX || U * kUnitU32 > INT32_MAX || T * kTileRows > INT32_MAX)
+    if (N > INT32_MAX || K > INT32_MAX || U * kUnitU32 > INT32_MAX || T * kTileRows > INT32_MAX ||
+        T * U > INT32_MAX)
         return cudaErrorNotSupported;
     if (reinterpret_cast<uintptr_t>(W) % 16 != 0 || reinterpret_cast<uintptr_t>(X) % 16 != 0)
         return cudaErrorNotSupported;
@@ -888,7 +894,7 @@ cudaError_t launch_pn_gemv_mma(int type, const uint8_t* W, int64_t N, int64_t K,
     a.M = M;
     a.sc.T = static_cast<int>(T);
     a.sc.U = static_cast<int>(U);
-    a.sc.items = T * U;
+    a.sc.items = static_cast<int>(T * U);
     const MmaConfig c = (cfg.rw > 0 || cfg.S > 0 || cfg.ns > 0) ? cfg : env_config();
     return (type == kTypePn3t) ? launch_typed<kTypePn3t>(a, c, static_weights, stream)
                                : launch_typed<kTypePn4t>(a, c, static_weights, stream);
