@@ -378,6 +378,30 @@ def run_ours(args):
         pg.destroy_process_group()
 
 
+def run_single(args):
+    """One projection of layer 0, called a few times on the default stream: the small case the
+    committed ncu summaries are captured on (one kernel, few launches, a few GB at most)."""
+    import block_quantized_weight_pn3t_gb300 as pnq
+    from block_quantized_weight_pn3t_gb300 import synth
+    names = [p[0] for p in PROJECTIONS]
+    if args.single not in names:
+        raise SystemExit(f"--single must be one of {names}")
+    p = names.index(args.single)
+    _, t, N, K = PROJECTIONS[p]
+    torch.cuda.set_device(0)
+    W = synth.pn_random_blocks(t, N, K, seed=SEED, stream=p, device="cuda")
+    X = torch.from_numpy(host_x(args.m)[K]).cuda()
+    Y = torch.empty((args.m, N), dtype=torch.float32, device="cuda")
+    for _ in range(args.warmup):
+        pnq.gemv(t, W, X, N, K, Y=Y, flags=pnq.GEMV_STATIC_WEIGHTS)
+    torch.cuda.synchronize()
+    err = pnq.device_error()
+    print(json.dumps({"single": args.single, "type": t, "N": N, "K": K, "M": args.m, "launches": args.warmup,
+                      "weight_bytes": N * row_bytes(t, K), "device_error": err}))
+    if err:
+        raise SystemExit(1)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -387,10 +411,14 @@ def main():
     ap.add_argument("--m", type=int, default=1, help="activation rows (1..16)")
     ap.add_argument("--layers", type=int, default=64)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--single", default=None,
+                    help="run one projection of layer 0 --warmup times and exit (profiling case)")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
-    if args.impl == "reference":
+    if args.single:
+        run_single(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)
