@@ -25,6 +25,7 @@ class Status(enum.IntEnum):
     ERR_CUDA = -5
     ERR_DEVICE = -6
     ERR_FLAGS = -7
+    ERR_SCRATCH = -8
 
 
 GEMV_STATIC_WEIGHTS = 1
@@ -62,6 +63,8 @@ def lib() -> ctypes.CDLL:
         L.pnq_gemv.argtypes = [I, P, I64, I64, P, I, P, P]
         L.pnq_gemv_ex.restype = I
         L.pnq_gemv_ex.argtypes = [I, P, I64, I64, P, I, P, ctypes.c_uint, P]
+        L.pnq_gemv_noalloc.restype = I
+        L.pnq_gemv_noalloc.argtypes = [I, P, I64, I64, P, I, P, ctypes.c_uint, P]
         L.pnq_dequantize_row.restype = I
         L.pnq_dequantize_row.argtypes = [I, P, I64, I64, P, P]
         L.pnq_validate_row.restype = I
@@ -102,6 +105,11 @@ def gemv_ptr(type_: int, W, N: int, K: int, X: int, M: int, Y: int, stream: int 
 def gemv_ex_ptr(type_: int, W, N: int, K: int, X: int, M: int, Y: int, flags: int, stream: int = 0) -> int:
     return lib().pnq_gemv_ex(type_, _w_arg(type_, W), N, K, ctypes.c_void_p(X), M, ctypes.c_void_p(Y),
                              flags, ctypes.c_void_p(stream))
+
+
+def gemv_noalloc_ptr(type_: int, W, N: int, K: int, X: int, M: int, Y: int, flags: int = 0, stream: int = 0) -> int:
+    return lib().pnq_gemv_noalloc(type_, _w_arg(type_, W), N, K, ctypes.c_void_p(X), M, ctypes.c_void_p(Y),
+                                  flags, ctypes.c_void_p(stream))
 
 
 def dequantize_row_ptr(type_: int, W, n_rows: int, K: int, out: int, stream: int = 0) -> int:
@@ -147,6 +155,18 @@ def gemv(type_: int, W, X, N: int, K: int, Y=None, stream=None, flags: int = 0):
         Y = torch.empty((M, N), dtype=torch.float32, device=X.device)
     _check(gemv_ex_ptr(type_, _weights(type_, W), N, K, X.data_ptr(), M, Y.data_ptr(), flags,
                        _stream_handle(stream)), "pnq_gemv_ex")
+    return Y
+
+
+def gemv_noalloc(type_: int, W, X, N: int, K: int, Y=None, stream=None, flags: int = 0):
+    """gemv through pnq_gemv_noalloc (no device allocation; PnqError ERR_SCRATCH when the shape
+    needs more than the library's built-in scratch)."""
+    import torch
+    M = X.shape[0] if X.dim() == 2 else 1
+    if Y is None:
+        Y = torch.empty((M, N), dtype=torch.float32, device=X.device)
+    _check(gemv_noalloc_ptr(type_, _weights(type_, W), N, K, X.data_ptr(), M, Y.data_ptr(), flags,
+                            _stream_handle(stream)), "pnq_gemv_noalloc")
     return Y
 
 

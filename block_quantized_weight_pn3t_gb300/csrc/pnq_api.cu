@@ -16,6 +16,12 @@
 // device that loads the library).
 __device__ int g_pnq_error_word = 0;
 
+// Scratch of pnq_gemv_noalloc: fp32 partial sums, then the tile counters (zero at load; every
+// launch leaves them zero).
+constexpr size_t kNoAllocCounters = 16384;
+constexpr size_t kNoAllocFloats = PNQ_NOALLOC_SCRATCH_BYTES / 4 - kNoAllocCounters;
+static __device__ __align__(256) float g_pnq_noalloc_scratch[PNQ_NOALLOC_SCRATCH_BYTES / 4];
+
 namespace pnq {
 
 namespace {
@@ -26,6 +32,24 @@ int current_device() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
     return dev;
+}
+
+// pnq_gemv_noalloc's scratch on the current device (address looked up once per device).
+ExtWorkspace noalloc_scratch() {
+    static float* ptrs[kMaxDevices] = {};
+    ExtWorkspace w;
+    const int dev = current_device();
+    if (dev < 0) return w;
+    if (!ptrs[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_pnq_noalloc_scratch) != cudaSuccess) return w;
+        ptrs[dev] = static_cast<float*>(p);
+    }
+    w.ws = ptrs[dev];
+    w.floats = kNoAllocFloats;
+    w.cnt = reinterpret_cast<uint32_t*>(ptrs[dev] + kNoAllocFloats);
+    w.counters = kNoAllocCounters;
+    return w;
 }
 
 int* error_word() {
@@ -177,8 +201,10 @@ cudaError_t stream_workspace(cudaStream_t stream, size_t floats, size_t counters
 
 using namespace pnq;
 
-extern "C" int pnq_gemv_ex(int type, const void* W, int64_t N, int64_t K, const void* X, int M, float* Y,
-                           unsigned int flags, cudaStream_t stream) {
+namespace {
+
+int gemv_impl(int type, const void* W, int64_t N, int64_t K, const void* X, int M, float* Y, unsigned int flags,
+              cudaStream_t stream, bool no_alloc) {
     Nvfp4View nv{};
     int rc = check_common(type, W, N, K, &nv);
     if (rc != PNQ_OK) return rc;
@@ -204,15 +230,33 @@ extern "C" int pnq_gemv_ex(int type, const void* W, int64_t N, int64_t K, const 
     const uint8_t* w = static_cast<const uint8_t*>(W);
     const float* x = static_cast<const float*>(X);
     if (mode != 1 && aligned(w, 16) && (K / block_weights(type)) % 8 == 0) {
-        if (mode == 3) {
+        if (mode == 3 && !no_alloc) {
             const cudaError_t e = launch_pn_gemv_tc(type, w, N, K, x, M, Y, error_word(), static_w, stream);
             if (e != cudaErrorNotSupported) return map_cuda(e);
         }
+        ExtWorkspace ext;
+        if (no_alloc) {
+            ext = noalloc_scratch();
+            if (!ext.ws) return PNQ_ERR_CUDA;
+        }
         const cudaError_t e =
-            launch_pn_gemv_mma(type, w, N, K, x, M, Y, error_word(), MmaConfig{0, 0, 0, 0}, static_w, stream);
+            launch_pn_gemv_mma(type, w, N, K, x, M, Y, error_word(), MmaConfig{0, 0, 0, 0}, static_w, stream, ext);
+        if (no_alloc && e == cudaErrorMemoryAllocation) return PNQ_ERR_SCRATCH;
         if (e != cudaErrorNotSupported) return map_cuda(e);
     }
     return map_cuda(launch_pn_gemv_simt(type, w, N, K, x, M, Y, stream));
+}
+
+}  // namespace
+
+extern "C" int pnq_gemv_ex(int type, const void* W, int64_t N, int64_t K, const void* X, int M, float* Y,
+                           unsigned int flags, cudaStream_t stream) {
+    return gemv_impl(type, W, N, K, X, M, Y, flags, stream, false);
+}
+
+extern "C" int pnq_gemv_noalloc(int type, const void* W, int64_t N, int64_t K, const void* X, int M, float* Y,
+                                unsigned int flags, cudaStream_t stream) {
+    return gemv_impl(type, W, N, K, X, M, Y, flags, stream, true);
 }
 
 extern "C" int pnq_gemv(int type, const void* W, int64_t N, int64_t K, const void* X, int M, float* Y,

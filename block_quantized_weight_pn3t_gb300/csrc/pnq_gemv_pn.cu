@@ -720,6 +720,7 @@ uint32_t align_up(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
 
 struct Plan {
     Sched sc{};
+    bool publish = false;  // some tile is shared by several CTAs (the workspace is used)
     int NS = 0, x_stage = 0, span_max = 0, xpitch = 0, list_cap = 0;
     uint32_t bar_off = 0, misc_off = 0, list_off = 0, z_off = 0, part_off = 0, b_off = 0, stage_off = 0, total = 0;
 };
@@ -780,6 +781,7 @@ bool make_plan(int blk_weights, int bfu, int M, int64_t T, int64_t U, int sms, b
             const double cost = static_cast<double>((items + G - 1) / G) + (publish ? 2.5 : 0.0);
             if (!found || cost < best) {
                 best = cost;
+                q.publish = publish;
                 p = q;
                 found = true;
             }
@@ -809,7 +811,8 @@ MmaConfig env_config() {
 }
 
 template <int TYPE, int NT, int TPW>
-cudaError_t launch_cfg(PnArgs& a, const MmaConfig& cfg, bool static_weights, cudaStream_t stream) {
+cudaError_t launch_cfg(PnArgs& a, const MmaConfig& cfg, bool static_weights, cudaStream_t stream,
+                       const ExtWorkspace& ext) {
     using F = PnFmt<TYPE>;
     using C = Cfg<TYPE, NT, TPW>;
     Plan p;
@@ -826,9 +829,17 @@ cudaError_t launch_cfg(PnArgs& a, const MmaConfig& cfg, bool static_weights, cud
         if (e != cudaSuccess) return e;
         opted[dev] = true;
     }
-    e = stream_workspace(stream, static_cast<size_t>(a.sc.T) * a.sc.U * a.M * kTileRows, static_cast<size_t>(a.sc.T),
-                         &a.ws, &a.cnt);
-    if (e != cudaSuccess) return e;
+    const size_t ws_floats = static_cast<size_t>(a.sc.T) * a.sc.U * a.M * kTileRows;
+    if (ext.ws) {
+        // the caller's scratch: too small only matters when CTAs share tiles
+        if (p.publish && (ext.floats < ws_floats || ext.counters < static_cast<size_t>(a.sc.T)))
+            return cudaErrorMemoryAllocation;
+        a.ws = ext.ws;
+        a.cnt = ext.cnt;
+    } else {
+        e = stream_workspace(stream, ws_floats, static_cast<size_t>(a.sc.T), &a.ws, &a.cnt);
+        if (e != cudaSuccess) return e;
+    }
     a.sc = p.sc;
     a.NS = p.NS;
     a.x_stage = p.x_stage;
@@ -857,23 +868,25 @@ cudaError_t launch_cfg(PnArgs& a, const MmaConfig& cfg, bool static_weights, cud
 }
 
 template <int TYPE>
-cudaError_t launch_typed(PnArgs& a, const MmaConfig& cfg, bool static_weights, cudaStream_t stream) {
+cudaError_t launch_typed(PnArgs& a, const MmaConfig& cfg, bool static_weights, cudaStream_t stream,
+                         const ExtWorkspace& ext) {
     const int nt = (2 * a.M + 7) / 8;
     // one tile per warp (16 consumer warps) for the matrix-vector range; two tiles per warp
     // (8 consumer warps, B fragments reused across the tiles) for wider batches
     const int tpw = cfg.rw > 0 ? cfg.rw : (nt == 1 ? 1 : 2);
-    if (nt == 1) return tpw == 1 ? launch_cfg<TYPE, 1, 1>(a, cfg, static_weights, stream)
-                                 : launch_cfg<TYPE, 1, 2>(a, cfg, static_weights, stream);
-    if (nt == 2) return tpw == 1 ? launch_cfg<TYPE, 2, 1>(a, cfg, static_weights, stream)
-                                 : launch_cfg<TYPE, 2, 2>(a, cfg, static_weights, stream);
-    return tpw == 1 ? launch_cfg<TYPE, 4, 1>(a, cfg, static_weights, stream)
-                    : launch_cfg<TYPE, 4, 2>(a, cfg, static_weights, stream);
+    if (nt == 1) return tpw == 1 ? launch_cfg<TYPE, 1, 1>(a, cfg, static_weights, stream, ext)
+                                 : launch_cfg<TYPE, 1, 2>(a, cfg, static_weights, stream, ext);
+    if (nt == 2) return tpw == 1 ? launch_cfg<TYPE, 2, 1>(a, cfg, static_weights, stream, ext)
+                                 : launch_cfg<TYPE, 2, 2>(a, cfg, static_weights, stream, ext);
+    return tpw == 1 ? launch_cfg<TYPE, 4, 1>(a, cfg, static_weights, stream, ext)
+                    : launch_cfg<TYPE, 4, 2>(a, cfg, static_weights, stream, ext);
 }
 
 }  // namespace
 
 cudaError_t launch_pn_gemv_mma(int type, const uint8_t* W, int64_t N, int64_t K, const float* X, int M, float* Y,
-                               int* err, MmaConfig cfg, bool static_weights, cudaStream_t stream) {
+                               int* err, MmaConfig cfg, bool static_weights, cudaStream_t stream,
+                               const ExtWorkspace& ext) {
     if (N == 0) return cudaSuccess;
     const int blk = (type == kTypePn3t) ? 80 : 64;
     const int64_t nb = K / blk;
@@ -896,8 +909,8 @@ cudaError_t launch_pn_gemv_mma(int type, const uint8_t* W, int64_t N, int64_t K,
     a.sc.U = static_cast<int>(U);
     a.sc.items = static_cast<int>(T * U);
     const MmaConfig c = (cfg.rw > 0 || cfg.S > 0 || cfg.ns > 0) ? cfg : env_config();
-    return (type == kTypePn3t) ? launch_typed<kTypePn3t>(a, c, static_weights, stream)
-                               : launch_typed<kTypePn4t>(a, c, static_weights, stream);
+    return (type == kTypePn3t) ? launch_typed<kTypePn3t>(a, c, static_weights, stream, ext)
+                               : launch_typed<kTypePn4t>(a, c, static_weights, stream, ext);
 }
 
 }  // namespace pnq

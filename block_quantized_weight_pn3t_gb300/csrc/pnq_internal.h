@@ -53,8 +53,16 @@ cudaError_t launch_nvfp4_gemv_simt(const Nvfp4View& w, int64_t N, int64_t K, con
 // static_weights: the weights are not written by work queued earlier in the stream, so they
 // may be prefetched before the previous grid completes. Returns cudaErrorNotSupported when
 // the shape is outside the fast path's range (the caller then uses the generic path).
+// Workspace handed in by the caller (nullptr ws: the per-stream workspace is used).
+struct ExtWorkspace {
+    float* ws = nullptr;
+    uint32_t* cnt = nullptr;
+    size_t floats = 0, counters = 0;
+};
+
 cudaError_t launch_pn_gemv_mma(int type, const uint8_t* W, int64_t N, int64_t K, const float* X, int M,
-                               float* Y, int* err, MmaConfig cfg, bool static_weights, cudaStream_t stream);
+                               float* Y, int* err, MmaConfig cfg, bool static_weights, cudaStream_t stream,
+                               const ExtWorkspace& ext = ExtWorkspace{});
 // Tensor-core path (tcgen05, tensor memory): 16-byte aligned weights and x, (K / block) a
 // multiple of 8. Keeps a per-(device, stream) workspace of partial rows. Returns
 // cudaErrorNotSupported outside its range.

@@ -54,7 +54,8 @@ enum pnq_status {
     PNQ_ERR_ALIGN = -4,  /* a pointer misses its minimum alignment (see each call) */
     PNQ_ERR_CUDA = -5,   /* a CUDA call failed (launch error, no device, bad stream) */
     PNQ_ERR_DEVICE = -6, /* a kernel gave up on an internal wait (see pnq_device_error) */
-    PNQ_ERR_FLAGS = -7   /* unknown bit in a flags argument */
+    PNQ_ERR_FLAGS = -7,  /* unknown bit in a flags argument */
+    PNQ_ERR_SCRATCH = -8 /* pnq_gemv_noalloc: the shape needs more than the built-in scratch */
 };
 
 /* Flags of pnq_gemv_ex. */
@@ -103,6 +104,19 @@ int pnq_gemv(int type, const void* W, int64_t N, int64_t K, const void* X, int M
  */
 int pnq_gemv_ex(int type, const void* W, int64_t N, int64_t K, const void* X, int M, float* Y,
                 unsigned int flags, cudaStream_t stream);
+
+/*
+ * pnq_gemv_noalloc -- pnq_gemv_ex that allocates nothing. The pages define no counterpart:
+ * it is a library convenience for callers that must not allocate device memory. The fast PN
+ * path's cross-CTA partial sums then live in one file-scope device array of the library
+ * (PNQ_NOALLOC_SCRATCH_BYTES, shared by every call on the device, so calls through this entry
+ * must be ordered with each other, e.g. on one stream) instead of the per-stream workspace
+ * pnq_gemv keeps. A shape whose partial sums need more than that returns PNQ_ERR_SCRATCH
+ * before anything is launched; otherwise results are identical to pnq_gemv_ex.
+ */
+#define PNQ_NOALLOC_SCRATCH_BYTES (4u * 1024u * 1024u)
+int pnq_gemv_noalloc(int type, const void* W, int64_t N, int64_t K, const void* X, int M, float* Y,
+                     unsigned int flags, cudaStream_t stream);
 
 /*
  * pnq_dequantize_row -- out[r][k] = the fp32 weight, bit-exact:
