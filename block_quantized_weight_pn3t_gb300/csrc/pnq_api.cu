@@ -152,7 +152,8 @@ struct Workspace {
 
 }  // namespace
 
-bool encode_u32_map(CUtensorMap* map, const void* base, int64_t rows, int64_t row_u32, int box_x, int box_y) {
+bool encode_u32_map(CUtensorMap* map, const void* base, int64_t rows, int64_t row_u32, int box_x, int box_y,
+                    bool swizzle_128b) {
     EncodeFn enc = tensor_map_encoder();
     if (!enc) return false;
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(row_u32), static_cast<cuuint64_t>(rows)};
@@ -160,8 +161,8 @@ bool encode_u32_map(CUtensorMap* map, const void* base, int64_t rows, int64_t ro
     const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_x), static_cast<cuuint32_t>(box_y)};
     const cuuint32_t estr[2] = {1, 1};
     return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(base), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+               CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle_128b ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 cudaError_t stream_workspace(cudaStream_t stream, size_t floats, size_t counters, float** ws, uint32_t** cnt) {
@@ -216,12 +217,18 @@ int gemv_impl(int type, const void* W, int64_t N, int64_t K, const void* X, int 
     if (!aligned(Y, 4)) return PNQ_ERR_ALIGN;
     const bool static_w = (flags & PNQ_GEMV_STATIC_WEIGHTS) != 0;
     const int mode = forced_kernel();
+    ExtWorkspace ext;
+    if (no_alloc) {
+        ext = noalloc_scratch();
+        if (!ext.ws) return PNQ_ERR_CUDA;
+    }
     if (type == PNQ_NVFP4) {
         if (!aligned(X, 2)) return PNQ_ERR_ALIGN;
         const uint16_t* x = static_cast<const uint16_t*>(X);
-        if (mode != 1 && aligned(nv.codes, 16) && aligned(nv.scales, 16) && K % 256 == 0) {
-            const cudaError_t e =
-                launch_nvfp4_gemv_mma(nv, N, K, x, M, Y, error_word(), MmaConfig{0, 0, 0, 0}, static_w, stream);
+        if (mode != 1 && aligned(nv.codes, 16) && aligned(nv.scales, 16) && aligned(x, 16) && K % 256 == 0) {
+            const cudaError_t e = launch_nvfp4_gemv_mma(nv, N, K, x, M, Y, error_word(), MmaConfig{0, 0, 0, 0},
+                                                        static_w, stream, ext);
+            if (no_alloc && e == cudaErrorMemoryAllocation) return PNQ_ERR_SCRATCH;
             if (e != cudaErrorNotSupported) return map_cuda(e);
         }
         return map_cuda(launch_nvfp4_gemv_simt(nv, N, K, x, M, Y, stream));
@@ -233,11 +240,6 @@ int gemv_impl(int type, const void* W, int64_t N, int64_t K, const void* X, int 
         if (mode == 3 && !no_alloc) {
             const cudaError_t e = launch_pn_gemv_tc(type, w, N, K, x, M, Y, error_word(), static_w, stream);
             if (e != cudaErrorNotSupported) return map_cuda(e);
-        }
-        ExtWorkspace ext;
-        if (no_alloc) {
-            ext = noalloc_scratch();
-            if (!ext.ws) return PNQ_ERR_CUDA;
         }
         const cudaError_t e =
             launch_pn_gemv_mma(type, w, N, K, x, M, Y, error_word(), MmaConfig{0, 0, 0, 0}, static_w, stream, ext);

@@ -21,12 +21,22 @@ struct MmaConfig {
     int ns;   // pipeline stages
 };
 
+// Workspace handed in by the caller (nullptr ws: the per-stream workspace is used).
+struct ExtWorkspace {
+    float* ws = nullptr;
+    uint32_t* cnt = nullptr;
+    size_t floats = 0, counters = 0;
+};
+
 int device_sm_count();
 
 // 2-D tensor map over a row-major u32 matrix [rows][row_u32] (row pitch a multiple of 16
-// bytes) with box {box_x, box_y}; rows past the end read as zeros. False when the driver entry
-// point is missing or the encoder rejects the arguments.
-bool encode_u32_map(CUtensorMap* map, const void* base, int64_t rows, int64_t row_u32, int box_x, int box_y);
+// bytes) with box {box_x, box_y}; rows past the end read as zeros. swizzle_128b: the copy
+// stores 16-byte chunk c of box row r at chunk c ^ (r % 8) of that row (box rows of 128 bytes,
+// shared destination 1024-byte aligned). False when the driver entry point is missing or the
+// encoder rejects the arguments.
+bool encode_u32_map(CUtensorMap* map, const void* base, int64_t rows, int64_t row_u32, int box_x, int box_y,
+                    bool swizzle_128b = false);
 
 // Workspace of the stream-K GEMV kernels, one per (device, stream): `floats` partial sums and
 // `counters` tile counters (zero between launches). Grows on demand; outgrown buffers stay
@@ -53,13 +63,6 @@ cudaError_t launch_nvfp4_gemv_simt(const Nvfp4View& w, int64_t N, int64_t K, con
 // static_weights: the weights are not written by work queued earlier in the stream, so they
 // may be prefetched before the previous grid completes. Returns cudaErrorNotSupported when
 // the shape is outside the fast path's range (the caller then uses the generic path).
-// Workspace handed in by the caller (nullptr ws: the per-stream workspace is used).
-struct ExtWorkspace {
-    float* ws = nullptr;
-    uint32_t* cnt = nullptr;
-    size_t floats = 0, counters = 0;
-};
-
 cudaError_t launch_pn_gemv_mma(int type, const uint8_t* W, int64_t N, int64_t K, const float* X, int M,
                                float* Y, int* err, MmaConfig cfg, bool static_weights, cudaStream_t stream,
                                const ExtWorkspace& ext = ExtWorkspace{});
@@ -69,6 +72,7 @@ cudaError_t launch_pn_gemv_mma(int type, const uint8_t* W, int64_t N, int64_t K,
 cudaError_t launch_pn_gemv_tc(int type, const uint8_t* W, int64_t N, int64_t K, const float* X, int M, float* Y,
                               int* err, bool static_weights, cudaStream_t stream);
 cudaError_t launch_nvfp4_gemv_mma(const Nvfp4View& w, int64_t N, int64_t K, const uint16_t* X, int M,
-                                  float* Y, int* err, MmaConfig cfg, bool static_weights, cudaStream_t stream);
+                                  float* Y, int* err, MmaConfig cfg, bool static_weights, cudaStream_t stream,
+                                  const ExtWorkspace& ext = ExtWorkspace{});
 
 }  // namespace pnq

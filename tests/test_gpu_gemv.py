@@ -76,7 +76,7 @@ def test_pn_shapes(oracle, type_, nblk, N, M):
 
 @pytest.mark.parametrize("K", [256, 768, 80, 528])
 @pytest.mark.parametrize("N", [1, 33, 130])
-@pytest.mark.parametrize("M", [1, 3, 4, 5, 8, 16])
+@pytest.mark.parametrize("M", [1, 3, 4, 5, 8, 9, 16])
 def test_nvfp4_shapes(oracle, K, N, M):
     seed = hash((K, N, M)) % 1000
     codes, scales, g = synth.nvfp4_random(N, K, seed=seed)
@@ -186,7 +186,7 @@ for type_, N, K, M in [(124, 200, 80*48, 1), (125, 130, 64*80, 3), (125, 64, 64*
         Y = pnq.gemv(type_, W.cuda(), torch.from_numpy(X).cuda(), N, K, flags=flags).cpu().numpy()
         Yr, Ar = oracle.gemv(type_, W.numpy(), N, K, X)
         assert_within_tolerance(Y, Yr, Ar, str((type_, N, K, M, flags)))
-for N, K, M in [(130, 256*6, 1), (33, 256*9, 5), (64, 256*2, 16)]:
+for N, K, M in [(130, 256*6, 1), (33, 256*9, 5), (64, 256*2, 16), (300, 256*10, 12)]:
     c, s, g = synth.nvfp4_random(N, K, seed=K)
     Xb = synth.activations_bf16(M, K, seed=K)
     Y = pnq.gemv(1004, (c.cuda(), s.cuda(), g), torch.from_numpy(Xb.view(np.int16)).cuda(), N, K).cpu().numpy()
@@ -197,14 +197,14 @@ print(json.dumps({{"ok": True, "device_error": pnq.device_error()}}))
 """
 
 
-@pytest.mark.parametrize("pn_cfg,nv_cfg", [("1,0,0,0", "2,1,0,2"), ("2,0,0,0", "4,2,0,3"), ("1,7,0,2", "2,4,0,4"),
-                                            ("2,13,0,3", "4,8,0,5"), ("1,152,0,8", "4,1,0,8"),
-                                            ("2,3,0,5", "2,16,0,6"), ("1,40,0,4", "4,4,0,0")])
+@pytest.mark.parametrize("pn_cfg,nv_cfg", [("1,0,0,0", "2,0,0,0"), ("2,0,0,0", "1,0,0,0"), ("1,7,0,2", "2,7,0,3"),
+                                            ("2,13,0,3", "1,13,0,3"), ("1,152,0,8", "1,152,0,8"),
+                                            ("2,3,0,5", "2,3,0,5"), ("1,40,0,4", "1,40,0,4")])
 def test_tile_and_grid_configs(pn_cfg, nv_cfg):
     """Forced configurations, read once per process (so each runs in a child): PN path through
-    PNQ_PN_CFG "tiles per warp, grid size, _, stages" (small grids make CTAs span several K
-    units); NVFP4 path through PNQ_GEMV_CFG "consumer warps, cluster size, _, stages"."""
-    env = dict(os.environ, PNQ_PN_CFG=pn_cfg, PNQ_GEMV_CFG=nv_cfg, PNQ_FORCE_KERNEL="mma")
+    PNQ_PN_CFG, NVFP4 path through PNQ_NV_CFG, both "tiles per warp, grid size, _, stages"
+    (small grids make CTAs span several K units and share row tiles)."""
+    env = dict(os.environ, PNQ_PN_CFG=pn_cfg, PNQ_NV_CFG=nv_cfg, PNQ_FORCE_KERNEL="mma")
     r = subprocess.run([sys.executable, "-c", CHILD.format(root=ROOT)], env=env, capture_output=True, text=True,
                        timeout=600)
     assert r.returncode == 0, r.stderr[-3000:]
