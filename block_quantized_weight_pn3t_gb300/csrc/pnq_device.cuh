@@ -24,7 +24,7 @@ template <> struct PnFmt<kTypePn4t> {
 };
 
 // Site codes written to the device error word when a bounded wait gives up.
-enum ErrSite : int { kErrFullWait = 1, kErrEmptyWait = 2, kErrDrainWait = 3, kErrReduceWait = 4 };
+enum ErrSite : int { kErrFullWait = 1, kErrEmptyWait = 2, kErrDrainWait = 3, kErrReduceWait = 4, kErrOperandWait = 5 };
 
 // The device error word lives in pnq_api.cu; kernels receive its address. It holds 0, or the
 // site code of the first bounded wait that gave up.
@@ -300,6 +300,18 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
 // core operand reads, bulk copies).
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// 16-byte asynchronous copy global -> shared through L2 only (data written by the previous grid
+// in the stream is seen once griddepcontrol.wait has returned), with commit groups.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// wait until at most N of this thread's committed groups are still in flight
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 // Named barrier that also ANDs a predicate over the participating threads: every thread gets

@@ -6,7 +6,7 @@
 // x is bf16. The weights are decoded in registers just before the multiply.
 //
 // Work split: the stream-K items of pnq_streamk.cuh, here 128 rows x one K unit of 256 weights
-// (128 code bytes and 16 scale bytes per row).
+// (128 code bytes and 16 scale bytes per row), tile-major.
 //
 // Memory pipeline. A producer thread loads one item per stage with two tensor-map copies: the
 // codes (128 rows x 128 bytes, with the 128-byte swizzle: 16-byte chunk c of row r lands at chunk
@@ -21,8 +21,9 @@
 // of the half; B column m holds the matching x pairs of activation row m, scaled by 2^sigma (per
 // CTA and row, so that max|x| * 2^sigma lies in [2^14, 2^15)). A bf16 value scaled so is exact in
 // fp16 down to 2^-14 (8 significant bits < 11); below that it rounds at 2^-24, 2^-38 of the row's
-// largest |x|. Two accumulator chains (even and odd slices) per tile; g * 2^-sigma is applied to
-// the row sums.
+// largest |x|. The B fragments of a K unit are made by builder warps (sigma per unit and row);
+// two accumulator chains (even and odd slices) per tile; each item's sums are scaled by
+// g * 2^-sigma of its unit.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -48,9 +49,9 @@ template <int NT, int TPW>
 struct NvCfg {
     static constexpr int TG = 8 / TPW;            // tile groups per half
     static constexpr int CW = 2 * TG;             // consumer warps
-    static constexpr int PRODUCER = CW, REDUCER = CW + 1;
-    static constexpr int THREADS = 32 * (CW + 2);
-    static constexpr int NCT = 32 * CW;           // consumer threads
+    static constexpr int NB = (TPW == 1) ? 2 : 6;  // builder warps (within the register budget)
+    static constexpr int PRODUCER = CW, REDUCER = CW + 1, BUILDER = CW + 2;
+    static constexpr int THREADS = 32 * (CW + 2 + NB);
     static constexpr int BFU = NT * 16 * 256;     // fragment bytes per unit: 16 slices x 32 lanes x 8 B per n8 tile
 };
 
@@ -63,29 +64,40 @@ struct NvArgs {
     uint32_t* cnt;
     int* err;
     Sched sc;
-    int N, K, M, NS, x_stage;
-    unsigned flags;
+    int N, K, M, NS, RB, XB;
+    int x_stage;     // resident mode with x in the weight stages: the first stage holding x
+    unsigned flags;  // kStaticWeights, kResident, kXOverlap
     float g;
-    uint32_t bar_off, misc_off, list_off, part_off, b_off, stage_off;
+    uint32_t list_off, part_off, xs_off, ring_off, stage_off, slot_bytes;
     int list_cap;
 };
 
+// Shared-memory regions (offsets from the 1024-aligned base): barriers at 0, lists, row sums,
+// x buffers, operand slots (a ring, or one per unit of the share in resident mode), weight
+// stages. x buffer b (or unit slot b in resident mode) = [M][256] bf16, possibly inside the last
+// weight stages.
 struct NvSmem {
     uint8_t* base;
     uint32_t bar0;
-    int NS;
-    uint32_t misc_off, part_off, b_off, stage_off, list_off;
+    int NS, RB, M;
+    uint32_t list_off, part_off, xs_off, ring_off, stage_off, slot_bytes;
     int list_cap;
     __device__ uint32_t full(int s) const { return bar0 + 8u * s; }
     __device__ uint32_t empty(int s) const { return bar0 + 8u * (NS + s); }
-    __device__ uint32_t x_free() const { return bar0 + 8u * (2 * NS); }
-    __device__ uint32_t part_full(int b) const { return bar0 + 8u * (2 * NS + 1 + b); }
-    __device__ uint32_t part_free(int b) const { return bar0 + 8u * (2 * NS + 3 + b); }
-    __device__ uint32_t* maxbits() const { return reinterpret_cast<uint32_t*>(base + misc_off); }
-    __device__ float* sig_in() const { return reinterpret_cast<float*>(base + misc_off + 64); }
-    __device__ float* sig_out() const { return reinterpret_cast<float*>(base + misc_off + 128); }
+    __device__ uint32_t op_full(int s) const { return bar0 + 8u * (2 * NS + s); }
+    __device__ uint32_t op_empty(int s) const { return bar0 + 8u * (2 * NS + RB + s); }
+    __device__ uint32_t part_full(int b) const { return bar0 + 8u * (2 * NS + 2 * RB + b); }
+    __device__ uint32_t part_free(int b) const { return bar0 + 8u * (2 * NS + 2 * RB + 2 + b); }
+    __device__ uint32_t x_free() const { return bar0 + 8u * (2 * NS + 2 * RB + 4); }
     __device__ float* part() const { return reinterpret_cast<float*>(base + part_off); }
-    __device__ uint8_t* b() const { return base + b_off; }
+    __device__ uint16_t* xs(int buf) const {  // [M][256] bf16 x rows of one K unit
+        return reinterpret_cast<uint16_t*>(base + xs_off) + static_cast<size_t>(buf) * M * kUnitK;
+    }
+    __device__ uint8_t* slot(int s) const { return base + ring_off + static_cast<uint32_t>(s) * slot_bytes; }
+    template <int NT>
+    __device__ float* slot_so(int s) const {  // [M] g * 2^-sigma
+        return reinterpret_cast<float*>(slot(s) + NvCfg<NT, 1>::BFU);
+    }
     __device__ uint8_t* stage(int s) const { return base + stage_off + static_cast<uint32_t>(s) * kStageBytes; }
     __device__ int* n_finish() const { return reinterpret_cast<int*>(base + list_off); }
     __device__ int* pending() const { return reinterpret_cast<int*>(base + list_off) + 4; }
@@ -94,81 +106,48 @@ struct NvSmem {
 
 __device__ __forceinline__ float bf16_to_float(uint16_t h) { return __uint_as_float(static_cast<uint32_t>(h) << 16); }
 
-// sigma per activation row and the B fragments of the CTA's K units (consumer threads only).
-// x slice: units u0, u0 + 1, .. (mod U) of every row, bf16, [m][span * 256] in shared memory.
-template <int NT, int TPW>
-__device__ __forceinline__ void nv_fill(const NvSmem& sm, const uint16_t* X, int K, int U, int u0, int span,
-                                        uint16_t* xs, int M, float g) {
-    using C = NvCfg<NT, TPW>;
-    const int tid = threadIdx.x, lane = tid & 31;
-    const int xlen = span * kUnitK;
-    uint32_t* maxbits = sm.maxbits();
-    float* sig_in = sm.sig_in();
-    float* sig_out = sm.sig_out();
-    for (int m = 0; m < M; ++m) {
-        const uint16_t* xg = X + static_cast<size_t>(m) * K;
-        uint16_t* xd = xs + m * xlen;
-        uint32_t mx = 0;
-        for (int q = tid; q < span * (kUnitK / 8); q += C::NCT) {
-            const int sl = q / (kUnitK / 8);
-            int u = u0 + sl;
-            if (u >= U) u -= U;
-            const int off = 8 * q - sl * kUnitK;
-            const uint4 v = __ldcg(reinterpret_cast<const uint4*>(xg + static_cast<size_t>(u) * kUnitK + off));
-            *reinterpret_cast<uint4*>(xd + sl * kUnitK + off) = v;
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+// Operands of activation row m for one K unit (one builder warp): sigma from the row's largest
+// |x| over the unit, the B fragments (column m) and g * 2^-sigma. xr = the row's 256 bf16 x
+// values in shared memory. Lane (P, c) = (lane / 4, lane % 4) builds the record of slices
+// S = 2P, 2P + 1 (half S / 8, q = (S % 8) / 4, byte b = S % 4): register r holds the x pair at
+// k = 8 * (16 * half + c + 8q + 4r) + 2b; 16-byte record [b0, b1 of 2P; b0, b1 of 2P + 1] in the
+// lane of B column m.
+template <int NT>
+__device__ __forceinline__ void nv_build_row(uint8_t* slot_b, float* slot_so, const uint16_t* xr, int m, float g,
+                                             int lane) {
+    const uint4 xv = reinterpret_cast<const uint4*>(xr)[lane];
+    const uint32_t w[4] = {xv.x, xv.y, xv.z, xv.w};
+    uint32_t mx = 0;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) mx = max(mx, max(w[i] & 0x7FFFu, (w[i] >> 16) & 0x7FFFu));
-        }
-        mx = __reduce_max_sync(0xffffffffu, mx);
-        if (lane == 0) atomicMax(&maxbits[m], mx << 16);  // the fp32 bits of max |x|
-    }
-    fence_proxy_async_smem();  // these bytes are later overwritten by tensor-map copies
-    named_sync(1, C::NCT);
-    if (tid < M) {
-        const uint32_t bits = maxbits[tid];
-        const int E = static_cast<int>(bits >> 23);
-        int sg = (bits == 0 || E >= 255) ? 0 : 141 - E;  // max < 2^(E-126)
-        sg = min(100, max(-100, sg));
-        sig_in[tid] = exp2i(sg);
-        sig_out[tid] = exp2i(-sg) * g;
-    }
-    named_sync(1, C::NCT);
-    // B fragments: one item per (unit, pair of slices P, lane column c), rows m inside. Slice
-    // S = 2P or 2P + 1 (half S / 8, q = (S % 8) / 4, byte b = S % 4); register r of lane column c
-    // holds the x pair at k = 8 * (16 * half + c + 8q + 4r) + 2b, in the lane of B column m, as
-    // 16-byte lane records [b0, b1 of 2P; b0, b1 of 2P + 1].
-    uint8_t* bbase = sm.b();
-    const int items = span * 8 * 4;
-    for (int it = tid; it < items; it += C::NCT) {
-        const int c = it & 3, rest = it >> 2;
-        const int P = rest & 7, slot = rest >> 3;
-        for (int m = 0; m < M; ++m) {
-            const uint16_t* xb = xs + m * xlen + slot * kUnitK;
-            const float si = sig_in[m];
-            uint32_t v[4];
+    for (int i = 0; i < 4; ++i) mx = max(mx, max(w[i] & 0x7FFFu, (w[i] >> 16) & 0x7FFFu));
+    const uint32_t bits = __reduce_max_sync(0xffffffffu, mx) << 16;  // the fp32 bits of max |x|
+    const int E = static_cast<int>(bits >> 23);
+    int sg = (bits == 0 || E >= 255) ? 0 : 141 - E;  // max < 2^(E-126)
+    sg = min(100, max(-100, sg));
+    const float si = exp2i(sg);
+    const int P = lane >> 2, c = lane & 3;
+    const uint32_t* x32 = reinterpret_cast<const uint32_t*>(xr);
+    uint32_t v[4];
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {  // q4 = 2 * (slice - 2P) + register
-                const int S = 2 * P + (q4 >> 1), r = q4 & 1;
-                const int half = S >> 3, q = (S >> 2) & 1, b = S & 3;
-                const int k = 8 * (16 * half + c + 8 * q + 4 * r) + 2 * b;
-                const uint32_t pair = *reinterpret_cast<const uint32_t*>(xb + k);
-                const float v0 = bf16_to_float(static_cast<uint16_t>(pair & 0xFFFFu)) * si;
-                const float v1 = bf16_to_float(static_cast<uint16_t>(pair >> 16)) * si;
-                v[q4] = pack_half2(__float2half_rn(v0), __float2half_rn(v1));
-            }
-            uint8_t* tb = bbase + slot * C::BFU + (m >> 3) * 4096 + P * 512;
-            *reinterpret_cast<uint4*>(tb + ((((m & 7) << 2) | c) * 16)) = make_uint4(v[0], v[1], v[2], v[3]);
-        }
+    for (int q4 = 0; q4 < 4; ++q4) {  // q4 = 2 * (slice - 2P) + register
+        const int S = 2 * P + (q4 >> 1), r = q4 & 1;
+        const int half = S >> 3, q = (S >> 2) & 1, b = S & 3;
+        const uint32_t pair = x32[4 * (16 * half + c + 8 * q + 4 * r) + b];
+        const float v0 = bf16_to_float(static_cast<uint16_t>(pair & 0xFFFFu)) * si;
+        const float v1 = bf16_to_float(static_cast<uint16_t>(pair >> 16)) * si;
+        v[q4] = pack_half2(__float2half_rn(v0), __float2half_rn(v1));
     }
-    named_sync(1, C::NCT);
+    uint8_t* tb = slot_b + (m >> 3) * 4096 + P * 512;
+    *reinterpret_cast<uint4*>(tb + ((((m & 7) << 2) | c) * 16)) = make_uint4(v[0], v[1], v[2], v[3]);
+    if (lane == 0) slot_so[m] = exp2i(-sg) * g;
 }
 
-// One half-unit H of an item for the warp's TPW tiles: decode, multiply, add the row sums.
+// One half-unit H of an item for the warp's TPW tiles: decode, multiply, add the row sums times
+// the unit's factors f (g * 2^-sigma of the lane's two columns).
 template <int NT, int TPW, int H>
 __device__ __forceinline__ void nv_half(const uint8_t* stage, const uint8_t* bf, const int (&r0)[TPW], int g, int tig,
                                         int lane, const bool (&live)[NT], uint32_t sel0, uint32_t sel1,
-                                        float (&acc)[TPW][NT][4]) {
+                                        const float (&f)[NT][2], float (&acc)[TPW][NT][4]) {
     // B fragments of the half's 8 slices (4 records of 16 bytes per tile)
     uint32_t b[NT][kSlices][2];
 #pragma unroll
@@ -228,15 +207,17 @@ __device__ __forceinline__ void nv_half(const uint8_t* stage, const uint8_t* bf,
 #pragma unroll
         for (int t = 0; t < NT; ++t)
 #pragma unroll
-            for (int i = 0; i < 4; ++i) acc[tp][t][i] += c2[0][t][i] + c2[1][t][i];
+            for (int i = 0; i < 4; ++i) acc[tp][t][i] = fmaf(c2[0][t][i] + c2[1][t][i], f[t][i & 1], acc[tp][t][i]);
     }
 }
 
 template <int NT, int TPW, int H>
-__device__ __forceinline__ void nv_consumer_loop(const NvSmem& sm, const Ctx& cx, int i0, int n_items, int u0) {
+__device__ __forceinline__ void nv_consumer_loop(const NvSmem& sm, const Ctx& cx, int i0, int n_items) {
     using C = NvCfg<NT, TPW>;
     const Sched& sc = cx.sc;
-    const int M = cx.M, NS = cx.NS, U = sc.U;
+    const int M = cx.M, NS = cx.NS, RB = cx.RB, U = sc.U;
+    const bool resident = (cx.flags & kResident) != 0;
+    const int u0 = sc.unit_of(i0);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, tig = lane & 3;
     const int tg = warp % C::TG;
@@ -247,7 +228,6 @@ __device__ __forceinline__ void nv_consumer_loop(const NvSmem& sm, const Ctx& cx
     int r0[TPW];
 #pragma unroll
     for (int tp = 0; tp < TPW; ++tp) r0[tp] = 16 * (TPW * tg + tp) + g;
-    const float* sig_out = sm.sig_out();
     float* part = sm.part();
     bool ok = true;
     float acc[TPW][NT][4];  // [rows g | g + 8][columns 2c | 2c + 1]: c0, c1 row g, c2, c3 row g + 8
@@ -273,8 +253,8 @@ __device__ __forceinline__ void nv_consumer_loop(const NvSmem& sm, const Ctx& cx
                     const int m = 8 * t + 2 * tig + i;
                     if (m < M) {
                         float* dst = part + ((H * 2 + buf) * M + m) * kPartPitch + r0[tp];
-                        dst[0] = acc[tp][t][i] * sig_out[m];
-                        dst[8] = acc[tp][t][2 + i] * sig_out[m];
+                        dst[0] = acc[tp][t][i];
+                        dst[8] = acc[tp][t][2 + i];
                     }
                     acc[tp][t][i] = acc[tp][t][2 + i] = 0.0f;
                 }
@@ -283,20 +263,36 @@ __device__ __forceinline__ void nv_consumer_loop(const NvSmem& sm, const Ctx& cx
         ++e;
     };
     int t_i = sc.tile_of(i0), u_i = sc.unit_of(i0);
-    int cur_t = t_i;
+    int cur_t = t_i, r = -1, u_run = -1;
     for (int gi = 0; gi < n_items && ok; ++gi, next_item(sc, t_i, u_i)) {
         if (t_i != cur_t) {
             emit();
             if (!ok) break;
             cur_t = t_i;
         }
-        const int slot = (u_i >= u0) ? u_i - u0 : u_i - u0 + U;
+        if (!resident && u_i != u_run) {  // a new run: its operands
+            if (!consumer_next_run(sm, RB, lane, r)) {
+                ok = false;
+                break;
+            }
+            u_run = u_i;
+        }
         const int s = gi % NS;
         if (!mbar_wait_warp(sm.full(s), (gi / NS) & 1)) {
             ok = false;
             break;
         }
-        nv_half<NT, TPW, H>(sm.stage(s), sm.b() + slot * C::BFU, r0, g, tig, lane, live, sel0, sel1, acc);
+        const int os = resident ? ((u_i >= u0) ? u_i - u0 : u_i - u0 + U) : r % RB;
+        const float* so = sm.slot_so<NT>(os);
+        float f[NT][2];  // g * 2^-sigma of the unit for the lane's columns 2c, 2c + 1
+#pragma unroll
+        for (int t = 0; t < NT; ++t)
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const int m = 8 * t + 2 * tig + i;
+                f[t][i] = (m < M) ? so[m] : 0.0f;
+            }
+        nv_half<NT, TPW, H>(sm.stage(s), sm.slot(os), r0, g, tig, lane, live, sel0, sel1, f, acc);
         __syncwarp();
         if (lane == 0) mbar_arrive(sm.empty(s));
     }
@@ -309,32 +305,33 @@ __global__ void __launch_bounds__(NvCfg<NT, TPW>::THREADS, 1) nvfp4_gemv_kernel(
     using C = NvCfg<NT, TPW>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* base = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
-    const NvSmem sm{base,       smem_addr(base + a.bar_off), a.NS,       a.misc_off, a.part_off,
-                    a.b_off,    a.stage_off,                 a.list_off, a.list_cap};
-    const Ctx cx{a.sc, a.X, a.Y, a.ws, a.cnt, a.err, a.N, a.K, a.M, a.NS, a.x_stage, 0, a.flags};
+    const NvSmem sm{base,       smem_addr(base), a.NS,       a.RB,         a.M,          a.list_off, a.part_off,
+                    a.xs_off,   a.ring_off,      a.stage_off, a.slot_bytes, a.list_cap};
+    const Ctx cx{a.sc, a.X, a.Y, a.ws, a.cnt, a.err, a.N, a.K, a.M, a.NS, a.RB, a.flags};
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     const Sched& sc = cx.sc;
     const int i0 = sc.first(blockIdx.x), i1 = sc.first(blockIdx.x + 1);
     const int n_items = i1 - i0;
-    const int u0 = n_items > 0 ? sc.unit_of(i0) : 0;
-    const int span = sc.span(i0, i1);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < a.NS; ++s) {
             mbar_init(sm.full(s), 1);
             mbar_init(sm.empty(s), C::CW);
         }
-        mbar_init(sm.x_free(), 1);
+        for (int s = 0; s < a.RB; ++s) {
+            mbar_init(sm.op_full(s), C::NB);
+            mbar_init(sm.op_empty(s), C::CW);
+        }
         for (int b = 0; b < 2; ++b) {
             mbar_init(sm.part_full(b), C::CW);
             mbar_init(sm.part_free(b), 1);
         }
+        mbar_init(sm.x_free(), 1);
         mbar_fence_init();
         griddep_launch_dependents();
+        *sm.n_finish() = 0;
     }
-    if (threadIdx.x < 16) sm.maxbits()[threadIdx.x] = 0u;
-    if (threadIdx.x == 0) *sm.n_finish() = 0;
     __syncthreads();
 
     if (warp == C::PRODUCER) {
@@ -343,11 +340,12 @@ __global__ void __launch_bounds__(NvCfg<NT, TPW>::THREADS, 1) nvfp4_gemv_kernel(
             const uint64_t pol = l2_policy_evict_first();
             bool ok = true;
             int t_n = sc.tile_of(i0), u_n = sc.unit_of(i0);
+            const int x_stage = (cx.flags & kXOverlap) ? a.x_stage : cx.NS;  // stages holding x at first
             auto issue = [&](int gi) {
                 const int s = gi % cx.NS;
                 if (gi >= cx.NS) {
                     if (!mbar_wait_bounded(sm.empty(s), ((gi / cx.NS) - 1) & 1)) return false;
-                } else if (s >= cx.x_stage) {
+                } else if (s >= x_stage) {
                     if (!mbar_wait_bounded(sm.x_free(), 0)) return false;
                 }
                 mbar_arrive_expect_tx(sm.full(s), static_cast<uint32_t>(kStageBytes));
@@ -359,9 +357,9 @@ __global__ void __launch_bounds__(NvCfg<NT, TPW>::THREADS, 1) nvfp4_gemv_kernel(
             };
             int gi = 0;
             if (cx.flags & kStaticWeights) {
-                // the weights are not written by earlier work in the stream: start streaming
-                // them into the stages that will not hold x before the previous grid completes
-                for (; ok && gi < min(n_items, cx.x_stage); ++gi) ok = issue(gi);
+                // the weights are not written by earlier work in the stream: fill the stages
+                // (those not holding x) before the previous grid completes
+                for (; ok && gi < min(n_items, x_stage); ++gi) ok = issue(gi);
             }
             griddep_wait();  // without the static-weights flag W may be written by the previous grid
             for (; ok && gi < n_items; ++gi) ok = issue(gi);
@@ -402,62 +400,160 @@ __global__ void __launch_bounds__(NvCfg<NT, TPW>::THREADS, 1) nvfp4_gemv_kernel(
             if (np > 0) count_shares(cx, sm, np, lane);
             if (!ok && lane == 0) record_error(cx.err, kErrReduceWait);
         }
+    } else if (a.flags & kResident) {
+        // ---------------- resident operands: consumers and builders build all units' ----------------
+        // (unit slot k = unit u0 + k mod U; jobs = (slot, row))
+        if (n_items > 0) {
+            const int u0 = sc.unit_of(i0);
+            const int span = sc.span(i0, i1);
+            const int pw = (warp < C::CW) ? warp : warp - C::BUILDER + C::CW;
+            const int M = cx.M;
+            auto copy = [&](int c) {
+                const int row = c >> 5, q = c & 31;  // row = k * M + m, 32 chunks of 16 bytes
+                const int k = row / M, m = row - k * M;
+                int u = u0 + k;
+                if (u >= sc.U) u -= sc.U;
+                cp_async16(smem_addr(sm.xs(k) + m * kUnitK) + 16u * q,
+                           a.X + static_cast<size_t>(m) * cx.K + static_cast<size_t>(u) * kUnitK + 8 * q);
+            };
+            auto job = [&](int i) {
+                const int k = i / M, m = i - k * M;
+                nv_build_row<NT>(sm.slot(k), sm.slot_so<NT>(k), sm.xs(k) + m * kUnitK, m, a.g, lane);
+            };
+            resident_prologue(pw, C::CW + C::NB, lane, span * M * 32, span * M, copy, job);
+            if (threadIdx.x == 0 && (a.flags & kXOverlap)) mbar_arrive(sm.x_free());
+            if (warp < C::TG)
+                nv_consumer_loop<NT, TPW, 0>(sm, cx, i0, n_items);
+            else if (warp < C::CW)
+                nv_consumer_loop<NT, TPW, 1>(sm, cx, i0, n_items);
+        }
+    } else if (warp >= C::BUILDER) {
+        // ---------------- builders: operands of each run; rows m = b, b + NB, .. ----------------
+        if (n_items > 0) {
+            griddep_wait();  // X belongs to the previous grid until now
+            const int b = warp - C::BUILDER;
+            auto issue = [&](int u, int buf) {
+                uint16_t* xb = sm.xs(buf);
+                for (int m = b; m < cx.M; m += C::NB)
+                    cp_async16(smem_addr(xb + m * kUnitK) + 16u * lane,
+                               a.X + static_cast<size_t>(m) * cx.K + static_cast<size_t>(u) * kUnitK + 8 * lane);
+            };
+            auto build = [&](int slot, int buf) {
+                const uint16_t* xb = sm.xs(buf);
+                for (int m = b; m < cx.M; m += C::NB)
+                    nv_build_row<NT>(sm.slot(slot), sm.slot_so<NT>(slot), xb + m * kUnitK, m, a.g, lane);
+            };
+            bool ok;
+            if (a.XB == 4)
+                ok = builder_loop<4>(sm, sc, i0, n_items, cx.RB, lane, issue, build);
+            else if (a.XB == 2)
+                ok = builder_loop<2>(sm, sc, i0, n_items, cx.RB, lane, issue, build);
+            else
+                ok = builder_loop<1>(sm, sc, i0, n_items, cx.RB, lane, issue, build);
+            if (!ok && lane == 0) record_error(cx.err, kErrOperandWait);
+        }
     } else {
         // ---------------- consumer warps ----------------
         if (n_items > 0) {
-            griddep_wait();  // X belongs to the previous grid until now
-            uint16_t* xs = reinterpret_cast<uint16_t*>(sm.stage(cx.x_stage));
-            nv_fill<NT, TPW>(sm, a.X, cx.K, sc.U, u0, span, xs, cx.M, a.g);
-            if (threadIdx.x == 0) mbar_arrive(sm.x_free());  // the x stages may now take weights
             if (warp < C::TG)
-                nv_consumer_loop<NT, TPW, 0>(sm, cx, i0, n_items, u0);
+                nv_consumer_loop<NT, TPW, 0>(sm, cx, i0, n_items);
             else
-                nv_consumer_loop<NT, TPW, 1>(sm, cx, i0, n_items, u0);
+                nv_consumer_loop<NT, TPW, 1>(sm, cx, i0, n_items);
         }
     }
     // the tiles this CTA completed: every warp sums some of them
     __syncthreads();
-    const int nf = *sm.n_finish();
-    for (int k = warp; k < nf; k += C::THREADS / 32) finish_tile(cx, sm.finish()[k], lane);
+    finish_tiles(cx, sm, warp, C::THREADS / 32, lane);
 }
 
 // ---- host side --------------------------------------------------------------------------------------
 
+constexpr int kDefaultStages = 6;
+
 struct NvPlan {
     Sched sc{};
     bool publish = false;
-    int NS = 0, x_stage = 0, span_max = 0, list_cap = 0;
-    uint32_t bar_off = 0, misc_off = 0, list_off = 0, part_off = 0, b_off = 0, stage_off = 0, total = 0;
+    unsigned mode = 0;  // kResident, kXOverlap
+    int NS = 0, RB = 0, XB = 0, x_stage = 0, list_cap = 0;
+    uint32_t list_off = 0, part_off = 0, xs_off = 0, ring_off = 0, stage_off = 0, slot_bytes = 0, total = 0;
 };
 
-bool nv_layout(int bfu, int M, int ns_req, NvPlan& p) {
-    p.span_max = 0;
-    for (int c = 0; c < p.sc.G; ++c) p.span_max = std::max(p.span_max, p.sc.span(p.sc.first(c), p.sc.first(c + 1)));
-    p.bar_off = 0;
-    p.misc_off = 8u * (2 * kMaxStages + 6);
+// Barriers, lists and row sums at the start; returns the first free (128-aligned) offset.
+uint32_t nv_head_layout(int bfu, int M, NvPlan& p) {
     p.list_cap = (p.sc.items + p.sc.G - 1) / p.sc.G;
-    p.list_off = align_up(p.misc_off + 192u, 16);
+    p.list_off = align_up(8u * kBarriers, 16);
     p.part_off = align_up(p.list_off + (2u * p.list_cap + 4u) * 4u, 16);
-    p.b_off = align_up(p.part_off + 4u * M * kPartPitch * 4u, 128);
-    p.stage_off = align_up(p.b_off + static_cast<uint32_t>(p.span_max) * static_cast<uint32_t>(bfu), 1024);
-    const uint64_t xbytes = static_cast<uint64_t>(M) * p.span_max * kUnitK * 2u;
-    const int x_stages = static_cast<int>((xbytes + kStageBytes - 1) / kStageBytes);
-    for (int ns = kMaxStages; ns >= 2; --ns) {
-        if (ns_req > 0 && ns != ns_req) continue;
-        const uint64_t total = p.stage_off + static_cast<uint64_t>(ns) * kStageBytes;
-        if (total + 1024u <= kSmemLimit && ns >= x_stages && (ns_req > 0 || ns >= 3)) {
-            p.NS = ns;
-            p.x_stage = ns - x_stages;
-            p.total = static_cast<uint32_t>(total);
-            return true;
-        }
+    p.slot_bytes = align_up(static_cast<uint32_t>(bfu) + 64u, 128);
+    return align_up(p.part_off + 4u * M * kPartPitch * 4u, 128);
+}
+
+bool nv_layout(int bfu, int M, int NS, int RB, int XB, NvPlan& p) {
+    p.xs_off = nv_head_layout(bfu, M, p);
+    p.ring_off = align_up(p.xs_off + static_cast<uint32_t>(XB) * M * kUnitK * 2u, 128);
+    p.stage_off = align_up(p.ring_off + static_cast<uint32_t>(RB) * p.slot_bytes, 1024);
+    const uint64_t total = p.stage_off + static_cast<uint64_t>(NS) * kStageBytes;
+    if (total + 1024u > kSmemLimit) return false;
+    p.mode = 0;
+    p.NS = NS;
+    p.RB = RB;
+    p.XB = XB;
+    p.total = static_cast<uint32_t>(total);
+    return true;
+}
+
+// Resident layout: one operand slot per unit of the largest share, x of the share in its own
+// region or (overlap) in the last weight stages until the operands are built.
+bool nv_layout_resident(int bfu, int M, int NS, bool overlap, NvPlan& p) {
+    int span = 0;
+    for (int c = 0; c < p.sc.G; ++c) span = std::max(span, p.sc.span(p.sc.first(c), p.sc.first(c + 1)));
+    uint64_t off = nv_head_layout(bfu, M, p);
+    const uint64_t xbytes = static_cast<uint64_t>(span) * M * kUnitK * 2u;
+    if (!overlap) {
+        p.xs_off = static_cast<uint32_t>(off);
+        off = (off + xbytes + 127) / 128 * 128;
     }
+    p.ring_off = static_cast<uint32_t>(off);
+    const uint64_t stage_off = (off + static_cast<uint64_t>(span) * p.slot_bytes + 1023) / 1024 * 1024;
+    const uint64_t total = stage_off + static_cast<uint64_t>(NS) * kStageBytes;
+    if (total + 1024u > kSmemLimit) return false;
+    p.stage_off = static_cast<uint32_t>(stage_off);
+    p.x_stage = NS;
+    if (overlap) {
+        const int x_stages = static_cast<int>((xbytes + kStageBytes - 1) / kStageBytes);
+        if (x_stages > NS) return false;
+        p.x_stage = NS - x_stages;
+        p.xs_off = p.stage_off + static_cast<uint32_t>(p.x_stage) * kStageBytes;
+    }
+    p.mode = kResident | (overlap ? kXOverlap : 0u);
+    p.NS = NS;
+    p.RB = 0;
+    p.XB = 0;
+    p.total = static_cast<uint32_t>(total);
+    return true;
+}
+
+// As the PN path: resident operands when they fit with at least 3 weight stages, else the
+// streaming ring (deepest weight ring, then x prefetch and operand ring).
+bool nv_fit(int bfu, int M, int ns_req, int rb_req, NvPlan& p) {
+    const int ns_max = ns_req > 0 ? ns_req : kDefaultStages;
+    const int ns_lo = ns_req > 0 ? ns_req : 3;
+    if (rb_req <= 0)
+        for (bool overlap : {false, true})
+            for (int ns = ns_max; ns >= ns_lo; --ns)
+                if (nv_layout_resident(bfu, M, ns, overlap, p)) return true;
+    for (int ns_min : {3, 2})
+        for (int xb : {4, 2, 1})
+            for (int rb : {3, 2}) {
+                if (rb_req > 0 && rb != 3) continue;
+                const int r = rb_req > 0 ? std::min(std::max(rb_req, 2), 4) : rb;  // one slot would deadlock
+                for (int ns = ns_max; ns >= (ns_req > 0 ? ns_req : ns_min); --ns)
+                    if (nv_layout(bfu, M, ns, r, xb, p)) return true;
+            }
     return false;
 }
 
-// Same choice as the PN path: one CTA per SM (stream-K) or one per row tile; tile-major when
-// the operands of a share fit.
-bool nv_plan(int bfu, int M, int64_t T, int64_t U, int sms, bool grid_forced, int ns_req, NvPlan& p) {
+// Same choice as the PN path: one CTA per SM (stream-K) or one per row tile.
+bool nv_plan(int bfu, int M, int64_t T, int64_t U, int sms, bool grid_forced, int ns_req, int rb_req, NvPlan& p) {
     const int64_t items = T * U;
     int64_t cands[2] = {std::min<int64_t>(sms, items), 0};
     if (!grid_forced && T < sms) cands[1] = T;
@@ -465,32 +561,28 @@ bool nv_plan(int bfu, int M, int64_t T, int64_t U, int sms, bool grid_forced, in
     double best = 0.0;
     for (int64_t G : cands) {
         if (G <= 0) continue;
-        for (int tm = 1; tm >= 0; --tm) {
-            NvPlan q;
-            q.sc.items = static_cast<int>(items);
-            q.sc.T = static_cast<int>(T);
-            q.sc.U = static_cast<int>(U);
-            q.sc.G = static_cast<int>(G);
-            q.sc.tile_major = tm;
-            if (!nv_layout(bfu, M, ns_req, q)) continue;
-            bool publish = false;
-            for (int c = 1; c < G && !publish; ++c) publish = q.sc.tile_of(q.sc.first(c)) == q.sc.tile_of(q.sc.first(c) - 1);
-            if (!tm && U > 1) publish = true;
-            // items here are half the bytes of a PN item: the reduction tail weighs more
-            const double cost = static_cast<double>((items + G - 1) / G) + (publish ? 5.0 : 0.0);
-            if (!found || cost < best) {
-                best = cost;
-                q.publish = publish;
-                p = q;
-                found = true;
-            }
-            break;
+        NvPlan q;
+        q.sc.items = static_cast<int>(items);
+        q.sc.T = static_cast<int>(T);
+        q.sc.U = static_cast<int>(U);
+        q.sc.G = static_cast<int>(G);
+        q.sc.tile_major = 1;
+        if (!nv_fit(bfu, M, ns_req, rb_req, q)) continue;
+        bool publish = false;
+        for (int c = 1; c < G && !publish; ++c) publish = q.sc.tile_of(q.sc.first(c)) == q.sc.tile_of(q.sc.first(c) - 1);
+        // items here are half the bytes of a PN item: the reduction tail weighs more
+        const double cost = static_cast<double>((items + G - 1) / G) + (publish ? 5.0 : 0.0);
+        if (!found || cost < best) {
+            best = cost;
+            q.publish = publish;
+            p = q;
+            found = true;
         }
     }
     return found;
 }
 
-// Environment override PNQ_NV_CFG="tpw,grid,_,ns" (fields 0 = automatic), read once.
+// Environment override PNQ_NV_CFG="tpw,grid,rb,ns" (fields 0 = automatic), read once.
 MmaConfig nv_env_config() {
     static MmaConfig cfg = [] {
         MmaConfig c{0, 0, 0, 0};
@@ -514,8 +606,8 @@ cudaError_t nv_launch_cfg(NvArgs& a, const MmaConfig& cfg, bool static_weights, 
                           const ExtWorkspace& ext) {
     using C = NvCfg<NT, TPW>;
     NvPlan p;
-    const int cap = cfg.S > 0 ? std::min(cfg.S, device_sm_count()) : device_sm_count();
-    if (!nv_plan(C::BFU, a.M, a.sc.T, a.sc.U, cap, cfg.S > 0, cfg.ns, p)) return cudaErrorNotSupported;
+    const int cap = cfg.grid > 0 ? std::min(cfg.grid, device_sm_count()) : device_sm_count();
+    if (!nv_plan(C::BFU, a.M, a.sc.T, a.sc.U, cap, cfg.grid > 0, cfg.ns, cfg.rb, p)) return cudaErrorNotSupported;
     auto kern = nvfp4_gemv_kernel<NT, TPW>;
     static bool opted[64] = {};
     int dev = 0;
@@ -539,15 +631,17 @@ cudaError_t nv_launch_cfg(NvArgs& a, const MmaConfig& cfg, bool static_weights, 
     }
     a.sc = p.sc;
     a.NS = p.NS;
+    a.RB = p.RB;
+    a.XB = p.XB;
+    a.flags = (static_weights ? kStaticWeights : 0u) | p.mode;
     a.x_stage = p.x_stage;
-    a.flags = static_weights ? kStaticWeights : 0u;
-    a.bar_off = p.bar_off;
-    a.misc_off = p.misc_off;
     a.list_off = p.list_off;
-    a.part_off = p.part_off;
-    a.b_off = p.b_off;
-    a.stage_off = p.stage_off;
     a.list_cap = p.list_cap;
+    a.part_off = p.part_off;
+    a.xs_off = p.xs_off;
+    a.ring_off = p.ring_off;
+    a.stage_off = p.stage_off;
+    a.slot_bytes = p.slot_bytes;
     cudaLaunchConfig_t lc{};
     lc.gridDim = dim3(p.sc.G, 1, 1);
     lc.blockDim = dim3(C::THREADS, 1, 1);
@@ -588,11 +682,12 @@ cudaError_t launch_nvfp4_gemv_mma(const Nvfp4View& w, int64_t N, int64_t K, cons
     a.sc.U = static_cast<int>(U);
     a.sc.items = static_cast<int>(T * U);
     const MmaConfig env = nv_env_config();
-    if (cfg.rw <= 0) cfg.rw = env.rw;
-    if (cfg.S <= 0) cfg.S = env.S;
+    if (cfg.tpw <= 0) cfg.tpw = env.tpw;
+    if (cfg.grid <= 0) cfg.grid = env.grid;
+    if (cfg.rb <= 0) cfg.rb = env.rb;
     if (cfg.ns <= 0) cfg.ns = env.ns;
     const int nt = (M + 7) / 8;
-    const int tpw = cfg.rw > 0 ? cfg.rw : 1;
+    const int tpw = cfg.tpw > 0 ? cfg.tpw : (nt == 1 ? 1 : 2);
     if (nt == 1) return tpw == 1 ? nv_launch_cfg<1, 1>(a, cfg, static_weights, stream, ext)
                                  : nv_launch_cfg<1, 2>(a, cfg, static_weights, stream, ext);
     return tpw == 1 ? nv_launch_cfg<2, 1>(a, cfg, static_weights, stream, ext)

@@ -10,16 +10,15 @@
 // 100 cycles whatever N <= 128 is (2048 weights each) -- both measured on this part -- so for
 // the narrow N of a GEMV the warp-level MMA has the throughput and tcgen05 does not.
 //
-// Items and schedule (stream-K). The weight matrix is cut into items of 128 rows x one K unit
-// of 8 blocks (272 bytes per row). Items are numbered unit-major (item = u * T + t for row tile
-// t of T) and every CTA of a persistent grid (one per SM) takes an equal contiguous share, so
-// all SMs stream the same number of bytes and a CTA's items touch at most a few K units.
+// Items and schedule (stream-K, pnq_streamk.cuh). The weight matrix is cut into items of 128
+// rows x one K unit of 8 blocks (272 bytes per row), numbered tile-major; every CTA of a
+// persistent grid (one per SM) takes an equal contiguous share, so all SMs stream the same
+// number of bytes.
 //
 // Memory pipeline. One producer thread loads one item per stage with a 2-D tensor-map copy
 // (box 272 bytes x 128 rows, L2 evict-first; rows past N read as zeros) into an NS-stage ring
-// under mbarriers; at start it also copies the CTA's slice of x (fp32) into the last stages.
-// With the static-weights flag the first stages are requested before the previous grid in the
-// stream has finished.
+// under mbarriers. With the static-weights flag the first stages are requested before the
+// previous grid in the stream has finished.
 //
 // Decode and multiply (consumer warps). Warp = TPW tiles of 16 rows x half a unit (4 blocks).
 // A 32-bit word of a block holds two codes at the same shift in its two 16-bit halves; masking
@@ -29,18 +28,16 @@
 // free as long as B uses the same order, so the 2-byte aligned words of even blocks are read as
 // aligned words pairing the high half of word i-1 with the low half of word i (one PRMT).
 //
-// B operand: x times 8^-j (16^-j) times 2^sigma (per CTA and activation row, so that max|x| *
-// 2^sigma lies in [2^14, 2^15)), split into fp16 hi + lo parts (~22 bits) that take mma
-// columns 2m and 2m + 1 (NT = ceil(2M / 8) n8 tiles). The fragments of the CTA's blocks are
-// built once in shared memory in register order.
+// B operand (builder warps): x times 8^-j (16^-j) times 2^sigma (per K unit and activation row,
+// so that max|x| * 2^sigma lies in [2^14, 2^15)), split into fp16 hi + lo parts (~22 bits) that
+// take mma columns 2m and 2m + 1 (NT = ceil(2M / 8) n8 tiles), stored per block in register
+// order. Beside them: Z = z * 2^(sigma - 24) * (sum of the block's x), and 2^(24 - sigma).
 //
-// Block scale and zero point: acc += d * (c - Z) per block, Z = z * (sum over the block of B
-// times 2^-24 * 8^j), precomputed beside B in fp32.
+// Block scale and zero point: per item a_m = sum over its blocks of d * (c - Z); the tile's row
+// sum gains a_m * 2^(24 - sigma).
 //
-// Reduction. At the end of an item the consumer warps leave their row sums (two halves) in
-// shared memory; a reducer warp adds them, writes the item's rows to a workspace slot and
-// counts the item on its row tile; the CTA that brings a tile's count to U sums the tile's U
-// slots in unit order (so the result does not depend on timing) and writes Y.
+// Reduction (pnq_streamk.cuh): whole tiles go from the reducer warp to Y, shares of a tile
+// that several CTAs cover meet in the workspace and are summed in unit order.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -64,11 +61,12 @@ constexpr int kHalfBlocks = 4;                         // blocks per consumer wa
 template <int TYPE, int NT, int TPW>
 struct Cfg {
     static constexpr int STEPS = PnFmt<TYPE>::PAIRS;
+    static constexpr int UK = kUnitBlocks * PnFmt<TYPE>::BLK;  // weights of a row per unit
     static constexpr int TG = 8 / TPW;             // tile groups per half
     static constexpr int CW = 2 * TG;              // consumer warps
-    static constexpr int PRODUCER = CW, REDUCER = CW + 1;
-    static constexpr int THREADS = 32 * (CW + 2);
-    static constexpr int NCT = 32 * CW;            // consumer threads
+    static constexpr int NB = (TPW == 1 || NT >= 4) ? 2 : 6;  // builder warps (within the register budget)
+    static constexpr int PRODUCER = CW, REDUCER = CW + 1, BUILDER = CW + 2;
+    static constexpr int THREADS = 32 * (CW + 2 + NB);
     static constexpr int BFU = NT * 256 * STEPS;   // fragment bytes per block
 };
 
@@ -80,9 +78,10 @@ struct PnArgs {
     uint32_t* cnt;   // [T] shares counted per row tile (zero between launches)
     int* err;
     Sched sc;
-    int N, K, M, NS, x_stage, xpitch;
-    unsigned flags;
-    uint32_t bar_off, misc_off, z_off, part_off, b_off, stage_off, list_off;
+    int N, K, M, NS, RB, XB;
+    int x_stage;     // resident mode with x in the weight stages: the first stage holding x
+    unsigned flags;  // kStaticWeights, kResident, kXOverlap
+    uint32_t list_off, part_off, xs_off, ring_off, stage_off, slot_bytes;
     int list_cap;
 };
 
@@ -124,39 +123,37 @@ __device__ __forceinline__ float ld_half(const uint8_t* p) {
     return __half2float(*reinterpret_cast<const __half*>(p));
 }
 
-// Shared-memory regions (offsets from the 1024-aligned base).
+// Shared-memory regions (offsets from the 1024-aligned base): barriers at 0, lists, row sums,
+// x buffers, operand slots (a ring, or one per unit of the share in resident mode), weight
+// stages. Resident mode keeps x as [unit slot][M][UK] (possibly inside the last weight stages).
 struct Smem {
     uint8_t* base;
     uint32_t bar0;  // shared address of barrier 0
-    int NS;
-    uint32_t misc_off, z_off, part_off, b_off, stage_off, list_off;
+    int NS, RB, M, UK;
+    uint32_t list_off, part_off, xs_off, ring_off, stage_off, slot_bytes, z_off;
+    int list_cap;
     __device__ uint32_t full(int s) const { return bar0 + 8u * s; }
     __device__ uint32_t empty(int s) const { return bar0 + 8u * (NS + s); }
-    __device__ uint32_t x_free() const { return bar0 + 8u * (2 * NS + 1); }
-    __device__ uint32_t part_full(int b) const { return bar0 + 8u * (2 * NS + 2 + b); }
-    __device__ uint32_t part_free(int b) const { return bar0 + 8u * (2 * NS + 4 + b); }
-    __device__ uint32_t* maxbits() const { return reinterpret_cast<uint32_t*>(base + misc_off); }
-    __device__ float* sig_in() const { return reinterpret_cast<float*>(base + misc_off + 64); }
-    __device__ float* sig_out() const { return reinterpret_cast<float*>(base + misc_off + 128); }
-    __device__ float* z() const { return reinterpret_cast<float*>(base + z_off); }
+    __device__ uint32_t op_full(int s) const { return bar0 + 8u * (2 * NS + s); }
+    __device__ uint32_t op_empty(int s) const { return bar0 + 8u * (2 * NS + RB + s); }
+    __device__ uint32_t part_full(int b) const { return bar0 + 8u * (2 * NS + 2 * RB + b); }
+    __device__ uint32_t part_free(int b) const { return bar0 + 8u * (2 * NS + 2 * RB + 2 + b); }
+    __device__ uint32_t x_free() const { return bar0 + 8u * (2 * NS + 2 * RB + 4); }
     __device__ float* part() const { return reinterpret_cast<float*>(base + part_off); }
-    __device__ uint8_t* b() const { return base + b_off; }
+    int J;  // builder jobs per run (x rows per buffer)
+    __device__ float* xs(int buf) const {  // [J][UK] x rows of one K unit, one per builder job
+        return reinterpret_cast<float*>(base + xs_off) + static_cast<size_t>(buf) * J * UK;
+    }
+    __device__ uint8_t* slot(int s) const { return base + ring_off + static_cast<uint32_t>(s) * slot_bytes; }
+    __device__ float* slot_z(int s) const { return reinterpret_cast<float*>(slot(s) + z_off); }  // [8][M]
+    __device__ float* slot_so(int s) const { return slot_z(s) + kUnitBlocks * M; }                // [M]
     __device__ uint8_t* stage(int s) const { return base + stage_off + static_cast<uint32_t>(s) * kStageBytes; }
     // tiles whose partial shares wait to be counted, tiles this CTA completes (list_cap entries
     // each, list_cap >= the items of any CTA), and the number of the latter
-    int list_cap;
     __device__ int* n_finish() const { return reinterpret_cast<int*>(base + list_off); }
     __device__ int* pending() const { return reinterpret_cast<int*>(base + list_off) + 4; }
     __device__ int* finish() const { return reinterpret_cast<int*>(base + list_off) + 4 + list_cap; }
 };
-
-// A register (two halves) holding code 1 at slice j's position: the fp16 subnormal
-// 2^-24 * 8^j (pn3t) or 2^-24 * 16^j (pn4t) in both halves.
-template <int TYPE>
-__device__ __forceinline__ uint32_t code_one(int j) {
-    const int jj = (TYPE == kTypePn3t) ? (j < 3 ? j : j - 3) : (j & 1);
-    return 0x00010001u << (PnFmt<TYPE>::BITS * jj);
-}
 
 // B fragments of one block for every n8 tile: lanes whose column is in use load their records,
 // the others hold zeros.
@@ -185,83 +182,61 @@ __device__ __forceinline__ void load_bfrag(const uint8_t* bf, int lane, const bo
     }
 }
 
-// sigma per activation row, the B fragments and the per-block zero-point sums for the CTA's
-// nblk blocks (consumer threads only).
-template <int TYPE, int NT, int TPW>
-__device__ __forceinline__ void fill_operands(const Smem& sm, const float* X, int K, int U, int u0, int span,
-                                              float* xs, int xpitch, int M) {
+// Operands of activation row m for one K unit, blocks blk0 .. blk0 + NBLK - 1 (one builder
+// warp): sigma from the row's largest |x| over the unit, the blocks' B fragments and zero-point
+// terms Z, and (blk0 = 0) 2^(24 - sigma). xr = the row's UK x values in shared memory.
+template <int TYPE, int NT, int NBLK>
+__device__ __forceinline__ void build_row(uint8_t* slot_b, float* slot_z, float* slot_so, const float* xr, int m,
+                                          int M, int blk0, int lane) {
     using F = PnFmt<TYPE>;
-    using C = Cfg<TYPE, NT, TPW>;
     constexpr int STEPS = F::PAIRS;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int nblk = span * kUnitBlocks;
-    uint32_t* maxbits = sm.maxbits();
-    float* sig_in = sm.sig_in();
-    float* sig_out = sm.sig_out();
-    // x: the CTA's K units (slots 0..span-1 = units u0, u0+1, .. mod U) of every row, straight
-    // from global memory (L2 only: X may have been written by the previous grid), into shared
-    // memory at pitch xpitch; max |x| per row on the way (a non-negative float's bits order like
-    // its value)
+    constexpr int PAIRS = (STEPS + 1) / 2;  // records per lane column and block
     constexpr int UK = kUnitBlocks * F::BLK;
-    const int vec = span * (UK / 4);
-    for (int m = 0; m < M; ++m) {
-        const float* xg = X + static_cast<size_t>(m) * K;
-        float* xd = xs + m * xpitch;
-        uint32_t mx = 0;
-        for (int q = tid; q < vec; q += C::NCT) {
-            const int sl = q / (UK / 4);
-            int u = u0 + sl;
-            if (u >= U) u -= U;
-            const int off = 4 * q - sl * UK;
-            const float4 v = __ldcg(reinterpret_cast<const float4*>(xg + static_cast<size_t>(u) * UK + off));
-            *reinterpret_cast<float4*>(xd + sl * UK + off) = v;
-            mx = max(mx, max(max(__float_as_uint(v.x) & 0x7FFFFFFFu, __float_as_uint(v.y) & 0x7FFFFFFFu),
-                             max(__float_as_uint(v.z) & 0x7FFFFFFFu, __float_as_uint(v.w) & 0x7FFFFFFFu)));
-        }
-        mx = __reduce_max_sync(0xffffffffu, mx);
-        if (lane == 0) atomicMax(&maxbits[m], mx);
+    constexpr int BFU = NT * 256 * STEPS;
+    uint32_t mx = 0;  // a non-negative float's bits order like its value
+    for (int q = lane; q < UK / 4; q += 32) {
+        const float4 v = reinterpret_cast<const float4*>(xr)[q];
+        mx = max(mx, max(max(__float_as_uint(v.x) & 0x7FFFFFFFu, __float_as_uint(v.y) & 0x7FFFFFFFu),
+                         max(__float_as_uint(v.z) & 0x7FFFFFFFu, __float_as_uint(v.w) & 0x7FFFFFFFu)));
     }
-    fence_proxy_async_smem();  // these bytes are later overwritten by tensor-map copies
-    named_sync(1, C::NCT);
-    if (tid < M) {
-        const uint32_t bits = maxbits[tid];
-        const int E = static_cast<int>(bits >> 23);
-        int sg = (bits == 0 || E >= 255) ? 0 : 141 - E;  // max < 2^(E-126)
-        sg = min(100, max(-100, sg));
-        sig_in[tid] = exp2i(sg);
-        sig_out[tid] = exp2i(24 - sg);  // undoes sigma and the 2^-24 of the subnormal codes
-    }
-    named_sync(1, C::NCT);
-    // B fragments: one item per (block, pair of slices, lane column c), rows m inside. For slices
-    // 2p and 2p + 1 the item builds the registers b0 (decode register c) and b1 (register c + 4)
-    // of row m's hi column 2m and lo column 2m + 1 and stores them as the two 16-byte lane
-    // records (lane = 4 * (column % 8) + c; an odd last slice has 8-byte records).
-    uint8_t* bbase = sm.b();
-    constexpr int PAIRS = (STEPS + 1) / 2;
-    const int items = nblk * PAIRS * 4;
-    for (int it = tid; it < items; it += C::NCT) {
-        const int c = it & 3, rest = it >> 2;
-        const int pr = rest % PAIRS, blk = rest / PAIRS;
+    mx = __reduce_max_sync(0xffffffffu, mx);
+    const int E = static_cast<int>(mx >> 23);
+    int sg = (mx == 0 || E >= 255) ? 0 : 141 - E;  // max < 2^(E-126)
+    sg = min(100, max(-100, sg));
+    const float sig_in = exp2i(sg);
+    // lanes in groups of JL per block: lane column c and record pair pr of slices 2pr, 2pr + 1
+    // (registers b0 = decode register c, b1 = register c + 4) of the hi column 2m and lo column
+    // 2m + 1; 16-byte lane records (8-byte for an odd last slice alone), lane = 4 * (column % 8) + c
+    constexpr int JL = (PAIRS * 4 <= 8) ? 8 : 16;
+    constexpr int BPP = 32 / JL;  // blocks per pass
+    const int jl = lane % JL, pr = jl >> 2, c = jl & 3;
+    const int n = 2 * m;
+    const int lh = ((n & 7) << 2) | c, ll = (((n + 1) & 7) << 2) | c;
+#pragma unroll
+    for (int b0 = 0; b0 < NBLK; b0 += BPP) {
+        const int blk = blk0 + b0 + lane / JL;
         const int odd = blk & 1;
-        const bool single = (STEPS & 1) && pr == PAIRS - 1;  // the odd last slice alone
-        for (int m = 0; m < M; ++m) {
-            const float* xb = xs + m * xpitch + blk * F::BLK;
+        const float* xb = xr + blk * F::BLK;
+        float zs = 0.0f;  // this lane's part of the block's sum of x (each element once)
+        if (pr < PAIRS) {
+            const bool single = (STEPS & 1) && pr == PAIRS - 1;  // the odd last slice alone
             uint32_t hi[4] = {0u, 0u, 0u, 0u}, lo[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
             for (int q = 0; q < 4; ++q) {  // q = 2 * (slice - 2pr) + register
                 const int st = 2 * pr + (q >> 1), i = c + 4 * (q & 1);
                 if (st < STEPS) {
-                    const float sc = sig_in[m] * step_scale<TYPE>(st);
-                    const float v0 = xb[pn_elem(F::CPW, odd, i, st, 0)] * sc;
-                    const float v1 = xb[pn_elem(F::CPW, odd, i, st, 1)] * sc;
+                    const float x0 = xb[pn_elem(F::CPW, odd, i, st, 0)];
+                    const float x1 = xb[pn_elem(F::CPW, odd, i, st, 1)];
+                    zs += x0;
+                    zs += x1;
+                    const float sc = sig_in * step_scale<TYPE>(st);
+                    const float v0 = x0 * sc, v1 = x1 * sc;
                     const __half h0 = __float2half_rn(v0), h1 = __float2half_rn(v1);
                     hi[q] = pack_half2(h0, h1);
                     lo[q] = pack_half2(__float2half_rn(v0 - __half2float(h0)), __float2half_rn(v1 - __half2float(h1)));
                 }
             }
-            const int n = 2 * m;  // hi column; the lo column n + 1 is in the same n8 tile
-            uint8_t* tb = bbase + blk * C::BFU + (n >> 3) * 256 * STEPS + pr * 512;
-            const int lh = ((n & 7) << 2) | c, ll = (((n + 1) & 7) << 2) | c;
+            uint8_t* tb = slot_b + blk * BFU + (n >> 3) * 256 * STEPS + pr * 512;
             if (single) {
                 *reinterpret_cast<uint2*>(tb + lh * 8) = make_uint2(hi[0], hi[1]);
                 *reinterpret_cast<uint2*>(tb + ll * 8) = make_uint2(lo[0], lo[1]);
@@ -270,39 +245,16 @@ __device__ __forceinline__ void fill_operands(const Smem& sm, const float* X, in
                 *reinterpret_cast<uint4*>(tb + ll * 16) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
             }
         }
+#pragma unroll
+        for (int o = JL / 2; o > 0; o >>= 1) zs += __shfl_xor_sync(0xffffffffu, zs, o);  // within the group
+        // Z = z * sum over the block of 2^-24 * 8^j * B = z * 2^(sigma - 24) * (sum of x)
+        if (jl == 0) slot_z[blk * M + m] = static_cast<float>(F::Z) * zs * exp2i(sg - 24);
     }
-    named_sync(1, C::NCT);
-    // Z = z * sum over the block of (2^-24 * 8^j) * B, on the tensor core: an A operand with code
-    // 1 at slice j's position in every row and k (the subnormal 2^-24 * 8^j) sums B the same way
-    // the main loop's mma sums n * 2^-24 * 8^j * B. One warp per block.
-    float* z = sm.z();
-    const int g = lane >> 2, tig = lane & 3;
-    bool live[NT];
-#pragma unroll
-    for (int t = 0; t < NT; ++t) live[t] = (8 * t + g) < 2 * M;
-    for (int blk = warp; blk < nblk; blk += C::CW) {
-        uint32_t b[NT][STEPS][2];
-        load_bfrag<TYPE, NT>(bbase + blk * C::BFU, lane, live, b);
-#pragma unroll
-        for (int t = 0; t < NT; ++t) {
-            float c[4];
-#pragma unroll
-            for (int j = 0; j < STEPS; ++j) {
-                const uint32_t one = code_one<TYPE>(j);
-                if (j == 0)
-                    mma_f16_16816_z(c, one, one, one, one, b[t][j][0], b[t][j][1]);
-                else
-                    mma_f16_16816(c, one, one, one, one, b[t][j][0], b[t][j][1]);
-            }
-            const int m = 4 * t + tig;
-            if (g == 0 && m < M) z[blk * M + m] = static_cast<float>(F::Z) * (c[0] + c[1]);
-        }
-    }
-    named_sync(1, C::NCT);
+    if (lane == 0 && blk0 == 0) slot_so[m] = exp2i(24 - sg);  // undoes sigma and the 2^-24 of the codes
 }
 
 // One block B (of the unit, compile time) for the warp's TPW tiles: decode, multiply, fold
-// d * (c - Z) into acc[tile][t][row half].
+// d * (c - Z) into acc[tile][t][row half] (the item's sums, before 2^(24 - sigma)).
 template <int TYPE, int NT, int TPW, int B>
 __device__ __forceinline__ void pn_block(const uint8_t* const (&row0)[TPW], int tig, uint32_t sel,
                                          const uint8_t* bf, int lane, const bool (&live)[NT], const float* zb, int M,
@@ -365,10 +317,12 @@ __device__ __forceinline__ void pn_block(const uint8_t* const (&row0)[TPW], int 
 }
 
 template <int TYPE, int NT, int TPW, int H>
-__device__ __forceinline__ void consumer_loop(const Smem& sm, const Ctx& cx, int i0, int n_items, int u0) {
+__device__ __forceinline__ void consumer_loop(const Smem& sm, const Ctx& cx, int i0, int n_items) {
     using C = Cfg<TYPE, NT, TPW>;
     const Sched& sc = cx.sc;
-    const int M = cx.M, NS = cx.NS, U = sc.U;
+    const int M = cx.M, NS = cx.NS, RB = cx.RB, U = sc.U;
+    const bool resident = (cx.flags & kResident) != 0;
+    const int u0 = sc.unit_of(i0);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, tig = lane & 3;
     const int tg = warp % C::TG;  // tile group: rows 16 * TPW * tg ..
@@ -376,8 +330,6 @@ __device__ __forceinline__ void consumer_loop(const Smem& sm, const Ctx& cx, int
     bool live[NT];
 #pragma unroll
     for (int t = 0; t < NT; ++t) live[t] = (8 * t + g) < 2 * M;
-    const float* z = sm.z();
-    const float* sig_out = sm.sig_out();
     float* part = sm.part();
     bool ok = true;
     float acc[TPW][NT][2];
@@ -386,7 +338,7 @@ __device__ __forceinline__ void consumer_loop(const Smem& sm, const Ctx& cx, int
 #pragma unroll
         for (int t = 0; t < NT; ++t) acc[tp][t][0] = acc[tp][t][1] = 0.0f;
     int e = 0;  // row sums handed to the reducer so far
-    // hand the row sums of the tile just finished to the reducer (scaled back), then clear them
+    // hand the row sums of the tile just finished to the reducer, then clear them
     auto emit = [&]() {
         const int buf = e & 1;
         if (e >= 2 && !mbar_wait_warp(sm.part_free(buf), ((e >> 1) - 1) & 1)) {
@@ -400,8 +352,8 @@ __device__ __forceinline__ void consumer_loop(const Smem& sm, const Ctx& cx, int
                 const int m = 4 * t + tig;
                 if (m < M) {
                     float* dst = part + ((H * 2 + buf) * M + m) * kPartPitch + 16 * (TPW * tg + tp) + g;
-                    dst[0] = acc[tp][t][0] * sig_out[m];
-                    dst[8] = acc[tp][t][1] * sig_out[m];
+                    dst[0] = acc[tp][t][0];
+                    dst[8] = acc[tp][t][1];
                 }
                 acc[tp][t][0] = acc[tp][t][1] = 0.0f;
             }
@@ -410,14 +362,20 @@ __device__ __forceinline__ void consumer_loop(const Smem& sm, const Ctx& cx, int
         ++e;
     };
     int t_i = sc.tile_of(i0), u_i = sc.unit_of(i0);
-    int cur_t = t_i;
+    int cur_t = t_i, r = -1, u_run = -1;
     for (int gi = 0; gi < n_items && ok; ++gi, next_item(sc, t_i, u_i)) {
         if (t_i != cur_t) {
             emit();
             if (!ok) break;
             cur_t = t_i;
         }
-        const int slot = (u_i >= u0) ? u_i - u0 : u_i - u0 + U;
+        if (!resident && u_i != u_run) {  // a new run: its operands
+            if (!consumer_next_run(sm, RB, lane, r)) {
+                ok = false;
+                break;
+            }
+            u_run = u_i;
+        }
         const int s = gi % NS;
         if (!mbar_wait_warp(sm.full(s), (gi / NS) & 1)) {
             ok = false;
@@ -427,15 +385,32 @@ __device__ __forceinline__ void consumer_loop(const Smem& sm, const Ctx& cx, int
         const uint8_t* row0[TPW];
 #pragma unroll
         for (int tp = 0; tp < TPW; ++tp) row0[tp] = stage + (16 * (TPW * tg + tp) + g) * kUnitBytes;
-        const int blk0 = slot * kUnitBlocks + kHalfBlocks * H;
-        const uint8_t* bf0 = sm.b() + blk0 * C::BFU;
-        const float* z0 = z + blk0 * M;
-        pn_block<TYPE, NT, TPW, kHalfBlocks * H + 0>(row0, tig, sel, bf0 + 0 * C::BFU, lane, live, z0 + 0 * M, M, acc);
-        pn_block<TYPE, NT, TPW, kHalfBlocks * H + 1>(row0, tig, sel, bf0 + 1 * C::BFU, lane, live, z0 + 1 * M, M, acc);
-        pn_block<TYPE, NT, TPW, kHalfBlocks * H + 2>(row0, tig, sel, bf0 + 2 * C::BFU, lane, live, z0 + 2 * M, M, acc);
-        pn_block<TYPE, NT, TPW, kHalfBlocks * H + 3>(row0, tig, sel, bf0 + 3 * C::BFU, lane, live, z0 + 3 * M, M, acc);
+        const int os = resident ? ((u_i >= u0) ? u_i - u0 : u_i - u0 + U) : r % RB;
+        const uint8_t* bf0 = sm.slot(os) + kHalfBlocks * H * C::BFU;
+        const float* z0 = sm.slot_z(os) + kHalfBlocks * H * M;
+        float ai[TPW][NT][2];
+#pragma unroll
+        for (int tp = 0; tp < TPW; ++tp)
+#pragma unroll
+            for (int t = 0; t < NT; ++t) ai[tp][t][0] = ai[tp][t][1] = 0.0f;
+        pn_block<TYPE, NT, TPW, kHalfBlocks * H + 0>(row0, tig, sel, bf0 + 0 * C::BFU, lane, live, z0 + 0 * M, M, ai);
+        pn_block<TYPE, NT, TPW, kHalfBlocks * H + 1>(row0, tig, sel, bf0 + 1 * C::BFU, lane, live, z0 + 1 * M, M, ai);
+        pn_block<TYPE, NT, TPW, kHalfBlocks * H + 2>(row0, tig, sel, bf0 + 2 * C::BFU, lane, live, z0 + 2 * M, M, ai);
+        pn_block<TYPE, NT, TPW, kHalfBlocks * H + 3>(row0, tig, sel, bf0 + 3 * C::BFU, lane, live, z0 + 3 * M, M, ai);
         __syncwarp();
         if (lane == 0) mbar_arrive(sm.empty(s));
+        // the item's sums times 2^(24 - sigma) of its unit
+        const float* so = sm.slot_so(os);
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+            const int m = 4 * t + tig;
+            const float f = (m < M) ? so[m] : 0.0f;
+#pragma unroll
+            for (int tp = 0; tp < TPW; ++tp) {
+                acc[tp][t][0] = fmaf(ai[tp][t][0], f, acc[tp][t][0]);
+                acc[tp][t][1] = fmaf(ai[tp][t][1], f, acc[tp][t][1]);
+            }
+        }
     }
     if (ok && n_items > 0) emit();
     if (!ok && lane == 0) record_error(cx.err, kErrFullWait);
@@ -443,51 +418,55 @@ __device__ __forceinline__ void consumer_loop(const Smem& sm, const Ctx& cx, int
 
 template <int TYPE, int NT, int TPW>
 __global__ void __launch_bounds__(Cfg<TYPE, NT, TPW>::THREADS, 1) pn_gemv_kernel(const __grid_constant__ PnArgs a) {
-    using F = PnFmt<TYPE>;
     using C = Cfg<TYPE, NT, TPW>;
-    constexpr int UK = kUnitBlocks * F::BLK;  // weights of a row per unit
+    constexpr int UK = C::UK;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* base = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
-    const Smem sm{base,        smem_addr(base + a.bar_off), a.NS,       a.misc_off, a.z_off, a.part_off,
-                  a.b_off,     a.stage_off,                 a.list_off, a.list_cap};
-    const Ctx cx{a.sc, a.X, a.Y, a.ws, a.cnt, a.err, a.N, a.K, a.M, a.NS, a.x_stage, a.xpitch, a.flags};
+    // builder jobs: one per row, or two (block halves) per row when there are fewer rows than builders
+    const int parts = (a.M < C::NB) ? 2 : 1;
+    const Smem sm{base,         smem_addr(base), a.NS,       a.RB,         a.M,           UK,
+                  a.list_off,   a.part_off,      a.xs_off,   a.ring_off,   a.stage_off,   a.slot_bytes,
+                  static_cast<uint32_t>(kUnitBlocks * C::BFU), a.list_cap, a.M * parts};
+    const Ctx cx{a.sc, a.X, a.Y, a.ws, a.cnt, a.err, a.N, a.K, a.M, a.NS, a.RB, a.flags};
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    // this CTA's share of the items, and the K units it touches (slot = (u - u0) mod U)
+    // this CTA's share of the items
     const Sched& sc = cx.sc;
     const int i0 = sc.first(blockIdx.x), i1 = sc.first(blockIdx.x + 1);
-    const int n_items = static_cast<int>(i1 - i0);
-    const int u0 = n_items > 0 ? sc.unit_of(i0) : 0;
-    const int span = sc.span(i0, i1);
+    const int n_items = i1 - i0;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < a.NS; ++s) {
             mbar_init(sm.full(s), 1);
             mbar_init(sm.empty(s), C::CW);
         }
-        mbar_init(sm.x_free(), 1);
+        for (int s = 0; s < a.RB; ++s) {
+            mbar_init(sm.op_full(s), C::NB);
+            mbar_init(sm.op_empty(s), C::CW);
+        }
         for (int b = 0; b < 2; ++b) {
             mbar_init(sm.part_full(b), C::CW);
             mbar_init(sm.part_free(b), 1);
         }
+        mbar_init(sm.x_free(), 1);
         mbar_fence_init();
         griddep_launch_dependents();
+        *sm.n_finish() = 0;
     }
-    if (threadIdx.x < 16) sm.maxbits()[threadIdx.x] = 0u;
-    if (threadIdx.x == 0) *sm.n_finish() = 0;
     __syncthreads();
 
     if (warp == C::PRODUCER) {
-        // ---------------- producer: x slice + one tensor-map copy per item ----------------
+        // ---------------- producer: one tensor-map copy per item ----------------
         if (lane == 0 && n_items > 0) {
             const uint64_t pol = l2_policy_evict_first();
             bool ok = true;
             int t_n = sc.tile_of(i0), u_n = sc.unit_of(i0);  // next item to request
+            const int x_stage = (cx.flags & kXOverlap) ? a.x_stage : cx.NS;  // stages holding x at first
             auto issue = [&](int gi) {
                 const int s = gi % cx.NS;
                 if (gi >= cx.NS) {
                     if (!mbar_wait_bounded(sm.empty(s), ((gi / cx.NS) - 1) & 1)) return false;
-                } else if (s >= cx.x_stage) {
+                } else if (s >= x_stage) {
                     if (!mbar_wait_bounded(sm.x_free(), 0)) return false;
                 }
                 mbar_arrive_expect_tx(sm.full(s), static_cast<uint32_t>(kStageBytes));
@@ -497,9 +476,9 @@ __global__ void __launch_bounds__(Cfg<TYPE, NT, TPW>::THREADS, 1) pn_gemv_kernel
             };
             int gi = 0;
             if (cx.flags & kStaticWeights) {
-                // the weights are not written by earlier work in the stream: start streaming
-                // them into the stages that will not hold x before the previous grid completes
-                for (; ok && gi < min(n_items, cx.x_stage); ++gi) ok = issue(gi);
+                // the weights are not written by earlier work in the stream: fill the stages
+                // (those not holding x) before the previous grid completes
+                for (; ok && gi < min(n_items, x_stage); ++gi) ok = issue(gi);
             }
             griddep_wait();  // without the static-weights flag W may be written by the previous grid
             for (; ok && gi < n_items; ++gi) ok = issue(gi);
@@ -540,69 +519,182 @@ __global__ void __launch_bounds__(Cfg<TYPE, NT, TPW>::THREADS, 1) pn_gemv_kernel
             if (np > 0) count_shares(cx, sm, np, lane);
             if (!ok && lane == 0) record_error(cx.err, kErrReduceWait);
         }
+    } else if (a.flags & kResident) {
+        // ---------------- resident operands: consumers and builders build all units' ----------------
+        // (unit slot k = unit u0 + k mod U; jobs = (slot, row, block half))
+        if (n_items > 0) {
+            const int u0 = sc.unit_of(i0);
+            const int span = sc.span(i0, i1);
+            const int pw = (warp < C::CW) ? warp : warp - C::BUILDER + C::CW;
+            const int M = cx.M;
+            const float* X = static_cast<const float*>(cx.X);
+            float* xs = sm.xs(0);
+            constexpr int CH = UK / 4;  // 16-byte chunks per row and unit
+            auto copy = [&](int c) {
+                const int row = c / CH, q = c - row * CH;  // row = k * M + m
+                const int k = row / M, m = row - k * M;
+                int u = u0 + k;
+                if (u >= sc.U) u -= sc.U;
+                cp_async16(smem_addr(xs + static_cast<size_t>(row) * UK) + 16u * q,
+                           X + static_cast<size_t>(m) * cx.K + static_cast<size_t>(u) * UK + 4 * q);
+            };
+            auto job = [&](int i) {
+                const int k = i / (2 * M), j = i - k * 2 * M;
+                const int m = j >> 1, h = j & 1;
+                build_row<TYPE, NT, 4>(sm.slot(k), sm.slot_z(k), sm.slot_so(k), xs + static_cast<size_t>(k * M + m) * UK,
+                                       m, M, 4 * h, lane);
+            };
+            resident_prologue(pw, C::CW + C::NB, lane, span * M * CH, span * M * 2, copy, job);
+            if (threadIdx.x == 0 && (a.flags & kXOverlap)) mbar_arrive(sm.x_free());
+            if (warp < C::TG)
+                consumer_loop<TYPE, NT, TPW, 0>(sm, cx, i0, n_items);
+            else if (warp < C::CW)
+                consumer_loop<TYPE, NT, TPW, 1>(sm, cx, i0, n_items);
+        }
+    } else if (warp >= C::BUILDER) {
+        // ---------------- builders: operands of each run; jobs j = b, b + NB, .. ----------------
+        // job j = row j / parts, block part j % parts; its x row is copied to x row slot j
+        if (n_items > 0) {
+            griddep_wait();  // X belongs to the previous grid until now
+            const int b = warp - C::BUILDER;
+            const float* X = static_cast<const float*>(cx.X);
+            auto issue = [&](int u, int buf) {
+                float* xb = sm.xs(buf);
+                for (int j = b; j < sm.J; j += C::NB) {
+                    const float* src = X + static_cast<size_t>(j / parts) * cx.K + static_cast<size_t>(u) * UK;
+                    const uint32_t dst = smem_addr(xb + j * UK);
+                    for (int q = lane; q < UK / 4; q += 32) cp_async16(dst + 16u * q, src + 4 * q);
+                }
+            };
+            auto build = [&](int slot, int buf) {
+                const float* xb = sm.xs(buf);
+                for (int j = b; j < sm.J; j += C::NB) {
+                    if (parts == 2)
+                        build_row<TYPE, NT, 4>(sm.slot(slot), sm.slot_z(slot), sm.slot_so(slot), xb + j * UK, j >> 1,
+                                               cx.M, 4 * (j & 1), lane);
+                    else
+                        build_row<TYPE, NT, 8>(sm.slot(slot), sm.slot_z(slot), sm.slot_so(slot), xb + j * UK, j, cx.M,
+                                               0, lane);
+                }
+            };
+            bool ok;
+            if (a.XB == 4)
+                ok = builder_loop<4>(sm, sc, i0, n_items, cx.RB, lane, issue, build);
+            else if (a.XB == 2)
+                ok = builder_loop<2>(sm, sc, i0, n_items, cx.RB, lane, issue, build);
+            else
+                ok = builder_loop<1>(sm, sc, i0, n_items, cx.RB, lane, issue, build);
+            if (!ok && lane == 0) record_error(cx.err, kErrOperandWait);
+        }
     } else {
         // ---------------- consumer warps ----------------
         if (n_items > 0) {
-            griddep_wait();  // X belongs to the previous grid until now
-            float* xs = reinterpret_cast<float*>(sm.stage(cx.x_stage));
-            fill_operands<TYPE, NT, TPW>(sm, static_cast<const float*>(cx.X), cx.K, sc.U, u0, span, xs, cx.xpitch, cx.M);
-            if (threadIdx.x == 0) mbar_arrive(sm.x_free());  // the x stages may now take weights
             if (warp < C::TG)
-                consumer_loop<TYPE, NT, TPW, 0>(sm, cx, i0, n_items, u0);
+                consumer_loop<TYPE, NT, TPW, 0>(sm, cx, i0, n_items);
             else
-                consumer_loop<TYPE, NT, TPW, 1>(sm, cx, i0, n_items, u0);
+                consumer_loop<TYPE, NT, TPW, 1>(sm, cx, i0, n_items);
         }
     }
     // the tiles this CTA completed: every warp sums some of them
     __syncthreads();
-    const int nf = *sm.n_finish();
-    for (int k = warp; k < nf; k += C::THREADS / 32) finish_tile(cx, sm.finish()[k], lane);
+    finish_tiles(cx, sm, warp, C::THREADS / 32, lane);
 }
 
 // ---- host side --------------------------------------------------------------------------------------
 
+constexpr int kDefaultStages = 4;
+
 struct Plan {
     Sched sc{};
     bool publish = false;  // some tile is shared by several CTAs (the workspace is used)
-    int NS = 0, x_stage = 0, span_max = 0, xpitch = 0, list_cap = 0;
-    uint32_t bar_off = 0, misc_off = 0, list_off = 0, z_off = 0, part_off = 0, b_off = 0, stage_off = 0, total = 0;
+    unsigned mode = 0;     // kResident, kXOverlap
+    int NS = 0, RB = 0, XB = 0, x_stage = 0, list_cap = 0;
+    uint32_t list_off = 0, part_off = 0, xs_off = 0, ring_off = 0, stage_off = 0, slot_bytes = 0, total = 0;
 };
 
-// Shared-memory layout and stage count for one item order; false when it does not fit.
-bool layout(int blk_weights, int bfu, int M, int ns_req, Plan& p) {
-    p.span_max = 0;
-    for (int c = 0; c < p.sc.G; ++c) p.span_max = std::max(p.span_max, p.sc.span(p.sc.first(c), p.sc.first(c + 1)));
-    const uint32_t nblk = static_cast<uint32_t>(p.span_max) * kUnitBlocks;
-    p.xpitch = static_cast<int>(nblk) * blk_weights + 4;
-    p.bar_off = 0;
-    p.misc_off = 8u * (2 * kMaxStages + 6);
+// Barriers, lists and row sums at the start; returns the first free (128-aligned) offset.
+uint32_t head_layout(int bfu, int M, Plan& p) {
     p.list_cap = (p.sc.items + p.sc.G - 1) / p.sc.G;
-    p.list_off = align_up(p.misc_off + 192u, 16);
-    p.z_off = align_up(p.list_off + (2u * p.list_cap + 4u) * 4u, 16);
-    p.part_off = align_up(p.z_off + nblk * M * 4u, 16);
-    p.b_off = align_up(p.part_off + 4u * M * kPartPitch * 4u, 128);
-    p.stage_off = align_up(p.b_off + nblk * static_cast<uint32_t>(bfu), 1024);
-    const uint64_t xbytes = static_cast<uint64_t>(M) * p.xpitch * 4u;
-    const int x_stages = static_cast<int>((xbytes + kStageBytes - 1) / kStageBytes);
-    for (int ns = kMaxStages; ns >= 2; --ns) {
-        if (ns_req > 0 && ns != ns_req) continue;
-        const uint64_t total = p.stage_off + static_cast<uint64_t>(ns) * kStageBytes;
-        // at least three stages unless forced, and one stage free of x when the ring allows it
-        if (total + 1024u <= kSmemLimit && ns >= x_stages && (ns_req > 0 || ns >= 3)) {
-            p.NS = ns;
-            p.x_stage = ns - x_stages;
-            p.total = static_cast<uint32_t>(total);
-            return true;
-        }
+    p.list_off = align_up(8u * kBarriers, 16);
+    p.part_off = align_up(p.list_off + (2u * p.list_cap + 4u) * 4u, 16);
+    p.slot_bytes = align_up(kUnitBlocks * static_cast<uint32_t>(bfu) + (kUnitBlocks + 1u) * M * 4u, 128);
+    return align_up(p.part_off + 4u * M * kPartPitch * 4u, 128);
+}
+
+// Streaming layout: NS weight stages, RB operand slots and XB x buffers; false when it does not fit.
+bool layout(int uk, int bfu, int M, int nb, int NS, int RB, int XB, Plan& p) {
+    p.xs_off = head_layout(bfu, M, p);
+    const uint32_t jobs = static_cast<uint32_t>(M) * (M < nb ? 2u : 1u);  // x rows per buffer
+    p.ring_off = align_up(p.xs_off + static_cast<uint32_t>(XB) * jobs * uk * 4u, 128);
+    p.stage_off = align_up(p.ring_off + static_cast<uint32_t>(RB) * p.slot_bytes, 1024);
+    const uint64_t total = p.stage_off + static_cast<uint64_t>(NS) * kStageBytes;
+    if (total + 1024u > kSmemLimit) return false;
+    p.mode = 0;
+    p.NS = NS;
+    p.RB = RB;
+    p.XB = XB;
+    p.total = static_cast<uint32_t>(total);
+    return true;
+}
+
+// Resident layout: one operand slot per unit of the largest share, x of the share in its own
+// region or (overlap) in the last weight stages until the operands are built.
+bool layout_resident(int uk, int bfu, int M, int NS, bool overlap, Plan& p) {
+    int span = 0;
+    for (int c = 0; c < p.sc.G; ++c) span = std::max(span, p.sc.span(p.sc.first(c), p.sc.first(c + 1)));
+    uint64_t off = head_layout(bfu, M, p);
+    const uint64_t xbytes = static_cast<uint64_t>(span) * M * uk * 4u;
+    if (!overlap) {
+        p.xs_off = static_cast<uint32_t>(off);
+        off = (off + xbytes + 127) / 128 * 128;
     }
+    p.ring_off = static_cast<uint32_t>(off);
+    const uint64_t stage_off = (off + static_cast<uint64_t>(span) * p.slot_bytes + 1023) / 1024 * 1024;
+    const uint64_t total = stage_off + static_cast<uint64_t>(NS) * kStageBytes;
+    if (total + 1024u > kSmemLimit) return false;
+    p.stage_off = static_cast<uint32_t>(stage_off);
+    p.x_stage = NS;
+    if (overlap) {
+        const int x_stages = static_cast<int>((xbytes + kStageBytes - 1) / kStageBytes);
+        if (x_stages > NS) return false;
+        p.x_stage = NS - x_stages;
+        p.xs_off = p.stage_off + static_cast<uint32_t>(p.x_stage) * kStageBytes;
+    }
+    p.mode = kResident | (overlap ? kXOverlap : 0u);
+    p.NS = NS;
+    p.RB = 0;
+    p.XB = 0;
+    p.total = static_cast<uint32_t>(total);
+    return true;
+}
+
+// Resident operands when they fit with at least 3 weight stages (x in its own region first),
+// else the streaming ring: the deepest weight ring up to ns_max (at least 3 stages when
+// possible), then the deepest x prefetch and operand ring that fit. ns_req forces the stage
+// count, rb_req > 0 the streaming ring with that many slots.
+bool fit(int uk, int bfu, int M, int nb, int ns_req, int rb_req, Plan& p) {
+    const int ns_max = ns_req > 0 ? ns_req : kDefaultStages;
+    const int ns_lo = ns_req > 0 ? ns_req : 3;
+    if (rb_req <= 0)
+        for (bool overlap : {false, true})
+            for (int ns = ns_max; ns >= ns_lo; --ns)
+                if (layout_resident(uk, bfu, M, ns, overlap, p)) return true;
+    for (int ns_min : {3, 2})
+        for (int xb : {4, 2, 1})
+            for (int rb : {3, 2}) {
+                if (rb_req > 0 && rb != 3) continue;
+                const int r = rb_req > 0 ? std::min(std::max(rb_req, 2), 4) : rb;  // one slot would deadlock
+                for (int ns = ns_max; ns >= (ns_req > 0 ? ns_req : ns_min); --ns)
+                    if (layout(uk, bfu, M, nb, ns, r, xb, p)) return true;
+            }
     return false;
 }
 
-// Grid, item order, stage count and layout. Candidates: one CTA per SM (stream-K), and one CTA
-// per row tile when there are fewer tiles than SMs (every tile whole, nothing to reduce across
-// CTAs). Tile-major when the operands of a share fit, else unit-major. Picks the smallest
-// estimate of (items of the busiest CTA) x (time per item) + (cross-CTA reduction tail).
-bool make_plan(int blk_weights, int bfu, int M, int64_t T, int64_t U, int sms, bool grid_forced, int ns_req, Plan& p) {
+// Grid and layout. Candidates: one CTA per SM (stream-K), and one CTA per row tile when there
+// are fewer tiles than SMs (every tile whole, nothing to reduce across CTAs). Picks the smallest
+// estimate of (items of the busiest CTA) + (cross-CTA reduction tail).
+bool make_plan(int uk, int bfu, int M, int nb, int64_t T, int64_t U, int sms, bool grid_forced, int ns_req,
+               int rb_req, Plan& p) {
     const int64_t items = T * U;
     int64_t cands[2] = {std::min<int64_t>(sms, items), 0};
     if (!grid_forced && T < sms) cands[1] = T;
@@ -610,31 +702,27 @@ bool make_plan(int blk_weights, int bfu, int M, int64_t T, int64_t U, int sms, b
     double best = 0.0;
     for (int64_t G : cands) {
         if (G <= 0) continue;
-        for (int tm = 1; tm >= 0; --tm) {
-            Plan q;
-            q.sc.items = items;
-            q.sc.T = static_cast<int>(T);
-            q.sc.U = static_cast<int>(U);
-            q.sc.G = static_cast<int>(G);
-            q.sc.tile_major = tm;
-            if (!layout(blk_weights, bfu, M, ns_req, q)) continue;
-            bool publish = false;
-            for (int c = 1; c < G && !publish; ++c) publish = q.sc.tile_of(q.sc.first(c)) == q.sc.tile_of(q.sc.first(c) - 1);
-            if (!tm && U > 1) publish = true;
-            const double cost = static_cast<double>((items + G - 1) / G) + (publish ? 2.5 : 0.0);
-            if (!found || cost < best) {
-                best = cost;
-                q.publish = publish;
-                p = q;
-                found = true;
-            }
-            break;  // unit-major only when tile-major does not fit
+        Plan q;
+        q.sc.items = static_cast<int>(items);
+        q.sc.T = static_cast<int>(T);
+        q.sc.U = static_cast<int>(U);
+        q.sc.G = static_cast<int>(G);
+        q.sc.tile_major = 1;
+        if (!fit(uk, bfu, M, nb, ns_req, rb_req, q)) continue;
+        bool publish = false;
+        for (int c = 1; c < G && !publish; ++c) publish = q.sc.tile_of(q.sc.first(c)) == q.sc.tile_of(q.sc.first(c) - 1);
+        const double cost = static_cast<double>((items + G - 1) / G) + (publish ? 2.5 : 0.0);
+        if (!found || cost < best) {
+            best = cost;
+            q.publish = publish;
+            p = q;
+            found = true;
         }
     }
     return found;
 }
 
-// Environment override PNQ_PN_CFG="tpw,grid,_,ns" (fields 0 = automatic), read once.
+// Environment override PNQ_PN_CFG="tpw,grid,rb,ns" (fields 0 = automatic), read once.
 MmaConfig env_config() {
     static MmaConfig cfg = [] {
         MmaConfig c{0, 0, 0, 0};
@@ -656,11 +744,11 @@ MmaConfig env_config() {
 template <int TYPE, int NT, int TPW>
 cudaError_t launch_cfg(PnArgs& a, const MmaConfig& cfg, bool static_weights, cudaStream_t stream,
                        const ExtWorkspace& ext) {
-    using F = PnFmt<TYPE>;
     using C = Cfg<TYPE, NT, TPW>;
     Plan p;
-    const int cap = cfg.S > 0 ? std::min(cfg.S, device_sm_count()) : device_sm_count();
-    if (!make_plan(F::BLK, C::BFU, a.M, a.sc.T, a.sc.U, cap, cfg.S > 0, cfg.ns, p)) return cudaErrorNotSupported;
+    const int cap = cfg.grid > 0 ? std::min(cfg.grid, device_sm_count()) : device_sm_count();
+    if (!make_plan(C::UK, C::BFU, a.M, C::NB, a.sc.T, a.sc.U, cap, cfg.grid > 0, cfg.ns, cfg.rb, p))
+        return cudaErrorNotSupported;
     auto kern = pn_gemv_kernel<TYPE, NT, TPW>;
     static bool opted[64] = {};
     int dev = 0;
@@ -685,17 +773,17 @@ cudaError_t launch_cfg(PnArgs& a, const MmaConfig& cfg, bool static_weights, cud
     }
     a.sc = p.sc;
     a.NS = p.NS;
+    a.RB = p.RB;
+    a.XB = p.XB;
+    a.flags = (static_weights ? kStaticWeights : 0u) | p.mode;
     a.x_stage = p.x_stage;
-    a.xpitch = p.xpitch;
-    a.flags = static_weights ? kStaticWeights : 0u;
-    a.bar_off = p.bar_off;
-    a.misc_off = p.misc_off;
     a.list_off = p.list_off;
     a.list_cap = p.list_cap;
-    a.z_off = p.z_off;
     a.part_off = p.part_off;
-    a.b_off = p.b_off;
+    a.xs_off = p.xs_off;
+    a.ring_off = p.ring_off;
     a.stage_off = p.stage_off;
+    a.slot_bytes = p.slot_bytes;
     cudaLaunchConfig_t lc{};
     lc.gridDim = dim3(p.sc.G, 1, 1);
     lc.blockDim = dim3(C::THREADS, 1, 1);
@@ -716,7 +804,7 @@ cudaError_t launch_typed(PnArgs& a, const MmaConfig& cfg, bool static_weights, c
     const int nt = (2 * a.M + 7) / 8;
     // one tile per warp (16 consumer warps) for the matrix-vector range; two tiles per warp
     // (8 consumer warps, B fragments reused across the tiles) for wider batches
-    const int tpw = cfg.rw > 0 ? cfg.rw : (nt == 1 ? 1 : 2);
+    const int tpw = cfg.tpw > 0 ? cfg.tpw : (nt == 1 ? 1 : 2);
     if (nt == 1) return tpw == 1 ? launch_cfg<TYPE, 1, 1>(a, cfg, static_weights, stream, ext)
                                  : launch_cfg<TYPE, 1, 2>(a, cfg, static_weights, stream, ext);
     if (nt == 2) return tpw == 1 ? launch_cfg<TYPE, 2, 1>(a, cfg, static_weights, stream, ext)
@@ -751,7 +839,7 @@ cudaError_t launch_pn_gemv_mma(int type, const uint8_t* W, int64_t N, int64_t K,
     a.sc.T = static_cast<int>(T);
     a.sc.U = static_cast<int>(U);
     a.sc.items = static_cast<int>(T * U);
-    const MmaConfig c = (cfg.rw > 0 || cfg.S > 0 || cfg.ns > 0) ? cfg : env_config();
+    const MmaConfig c = (cfg.tpw > 0 || cfg.grid > 0 || cfg.rb > 0 || cfg.ns > 0) ? cfg : env_config();
     return (type == kTypePn3t) ? launch_typed<kTypePn3t>(a, c, static_weights, stream, ext)
                                : launch_typed<kTypePn4t>(a, c, static_weights, stream, ext);
 }

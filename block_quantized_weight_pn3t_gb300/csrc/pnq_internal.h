@@ -13,12 +13,12 @@ struct Nvfp4View {
     float g;                // global multiplier
 };
 
-// Tile configuration of the tensor-core GEMV (fast path); fields <= 0 are chosen automatically.
+// Configuration of the tensor-core GEMV (fast path); fields <= 0 are chosen automatically.
 struct MmaConfig {
-    int rw;   // consumer warps per CTA (2, 4 or 8)
-    int S;    // K split = cluster size along K (1 = persistent grid, no cluster)
-    int tpw;  // unused (tiles per pass equal the consumer warps)
-    int ns;   // pipeline stages
+    int tpw;   // row tiles of 16 per consumer warp (1: 16 consumer warps, 2: 8)
+    int grid;  // CTAs (at most one per SM)
+    int rb;    // operand ring slots
+    int ns;    // weight pipeline stages
 };
 
 // Workspace handed in by the caller (nullptr ws: the per-stream workspace is used).

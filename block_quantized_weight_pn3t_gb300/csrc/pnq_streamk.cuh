@@ -5,6 +5,14 @@
 // warp writes a tile the CTA covered whole straight to Y, and otherwise stores the CTA's share of
 // it in a workspace slot; at the end the CTA counts its shares (one atomic each) and the CTA
 // that completes a tile sums its slots in unit order (so results do not depend on timing).
+//
+// Operands. The x fragments an item multiplies with depend only on its K unit. When the operands
+// of all units of a CTA's share fit in shared memory (resident mode), the consumer and builder
+// warps build them together once, before the first item (this overlaps the first weight copies),
+// and the items then run without further synchronisation. Otherwise (wide batches) builder warps
+// make them for each run of consecutive items with the same unit into a ring of RB slots (full /
+// empty mbarriers) ahead of the consumers, from x copied into shared memory with cp.async (XB
+// buffers), so shared memory does not grow with the share.
 #pragma once
 
 #include <cstdint>
@@ -18,6 +26,11 @@ constexpr int kTileRows = 128;        // rows per item
 constexpr int kPartPitch = 132;       // floats per (half, buffer, m) row-sum vector in shared memory
 constexpr int kMaxStages = 8;
 constexpr unsigned kStaticWeights = 1u;
+constexpr unsigned kResident = 2u;  // operands of the whole share built in the prologue
+constexpr unsigned kXOverlap = 4u;  // ... from x held in the last weight stages until then
+// barriers: full / empty per stage, op_full / op_empty per ring slot (<= 4), part_full / part_free
+// (2 each), x_free
+constexpr int kBarriers = 2 * kMaxStages + 2 * 4 + 5;
 constexpr size_t kSmemLimit = 227u * 1024u;
 
 // Item numbering. Tile-major (item = t * U + u): a CTA's share covers one or two row tiles and
@@ -60,7 +73,7 @@ struct Ctx {
     float* ws;
     uint32_t* cnt;
     int* err;
-    int N, K, M, NS, x_stage, xpitch;
+    int N, K, M, NS, RB;
     unsigned flags;
 };
 
@@ -75,6 +88,87 @@ __device__ __forceinline__ void next_item(const Sched& sc, int& t, int& u) {
         t = 0;
         ++u;
     }
+}
+
+// A run: consecutive items of a CTA's share with the same K unit (one item in tile-major order
+// unless U = 1). gi = index of its first item within the share.
+struct RunCursor {
+    int gi, t, u;
+};
+
+// Advance to the next run; false when the share has no more items.
+__device__ __forceinline__ bool next_run(const Sched& sc, int n_items, RunCursor& rc) {
+    const int u_prev = rc.u;
+    do {
+        next_item(sc, rc.t, rc.u);
+        ++rc.gi;
+    } while (rc.gi < n_items && rc.u == u_prev);
+    return rc.gi < n_items;
+}
+
+// One builder warp's loop over the runs of its CTA's share: issue(u, buf) starts the cp.async
+// copies of unit u's x rows (this warp's jobs) into x buffer buf, build(slot, buf) turns them
+// into the operands of ring slot `slot`. The copies run XB - 1 runs ahead of the build (x loads
+// wait behind the weight stream, some microseconds under load). A slot is rebuilt only after
+// the consumers released it. False if a wait gave up.
+template <int XB, class SM, class Issue, class Build>
+__device__ __forceinline__ bool builder_loop(const SM& sm, const Sched& sc, int i0, int n_items, int RB, int lane,
+                                             Issue&& issue, Build&& build) {
+    RunCursor cur{0, sc.tile_of(i0), sc.unit_of(i0)};
+    RunCursor iss = cur;  // the next run to copy
+    bool more = true;     // iss is a run of the share
+#pragma unroll
+    for (int k = 0; k < XB; ++k) {
+        if (more) {
+            issue(iss.u, k);
+            more = next_run(sc, n_items, iss);
+        }
+        cp_async_commit();  // one group per run (empty past the end)
+    }
+    for (int r = 0;; ++r) {
+        cp_async_wait<XB - 1>();  // group r: the copies of run r have landed
+        __syncwarp();
+        const int slot = r % RB;
+        if (r >= RB && !mbar_wait_warp(sm.op_empty(slot), ((r / RB) - 1) & 1)) return false;
+        build(slot, r % XB);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sm.op_full(slot));
+        if (!next_run(sc, n_items, cur)) return true;
+        if (more) {
+            issue(iss.u, r % XB);  // run r + XB into the buffer run r used
+            more = next_run(sc, n_items, iss);
+        }
+        cp_async_commit();
+    }
+}
+
+// Resident mode: the participating warps (index pw of npw) copy the x rows of the CTA's units
+// (copy(c) issues 16-byte chunk c of n_chunks) and then run every build job (job(i), i < n_jobs),
+// with a named barrier after each phase. Afterwards the x bytes may be overwritten by
+// tensor-map copies (generic-proxy reads ordered before them).
+template <class CopyF, class JobF>
+__device__ __forceinline__ void resident_prologue(int pw, int npw, int lane, int n_chunks, int n_jobs, CopyF&& copy,
+                                                  JobF&& job) {
+    griddep_wait();  // X belongs to the previous grid until now
+    for (int c = pw * 32 + lane; c < n_chunks; c += npw * 32) copy(c);
+    cp_async_commit();
+    cp_async_wait<0>();
+    named_sync(1, npw * 32);
+    for (int i = pw; i < n_jobs; i += npw) job(i);
+    fence_proxy_async_smem();
+    named_sync(1, npw * 32);
+}
+
+// Consumer side of the ring: at the first item of a new run release the previous run's slot and
+// wait for this one's operands. r = the run of the current item (-1 before the first).
+template <class SM>
+__device__ __forceinline__ bool consumer_next_run(const SM& sm, int RB, int lane, int& r) {
+    if (r >= 0) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sm.op_empty(r % RB));
+    }
+    ++r;
+    return mbar_wait_warp(sm.op_full(r % RB), (r / RB) & 1);
 }
 
 // Y rows t*128 + 4*lane .. + 3 of activation row m.
@@ -146,30 +240,44 @@ __device__ __forceinline__ void count_shares(const Ctx& a, const SM& sm, int np,
     __threadfence();  // what the other CTAs stored before counting is seen by the finishers
 }
 
-// Sum the shares of tile t in unit order into Y and clear its counter (one warp).
-__device__ __forceinline__ void finish_tile(const Ctx& a, int t, int lane) {
+// Sum the shares of tile t for activation row m in unit order into Y (one warp). The slot
+// loads go out four at a time; the additions keep unit order, so the sum does not depend on
+// which CTA finishes the tile. The m == 0 call clears the tile's counter for the next launch
+// (no other CTA reads it again in this one).
+__device__ __forceinline__ void finish_tile(const Ctx& a, int t, int m, int lane) {
     const Sched& sc = a.sc;
-    for (int m = 0; m < a.M; ++m) {
-        float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-        auto add_slot = [&](int u) {
-            const float* slot = a.ws + ((static_cast<size_t>(t) * sc.U + u) * a.M + m) * kTileRows;
-            const float4 v = __ldcg(reinterpret_cast<const float4*>(slot) + lane);
-            acc.x += v.x;
-            acc.y += v.y;
-            acc.z += v.z;
-            acc.w += v.w;
-        };
-        if (sc.consecutive()) {
-            const int a0 = sc.item(t, 0);
-            add_slot(0);
-            for (int c = sc.owner(a0) + 1; c <= sc.owner(a0 + sc.U - 1); ++c) add_slot(sc.first(c) - a0);
-        } else {
-            for (int u = 0; u < sc.U; ++u) add_slot(u);
-        }
-        put_y(a, t, m, lane, acc);
+    const bool consec = sc.consecutive();
+    const int a0 = sc.item(t, 0);
+    const int c_lo = consec ? sc.owner(a0) : 0;
+    const int n = consec ? sc.owner(a0 + sc.U - 1) - c_lo + 1 : sc.U;  // shares of the tile
+    const float* base = a.ws + (static_cast<size_t>(t) * sc.U * a.M + m) * kTileRows;
+    auto unit_of_share = [&](int j) { return !consec ? j : (j == 0 ? 0 : sc.first(c_lo + j) - a0); };
+    float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    for (int j0 = 0; j0 < n; j0 += 4) {
+        float4 v[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            if (j0 + i < n)
+                v[i] = __ldcg(reinterpret_cast<const float4*>(
+                                  base + static_cast<size_t>(unit_of_share(j0 + i)) * a.M * kTileRows) + lane);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            if (j0 + i < n) {
+                acc.x += v[i].x;
+                acc.y += v[i].y;
+                acc.z += v[i].z;
+                acc.w += v[i].w;
+            }
     }
-    __syncwarp();
-    if (lane == 0) a.cnt[t] = 0u;  // ready for the next launch
+    put_y(a, t, m, lane, acc);
+    if (m == 0 && lane == 0) a.cnt[t] = 0u;  // ready for the next launch
+}
+
+// The tiles this CTA completed, (tile, activation row) pairs spread over all nwarps warps.
+template <class SM>
+__device__ __forceinline__ void finish_tiles(const Ctx& a, const SM& sm, int warp, int nwarps, int lane) {
+    const int nf = *sm.n_finish();
+    for (int k = warp; k < nf * a.M; k += nwarps) finish_tile(a, sm.finish()[k / a.M], k % a.M, lane);
 }
 
 // ---- host ----------------------------------------------------------------------------------
