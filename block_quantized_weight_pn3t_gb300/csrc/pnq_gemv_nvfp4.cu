@@ -408,19 +408,18 @@ __global__ void __launch_bounds__(NvCfg<NT, TPW>::THREADS, 1) nvfp4_gemv_kernel(
             const int span = sc.span(i0, i1);
             const int pw = (warp < C::CW) ? warp : warp - C::BUILDER + C::CW;
             const int M = cx.M;
-            auto copy = [&](int c) {
-                const int row = c >> 5, q = c & 31;  // row = k * M + m, 32 chunks of 16 bytes
+            auto copy = [&](int row) {  // x row slot row = k * M + m, by one warp (32 chunks of 16 bytes)
                 const int k = row / M, m = row - k * M;
                 int u = u0 + k;
                 if (u >= sc.U) u -= sc.U;
-                cp_async16(smem_addr(sm.xs(k) + m * kUnitK) + 16u * q,
-                           a.X + static_cast<size_t>(m) * cx.K + static_cast<size_t>(u) * kUnitK + 8 * q);
+                cp_async16(smem_addr(sm.xs(k) + m * kUnitK) + 16u * lane,
+                           a.X + static_cast<size_t>(m) * cx.K + static_cast<size_t>(u) * kUnitK + 8 * lane);
             };
             auto job = [&](int i) {
                 const int k = i / M, m = i - k * M;
                 nv_build_row<NT>(sm.slot(k), sm.slot_so<NT>(k), sm.xs(k) + m * kUnitK, m, a.g, lane);
             };
-            resident_prologue(pw, C::CW + C::NB, lane, span * M * 32, span * M, copy, job);
+            resident_prologue(pw, C::CW + C::NB, span * M, span * M, (a.flags & kXOverlap) != 0, copy, job);
             if (threadIdx.x == 0 && (a.flags & kXOverlap)) mbar_arrive(sm.x_free());
             if (warp < C::TG)
                 nv_consumer_loop<NT, TPW, 0>(sm, cx, i0, n_items);
@@ -468,7 +467,7 @@ __global__ void __launch_bounds__(NvCfg<NT, TPW>::THREADS, 1) nvfp4_gemv_kernel(
 
 // ---- host side --------------------------------------------------------------------------------------
 
-constexpr int kDefaultStages = 6;
+constexpr int kDefaultStages = 8;
 
 struct NvPlan {
     Sched sc{};
@@ -532,15 +531,16 @@ bool nv_layout_resident(int bfu, int M, int NS, bool overlap, NvPlan& p) {
     return true;
 }
 
-// As the PN path: resident operands when they fit with at least 3 weight stages, else the
-// streaming ring (deepest weight ring, then x prefetch and operand ring).
-bool nv_fit(int bfu, int M, int ns_req, int rb_req, NvPlan& p) {
+bool nv_fit_resident(int bfu, int M, int ns_req, NvPlan& p) {
+    const int ns_max = ns_req > 0 ? ns_req : kDefaultStages, ns_lo = ns_req > 0 ? ns_req : 3;
+    for (bool overlap : {false, true})
+        for (int ns = ns_max; ns >= ns_lo; --ns)
+            if (nv_layout_resident(bfu, M, ns, overlap, p)) return true;
+    return false;
+}
+
+bool nv_fit_stream(int bfu, int M, int ns_req, int rb_req, NvPlan& p) {
     const int ns_max = ns_req > 0 ? ns_req : kDefaultStages;
-    const int ns_lo = ns_req > 0 ? ns_req : 3;
-    if (rb_req <= 0)
-        for (bool overlap : {false, true})
-            for (int ns = ns_max; ns >= ns_lo; --ns)
-                if (nv_layout_resident(bfu, M, ns, overlap, p)) return true;
     for (int ns_min : {3, 2})
         for (int xb : {4, 2, 1})
             for (int rb : {3, 2}) {
@@ -552,49 +552,81 @@ bool nv_fit(int bfu, int M, int ns_req, int rb_req, NvPlan& p) {
     return false;
 }
 
-// Same choice as the PN path: one CTA per SM (stream-K) or one per row tile.
-bool nv_plan(int bfu, int M, int64_t T, int64_t U, int sms, bool grid_forced, int ns_req, int rb_req, NvPlan& p) {
+// The PN path's choice: tile-major items with resident operands when they fit (stream-K grid
+// or one CTA per tile); otherwise, for wide batches, tile-major items with the streaming ring
+// (order = 2: grouped unit-major items with resident operands when they fit).
+bool nv_plan(int bfu, int M, int64_t T, int64_t U, int sms, bool grid_forced, int ns_req, int rb_req, int order,
+             NvPlan& p) {
     const int64_t items = T * U;
-    int64_t cands[2] = {std::min<int64_t>(sms, items), 0};
+    const int64_t G0 = std::min<int64_t>(sms, items);
+    int64_t cands[2] = {G0, 0};
     if (!grid_forced && T < sms) cands[1] = T;
-    bool found = false;
-    double best = 0.0;
-    for (int64_t G : cands) {
-        if (G <= 0) continue;
+    auto base = [&](int64_t G) {
         NvPlan q;
         q.sc.items = static_cast<int>(items);
         q.sc.T = static_cast<int>(T);
         q.sc.U = static_cast<int>(U);
         q.sc.G = static_cast<int>(G);
         q.sc.tile_major = 1;
-        if (!nv_fit(bfu, M, ns_req, rb_req, q)) continue;
-        bool publish = false;
-        for (int c = 1; c < G && !publish; ++c) publish = q.sc.tile_of(q.sc.first(c)) == q.sc.tile_of(q.sc.first(c) - 1);
-        // items here are half the bytes of a PN item: the reduction tail weighs more
-        const double cost = static_cast<double>((items + G - 1) / G) + (publish ? 5.0 : 0.0);
-        if (!found || cost < best) {
-            best = cost;
-            q.publish = publish;
-            p = q;
-            found = true;
+        q.sc.tg = 1;
+        return q;
+    };
+    auto publishes = [](const NvPlan& q) {
+        if (!q.sc.tile_major && q.sc.U > 1) return true;
+        for (int c = 1; c < q.sc.G; ++c)
+            if (q.sc.tile_of(q.sc.first(c)) == q.sc.tile_of(q.sc.first(c) - 1)) return true;
+        return false;
+    };
+    bool found = false;
+    double best = 0.0;
+    if (rb_req <= 0 && order != 2)
+        for (int64_t G : cands) {
+            if (G <= 0) continue;
+            NvPlan q = base(G);
+            if (!nv_fit_resident(bfu, M, ns_req, q)) continue;
+            q.publish = publishes(q);
+            // items here are half the bytes of a PN item: the reduction tail weighs more
+            const double cost = static_cast<double>((items + G - 1) / G) + (q.publish ? 5.0 : 0.0);
+            if (!found || cost < best) {
+                best = cost;
+                p = q;
+                found = true;
+            }
+        }
+    if (found) return true;
+    if (rb_req <= 0 && order == 2 && T > 1 && U > 1) {
+        for (int64_t tg : {2, 4, 8, 16, 32, 64, 128}) {
+            NvPlan q = base(G0);
+            q.sc.tile_major = 0;
+            q.sc.tg = static_cast<int>(std::min<int64_t>(tg, T));
+            if (nv_fit_resident(bfu, M, ns_req, q)) {
+                q.publish = publishes(q);
+                p = q;
+                return true;
+            }
+            if (tg >= T) break;
         }
     }
-    return found;
+    NvPlan q = base(G0);
+    if (!nv_fit_stream(bfu, M, ns_req, rb_req, q)) return false;
+    q.publish = publishes(q);
+    p = q;
+    return true;
 }
 
-// Environment override PNQ_NV_CFG="tpw,grid,rb,ns" (fields 0 = automatic), read once.
+// Environment override PNQ_NV_CFG="tpw,grid,rb,ns,order" (fields 0 = automatic), read once.
 MmaConfig nv_env_config() {
     static MmaConfig cfg = [] {
-        MmaConfig c{0, 0, 0, 0};
+        MmaConfig c{0, 0, 0, 0, 0};
         if (const char* s = std::getenv("PNQ_NV_CFG")) {
-            int v[4] = {0, 0, 0, 0};
+            int v[5] = {0, 0, 0, 0, 0};
             int n = 0;
             const char* p = s;
-            while (*p && n < 4) {
+            while (*p && n < 5) {
                 v[n++] = static_cast<int>(std::strtol(p, const_cast<char**>(&p), 10));
                 if (*p == ',') ++p;
             }
-            c = MmaConfig{v[0], v[1], v[2], v[3]};
+            c = MmaConfig{v[0], v[1], v[2], v[3], v[4]};
         }
         return c;
     }();
@@ -607,7 +639,8 @@ cudaError_t nv_launch_cfg(NvArgs& a, const MmaConfig& cfg, bool static_weights, 
     using C = NvCfg<NT, TPW>;
     NvPlan p;
     const int cap = cfg.grid > 0 ? std::min(cfg.grid, device_sm_count()) : device_sm_count();
-    if (!nv_plan(C::BFU, a.M, a.sc.T, a.sc.U, cap, cfg.grid > 0, cfg.ns, cfg.rb, p)) return cudaErrorNotSupported;
+    if (!nv_plan(C::BFU, a.M, a.sc.T, a.sc.U, cap, cfg.grid > 0, cfg.ns, cfg.rb, cfg.order, p))
+        return cudaErrorNotSupported;
     auto kern = nvfp4_gemv_kernel<NT, TPW>;
     static bool opted[64] = {};
     int dev = 0;
@@ -686,6 +719,7 @@ cudaError_t launch_nvfp4_gemv_mma(const Nvfp4View& w, int64_t N, int64_t K, cons
     if (cfg.grid <= 0) cfg.grid = env.grid;
     if (cfg.rb <= 0) cfg.rb = env.rb;
     if (cfg.ns <= 0) cfg.ns = env.ns;
+    if (cfg.order <= 0) cfg.order = env.order;
     const int nt = (M + 7) / 8;
     const int tpw = cfg.tpw > 0 ? cfg.tpw : (nt == 1 ? 1 : 2);
     if (nt == 1) return tpw == 1 ? nv_launch_cfg<1, 1>(a, cfg, static_weights, stream, ext)

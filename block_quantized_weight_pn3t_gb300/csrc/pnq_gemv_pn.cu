@@ -182,18 +182,53 @@ __device__ __forceinline__ void load_bfrag(const uint8_t* bf, int lane, const bo
     }
 }
 
-// Operands of activation row m for one K unit, blocks blk0 .. blk0 + NBLK - 1 (one builder
-// warp): sigma from the row's largest |x| over the unit, the blocks' B fragments and zero-point
-// terms Z, and (blk0 = 0) 2^(24 - sigma). xr = the row's UK x values in shared memory.
+// Per-lane constants of build_row, the same for every block pair, unit and row: the lane builds
+// the record of lane column c and record pair pr (slices 2pr, 2pr + 1; registers b0 = decode
+// register c, b1 = register c + 4) for blocks of parity `odd` (JL lanes per block, blocks of a
+// pass start at an even index). off[q][h] = element of half h of register q, ss[q] = step scale.
+template <int TYPE>
+struct BuildLane {
+    static constexpr int STEPS = PnFmt<TYPE>::PAIRS;
+    static constexpr int PAIRS = (STEPS + 1) / 2;           // records per lane column and block
+    static constexpr int JL = (PAIRS * 4 <= 8) ? 8 : 16;    // lanes per block
+    static constexpr int BPP = 32 / JL;                     // blocks per pass
+    int off[4][2];
+    float ss[4];
+    int pr, c;
+    unsigned act;  // bit q: slice 2pr + q / 2 exists
+    __device__ explicit BuildLane(int lane) {
+        using F = PnFmt<TYPE>;
+        const int jl = lane % JL, odd = (lane / JL) & 1;
+        pr = jl >> 2;
+        c = jl & 3;
+        act = 0;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {  // q = 2 * (slice - 2pr) + register
+            const int st = 2 * pr + (q >> 1), i = c + 4 * (q & 1);
+            const bool on = pr < PAIRS && st < STEPS;
+            act |= on ? (1u << q) : 0u;
+            off[q][0] = on ? pn_elem(F::CPW, odd, i, st, 0) : 0;
+            off[q][1] = on ? pn_elem(F::CPW, odd, i, st, 1) : 0;
+            ss[q] = on ? step_scale<TYPE>(st) : 0.0f;
+        }
+    }
+};
+
+// Operands of activation row m for one K unit, blocks blk0 .. blk0 + NBLK - 1 (one warp): sigma
+// from the row's largest |x| over the unit, the blocks' B fragments (hi column 2m, lo column
+// 2m + 1; 16-byte lane records, 8-byte for an odd last slice alone; lane = 4 * (column % 8) + c)
+// and zero-point terms Z, and (blk0 = 0) 2^(24 - sigma). xr = the row's UK x values in shared
+// memory.
 template <int TYPE, int NT, int NBLK>
 __device__ __forceinline__ void build_row(uint8_t* slot_b, float* slot_z, float* slot_so, const float* xr, int m,
-                                          int M, int blk0, int lane) {
+                                          int M, int blk0, int lane, const BuildLane<TYPE>& L) {
     using F = PnFmt<TYPE>;
+    using BL = BuildLane<TYPE>;
     constexpr int STEPS = F::PAIRS;
-    constexpr int PAIRS = (STEPS + 1) / 2;  // records per lane column and block
     constexpr int UK = kUnitBlocks * F::BLK;
     constexpr int BFU = NT * 256 * STEPS;
     uint32_t mx = 0;  // a non-negative float's bits order like its value
+#pragma unroll
     for (int q = lane; q < UK / 4; q += 32) {
         const float4 v = reinterpret_cast<const float4*>(xr)[q];
         mx = max(mx, max(max(__float_as_uint(v.x) & 0x7FFFFFFFu, __float_as_uint(v.y) & 0x7FFFFFFFu),
@@ -204,39 +239,33 @@ __device__ __forceinline__ void build_row(uint8_t* slot_b, float* slot_z, float*
     int sg = (mx == 0 || E >= 255) ? 0 : 141 - E;  // max < 2^(E-126)
     sg = min(100, max(-100, sg));
     const float sig_in = exp2i(sg);
-    // lanes in groups of JL per block: lane column c and record pair pr of slices 2pr, 2pr + 1
-    // (registers b0 = decode register c, b1 = register c + 4) of the hi column 2m and lo column
-    // 2m + 1; 16-byte lane records (8-byte for an odd last slice alone), lane = 4 * (column % 8) + c
-    constexpr int JL = (PAIRS * 4 <= 8) ? 8 : 16;
-    constexpr int BPP = 32 / JL;  // blocks per pass
-    const int jl = lane % JL, pr = jl >> 2, c = jl & 3;
-    const int n = 2 * m;
-    const int lh = ((n & 7) << 2) | c, ll = (((n + 1) & 7) << 2) | c;
+    float sc[4];
 #pragma unroll
-    for (int b0 = 0; b0 < NBLK; b0 += BPP) {
-        const int blk = blk0 + b0 + lane / JL;
-        const int odd = blk & 1;
+    for (int q = 0; q < 4; ++q) sc[q] = sig_in * L.ss[q];
+    const int n = 2 * m;
+    const int lh = ((n & 7) << 2) | L.c, ll = (((n + 1) & 7) << 2) | L.c;
+    const bool single = (STEPS & 1) && L.pr == BL::PAIRS - 1;  // the odd last slice alone
+    const int jl = lane % BL::JL;
+#pragma unroll
+    for (int b0 = 0; b0 < NBLK; b0 += BL::BPP) {
+        const int blk = blk0 + b0 + lane / BL::JL;
         const float* xb = xr + blk * F::BLK;
         float zs = 0.0f;  // this lane's part of the block's sum of x (each element once)
-        if (pr < PAIRS) {
-            const bool single = (STEPS & 1) && pr == PAIRS - 1;  // the odd last slice alone
+        if (L.act) {
             uint32_t hi[4] = {0u, 0u, 0u, 0u}, lo[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {  // q = 2 * (slice - 2pr) + register
-                const int st = 2 * pr + (q >> 1), i = c + 4 * (q & 1);
-                if (st < STEPS) {
-                    const float x0 = xb[pn_elem(F::CPW, odd, i, st, 0)];
-                    const float x1 = xb[pn_elem(F::CPW, odd, i, st, 1)];
+            for (int q = 0; q < 4; ++q) {
+                if (L.act & (1u << q)) {
+                    const float x0 = xb[L.off[q][0]], x1 = xb[L.off[q][1]];
                     zs += x0;
                     zs += x1;
-                    const float sc = sig_in * step_scale<TYPE>(st);
-                    const float v0 = x0 * sc, v1 = x1 * sc;
+                    const float v0 = x0 * sc[q], v1 = x1 * sc[q];
                     const __half h0 = __float2half_rn(v0), h1 = __float2half_rn(v1);
                     hi[q] = pack_half2(h0, h1);
                     lo[q] = pack_half2(__float2half_rn(v0 - __half2float(h0)), __float2half_rn(v1 - __half2float(h1)));
                 }
             }
-            uint8_t* tb = slot_b + blk * BFU + (n >> 3) * 256 * STEPS + pr * 512;
+            uint8_t* tb = slot_b + blk * BFU + (n >> 3) * 256 * STEPS + L.pr * 512;
             if (single) {
                 *reinterpret_cast<uint2*>(tb + lh * 8) = make_uint2(hi[0], hi[1]);
                 *reinterpret_cast<uint2*>(tb + ll * 8) = make_uint2(lo[0], lo[1]);
@@ -246,7 +275,7 @@ __device__ __forceinline__ void build_row(uint8_t* slot_b, float* slot_z, float*
             }
         }
 #pragma unroll
-        for (int o = JL / 2; o > 0; o >>= 1) zs += __shfl_xor_sync(0xffffffffu, zs, o);  // within the group
+        for (int o = BL::JL / 2; o > 0; o >>= 1) zs += __shfl_xor_sync(0xffffffffu, zs, o);  // within the group
         // Z = z * sum over the block of 2^-24 * 8^j * B = z * 2^(sigma - 24) * (sum of x)
         if (jl == 0) slot_z[blk * M + m] = static_cast<float>(F::Z) * zs * exp2i(sg - 24);
     }
@@ -530,21 +559,23 @@ __global__ void __launch_bounds__(Cfg<TYPE, NT, TPW>::THREADS, 1) pn_gemv_kernel
             const float* X = static_cast<const float*>(cx.X);
             float* xs = sm.xs(0);
             constexpr int CH = UK / 4;  // 16-byte chunks per row and unit
-            auto copy = [&](int c) {
-                const int row = c / CH, q = c - row * CH;  // row = k * M + m
+            auto copy = [&](int row) {     // x row slot row = k * M + m, by one warp
                 const int k = row / M, m = row - k * M;
                 int u = u0 + k;
                 if (u >= sc.U) u -= sc.U;
-                cp_async16(smem_addr(xs + static_cast<size_t>(row) * UK) + 16u * q,
-                           X + static_cast<size_t>(m) * cx.K + static_cast<size_t>(u) * UK + 4 * q);
+                const float* src = X + static_cast<size_t>(m) * cx.K + static_cast<size_t>(u) * UK;
+                const uint32_t dst = smem_addr(xs + static_cast<size_t>(row) * UK);
+#pragma unroll
+                for (int q = lane; q < CH; q += 32) cp_async16(dst + 16u * q, src + 4 * q);
             };
+            const BuildLane<TYPE> bl(lane);
             auto job = [&](int i) {
                 const int k = i / (2 * M), j = i - k * 2 * M;
                 const int m = j >> 1, h = j & 1;
                 build_row<TYPE, NT, 4>(sm.slot(k), sm.slot_z(k), sm.slot_so(k), xs + static_cast<size_t>(k * M + m) * UK,
-                                       m, M, 4 * h, lane);
+                                       m, M, 4 * h, lane, bl);
             };
-            resident_prologue(pw, C::CW + C::NB, lane, span * M * CH, span * M * 2, copy, job);
+            resident_prologue(pw, C::CW + C::NB, span * M, span * M * 2, (a.flags & kXOverlap) != 0, copy, job);
             if (threadIdx.x == 0 && (a.flags & kXOverlap)) mbar_arrive(sm.x_free());
             if (warp < C::TG)
                 consumer_loop<TYPE, NT, TPW, 0>(sm, cx, i0, n_items);
@@ -566,15 +597,16 @@ __global__ void __launch_bounds__(Cfg<TYPE, NT, TPW>::THREADS, 1) pn_gemv_kernel
                     for (int q = lane; q < UK / 4; q += 32) cp_async16(dst + 16u * q, src + 4 * q);
                 }
             };
+            const BuildLane<TYPE> bl(lane);
             auto build = [&](int slot, int buf) {
                 const float* xb = sm.xs(buf);
                 for (int j = b; j < sm.J; j += C::NB) {
                     if (parts == 2)
                         build_row<TYPE, NT, 4>(sm.slot(slot), sm.slot_z(slot), sm.slot_so(slot), xb + j * UK, j >> 1,
-                                               cx.M, 4 * (j & 1), lane);
+                                               cx.M, 4 * (j & 1), lane, bl);
                     else
                         build_row<TYPE, NT, 8>(sm.slot(slot), sm.slot_z(slot), sm.slot_so(slot), xb + j * UK, j, cx.M,
-                                               0, lane);
+                                               0, lane, bl);
                 }
             };
             bool ok;
@@ -668,17 +700,21 @@ bool layout_resident(int uk, int bfu, int M, int NS, bool overlap, Plan& p) {
     return true;
 }
 
-// Resident operands when they fit with at least 3 weight stages (x in its own region first),
-// else the streaming ring: the deepest weight ring up to ns_max (at least 3 stages when
-// possible), then the deepest x prefetch and operand ring that fit. ns_req forces the stage
-// count, rb_req > 0 the streaming ring with that many slots.
-bool fit(int uk, int bfu, int M, int nb, int ns_req, int rb_req, Plan& p) {
+// Resident operands with the deepest weight ring up to ns_max (at least 3 stages), x in its own
+// region when that fits (measured faster than a deeper ring whose last stages wait for x), else
+// in the weight stages.
+bool fit_resident(int uk, int bfu, int M, int ns_req, Plan& p) {
+    const int ns_max = ns_req > 0 ? ns_req : kDefaultStages, ns_lo = ns_req > 0 ? ns_req : 3;
+    for (bool overlap : {false, true})
+        for (int ns = ns_max; ns >= ns_lo; --ns)
+            if (layout_resident(uk, bfu, M, ns, overlap, p)) return true;
+    return false;
+}
+
+// Streaming ring: the deepest weight ring up to ns_max (at least 3 stages when possible), then
+// the deepest x prefetch and operand ring that fit; rb_req > 0 forces the ring's slots.
+bool fit_stream(int uk, int bfu, int M, int nb, int ns_req, int rb_req, Plan& p) {
     const int ns_max = ns_req > 0 ? ns_req : kDefaultStages;
-    const int ns_lo = ns_req > 0 ? ns_req : 3;
-    if (rb_req <= 0)
-        for (bool overlap : {false, true})
-            for (int ns = ns_max; ns >= ns_lo; --ns)
-                if (layout_resident(uk, bfu, M, ns, overlap, p)) return true;
     for (int ns_min : {3, 2})
         for (int xb : {4, 2, 1})
             for (int rb : {3, 2}) {
@@ -690,51 +726,84 @@ bool fit(int uk, int bfu, int M, int nb, int ns_req, int rb_req, Plan& p) {
     return false;
 }
 
-// Grid and layout. Candidates: one CTA per SM (stream-K), and one CTA per row tile when there
-// are fewer tiles than SMs (every tile whole, nothing to reduce across CTAs). Picks the smallest
-// estimate of (items of the busiest CTA) + (cross-CTA reduction tail).
+// Grid, item order and layout. Tile-major items with resident operands when they fit: grid of
+// one CTA per SM (stream-K) or, with fewer row tiles than SMs, one CTA per tile (nothing to
+// reduce across CTAs), whichever has the smaller estimate of (items of the busiest CTA) +
+// (cross-CTA reduction tail). Otherwise (wide batches) one CTA per SM with grouped unit-major
+// items (the smallest group whose operands fit, resident) or, when that does not fit or
+// order = 1, tile-major items with the streaming ring. rb_req > 0 forces the streaming ring,
+// order = 2 the grouped order.
 bool make_plan(int uk, int bfu, int M, int nb, int64_t T, int64_t U, int sms, bool grid_forced, int ns_req,
-               int rb_req, Plan& p) {
+               int rb_req, int order, Plan& p) {
     const int64_t items = T * U;
-    int64_t cands[2] = {std::min<int64_t>(sms, items), 0};
+    const int64_t G0 = std::min<int64_t>(sms, items);
+    int64_t cands[2] = {G0, 0};
     if (!grid_forced && T < sms) cands[1] = T;
-    bool found = false;
-    double best = 0.0;
-    for (int64_t G : cands) {
-        if (G <= 0) continue;
+    auto base = [&](int64_t G) {
         Plan q;
         q.sc.items = static_cast<int>(items);
         q.sc.T = static_cast<int>(T);
         q.sc.U = static_cast<int>(U);
         q.sc.G = static_cast<int>(G);
         q.sc.tile_major = 1;
-        if (!fit(uk, bfu, M, nb, ns_req, rb_req, q)) continue;
-        bool publish = false;
-        for (int c = 1; c < G && !publish; ++c) publish = q.sc.tile_of(q.sc.first(c)) == q.sc.tile_of(q.sc.first(c) - 1);
-        const double cost = static_cast<double>((items + G - 1) / G) + (publish ? 2.5 : 0.0);
-        if (!found || cost < best) {
-            best = cost;
-            q.publish = publish;
-            p = q;
-            found = true;
+        q.sc.tg = 1;
+        return q;
+    };
+    auto publishes = [](const Plan& q) {
+        if (!q.sc.tile_major && q.sc.U > 1) return true;
+        for (int c = 1; c < q.sc.G; ++c)
+            if (q.sc.tile_of(q.sc.first(c)) == q.sc.tile_of(q.sc.first(c) - 1)) return true;
+        return false;
+    };
+    bool found = false;
+    double best = 0.0;
+    if (rb_req <= 0 && order != 2)
+        for (int64_t G : cands) {
+            if (G <= 0) continue;
+            Plan q = base(G);
+            if (!fit_resident(uk, bfu, M, ns_req, q)) continue;
+            q.publish = publishes(q);
+            const double cost = static_cast<double>((items + G - 1) / G) + (q.publish ? 2.5 : 0.0);
+            if (!found || cost < best) {
+                best = cost;
+                p = q;
+                found = true;
+            }
+        }
+    if (found) return true;
+    if (rb_req <= 0 && order != 1 && T > 1 && U > 1) {
+        for (int64_t tg : {2, 4, 8, 16, 32, 64, 128}) {
+            Plan q = base(G0);
+            q.sc.tile_major = 0;
+            q.sc.tg = static_cast<int>(std::min<int64_t>(tg, T));
+            if (fit_resident(uk, bfu, M, ns_req, q)) {
+                q.publish = publishes(q);
+                p = q;
+                return true;
+            }
+            if (tg >= T) break;
         }
     }
-    return found;
+    Plan q = base(G0);
+    if (!fit_stream(uk, bfu, M, nb, ns_req, rb_req, q)) return false;
+    q.publish = publishes(q);
+    p = q;
+    return true;
 }
 
-// Environment override PNQ_PN_CFG="tpw,grid,rb,ns" (fields 0 = automatic), read once.
+// Environment override PNQ_PN_CFG="tpw,grid,rb,ns,order" (fields 0 = automatic), read once.
 MmaConfig env_config() {
     static MmaConfig cfg = [] {
-        MmaConfig c{0, 0, 0, 0};
+        MmaConfig c{0, 0, 0, 0, 0};
         if (const char* s = std::getenv("PNQ_PN_CFG")) {
-            int v[4] = {0, 0, 0, 0};
+            int v[5] = {0, 0, 0, 0, 0};
             int n = 0;
             const char* p = s;
-            while (*p && n < 4) {
+            while (*p && n < 5) {
                 v[n++] = static_cast<int>(std::strtol(p, const_cast<char**>(&p), 10));
                 if (*p == ',') ++p;
             }
-            c = MmaConfig{v[0], v[1], v[2], v[3]};
+            c = MmaConfig{v[0], v[1], v[2], v[3], v[4]};
         }
         return c;
     }();
@@ -747,7 +816,7 @@ cudaError_t launch_cfg(PnArgs& a, const MmaConfig& cfg, bool static_weights, cud
     using C = Cfg<TYPE, NT, TPW>;
     Plan p;
     const int cap = cfg.grid > 0 ? std::min(cfg.grid, device_sm_count()) : device_sm_count();
-    if (!make_plan(C::UK, C::BFU, a.M, C::NB, a.sc.T, a.sc.U, cap, cfg.grid > 0, cfg.ns, cfg.rb, p))
+    if (!make_plan(C::UK, C::BFU, a.M, C::NB, a.sc.T, a.sc.U, cap, cfg.grid > 0, cfg.ns, cfg.rb, cfg.order, p))
         return cudaErrorNotSupported;
     auto kern = pn_gemv_kernel<TYPE, NT, TPW>;
     static bool opted[64] = {};
@@ -839,7 +908,7 @@ cudaError_t launch_pn_gemv_mma(int type, const uint8_t* W, int64_t N, int64_t K,
     a.sc.T = static_cast<int>(T);
     a.sc.U = static_cast<int>(U);
     a.sc.items = static_cast<int>(T * U);
-    const MmaConfig c = (cfg.tpw > 0 || cfg.grid > 0 || cfg.rb > 0 || cfg.ns > 0) ? cfg : env_config();
+    const MmaConfig c = (cfg.tpw > 0 || cfg.grid > 0 || cfg.rb > 0 || cfg.ns > 0 || cfg.order > 0) ? cfg : env_config();
     return (type == kTypePn3t) ? launch_typed<kTypePn3t>(a, c, static_weights, stream, ext)
                                : launch_typed<kTypePn4t>(a, c, static_weights, stream, ext);
 }

@@ -19,6 +19,8 @@ struct MmaConfig {
     int grid;  // CTAs (at most one per SM)
     int rb;    // operand ring slots
     int ns;    // weight pipeline stages
+    int order; // wide batches: 1 = tile-major items with streamed operands, 2 = grouped unit-major
+               // items with resident operands
 };
 
 // Workspace handed in by the caller (nullptr ws: the per-stream workspace is used).

@@ -34,25 +34,44 @@ constexpr int kBarriers = 2 * kMaxStages + 2 * 4 + 5;
 constexpr size_t kSmemLimit = 227u * 1024u;
 
 // Item numbering. Tile-major (item = t * U + u): a CTA's share covers one or two row tiles and
-// at most U units, and it accumulates a tile over consecutive items. Unit-major (item = u * T + t):
-// a CTA's share touches at most a few units (for operands that would not fit otherwise). CTA c
-// of G takes items [c * items / G, (c + 1) * items / G).
+// at most U units, and it accumulates a tile over consecutive items. Grouped unit-major: row
+// tiles in groups of tg (the last may be smaller), the groups one after another, inside a group
+// item = base + u * n + (t - t0) (n tiles from t0): a CTA's share touches few units (so the
+// operands of wide batches fit), every item of a group of n >= 2 tiles is a share of its own,
+// and the tiles complete group by group. CTA c of G takes items [c * items / G, (c+1) * items / G).
 struct Sched {
     int items;  // T * U < 2^31 (checked by the host)
-    int T, U, G, tile_major;
-    __host__ __device__ int tile_of(int i) const { return tile_major ? i / U : i % T; }
-    __host__ __device__ int unit_of(int i) const { return tile_major ? i % U : i / T; }
-    __host__ __device__ int item(int t, int u) const { return tile_major ? t * U + u : u * T + t; }
+    int T, U, G, tile_major, tg;
+    __host__ __device__ int group_items() const { return tg * U; }
+    __host__ __device__ int tile_of(int i) const {
+        if (tile_major) return i / U;
+        const int grp = i / group_items(), t0 = grp * tg, n = min(tg, T - t0);
+        return t0 + (i - grp * group_items()) % n;
+    }
+    __host__ __device__ int unit_of(int i) const {
+        if (tile_major) return i % U;
+        const int grp = i / group_items(), t0 = grp * tg, n = min(tg, T - t0);
+        return (i - grp * group_items()) / n;
+    }
+    __host__ __device__ int item(int t, int u) const {
+        if (tile_major) return t * U + u;
+        const int grp = t / tg, t0 = grp * tg, n = min(tg, T - t0);
+        return grp * group_items() + u * n + (t - t0);
+    }
     __host__ __device__ int first(int c) const { return static_cast<int>(static_cast<long long>(c) * items / G); }
     __host__ __device__ int owner(int i) const {
         return static_cast<int>((static_cast<long long>(i + 1) * G - 1) / items);
     }
-    // A share is a run of consecutive items of one CTA within a tile. Tile-major (or T = 1):
-    // the items of tile t are consecutive, a share starts at unit 0 and at the first item of
-    // every CTA that begins inside the tile. Unit-major: every unit is a share of its own.
-    __host__ __device__ bool consecutive() const { return tile_major || T == 1; }
+    // A share is a run of consecutive items of one CTA within a tile. When the items of tile t
+    // are consecutive (tile-major, or a group of one tile) a share starts at unit 0 and at the
+    // first item of every CTA that begins inside the tile; otherwise every unit is a share.
+    __host__ __device__ bool consecutive(int t) const {
+        if (tile_major) return true;
+        const int t0 = (t / tg) * tg;
+        return min(tg, T - t0) == 1;
+    }
     __host__ __device__ int shares(int t) const {
-        if (!consecutive()) return U;
+        if (!consecutive(t)) return U;
         const int a0 = item(t, 0);
         return owner(a0 + U - 1) - owner(a0) + 1;
     }
@@ -60,7 +79,11 @@ struct Sched {
     __host__ __device__ int span(int i0, int i1) const {
         if (i1 <= i0) return 0;
         if (tile_major) return i1 - i0 < U ? i1 - i0 : U;
-        return unit_of(i1 - 1) - unit_of(i0) + 1;
+        const int n_min = T % tg == 0 ? tg : min(tg, T % tg);  // the smallest group
+        if (i1 - i0 >= n_min * U) return U;
+        int d = unit_of(i1 - 1) - unit_of(i0);  // at most one group boundary in between
+        if (d < 0) d += U;
+        return d + 1;
     }
 };
 
@@ -84,9 +107,15 @@ __device__ __forceinline__ void next_item(const Sched& sc, int& t, int& u) {
             u = 0;
             ++t;
         }
-    } else if (++t == sc.T) {
-        t = 0;
-        ++u;
+        return;
+    }
+    const int t0 = (t / sc.tg) * sc.tg, t_end = min(t0 + sc.tg, sc.T);
+    if (++t == t_end) {
+        t = t0;
+        if (++u == sc.U) {  // next group
+            u = 0;
+            t = t_end;
+        }
     }
 }
 
@@ -143,19 +172,19 @@ __device__ __forceinline__ bool builder_loop(const SM& sm, const Sched& sc, int 
 }
 
 // Resident mode: the participating warps (index pw of npw) copy the x rows of the CTA's units
-// (copy(c) issues 16-byte chunk c of n_chunks) and then run every build job (job(i), i < n_jobs),
-// with a named barrier after each phase. Afterwards the x bytes may be overwritten by
-// tensor-map copies (generic-proxy reads ordered before them).
+// (copy(r) issues row r of n_rows, one warp per row) and then run every build job (job(i),
+// i < n_jobs), with a named barrier after each phase. With overlap the x bytes live in weight
+// stages that tensor-map copies overwrite next: the generic-proxy reads are fenced first.
 template <class CopyF, class JobF>
-__device__ __forceinline__ void resident_prologue(int pw, int npw, int lane, int n_chunks, int n_jobs, CopyF&& copy,
+__device__ __forceinline__ void resident_prologue(int pw, int npw, int n_rows, int n_jobs, bool overlap, CopyF&& copy,
                                                   JobF&& job) {
     griddep_wait();  // X belongs to the previous grid until now
-    for (int c = pw * 32 + lane; c < n_chunks; c += npw * 32) copy(c);
+    for (int r = pw; r < n_rows; r += npw) copy(r);
     cp_async_commit();
     cp_async_wait<0>();
     named_sync(1, npw * 32);
     for (int i = pw; i < n_jobs; i += npw) job(i);
-    fence_proxy_async_smem();
+    if (overlap) fence_proxy_async_smem();
     named_sync(1, npw * 32);
 }
 
@@ -246,7 +275,7 @@ __device__ __forceinline__ void count_shares(const Ctx& a, const SM& sm, int np,
 // (no other CTA reads it again in this one).
 __device__ __forceinline__ void finish_tile(const Ctx& a, int t, int m, int lane) {
     const Sched& sc = a.sc;
-    const bool consec = sc.consecutive();
+    const bool consec = sc.consecutive(t);
     const int a0 = sc.item(t, 0);
     const int c_lo = consec ? sc.owner(a0) : 0;
     const int n = consec ? sc.owner(a0 + sc.U - 1) - c_lo + 1 : sc.U;  // shares of the tile

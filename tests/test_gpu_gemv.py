@@ -199,11 +199,14 @@ print(json.dumps({{"ok": True, "device_error": pnq.device_error()}}))
 
 @pytest.mark.parametrize("pn_cfg,nv_cfg", [("1,0,0,0", "2,0,0,0"), ("2,0,0,0", "1,0,0,0"), ("1,7,0,2", "2,7,3,3"),
                                             ("2,13,3,3", "1,13,0,3"), ("1,152,0,8", "1,152,4,8"),
-                                            ("2,3,4,5", "2,3,2,5"), ("1,40,3,4", "1,40,0,4")])
+                                            ("2,3,4,5", "2,3,2,5"), ("1,40,3,4", "1,40,0,4"),
+                                            ("1,0,0,0,2", "1,0,0,0,2"), ("2,13,0,3,2", "2,40,0,0,2"),
+                                            ("1,0,0,0,1", "2,0,3,0,1")])
 def test_tile_and_grid_configs(pn_cfg, nv_cfg):
     """Forced configurations, read once per process (so each runs in a child): PN path through
     PNQ_PN_CFG, NVFP4 path through PNQ_NV_CFG, both "tiles per warp, grid size, operand slots,
-    stages" (small grids make CTAs span several K units and share row tiles)."""
+    stages, item order" (small grids make CTAs span several K units and share row tiles; order 2
+    = grouped unit-major items, operand slots > 0 = the streaming ring)."""
     env = dict(os.environ, PNQ_PN_CFG=pn_cfg, PNQ_NV_CFG=nv_cfg, PNQ_FORCE_KERNEL="mma")
     r = subprocess.run([sys.executable, "-c", CHILD.format(root=ROOT)], env=env, capture_output=True, text=True,
                        timeout=600)
