@@ -371,6 +371,22 @@ __device__ __forceinline__ uint32_t pack_half2(__half lo, __half hi) {
            (static_cast<uint32_t>(__half_as_ushort(hi)) << 16);
 }
 
+// Two floats -> f16x2 (low half = a), rounded to nearest even, in one conversion instruction.
+__device__ __forceinline__ uint32_t f32x2_to_f16x2(float a, float b) {
+    uint32_t d;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(b), "f"(a));
+    return d;
+}
+
+// v = hi + lo exactly, hi = v rounded to its leading 11 significant bits (Veltkamp's splitting
+// with the factor 2^13 + 1 for 24-bit floats; the operations must not be contracted), so that hi
+// is exact in fp16 for 2^-14 <= |hi| < 65520 and lo carries the remaining 13 bits.
+__device__ __forceinline__ void split11(float v, float& hi, float& lo) {
+    const float c = __fmul_rn(v, 8193.0f);
+    hi = __fsub_rn(c, __fsub_rn(c, v));
+    lo = __fsub_rn(v, hi);
+}
+
 // Byte i (0..3) of w as two E2M1 codes (low nibble first) -> f16x2 with the exact values.
 template <int I>
 __device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t w) {

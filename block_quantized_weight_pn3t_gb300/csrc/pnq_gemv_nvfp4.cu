@@ -104,8 +104,6 @@ struct NvSmem {
     __device__ int* finish() const { return reinterpret_cast<int*>(base + list_off) + 4 + list_cap; }
 };
 
-__device__ __forceinline__ float bf16_to_float(uint16_t h) { return __uint_as_float(static_cast<uint32_t>(h) << 16); }
-
 // Operands of activation row m for one K unit (one builder warp): sigma from the row's largest
 // |x| over the unit, the B fragments (column m) and g * 2^-sigma. xr = the row's 256 bf16 x
 // values in shared memory. Lane (P, c) = (lane / 4, lane % 4) builds the record of slices
@@ -133,9 +131,9 @@ __device__ __forceinline__ void nv_build_row(uint8_t* slot_b, float* slot_so, co
         const int S = 2 * P + (q4 >> 1), r = q4 & 1;
         const int half = S >> 3, q = (S >> 2) & 1, b = S & 3;
         const uint32_t pair = x32[4 * (16 * half + c + 8 * q + 4 * r) + b];
-        const float v0 = bf16_to_float(static_cast<uint16_t>(pair & 0xFFFFu)) * si;
-        const float v1 = bf16_to_float(static_cast<uint16_t>(pair >> 16)) * si;
-        v[q4] = pack_half2(__float2half_rn(v0), __float2half_rn(v1));
+        const float v0 = __uint_as_float(pair << 16) * si;          // low bf16
+        const float v1 = __uint_as_float(pair & 0xFFFF0000u) * si;  // high bf16
+        v[q4] = f32x2_to_f16x2(v0, v1);
     }
     uint8_t* tb = slot_b + (m >> 3) * 4096 + P * 512;
     *reinterpret_cast<uint4*>(tb + ((((m & 7) << 2) | c) * 16)) = make_uint4(v[0], v[1], v[2], v[3]);

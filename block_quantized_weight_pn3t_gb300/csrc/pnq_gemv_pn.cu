@@ -29,8 +29,9 @@
 // aligned words pairing the high half of word i-1 with the low half of word i (one PRMT).
 //
 // B operand (builder warps): x times 8^-j (16^-j) times 2^sigma (per K unit and activation row,
-// so that max|x| * 2^sigma lies in [2^14, 2^15)), split into fp16 hi + lo parts (~22 bits) that
-// take mma columns 2m and 2m + 1 (NT = ceil(2M / 8) n8 tiles), stored per block in register
+// so that max|x| * 2^sigma lies in [2^14, 2^15)), split into fp16 hi + lo parts (~22 bits: hi =
+// the leading 11 bits by Veltkamp's splitting, lo = the rest rounded to fp16) that take mma
+// columns 2m and 2m + 1 (NT = ceil(2M / 8) n8 tiles), stored per block in register
 // order. Beside them: Z = z * 2^(sigma - 24) * (sum of the block's x), and 2^(24 - sigma).
 //
 // Block scale and zero point: per item a_m = sum over its blocks of d * (c - Z); the tile's row
@@ -259,10 +260,11 @@ __device__ __forceinline__ void build_row(uint8_t* slot_b, float* slot_z, float*
                     const float x0 = xb[L.off[q][0]], x1 = xb[L.off[q][1]];
                     zs += x0;
                     zs += x1;
-                    const float v0 = x0 * sc[q], v1 = x1 * sc[q];
-                    const __half h0 = __float2half_rn(v0), h1 = __float2half_rn(v1);
-                    hi[q] = pack_half2(h0, h1);
-                    lo[q] = pack_half2(__float2half_rn(v0 - __half2float(h0)), __float2half_rn(v1 - __half2float(h1)));
+                    float h0, h1, l0, l1;
+                    split11(x0 * sc[q], h0, l0);
+                    split11(x1 * sc[q], h1, l1);
+                    hi[q] = f32x2_to_f16x2(h0, h1);  // exact
+                    lo[q] = f32x2_to_f16x2(l0, l1);
                 }
             }
             uint8_t* tb = slot_b + blk * BFU + (n >> 3) * 256 * STEPS + L.pr * 512;
