@@ -119,7 +119,7 @@ class ClockSampler:
 
 def kernel_source_digest():
     h = hashlib.sha256()
-    for fn in ("pnq_gemv_pn.cu", "pnq_device.cuh"):
+    for fn in ("pnq_gemv_pn.cu", "pnq_streamk.cuh", "pnq_device.cuh"):
         with open(os.path.join(ROOT, "block_quantized_weight_pn3t_gb300", "csrc", fn), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
