@@ -314,6 +314,15 @@ __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
+// atomicAdd with acquire-release semantics at GPU scope: the writes that happen before it (in
+// this thread, or in threads ordered before it by a barrier) are visible to whoever observes the
+// new value, and this thread's later reads see what the earlier incrementers wrote before theirs.
+__device__ __forceinline__ uint32_t atomic_add_acq_rel(uint32_t* p, uint32_t v) {
+    uint32_t old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
 // Named barrier that also ANDs a predicate over the participating threads: every thread gets
 // the same answer, so all of them take the same branch afterwards.
 __device__ __forceinline__ bool named_sync_and(uint32_t id, uint32_t threads, bool pred) {

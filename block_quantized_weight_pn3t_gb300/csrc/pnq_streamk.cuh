@@ -247,8 +247,7 @@ __device__ __forceinline__ bool reduce_share(const Ctx& a, const SM& sm, int buf
 // the ones that complete their tile are appended to finish[] (n_finish[0] entries). One warp.
 template <class SM>
 __device__ __forceinline__ void count_shares(const Ctx& a, const SM& sm, int np, int lane) {
-    __threadfence();  // the slots are visible before they are counted
-    __syncwarp();
+    __syncwarp();  // every lane's slot stores come before the (releasing) counts
     int* pend = sm.pending();
     int* fin = sm.finish();
     for (int k0 = 0; k0 < np; k0 += 32) {
@@ -257,7 +256,7 @@ __device__ __forceinline__ void count_shares(const Ctx& a, const SM& sm, int np,
         int t = 0;
         if (k < np) {
             t = pend[k];
-            last = atomicAdd(a.cnt + t, 1u) == static_cast<unsigned>(a.sc.shares(t) - 1);
+            last = atomic_add_acq_rel(a.cnt + t, 1u) == static_cast<unsigned>(a.sc.shares(t) - 1);
         }
         const unsigned mask = __ballot_sync(0xffffffffu, last);
         const int base = *sm.n_finish();
@@ -266,7 +265,8 @@ __device__ __forceinline__ void count_shares(const Ctx& a, const SM& sm, int np,
         if (lane == 0) *sm.n_finish() = base + __popc(mask);
         __syncwarp();
     }
-    __threadfence();  // what the other CTAs stored before counting is seen by the finishers
+    // the finishers read the other CTAs' slots after the CTA barrier that follows: the acquiring
+    // count that completed the tile orders those reads after the other CTAs' releasing counts
 }
 
 // Sum the shares of tile t for activation row m in unit order into Y (one warp). The slot
