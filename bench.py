@@ -361,7 +361,7 @@ def run_ours(args):
                        "graph": "one CUDA graph per step, 448 pnq_gemv launches", "parallelism": f"replicas x{world}"},
             "roofline": {"bound": "hbm", "achieved": round(dom_gbs, 2), "peak": peak, "unit": "GB/s",
                          "frac": round(dom_gbs / peak, 4), "traffic": traffic,
-                         "kernel": "pn_gemv_kernel<pn3t, NT=1>", "launches": len(dom),
+                         "kernel": f"pn_gemv_kernel<pn3t, NT={min(4, 1 << ((2 * M + 7) // 8 - 1).bit_length())}>", "launches": len(dom),
                          "algorithmic_bytes_per_launch": round(dom_bytes / len(dom)),
                          "avg_launch_us": round(sum(dur_ms) / len(dur_ms) * 1e3, 3),
                          "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({peak_kind})"},
