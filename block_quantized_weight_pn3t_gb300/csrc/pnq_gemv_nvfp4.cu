@@ -66,6 +66,7 @@ struct NvArgs {
     Sched sc;
     int N, K, M, NS, RB, XB;
     int x_stage;     // resident mode with x in the weight stages: the first stage holding x
+    int pf;          // static weights: stages requested before griddepcontrol.wait
     unsigned flags;  // kStaticWeights, kResident, kXOverlap
     float g;
     uint32_t list_off, part_off, xs_off, ring_off, stage_off, slot_bytes;
@@ -357,7 +358,7 @@ __global__ void __launch_bounds__(NvCfg<NT, TPW>::THREADS, 1) nvfp4_gemv_kernel(
             if (cx.flags & kStaticWeights) {
                 // the weights are not written by earlier work in the stream: fill the stages
                 // (those not holding x) before the previous grid completes
-                for (; ok && gi < min(n_items, x_stage); ++gi) ok = issue(gi);
+                for (; ok && gi < min(n_items, min(x_stage, a.pf)); ++gi) ok = issue(gi);
             }
             griddep_wait();  // without the static-weights flag W may be written by the previous grid
             for (; ok && gi < n_items; ++gi) ok = issue(gi);
@@ -413,12 +414,13 @@ __global__ void __launch_bounds__(NvCfg<NT, TPW>::THREADS, 1) nvfp4_gemv_kernel(
                 cp_async16(smem_addr(sm.xs(k) + m * kUnitK) + 16u * lane,
                            a.X + static_cast<size_t>(m) * cx.K + static_cast<size_t>(u) * kUnitK + 8 * lane);
             };
+            const bool overlap = (a.flags & kXOverlap) != 0;
             auto job = [&](int i) {
                 const int k = i / M, m = i - k * M;
                 nv_build_row<NT>(sm.slot(k), sm.slot_so<NT>(k), sm.xs(k) + m * kUnitK, m, a.g, lane);
             };
-            resident_prologue(pw, C::CW + C::NB, span * M, span * M, (a.flags & kXOverlap) != 0, copy, job);
-            if (threadIdx.x == 0 && (a.flags & kXOverlap)) mbar_arrive(sm.x_free());
+            resident_prologue(pw, C::CW + C::NB, span * M, span * M, overlap, copy, job);
+            if (threadIdx.x == 0 && overlap) mbar_arrive(sm.x_free());
             if (warp < C::TG)
                 nv_consumer_loop<NT, TPW, 0>(sm, cx, i0, n_items);
             else if (warp < C::CW)
@@ -476,16 +478,16 @@ struct NvPlan {
 };
 
 // Barriers, lists and row sums at the start; returns the first free (128-aligned) offset.
-uint32_t nv_head_layout(int bfu, int M, NvPlan& p) {
+uint32_t nv_head_layout(int bfu, int M, int NS, int RB, NvPlan& p) {
     p.list_cap = (p.sc.items + p.sc.G - 1) / p.sc.G;
-    p.list_off = align_up(8u * kBarriers, 16);
+    p.list_off = align_up(8u * (2u * NS + 2u * RB + 5u), 16);  // full, empty, op_full, op_empty, part x 4, x_free
     p.part_off = align_up(p.list_off + (2u * p.list_cap + 4u) * 4u, 16);
     p.slot_bytes = align_up(static_cast<uint32_t>(bfu) + 64u, 128);
     return align_up(p.part_off + 4u * M * kPartPitch * 4u, 128);
 }
 
 bool nv_layout(int bfu, int M, int NS, int RB, int XB, NvPlan& p) {
-    p.xs_off = nv_head_layout(bfu, M, p);
+    p.xs_off = nv_head_layout(bfu, M, NS, RB, p);
     p.ring_off = align_up(p.xs_off + static_cast<uint32_t>(XB) * M * kUnitK * 2u, 128);
     p.stage_off = align_up(p.ring_off + static_cast<uint32_t>(RB) * p.slot_bytes, 1024);
     const uint64_t total = p.stage_off + static_cast<uint64_t>(NS) * kStageBytes;
@@ -503,7 +505,7 @@ bool nv_layout(int bfu, int M, int NS, int RB, int XB, NvPlan& p) {
 bool nv_layout_resident(int bfu, int M, int NS, bool overlap, NvPlan& p) {
     int span = 0;
     for (int c = 0; c < p.sc.G; ++c) span = std::max(span, p.sc.span(p.sc.first(c), p.sc.first(c + 1)));
-    uint64_t off = nv_head_layout(bfu, M, p);
+    uint64_t off = nv_head_layout(bfu, M, NS, 0, p);
     const uint64_t xbytes = static_cast<uint64_t>(span) * M * kUnitK * 2u;
     if (!overlap) {
         p.xs_off = static_cast<uint32_t>(off);
@@ -612,19 +614,19 @@ bool nv_plan(int bfu, int M, int64_t T, int64_t U, int sms, bool grid_forced, in
     return true;
 }
 
-// Environment override PNQ_NV_CFG="tpw,grid,rb,ns,order" (fields 0 = automatic), read once.
+// Environment override PNQ_NV_CFG="tpw,grid,rb,ns,order,pf" (fields 0 = automatic), read once.
 MmaConfig nv_env_config() {
     static MmaConfig cfg = [] {
-        MmaConfig c{0, 0, 0, 0, 0};
+        MmaConfig c{0, 0, 0, 0, 0, 0};
         if (const char* s = std::getenv("PNQ_NV_CFG")) {
-            int v[5] = {0, 0, 0, 0, 0};
+            int v[6] = {0, 0, 0, 0, 0, 0};
             int n = 0;
             const char* p = s;
-            while (*p && n < 5) {
+            while (*p && n < 6) {
                 v[n++] = static_cast<int>(std::strtol(p, const_cast<char**>(&p), 10));
                 if (*p == ',') ++p;
             }
-            c = MmaConfig{v[0], v[1], v[2], v[3], v[4]};
+            c = MmaConfig{v[0], v[1], v[2], v[3], v[4], v[5]};
         }
         return c;
     }();
@@ -666,6 +668,7 @@ cudaError_t nv_launch_cfg(NvArgs& a, const MmaConfig& cfg, bool static_weights, 
     a.XB = p.XB;
     a.flags = (static_weights ? kStaticWeights : 0u) | p.mode;
     a.x_stage = p.x_stage;
+    a.pf = cfg.pf > 0 ? cfg.pf : p.NS;
     a.list_off = p.list_off;
     a.list_cap = p.list_cap;
     a.part_off = p.part_off;
@@ -718,6 +721,7 @@ cudaError_t launch_nvfp4_gemv_mma(const Nvfp4View& w, int64_t N, int64_t K, cons
     if (cfg.rb <= 0) cfg.rb = env.rb;
     if (cfg.ns <= 0) cfg.ns = env.ns;
     if (cfg.order <= 0) cfg.order = env.order;
+    if (cfg.pf <= 0) cfg.pf = env.pf;
     const int nt = (M + 7) / 8;
     const int tpw = cfg.tpw > 0 ? cfg.tpw : (nt == 1 ? 1 : 2);
     if (nt == 1) return tpw == 1 ? nv_launch_cfg<1, 1>(a, cfg, static_weights, stream, ext)

@@ -68,7 +68,10 @@ struct Cfg {
     static constexpr int NB = (TPW == 1 || NT >= 4) ? 2 : 6;  // builder warps (within the register budget)
     static constexpr int PRODUCER = CW, REDUCER = CW + 1, BUILDER = CW + 2;
     static constexpr int THREADS = 32 * (CW + 2 + NB);
-    static constexpr int BFU = NT * 256 * STEPS;   // fragment bytes per block
+    // B records: per block, n8 tile and pair of slices a group of `lg` 16-byte lane records; all
+    // 32 lanes with several tiles, only the lanes of columns < 2M (lg = 8M) with one
+    static __host__ __device__ int lg(int M) { return NT == 1 ? (8 * M < 32 ? 8 * M : 32) : 32; }
+    static __host__ __device__ int bfu(int M) { return NT * STEPS * lg(M) * 8; }  // bytes per block
 };
 
 struct PnArgs {
@@ -81,6 +84,7 @@ struct PnArgs {
     Sched sc;
     int N, K, M, NS, RB, XB;
     int x_stage;     // resident mode with x in the weight stages: the first stage holding x
+    int pf;          // static weights: stages requested before griddepcontrol.wait
     unsigned flags;  // kStaticWeights, kResident, kXOverlap
     uint32_t list_off, part_off, xs_off, ring_off, stage_off, slot_bytes;
     int list_cap;
@@ -157,18 +161,18 @@ struct Smem {
 };
 
 // B fragments of one block for every n8 tile: lanes whose column is in use load their records,
-// the others hold zeros.
+// the others hold zeros. rs = bytes of a record group (lg * 16).
 template <int TYPE, int NT>
-__device__ __forceinline__ void load_bfrag(const uint8_t* bf, int lane, const bool (&live)[NT],
+__device__ __forceinline__ void load_bfrag(const uint8_t* bf, int lane, const bool (&live)[NT], int rs,
                                            uint32_t (&b)[NT][PnFmt<TYPE>::PAIRS][2]) {
     constexpr int STEPS = PnFmt<TYPE>::PAIRS;
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
-        const uint8_t* base = bf + t * 256 * STEPS;
+        const uint8_t* base = bf + t * (rs / 2) * STEPS;
 #pragma unroll
         for (int q = 0; q < STEPS / 2; ++q) {
             uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            if (live[t]) v = *reinterpret_cast<const uint4*>(base + q * 512 + lane * 16);
+            if (live[t]) v = *reinterpret_cast<const uint4*>(base + q * rs + lane * 16);
             b[t][2 * q][0] = v.x;
             b[t][2 * q][1] = v.y;
             b[t][2 * q + 1][0] = v.z;
@@ -176,7 +180,7 @@ __device__ __forceinline__ void load_bfrag(const uint8_t* bf, int lane, const bo
         }
         if constexpr (STEPS & 1) {
             uint2 v = make_uint2(0u, 0u);
-            if (live[t]) v = *reinterpret_cast<const uint2*>(base + (STEPS / 2) * 512 + lane * 8);
+            if (live[t]) v = *reinterpret_cast<const uint2*>(base + (STEPS / 2) * rs + lane * 8);
             b[t][STEPS - 1][0] = v.x;
             b[t][STEPS - 1][1] = v.y;
         }
@@ -222,12 +226,12 @@ struct BuildLane {
 // memory.
 template <int TYPE, int NT, int NBLK>
 __device__ __forceinline__ void build_row(uint8_t* slot_b, float* slot_z, float* slot_so, const float* xr, int m,
-                                          int M, int blk0, int lane, const BuildLane<TYPE>& L) {
+                                          int M, int blk0, int lane, const BuildLane<TYPE>& L, int rs) {
     using F = PnFmt<TYPE>;
     using BL = BuildLane<TYPE>;
     constexpr int STEPS = F::PAIRS;
     constexpr int UK = kUnitBlocks * F::BLK;
-    constexpr int BFU = NT * 256 * STEPS;
+    const int ts = (rs / 2) * STEPS, bfu = NT * ts;  // bytes per n8 tile and per block
     uint32_t mx = 0;  // a non-negative float's bits order like its value
 #pragma unroll
     for (int q = lane; q < UK / 4; q += 32) {
@@ -267,7 +271,7 @@ __device__ __forceinline__ void build_row(uint8_t* slot_b, float* slot_z, float*
                     lo[q] = f32x2_to_f16x2(l0, l1);
                 }
             }
-            uint8_t* tb = slot_b + blk * BFU + (n >> 3) * 256 * STEPS + L.pr * 512;
+            uint8_t* tb = slot_b + blk * bfu + (n >> 3) * ts + L.pr * rs;
             if (single) {
                 *reinterpret_cast<uint2*>(tb + lh * 8) = make_uint2(hi[0], hi[1]);
                 *reinterpret_cast<uint2*>(tb + ll * 8) = make_uint2(lo[0], lo[1]);
@@ -288,15 +292,15 @@ __device__ __forceinline__ void build_row(uint8_t* slot_b, float* slot_z, float*
 // d * (c - Z) into acc[tile][t][row half] (the item's sums, before 2^(24 - sigma)).
 template <int TYPE, int NT, int TPW, int B>
 __device__ __forceinline__ void pn_block(const uint8_t* const (&row0)[TPW], int tig, uint32_t sel,
-                                         const uint8_t* bf, int lane, const bool (&live)[NT], const float* zb, int M,
-                                         float (&acc)[TPW][NT][2]) {
+                                         const uint8_t* bf, int lane, const bool (&live)[NT], int rs, const float* zb,
+                                         int M, float (&acc)[TPW][NT][2]) {
     using F = PnFmt<TYPE>;
     constexpr int STEPS = F::PAIRS;
     constexpr int OFF = kBlockBytes * B;
     constexpr int SH = (TYPE == kTypePn3t) ? 9 : 8;
     // B fragments (columns past 2M are zero and are not read)
     uint32_t b[NT][STEPS][2];
-    load_bfrag<TYPE, NT>(bf, lane, live, b);
+    load_bfrag<TYPE, NT>(bf, lane, live, rs, b);
     float zt[NT];
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
@@ -358,6 +362,7 @@ __device__ __forceinline__ void consumer_loop(const Smem& sm, const Ctx& cx, int
     const int g = lane >> 2, tig = lane & 3;
     const int tg = warp % C::TG;  // tile group: rows 16 * TPW * tg ..
     const uint32_t sel = (tig == 0) ? 0x5432u : 0x3210u;  // even blocks: register 0 pairs words 0 and 7
+    const int rs = C::lg(M) * 16, bfu = C::bfu(M);  // record group and block fragment bytes
     bool live[NT];
 #pragma unroll
     for (int t = 0; t < NT; ++t) live[t] = (8 * t + g) < 2 * M;
@@ -417,17 +422,21 @@ __device__ __forceinline__ void consumer_loop(const Smem& sm, const Ctx& cx, int
 #pragma unroll
         for (int tp = 0; tp < TPW; ++tp) row0[tp] = stage + (16 * (TPW * tg + tp) + g) * kUnitBytes;
         const int os = resident ? ((u_i >= u0) ? u_i - u0 : u_i - u0 + U) : r % RB;
-        const uint8_t* bf0 = sm.slot(os) + kHalfBlocks * H * C::BFU;
+        const uint8_t* bf0 = sm.slot(os) + kHalfBlocks * H * bfu;
         const float* z0 = sm.slot_z(os) + kHalfBlocks * H * M;
         float ai[TPW][NT][2];
 #pragma unroll
         for (int tp = 0; tp < TPW; ++tp)
 #pragma unroll
             for (int t = 0; t < NT; ++t) ai[tp][t][0] = ai[tp][t][1] = 0.0f;
-        pn_block<TYPE, NT, TPW, kHalfBlocks * H + 0>(row0, tig, sel, bf0 + 0 * C::BFU, lane, live, z0 + 0 * M, M, ai);
-        pn_block<TYPE, NT, TPW, kHalfBlocks * H + 1>(row0, tig, sel, bf0 + 1 * C::BFU, lane, live, z0 + 1 * M, M, ai);
-        pn_block<TYPE, NT, TPW, kHalfBlocks * H + 2>(row0, tig, sel, bf0 + 2 * C::BFU, lane, live, z0 + 2 * M, M, ai);
-        pn_block<TYPE, NT, TPW, kHalfBlocks * H + 3>(row0, tig, sel, bf0 + 3 * C::BFU, lane, live, z0 + 3 * M, M, ai);
+        pn_block<TYPE, NT, TPW, kHalfBlocks * H + 0>(row0, tig, sel, bf0 + 0 * bfu, lane, live, rs, z0 + 0 * M, M,
+                                                     ai);
+        pn_block<TYPE, NT, TPW, kHalfBlocks * H + 1>(row0, tig, sel, bf0 + 1 * bfu, lane, live, rs, z0 + 1 * M, M,
+                                                     ai);
+        pn_block<TYPE, NT, TPW, kHalfBlocks * H + 2>(row0, tig, sel, bf0 + 2 * bfu, lane, live, rs, z0 + 2 * M, M,
+                                                     ai);
+        pn_block<TYPE, NT, TPW, kHalfBlocks * H + 3>(row0, tig, sel, bf0 + 3 * bfu, lane, live, rs, z0 + 3 * M, M,
+                                                     ai);
         __syncwarp();
         if (lane == 0) mbar_arrive(sm.empty(s));
         // the item's sums times 2^(24 - sigma) of its unit
@@ -457,7 +466,7 @@ __global__ void __launch_bounds__(Cfg<TYPE, NT, TPW>::THREADS, 1) pn_gemv_kernel
     const int parts = (a.M < C::NB) ? 2 : 1;
     const Smem sm{base,         smem_addr(base), a.NS,       a.RB,         a.M,           UK,
                   a.list_off,   a.part_off,      a.xs_off,   a.ring_off,   a.stage_off,   a.slot_bytes,
-                  static_cast<uint32_t>(kUnitBlocks * C::BFU), a.list_cap, a.M * parts};
+                  static_cast<uint32_t>(kUnitBlocks * C::bfu(a.M)), a.list_cap, a.M * parts};
     const Ctx cx{a.sc, a.X, a.Y, a.ws, a.cnt, a.err, a.N, a.K, a.M, a.NS, a.RB, a.flags};
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -509,7 +518,7 @@ __global__ void __launch_bounds__(Cfg<TYPE, NT, TPW>::THREADS, 1) pn_gemv_kernel
             if (cx.flags & kStaticWeights) {
                 // the weights are not written by earlier work in the stream: fill the stages
                 // (those not holding x) before the previous grid completes
-                for (; ok && gi < min(n_items, x_stage); ++gi) ok = issue(gi);
+                for (; ok && gi < min(n_items, min(x_stage, a.pf)); ++gi) ok = issue(gi);
             }
             griddep_wait();  // without the static-weights flag W may be written by the previous grid
             for (; ok && gi < n_items; ++gi) ok = issue(gi);
@@ -552,7 +561,9 @@ __global__ void __launch_bounds__(Cfg<TYPE, NT, TPW>::THREADS, 1) pn_gemv_kernel
         }
     } else if (a.flags & kResident) {
         // ---------------- resident operands: consumers and builders build all units' ----------------
-        // (unit slot k = unit u0 + k mod U; jobs = (slot, row, block half))
+        // (unit slot k = unit u0 + k mod U; jobs = (slot, row, block half)). Building only the
+        // first unit here and the rest in the builder warps behind the consumers measured slower:
+        // the prologue is mostly the x copy's latency, and two builder warps slow every item.
         if (n_items > 0) {
             const int u0 = sc.unit_of(i0);
             const int span = sc.span(i0, i1);
@@ -571,14 +582,16 @@ __global__ void __launch_bounds__(Cfg<TYPE, NT, TPW>::THREADS, 1) pn_gemv_kernel
                 for (int q = lane; q < CH; q += 32) cp_async16(dst + 16u * q, src + 4 * q);
             };
             const BuildLane<TYPE> bl(lane);
+            const int rs = C::lg(M) * 16;
+            const bool overlap = (a.flags & kXOverlap) != 0;
             auto job = [&](int i) {
                 const int k = i / (2 * M), j = i - k * 2 * M;
                 const int m = j >> 1, h = j & 1;
                 build_row<TYPE, NT, 4>(sm.slot(k), sm.slot_z(k), sm.slot_so(k), xs + static_cast<size_t>(k * M + m) * UK,
-                                       m, M, 4 * h, lane, bl);
+                                       m, M, 4 * h, lane, bl, rs);
             };
-            resident_prologue(pw, C::CW + C::NB, span * M, span * M * 2, (a.flags & kXOverlap) != 0, copy, job);
-            if (threadIdx.x == 0 && (a.flags & kXOverlap)) mbar_arrive(sm.x_free());
+            resident_prologue(pw, C::CW + C::NB, span * M, span * M * 2, overlap, copy, job);
+            if (threadIdx.x == 0 && overlap) mbar_arrive(sm.x_free());
             if (warp < C::TG)
                 consumer_loop<TYPE, NT, TPW, 0>(sm, cx, i0, n_items);
             else if (warp < C::CW)
@@ -605,10 +618,10 @@ __global__ void __launch_bounds__(Cfg<TYPE, NT, TPW>::THREADS, 1) pn_gemv_kernel
                 for (int j = b; j < sm.J; j += C::NB) {
                     if (parts == 2)
                         build_row<TYPE, NT, 4>(sm.slot(slot), sm.slot_z(slot), sm.slot_so(slot), xb + j * UK, j >> 1,
-                                               cx.M, 4 * (j & 1), lane, bl);
+                                               cx.M, 4 * (j & 1), lane, bl, C::lg(cx.M) * 16);
                     else
                         build_row<TYPE, NT, 8>(sm.slot(slot), sm.slot_z(slot), sm.slot_so(slot), xb + j * UK, j, cx.M,
-                                               0, lane, bl);
+                                               0, lane, bl, C::lg(cx.M) * 16);
                 }
             };
             bool ok;
@@ -636,7 +649,7 @@ __global__ void __launch_bounds__(Cfg<TYPE, NT, TPW>::THREADS, 1) pn_gemv_kernel
 
 // ---- host side --------------------------------------------------------------------------------------
 
-constexpr int kDefaultStages = 4;
+constexpr int kDefaultStages = 3;
 
 struct Plan {
     Sched sc{};
@@ -647,9 +660,9 @@ struct Plan {
 };
 
 // Barriers, lists and row sums at the start; returns the first free (128-aligned) offset.
-uint32_t head_layout(int bfu, int M, Plan& p) {
+uint32_t head_layout(int bfu, int M, int NS, int RB, Plan& p) {
     p.list_cap = (p.sc.items + p.sc.G - 1) / p.sc.G;
-    p.list_off = align_up(8u * kBarriers, 16);
+    p.list_off = align_up(8u * (2u * NS + 2u * RB + 5u), 16);  // full, empty, op_full, op_empty, part x 4, x_free
     p.part_off = align_up(p.list_off + (2u * p.list_cap + 4u) * 4u, 16);
     p.slot_bytes = align_up(kUnitBlocks * static_cast<uint32_t>(bfu) + (kUnitBlocks + 1u) * M * 4u, 128);
     return align_up(p.part_off + 4u * M * kPartPitch * 4u, 128);
@@ -657,7 +670,7 @@ uint32_t head_layout(int bfu, int M, Plan& p) {
 
 // Streaming layout: NS weight stages, RB operand slots and XB x buffers; false when it does not fit.
 bool layout(int uk, int bfu, int M, int nb, int NS, int RB, int XB, Plan& p) {
-    p.xs_off = head_layout(bfu, M, p);
+    p.xs_off = head_layout(bfu, M, NS, RB, p);
     const uint32_t jobs = static_cast<uint32_t>(M) * (M < nb ? 2u : 1u);  // x rows per buffer
     p.ring_off = align_up(p.xs_off + static_cast<uint32_t>(XB) * jobs * uk * 4u, 128);
     p.stage_off = align_up(p.ring_off + static_cast<uint32_t>(RB) * p.slot_bytes, 1024);
@@ -676,7 +689,7 @@ bool layout(int uk, int bfu, int M, int nb, int NS, int RB, int XB, Plan& p) {
 bool layout_resident(int uk, int bfu, int M, int NS, bool overlap, Plan& p) {
     int span = 0;
     for (int c = 0; c < p.sc.G; ++c) span = std::max(span, p.sc.span(p.sc.first(c), p.sc.first(c + 1)));
-    uint64_t off = head_layout(bfu, M, p);
+    uint64_t off = head_layout(bfu, M, NS, 0, p);
     const uint64_t xbytes = static_cast<uint64_t>(span) * M * uk * 4u;
     if (!overlap) {
         p.xs_off = static_cast<uint32_t>(off);
@@ -793,19 +806,19 @@ bool make_plan(int uk, int bfu, int M, int nb, int64_t T, int64_t U, int sms, bo
     return true;
 }
 
-// Environment override PNQ_PN_CFG="tpw,grid,rb,ns,order" (fields 0 = automatic), read once.
+// Environment override PNQ_PN_CFG="tpw,grid,rb,ns,order,pf" (fields 0 = automatic), read once.
 MmaConfig env_config() {
     static MmaConfig cfg = [] {
-        MmaConfig c{0, 0, 0, 0, 0};
+        MmaConfig c{0, 0, 0, 0, 0, 0};
         if (const char* s = std::getenv("PNQ_PN_CFG")) {
-            int v[5] = {0, 0, 0, 0, 0};
+            int v[6] = {0, 0, 0, 0, 0, 0};
             int n = 0;
             const char* p = s;
-            while (*p && n < 5) {
+            while (*p && n < 6) {
                 v[n++] = static_cast<int>(std::strtol(p, const_cast<char**>(&p), 10));
                 if (*p == ',') ++p;
             }
-            c = MmaConfig{v[0], v[1], v[2], v[3], v[4]};
+            c = MmaConfig{v[0], v[1], v[2], v[3], v[4], v[5]};
         }
         return c;
     }();
@@ -818,7 +831,7 @@ cudaError_t launch_cfg(PnArgs& a, const MmaConfig& cfg, bool static_weights, cud
     using C = Cfg<TYPE, NT, TPW>;
     Plan p;
     const int cap = cfg.grid > 0 ? std::min(cfg.grid, device_sm_count()) : device_sm_count();
-    if (!make_plan(C::UK, C::BFU, a.M, C::NB, a.sc.T, a.sc.U, cap, cfg.grid > 0, cfg.ns, cfg.rb, cfg.order, p))
+    if (!make_plan(C::UK, C::bfu(a.M), a.M, C::NB, a.sc.T, a.sc.U, cap, cfg.grid > 0, cfg.ns, cfg.rb, cfg.order, p))
         return cudaErrorNotSupported;
     auto kern = pn_gemv_kernel<TYPE, NT, TPW>;
     static bool opted[64] = {};
@@ -848,6 +861,7 @@ cudaError_t launch_cfg(PnArgs& a, const MmaConfig& cfg, bool static_weights, cud
     a.XB = p.XB;
     a.flags = (static_weights ? kStaticWeights : 0u) | p.mode;
     a.x_stage = p.x_stage;
+    a.pf = cfg.pf > 0 ? cfg.pf : p.NS;
     a.list_off = p.list_off;
     a.list_cap = p.list_cap;
     a.part_off = p.part_off;
@@ -910,7 +924,8 @@ cudaError_t launch_pn_gemv_mma(int type, const uint8_t* W, int64_t N, int64_t K,
     a.sc.T = static_cast<int>(T);
     a.sc.U = static_cast<int>(U);
     a.sc.items = static_cast<int>(T * U);
-    const MmaConfig c = (cfg.tpw > 0 || cfg.grid > 0 || cfg.rb > 0 || cfg.ns > 0 || cfg.order > 0) ? cfg : env_config();
+    const MmaConfig c =
+        (cfg.tpw > 0 || cfg.grid > 0 || cfg.rb > 0 || cfg.ns > 0 || cfg.order > 0 || cfg.pf > 0) ? cfg : env_config();
     return (type == kTypePn3t) ? launch_typed<kTypePn3t>(a, c, static_weights, stream, ext)
                                : launch_typed<kTypePn4t>(a, c, static_weights, stream, ext);
 }

@@ -21,6 +21,7 @@ struct MmaConfig {
     int ns;    // weight pipeline stages
     int order; // wide batches: 1 = tile-major items with streamed operands, 2 = grouped unit-major
                // items with resident operands
+    int pf;    // static weights: stages requested before the previous grid completes (0 = all)
 };
 
 // Workspace handed in by the caller (nullptr ws: the per-stream workspace is used).

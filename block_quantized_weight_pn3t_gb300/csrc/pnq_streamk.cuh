@@ -28,9 +28,6 @@ constexpr int kMaxStages = 8;
 constexpr unsigned kStaticWeights = 1u;
 constexpr unsigned kResident = 2u;  // operands of the whole share built in the prologue
 constexpr unsigned kXOverlap = 4u;  // ... from x held in the last weight stages until then
-// barriers: full / empty per stage, op_full / op_empty per ring slot (<= 4), part_full / part_free
-// (2 each), x_free
-constexpr int kBarriers = 2 * kMaxStages + 2 * 4 + 5;
 constexpr size_t kSmemLimit = 227u * 1024u;
 
 // Item numbering. Tile-major (item = t * U + u): a CTA's share covers one or two row tiles and
