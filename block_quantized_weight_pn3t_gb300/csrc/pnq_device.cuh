@@ -387,13 +387,39 @@ __device__ __forceinline__ uint32_t f32x2_to_f16x2(float a, float b) {
     return d;
 }
 
-// v = hi + lo exactly, hi = v rounded to its leading 11 significant bits (Veltkamp's splitting
-// with the factor 2^13 + 1 for 24-bit floats; the operations must not be contracted), so that hi
-// is exact in fp16 for 2^-14 <= |hi| < 65520 and lo carries the remaining 13 bits.
-__device__ __forceinline__ void split11(float v, float& hi, float& lo) {
-    const float c = __fmul_rn(v, 8193.0f);
-    hi = __fsub_rn(c, __fsub_rn(c, v));
-    lo = __fsub_rn(v, hi);
+// Packed fp32 pairs (two lanes in one 64-bit register; sm_100 family), round to nearest even;
+// explicit .rn operations are never contracted into fused multiply-adds.
+__device__ __forceinline__ uint64_t f32x2_pack(float lo, float hi) {
+    uint64_t d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
+    return d;
+}
+__device__ __forceinline__ void f32x2_unpack(uint64_t v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f32x2_mul(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t f32x2_sub(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t f32x2_add(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+// v = hi + lo exactly on both lanes of a pair: hi = v truncated to its leading 11 significant bits
+// (the low 13 mantissa bits cleared; exact in fp16 for 2^-14 <= |hi| < 65520), lo = v - hi
+// (exact, |lo| < 2^-10 |v|). Integer masking, so no compiler rewriting of the floating-point
+// steps can change it (a Veltkamp split in packed fp32 arithmetic was compiled to hi = v).
+__device__ __forceinline__ void split11x2(uint64_t v, uint64_t& hi, uint64_t& lo) {
+    hi = v & 0xFFFFE000FFFFE000ull;
+    lo = f32x2_sub(v, hi);
 }
 
 // Byte i (0..3) of w as two E2M1 codes (low nibble first) -> f16x2 with the exact values.

@@ -29,9 +29,9 @@
 // aligned words pairing the high half of word i-1 with the low half of word i (one PRMT).
 //
 // B operand (builder warps): x times 8^-j (16^-j) times 2^sigma (per K unit and activation row,
-// so that max|x| * 2^sigma lies in [2^14, 2^15)), split into fp16 hi + lo parts (~22 bits: hi =
-// the leading 11 bits by Veltkamp's splitting, lo = the rest rounded to fp16) that take mma
-// columns 2m and 2m + 1 (NT = ceil(2M / 8) n8 tiles), stored per block in register
+// so that max|x| * 2^sigma lies in [2^14, 2^15)), split into fp16 hi + lo parts (~21 bits: hi =
+// the leading 11 bits by truncation, lo = the rest rounded to fp16) that take mma columns 2m
+// and 2m + 1 (NT = ceil(2M / 8) n8 tiles), stored per block in register
 // order. Beside them: Z = z * 2^(sigma - 24) * (sum of the block's x), and 2^(24 - sigma).
 //
 // Block scale and zero point: per item a_m = sum over its blocks of d * (c - Z); the tile's row
@@ -255,18 +255,19 @@ __device__ __forceinline__ void build_row(uint8_t* slot_b, float* slot_z, float*
     for (int b0 = 0; b0 < NBLK; b0 += BL::BPP) {
         const int blk = blk0 + b0 + lane / BL::JL;
         const float* xb = xr + blk * F::BLK;
-        float zs = 0.0f;  // this lane's part of the block's sum of x (each element once)
+        uint64_t zs2 = 0;  // this lane's part of the block's sum of x (each element once), two lanes
         if (L.act) {
             uint32_t hi[4] = {0u, 0u, 0u, 0u}, lo[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 if (L.act & (1u << q)) {
-                    const float x0 = xb[L.off[q][0]], x1 = xb[L.off[q][1]];
-                    zs += x0;
-                    zs += x1;
+                    const uint64_t xp = f32x2_pack(xb[L.off[q][0]], xb[L.off[q][1]]);
+                    zs2 = f32x2_add(zs2, xp);
+                    uint64_t hp, lp;
+                    split11x2(f32x2_mul(xp, f32x2_pack(sc[q], sc[q])), hp, lp);
                     float h0, h1, l0, l1;
-                    split11(x0 * sc[q], h0, l0);
-                    split11(x1 * sc[q], h1, l1);
+                    f32x2_unpack(hp, h0, h1);
+                    f32x2_unpack(lp, l0, l1);
                     hi[q] = f32x2_to_f16x2(h0, h1);  // exact
                     lo[q] = f32x2_to_f16x2(l0, l1);
                 }
@@ -280,6 +281,9 @@ __device__ __forceinline__ void build_row(uint8_t* slot_b, float* slot_z, float*
                 *reinterpret_cast<uint4*>(tb + ll * 16) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
             }
         }
+        float zs, zs_hi;
+        f32x2_unpack(zs2, zs, zs_hi);
+        zs += zs_hi;
 #pragma unroll
         for (int o = BL::JL / 2; o > 0; o >>= 1) zs += __shfl_xor_sync(0xffffffffu, zs, o);  // within the group
         // Z = z * sum over the block of 2^-24 * 8^j * B = z * 2^(sigma - 24) * (sum of x)
