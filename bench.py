@@ -217,6 +217,16 @@ def run_reference(args):
 
 # ------------------------------------------------------------------------------- GPU arm
 
+def aggregate_replicas(times_ms, world, step_bytes, pg=None, device=None):
+    """Whole-job figures of `world` replicas of the step: each time is the slowest rank's (max over
+    ranks; pg = torch.distributed or None), each throughput = the bytes of all replicas / it."""
+    t = torch.tensor([float(v) for v in times_ms], dtype=torch.float64, device=device)
+    if pg is not None:
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    slowest = [float(v) for v in t.cpu()]
+    return slowest, [world * step_bytes / (v * 1e-3) / 1e9 for v in slowest]
+
+
 def run_ours(args):
     import block_quantized_weight_pn3t_gb300 as pnq
     from block_quantized_weight_pn3t_gb300 import synth
@@ -340,13 +350,7 @@ def run_ours(args):
         raise SystemExit(f"libpnq recorded a device error (site {err})")
 
     # ---- aggregate over ranks (replicas): bytes of all ranks / slowest rank
-    ms_max, ms_e2e_max = ms, ms_e2e
-    if pg:
-        t = torch.tensor([ms, ms_e2e], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms_max, ms_e2e_max = float(t[0]), float(t[1])
-    value = world * step_bytes / (ms_max * 1e-3) / 1e9
-    e2e_value = world * step_bytes / (ms_e2e_max * 1e-3) / 1e9
+    (ms_max, ms_e2e_max), (value, e2e_value) = aggregate_replicas([ms, ms_e2e], world, step_bytes, pg, dev)
 
     if rank == 0:
         line = {
