@@ -382,14 +382,39 @@ def run_ours(args):
         pg.destroy_process_group()
 
 
+NVFP4_SHAPES = {"nvfp4_17408x5120": (17408, 5120), "nvfp4_5120x17408": (5120, 17408)}
+
+
+def run_single_nvfp4(args):
+    """One NVFP4 GEMV (the NVFP4 workload: codes uniform, e4m3 scales of |N(0,1)|, g = 0.01, bf16
+    x), called --warmup times on the default stream: the small case of the NVFP4 ncu summary."""
+    import block_quantized_weight_pn3t_gb300 as pnq
+    from block_quantized_weight_pn3t_gb300 import synth
+    N, K = NVFP4_SHAPES[args.single]
+    torch.cuda.set_device(0)
+    codes, scales, g = synth.nvfp4_random(N, K, seed=SEED, device="cuda")
+    X = torch.from_numpy(synth.activations_bf16(args.m, K, seed=SEED).view(np.int16)).cuda()
+    Y = torch.empty((args.m, N), dtype=torch.float32, device="cuda")
+    for _ in range(args.warmup):
+        pnq.gemv(pnq.NVFP4, (codes, scales, g), X, N, K, Y=Y, flags=pnq.GEMV_STATIC_WEIGHTS)
+    torch.cuda.synchronize()
+    err = pnq.device_error()
+    print(json.dumps({"single": args.single, "type": pnq.NVFP4, "N": N, "K": K, "M": args.m, "launches": args.warmup,
+                      "weight_bytes": codes.numel() + scales.numel(), "device_error": err}))
+    if err:
+        raise SystemExit(1)
+
+
 def run_single(args):
     """One projection of layer 0, called a few times on the default stream: the small case the
     committed ncu summaries are captured on (one kernel, few launches, a few GB at most)."""
     import block_quantized_weight_pn3t_gb300 as pnq
     from block_quantized_weight_pn3t_gb300 import synth
     names = [p[0] for p in PROJECTIONS]
+    if args.single in NVFP4_SHAPES:
+        return run_single_nvfp4(args)
     if args.single not in names:
-        raise SystemExit(f"--single must be one of {names}")
+        raise SystemExit(f"--single must be one of {names + list(NVFP4_SHAPES)}")
     p = names.index(args.single)
     _, t, N, K = PROJECTIONS[p]
     torch.cuda.set_device(0)
