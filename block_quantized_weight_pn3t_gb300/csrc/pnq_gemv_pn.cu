@@ -11,9 +11,9 @@
 // the narrow N of a GEMV the warp-level MMA has the throughput and tcgen05 does not.
 //
 // Items and schedule (stream-K, pnq_streamk.cuh). The weight matrix is cut into items of 128
-// rows x one K unit of 8 blocks (272 bytes per row), numbered tile-major; every CTA of a
-// persistent grid (one per SM) takes an equal contiguous share, so all SMs stream the same
-// number of bytes.
+// rows x one K unit of 8 blocks (272 bytes per row), numbered tile-major (grouped unit-major for
+// wide batches whose operands would not fit otherwise); every CTA of a persistent grid (one per
+// SM) takes an equal contiguous share, so all SMs stream the same number of bytes.
 //
 // Memory pipeline. One producer thread loads one item per stage with a 2-D tensor-map copy
 // (box 272 bytes x 128 rows, L2 evict-first; rows past N read as zeros) into an NS-stage ring
@@ -28,11 +28,13 @@
 // free as long as B uses the same order, so the 2-byte aligned words of even blocks are read as
 // aligned words pairing the high half of word i-1 with the low half of word i (one PRMT).
 //
-// B operand (builder warps): x times 8^-j (16^-j) times 2^sigma (per K unit and activation row,
-// so that max|x| * 2^sigma lies in [2^14, 2^15)), split into fp16 hi + lo parts (~21 bits: hi =
-// the leading 11 bits by truncation, lo = the rest rounded to fp16) that take mma columns 2m
-// and 2m + 1 (NT = ceil(2M / 8) n8 tiles), stored per block in register
-// order. Beside them: Z = z * 2^(sigma - 24) * (sum of the block's x), and 2^(24 - sigma).
+// B operand: x times 8^-j (16^-j) times 2^sigma (per K unit and activation row, so that
+// max|x| * 2^sigma lies in [2^14, 2^15)), split into fp16 hi + lo parts (~21 bits: hi = the
+// leading 11 bits by truncation, lo = the rest rounded to fp16) that take mma columns 2m and
+// 2m + 1 (NT = ceil(2M / 8) n8 tiles), stored per block in register order. Beside them:
+// Z = z * 2^(sigma - 24) * (sum of the block's x), and 2^(24 - sigma). Built once per K unit of
+// the CTA's share by all consumer and builder warps before the first item (resident mode), or,
+// when those operands do not fit, by the builder warps into a ring ahead of the consumers.
 //
 // Block scale and zero point: per item a_m = sum over its blocks of d * (c - Z); the tile's row
 // sum gains a_m * 2^(24 - sigma).
