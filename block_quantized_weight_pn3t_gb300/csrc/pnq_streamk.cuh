@@ -267,7 +267,7 @@ __device__ __forceinline__ void count_shares(const Ctx& a, const SM& sm, int np,
 }
 
 // Sum the shares of tile t for activation row m in unit order into Y (one warp). The slot
-// loads go out four at a time; the additions keep unit order, so the sum does not depend on
+// loads go out eight at a time; the additions keep unit order, so the sum does not depend on
 // which CTA finishes the tile. The m == 0 call clears the tile's counter for the next launch
 // (no other CTA reads it again in this one).
 __device__ __forceinline__ void finish_tile(const Ctx& a, int t, int m, int lane) {
@@ -279,15 +279,16 @@ __device__ __forceinline__ void finish_tile(const Ctx& a, int t, int m, int lane
     const float* base = a.ws + (static_cast<size_t>(t) * sc.U * a.M + m) * kTileRows;
     auto unit_of_share = [&](int j) { return !consec ? j : (j == 0 ? 0 : sc.first(c_lo + j) - a0); };
     float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-    for (int j0 = 0; j0 < n; j0 += 4) {
-        float4 v[4];
+    constexpr int B = 8;  // slot loads in flight per lane
+    for (int j0 = 0; j0 < n; j0 += B) {
+        float4 v[B];
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
+        for (int i = 0; i < B; ++i)
             if (j0 + i < n)
                 v[i] = __ldcg(reinterpret_cast<const float4*>(
                                   base + static_cast<size_t>(unit_of_share(j0 + i)) * a.M * kTileRows) + lane);
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
+        for (int i = 0; i < B; ++i)
             if (j0 + i < n) {
                 acc.x += v[i].x;
                 acc.y += v[i].y;
