@@ -4,8 +4,13 @@
  *
  * Conventions shared by every entry point
  *   - Returns PNQ_OK (0) or a negative pnq_status. Nothing aborts; no kernel traps.
- *   - Device pointers are plain CUDA device addresses owned by the caller. The library
- *     allocates no device memory and keeps no per-call state.
+ *   - Device pointers are plain CUDA device addresses owned by the caller. The only device
+ *     memory the library allocates is the workspace of the fast GEMV paths (pnq_gemv,
+ *     pnq_gemv_ex): fp32 partial sums and u32 tile counters, one workspace per (device,
+ *     stream), allocated on the first call that needs it, grown when a larger shape comes
+ *     and kept until the process exits (a captured graph may still refer to an older one).
+ *     A failed allocation returns PNQ_ERR_CUDA. Two host threads must not call a GEMV on
+ *     the same stream at once. pnq_gemv_noalloc, dequantize and validate allocate nothing.
  *   - Calls are asynchronous and ordered on `stream` (0 = the legacy default stream).
  *     Argument errors are reported before anything is launched; a launch failure is
  *     reported as PNQ_ERR_CUDA. Results are valid once the stream reaches the call.
