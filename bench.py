@@ -140,6 +140,16 @@ def profiled_traffic(kernel_tag: str):
     return float(m_tr.group(1))
 
 
+def workload_config(M: int, L: int, n_calls: int, world: int) -> dict:
+    """The `config` object both arms report: the decode-step workload and how it is run."""
+    step_bytes = L * layer_bytes()
+    return {"workload": "qwen27b-decode-step-64x7", "layers": L, "M": M,
+            "projections": {n: f"{'pn3t' if t == PN3T else 'pn4t'} {N}x{K}" for n, t, N, K in PROJECTIONS},
+            "weight_bytes_per_step": step_bytes,
+            "l2": f"inputs larger than L2 (weights {step_bytes / L2_BYTES:.1f}x the L2 per step); no flush",
+            "graph": f"one CUDA graph per step, {n_calls} pnq_gemv launches", "parallelism": f"replicas x{world}"}
+
+
 def dist_info():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -207,8 +217,8 @@ def run_reference(args):
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 5), "unit": "GB/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": "qwen27b-decode-step-64x7", "M": args.m,
-                       "sample": "one of the 64 layers (all 7 projections) per step"},
+            "config": dict(workload_config(args.m, args.layers, args.layers * len(PROJECTIONS), args.gpus),
+                           sample="one of the layers (all 7 projections) per step, on the host cores"),
             "cpu_baseline": {"value": round(value, 5), "unit": "GB/s", "cores": 1, "kind": "oracle",
                              "sample": f"layer 0 of 64 (all 7 projections, {layer_bytes() / 1e6:.0f} MB), "
                                        f"M={args.m}, {args.steps} steps"},
@@ -373,13 +383,8 @@ def run_ours(args):
             "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms_max, 4), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f16-mma/f32-acc", "data": "synthetic",
-            "config": {"workload": "qwen27b-decode-step-64x7", "layers": L, "M": M,
-                       "projections": {n: f"{'pn3t' if t == PN3T else 'pn4t'} {N}x{K}" for n, t, N, K in PROJECTIONS},
-                       "weight_bytes_per_step": step_bytes, "us_per_step": round(ms_max * 1e3, 2),
-                       "hbm_fraction": round(value / world / peak, 4),
-                       "l2": f"inputs larger than L2 (weights {step_bytes / L2_BYTES:.1f}x the L2 per step); no flush",
-                       "graph": f"one CUDA graph per step, {len(calls)} pnq_gemv launches",
-                       "parallelism": f"replicas x{world}"},
+            "config": dict(workload_config(M, L, len(calls), world), us_per_step=round(ms_max * 1e3, 2),
+                           hbm_fraction=round(value / world / peak, 4)),
             "roofline": {"bound": "hbm", "achieved": round(dom_gbs, 2), "peak": peak, "unit": "GB/s",
                          "frac": round(dom_gbs / peak, 4), "traffic": traffic,
                          "kernel": f"pn_gemv_kernel<pn3t, NT={min(4, 1 << ((2 * M + 7) // 8 - 1).bit_length())}>", "launches": len(dom),

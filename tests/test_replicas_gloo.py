@@ -70,3 +70,23 @@ def test_reference_arm_prints_on_rank_0_only():
                         "--warmup", "3"], env=env, capture_output=True, text=True, timeout=300, cwd=ROOT)
     assert r.returncode == 0, r.stderr[-3000:]
     assert r.stdout.strip() == ""
+
+
+def test_reference_arm_line_matches_our_config():
+    """Rank 0's reference line: the contract's keys, the same workload `config` our arm reports
+    (plus how it was sampled), and e2e with no host-device bytes."""
+    sys.path.insert(0, ROOT)
+    import bench
+    env = dict(os.environ, WORLD_SIZE="1", RANK="0", LOCAL_RANK="0")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
+                        "--warmup", "3", "--layers", "2"], env=env, capture_output=True, text=True, timeout=300,
+                       cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-3000:]
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["metric"] == bench.METRIC and line["unit"] == "GB/s"
+    assert line["higher_is_better"] is True and line["value"] > 0
+    ours = bench.workload_config(1, 2, 2 * len(bench.PROJECTIONS), 1)
+    assert {k: v for k, v in line["config"].items() if k != "sample"} == ours
+    assert ours["weight_bytes_per_step"] == 2 * 172_130_304
+    assert line["cpu_baseline"]["value"] == line["value"] and line["cpu_baseline"]["kind"] == "oracle"
+    assert line["e2e"] == {"value": line["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
