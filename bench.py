@@ -37,7 +37,7 @@ sys.path.insert(0, ROOT)
 import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
-PN3T, PN4T = 124, 125
+PN3T, PN4T, NVFP4 = 124, 125, 1004
 BLK = {PN3T: 80, PN4T: 64}
 # name, type, N, K
 PROJECTIONS = [("attn_q", PN3T, 12288, 5120), ("attn_k", PN4T, 1024, 5120), ("attn_v", PN4T, 1024, 5120),
@@ -455,6 +455,74 @@ def run_single(args):
         raise SystemExit(1)
 
 
+CODEC_SHAPES = [(PN4T, 5120, 17408), (PN3T, 17408, 5120), (NVFP4, 17408, 5120)]
+
+
+def run_codec(args):
+    """Dequantize and validate on full-size shapes (pn4t 5120 x 17408, pn3t 17408 x 5120, NVFP4
+    17408 x 5120; weights generated on the device from the seed). Each call's time is the mean of
+    CUDA events around back-to-back calls on the current stream (`--steps`, at least one per weight
+    copy) after `--warmup` calls, rotating through weight copies that together exceed the L2
+    twice, so the weights come from HBM.
+    Algorithmic bytes per call: the weights read plus the fp32 weights written (dequantize); for
+    validate, the int32 row flags written plus the PN tensor (its d fields sit at a 34-byte stride,
+    so every 32-byte sector holds one and the whole tensor crosses the bus) or the NVFP4 scales
+    alone. One JSON line per operation and shape."""
+    import block_quantized_weight_pn3t_gb300 as pnq
+    from block_quantized_weight_pn3t_gb300 import synth
+    torch.cuda.set_device(0)
+    peak, peak_kind = measured_peaks()
+    out = None
+    for t, N, K in CODEC_SHAPES:
+        if t == NVFP4:
+            wbytes = N * K // 2 + N * K // 16
+            name = "nvfp4"
+        else:
+            wbytes = N * row_bytes(t, K)
+            name = "pn3t" if t == PN3T else "pn4t"
+        n_copies = max(2, -(-int(2 * L2_BYTES) // wbytes))
+        if t == NVFP4:
+            # validate reads only the scales: enough distinct scale tensors for them alone to
+            # exceed the L2 twice, paired with the code tensors in rotation
+            n_codes = n_copies
+            n_copies = max(n_codes, -(-int(2 * L2_BYTES) // (N * K // 16)))
+            gen = [synth.nvfp4_random(N, K, seed=SEED, stream=c, device="cuda") for c in range(n_codes)]
+            more = [synth.nvfp4_random(N, K, seed=SEED, stream=c, device="cuda")[1] for c in range(n_codes, n_copies)]
+            copies = [(gen[c % n_codes][0], gen[c][1] if c < n_codes else more[c - n_codes], gen[0][2])
+                      for c in range(n_copies)]
+        else:
+            copies = [synth.pn_random_blocks(t, N, K, seed=SEED, stream=c, device="cuda") for c in range(n_copies)]
+        if out is None or out.numel() < N * K:
+            out = torch.empty((N * K,), dtype=torch.float32, device="cuda")
+        flags = torch.empty((N,), dtype=torch.int32, device="cuda")
+        ops = [("dequantize_row", lambda W: pnq.dequantize_row(t, W, N, K, out=out[:N * K].view(N, K)),
+                wbytes + 4 * N * K),
+               ("validate_row", lambda W: pnq.validate_row(t, W, N, K, flags=flags),
+                (N * K // 16 if t == NVFP4 else wbytes) + 4 * N)]
+        for op, call, nbytes in ops:
+            for i in range(args.warmup):
+                call(copies[i % n_copies])
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            reps = max(args.steps, n_copies)  # every copy at least once, none reused while in L2
+            e0.record()
+            for i in range(args.warmup, args.warmup + reps):
+                call(copies[i % n_copies])
+            e1.record()
+            torch.cuda.synchronize()
+            us = e0.elapsed_time(e1) * 1e3 / reps
+            gbs = nbytes / (us * 1e-6) / 1e9
+            print(json.dumps({"op": op, "type": name, "N": N, "K": K, "calls": reps, "us_per_call": round(us, 3),
+                              "algorithmic_bytes": nbytes, "weight_copies": n_copies, "achieved": round(gbs, 1),
+                              "peak": peak, "unit": "GB/s", "frac": round(gbs / peak, 4),
+                              "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({peak_kind})"}), flush=True)
+        del copies
+        torch.cuda.empty_cache()
+    err = pnq.device_error()
+    if err:
+        raise SystemExit(f"libpnq recorded a device error (site {err})")
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -464,12 +532,16 @@ def main():
     ap.add_argument("--m", type=int, default=1, help="activation rows (1..16)")
     ap.add_argument("--layers", type=int, default=64)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--codec", action="store_true",
+                    help="time dequantize and validate on the full-size shapes and exit")
     ap.add_argument("--single", default=None,
                     help="run one projection of layer 0 --warmup times and exit (profiling case)")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
-    if args.single:
+    if args.codec:
+        run_codec(args)
+    elif args.single:
         run_single(args)
     elif args.impl == "reference":
         run_reference(args)
