@@ -40,10 +40,12 @@ _lib = None
 
 
 def lib() -> ctypes.CDLL:
+    """The oracle library, built on first use. PNQ_ORACLE_LIB names another build of the same
+    source to load instead (the mutation tests load copies with a planted mistake)."""
     global _lib
     if _lib is None:
-        build()
-        L = ctypes.CDLL(LIB_PATH)
+        path = os.environ.get("PNQ_ORACLE_LIB") or build()
+        L = ctypes.CDLL(path)
         P, I64, I32, F, D = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float, ctypes.c_double
         sig = {
             "pnq_ref_block_weights": (I32, [I32]),
