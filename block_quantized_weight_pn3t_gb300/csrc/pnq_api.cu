@@ -3,6 +3,7 @@
 #include "pnq_internal.h"
 
 #include <algorithm>
+#include <atomic>
 
 #include <cstdint>
 #include <cstdlib>
@@ -34,35 +35,38 @@ int current_device() {
     return dev;
 }
 
-// pnq_gemv_noalloc's scratch on the current device (address looked up once per device).
-ExtWorkspace noalloc_scratch() {
-    static float* ptrs[kMaxDevices] = {};
-    ExtWorkspace w;
+// Device address of a library __device__ symbol on the current device, looked up once per
+// device (host threads may race on the first lookup; they store the same address).
+template <typename T>
+T* symbol_address(std::atomic<T*> (&cache)[kMaxDevices], const void* symbol) {
     const int dev = current_device();
-    if (dev < 0) return w;
-    if (!ptrs[dev]) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_pnq_noalloc_scratch) != cudaSuccess) return w;
-        ptrs[dev] = static_cast<float*>(p);
+    if (dev < 0) return nullptr;
+    T* p = cache[dev].load(std::memory_order_relaxed);
+    if (!p) {
+        void* q = nullptr;
+        if (cudaGetSymbolAddress(&q, symbol) != cudaSuccess) return nullptr;
+        p = static_cast<T*>(q);
+        cache[dev].store(p, std::memory_order_relaxed);
     }
-    w.ws = ptrs[dev];
+    return p;
+}
+
+std::atomic<float*> g_noalloc_ptrs[kMaxDevices];
+std::atomic<int*> g_error_word_ptrs[kMaxDevices];
+
+// pnq_gemv_noalloc's scratch on the current device.
+ExtWorkspace noalloc_scratch() {
+    ExtWorkspace w;
+    float* base = symbol_address(g_noalloc_ptrs, static_cast<const void*>(g_pnq_noalloc_scratch));
+    if (!base) return w;
+    w.ws = base;
     w.floats = kNoAllocFloats;
-    w.cnt = reinterpret_cast<uint32_t*>(ptrs[dev] + kNoAllocFloats);
+    w.cnt = reinterpret_cast<uint32_t*>(base + kNoAllocFloats);
     w.counters = kNoAllocCounters;
     return w;
 }
 
-int* error_word() {
-    static int* ptrs[kMaxDevices] = {};
-    const int dev = current_device();
-    if (dev < 0) return nullptr;
-    if (!ptrs[dev]) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_pnq_error_word) != cudaSuccess) return nullptr;
-        ptrs[dev] = static_cast<int*>(p);
-    }
-    return ptrs[dev];
-}
+int* error_word() { return symbol_address(g_error_word_ptrs, static_cast<const void*>(&g_pnq_error_word)); }
 
 // "auto" (default: the mma.sync path whenever eligible), "simt" (generic path only), "mma"
 // (same as auto) or "tc" (the tcgen05 path whenever eligible; slower for M <= 16, kept as a
@@ -114,15 +118,15 @@ int check_common(int type, const void* W, int64_t rows, int64_t K, Nvfp4View* nv
 }  // namespace
 
 int device_sm_count() {
-    static int counts[kMaxDevices] = {};
+    static std::atomic<int> counts[kMaxDevices];
     const int dev = current_device();
     if (dev < 0) return 148;
-    if (!counts[dev]) {
-        int n = 0;
+    int n = counts[dev].load(std::memory_order_relaxed);
+    if (!n) {
         if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
-        counts[dev] = n;
+        counts[dev].store(n, std::memory_order_relaxed);
     }
-    return counts[dev];
+    return n;
 }
 
 namespace {
@@ -150,6 +154,25 @@ struct Workspace {
     size_t floats = 0, counters = 0;
 };
 
+// Every tile-counter buffer handed to a kernel, current or outgrown (a captured graph may still
+// use an outgrown one), so that clear_counters can reach them all.
+struct CounterBuffer {
+    int dev;
+    uint32_t* cnt;
+    size_t counters;
+};
+
+struct WorkspaceRegistry {
+    std::mutex mu;
+    std::map<std::pair<int, cudaStream_t>, Workspace> table;  // (device, stream) -> workspace
+    std::vector<CounterBuffer> counters;
+};
+
+WorkspaceRegistry& registry() {
+    static WorkspaceRegistry r;
+    return r;
+}
+
 }  // namespace
 
 bool encode_u32_map(CUtensorMap* map, const void* base, int64_t rows, int64_t row_u32, int box_x, int box_y,
@@ -166,14 +189,12 @@ bool encode_u32_map(CUtensorMap* map, const void* base, int64_t rows, int64_t ro
 }
 
 cudaError_t stream_workspace(cudaStream_t stream, size_t floats, size_t counters, float** ws, uint32_t** cnt) {
-    static std::mutex mu;
-    static std::map<std::pair<int, cudaStream_t>, Workspace> table;
-    static std::vector<void*> retired;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    std::lock_guard<std::mutex> lock(mu);
-    Workspace& w = table[{dev, stream}];
+    WorkspaceRegistry& r = registry();
+    std::lock_guard<std::mutex> lock(r.mu);
+    Workspace& w = r.table[{dev, stream}];
     if (w.floats < floats || w.counters < counters) {
         Workspace n;
         n.floats = std::max(floats, w.floats);
@@ -189,14 +210,37 @@ cudaError_t stream_workspace(cudaStream_t stream, size_t floats, size_t counters
         if (e != cudaSuccess) return e;
         e = cudaMemsetAsync(n.cnt, 0, n.counters * sizeof(uint32_t), stream);
         if (e != cudaSuccess) return e;
-        if (w.ws) retired.push_back(w.ws);
-        if (w.cnt) retired.push_back(w.cnt);
-        w = n;
+        r.counters.push_back(CounterBuffer{dev, n.cnt, n.counters});
+        w = n;  // the outgrown buffers stay allocated
     }
     *ws = w.ws;
     *cnt = w.cnt;
     return cudaSuccess;
 }
+
+namespace {
+
+// Zero every tile counter the library has handed to a kernel on the current device: the
+// workspaces' and, once it has been used, the no-alloc scratch's. A kernel that gave up on a
+// bounded wait may leave a tile's count part-way, and the next launch on that workspace would
+// then finish the tile early or never. The caller has synchronised the device.
+cudaError_t clear_counters() {
+    const int dev = current_device();
+    if (dev < 0) return cudaErrorInvalidDevice;
+    cudaError_t e = cudaSuccess;
+    {
+        WorkspaceRegistry& r = registry();
+        std::lock_guard<std::mutex> lock(r.mu);
+        for (const CounterBuffer& b : r.counters)
+            if (b.dev == dev && e == cudaSuccess) e = cudaMemset(b.cnt, 0, b.counters * sizeof(uint32_t));
+    }
+    float* scratch = g_noalloc_ptrs[dev].load(std::memory_order_relaxed);
+    if (scratch && e == cudaSuccess) e = cudaMemset(scratch + kNoAllocFloats, 0, kNoAllocCounters * sizeof(uint32_t));
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    return e;
+}
+
+}  // namespace
 
 }  // namespace pnq
 
@@ -293,7 +337,9 @@ extern "C" int pnq_validate_row(int type, const void* W, int64_t n_rows, int64_t
 extern "C" int pnq_device_error(int32_t* code) {
     if (!code) return PNQ_ERR_NULL;
     int v = 0;
+    if (cudaDeviceSynchronize() != cudaSuccess) return PNQ_ERR_CUDA;  // every stream, not only the default one
     if (cudaMemcpyFromSymbol(&v, g_pnq_error_word, sizeof(int)) != cudaSuccess) return PNQ_ERR_CUDA;
+    if (v != 0 && clear_counters() != cudaSuccess) return PNQ_ERR_CUDA;
     const int zero = 0;
     if (cudaMemcpyToSymbol(g_pnq_error_word, &zero, sizeof(int)) != cudaSuccess) return PNQ_ERR_CUDA;
     *code = v;

@@ -147,11 +147,14 @@ int pnq_validate_row(int type, const void* W, int64_t n_rows, int64_t K, int32_t
 
 /*
  * pnq_device_error -- reads and clears the library's device error word on the current
- * device (synchronous: waits for the device). *code = 0 when no kernel has given up on a
- * bounded internal wait since the last call; otherwise the nonzero site code of the first
- * one (1: a consumer's wait for data, 2: the producer's wait for a free stage, 3: the final
- * wait for copies in flight), and the call returns PNQ_ERR_DEVICE. Other returns: PNQ_OK,
- * PNQ_ERR_NULL, PNQ_ERR_CUDA. (Library plumbing; the pages define no such call.)
+ * device (synchronous: waits for all work on the device; not for use during stream capture).
+ * *code = 0 when no kernel has given up on a bounded internal wait since the last call;
+ * otherwise the nonzero site code of the first one (1: a consumer's wait for data, 2: the
+ * producer's wait for a free stage, 3: the final wait for copies in flight), and the call
+ * returns PNQ_ERR_DEVICE. With a nonzero code it also zeroes the tile counters of every GEMV
+ * workspace and of the no-alloc scratch on the device, so later GEMVs start from a clean
+ * state; the Y of a GEMV that gave up is unspecified. Other returns: PNQ_OK, PNQ_ERR_NULL,
+ * PNQ_ERR_CUDA. (Library plumbing; the pages define no such call.)
  */
 int pnq_device_error(int32_t* code);
 
