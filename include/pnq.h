@@ -111,13 +111,22 @@ int pnq_gemv_ex(int type, const void* W, int64_t N, int64_t K, const void* X, in
                 unsigned int flags, cudaStream_t stream);
 
 /*
- * pnq_gemv_noalloc -- pnq_gemv_ex that allocates nothing. The pages define no counterpart:
- * it is a library convenience for callers that must not allocate device memory. The fast PN
- * path's cross-CTA partial sums then live in one file-scope device array of the library
- * (PNQ_NOALLOC_SCRATCH_BYTES, shared by every call on the device, so calls through this entry
- * must be ordered with each other, e.g. on one stream) instead of the per-stream workspace
- * pnq_gemv keeps. A shape whose partial sums need more than that returns PNQ_ERR_SCRATCH
- * before anything is launched; otherwise results are identical to pnq_gemv_ex.
+ * pnq_gemv_noalloc -- pnq_gemv_ex that allocates nothing. The pages have no counterpart; it is
+ * for callers that cannot call cudaMalloc: code running under a caching or arena allocator that
+ * owns all device memory, a section being captured into a graph where a first-time allocation
+ * must not happen, or a runtime that forbids allocation after start-up. Same arguments, results
+ * (bit for bit) and errors as pnq_gemv_ex, plus PNQ_ERR_SCRATCH.
+ *   Scratch: the fast paths' (PN and NVFP4) cross-CTA partial sums and tile counters live in one
+ *   file-scope __device__ array of PNQ_NOALLOC_SCRATCH_BYTES (4 MiB) that every GPU loading the
+ *   library holds until the process exits. A shape that needs more (see the fast paths' work
+ *   split: row tiles x K units x M x 128 floats) returns PNQ_ERR_SCRATCH before anything is
+ *   launched; calls that fit never allocate, through CUDA or any library.
+ *   Set-up: the first call on a device, with that device current, looks up the array's device
+ *   address (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   Sharing: every call on a device uses the same array and leaves its tile counters at zero
+ *   (they start at zero when the library loads; pnq_device_error re-zeroes them after a kernel
+ *   gave up). Calls that overlap on the GPU (different streams, or graphs replayed
+ *   concurrently) race on the array: order them, e.g. on one stream.
  */
 #define PNQ_NOALLOC_SCRATCH_BYTES (4u * 1024u * 1024u)
 int pnq_gemv_noalloc(int type, const void* W, int64_t N, int64_t K, const void* X, int M, float* Y,
