@@ -78,7 +78,10 @@ struct Sched {
         if (tile_major) return i1 - i0 < U ? i1 - i0 : U;
         const int n_min = T % tg == 0 ? tg : min(tg, T % tg);  // the smallest group
         if (i1 - i0 >= n_min * U) return U;
-        int d = unit_of(i1 - 1) - unit_of(i0);  // at most one group boundary in between
+        // at most one group boundary in between; units rise inside a group and restart at 0
+        int d = unit_of(i1 - 1) - unit_of(i0);
+        const bool crosses = (i1 - 1) / group_items() != i0 / group_items();
+        if (crosses && d >= 0) return U;  // the rest of one group and the start of the next cover every unit
         if (d < 0) d += U;
         return d + 1;
     }
