@@ -45,6 +45,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdint>
 #include <cstdlib>
 
@@ -840,15 +841,15 @@ cudaError_t launch_cfg(PnArgs& a, const MmaConfig& cfg, bool static_weights, cud
     if (!make_plan(C::UK, C::bfu(a.M), a.M, C::NB, a.sc.T, a.sc.U, cap, cfg.grid > 0, cfg.ns, cfg.rb, cfg.order, p))
         return cudaErrorNotSupported;
     auto kern = pn_gemv_kernel<TYPE, NT, TPW>;
-    static bool opted[64] = {};
+    static std::atomic<bool> opted[64];  // the attribute is set once per device (threads may race to set it)
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!opted[dev]) {
+    if (!opted[dev].load(std::memory_order_relaxed)) {
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmemLimit));
         if (e != cudaSuccess) return e;
-        opted[dev] = true;
+        opted[dev].store(true, std::memory_order_relaxed);
     }
     const size_t ws_floats = static_cast<size_t>(a.sc.T) * a.sc.U * a.M * kTileRows;
     if (ext.ws) {

@@ -44,6 +44,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdint>
 #include <type_traits>
 #include <utility>
@@ -654,15 +655,15 @@ cudaError_t launch_mc(TcArgs& a, bool static_weights, cudaStream_t stream) {
     Plan p;
     if (!make_plan(F::BLK, F::PAIRS, PARTS, a.M, a.T, a.U, device_sm_count(), p)) return cudaErrorNotSupported;
     auto kern = pn_tc_gemv_kernel<TYPE, MC>;
-    static bool opted[64] = {};
+    static std::atomic<bool> opted[64];  // the attribute is set once per device (threads may race to set it)
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!opted[dev]) {
+    if (!opted[dev].load(std::memory_order_relaxed)) {
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmemLimit));
         if (e != cudaSuccess) return e;
-        opted[dev] = true;
+        opted[dev].store(true, std::memory_order_relaxed);
     }
     e = stream_workspace(stream, static_cast<size_t>(a.T) * a.U * a.M * kTileRows, static_cast<size_t>(a.T), &a.ws,
                          &a.cnt);
