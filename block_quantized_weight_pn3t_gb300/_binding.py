@@ -139,6 +139,46 @@ def _stream_handle(stream) -> int:
     return int(stream.cuda_stream)
 
 
+def _require(t, what: str, dtypes, numel: int | None = None) -> None:
+    """Raise PnqError unless t is a contiguous CUDA tensor of one of `dtypes` holding at least
+    `numel` elements (the library receives only its address)."""
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise PnqError(f"{what} must be a torch.Tensor, not {type(t).__name__}")
+    if t.dtype not in dtypes:
+        raise PnqError(f"{what} has dtype {t.dtype}; expected {' or '.join(str(d) for d in dtypes)}")
+    if not t.is_contiguous():
+        raise PnqError(f"{what} must be contiguous")
+    if numel is not None and t.numel() < numel:
+        raise PnqError(f"{what} holds {t.numel()} elements; the call needs {numel}")
+    if not t.is_cuda:
+        raise PnqError(f"{what} must be a CUDA tensor (device {t.device})")
+
+
+def _check_weights(type_: int, W, n_rows: int, K: int) -> None:
+    import torch
+    if type_ == NVFP4:
+        codes, scales, _g = W
+        whole = K > 0 and K % 16 == 0
+        _require(codes, "NVFP4 codes", (torch.uint8,), n_rows * K // 2 if whole else None)
+        _require(scales, "NVFP4 scales", (torch.uint8,), n_rows * K // 16 if whole else None)
+    elif type_ in BLOCK_WEIGHTS:
+        blk = BLOCK_WEIGHTS[type_]
+        _require(W, "W", (torch.uint8,), n_rows * (K // blk) * 34 if K > 0 and K % blk == 0 else None)
+    # an unknown type is left to the library (PNQ_ERR_TYPE)
+
+
+def _check_x(type_: int, X, K: int) -> int:
+    """The activation rows M of X ([M][K], or [K] for M = 1), after checking X."""
+    import torch
+    dtypes = (torch.bfloat16, torch.int16) if type_ == NVFP4 else (torch.float32,)
+    M = X.shape[0] if X.dim() == 2 else 1
+    _require(X, "X", dtypes)
+    if X.numel() != M * K:
+        raise PnqError(f"X has shape {tuple(X.shape)}; expected [M][{K}] or [{K}]")
+    return M
+
+
 def _weights(type_: int, W):
     if type_ == NVFP4:
         codes, scales, g = W
@@ -150,9 +190,11 @@ def gemv(type_: int, W, X, N: int, K: int, Y=None, stream=None, flags: int = 0):
     """Y[m][n] = sum_k W[n][k] X[m][k]. W: uint8 CUDA tensor of PN blocks, or (codes, scales, g)
     for NVFP4. X: CUDA [M][K] fp32 (PN) or bf16 (NVFP4). Returns Y (CUDA fp32 [M][N])."""
     import torch
-    M = X.shape[0] if X.dim() == 2 else 1
+    _check_weights(type_, W, N, K)
+    M = _check_x(type_, X, K)
     if Y is None:
         Y = torch.empty((M, N), dtype=torch.float32, device=X.device)
+    _require(Y, "Y", (torch.float32,), M * N)
     _check(gemv_ex_ptr(type_, _weights(type_, W), N, K, X.data_ptr(), M, Y.data_ptr(), flags,
                        _stream_handle(stream)), "pnq_gemv_ex")
     return Y
@@ -162,9 +204,11 @@ def gemv_noalloc(type_: int, W, X, N: int, K: int, Y=None, stream=None, flags: i
     """gemv through pnq_gemv_noalloc (no device allocation; PnqError ERR_SCRATCH when the shape
     needs more than the library's built-in scratch)."""
     import torch
-    M = X.shape[0] if X.dim() == 2 else 1
+    _check_weights(type_, W, N, K)
+    M = _check_x(type_, X, K)
     if Y is None:
         Y = torch.empty((M, N), dtype=torch.float32, device=X.device)
+    _require(Y, "Y", (torch.float32,), M * N)
     _check(gemv_noalloc_ptr(type_, _weights(type_, W), N, K, X.data_ptr(), M, Y.data_ptr(), flags,
                             _stream_handle(stream)), "pnq_gemv_noalloc")
     return Y
@@ -172,9 +216,11 @@ def gemv_noalloc(type_: int, W, X, N: int, K: int, Y=None, stream=None, flags: i
 
 def dequantize_row(type_: int, W, n_rows: int, K: int, out=None, stream=None):
     import torch
+    _check_weights(type_, W, n_rows, K)
     if out is None:
         dev = W[0].device if type_ == NVFP4 else W.device
         out = torch.empty((n_rows, K), dtype=torch.float32, device=dev)
+    _require(out, "out", (torch.float32,), n_rows * K)
     _check(dequantize_row_ptr(type_, _weights(type_, W), n_rows, K, out.data_ptr(), _stream_handle(stream)),
            "pnq_dequantize_row")
     return out
@@ -182,9 +228,11 @@ def dequantize_row(type_: int, W, n_rows: int, K: int, out=None, stream=None):
 
 def validate_row(type_: int, W, n_rows: int, K: int, flags=None, stream=None):
     import torch
+    _check_weights(type_, W, n_rows, K)
     if flags is None:
         dev = W[0].device if type_ == NVFP4 else W.device
         flags = torch.empty((n_rows,), dtype=torch.int32, device=dev)
+    _require(flags, "flags", (torch.int32,), n_rows)
     _check(validate_row_ptr(type_, _weights(type_, W), n_rows, K, flags.data_ptr(), _stream_handle(stream)),
            "pnq_validate_row")
     return flags

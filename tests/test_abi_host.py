@@ -89,3 +89,37 @@ def test_binding_raises_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(_binding, "_LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(pnq.PnqError):
         _binding.lib()
+
+
+def test_wrappers_check_tensors_before_the_library(monkeypatch):
+    """The torch wrappers pass only addresses, so they refuse a tensor of the wrong dtype, a
+    non-contiguous one, one too small for the call, or a host tensor, before anything reaches
+    the library."""
+    import torch
+    from block_quantized_weight_pn3t_gb300 import _binding
+
+    def no_library():
+        raise AssertionError("the library was called")
+    monkeypatch.setattr(_binding, "lib", no_library)
+    req = _binding._require
+    with pytest.raises(pnq.PnqError, match="dtype"):
+        req(torch.zeros(8, dtype=torch.float64), "X", (torch.float32,))
+    with pytest.raises(pnq.PnqError, match="contiguous"):
+        req(torch.zeros(4, 8, dtype=torch.float32).t(), "X", (torch.float32,))
+    with pytest.raises(pnq.PnqError, match="elements"):
+        req(torch.zeros(8, dtype=torch.float32), "Y", (torch.float32,), 9)
+    with pytest.raises(pnq.PnqError, match="CUDA"):
+        req(torch.zeros(8, dtype=torch.float32), "Y", (torch.float32,), 8)
+    with pytest.raises(pnq.PnqError, match="torch.Tensor"):
+        req([0.0] * 8, "Y", (torch.float32,))
+    N, K = 4, 640
+    W = torch.zeros(N * (K // 80) * 34, dtype=torch.uint8)
+    with pytest.raises(pnq.PnqError, match="elements"):  # one byte short of 4 rows of pn3t
+        pnq.gemv(pnq.PN3T, W[:-1], torch.zeros(1, K), N, K)
+    with pytest.raises(pnq.PnqError, match="CUDA"):
+        pnq.gemv(pnq.PN3T, W, torch.zeros(1, K), N, K)
+    with pytest.raises(pnq.PnqError, match="CUDA"):
+        pnq.dequantize_row(pnq.PN3T, W, N, K)
+    with pytest.raises(pnq.PnqError, match="CUDA"):
+        pnq.validate_row(pnq.NVFP4, (torch.zeros(N * 128, dtype=torch.uint8), torch.zeros(N * 16, dtype=torch.uint8),
+                                     0.01), N, 256)
