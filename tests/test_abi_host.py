@@ -123,3 +123,40 @@ def test_wrappers_check_tensors_before_the_library(monkeypatch):
     with pytest.raises(pnq.PnqError, match="CUDA"):
         pnq.validate_row(pnq.NVFP4, (torch.zeros(N * 128, dtype=torch.uint8), torch.zeros(N * 16, dtype=torch.uint8),
                                      0.01), N, 256)
+
+
+C_CLIENT = r"""
+#include "pnq.h"
+#include <stdio.h>
+int main(void) {
+    pnq_nvfp4_weights w = {0, 0, 0.01f};
+    int32_t code = 0;
+    int rc = pnq_gemv(PNQ_PN3T, 0, 0, 80, 0, 1, 0, (cudaStream_t)0);  /* N = 0: nothing launched */
+    printf("%s|%d|%d|%d\n", pnq_version(), rc, (int)sizeof(w), PNQ_ERR_SCRATCH);
+    (void)code; (void)pnq_device_error; (void)pnq_gemv_ex; (void)pnq_gemv_noalloc;
+    (void)pnq_dequantize_row; (void)pnq_validate_row;
+    return 0;
+}
+"""
+
+
+def test_header_is_plain_c(lib, tmp_path):
+    """include/pnq.h compiles as C99 and a C program links against libpnq.so and calls it."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if not gcc:
+        pytest.skip("gcc not found")
+    src = tmp_path / "client.c"
+    src.write_text(C_CLIENT)
+    exe = tmp_path / "client"
+    libdir = os.path.dirname(pnq.lib_path())
+    cuda_inc = os.path.join(os.path.dirname(os.path.dirname(os.path.realpath(shutil.which("nvcc") or
+                                                                             "/usr/local/cuda/bin/nvcc"))), "include")
+    subprocess.check_call([gcc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-I", os.path.join(ROOT, "include"), "-I",
+                           cuda_inc, str(src), "-L", libdir, "-lpnq", f"-Wl,-rpath,{libdir}", "-o", str(exe)])
+    out = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert out.returncode == 0, out.stderr
+    version, rc, size, scratch = out.stdout.strip().split("|")
+    assert version.startswith("pnq ") and int(rc) == Status.OK and int(scratch) == Status.ERR_SCRATCH
+    assert int(size) == ctypes.sizeof(pnq._binding.pnq_nvfp4_weights)
