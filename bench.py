@@ -120,7 +120,7 @@ class ClockSampler:
 
 def kernel_source_digest():
     h = hashlib.sha256()
-    for fn in ("pnq_gemv_pn.cu", "pnq_streamk.cuh", "pnq_device.cuh"):
+    for fn in ("pnq_gemv_pn.cu", "pnq_split.cuh", "pnq_device.cuh"):
         with open(os.path.join(ROOT, "block_quantized_weight_pn3t_gb300", "csrc", fn), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -182,7 +182,9 @@ def oracle_layer(oracle, layer_w, xs):
 
 
 def cpu_baseline(M: int, budget_s: float = 12.0):
-    """The oracle (single-threaded C, fp64) on whole sampled layers until ~budget_s of CPU time."""
+    """The oracle (single-threaded C, fp64) on whole sampled layers until ~budget_s of CPU time on one
+    core, then the same oracle on every host core (one spawned process per core, rows split evenly,
+    a barrier before the timed part): the all-cores figure is the line's value."""
     import oracle
     oracle.lib()
     xs = host_x(M)
@@ -193,9 +195,64 @@ def cpu_baseline(M: int, budget_s: float = 12.0):
         nbytes += oracle_layer(oracle, w, xs)
         elapsed += time.perf_counter() - t0
         layers += 1
-    return {"value": round(nbytes / elapsed / 1e9, 5), "unit": "GB/s", "cores": 1, "kind": "oracle",
+    one = {"value": round(nbytes / elapsed / 1e9, 5), "unit": "GB/s", "cores": 1,
+           "sample": f"layers 0..{layers - 1} of 64 (all 7 projections, {nbytes / 1e6:.0f} MB of weights), M={M}, "
+                     f"{elapsed:.1f} s of single-thread fp64 CPU work"}
+    try:
+        allc = cpu_baseline_all_cores(M)
+    except Exception as e:  # the single-core figure stands alone
+        return dict(one, kind="oracle", all_cores_error=str(e)[:200])
+    return dict(allc, kind="oracle", single_core=one)
+
+
+def _oracle_worker_init(barrier):
+    global _BARRIER
+    _BARRIER = barrier
+
+
+def _oracle_worker(task):
+    """One host core: regenerate its rows of the sampled layers, wait for the others, then run the
+    oracle on them; returns (weight bytes, seconds of oracle work)."""
+    import oracle
+    from block_quantized_weight_pn3t_gb300 import synth
+    M, layers, worker, workers = task
+    oracle.lib()
+    xs = host_x(M)
+    work = []
+    for layer in range(layers):
+        for p, (name, t, N, K) in enumerate(PROJECTIONS):
+            r0, r1 = N * worker // workers, N * (worker + 1) // workers
+            if r1 > r0:
+                rows = torch.arange(r0, r1, dtype=torch.int64)
+                work.append((t, synth.pn_random_blocks(t, N, K, seed=SEED, stream=layer * 8 + p, rows=rows).numpy(),
+                             r1 - r0, K))
+    _BARRIER.wait()
+    t0 = time.perf_counter()
+    nbytes = 0
+    for t, W, n, K in work:
+        oracle.gemv(t, W, n, K, xs[K])
+        nbytes += W.nbytes
+    return nbytes, time.perf_counter() - t0
+
+
+def cpu_baseline_all_cores(M: int, layers: int = 8):
+    import concurrent.futures
+    import multiprocessing
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+    ctx = multiprocessing.get_context("spawn")
+    barrier = ctx.Barrier(cores)
+    with concurrent.futures.ProcessPoolExecutor(cores, mp_context=ctx, initializer=_oracle_worker_init,
+                                                initargs=(barrier,)) as ex:
+        res = list(ex.map(_oracle_worker, [(M, layers, w, cores) for w in range(cores)]))
+    nbytes = sum(r[0] for r in res)
+    wall = max(r[1] for r in res)
+    return {"value": round(nbytes / wall / 1e9, 5), "unit": "GB/s", "cores": cores,
             "sample": f"layers 0..{layers - 1} of 64 (all 7 projections, {nbytes / 1e6:.0f} MB of weights), M={M}, "
-                      f"{elapsed:.1f} s of single-thread fp64 CPU work"}
+                      f"rows split over {cores} spawned processes (one per core), {wall:.2f} s wall "
+                      f"(slowest process) of fp64 CPU work"}
+
+
+REF_ROW_FRACTION = 16  # the reference arm's step: the first 1/16 of every projection's rows of layer 0
 
 
 def run_reference(args):
@@ -203,25 +260,40 @@ def run_reference(args):
     if rank != 0:
         return
     import oracle
+    from block_quantized_weight_pn3t_gb300 import synth
     oracle.lib()
     xs = host_x(args.m)
-    w = host_layer(0)
+    sample = []
+    for p, (name, t, N, K) in enumerate(PROJECTIONS):
+        n = max(1, N // REF_ROW_FRACTION)
+        W = synth.pn_random_blocks(t, N, K, seed=SEED, stream=p, rows=torch.arange(n, dtype=torch.int64)).numpy()
+        sample.append((t, W, n, K))
+
+    def step():
+        nb = 0
+        for t, W, n, K in sample:
+            oracle.gemv(t, W, n, K, xs[K])
+            nb += W.nbytes
+        return nb
+
     for _ in range(args.warmup):
-        oracle_layer(oracle, w, xs)
+        step()
     t0 = time.perf_counter()
     nbytes = 0
     for _ in range(args.steps):
-        nbytes += oracle_layer(oracle, w, xs)
+        nbytes += step()
     dt = time.perf_counter() - t0
     value = nbytes / dt / 1e9
+    sample_bytes = sum(W.nbytes for _, W, _, _ in sample)
+    desc = (f"the first 1/{REF_ROW_FRACTION} of the rows of each of layer 0's 7 projections "
+            f"({sample_bytes / 1e6:.1f} MB of weights) per step, M={args.m}, one host core")
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 5), "unit": "GB/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": dict(workload_config(args.m, args.layers, args.layers * len(PROJECTIONS), args.gpus),
-                           sample="one of the layers (all 7 projections) per step, on the host cores"),
+                           sample=desc),
             "cpu_baseline": {"value": round(value, 5), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                             "sample": f"layer 0 of 64 (all 7 projections, {layer_bytes() / 1e6:.0f} MB), "
-                                       f"M={args.m}, {args.steps} steps"},
+                             "sample": f"{desc}, {args.steps} steps"},
             "e2e": {"value": round(value, 5), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -236,6 +308,66 @@ def aggregate_replicas(times_ms, world, step_bytes, pg=None, device=None):
         pg.all_reduce(t, op=pg.ReduceOp.MAX)
     slowest = [float(v) for v in t.cpu()]
     return slowest, [world * step_bytes / (v * 1e-3) / 1e9 for v in slowest]
+
+
+def graph_us_per_launch(launch, n_launch, stream, reps, warmup):
+    """launch(h) issues n_launch GEMVs on stream handle h; captured once in a CUDA graph, replayed
+    `warmup` times, then `reps` replays timed with CUDA events on the replay stream: us per GEMV."""
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        launch(torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    for _ in range(warmup):
+        g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) * 1e3 / (reps * n_launch)
+
+
+SINGLE_SHAPES = [("pn4t 5120x17408 M=1 (down-projection shape)", PN4T, 5120, 17408),
+                 ("nvfp4 17408x5120 M=1", NVFP4, 17408, 5120), ("nvfp4 5120x17408 M=1", NVFP4, 5120, 17408)]
+
+
+def single_call_lines(dev, stream, flags, peak, warmup):
+    """One GEMV shape at a time (M = 1, the same flags as the step), called back to back in a
+    graph that rotates through weight copies whose total exceeds the L2 twice (so every call
+    reads HBM): us per call, weight GB/s and the fraction of the measured HBM rate."""
+    import block_quantized_weight_pn3t_gb300 as pnq
+    from block_quantized_weight_pn3t_gb300 import synth
+    out = []
+    for label, t, N, K in SINGLE_SHAPES:
+        wbytes = N * K // 2 + N * K // 16 if t == NVFP4 else N * row_bytes(t, K)
+        n_copies = max(3, -(-int(2 * L2_BYTES) // wbytes))
+        if t == NVFP4:
+            ws = [synth.nvfp4_random(N, K, seed=SEED, stream=c, device=dev) for c in range(n_copies)]
+            descs = [pnq.nvfp4_weights(c.data_ptr(), sc.data_ptr(), g) for c, sc, g in ws]
+            X = torch.from_numpy(synth.activations_bf16(1, K, seed=SEED).view(np.int16)).to(dev)
+        else:
+            ws = [synth.pn_random_blocks(t, N, K, seed=SEED, stream=c, device=dev) for c in range(n_copies)]
+            descs = [w.data_ptr() for w in ws]
+            X = torch.from_numpy(synth.activations(1, K, seed=SEED)).to(dev)
+        Y = torch.empty((1, N), dtype=torch.float32, device=dev)
+        n = n_copies * max(1, 60 // n_copies)
+
+        def launch(h):
+            for i in range(n):
+                rc = pnq.gemv_ex_ptr(t, descs[i % n_copies], N, K, X.data_ptr(), 1, Y.data_ptr(), flags, h)
+                if rc != 0:
+                    raise pnq.PnqError("pnq_gemv", rc)
+
+        us = graph_us_per_launch(launch, n, stream, reps=5, warmup=warmup)
+        gbs = wbytes / (us * 1e-6) / 1e9
+        out.append({"shape": label, "us_per_call": round(us, 3), "weight_bytes": wbytes, "achieved": round(gbs, 1),
+                    "frac": round(gbs / peak, 4), "weight_copies": n_copies, "launches": n})
+        del ws
+        torch.cuda.empty_cache()
+    return out
 
 
 def run_ours(args):
@@ -371,6 +503,22 @@ def run_ours(args):
     peak, peak_kind = measured_peaks()
     traffic = profiled_traffic("pn3t_gemv_m1_decode_step") if M == 1 else None
 
+    # ---- each projection's launches of the step (one per layer) back to back in a graph of their own
+    per_proj = {}
+    for p, (name, t, N, K) in enumerate(PROJECTIONS):
+        sub = calls[p::len(PROJECTIONS)]
+
+        def launch(h, sub=sub):
+            for t_, w, N_, K_, x, y in sub:
+                rc = pnq.gemv_ex_ptr(t_, w, N_, K_, x, M, y, flags, h)
+                if rc != 0:
+                    raise pnq.PnqError("pnq_gemv", rc)
+
+        us = graph_us_per_launch(launch, len(sub), stream, reps=max(3, args.steps // 20), warmup=args.warmup)
+        gbs = N * row_bytes(t, K) / (us * 1e-6) / 1e9
+        per_proj[name] = {"us_per_call": round(us, 3), "achieved": round(gbs, 1), "frac": round(gbs / peak, 4)}
+    singles = single_call_lines(dev, stream, flags, peak, args.warmup) if M == 1 and not args.no_singles else None
+
     err = pnq.device_error()
     if err:
         raise SystemExit(f"libpnq recorded a device error (site {err})")
@@ -397,7 +545,12 @@ def run_ours(args):
                     "d2h_bytes_per_step": d2h, "ms_per_step": round(ms_e2e_max, 4)},
             "gpu_launches": args.steps * len(calls),
             "clocks": clocks,
+            "per_projection": {"timing": f"each projection's {L} launches of the step captured back to back in a "
+                                         f"graph of their own (same flags), events around the replays",
+                               "unit": "us per call; weight GB/s; fraction of the measured HBM rate", **per_proj},
         }
+        if singles is not None:
+            line["single_calls"] = singles
         if not args.no_cpu_baseline and world == 1:
             line["cpu_baseline"] = cpu_baseline(M)
         print(json.dumps(line), flush=True)
@@ -526,12 +679,13 @@ def run_codec(args):
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--m", type=int, default=1, help="activation rows (1..16)")
     ap.add_argument("--layers", type=int, default=64)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-singles", action="store_true", help="skip the single-GEMV lines of the JSON line")
     ap.add_argument("--codec", action="store_true",
                     help="time dequantize and validate on the full-size shapes and exit")
     ap.add_argument("--single", default=None,

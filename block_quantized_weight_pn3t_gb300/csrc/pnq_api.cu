@@ -17,12 +17,6 @@
 // device that loads the library).
 __device__ int g_pnq_error_word = 0;
 
-// Scratch of pnq_gemv_noalloc: fp32 partial sums, then the tile counters (zero at load; every
-// launch leaves them zero).
-constexpr size_t kNoAllocCounters = 16384;
-constexpr size_t kNoAllocFloats = PNQ_NOALLOC_SCRATCH_BYTES / 4 - kNoAllocCounters;
-static __device__ __align__(256) float g_pnq_noalloc_scratch[PNQ_NOALLOC_SCRATCH_BYTES / 4];
-
 namespace pnq {
 
 namespace {
@@ -51,32 +45,17 @@ T* symbol_address(std::atomic<T*> (&cache)[kMaxDevices], const void* symbol) {
     return p;
 }
 
-std::atomic<float*> g_noalloc_ptrs[kMaxDevices];
 std::atomic<int*> g_error_word_ptrs[kMaxDevices];
-
-// pnq_gemv_noalloc's scratch on the current device.
-ExtWorkspace noalloc_scratch() {
-    ExtWorkspace w;
-    float* base = symbol_address(g_noalloc_ptrs, static_cast<const void*>(g_pnq_noalloc_scratch));
-    if (!base) return w;
-    w.ws = base;
-    w.floats = kNoAllocFloats;
-    w.cnt = reinterpret_cast<uint32_t*>(base + kNoAllocFloats);
-    w.counters = kNoAllocCounters;
-    return w;
-}
 
 int* error_word() { return symbol_address(g_error_word_ptrs, static_cast<const void*>(&g_pnq_error_word)); }
 
-// "auto" (default: the mma.sync path whenever eligible), "simt" (generic path only), "mma"
-// (same as auto) or "tc" (the tcgen05 path whenever eligible; slower for M <= 16, kept as a
-// measured alternative).
+// "auto" (default: the mma.sync path whenever eligible), "simt" (generic path only) or "mma"
+// (same as auto).
 int forced_kernel() {
     static int mode = [] {
         const char* s = std::getenv("PNQ_FORCE_KERNEL");
         if (s && std::strcmp(s, "simt") == 0) return 1;
         if (s && std::strcmp(s, "mma") == 0) return 2;
-        if (s && std::strcmp(s, "tc") == 0) return 3;
         return 0;
     }();
     return mode;
@@ -148,31 +127,6 @@ EncodeFn tensor_map_encoder() {
     return fn;
 }
 
-struct Workspace {
-    float* ws = nullptr;
-    uint32_t* cnt = nullptr;
-    size_t floats = 0, counters = 0;
-};
-
-// Every tile-counter buffer handed to a kernel, current or outgrown (a captured graph may still
-// use an outgrown one), so that clear_counters can reach them all.
-struct CounterBuffer {
-    int dev;
-    uint32_t* cnt;
-    size_t counters;
-};
-
-struct WorkspaceRegistry {
-    std::mutex mu;
-    std::map<std::pair<int, cudaStream_t>, Workspace> table;  // (device, stream) -> workspace
-    std::vector<CounterBuffer> counters;
-};
-
-WorkspaceRegistry& registry() {
-    static WorkspaceRegistry r;
-    return r;
-}
-
 }  // namespace
 
 bool encode_u32_map(CUtensorMap* map, const void* base, int64_t rows, int64_t row_u32, int box_x, int box_y,
@@ -188,60 +142,6 @@ bool encode_u32_map(CUtensorMap* map, const void* base, int64_t rows, int64_t ro
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-cudaError_t stream_workspace(cudaStream_t stream, size_t floats, size_t counters, float** ws, uint32_t** cnt) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    WorkspaceRegistry& r = registry();
-    std::lock_guard<std::mutex> lock(r.mu);
-    Workspace& w = r.table[{dev, stream}];
-    if (w.floats < floats || w.counters < counters) {
-        Workspace n;
-        n.floats = std::max(floats, w.floats);
-        n.counters = std::max(counters, w.counters);
-        cudaStreamCaptureMode mode = cudaStreamCaptureModeRelaxed;
-        cudaThreadExchangeStreamCaptureMode(&mode);
-        e = cudaMalloc(&n.ws, n.floats * sizeof(float));
-        if (e == cudaSuccess) {
-            e = cudaMalloc(&n.cnt, n.counters * sizeof(uint32_t));
-            if (e != cudaSuccess) cudaFree(n.ws);
-        }
-        cudaThreadExchangeStreamCaptureMode(&mode);
-        if (e != cudaSuccess) return e;
-        e = cudaMemsetAsync(n.cnt, 0, n.counters * sizeof(uint32_t), stream);
-        if (e != cudaSuccess) return e;
-        r.counters.push_back(CounterBuffer{dev, n.cnt, n.counters});
-        w = n;  // the outgrown buffers stay allocated
-    }
-    *ws = w.ws;
-    *cnt = w.cnt;
-    return cudaSuccess;
-}
-
-namespace {
-
-// Zero every tile counter the library has handed to a kernel on the current device: the
-// workspaces' and, once it has been used, the no-alloc scratch's. A kernel that gave up on a
-// bounded wait may leave a tile's count part-way, and the next launch on that workspace would
-// then finish the tile early or never. The caller has synchronised the device.
-cudaError_t clear_counters() {
-    const int dev = current_device();
-    if (dev < 0) return cudaErrorInvalidDevice;
-    cudaError_t e = cudaSuccess;
-    {
-        WorkspaceRegistry& r = registry();
-        std::lock_guard<std::mutex> lock(r.mu);
-        for (const CounterBuffer& b : r.counters)
-            if (b.dev == dev && e == cudaSuccess) e = cudaMemset(b.cnt, 0, b.counters * sizeof(uint32_t));
-    }
-    float* scratch = g_noalloc_ptrs[dev].load(std::memory_order_relaxed);
-    if (scratch && e == cudaSuccess) e = cudaMemset(scratch + kNoAllocFloats, 0, kNoAllocCounters * sizeof(uint32_t));
-    if (e == cudaSuccess) e = cudaDeviceSynchronize();
-    return e;
-}
-
-}  // namespace
-
 }  // namespace pnq
 
 using namespace pnq;
@@ -249,7 +149,7 @@ using namespace pnq;
 namespace {
 
 int gemv_impl(int type, const void* W, int64_t N, int64_t K, const void* X, int M, float* Y, unsigned int flags,
-              cudaStream_t stream, bool no_alloc) {
+              cudaStream_t stream) {
     Nvfp4View nv{};
     int rc = check_common(type, W, N, K, &nv);
     if (rc != PNQ_OK) return rc;
@@ -261,18 +161,11 @@ int gemv_impl(int type, const void* W, int64_t N, int64_t K, const void* X, int 
     if (!aligned(Y, 4)) return PNQ_ERR_ALIGN;
     const bool static_w = (flags & PNQ_GEMV_STATIC_WEIGHTS) != 0;
     const int mode = forced_kernel();
-    ExtWorkspace ext;
-    if (no_alloc) {
-        ext = noalloc_scratch();
-        if (!ext.ws) return PNQ_ERR_CUDA;
-    }
     if (type == PNQ_NVFP4) {
         if (!aligned(X, 2)) return PNQ_ERR_ALIGN;
         const uint16_t* x = static_cast<const uint16_t*>(X);
         if (mode != 1 && aligned(nv.codes, 16) && aligned(nv.scales, 16) && aligned(x, 16) && K % 256 == 0) {
-            const cudaError_t e = launch_nvfp4_gemv_mma(nv, N, K, x, M, Y, error_word(), MmaConfig{0, 0, 0, 0},
-                                                        static_w, stream, ext);
-            if (no_alloc && e == cudaErrorMemoryAllocation) return PNQ_ERR_SCRATCH;
+            const cudaError_t e = launch_nvfp4_gemv_mma(nv, N, K, x, M, Y, error_word(), 0, 0, static_w, stream);
             if (e != cudaErrorNotSupported) return map_cuda(e);
         }
         return map_cuda(launch_nvfp4_gemv_simt(nv, N, K, x, M, Y, stream));
@@ -281,13 +174,7 @@ int gemv_impl(int type, const void* W, int64_t N, int64_t K, const void* X, int 
     const uint8_t* w = static_cast<const uint8_t*>(W);
     const float* x = static_cast<const float*>(X);
     if (mode != 1 && aligned(w, 16) && (K / block_weights(type)) % 8 == 0) {
-        if (mode == 3 && !no_alloc) {
-            const cudaError_t e = launch_pn_gemv_tc(type, w, N, K, x, M, Y, error_word(), static_w, stream);
-            if (e != cudaErrorNotSupported) return map_cuda(e);
-        }
-        const cudaError_t e =
-            launch_pn_gemv_mma(type, w, N, K, x, M, Y, error_word(), MmaConfig{0, 0, 0, 0}, static_w, stream, ext);
-        if (no_alloc && e == cudaErrorMemoryAllocation) return PNQ_ERR_SCRATCH;
+        const cudaError_t e = launch_pn_gemv_mma(type, w, N, K, x, M, Y, error_word(), 0, 0, static_w, stream);
         if (e != cudaErrorNotSupported) return map_cuda(e);
     }
     return map_cuda(launch_pn_gemv_simt(type, w, N, K, x, M, Y, stream));
@@ -297,12 +184,12 @@ int gemv_impl(int type, const void* W, int64_t N, int64_t K, const void* X, int 
 
 extern "C" int pnq_gemv_ex(int type, const void* W, int64_t N, int64_t K, const void* X, int M, float* Y,
                            unsigned int flags, cudaStream_t stream) {
-    return gemv_impl(type, W, N, K, X, M, Y, flags, stream, false);
+    return gemv_impl(type, W, N, K, X, M, Y, flags, stream);
 }
 
 extern "C" int pnq_gemv_noalloc(int type, const void* W, int64_t N, int64_t K, const void* X, int M, float* Y,
                                 unsigned int flags, cudaStream_t stream) {
-    return gemv_impl(type, W, N, K, X, M, Y, flags, stream, true);
+    return gemv_impl(type, W, N, K, X, M, Y, flags, stream);
 }
 
 extern "C" int pnq_gemv(int type, const void* W, int64_t N, int64_t K, const void* X, int M, float* Y,
@@ -339,7 +226,6 @@ extern "C" int pnq_device_error(int32_t* code) {
     int v = 0;
     if (cudaDeviceSynchronize() != cudaSuccess) return PNQ_ERR_CUDA;  // every stream, not only the default one
     if (cudaMemcpyFromSymbol(&v, g_pnq_error_word, sizeof(int)) != cudaSuccess) return PNQ_ERR_CUDA;
-    if (v != 0 && clear_counters() != cudaSuccess) return PNQ_ERR_CUDA;
     const int zero = 0;
     if (cudaMemcpyToSymbol(g_pnq_error_word, &zero, sizeof(int)) != cudaSuccess) return PNQ_ERR_CUDA;
     *code = v;

@@ -8,6 +8,9 @@
 #include <cstdint>
 #include <cuda_fp16.h>
 
+#include <type_traits>
+#include <utility>
+
 namespace pnq {
 
 constexpr int kBlockBytes = 34;
@@ -24,7 +27,7 @@ template <> struct PnFmt<kTypePn4t> {
 };
 
 // Site codes written to the device error word when a bounded wait gives up.
-enum ErrSite : int { kErrFullWait = 1, kErrEmptyWait = 2, kErrDrainWait = 3, kErrReduceWait = 4, kErrOperandWait = 5 };
+enum ErrSite : int { kErrFullWait = 1, kErrEmptyWait = 2, kErrDrainWait = 3, kErrOperandWait = 5 };
 
 // The device error word lives in pnq_api.cu; kernels receive its address. It holds 0, or the
 // site code of the first bounded wait that gave up.
@@ -135,6 +138,12 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int 
         "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
         "l"(tmap), "r"(x), "r"(y), "r"(bar), "l"(policy)
         : "memory");
+}
+
+// The same box fetched into L2 only (no shared memory, no completion to wait for).
+__device__ __forceinline__ void tma_prefetch_l2_2d(const void* tmap, int x, int y) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(tmap), "r"(x), "r"(y)
+                 : "memory");
 }
 
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
@@ -313,6 +322,19 @@ template <int N>
 __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
+// the same with n (0..7) known only at run time
+__device__ __forceinline__ void cp_async_wait_dyn(int n) {
+    switch (n) {
+        case 0: cp_async_wait<0>(); break;
+        case 1: cp_async_wait<1>(); break;
+        case 2: cp_async_wait<2>(); break;
+        case 3: cp_async_wait<3>(); break;
+        case 4: cp_async_wait<4>(); break;
+        case 5: cp_async_wait<5>(); break;
+        case 6: cp_async_wait<6>(); break;
+        default: cp_async_wait<7>(); break;
+    }
+}
 
 // atomicAdd with acquire-release semantics at GPU scope: the writes that happen before it (in
 // this thread, or in threads ordered before it by a barrier) are visible to whoever observes the
@@ -486,5 +508,47 @@ __device__ __forceinline__ float e4m3_to_f32(uint32_t b) {
 
 // Power of two 2^e as fp32 for e in [-126, 127].
 __device__ __forceinline__ float exp2i(int e) { return __uint_as_float(static_cast<uint32_t>(e + 127) << 23); }
+
+// ---- shared-memory loads at a 32-bit shared address plus a compile-time offset ------------
+// (the offset is encoded in the instruction, so unrolled code needs one address register per
+// base, and the loads are never generic ones)
+
+template <int OFF>
+__device__ __forceinline__ uint32_t ld_shared_u32(uint32_t a) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1+%2];" : "=r"(v) : "r"(a), "n"(OFF) : "memory");
+    return v;
+}
+template <int OFF>
+__device__ __forceinline__ float ld_shared_f32(uint32_t a) {
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1+%2];" : "=f"(v) : "r"(a), "n"(OFF) : "memory");
+    return v;
+}
+template <int OFF>
+__device__ __forceinline__ uint2 ld_shared_v2(uint32_t a) {
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2+%3];" : "=r"(v.x), "=r"(v.y) : "r"(a), "n"(OFF) : "memory");
+    return v;
+}
+template <int OFF>
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t a) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4+%5];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(a), "n"(OFF)
+                 : "memory");
+    return v;
+}
+
+// f(std::integral_constant<int, I>) for I = 0 .. N - 1, unrolled at compile time.
+template <class F, int... I>
+__device__ __forceinline__ void static_for_impl(F&& f, std::integer_sequence<int, I...>) {
+    (f(std::integral_constant<int, I>{}), ...);
+}
+template <int N, class F>
+__device__ __forceinline__ void static_for(F&& f) {
+    static_for_impl(f, std::make_integer_sequence<int, N>{});
+}
 
 }  // namespace pnq

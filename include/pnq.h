@@ -4,13 +4,11 @@
  *
  * Conventions shared by every entry point
  *   - Returns PNQ_OK (0) or a negative pnq_status. Nothing aborts; no kernel traps.
- *   - Device pointers are plain CUDA device addresses owned by the caller. The only device
- *     memory the library allocates is the workspace of the fast GEMV paths (pnq_gemv,
- *     pnq_gemv_ex): fp32 partial sums and u32 tile counters, one workspace per (device,
- *     stream), allocated on the first call that needs it, grown when a larger shape comes
- *     and kept until the process exits (a captured graph may still refer to an older one).
- *     A failed allocation returns PNQ_ERR_CUDA. Two host threads must not call a GEMV on
- *     the same stream at once. pnq_gemv_noalloc, dequantize and validate allocate nothing.
+ *   - Device pointers are plain CUDA device addresses owned by the caller. The library
+ *     allocates no device memory in any entry point: the fast GEMV paths sum their partial
+ *     results on chip (shared memory, and distributed shared memory between the two CTAs of
+ *     a thread-block cluster), so calls may be made from any stream, during stream capture,
+ *     and from several host threads at once.
  *   - Calls are asynchronous and ordered on `stream` (0 = the legacy default stream).
  *     Argument errors are reported before anything is launched; a launch failure is
  *     reported as PNQ_ERR_CUDA. Results are valid once the stream reaches the call.
@@ -35,8 +33,10 @@
  *     multiplier (the TandemLLM reading).
  *
  * Fast paths (taken automatically, never required)
- *   PN: W 16-byte aligned and (K/BLK) % 8 == 0.  NVFP4: codes and scales 16-byte
- *   aligned and K % 256 == 0. Other layouts run a slower path with identical results.
+ *   PN: W and X 16-byte aligned and (K/BLK) % 8 == 0.  NVFP4: codes, scales and X 16-byte
+ *   aligned and K % 256 == 0. Other layouts run a slower (generic) path within the same
+ *   accuracy bound; it is several times slower, so callers who care about speed should
+ *   allocate W and X with 16-byte alignment (any cudaMalloc result is 256-byte aligned).
  */
 #ifndef PNQ_H
 #define PNQ_H
@@ -60,7 +60,7 @@ enum pnq_status {
     PNQ_ERR_CUDA = -5,   /* a CUDA call failed (launch error, no device, bad stream) */
     PNQ_ERR_DEVICE = -6, /* a kernel gave up on an internal wait (see pnq_device_error) */
     PNQ_ERR_FLAGS = -7,  /* unknown bit in a flags argument */
-    PNQ_ERR_SCRATCH = -8 /* pnq_gemv_noalloc: the shape needs more than the built-in scratch */
+    PNQ_ERR_SCRATCH = -8 /* reserved (no entry point of this version returns it) */
 };
 
 /* Flags of pnq_gemv_ex. */
@@ -115,20 +115,12 @@ int pnq_gemv_ex(int type, const void* W, int64_t N, int64_t K, const void* X, in
  * for callers that cannot call cudaMalloc: code running under a caching or arena allocator that
  * owns all device memory, a section being captured into a graph where a first-time allocation
  * must not happen, or a runtime that forbids allocation after start-up. Same arguments, results
- * (bit for bit) and errors as pnq_gemv_ex, plus PNQ_ERR_SCRATCH.
- *   Scratch: the fast paths' (PN and NVFP4) cross-CTA partial sums and tile counters live in one
- *   file-scope __device__ array of PNQ_NOALLOC_SCRATCH_BYTES (4 MiB) that every GPU loading the
- *   library holds until the process exits. A shape that needs more (see the fast paths' work
- *   split: row tiles x K units x M x 128 floats) returns PNQ_ERR_SCRATCH before anything is
- *   launched; calls that fit never allocate, through CUDA or any library.
- *   Set-up: the first call on a device, with that device current, looks up the array's device
- *   address (cudaGetSymbolAddress); make that first call before any stream capture.
- *   Sharing: every call on a device uses the same array and leaves its tile counters at zero
- *   (they start at zero when the library loads; pnq_device_error re-zeroes them after a kernel
- *   gave up). Calls that overlap on the GPU (different streams, or graphs replayed
- *   concurrently) race on the array: order them, e.g. on one stream.
+ * (bit for bit) and errors as pnq_gemv_ex.
+ *   Scratch: none. The fast paths keep every partial sum on chip (see the conventions above),
+ *   so this entry point runs exactly the kernels pnq_gemv_ex runs; it stays as the name a
+ *   caller can hold the library to: whatever later versions add, it will never allocate, and it
+ *   never returns PNQ_ERR_SCRATCH in this version. Calls on different streams may overlap.
  */
-#define PNQ_NOALLOC_SCRATCH_BYTES (4u * 1024u * 1024u)
 int pnq_gemv_noalloc(int type, const void* W, int64_t N, int64_t K, const void* X, int M, float* Y,
                      unsigned int flags, cudaStream_t stream);
 
@@ -158,12 +150,12 @@ int pnq_validate_row(int type, const void* W, int64_t n_rows, int64_t K, int32_t
  * pnq_device_error -- reads and clears the library's device error word on the current
  * device (synchronous: waits for all work on the device; not for use during stream capture).
  * *code = 0 when no kernel has given up on a bounded internal wait since the last call;
- * otherwise the nonzero site code of the first one (1: a consumer's wait for data, 2: the
- * producer's wait for a free stage, 3: the final wait for copies in flight), and the call
- * returns PNQ_ERR_DEVICE. With a nonzero code it also zeroes the tile counters of every GEMV
- * workspace and of the no-alloc scratch on the device, so later GEMVs start from a clean
- * state; the Y of a GEMV that gave up is unspecified. Other returns: PNQ_OK, PNQ_ERR_NULL,
- * PNQ_ERR_CUDA. (Library plumbing; the pages define no such call.)
+ * otherwise the nonzero site code of the first one (1: a consumer's wait for a weight stage or
+ * for the operands of a K unit, 2: the producer's wait for a free stage, 3: the producer's final
+ * wait for copies in flight, 5: a builder's wait for a free operand slot), and the call returns
+ * PNQ_ERR_DEVICE. The Y of a GEMV that gave up is unspecified; later GEMVs are unaffected (no
+ * state outlives a launch). Other returns: PNQ_OK, PNQ_ERR_NULL, PNQ_ERR_CUDA. (Library
+ * plumbing; the pages define no such call.)
  */
 int pnq_device_error(int32_t* code);
 

@@ -179,7 +179,8 @@ from block_quantized_weight_pn3t_gb300 import synth
 import oracle
 from gpu_util import assert_within_tolerance
 out = []
-for type_, N, K, M in [(124, 200, 80*48, 1), (125, 130, 64*80, 3), (125, 64, 64*8, 16), (124, 17, 80*16, 8)]:
+for type_, N, K, M in [(124, 200, 80*48, 1), (125, 130, 64*80, 3), (125, 64, 64*8, 16), (124, 17, 80*16, 8),
+                      (124, 1000, 80*16, 4), (125, 777, 64*272, 2), (124, 9, 80*8, 1), (125, 2500, 64*24, 12)]:
     W = synth.pn_random_blocks(type_, N, K, seed=N + K)
     X = synth.activations(M, K, seed=M)
     for flags in (0, pnq.GEMV_STATIC_WEIGHTS):
@@ -197,16 +198,13 @@ print(json.dumps({{"ok": True, "device_error": pnq.device_error()}}))
 """
 
 
-@pytest.mark.parametrize("pn_cfg,nv_cfg", [("1,0,0,0", "2,0,0,0"), ("2,0,0,0", "1,0,0,0"), ("1,7,0,2", "2,7,3,3"),
-                                            ("2,13,3,3", "1,13,0,3"), ("1,152,0,8", "1,152,4,8"),
-                                            ("2,3,4,5", "2,3,2,5"), ("1,40,3,4", "1,40,0,4"),
-                                            ("1,0,0,0,2", "1,0,0,0,2"), ("2,13,0,3,2", "2,40,0,0,2"),
-                                            ("1,0,0,0,1", "2,0,3,0,1")])
+@pytest.mark.parametrize("pn_cfg,nv_cfg", [("1,0", "2,0"), ("2,0", "1,0"), ("1,3", "1,6"), ("2,3", "2,3"),
+                                            ("1,6", "2,4"), ("2,6", "1,3"), ("2,4", "0,5"), ("1,5", "0,3"),
+                                            ("0,3", "1,4"), ("0,6", "2,6")])
 def test_tile_and_grid_configs(pn_cfg, nv_cfg):
-    """Forced configurations, read once per process (so each runs in a child): PN path through
-    PNQ_PN_CFG, NVFP4 path through PNQ_NV_CFG, both "tiles per warp, grid size, operand slots,
-    stages, item order" (small grids make CTAs span several K units and share row tiles; order 2
-    = grouped unit-major items, operand slots > 0 = the streaming ring)."""
+    """Forced configurations, read once per process (so each runs in a child): the PN path through
+    PNQ_PN_CFG and the NVFP4 path through PNQ_NV_CFG, both "CTAs per cluster, weight stages" (0 =
+    automatic)."""
     env = dict(os.environ, PNQ_PN_CFG=pn_cfg, PNQ_NV_CFG=nv_cfg, PNQ_FORCE_KERNEL="mma")
     r = subprocess.run([sys.executable, "-c", CHILD.format(root=ROOT)], env=env, capture_output=True, text=True,
                        timeout=600)

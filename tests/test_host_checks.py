@@ -1,15 +1,11 @@
 """Host checks of the fast paths' launch logic, compiled for the CPU with nvcc (no GPU needed:
 kernels are compiled but never launched):
 
-- tests/host/sched_check.cu: the stream-K work split the tensor-core GEMV kernels share (Sched
-  in csrc/pnq_streamk.cuh) over thousands of (row tiles, K units, grid, item order)
-  configurations against brute force: item bijection, CTA shares, each tile's partial-share
-  count (the tile counter's target), the workspace slots the finishing CTA reads, and the
-  resident operand span.
-- tests/host/plan_check_pn.cu, plan_check_nvfp4.cu: the PN and NVFP4 launch planners over
-  shapes, batch widths 1-16 and forced configurations: every accepted plan's shared-memory
-  regions are disjoint, aligned and inside the limit, the share lists hold the largest share,
-  the resident slots cover the widest share, and the workspace flag matches tile sharing.
+- tests/host/split_check.cu: the cluster work split (csrc/pnq_split.cuh) and the launch planner
+  (csrc/pnq_cluster.cuh) with the PN and NVFP4 format policies: row ranges and item shares tile
+  the matrix, stage walks visit exactly a CTA's items, a row group always falls to one consumer
+  warp, and every plan's shared-memory regions are disjoint, aligned and inside the budget it
+  claims (two CTAs per SM, or one).
 """
 import concurrent.futures
 import os
@@ -21,7 +17,7 @@ import pytest
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 CSRC = os.path.join(ROOT, "block_quantized_weight_pn3t_gb300", "csrc")
 HOST = os.path.join(ROOT, "tests", "host")
-CHECKS = {"sched_check": 5000, "plan_check_pn": 100000, "plan_check_nvfp4": 100000}  # least count expected
+CHECKS = {"split_check": 60000}  # least count expected
 
 
 def nvcc():
