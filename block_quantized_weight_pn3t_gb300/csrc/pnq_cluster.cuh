@@ -136,18 +136,6 @@ __global__ void __launch_bounds__(F::THREADS, F::MINB) cluster_gemv_kernel(const
             const int pieces_c = ct.rows / kPieceRows;
             for (; ok && wk.next(st); ++s) {
                 const int slot = s % S;
-                if (s == S && (a.flags & kStaticWeights)) {
-                    // the ring is full: ask L2 for the rest of the share now, so HBM keeps streaming
-                    // while this grid waits for x and for its previous grid (the copies below then
-                    // hit L2)
-                    StageWalk pw = wk;
-                    Stage ps = st;
-                    do {
-                        const int q0 = 2 * ps.g0, q1 = min(2 * ps.g1, pieces_c);
-                        const int rb = static_cast<int>(ct.row0) + q0 * kPieceRows;
-                        for (int p = 0; p < q1 - q0; ++p) F::prefetch(ka.map, ps.u, rb + p * kPieceRows);
-                    } while (pw.next(ps));
-                }
                 if (s >= S && !mbar_wait_bounded(sm.empty(slot), ((s / S) - 1) & 1)) {
                     ok = false;
                     break;
@@ -156,8 +144,14 @@ __global__ void __launch_bounds__(F::THREADS, F::MINB) cluster_gemv_kernel(const
                 mbar_arrive_expect_tx(sm.full(slot), static_cast<uint32_t>((pc1 - pc0) * F::PIECE_TX));
                 const uint32_t dst = smem_addr(sm.stage(slot));
                 const int row_b = static_cast<int>(ct.row0) + pc0 * kPieceRows;
-                for (int p = 0; p < pc1 - pc0; ++p)
-                    F::issue(ka.map, dst, p, st.u, row_b + p * kPieceRows, sm.full(slot), pol);
+                if (pc1 - pc0 == 2 * kStageGroups) {
+                    // a whole stage: one copy of 64 rows (the copy engine's cost grows with the number
+                    // of copies and rows it handles, far more than with bytes)
+                    F::issue_stage(ka.map, dst, st.u, row_b, sm.full(slot), pol);
+                } else {
+                    for (int p = 0; p < pc1 - pc0; ++p)
+                        F::issue(ka.map, dst, p, st.u, row_b + p * kPieceRows, sm.full(slot), pol);
+                }
             }
             if (!ok) record_error(a.err, kErrEmptyWait);
             // every copy issued has landed before the CTA may exit
@@ -323,8 +317,11 @@ inline int cl_units(const Split::Cta& t) {
 // Estimated time of one CTA's share: its bytes at the per-SM share of HBM, the serial work of its
 // busiest consumer warp (F::GROUP_S seconds per row group and unit), or the round trips for x
 // (XS units in flight, ~0.8 us each), whichever is longest, plus the cluster's final sum.
+// per = CTAs of this launch sharing an SM (its HBM share and issue slots); S = weight stages: a
+// CTA's stream rate is bounded by the stages in flight (all but the two its consumer groups hold)
+// over the loaded HBM latency (~1.8 us).
 template <class F>
-double cl_cta_cost(const Split& sp, int block, int XS) {
+double cl_cta_cost(const Split& sp, int block, int XS, int per, int S) {
     const Split::Cta t = sp.cta(block);
     StageWalk wk(t);
     Stage st;
@@ -337,8 +334,9 @@ double cl_cta_cost(const Split& sp, int block, int XS) {
     }
     int most = 0;
     for (int w : per_warp) most = std::max(most, w);
-    const double bytes_s = static_cast<double>(pieces) * F::PIECE_TX / 42e9;
-    const double warp_s = most * F::GROUP_S;
+    const double rate = std::min(42e9 / per, std::max(1, S - 2) * static_cast<double>(F::STAGE_BYTES) / 1.8e-6);
+    const double bytes_s = static_cast<double>(pieces) * F::PIECE_TX / rate;
+    const double warp_s = most * F::GROUP_S * (per > 1 ? 1.4 : 1.0);
     const double x_s = (cl_units(t) + XS - 1) / XS * 0.8e-6;
     return std::max(std::max(bytes_s, warp_s), x_s) + (sp.C > 1 ? 0.3e-6 : 0.0);
 }
@@ -359,16 +357,19 @@ inline int cl_rows_max(const Split& sp) {
     return static_cast<int>((most * kPieceRows + kGroupRows - 1) / kGroupRows * kGroupRows);
 }
 
-// A layout that leaves room for a second CTA per SM, else one that fits one: x slots for as many
-// of the CTA's units as possible (up to 8; then 4, 2, 1), and within that the deepest weight ring
-// (6..3 stages, or s_req). nu = the most units any CTA of the plan touches.
+// A layout for one CTA per SM (pair = false: up to the whole shared memory) or two (pair = true):
+// x slots for as many of the CTA's units as possible (up to 4; then 2, 1), and within that the
+// deepest weight ring (kMaxStages..3 stages, or s_req). nu = the most units any CTA of the plan
+// touches.
+constexpr int kMaxStages = 12;
 template <class F>
-bool cl_fit_layout(int M, int s_req, int nu, ClPlan& q) {
+bool cl_fit_layout(int M, int s_req, int nu, bool pair, ClPlan& q) {
     for (uint32_t budget : {kSmemPair, kSmemOne}) {
-        if (budget == kSmemPair && F::MINB < 2) continue;
-        for (int xs : {8, 4, 2, 1}) {
+        if (budget == kSmemPair && (F::MINB < 2 || !pair)) continue;
+        if (budget == kSmemOne && pair) continue;
+        for (int xs : {4, 2, 1}) {
             const int XS = std::max(1, std::min(xs, nu));
-            for (int S = (s_req > 0 ? s_req : 6); S >= (s_req > 0 ? s_req : 3); --S) {
+            for (int S = (s_req > 0 ? s_req : kMaxStages); S >= (s_req > 0 ? s_req : 3); --S) {
                 cl_layout<F>(M, S, XS, q);
                 if (q.total + 1024u <= budget) {
                     q.minb = (budget == kSmemPair) ? 2 : 1;
@@ -380,36 +381,41 @@ bool cl_fit_layout(int M, int s_req, int nu, ClPlan& q) {
     return false;
 }
 
-// Cluster size (1 or 2: both spread one CTA per SM over all SMs of the part), clusters and ring
-// depth for one shape: the plan with the smallest estimated time.
+// Cluster size (1 or 2: both spread one CTA per SM over all SMs of the part), CTAs of the launch
+// per SM (2 when two fit: twice the warps on the launch's work), clusters and ring depth for one
+// shape: the plan with the smallest estimated time. c_req / s_req / k_req > 0 force the cluster
+// size, the stages and the CTAs per SM.
 template <class F>
-bool cl_make_plan(int64_t N, int U, int M, int sms, int c_req, int s_req, ClPlan& p) {
+bool cl_make_plan(int64_t N, int U, int M, int sms, int c_req, int s_req, int k_req, ClPlan& p) {
     bool found = false;
     double best = 0.0;
-    for (int C : {1, 2}) {
-        if (c_req > 0 && C != c_req) continue;
-        if (sms / C < 1) continue;
-        for (int waves = 1; waves <= 64; ++waves) {
-            Split sp = cl_split(N, U, sms, C, waves);
-            if (static_cast<int64_t>(cl_rows_max(sp) / kGroupRows) * U > INT32_MAX) continue;
-            ClPlan q;
-            q.sp = sp;
-            q.rc = cl_rows_max(sp);
-            int nu = 0;
-            for (int b = 0; b < sp.ncl * C; ++b) nu = std::max(nu, cl_units(sp.cta(b)));
-            if (!cl_fit_layout<F>(M, s_req, nu, q)) {
-                if (sp.ncl >= sp.pieces) break;
-                continue;  // more, smaller clusters
+    for (int per : {2, 1}) {
+        if ((per == 2 && F::MINB < 2) || (k_req > 0 && per != k_req)) continue;
+        for (int C : {1, 2}) {
+            if (c_req > 0 && C != c_req) continue;
+            if (sms / C < 1) continue;
+            for (int waves = 1; waves <= 64; ++waves) {
+                Split sp = cl_split(N, U, sms * per, C, waves);
+                if (static_cast<int64_t>(cl_rows_max(sp) / kGroupRows) * U > INT32_MAX) continue;
+                ClPlan q;
+                q.sp = sp;
+                q.rc = cl_rows_max(sp);
+                int nu = 0;
+                for (int b = 0; b < sp.ncl * C; ++b) nu = std::max(nu, cl_units(sp.cta(b)));
+                if (!cl_fit_layout<F>(M, s_req, nu, per == 2, q)) {
+                    if (sp.ncl >= sp.pieces) break;
+                    continue;  // more, smaller clusters
+                }
+                double cost = 0.0;
+                for (int b = 0; b < sp.ncl * C; ++b) cost = std::max(cost, cl_cta_cost<F>(sp, b, q.xs, per, q.S));
+                cost *= waves;
+                if (!found || cost < best * 0.98) {
+                    p = q;
+                    best = cost;
+                    found = true;
+                }
+                break;
             }
-            double cost = 0.0;
-            for (int b = 0; b < sp.ncl * C; ++b) cost = std::max(cost, cl_cta_cost<F>(sp, b, q.xs));
-            cost *= waves;
-            if (!found || cost < best * 0.98) {
-                p = q;
-                best = cost;
-                found = true;
-            }
-            break;
         }
     }
     return found;
@@ -417,18 +423,18 @@ bool cl_make_plan(int64_t N, int U, int M, int sms, int c_req, int s_req, ClPlan
 
 struct PlanKey {
     const void* kern;
-    int M, sms, c, s, U;
+    int M, sms, c, s, k, U;
     int64_t N;
     bool operator<(const PlanKey& o) const {
-        return std::tie(kern, M, sms, c, s, U, N) < std::tie(o.kern, o.M, o.sms, o.c, o.s, o.U, o.N);
+        return std::tie(kern, M, sms, c, s, k, U, N) < std::tie(o.kern, o.M, o.sms, o.c, o.s, o.k, o.U, o.N);
     }
 };
 
 template <class F>
-bool cl_cached_plan(int64_t N, int U, int M, int sms, int c_req, int s_req, ClPlan& p) {
+bool cl_cached_plan(int64_t N, int U, int M, int sms, int c_req, int s_req, int k_req, ClPlan& p) {
     static std::mutex mu;
     static std::map<PlanKey, ClPlan> cache;
-    const PlanKey key{reinterpret_cast<const void*>(&cl_make_plan<F>), M, sms, c_req, s_req, U, N};
+    const PlanKey key{reinterpret_cast<const void*>(&cl_make_plan<F>), M, sms, c_req, s_req, k_req, U, N};
     {
         std::lock_guard<std::mutex> lock(mu);
         auto it = cache.find(key);
@@ -437,7 +443,7 @@ bool cl_cached_plan(int64_t N, int U, int M, int sms, int c_req, int s_req, ClPl
             return true;
         }
     }
-    if (!cl_make_plan<F>(N, U, M, sms, c_req, s_req, p)) return false;
+    if (!cl_make_plan<F>(N, U, M, sms, c_req, s_req, k_req, p)) return false;
     std::lock_guard<std::mutex> lock(mu);
     if (cache.size() < 4096) cache.emplace(key, p);
     return true;
@@ -445,10 +451,10 @@ bool cl_cached_plan(int64_t N, int U, int M, int sms, int c_req, int s_req, ClPl
 
 // Plans and launches one GEMV; ka.map / ka.e / X, Y, err, N, K, M filled by the caller.
 template <class F>
-cudaError_t cl_launch(KArgs<F>& ka, int64_t N, int U, int c_req, int s_req, bool static_weights,
+cudaError_t cl_launch(KArgs<F>& ka, int64_t N, int U, const int (&req)[3], bool static_weights,
                       cudaStream_t stream) {
     ClPlan p;
-    if (!cl_cached_plan<F>(N, U, ka.c.M, device_sm_count(), c_req, s_req, p)) return cudaErrorNotSupported;
+    if (!cl_cached_plan<F>(N, U, ka.c.M, device_sm_count(), req[0], req[1], req[2], p)) return cudaErrorNotSupported;
     auto kern = cluster_gemv_kernel<F>;
     static std::atomic<bool> opted[64];  // the attribute is set once per device (threads may race to set it)
     int dev = 0;
@@ -489,13 +495,14 @@ cudaError_t cl_launch(KArgs<F>& ka, int64_t N, int U, int c_req, int s_req, bool
     return cudaLaunchKernelEx(&lc, kern, ka);
 }
 
-// Environment override "cluster,stages" (fields 0 = automatic) from variable `name`, read once per
-// call site (each fast path keeps its own static copy).
-inline void env_cluster_config(const char* name, int (&v)[2]) {
-    v[0] = v[1] = 0;
+// Environment override "cluster,stages,ctas per SM[,path]" (fields 0 = automatic) from variable
+// `name`, read once per call site (each fast path keeps its own static copy).
+template <int NV>
+inline void env_cluster_config(const char* name, int (&v)[NV]) {
+    for (int n = 0; n < NV; ++n) v[n] = 0;
     if (const char* e = std::getenv(name)) {
         const char* p = e;
-        for (int n = 0; n < 2 && *p; ++n) {
+        for (int n = 0; n < NV && *p; ++n) {
             v[n] = static_cast<int>(std::strtol(p, const_cast<char**>(&p), 10));
             if (*p == ',') ++p;
         }

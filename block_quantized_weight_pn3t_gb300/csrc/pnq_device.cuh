@@ -91,13 +91,15 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parit
 }
 
 // Waits for the phase with the given parity; gives up after ~limit_ns of wall time and
-// returns false (the caller records the error and skips its work).
+// returns false (the caller records the error and skips its work). The probe is the plain
+// try_wait (it blocks for a short, hardware-chosen time); a suspend-time hint let waiters
+// sleep far past the phase's completion when the last arrival was a bulk copy's.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
                                                   uint64_t limit_ns = 2000000000ull) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     while (true) {
-        if (mbar_try_wait_sleep(bar, parity, 1000000u)) return true;
+        if (mbar_try_wait(bar, parity)) return true;
         if (global_timer_ns() - t0 > limit_ns) return false;
     }
 }
@@ -138,12 +140,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int 
         "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
         "l"(tmap), "r"(x), "r"(y), "r"(bar), "l"(policy)
         : "memory");
-}
-
-// The same box fetched into L2 only (no shared memory, no completion to wait for).
-__device__ __forceinline__ void tma_prefetch_l2_2d(const void* tmap, int x, int y) {
-    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(tmap), "r"(x), "r"(y)
-                 : "memory");
 }
 
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }

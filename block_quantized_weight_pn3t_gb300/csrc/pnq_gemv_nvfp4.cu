@@ -77,7 +77,7 @@ __device__ __forceinline__ void nv_build_row(uint8_t* rec, float* so, const uint
 // The NVFP4 format policy of the cluster pipeline.
 template <int NT>
 struct NvMma {
-    static constexpr int MAPS = 2;  // codes, scales
+    static constexpr int MAPS = 4;  // codes, scales with 8-row boxes (pieces); the same with 64-row boxes (stages)
     struct Extra {
         float g;
     };
@@ -110,9 +110,10 @@ struct NvMma {
         tma_load_2d(dst + p * kPieceRows * kCodeRow, &maps[0], u * (kCodeRow / 4), row, bar, pol);
         tma_load_2d(dst + kCodeStage + p * kPieceRows * kScaleRow, &maps[1], u * (kScaleRow / 4), row, bar, pol);
     }
-    static __device__ __forceinline__ void prefetch(const CUtensorMap* maps, int u, int row) {
-        tma_prefetch_l2_2d(&maps[0], u * (kCodeRow / 4), row);
-        tma_prefetch_l2_2d(&maps[1], u * (kScaleRow / 4), row);
+    static __device__ __forceinline__ void issue_stage(const CUtensorMap* maps, uint32_t dst, int u, int row,
+                                                       uint32_t bar, uint64_t pol) {
+        tma_load_2d(dst, &maps[2], u * (kCodeRow / 4), row, bar, pol);
+        tma_load_2d(dst + kCodeStage, &maps[3], u * (kScaleRow / 4), row, bar, pol);
     }
     static __device__ __forceinline__ void zero_half(uint8_t* stg, int lg, int lane) {
         uint32_t* zc = reinterpret_cast<uint32_t*>(stg + (lg * kGroupRows + 8) * kCodeRow);
@@ -202,11 +203,10 @@ struct NvMma {
 };
 
 template <int NT>
-cudaError_t launch_nt(const CUtensorMap (&maps)[2], float g, const uint16_t* X, float* Y, int* err, int64_t N,
-                      int64_t K, int M, int U, int c_req, int s_req, bool static_weights, cudaStream_t stream) {
+cudaError_t launch_nt(const CUtensorMap (&maps)[4], float g, const uint16_t* X, float* Y, int* err, int64_t N,
+                      int64_t K, int M, int U, const int (&req)[3], bool static_weights, cudaStream_t stream) {
     KArgs<NvMma<NT>> ka{};
-    ka.map[0] = maps[0];
-    ka.map[1] = maps[1];
+    for (int i = 0; i < 4; ++i) ka.map[i] = maps[i];
     ka.e.g = g;
     ka.c.X = X;
     ka.c.Y = Y;
@@ -214,7 +214,7 @@ cudaError_t launch_nt(const CUtensorMap (&maps)[2], float g, const uint16_t* X, 
     ka.c.N = static_cast<int>(N);
     ka.c.K = static_cast<int>(K);
     ka.c.M = M;
-    return cl_launch<NvMma<NT>>(ka, N, U, c_req, s_req, static_weights, stream);
+    return cl_launch<NvMma<NT>>(ka, N, U, req, static_weights, stream);
 }
 
 }  // namespace
@@ -227,18 +227,19 @@ cudaError_t launch_nvfp4_gemv_mma(const Nvfp4View& w, int64_t N, int64_t K, cons
     if (reinterpret_cast<uintptr_t>(w.codes) % 16 != 0 || reinterpret_cast<uintptr_t>(w.scales) % 16 != 0 ||
         reinterpret_cast<uintptr_t>(X) % 16 != 0)
         return cudaErrorNotSupported;
-    CUtensorMap maps[2];
+    CUtensorMap maps[4];
     if (!encode_u32_map(&maps[0], w.codes, N, K / 8, kCodeRow / 4, kPieceRows, true) ||
-        !encode_u32_map(&maps[1], w.scales, N, K / 64, kScaleRow / 4, kPieceRows, false))
+        !encode_u32_map(&maps[1], w.scales, N, K / 64, kScaleRow / 4, kPieceRows, false) ||
+        !encode_u32_map(&maps[2], w.codes, N, K / 8, kCodeRow / 4, kStageRows, true) ||
+        !encode_u32_map(&maps[3], w.scales, N, K / 64, kScaleRow / 4, kStageRows, false))
         return cudaErrorNotSupported;
-    static int env[2];  // PNQ_NV_CFG = "CTAs per cluster, stages", read once
+    static int env[3];  // PNQ_NV_CFG = "CTAs per cluster, stages, CTAs per SM", read once
     static std::once_flag once;
     std::call_once(once, [] { env_cluster_config("PNQ_NV_CFG", env); });
-    if (c_req <= 0) c_req = env[0];
-    if (s_req <= 0) s_req = env[1];
+    const int req[3] = {c_req > 0 ? c_req : env[0], s_req > 0 ? s_req : env[1], env[2]};
     const int U = static_cast<int>(K / kUnitK);
-    if (M <= 8) return launch_nt<1>(maps, w.g, X, Y, err, N, K, M, U, c_req, s_req, static_weights, stream);
-    return launch_nt<2>(maps, w.g, X, Y, err, N, K, M, U, c_req, s_req, static_weights, stream);
+    if (M <= 8) return launch_nt<1>(maps, w.g, X, Y, err, N, K, M, U, req, static_weights, stream);
+    return launch_nt<2>(maps, w.g, X, Y, err, N, K, M, U, req, static_weights, stream);
 }
 
 }  // namespace pnq

@@ -42,14 +42,17 @@ constexpr int kUnitU32 = kUnitBytes / 4;                 // 68
 constexpr int kStageBytes = kStageRows * kUnitBytes;     // 17408
 constexpr int kPieceBytes = kPieceRows * kUnitBytes;     // 2176 (one copy)
 
-template <int TYPE, int NT>
+// LR = lanes whose B records are stored (32, or the 8M lanes of the live columns when one n8 tile
+// is only partly used: the other lanes read a live column's record).
+template <int TYPE, int NT, int LR = 32>
 struct Cfg {
     using F = PnFmt<TYPE>;
     static constexpr int STEPS = F::PAIRS;
     static constexpr int UK = kUnitBlocks * F::BLK;     // weights of a row per unit (640 / 512)
     // B records of one (block, n8 tile): STEPS / 2 pairs of steps as 16-byte lane records, then
     // the odd last step as 8-byte lane records
-    static constexpr int PB = (STEPS / 2) * 512 + (STEPS & 1) * 256;
+    static constexpr int PAIR = LR * 16;                // bytes of one pair-of-steps record group
+    static constexpr int PB = (STEPS / 2) * PAIR + (STEPS & 1) * LR * 8;
     static constexpr int REC = kUnitBlocks * NT * PB;   // bytes of one unit's B operands
     static constexpr int SH = (TYPE == kTypePn3t) ? 9 : 8;
     static constexpr int JS = (TYPE == kTypePn3t) ? 3 : 2;  // pairs below the shift
@@ -88,9 +91,9 @@ __device__ __forceinline__ int pn_elem(int cpw, bool odd, int c, int r, int j, i
 // B operands of one K unit for activation row m (one builder warp): sigma from the row's largest
 // |x| over the unit, the hi / lo lane records of every (block, lane column, pair) and the blocks'
 // zero-point terms; xr = the unit's x row in shared memory.
-template <int TYPE, int NT>
+template <int TYPE, int NT, int LR = 32>
 __device__ __forceinline__ void build_row(uint8_t* rec, float* zb, float* so, const float* xr, int m, int lane) {
-    using C = Cfg<TYPE, NT>;
+    using C = Cfg<TYPE, NT, LR>;
     using F = PnFmt<TYPE>;
     constexpr int STEPS = C::STEPS, UK = C::UK;
     uint32_t mx = 0;  // a non-negative float's bits order like its value
@@ -131,11 +134,11 @@ __device__ __forceinline__ void build_row(uint8_t* rec, float* zb, float* so, co
             }
             uint8_t* tb = rec + (blk * NT + t) * C::PB;
             if (j < 2 * (STEPS / 2)) {
-                uint8_t* p = tb + (j >> 1) * 512 + (j & 1) * 8;
+                uint8_t* p = tb + (j >> 1) * C::PAIR + (j & 1) * 8;
                 *reinterpret_cast<uint2*>(p + (lh + c) * 16) = make_uint2(hi[0], hi[1]);
                 *reinterpret_cast<uint2*>(p + (ll + c) * 16) = make_uint2(lo[0], lo[1]);
             } else {
-                uint8_t* p = tb + (STEPS / 2) * 512;
+                uint8_t* p = tb + (STEPS / 2) * C::PAIR;
                 *reinterpret_cast<uint2*>(p + (lh + c) * 8) = make_uint2(hi[0], hi[1]);
                 *reinterpret_cast<uint2*>(p + (ll + c) * 8) = make_uint2(lo[0], lo[1]);
             }
@@ -162,30 +165,31 @@ __device__ __forceinline__ void build_row(uint8_t* rec, float* zb, float* so, co
 // activation row 4t + c). The blocks' mma chains are interleaved step by step, so a warp keeps
 // NBK independent accumulations in flight. Every shared-memory load is a 32-bit shared address
 // in a register plus a compile-time offset:
-//   srow / srow_c: row g of the group (srow_c = srow + 4c, lane column c's words);
+//   srow[h] / srow_c[h]: row g (h = 0) and row g + 8 (h = 1) of the group at the K unit's first
+//   byte (srow_c = srow + 4c, lane column c's words), so any row stride works;
 //   srec[t]: the B records of tile t at the lane's record (lanes of columns past 2M read a live
 //   column's record: their sums are never used), srec_h[t] the same for 8-byte records;
 //   szb[t]: the zero-point term of the lane's activation row (clamped the same way).
-template <int TYPE, int NT, int B0, int NBK>
-__device__ __forceinline__ void pn_blocks(uint32_t srow, uint32_t srow_c, uint32_t sel, const uint32_t (&srec)[NT],
-                                          const uint32_t (&srec_h)[NT], const uint32_t (&szb)[NT],
-                                          float (&acc)[NT][2]) {
-    using Cf = Cfg<TYPE, NT>;
+template <int TYPE, int NT, int B0, int NBK, int LR = 32>
+__device__ __forceinline__ void pn_blocks(const uint32_t (&srow)[2], const uint32_t (&srow_c)[2], uint32_t sel,
+                                          const uint32_t (&srec)[NT], const uint32_t (&srec_h)[NT],
+                                          const uint32_t (&szb)[NT], float (&acc)[NT][2]) {
+    using Cf = Cfg<TYPE, NT, LR>;
     constexpr int STEPS = Cf::STEPS;
     uint32_t ra[NBK][2], rb[NBK][2], sa[NBK][2], sb[NBK][2];
     float d[NBK][2], z[NBK][NT];
     static_for<NBK>([&](auto I) {
         constexpr int i = decltype(I)::value, B = B0 + i;
         static_for<2>([&](auto Hh) {
-            constexpr int h = decltype(Hh)::value, OFF = h * 8 * kUnitBytes + kBlockBytes * B;
+            constexpr int h = decltype(Hh)::value, OFF = kBlockBytes * B;
             if constexpr (B & 1) {
-                ra[i][h] = ld_shared_u32<OFF + 2>(srow_c);
-                rb[i][h] = ld_shared_u32<OFF + 18>(srow_c);
-                d[i][h] = half_hi(ld_shared_u32<OFF - 2>(srow));
+                ra[i][h] = ld_shared_u32<OFF + 2>(srow_c[h]);
+                rb[i][h] = ld_shared_u32<OFF + 18>(srow_c[h]);
+                d[i][h] = half_hi(ld_shared_u32<OFF - 2>(srow[h]));
             } else {
-                const uint32_t q0 = ld_shared_u32<OFF>(srow);
-                ra[i][h] = ld_shared_u32<OFF + 4>(srow_c);
-                rb[i][h] = prmt(ld_shared_u32<OFF + 20>(srow_c), q0, sel);
+                const uint32_t q0 = ld_shared_u32<OFF>(srow[h]);
+                ra[i][h] = ld_shared_u32<OFF + 4>(srow_c[h]);
+                rb[i][h] = prmt(ld_shared_u32<OFF + 20>(srow_c[h]), q0, sel);
                 d[i][h] = half_lo(q0);
             }
             sa[i][h] = ra[i][h] >> Cf::SH;
@@ -205,9 +209,9 @@ __device__ __forceinline__ void pn_blocks(uint32_t srow, uint32_t srow_c, uint32
             static_for<NT>([&](auto T) {
                 constexpr int t = decltype(T)::value, RT = (B * NT + t) * Cf::PB;
                 if constexpr ((J & 1) == 0 && J + 1 < STEPS) {
-                    bq[i][t] = ld_shared_v4<RT + (J >> 1) * 512>(srec[t]);
+                    bq[i][t] = ld_shared_v4<RT + (J >> 1) * Cf::PAIR>(srec[t]);
                 } else if constexpr ((J & 1) == 0) {
-                    const uint2 v = ld_shared_v2<RT + (STEPS / 2) * 512>(srec_h[t]);
+                    const uint2 v = ld_shared_v2<RT + (STEPS / 2) * Cf::PAIR>(srec_h[t]);
                     bq[i][t].x = v.x;
                     bq[i][t].y = v.y;
                 }
@@ -239,7 +243,7 @@ __device__ __forceinline__ void pn_blocks(uint32_t srow, uint32_t srow_c, uint32
 template <int TYPE, int NT>
 struct PnMma {
     using C = Cfg<TYPE, NT>;
-    static constexpr int MAPS = 1;
+    static constexpr int MAPS = 2;  // the weights with 8-row boxes (pieces) and 64-row boxes (stages)
     struct Extra {};
     static constexpr int NB = (NT == 4) ? 3 : NT;  // builder warps (12 warps at most: 168 registers)
     static constexpr int THREADS = 32 * (kConsumerWarps + 1 + NB);
@@ -269,8 +273,9 @@ struct PnMma {
                                                  uint32_t bar, uint64_t pol) {
         tma_load_2d(dst + p * kPieceBytes, &maps[0], u * kUnitU32, row, bar, pol);
     }
-    static __device__ __forceinline__ void prefetch(const CUtensorMap* maps, int u, int row) {
-        tma_prefetch_l2_2d(&maps[0], u * kUnitU32, row);
+    static __device__ __forceinline__ void issue_stage(const CUtensorMap* maps, uint32_t dst, int u, int row,
+                                                       uint32_t bar, uint64_t pol) {
+        tma_load_2d(dst, &maps[1], u * kUnitU32, row, bar, pol);
     }
     static __device__ __forceinline__ void zero_half(uint8_t* stg, int lg, int lane) {
         uint32_t* zp = reinterpret_cast<uint32_t*>(stg + (lg * kGroupRows + 8) * kUnitBytes);
@@ -282,8 +287,9 @@ struct PnMma {
     }
     static __device__ __forceinline__ void group(const uint8_t* stg, int lg, const uint8_t* recu, const float* zbu,
                                                  int, const Lane& ln, Acc& acc) {
-        const uint32_t srow = smem_addr(stg) + static_cast<uint32_t>((lg * kGroupRows + ln.g) * kUnitBytes);
-        const uint32_t srow_c = srow + 4u * ln.c;
+        const uint32_t s0 = smem_addr(stg) + static_cast<uint32_t>((lg * kGroupRows + ln.g) * kUnitBytes);
+        const uint32_t srow[2] = {s0, s0 + 8u * kUnitBytes};
+        const uint32_t srow_c[2] = {s0 + 4u * ln.c, s0 + 8u * kUnitBytes + 4u * ln.c};
         const uint32_t rec_s = smem_addr(recu), zb_s = smem_addr(zbu);
         uint32_t srec[NT], srec_h[NT], szb[NT];
 #pragma unroll
@@ -325,29 +331,280 @@ struct PnMma {
     }
 };
 
+// ---- row-stream path (M <= 4, rows of at most a few KB) -------------------------------------------
+//
+// Each CTA owns a contiguous range of whole rows, so nothing is summed across CTAs, and a 16-row
+// group of them is one contiguous range of HBM that a single bulk copy brings into a stage (the
+// copy engine streams such copies at the full HBM rate; strips of a longer row need one request per
+// row and stream far slower). Consumer warp w owns the K units u = w, w + 8, ..: it builds their B
+// operands itself (x of its units only) and multiplies every row group over them, keeping its
+// per-row sums in its own slice of shared memory; the slices are summed in warp order at the end.
+
+constexpr int kRsWarps = 8;  // consumer warps; one producer warp more
+constexpr int kRsThreads = 32 * (kRsWarps + 1);
+constexpr int kRsMaxUnits = 2 * kRsWarps;  // K units a launch can take (two per warp)
+constexpr int kRsMaxRowBytes = 4096;       // rows longer than this take the strip path
+
+// Zeros for the rows of a CTA's last 16-row group that lie past its range (copied in by the copy
+// engine like the weights, so no warp has to clear shared memory).
+__device__ __align__(128) uint8_t g_pnq_zero_rows[(kGroupRows - 1) * kRsMaxRowBytes];
+
+struct RsArgs {
+    const uint8_t* W;
+    const float* X;
+    float* Y;
+    int* err;
+    int N, K, M, U, G, S;  // G CTAs, S stages
+    int row_bytes, rows_pad;  // rows_pad: partial rows per (warp, activation row), >= any CTA's rows
+    unsigned flags;
+    uint32_t off_rec, off_zb, off_x, off_part, off_stage, stage_bytes;
+};
+
+template <int TYPE, int LR>
+__global__ void __launch_bounds__(kRsThreads, 1) pn_rows_kernel(const __grid_constant__ RsArgs a) {
+    using C = Cfg<TYPE, 1, LR>;
+    constexpr int ZB = kUnitBlocks * 16 + 16;  // zero-point terms [block][m], then 2^(24 - sigma) [m]
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* base = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+    const uint32_t bar0 = smem_addr(base);
+    const int S = a.S, M = a.M, U = a.U;
+    auto full = [&](int s) { return bar0 + 8u * s; };
+    auto empty = [&](int s) { return bar0 + 8u * (S + s); };
+    auto stage = [&](int s) { return base + a.off_stage + static_cast<uint32_t>(s) * a.stage_bytes; };
+    auto rec = [&](int u) { return base + a.off_rec + static_cast<uint32_t>(u) * C::REC; };
+    auto zbu = [&](int u) { return reinterpret_cast<float*>(base + a.off_zb) + u * ZB; };
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int active = min(kRsWarps, U);  // consumer warps that own units
+    const int64_t r0 = static_cast<int64_t>(blockIdx.x) * a.N / a.G, r1 = static_cast<int64_t>(blockIdx.x + 1) * a.N / a.G;
+    const int nrows = static_cast<int>(r1 - r0);
+    const int ngroups = (nrows + kGroupRows - 1) / kGroupRows;
+    float* part = reinterpret_cast<float*>(base + a.off_part);  // [warp][m][rows_pad]
+
+    if (threadIdx.x == 0) {
+        griddep_launch_dependents();
+        for (int s = 0; s < S; ++s) {
+            mbar_init(full(s), 1);
+            mbar_init(empty(s), active);
+        }
+        mbar_fence_init();
+    }
+    __syncthreads();
+
+    if (warp == kRsWarps) {
+        // ---------------- producer: one bulk copy per 16-row group ----------------
+        if (lane == 0 && ngroups > 0) {
+            const uint64_t pol = l2_policy_evict_first();
+            if (!(a.flags & kStaticWeights)) griddep_wait();  // W may be written by the previous grid
+            bool ok = true;
+            int i = 0;
+            for (; i < ngroups; ++i) {
+                const int slot = i % S;
+                if (i >= S && !mbar_wait_bounded(empty(slot), ((i / S) - 1) & 1)) {
+                    ok = false;
+                    break;
+                }
+                const int rows = min(kGroupRows, nrows - i * kGroupRows);
+                const uint32_t bytes = static_cast<uint32_t>(rows * a.row_bytes);
+                const uint32_t tail = static_cast<uint32_t>((kGroupRows - rows) * a.row_bytes);
+                mbar_arrive_expect_tx(full(slot), bytes + tail);
+                bulk_g2s(smem_addr(stage(slot)), a.W + (r0 + i * kGroupRows) * a.row_bytes, bytes, full(slot), pol);
+                // the last group's rows past the CTA's: zeros (d = 0 and codes 0 add nothing)
+                if (tail) bulk_g2s_plain(smem_addr(stage(slot)) + bytes, g_pnq_zero_rows, tail, full(slot));
+            }
+            if (!ok) record_error(a.err, kErrEmptyWait);
+            bool drained = true;  // every copy issued has landed before the CTA may exit
+            for (int gg = max(0, i - S); drained && gg < i; ++gg) drained = mbar_wait_bounded(full(gg % S), (gg / S) & 1);
+            if (!drained) record_error(a.err, kErrDrainWait);
+        }
+        __syncwarp();
+    } else if (warp < active && ngroups > 0) {
+        // ---------------- consumer warp: B operands of its units, then every row group ----------------
+        griddep_wait();  // X belongs to the previous grid until now
+        float* xb = reinterpret_cast<float*>(base + a.off_x) + warp * 2 * C::UK;  // two x rows
+        for (int u = warp; u < U; u += kRsWarps) {
+            auto load = [&](int m) {
+                if (m < M) {
+                    const float* src = a.X + static_cast<size_t>(m) * a.K + static_cast<size_t>(u) * C::UK;
+                    const uint32_t dst = smem_addr(xb + (m & 1) * C::UK);
+                    for (int q = lane; q < C::UK / 4; q += 32) cp_async16(dst + 16u * q, src + 4 * q);
+                }
+                cp_async_commit();
+            };
+            load(0);
+            load(1);
+            for (int m = 0; m < M; ++m) {
+                cp_async_wait<1>();  // row m has landed (row m + 1 may still be in flight)
+                __syncwarp();
+                build_row<TYPE, 1, LR>(rec(u), zbu(u), zbu(u) + kUnitBlocks * 16, xb + (m & 1) * C::UK, m, lane);
+                __syncwarp();
+                load(m + 2);
+            }
+            cp_async_wait<0>();
+            __syncwarp();
+        }
+        // the lane's B record and zero-point offsets (columns past 2M read a live column's)
+        const int g = lane >> 2, c = lane & 3;
+        const uint32_t sel = (c == 3) ? 0x7610u : 0x3210u;
+        const uint32_t boff = static_cast<uint32_t>((4 * min(g, 2 * M - 1) + c) * 16);
+        const int mz = min(c, M - 1);
+        bool ok = true;
+        for (int i = 0; i < ngroups; ++i) {
+            const int slot = i % S;
+            if (!mbar_wait_warp(full(slot), (i / S) & 1)) {
+                ok = false;
+                break;
+            }
+            const int rows = min(kGroupRows, nrows - i * kGroupRows);
+            const uint32_t s0 = smem_addr(stage(slot)) + static_cast<uint32_t>(g * a.row_bytes);
+            const uint32_t s8 = s0 + static_cast<uint32_t>(8 * a.row_bytes);
+            float tot0 = 0.0f, tot1 = 0.0f;
+            for (int u = warp; u < U; u += kRsWarps) {
+                const uint32_t uo = static_cast<uint32_t>(u * kUnitBytes);
+                const uint32_t srow[2] = {s0 + uo, s8 + uo};
+                const uint32_t srow_c[2] = {s0 + uo + 4u * c, s8 + uo + 4u * c};
+                const uint32_t rs = smem_addr(rec(u));
+                const uint32_t srec[1] = {rs + boff}, srec_h[1] = {rs + boff / 2};
+                const uint32_t szb[1] = {smem_addr(zbu(u)) + 4u * mz};
+                float acc[1][2] = {{0.0f, 0.0f}};
+                pn_blocks<TYPE, 1, 0, 4, LR>(srow, srow_c, sel, srec, srec_h, szb, acc);
+                pn_blocks<TYPE, 1, 4, 4, LR>(srow, srow_c, sel, srec, srec_h, szb, acc);
+                const float f = zbu(u)[kUnitBlocks * 16 + mz];  // 2^(24 - sigma) of the unit
+                tot0 = fmaf(acc[0][0], f, tot0);
+                tot1 = fmaf(acc[0][1], f, tot1);
+            }
+            if (c < M) {
+                float* pr = part + (warp * M + c) * a.rows_pad + i * kGroupRows + g;
+                pr[0] = tot0;
+                pr[8] = tot1;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty(slot));
+        }
+        if (!ok && lane == 0) record_error(a.err, kErrFullWait);
+    }
+
+    // ---------------- the warps' row sums -> Y ----------------
+    __syncthreads();
+    griddep_wait();  // Y may still be read by the previous grid
+    for (int e = threadIdx.x; e < M * nrows; e += kRsThreads) {
+        const int m = e / nrows, r = e - m * nrows;
+        float v = 0.0f;
+        for (int w = 0; w < active; ++w) v += part[(w * M + m) * a.rows_pad + r];
+        a.Y[static_cast<size_t>(m) * a.N + r0 + r] = v;
+    }
+}
+
+struct RsPlan {
+    int G = 0, S = 0, rows_pad = 0;
+    uint32_t off_rec = 0, off_zb = 0, off_x = 0, off_part = 0, off_stage = 0, stage_bytes = 0, total = 0;
+};
+
+// Grid (one CTA per SM, or one per row when there are fewer rows) and the deepest ring of 16-row
+// stages (2..8) that fits; false when even two stages do not.
+template <int TYPE, int LR>
+bool rs_plan(int64_t N, int U, int M, int row_bytes, int sms, int s_req, RsPlan& p) {
+    using C = Cfg<TYPE, 1, LR>;
+    if (U > kRsMaxUnits) return false;
+    p.G = static_cast<int>(std::min<int64_t>(sms, N));
+    const int64_t rows_max = (N + p.G - 1) / p.G;
+    p.rows_pad = static_cast<int>((rows_max + kGroupRows - 1) / kGroupRows * kGroupRows);
+    p.stage_bytes = align_up(static_cast<uint32_t>(kGroupRows * row_bytes), 1024);
+    for (int S = (s_req > 0 ? s_req : 8); S >= (s_req > 0 ? s_req : 2); --S) {
+        p.S = S;
+        p.off_rec = align_up(8u * 2u * S, 128);
+        p.off_zb = align_up(p.off_rec + static_cast<uint32_t>(U) * C::REC, 16);
+        p.off_x = align_up(p.off_zb + static_cast<uint32_t>(U) * (kUnitBlocks * 16 + 16) * 4u, 16);
+        p.off_part = align_up(p.off_x + kRsWarps * 2u * C::UK * 4u, 16);
+        p.off_stage = align_up(p.off_part + kRsWarps * static_cast<uint32_t>(M * p.rows_pad) * 4u, 1024);
+        p.total = p.off_stage + static_cast<uint32_t>(S) * p.stage_bytes;
+        if (p.total + 1024u <= kSmemOne) return true;
+    }
+    return false;
+}
+
+template <int TYPE, int LR>
+cudaError_t launch_rows(const uint8_t* W, const float* X, float* Y, int* err, int64_t N, int64_t K, int M, int U,
+                        int row_bytes, int s_req, bool static_weights, cudaStream_t stream) {
+    RsPlan p;
+    if (!rs_plan<TYPE, LR>(N, U, M, row_bytes, device_sm_count(), s_req, p)) return cudaErrorNotSupported;
+    auto kern = pn_rows_kernel<TYPE, LR>;
+    static std::atomic<bool> opted[64];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!opted[dev].load(std::memory_order_relaxed)) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmemOne));
+        if (e != cudaSuccess) return e;
+        opted[dev].store(true, std::memory_order_relaxed);
+    }
+    RsArgs a{};
+    a.W = W;
+    a.X = X;
+    a.Y = Y;
+    a.err = err;
+    a.N = static_cast<int>(N);
+    a.K = static_cast<int>(K);
+    a.M = M;
+    a.U = U;
+    a.G = p.G;
+    a.S = p.S;
+    a.row_bytes = row_bytes;
+    a.rows_pad = p.rows_pad;
+    a.flags = static_weights ? kStaticWeights : 0u;
+    a.off_rec = p.off_rec;
+    a.off_zb = p.off_zb;
+    a.off_x = p.off_x;
+    a.off_part = p.off_part;
+    a.off_stage = p.off_stage;
+    a.stage_bytes = p.stage_bytes;
+    cudaLaunchConfig_t lc{};
+    lc.gridDim = dim3(p.G, 1, 1);
+    lc.blockDim = dim3(kRsThreads, 1, 1);
+    lc.dynamicSmemBytes = p.total + 1024u;
+    lc.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+    return cudaLaunchKernelEx(&lc, kern, a);
+}
+
+template <int TYPE>
+cudaError_t launch_rows_typed(const uint8_t* W, const float* X, float* Y, int* err, int64_t N, int64_t K, int M,
+                              int U, int row_bytes, int s_req, bool static_weights, cudaStream_t stream) {
+    switch (M) {
+        case 1: return launch_rows<TYPE, 8>(W, X, Y, err, N, K, M, U, row_bytes, s_req, static_weights, stream);
+        case 2: return launch_rows<TYPE, 16>(W, X, Y, err, N, K, M, U, row_bytes, s_req, static_weights, stream);
+        case 3: return launch_rows<TYPE, 24>(W, X, Y, err, N, K, M, U, row_bytes, s_req, static_weights, stream);
+        case 4: return launch_rows<TYPE, 32>(W, X, Y, err, N, K, M, U, row_bytes, s_req, static_weights, stream);
+        default: return cudaErrorNotSupported;
+    }
+}
+
 template <class F>
-cudaError_t launch_policy(const CUtensorMap& map, const float* X, float* Y, int* err, int64_t N, int64_t K, int M,
-                          int U, int c_req, int s_req, bool static_weights, cudaStream_t stream) {
+cudaError_t launch_policy(const CUtensorMap (&map)[2], const float* X, float* Y, int* err, int64_t N, int64_t K,
+                          int M, int U, const int (&req)[3], bool static_weights, cudaStream_t stream) {
     KArgs<F> ka{};
-    ka.map[0] = map;
+    ka.map[0] = map[0];
+    ka.map[1] = map[1];
     ka.c.X = X;
     ka.c.Y = Y;
     ka.c.err = err;
     ka.c.N = static_cast<int>(N);
     ka.c.K = static_cast<int>(K);
     ka.c.M = M;
-    return cl_launch<F>(ka, N, U, c_req, s_req, static_weights, stream);
+    return cl_launch<F>(ka, N, U, req, static_weights, stream);
 }
 
 template <int TYPE>
-cudaError_t launch_typed(const CUtensorMap& map, const float* X, float* Y, int* err, int64_t N, int64_t K, int M,
-                         int U, int c_req, int s_req, bool static_weights, cudaStream_t stream) {
+cudaError_t launch_typed(const CUtensorMap (&map)[2], const float* X, float* Y, int* err, int64_t N, int64_t K, int M,
+                         int U, const int (&req)[3], bool static_weights, cudaStream_t stream) {
     const int nt = (2 * M + 7) / 8;
-    if (nt == 1)
-        return launch_policy<PnMma<TYPE, 1>>(map, X, Y, err, N, K, M, U, c_req, s_req, static_weights, stream);
-    if (nt == 2)
-        return launch_policy<PnMma<TYPE, 2>>(map, X, Y, err, N, K, M, U, c_req, s_req, static_weights, stream);
-    return launch_policy<PnMma<TYPE, 4>>(map, X, Y, err, N, K, M, U, c_req, s_req, static_weights, stream);
+    if (nt == 1) return launch_policy<PnMma<TYPE, 1>>(map, X, Y, err, N, K, M, U, req, static_weights, stream);
+    if (nt == 2) return launch_policy<PnMma<TYPE, 2>>(map, X, Y, err, N, K, M, U, req, static_weights, stream);
+    return launch_policy<PnMma<TYPE, 4>>(map, X, Y, err, N, K, M, U, req, static_weights, stream);
 }
 
 }  // namespace
@@ -362,17 +619,27 @@ cudaError_t launch_pn_gemv_mma(int type, const uint8_t* W, int64_t N, int64_t K,
     if (N > INT32_MAX - 64 || K > INT32_MAX || U * kUnitU32 > INT32_MAX) return cudaErrorNotSupported;
     if (reinterpret_cast<uintptr_t>(W) % 16 != 0 || reinterpret_cast<uintptr_t>(X) % 16 != 0)
         return cudaErrorNotSupported;
-    CUtensorMap map;
-    if (!encode_u32_map(&map, W, N, nb * kBlockBytes / 4, kUnitU32, kPieceRows)) return cudaErrorNotSupported;
-    static int env[2];  // PNQ_PN_CFG = "CTAs per cluster, stages", read once
+    CUtensorMap map[2];
+    if (!encode_u32_map(&map[0], W, N, nb * kBlockBytes / 4, kUnitU32, kPieceRows) ||
+        !encode_u32_map(&map[1], W, N, nb * kBlockBytes / 4, kUnitU32, kStageRows))
+        return cudaErrorNotSupported;
+    static int env[4];  // PNQ_PN_CFG = "CTAs per cluster, stages, CTAs per SM, path (1 rows, 2 strips)"
     static std::once_flag once;
     std::call_once(once, [] { env_cluster_config("PNQ_PN_CFG", env); });
-    if (c_req <= 0) c_req = env[0];
-    if (s_req <= 0) s_req = env[1];
+    const int req[3] = {c_req > 0 ? c_req : env[0], s_req > 0 ? s_req : env[1], env[2]};
+    // whole rows per CTA when a 16-row group is small enough to stage (M <= 4)
+    const int row_bytes = static_cast<int>(nb * kBlockBytes);
+    if (env[3] != 2 && M <= 4 && row_bytes <= kRsMaxRowBytes && c_req <= 0) {
+        const cudaError_t e = (type == kTypePn3t)
+                                  ? launch_rows_typed<kTypePn3t>(W, X, Y, err, N, K, M, static_cast<int>(U), row_bytes,
+                                                                 req[1], static_weights, stream)
+                                  : launch_rows_typed<kTypePn4t>(W, X, Y, err, N, K, M, static_cast<int>(U), row_bytes,
+                                                                 req[1], static_weights, stream);
+        if (e != cudaErrorNotSupported || env[3] == 1) return e;
+    }
     return (type == kTypePn3t)
-               ? launch_typed<kTypePn3t>(map, X, Y, err, N, K, M, static_cast<int>(U), c_req, s_req, static_weights, stream)
-               : launch_typed<kTypePn4t>(map, X, Y, err, N, K, M, static_cast<int>(U), c_req, s_req, static_weights,
-                                         stream);
+               ? launch_typed<kTypePn3t>(map, X, Y, err, N, K, M, static_cast<int>(U), req, static_weights, stream)
+               : launch_typed<kTypePn4t>(map, X, Y, err, N, K, M, static_cast<int>(U), req, static_weights, stream);
 }
 
 }  // namespace pnq

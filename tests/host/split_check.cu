@@ -93,7 +93,7 @@ void check_plan(const char* name, int64_t N, int U, int M, int c_req, int s_req)
     char what[160];
     std::snprintf(what, sizeof what, "%s M %d N %lld U %d C %d S %d", name, M, (long long)N, U, c_req, s_req);
     pnq::ClPlan p;
-    if (!pnq::cl_make_plan<Pol>(N, U, M, 152, c_req, s_req, p)) {
+    if (!pnq::cl_make_plan<Pol>(N, U, M, 152, c_req, s_req, 0, p)) {
         if (c_req == 0 && s_req == 0) FAIL("no plan");
         return;
     }
@@ -103,10 +103,12 @@ void check_plan(const char* name, int64_t N, int U, int M, int c_req, int s_req)
     if (p.sp.C != 1 && p.sp.C != 2) FAIL("cluster of %d", p.sp.C);
     if (c_req > 0 && p.sp.C != c_req) FAIL("forced cluster %d, planned %d", c_req, p.sp.C);
     if (s_req > 0 && p.S != s_req) FAIL("forced %d stages, planned %d", s_req, p.S);
-    if (p.S < 3 || p.S > 6) FAIL("%d stages", p.S);
+    if (p.S < 3 || p.S > pnq::kMaxStages) FAIL("%d stages", p.S);
     if (p.xs < 1 || p.xs > 8) FAIL("%d x slots", p.xs);
-    // one wave of clusters (or whole waves when a wide cluster's partials would not fit)
-    if (p.sp.ncl * p.sp.C > 152 && (p.sp.ncl % (152 / p.sp.C) != 0 && p.sp.ncl != p.sp.pieces))
+    // one or two CTAs per SM (two only in the pair budget), in whole waves when a wide cluster's
+    // partials would not fit otherwise
+    const int slots = 152 * p.minb;
+    if (p.sp.ncl * p.sp.C > slots && (p.sp.ncl % (slots / p.sp.C) != 0 && p.sp.ncl != p.sp.pieces))
         FAIL("grid %d", p.sp.ncl * p.sp.C);
     for (int c = 0; c < p.sp.ncl; ++c) {
         const int rows = static_cast<int>((p.sp.piece0(c + 1) - p.sp.piece0(c)) * pnq::kPieceRows);
@@ -142,7 +144,7 @@ void run_type() {
         for (int U : Us)
             for (int M = 1; M <= 16 && !failures; ++M)
                 for (int c : {0, 1, 2})
-                    for (int s : {0, 3, 4, 6}) {
+                    for (int s : {0, 3, 6, 12}) {
                         const int nt = (2 * M + 7) / 8;
                         const char* nm = TYPE == pnq::kTypePn3t ? "pn3t" : "pn4t";
                         if (nt == 1) check_plan<pnq::PnMma<TYPE, 1>>(nm, N, U, M, c, s);
