@@ -90,8 +90,9 @@ __device__ __forceinline__ int pn_elem(int cpw, bool odd, int c, int r, int j, i
 
 // B operands of one K unit for activation row m (one builder warp): sigma from the row's largest
 // |x| over the unit, the hi / lo lane records of every (block, lane column, pair) and the blocks'
-// zero-point terms; xr = the unit's x row in shared memory.
-template <int TYPE, int NT, int LR = 32>
+// zero-point terms (zb[block * ZS + m]: ZS activation rows per block); xr = the unit's x row in
+// shared memory.
+template <int TYPE, int NT, int LR = 32, int ZS = 16>
 __device__ __forceinline__ void build_row(uint8_t* rec, float* zb, float* so, const float* xr, int m, int lane) {
     using C = Cfg<TYPE, NT, LR>;
     using F = PnFmt<TYPE>;
@@ -144,18 +145,25 @@ __device__ __forceinline__ void build_row(uint8_t* rec, float* zb, float* so, co
             }
         }
     }
-    // zero-point terms: lane = 4 * block + quarter sums a quarter of the block in element order
+    // zero-point terms: lane = 4 * block + quarter sums a quarter of the block, starting at its
+    // element (lane mod QN) and wrapping around (the lanes' quarters are QN floats apart, so in
+    // element order the lanes of a load would share a few banks; rotated, no bank serves more
+    // than two of them)
     {
         const int blk = lane >> 2, qt = lane & 3;
         constexpr int QN = F::BLK / 4;
         const float* xq = xr + blk * F::BLK + qt * QN;
         float s = 0.0f;
+        int e = lane % QN;
 #pragma unroll
-        for (int e = 0; e < QN; ++e) s += xq[e];
+        for (int t = 0; t < QN; ++t) {
+            s += xq[e];
+            e = (e == QN - 1) ? 0 : e + 1;
+        }
         s += __shfl_xor_sync(0xffffffffu, s, 1);
         s += __shfl_xor_sync(0xffffffffu, s, 2);
         // Z = z * sum over the block of 2^-24 * 2^shift * B = z * 2^(sigma - 24) * (sum of x)
-        if (qt == 0) zb[blk * 16 + m] = static_cast<float>(F::Z) * s * exp2i(sg - 24);
+        if (qt == 0) zb[blk * ZS + m] = static_cast<float>(F::Z) * s * exp2i(sg - 24);
     }
     if (lane == 0) so[m] = exp2i(24 - sg);  // undoes sigma and the 2^-24 of the codes
 }
@@ -169,8 +177,9 @@ __device__ __forceinline__ void build_row(uint8_t* rec, float* zb, float* so, co
 //   byte (srow_c = srow + 4c, lane column c's words), so any row stride works;
 //   srec[t]: the B records of tile t at the lane's record (lanes of columns past 2M read a live
 //   column's record: their sums are never used), srec_h[t] the same for 8-byte records;
-//   szb[t]: the zero-point term of the lane's activation row (clamped the same way).
-template <int TYPE, int NT, int B0, int NBK, int LR = 32>
+//   szb[t]: the zero-point term of the lane's activation row (clamped the same way) in a table of
+//   ZS activation rows per block.
+template <int TYPE, int NT, int B0, int NBK, int LR = 32, int ZS = 16>
 __device__ __forceinline__ void pn_blocks(const uint32_t (&srow)[2], const uint32_t (&srow_c)[2], uint32_t sel,
                                           const uint32_t (&srec)[NT], const uint32_t (&srec_h)[NT],
                                           const uint32_t (&szb)[NT], float (&acc)[NT][2]) {
@@ -197,7 +206,7 @@ __device__ __forceinline__ void pn_blocks(const uint32_t (&srow)[2], const uint3
         });
         static_for<NT>([&](auto T) {
             constexpr int t = decltype(T)::value;
-            z[i][t] = ld_shared_f32<4 * 16 * B>(szb[t]);
+            z[i][t] = ld_shared_f32<4 * ZS * B>(szb[t]);
         });
     });
     float acc4[NBK][NT][4];
@@ -331,23 +340,44 @@ struct PnMma {
     }
 };
 
-// ---- row-stream path (M <= 4, rows of at most a few KB) -------------------------------------------
+// ---- row-stream path (M <= 4) ----------------------------------------------------------------------
 //
-// Each CTA owns a contiguous range of whole rows, so nothing is summed across CTAs, and a 16-row
-// group of them is one contiguous range of HBM that a single bulk copy brings into a stage (the
-// copy engine streams such copies at the full HBM rate; strips of a longer row need one request per
-// row and stream far slower). Consumer warp w owns the K units u = w, w + 8, ..: it builds their B
-// operands itself (x of its units only) and multiplies every row group over them, keeping its
-// per-row sums in its own slice of shared memory; the slices are summed in warp order at the end.
+// Each CTA owns a contiguous range of whole rows, so nothing is summed across CTAs. A stage holds
+// 16 rows of the CTA (a row group): sixteen 1-D bulk copies, one per row, issued by the lanes of two
+// producer warps, eight rows each (copies issued from two warps stream at the full HBM rate, one
+// warp's at about two thirds of it; 2-D boxes of 272-byte strips stream far slower). A stage row
+// is `pitch` bytes apart: its length, padded by 16 bytes where needed so that pitch / 16 is odd,
+// which puts the 32 words a warp loads at once (8 rows x 4 lane columns) in 32 different
+// shared-memory banks.
+//
+// Whole rows (SEG = false; rows of up to 16 K units): consumer warp w owns the units u = w, w + 8,
+// ..; it streams the x of its own (unit, activation row) pairs through two buffers of its own,
+// builds their B operands and multiplies every row group over them, storing its per-row sums in
+// its own slice of shared memory.
+//
+// Row segments (SEG = true; longer rows): the units of a row are cut into `nseg` segments of
+// near-equal length and a stage holds one segment of a row group. All of x ([M][K] fp32) comes in
+// with one bulk copy per activation row, issued by consumer warp 0 once the previous grid is done
+// (loads issued one unit at a time would each wait behind every weight copy in flight on the SM);
+// the consumer warps then build the B operands of all units between them, (unit, activation row)
+// pairs p = w, w + 8, .. for warp w, and meet at a barrier. The (row group, unit) tasks of the
+// stages are dealt to the warps in turn, so each warp gets the same number of tasks to within one
+// whatever the segment lengths; a warp adds its task sums into its own slice of per-row sums.
+//
+// Either way the slices are summed in warp order at the end.
 
-constexpr int kRsWarps = 8;  // consumer warps; one producer warp more
-constexpr int kRsThreads = 32 * (kRsWarps + 1);
-constexpr int kRsMaxUnits = 2 * kRsWarps;  // K units a launch can take (two per warp)
-constexpr int kRsMaxRowBytes = 4096;       // rows longer than this take the strip path
+constexpr int kRsWarps = 8;      // consumer warps
+constexpr int kRsProducers = 2;  // producer warps, rows 0..7 and 8..15 of each group
+constexpr int kRsThreads = 32 * (kRsWarps + kRsProducers);
+constexpr int kRsWholeUnits = 16;  // longest whole row (units); longer rows are cut into segments
+constexpr int kRsMaxSeg = 32;      // segments of a row at most
+constexpr int kRsZs = 4;           // activation rows of the zero-point table (M <= 4)
+constexpr int kRsZb = kUnitBlocks * kRsZs + kRsZs;  // floats per unit: terms [block][m], then 2^(24 - sigma) [m]
+constexpr uint32_t kRsConsumerBar = 1;              // named barrier of the consumer warps
 
-// Zeros for the rows of a CTA's last 16-row group that lie past its range (copied in by the copy
-// engine like the weights, so no warp has to clear shared memory).
-__device__ __align__(128) uint8_t g_pnq_zero_rows[(kGroupRows - 1) * kRsMaxRowBytes];
+// Stage pitch of a row (segment) of `bytes` (a multiple of 16): the least multiple of 16 >= bytes
+// whose quotient by 16 is odd.
+constexpr int rs_pitch(int bytes) { return ((bytes / 16) & 1) ? bytes : bytes + 16; }
 
 struct RsArgs {
     const uint8_t* W;
@@ -355,130 +385,201 @@ struct RsArgs {
     float* Y;
     int* err;
     int N, K, M, U, G, S;  // G CTAs, S stages
-    int row_bytes, rows_pad;  // rows_pad: partial rows per (warp, activation row), >= any CTA's rows
+    int nseg;              // segments of a row (units [j U / nseg, (j + 1) U / nseg) for segment j)
+    int row_bytes, pitch;  // a weight row in HBM; a whole row's stride in a stage
+    int rows_pad;          // partial rows per (warp, activation row), >= any CTA's rows
     unsigned flags;
     uint32_t off_rec, off_zb, off_x, off_part, off_stage, stage_bytes;
 };
 
-template <int TYPE, int LR>
+template <int TYPE, int LR, bool SEG>
 __global__ void __launch_bounds__(kRsThreads, 1) pn_rows_kernel(const __grid_constant__ RsArgs a) {
     using C = Cfg<TYPE, 1, LR>;
-    constexpr int ZB = kUnitBlocks * 16 + 16;  // zero-point terms [block][m], then 2^(24 - sigma) [m]
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* base = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     const uint32_t bar0 = smem_addr(base);
-    const int S = a.S, M = a.M, U = a.U;
+    const int S = a.S, M = a.M, U = a.U, nseg = SEG ? a.nseg : 1;
     auto full = [&](int s) { return bar0 + 8u * s; };
     auto empty = [&](int s) { return bar0 + 8u * (S + s); };
+    const uint32_t xfull = bar0 + 8u * (2 * S);  // all of x has landed (SEG)
     auto stage = [&](int s) { return base + a.off_stage + static_cast<uint32_t>(s) * a.stage_bytes; };
     auto rec = [&](int u) { return base + a.off_rec + static_cast<uint32_t>(u) * C::REC; };
-    auto zbu = [&](int u) { return reinterpret_cast<float*>(base + a.off_zb) + u * ZB; };
+    auto zbu = [&](int u) { return reinterpret_cast<float*>(base + a.off_zb) + u * kRsZb; };
+    __shared__ int seg_tab[kRsMaxSeg + 1];  // first unit of segment j (seg_tab[nseg] = U)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int active = min(kRsWarps, U);  // consumer warps that own units
+    const int active = SEG ? kRsWarps : min(kRsWarps, U);  // consumer warps with work
     const int64_t r0 = static_cast<int64_t>(blockIdx.x) * a.N / a.G, r1 = static_cast<int64_t>(blockIdx.x + 1) * a.N / a.G;
     const int nrows = static_cast<int>(r1 - r0);
-    const int ngroups = (nrows + kGroupRows - 1) / kGroupRows;
+    const int nstages = (nrows + kGroupRows - 1) / kGroupRows * nseg;  // (row group, segment), segment fastest
     float* part = reinterpret_cast<float*>(base + a.off_part);  // [warp][m][rows_pad]
 
     if (threadIdx.x == 0) {
         griddep_launch_dependents();
         for (int s = 0; s < S; ++s) {
-            mbar_init(full(s), 1);
+            mbar_init(full(s), kRsProducers);
             mbar_init(empty(s), active);
+        }
+        if (SEG) {
+            for (int j = 0; j <= nseg; ++j) seg_tab[j] = j * U / nseg;
+            mbar_init(xfull, 1);
         }
         mbar_fence_init();
     }
     __syncthreads();
 
-    if (warp == kRsWarps) {
-        // ---------------- producer: one bulk copy per 16-row group ----------------
-        if (lane == 0 && ngroups > 0) {
-            const uint64_t pol = l2_policy_evict_first();
-            if (!(a.flags & kStaticWeights)) griddep_wait();  // W may be written by the previous grid
-            bool ok = true;
-            int i = 0;
-            for (; i < ngroups; ++i) {
-                const int slot = i % S;
-                if (i >= S && !mbar_wait_bounded(empty(slot), ((i / S) - 1) & 1)) {
-                    ok = false;
-                    break;
-                }
-                const int rows = min(kGroupRows, nrows - i * kGroupRows);
-                const uint32_t bytes = static_cast<uint32_t>(rows * a.row_bytes);
-                const uint32_t tail = static_cast<uint32_t>((kGroupRows - rows) * a.row_bytes);
-                mbar_arrive_expect_tx(full(slot), bytes + tail);
-                bulk_g2s(smem_addr(stage(slot)), a.W + (r0 + i * kGroupRows) * a.row_bytes, bytes, full(slot), pol);
-                // the last group's rows past the CTA's: zeros (d = 0 and codes 0 add nothing)
-                if (tail) bulk_g2s_plain(smem_addr(stage(slot)) + bytes, g_pnq_zero_rows, tail, full(slot));
+    if (warp >= kRsWarps) {
+        // ---------------- producers: one bulk copy per row, lane r of warp p copying row 8p + r ----------------
+        const int pr = (warp - kRsWarps) * 8;  // the warp's first row of a group
+        const uint64_t pol = l2_policy_evict_first();
+        if (!(a.flags & kStaticWeights)) griddep_wait();  // W may be written by the previous grid
+        bool ok = true;
+        int s = 0;
+        for (int i = 0, j = 0; s < nstages; ++s) {
+            const int slot = s % S;
+            if (s >= S && !mbar_wait_warp(empty(slot), ((s / S) - 1) & 1)) {
+                ok = false;
+                break;
             }
-            if (!ok) record_error(a.err, kErrEmptyWait);
-            bool drained = true;  // every copy issued has landed before the CTA may exit
-            for (int gg = max(0, i - S); drained && gg < i; ++gg) drained = mbar_wait_bounded(full(gg % S), (gg / S) & 1);
-            if (!drained) record_error(a.err, kErrDrainWait);
+            // rows of the last group past the CTA's range are not copied: a row's products depend
+            // on that row alone, and those rows' sums are never stored
+            const int mine = min(8, max(0, nrows - i * kGroupRows - pr));
+            int u0 = 0, bytes = a.row_bytes, pitch = a.pitch;
+            if (SEG) {
+                u0 = seg_tab[j];
+                bytes = (seg_tab[j + 1] - u0) * kUnitBytes;
+                pitch = rs_pitch(bytes);
+            }
+            if (lane == 0) mbar_arrive_expect_tx(full(slot), static_cast<uint32_t>(mine * bytes));
+            __syncwarp();
+            if (lane < mine)
+                bulk_g2s(smem_addr(stage(slot)) + static_cast<uint32_t>((pr + lane) * pitch),
+                         a.W + (r0 + i * kGroupRows + pr + lane) * a.row_bytes + u0 * kUnitBytes,
+                         static_cast<uint32_t>(bytes), full(slot), pol);
+            if (++j == nseg) {
+                j = 0;
+                ++i;
+            }
         }
-        __syncwarp();
-    } else if (warp < active && ngroups > 0) {
-        // ---------------- consumer warp: B operands of its units, then every row group ----------------
-        griddep_wait();  // X belongs to the previous grid until now
-        float* xb = reinterpret_cast<float*>(base + a.off_x) + warp * 2 * C::UK;  // two x rows
-        for (int u = warp; u < U; u += kRsWarps) {
-            auto load = [&](int m) {
-                if (m < M) {
+        if (!ok && lane == 0) record_error(a.err, kErrEmptyWait);
+        bool drained = true;  // every copy issued has landed before the CTA may exit
+        for (int gg = max(0, s - S); drained && gg < s; ++gg) drained = mbar_wait_warp(full(gg % S), (gg / S) & 1);
+        if (!drained && lane == 0) record_error(a.err, kErrDrainWait);
+    } else if (warp < active) {
+        // ---------------- consumer warps ----------------
+        const int g = lane >> 2, c = lane & 3;
+        const uint32_t sel = (c == 3) ? 0x7610u : 0x3210u;
+        // the lane's B record and zero-point offsets (columns past 2M read a live column's)
+        const uint32_t boff = static_cast<uint32_t>((4 * min(g, 2 * M - 1) + c) * 16);
+        const int mz = min(c, M - 1);
+        float* mine = part + warp * M * a.rows_pad;
+        // one (row group, unit) task: rows g, g + 8 of the stage rows s0 / s8, at byte uo of them
+        auto task = [&](uint32_t s0, uint32_t s8, uint32_t uo, int u, float& tot0, float& tot1) {
+            const uint32_t srow[2] = {s0 + uo, s8 + uo};
+            const uint32_t srow_c[2] = {s0 + uo + 4u * c, s8 + uo + 4u * c};
+            const uint32_t rs = smem_addr(rec(u));
+            const uint32_t srec[1] = {rs + boff}, srec_h[1] = {rs + boff / 2};
+            const uint32_t szb[1] = {smem_addr(zbu(u)) + 4u * mz};
+            float acc[1][2] = {{0.0f, 0.0f}};
+            pn_blocks<TYPE, 1, 0, 4, LR, kRsZs>(srow, srow_c, sel, srec, srec_h, szb, acc);
+            pn_blocks<TYPE, 1, 4, 4, LR, kRsZs>(srow, srow_c, sel, srec, srec_h, szb, acc);
+            const float f = zbu(u)[kUnitBlocks * kRsZs + mz];  // 2^(24 - sigma) of the unit
+            tot0 = fmaf(acc[0][0], f, tot0);
+            tot1 = fmaf(acc[0][1], f, tot1);
+        };
+        bool ok = true;
+        if constexpr (!SEG) {
+            griddep_wait();  // X belongs to the previous grid until now
+            // (unit, activation row) pairs of the warp's units, in order; x of pair q + 2 is in
+            // flight while pair q builds
+            float* xb = reinterpret_cast<float*>(base + a.off_x) + warp * 2 * C::UK;  // two x rows
+            const int npair = ((U - warp + kRsWarps - 1) / kRsWarps) * M;
+            auto load = [&](int q) {
+                if (q < npair) {
+                    const int u = warp + (q / M) * kRsWarps, m = q % M;
                     const float* src = a.X + static_cast<size_t>(m) * a.K + static_cast<size_t>(u) * C::UK;
-                    const uint32_t dst = smem_addr(xb + (m & 1) * C::UK);
-                    for (int q = lane; q < C::UK / 4; q += 32) cp_async16(dst + 16u * q, src + 4 * q);
+                    const uint32_t dst = smem_addr(xb + (q & 1) * C::UK);
+                    for (int v = lane; v < C::UK / 4; v += 32) cp_async16(dst + 16u * v, src + 4 * v);
                 }
                 cp_async_commit();
             };
             load(0);
             load(1);
-            for (int m = 0; m < M; ++m) {
-                cp_async_wait<1>();  // row m has landed (row m + 1 may still be in flight)
+            for (int q = 0; q < npair; ++q) {
+                const int u = warp + (q / M) * kRsWarps, m = q % M;
+                cp_async_wait<1>();  // pair q's x has landed (pair q + 1's may still be in flight)
                 __syncwarp();
-                build_row<TYPE, 1, LR>(rec(u), zbu(u), zbu(u) + kUnitBlocks * 16, xb + (m & 1) * C::UK, m, lane);
+                build_row<TYPE, 1, LR, kRsZs>(rec(u), zbu(u), zbu(u) + kUnitBlocks * kRsZs, xb + (q & 1) * C::UK, m,
+                                              lane);
                 __syncwarp();
-                load(m + 2);
+                load(q + 2);
             }
             cp_async_wait<0>();
             __syncwarp();
-        }
-        // the lane's B record and zero-point offsets (columns past 2M read a live column's)
-        const int g = lane >> 2, c = lane & 3;
-        const uint32_t sel = (c == 3) ? 0x7610u : 0x3210u;
-        const uint32_t boff = static_cast<uint32_t>((4 * min(g, 2 * M - 1) + c) * 16);
-        const int mz = min(c, M - 1);
-        bool ok = true;
-        for (int i = 0; i < ngroups; ++i) {
-            const int slot = i % S;
-            if (!mbar_wait_warp(full(slot), (i / S) & 1)) {
-                ok = false;
-                break;
+            for (int i = 0; i < nstages; ++i) {
+                const int slot = i % S;
+                if (!mbar_wait_warp(full(slot), (i / S) & 1)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t s0 = smem_addr(stage(slot)) + static_cast<uint32_t>(g * a.pitch);
+                const uint32_t s8 = s0 + static_cast<uint32_t>(8 * a.pitch);
+                float tot0 = 0.0f, tot1 = 0.0f;
+                for (int u = warp; u < U; u += kRsWarps) task(s0, s8, static_cast<uint32_t>(u * kUnitBytes), u, tot0, tot1);
+                if (c < M) {
+                    float* pr = mine + c * a.rows_pad + i * kGroupRows + g;
+                    pr[0] = tot0;
+                    pr[8] = tot1;
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(empty(slot));
             }
-            const int rows = min(kGroupRows, nrows - i * kGroupRows);
-            const uint32_t s0 = smem_addr(stage(slot)) + static_cast<uint32_t>(g * a.row_bytes);
-            const uint32_t s8 = s0 + static_cast<uint32_t>(8 * a.row_bytes);
-            float tot0 = 0.0f, tot1 = 0.0f;
-            for (int u = warp; u < U; u += kRsWarps) {
-                const uint32_t uo = static_cast<uint32_t>(u * kUnitBytes);
-                const uint32_t srow[2] = {s0 + uo, s8 + uo};
-                const uint32_t srow_c[2] = {s0 + uo + 4u * c, s8 + uo + 4u * c};
-                const uint32_t rs = smem_addr(rec(u));
-                const uint32_t srec[1] = {rs + boff}, srec_h[1] = {rs + boff / 2};
-                const uint32_t szb[1] = {smem_addr(zbu(u)) + 4u * mz};
-                float acc[1][2] = {{0.0f, 0.0f}};
-                pn_blocks<TYPE, 1, 0, 4, LR>(srow, srow_c, sel, srec, srec_h, szb, acc);
-                pn_blocks<TYPE, 1, 4, 4, LR>(srow, srow_c, sel, srec, srec_h, szb, acc);
-                const float f = zbu(u)[kUnitBlocks * 16 + mz];  // 2^(24 - sigma) of the unit
-                tot0 = fmaf(acc[0][0], f, tot0);
-                tot1 = fmaf(acc[0][1], f, tot1);
+        } else {
+            for (int e = lane; e < M * a.rows_pad; e += 32) mine[e] = 0.0f;
+            const float* xs = reinterpret_cast<const float*>(base + a.off_x);  // [M][K]
+            if (warp == 0) {
+                griddep_wait();  // X belongs to the previous grid until now
+                if (lane == 0) {
+                    const uint32_t row = static_cast<uint32_t>(a.K) * 4u;
+                    mbar_arrive_expect_tx(xfull, row * static_cast<uint32_t>(M));
+                    for (int m = 0; m < M; ++m)
+                        bulk_g2s_plain(smem_addr(xs) + m * row, a.X + static_cast<size_t>(m) * a.K, row, xfull);
+                }
             }
-            if (c < M) {
-                float* pr = part + (warp * M + c) * a.rows_pad + i * kGroupRows + g;
-                pr[0] = tot0;
-                pr[8] = tot1;
+            ok = mbar_wait_warp(xfull, 0);
+            if (ok)
+                for (int p = warp; p < U * M; p += kRsWarps) {
+                    const int u = p / M, m = p - u * M;
+                    build_row<TYPE, 1, LR, kRsZs>(rec(u), zbu(u), zbu(u) + kUnitBlocks * kRsZs,
+                                                  xs + static_cast<size_t>(m) * a.K + u * C::UK, m, lane);
+                }
+            named_sync(kRsConsumerBar, 32 * kRsWarps);  // every unit's operands are built
+            int k0 = warp;  // the warp's first task of the next stage (tasks of a stage: its units in order)
+            for (int s = 0, i = 0, j = 0; ok && s < nstages; ++s) {
+                const int slot = s % S;
+                if (!mbar_wait_warp(full(slot), (s / S) & 1)) {
+                    ok = false;
+                    break;
+                }
+                const int u0 = seg_tab[j], n = seg_tab[j + 1] - u0;
+                const uint32_t pitch = static_cast<uint32_t>(rs_pitch(n * kUnitBytes));
+                const uint32_t s0 = smem_addr(stage(slot)) + g * pitch, s8 = s0 + 8u * pitch;
+                if (k0 < n) {
+                    float tot0 = 0.0f, tot1 = 0.0f;
+                    for (int k = k0; k < n; k += kRsWarps) task(s0, s8, static_cast<uint32_t>(k * kUnitBytes), u0 + k, tot0, tot1);
+                    if (c < M) {
+                        float* pr = mine + c * a.rows_pad + i * kGroupRows + g;
+                        pr[0] += tot0;
+                        pr[8] += tot1;
+                    }
+                }
+                k0 = (k0 - n) & (kRsWarps - 1);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(empty(slot));
+                if (++j == nseg) {
+                    j = 0;
+                    ++i;
+                }
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(empty(slot));
         }
         if (!ok && lane == 0) record_error(a.err, kErrFullWait);
     }
@@ -495,39 +596,47 @@ __global__ void __launch_bounds__(kRsThreads, 1) pn_rows_kernel(const __grid_con
 }
 
 struct RsPlan {
-    int G = 0, S = 0, rows_pad = 0;
+    int G = 0, S = 0, nseg = 0, rows_pad = 0, pitch = 0;
     uint32_t off_rec = 0, off_zb = 0, off_x = 0, off_part = 0, off_stage = 0, stage_bytes = 0, total = 0;
 };
 
-// Grid (one CTA per SM, or one per row when there are fewer rows) and the deepest ring of 16-row
-// stages (2..8) that fits; false when even two stages do not.
+// Grid (one CTA per SM, or one per row when there are fewer rows), segments per row and the ring
+// of stages. Rows of at most 16 units stay whole (per-warp x buffers), with the deepest ring of
+// 8..2 stages that fits. Longer rows are cut into segments of at most 8, 6 then 4 units (all of x
+// staged), the first with a ring of 8..3 stages, then 2 as a last resort. False when nothing fits.
 template <int TYPE, int LR>
-bool rs_plan(int64_t N, int U, int M, int row_bytes, int sms, int s_req, RsPlan& p) {
+bool rs_plan(int64_t N, int U, int M, int sms, int s_req, RsPlan& p) {
     using C = Cfg<TYPE, 1, LR>;
-    if (U > kRsMaxUnits) return false;
+    if (U < 1 || M < 1 || M > kRsZs || (U + 3) / 4 > kRsMaxSeg) return false;
     p.G = static_cast<int>(std::min<int64_t>(sms, N));
     const int64_t rows_max = (N + p.G - 1) / p.G;
     p.rows_pad = static_cast<int>((rows_max + kGroupRows - 1) / kGroupRows * kGroupRows);
-    p.stage_bytes = align_up(static_cast<uint32_t>(kGroupRows * row_bytes), 1024);
-    for (int S = (s_req > 0 ? s_req : 8); S >= (s_req > 0 ? s_req : 2); --S) {
-        p.S = S;
-        p.off_rec = align_up(8u * 2u * S, 128);
-        p.off_zb = align_up(p.off_rec + static_cast<uint32_t>(U) * C::REC, 16);
-        p.off_x = align_up(p.off_zb + static_cast<uint32_t>(U) * (kUnitBlocks * 16 + 16) * 4u, 16);
-        p.off_part = align_up(p.off_x + kRsWarps * 2u * C::UK * 4u, 16);
-        p.off_stage = align_up(p.off_part + kRsWarps * static_cast<uint32_t>(M * p.rows_pad) * 4u, 1024);
-        p.total = p.off_stage + static_cast<uint32_t>(S) * p.stage_bytes;
-        if (p.total + 1024u <= kSmemOne) return true;
-    }
+    const bool whole = U <= kRsWholeUnits;
+    p.off_rec = align_up(8u * (2u * kMaxStages + 1), 128);
+    p.off_zb = align_up(p.off_rec + static_cast<uint32_t>(U) * C::REC, 16);
+    p.off_x = align_up(p.off_zb + static_cast<uint32_t>(U) * kRsZb * 4u, 16);
+    const uint32_t xbytes = whole ? kRsWarps * 2u * C::UK * 4u : static_cast<uint32_t>(M) * U * C::UK * 4u;
+    p.off_part = align_up(p.off_x + xbytes, 16);
+    p.off_stage = align_up(p.off_part + kRsWarps * static_cast<uint32_t>(M * p.rows_pad) * 4u, 128);
+    const int cap[3] = {8, 6, 4};
+    for (int s_lo : {3, 2})
+        for (int t = 0; t < (whole ? 1 : 3); ++t) {
+            p.nseg = whole ? 1 : (U + cap[t] - 1) / cap[t];
+            const int longest = (U + p.nseg - 1) / p.nseg;
+            p.pitch = rs_pitch(longest * kUnitBytes);
+            p.stage_bytes = align_up(static_cast<uint32_t>(kGroupRows * p.pitch), 128);
+            for (int S = (s_req > 0 ? s_req : 8); S >= (s_req > 0 ? s_req : s_lo); --S) {
+                p.S = S;
+                p.total = p.off_stage + static_cast<uint32_t>(S) * p.stage_bytes;
+                if (S <= kMaxStages && p.total + 1024u <= kSmemOne) return true;
+            }
+        }
     return false;
 }
 
-template <int TYPE, int LR>
-cudaError_t launch_rows(const uint8_t* W, const float* X, float* Y, int* err, int64_t N, int64_t K, int M, int U,
-                        int row_bytes, int s_req, bool static_weights, cudaStream_t stream) {
-    RsPlan p;
-    if (!rs_plan<TYPE, LR>(N, U, M, row_bytes, device_sm_count(), s_req, p)) return cudaErrorNotSupported;
-    auto kern = pn_rows_kernel<TYPE, LR>;
+template <int TYPE, int LR, bool SEG>
+cudaError_t launch_rows_kernel(const RsArgs& a, const RsPlan& p, cudaStream_t stream) {
+    auto kern = pn_rows_kernel<TYPE, LR, SEG>;
     static std::atomic<bool> opted[64];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -538,26 +647,6 @@ cudaError_t launch_rows(const uint8_t* W, const float* X, float* Y, int* err, in
         if (e != cudaSuccess) return e;
         opted[dev].store(true, std::memory_order_relaxed);
     }
-    RsArgs a{};
-    a.W = W;
-    a.X = X;
-    a.Y = Y;
-    a.err = err;
-    a.N = static_cast<int>(N);
-    a.K = static_cast<int>(K);
-    a.M = M;
-    a.U = U;
-    a.G = p.G;
-    a.S = p.S;
-    a.row_bytes = row_bytes;
-    a.rows_pad = p.rows_pad;
-    a.flags = static_weights ? kStaticWeights : 0u;
-    a.off_rec = p.off_rec;
-    a.off_zb = p.off_zb;
-    a.off_x = p.off_x;
-    a.off_part = p.off_part;
-    a.off_stage = p.off_stage;
-    a.stage_bytes = p.stage_bytes;
     cudaLaunchConfig_t lc{};
     lc.gridDim = dim3(p.G, 1, 1);
     lc.blockDim = dim3(kRsThreads, 1, 1);
@@ -569,6 +658,36 @@ cudaError_t launch_rows(const uint8_t* W, const float* X, float* Y, int* err, in
     lc.attrs = attr;
     lc.numAttrs = 1;
     return cudaLaunchKernelEx(&lc, kern, a);
+}
+
+template <int TYPE, int LR>
+cudaError_t launch_rows(const uint8_t* W, const float* X, float* Y, int* err, int64_t N, int64_t K, int M, int U,
+                        int row_bytes, int s_req, bool static_weights, cudaStream_t stream) {
+    RsPlan p;
+    if (!rs_plan<TYPE, LR>(N, U, M, device_sm_count(), s_req, p)) return cudaErrorNotSupported;
+    RsArgs a{};
+    a.W = W;
+    a.X = X;
+    a.Y = Y;
+    a.err = err;
+    a.N = static_cast<int>(N);
+    a.K = static_cast<int>(K);
+    a.M = M;
+    a.U = U;
+    a.G = p.G;
+    a.S = p.S;
+    a.nseg = p.nseg;
+    a.row_bytes = row_bytes;
+    a.pitch = p.pitch;
+    a.rows_pad = p.rows_pad;
+    a.flags = static_weights ? kStaticWeights : 0u;
+    a.off_rec = p.off_rec;
+    a.off_zb = p.off_zb;
+    a.off_x = p.off_x;
+    a.off_part = p.off_part;
+    a.off_stage = p.off_stage;
+    a.stage_bytes = p.stage_bytes;
+    return p.nseg > 1 ? launch_rows_kernel<TYPE, LR, true>(a, p, stream) : launch_rows_kernel<TYPE, LR, false>(a, p, stream);
 }
 
 template <int TYPE>
@@ -627,9 +746,9 @@ cudaError_t launch_pn_gemv_mma(int type, const uint8_t* W, int64_t N, int64_t K,
     static std::once_flag once;
     std::call_once(once, [] { env_cluster_config("PNQ_PN_CFG", env); });
     const int req[3] = {c_req > 0 ? c_req : env[0], s_req > 0 ? s_req : env[1], env[2]};
-    // whole rows per CTA when a 16-row group is small enough to stage (M <= 4)
+    // whole rows per CTA when the B operands of every unit fit beside the stages (M <= 4)
     const int row_bytes = static_cast<int>(nb * kBlockBytes);
-    if (env[3] != 2 && M <= 4 && row_bytes <= kRsMaxRowBytes && c_req <= 0) {
+    if (env[3] != 2 && M <= 4 && c_req <= 0) {
         const cudaError_t e = (type == kTypePn3t)
                                   ? launch_rows_typed<kTypePn3t>(W, X, Y, err, N, K, M, static_cast<int>(U), row_bytes,
                                                                  req[1], static_weights, stream)

@@ -9,7 +9,11 @@
 //   - every plan keeps its shared-memory regions (barriers, per-unit terms, row partials, B
 //     operand slots, x slots, weight stages) disjoint, aligned and inside the per-CTA budget it
 //     claims (two CTAs per SM or one), sizes the partials for the widest cluster, and uses only
-//     cluster sizes that spread one CTA per SM (1 or 2).
+//     cluster sizes that spread one CTA per SM (1 or 2);
+//   - the row-stream plan (rs_plan): its regions are disjoint, aligned and inside one CTA's budget,
+//     every row segment's bulk copies are 16-byte aligned and land inside their stage, the
+//     segments of a row tile its units in order, and the dealing of (row group, unit) tasks to the
+//     consumer warps gives every task to exactly one warp, each warp the same count to within one.
 // Host code only: the kernels are compiled but never launched.
 #include "pnq_gemv_pn.cu"
 #include "pnq_gemv_nvfp4.cu"
@@ -157,6 +161,105 @@ void run_type() {
                     }
 }
 
+template <int TYPE, int LR>
+void check_rs_plan(int64_t N, int U, int M, int s_req) {
+    using C = pnq::Cfg<TYPE, 1, LR>;
+    char what[128];
+    std::snprintf(what, sizeof what, "rows %s N %lld U %d M %d s %d", TYPE == pnq::kTypePn3t ? "pn3t" : "pn4t",
+                  (long long)N, U, M, s_req);
+    pnq::RsPlan p;
+    if (!pnq::rs_plan<TYPE, LR>(N, U, M, 152, s_req, p)) return;
+    ++plans;
+    if (s_req > 0 && p.S != s_req) FAIL("forced %d stages, planned %d", s_req, p.S);
+    if (p.S < 2 || p.S > 8) FAIL("%d stages", p.S);
+    if (p.nseg < 1 || p.nseg > U) FAIL("%d segments", p.nseg);
+    if (p.total + 1024u > pnq::kSmemOne) FAIL("total %u", p.total);
+    if (p.G < 1 || p.G > 152 || p.G > N) FAIL("grid %d", p.G);
+    struct R {
+        uint64_t lo, hi;
+        const char* name;
+    };
+    if (p.nseg > pnq::kRsMaxSeg) FAIL("%d segments, table of %d", p.nseg, pnq::kRsMaxSeg);
+    const bool whole = U <= pnq::kRsWholeUnits;
+    if (whole != (p.nseg == 1)) FAIL("%d segments for %d units", p.nseg, U);
+    if (whole && p.pitch != pnq::rs_pitch(U * pnq::kUnitBytes)) FAIL("whole-row pitch %d", p.pitch);
+    const uint64_t xbytes = whole ? 4ull * pnq::kRsWarps * 2 * C::UK : 4ull * M * U * C::UK;
+    std::vector<R> r = {{0, 8ull * (2 * p.S + 1), "barriers"},
+                        {p.off_rec, p.off_rec + 1ull * U * C::REC, "B operands"},
+                        {p.off_zb, p.off_zb + 4ull * U * pnq::kRsZb, "zero-point terms"},
+                        {p.off_x, p.off_x + xbytes, "x rows"},
+                        {p.off_part, p.off_part + 4ull * pnq::kRsWarps * M * p.rows_pad, "row partials"},
+                        {p.off_stage, p.off_stage + 1ull * p.S * p.stage_bytes, "stages"}};
+    if (p.off_rec % 16 || p.off_zb % 16 || p.off_x % 16 || p.off_part % 16 || p.off_stage % 128 ||
+        p.stage_bytes % 128)
+        FAIL("misaligned region");
+    if (r.back().hi != p.total) FAIL("stages end at %llu, total %u", (unsigned long long)r.back().hi, p.total);
+    std::sort(r.begin(), r.end(), [](const R& a, const R& b) { return a.lo < b.lo; });
+    for (size_t k = 1; k < r.size(); ++k)
+        if (r[k].lo < r[k - 1].hi) FAIL("%s overlaps %s", r[k].name, r[k - 1].name);
+    // segments tile [0, U) in order; each one's 16 rows fit a stage at an aligned pitch
+    int prev = 0;
+    for (int j = 0; j < p.nseg; ++j) {
+        const int u0 = j * U / p.nseg, u1 = (j + 1) * U / p.nseg;
+        if (u0 != prev || u1 <= u0) FAIL("segment %d = [%d, %d)", j, u0, u1);
+        prev = u1;
+        const int bytes = (u1 - u0) * pnq::kUnitBytes, pitch = pnq::rs_pitch(bytes);
+        if (bytes % 16 || pitch % 16 || pitch < bytes || ((pitch / 16) & 1) == 0) FAIL("pitch %d of %d", pitch, bytes);
+        if (15u * pitch + bytes > p.stage_bytes) FAIL("segment %d overflows its stage", j);
+        if ((u0 * pnq::kUnitBytes) % 16) FAIL("segment %d source misaligned", j);
+    }
+    if (prev != U) FAIL("segments end at %d", prev);
+    // rows of every CTA, and the task dealing of its stages
+    for (int b = 0; b < p.G; ++b) {
+        const int64_t r0 = static_cast<int64_t>(b) * N / p.G, r1 = static_cast<int64_t>(b + 1) * N / p.G;
+        const int nrows = static_cast<int>(r1 - r0);
+        if (nrows < 1 || nrows > p.rows_pad || p.rows_pad % 16) FAIL("CTA %d of %d rows, partials %d", b, nrows, p.rows_pad);
+        if (b > 2 && b < p.G - 2 && N > 1000) continue;  // the dealing depends on rows only through the group count
+        const int ngroups = (nrows + 15) / 16;
+        std::vector<int> owner(static_cast<size_t>(ngroups) * U, -1), count(pnq::kRsWarps, 0);
+        std::vector<int> k0(pnq::kRsWarps);
+        for (int w = 0; w < pnq::kRsWarps; ++w) k0[w] = w;
+        for (int s = 0; s < ngroups * p.nseg; ++s) {
+            const int i = s / p.nseg, j = s % p.nseg, u0 = j * U / p.nseg, n = (j + 1) * U / p.nseg - u0;
+            for (int w = 0; w < pnq::kRsWarps; ++w) {
+                for (int k = k0[w]; k < n; k += pnq::kRsWarps) {
+                    int& o = owner[static_cast<size_t>(i) * U + u0 + k];
+                    if (o != -1) FAIL("task (%d, %d) dealt twice", i, u0 + k);
+                    o = w;
+                    ++count[w];
+                }
+                k0[w] = (k0[w] - n % pnq::kRsWarps + pnq::kRsWarps) % pnq::kRsWarps;
+            }
+        }
+        for (int o : owner)
+            if (o < 0) FAIL("a task of CTA %d is dealt to no warp", b);
+        const auto mm = std::minmax_element(count.begin(), count.end());
+        if (*mm.second - *mm.first > 1) FAIL("CTA %d: warps get %d..%d tasks", b, *mm.first, *mm.second);
+    }
+}
+
+template <int TYPE>
+void run_rows() {
+    for (int64_t N : {1, 7, 16, 17, 151, 152, 153, 777, 1024, 5120, 12288, 17408, 151936})
+        for (int U : {1, 2, 7, 8, 9, 12, 16, 17, 25, 33, 34, 48, 68})
+            for (int s : {0, 2, 3, 5})
+                for (int M = 1; M <= 4 && !failures; ++M) {
+                    if (M == 1) check_rs_plan<TYPE, 8>(N, U, M, s);
+                    if (M == 2) check_rs_plan<TYPE, 16>(N, U, M, s);
+                    if (M == 3) check_rs_plan<TYPE, 24>(N, U, M, s);
+                    if (M == 4) check_rs_plan<TYPE, 32>(N, U, M, s);
+                }
+    // the decode-step projections at M = 1 take the row-stream path
+    for (int64_t N : {1024, 5120, 12288, 17408})
+        for (int U : {8, 10, 12, 34}) {
+            pnq::RsPlan p;
+            if (!pnq::rs_plan<TYPE, 8>(N, U, 1, 152, 0, p)) {
+                const char* what = "rows plan";
+                FAIL("N %lld U %d M 1 has no row-stream plan", (long long)N, U);
+            }
+        }
+}
+
 }  // namespace
 
 int main() {
@@ -172,6 +275,8 @@ int main() {
                 }
     run_type<pnq::kTypePn3t>();
     run_type<pnq::kTypePn4t>();
+    run_rows<pnq::kTypePn3t>();
+    run_rows<pnq::kTypePn4t>();
     if (failures) return 1;
     std::printf("ok %ld plans, %ld splits\n", plans, splits);
     return 0;

@@ -137,6 +137,20 @@ def sampled_rows(N, n=48, seed=0):
     return np.unique(np.concatenate([[0, 1, 15, 16, 63, 64, N - 1], rng.choice(N, n, replace=False)]))
 
 
+@pytest.mark.parametrize("type_,N,U,M", [(pnq.PN4T, 777, 34, 1), (pnq.PN3T, 300, 17, 1), (pnq.PN4T, 40, 33, 1),
+                                         (pnq.PN3T, 2000, 25, 1), (pnq.PN4T, 161, 20, 2), (pnq.PN3T, 999, 12, 3),
+                                         (pnq.PN4T, 153, 16, 4)])
+def test_pn_row_segments(oracle, type_, N, U, M):
+    """Rows long enough to be cut into K segments (U = K units of 8 blocks), with segments of unequal
+    length and CTAs whose last 16-row group is ragged."""
+    K = BLK[type_] * 8 * U
+    seed = 31 * U + N
+    W = synth.pn_random_blocks(type_, N, K, seed=seed).numpy()
+    X = synth.activations(M, K, seed=seed)
+    Yr, Ar = oracle.gemv(type_, W, N, K, X)
+    assert_within_tolerance(run_pn(type_, W, N, K, X), Yr, Ar, f"type={type_} N={N} U={U} M={M}")
+
+
 LAYER = [("gate", pnq.PN3T, 17408, 5120), ("up", pnq.PN3T, 17408, 5120), ("q", pnq.PN3T, 12288, 5120),
          ("k", pnq.PN4T, 1024, 5120), ("v", pnq.PN4T, 1024, 5120), ("o", pnq.PN4T, 5120, 6144),
          ("down", pnq.PN4T, 5120, 17408)]
@@ -180,7 +194,8 @@ import oracle
 from gpu_util import assert_within_tolerance
 out = []
 for type_, N, K, M in [(124, 200, 80*48, 1), (125, 130, 64*80, 3), (125, 64, 64*8, 16), (124, 17, 80*16, 8),
-                      (124, 1000, 80*16, 4), (125, 777, 64*272, 2), (124, 9, 80*8, 1), (125, 2500, 64*24, 12)]:
+                      (124, 1000, 80*16, 4), (125, 777, 64*272, 2), (124, 9, 80*8, 1), (125, 2500, 64*24, 12),
+                      (125, 300, 64*272, 1), (124, 500, 80*136, 1)]:
     W = synth.pn_random_blocks(type_, N, K, seed=N + K)
     X = synth.activations(M, K, seed=M)
     for flags in (0, pnq.GEMV_STATIC_WEIGHTS):
