@@ -365,6 +365,10 @@ struct PnMma {
 // whatever the segment lengths; a warp adds its task sums into its own slice of per-row sums.
 //
 // Either way the slices are summed in warp order at the end.
+//
+// The SM takes in bulk copies at about the HBM rate per SM, in issue order, so x requested after
+// the producer has filled the ring would land only behind all of it. The producer therefore issues
+// one stage, then waits until every consumer warp has requested its x, and fills the ring behind.
 
 constexpr int kRsWarps = 8;      // consumer warps
 constexpr int kRsProducers = 2;  // producer warps, rows 0..7 and 8..15 of each group
@@ -374,6 +378,7 @@ constexpr int kRsMaxSeg = 32;      // segments of a row at most
 constexpr int kRsZs = 4;           // activation rows of the zero-point table (M <= 4)
 constexpr int kRsZb = kUnitBlocks * kRsZs + kRsZs;  // floats per unit: terms [block][m], then 2^(24 - sigma) [m]
 constexpr uint32_t kRsConsumerBar = 1;              // named barrier of the consumer warps
+constexpr int kRsXAhead = 1;                        // weight stages issued before x is requested
 
 // Stage pitch of a row (segment) of `bytes` (a multiple of 16): the least multiple of 16 >= bytes
 // whose quotient by 16 is odd.
@@ -401,7 +406,8 @@ __global__ void __launch_bounds__(kRsThreads, 1) pn_rows_kernel(const __grid_con
     const int S = a.S, M = a.M, U = a.U, nseg = SEG ? a.nseg : 1;
     auto full = [&](int s) { return bar0 + 8u * s; };
     auto empty = [&](int s) { return bar0 + 8u * (S + s); };
-    const uint32_t xfull = bar0 + 8u * (2 * S);  // all of x has landed (SEG)
+    const uint32_t xfull = bar0 + 8u * (2 * S);      // all of x has landed (SEG)
+    const uint32_t xreq = bar0 + 8u * (2 * S + 1);   // every consumer warp has requested its x
     auto stage = [&](int s) { return base + a.off_stage + static_cast<uint32_t>(s) * a.stage_bytes; };
     auto rec = [&](int u) { return base + a.off_rec + static_cast<uint32_t>(u) * C::REC; };
     auto zbu = [&](int u) { return reinterpret_cast<float*>(base + a.off_zb) + u * kRsZb; };
@@ -423,6 +429,7 @@ __global__ void __launch_bounds__(kRsThreads, 1) pn_rows_kernel(const __grid_con
             for (int j = 0; j <= nseg; ++j) seg_tab[j] = j * U / nseg;
             mbar_init(xfull, 1);
         }
+        mbar_init(xreq, active);
         mbar_fence_init();
     }
     __syncthreads();
@@ -436,6 +443,10 @@ __global__ void __launch_bounds__(kRsThreads, 1) pn_rows_kernel(const __grid_con
         int s = 0;
         for (int i = 0, j = 0; s < nstages; ++s) {
             const int slot = s % S;
+            if (s == kRsXAhead && !mbar_wait_warp(xreq, 0)) {
+                ok = false;
+                break;
+            }
             if (s >= S && !mbar_wait_warp(empty(slot), ((s / S) - 1) & 1)) {
                 ok = false;
                 break;
@@ -504,6 +515,8 @@ __global__ void __launch_bounds__(kRsThreads, 1) pn_rows_kernel(const __grid_con
             };
             load(0);
             load(1);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(xreq);
             for (int q = 0; q < npair; ++q) {
                 const int u = warp + (q / M) * kRsWarps, m = q % M;
                 cp_async_wait<1>();  // pair q's x has landed (pair q + 1's may still be in flight)
@@ -544,7 +557,9 @@ __global__ void __launch_bounds__(kRsThreads, 1) pn_rows_kernel(const __grid_con
                     for (int m = 0; m < M; ++m)
                         bulk_g2s_plain(smem_addr(xs) + m * row, a.X + static_cast<size_t>(m) * a.K, row, xfull);
                 }
+                __syncwarp();
             }
+            if (lane == 0) mbar_arrive(xreq);
             ok = mbar_wait_warp(xfull, 0);
             if (ok)
                 for (int p = warp; p < U * M; p += kRsWarps) {
@@ -612,7 +627,7 @@ bool rs_plan(int64_t N, int U, int M, int sms, int s_req, RsPlan& p) {
     const int64_t rows_max = (N + p.G - 1) / p.G;
     p.rows_pad = static_cast<int>((rows_max + kGroupRows - 1) / kGroupRows * kGroupRows);
     const bool whole = U <= kRsWholeUnits;
-    p.off_rec = align_up(8u * (2u * kMaxStages + 1), 128);
+    p.off_rec = align_up(8u * (2u * kMaxStages + 2), 128);
     p.off_zb = align_up(p.off_rec + static_cast<uint32_t>(U) * C::REC, 16);
     p.off_x = align_up(p.off_zb + static_cast<uint32_t>(U) * kRsZb * 4u, 16);
     const uint32_t xbytes = whole ? kRsWarps * 2u * C::UK * 4u : static_cast<uint32_t>(M) * U * C::UK * 4u;

@@ -184,7 +184,7 @@ void check_rs_plan(int64_t N, int U, int M, int s_req) {
     if (whole != (p.nseg == 1)) FAIL("%d segments for %d units", p.nseg, U);
     if (whole && p.pitch != pnq::rs_pitch(U * pnq::kUnitBytes)) FAIL("whole-row pitch %d", p.pitch);
     const uint64_t xbytes = whole ? 4ull * pnq::kRsWarps * 2 * C::UK : 4ull * M * U * C::UK;
-    std::vector<R> r = {{0, 8ull * (2 * p.S + 1), "barriers"},
+    std::vector<R> r = {{0, 8ull * (2 * p.S + 2), "barriers"},
                         {p.off_rec, p.off_rec + 1ull * U * C::REC, "B operands"},
                         {p.off_zb, p.off_zb + 4ull * U * pnq::kRsZb, "zero-point terms"},
                         {p.off_x, p.off_x + xbytes, "x rows"},
