@@ -9,7 +9,8 @@ import ctypes
 import enum
 import os
 
-PN3T, PN4T, NVFP4 = 124, 125, 1004
+PN3T, PN4T, NVFP4, NVFP4_DIV = 124, 125, 1004, 1005
+NVFP4_TYPES = (NVFP4, NVFP4_DIV)
 BLOCK_WEIGHTS = {PN3T: 80, PN4T: 64}
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -88,7 +89,7 @@ def nvfp4_weights(codes_ptr: int, scales_ptr: int, global_scale: float) -> pnq_n
 
 def _w_arg(type_: int, W):
     """PN: W is a device address (int). NVFP4: W is a pnq_nvfp4_weights (passed by host pointer)."""
-    if type_ == NVFP4:
+    if type_ in NVFP4_TYPES:
         if not isinstance(W, pnq_nvfp4_weights):
             raise TypeError("NVFP4 weights must be a pnq_nvfp4_weights descriptor")
         return ctypes.byref(W)
@@ -157,7 +158,7 @@ def _require(t, what: str, dtypes, numel: int | None = None) -> None:
 
 def _check_weights(type_: int, W, n_rows: int, K: int) -> None:
     import torch
-    if type_ == NVFP4:
+    if type_ in NVFP4_TYPES:
         codes, scales, _g = W
         whole = K > 0 and K % 16 == 0
         _require(codes, "NVFP4 codes", (torch.uint8,), n_rows * K // 2 if whole else None)
@@ -171,7 +172,7 @@ def _check_weights(type_: int, W, n_rows: int, K: int) -> None:
 def _check_x(type_: int, X, K: int) -> int:
     """The activation rows M of X ([M][K], or [K] for M = 1), after checking X."""
     import torch
-    dtypes = (torch.bfloat16, torch.int16) if type_ == NVFP4 else (torch.float32,)
+    dtypes = (torch.bfloat16, torch.int16) if type_ in NVFP4_TYPES else (torch.float32,)
     M = X.shape[0] if X.dim() == 2 else 1
     _require(X, "X", dtypes)
     if X.numel() != M * K:
@@ -180,7 +181,7 @@ def _check_x(type_: int, X, K: int) -> int:
 
 
 def _weights(type_: int, W):
-    if type_ == NVFP4:
+    if type_ in NVFP4_TYPES:
         codes, scales, g = W
         return nvfp4_weights(codes.data_ptr(), scales.data_ptr(), g)
     return W.data_ptr()
@@ -218,7 +219,7 @@ def dequantize_row(type_: int, W, n_rows: int, K: int, out=None, stream=None):
     import torch
     _check_weights(type_, W, n_rows, K)
     if out is None:
-        dev = W[0].device if type_ == NVFP4 else W.device
+        dev = W[0].device if type_ in NVFP4_TYPES else W.device
         out = torch.empty((n_rows, K), dtype=torch.float32, device=dev)
     _require(out, "out", (torch.float32,), n_rows * K)
     _check(dequantize_row_ptr(type_, _weights(type_, W), n_rows, K, out.data_ptr(), _stream_handle(stream)),
@@ -230,7 +231,7 @@ def validate_row(type_: int, W, n_rows: int, K: int, flags=None, stream=None):
     import torch
     _check_weights(type_, W, n_rows, K)
     if flags is None:
-        dev = W[0].device if type_ == NVFP4 else W.device
+        dev = W[0].device if type_ in NVFP4_TYPES else W.device
         flags = torch.empty((n_rows,), dtype=torch.int32, device=dev)
     _require(flags, "flags", (torch.int32,), n_rows)
     _check(validate_row_ptr(type_, _weights(type_, W), n_rows, K, flags.data_ptr(), _stream_handle(stream)),

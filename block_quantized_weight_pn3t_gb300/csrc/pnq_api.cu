@@ -73,9 +73,9 @@ int map_cuda(cudaError_t e) { return e == cudaSuccess ? PNQ_OK : PNQ_ERR_CUDA; }
 
 // Shared shape / pointer checks. On success fills the NVFP4 view (when type is NVFP4).
 int check_common(int type, const void* W, int64_t rows, int64_t K, Nvfp4View* nv) {
-    if (type != PNQ_PN3T && type != PNQ_PN4T && type != PNQ_NVFP4) return PNQ_ERR_TYPE;
+    if (type != PNQ_PN3T && type != PNQ_PN4T && type != PNQ_NVFP4 && type != PNQ_NVFP4_DIV) return PNQ_ERR_TYPE;
     if (rows < 0 || K <= 0) return PNQ_ERR_SHAPE;
-    if (type == PNQ_NVFP4) {
+    if (type == PNQ_NVFP4 || type == PNQ_NVFP4_DIV) {
         if (K % 16 != 0) return PNQ_ERR_SHAPE;
         if (rows > INT64_MAX / K) return PNQ_ERR_SHAPE;
         if (!W) return PNQ_ERR_NULL;
@@ -84,6 +84,7 @@ int check_common(int type, const void* W, int64_t rows, int64_t K, Nvfp4View* nv
         nv->codes = d->codes;
         nv->scales = d->scales;
         nv->g = d->global_scale;
+        nv->div = type == PNQ_NVFP4_DIV;
         return PNQ_OK;
     }
     const int blk = block_weights(type);
@@ -161,11 +162,21 @@ int gemv_impl(int type, const void* W, int64_t N, int64_t K, const void* X, int 
     if (!aligned(Y, 4)) return PNQ_ERR_ALIGN;
     const bool static_w = (flags & PNQ_GEMV_STATIC_WEIGHTS) != 0;
     const int mode = forced_kernel();
-    if (type == PNQ_NVFP4) {
+    if (type == PNQ_NVFP4 || type == PNQ_NVFP4_DIV) {
         if (!aligned(X, 2)) return PNQ_ERR_ALIGN;
         const uint16_t* x = static_cast<const uint16_t*>(X);
-        if (mode != 1 && aligned(nv.codes, 16) && aligned(nv.scales, 16) && aligned(x, 16) && K % 256 == 0) {
-            const cudaError_t e = launch_nvfp4_gemv_mma(nv, N, K, x, M, Y, error_word(), 0, 0, static_w, stream);
+        // the fast path scales by a multiplier: for a divisor d_w, fp32(1 / d_w) when that is a
+        // normal number (a relative change of at most 2^-24 per weight, inside the accuracy
+        // bound); otherwise the generic path divides each output by d_w
+        Nvfp4View fast = nv;
+        if (nv.div) {
+            fast.g = 1.0f / nv.g;
+            fast.div = false;
+        }
+        const bool mult_ok = !nv.div || (fast.g >= 1.17549435e-38f && fast.g <= 3.4028234663852886e38f);
+        if (mode != 1 && mult_ok && aligned(nv.codes, 16) && aligned(nv.scales, 16) && aligned(x, 16) &&
+            K % 256 == 0) {
+            const cudaError_t e = launch_nvfp4_gemv_mma(fast, N, K, x, M, Y, error_word(), 0, 0, static_w, stream);
             if (e != cudaErrorNotSupported) return map_cuda(e);
         }
         return map_cuda(launch_nvfp4_gemv_simt(nv, N, K, x, M, Y, stream));
@@ -205,7 +216,7 @@ extern "C" int pnq_dequantize_row(int type, const void* W, int64_t n_rows, int64
     if (n_rows == 0) return PNQ_OK;
     if (!out) return PNQ_ERR_NULL;
     if (!aligned(out, 4)) return PNQ_ERR_ALIGN;
-    if (type == PNQ_NVFP4) return map_cuda(launch_nvfp4_dequant(nv, n_rows, K, out, stream));
+    if (type == PNQ_NVFP4 || type == PNQ_NVFP4_DIV) return map_cuda(launch_nvfp4_dequant(nv, n_rows, K, out, stream));
     return map_cuda(launch_pn_dequant(type, static_cast<const uint8_t*>(W), n_rows, K, out, stream));
 }
 
@@ -217,7 +228,7 @@ extern "C" int pnq_validate_row(int type, const void* W, int64_t n_rows, int64_t
     if (n_rows == 0) return PNQ_OK;
     if (!flags) return PNQ_ERR_NULL;
     if (!aligned(flags, 4)) return PNQ_ERR_ALIGN;
-    if (type == PNQ_NVFP4) return map_cuda(launch_nvfp4_validate(nv, n_rows, K, flags, stream));
+    if (type == PNQ_NVFP4 || type == PNQ_NVFP4_DIV) return map_cuda(launch_nvfp4_validate(nv, n_rows, K, flags, stream));
     return map_cuda(launch_pn_validate(type, static_cast<const uint8_t*>(W), n_rows, K, flags, stream));
 }
 

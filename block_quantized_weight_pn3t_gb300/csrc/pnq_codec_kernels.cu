@@ -47,6 +47,7 @@ __global__ void __launch_bounds__(kThreads) pn_dequant_kernel(const uint8_t* __r
 
 // One thread per code byte (two weights); code byte c of the flat [N][K/2] array belongs
 // to scale c / 8 of the flat [N][K/16] array.
+template <bool DIV>
 __global__ void __launch_bounds__(kThreads) nvfp4_dequant_kernel(const uint8_t* __restrict__ codes,
                                                                    const uint8_t* __restrict__ scales, float g,
                                                                    int64_t nbytes, float* __restrict__ out) {
@@ -54,11 +55,11 @@ __global__ void __launch_bounds__(kThreads) nvfp4_dequant_kernel(const uint8_t* 
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < nbytes; i += stride) {
         const uint32_t c = __ldg(codes + i);
         const float s = e4m3_to_f32(__ldg(scales + (i >> 3)));
-        // e2m1 * e4m3 is exact in fp32; the product with g is the single rounding.
+        // e2m1 * e4m3 is exact in fp32; the product with (quotient by) g is the single rounding.
         const float lo = e2m1_to_f32(c & 15u) * s;
         const float hi = e2m1_to_f32(c >> 4) * s;
-        out[2 * i] = __fmul_rn(lo, g);
-        out[2 * i + 1] = __fmul_rn(hi, g);
+        out[2 * i] = DIV ? __fdiv_rn(lo, g) : __fmul_rn(lo, g);
+        out[2 * i + 1] = DIV ? __fdiv_rn(hi, g) : __fmul_rn(hi, g);
     }
 }
 
@@ -126,7 +127,10 @@ cudaError_t launch_nvfp4_dequant(const Nvfp4View& w, int64_t n_rows, int64_t K, 
                                  cudaStream_t stream) {
     const int64_t nbytes = n_rows * (K / 2);
     if (nbytes == 0) return cudaSuccess;
-    nvfp4_dequant_kernel<<<grid_for(nbytes, 1), kThreads, 0, stream>>>(w.codes, w.scales, w.g, nbytes, out);
+    if (w.div)
+        nvfp4_dequant_kernel<true><<<grid_for(nbytes, 1), kThreads, 0, stream>>>(w.codes, w.scales, w.g, nbytes, out);
+    else
+        nvfp4_dequant_kernel<false><<<grid_for(nbytes, 1), kThreads, 0, stream>>>(w.codes, w.scales, w.g, nbytes, out);
     return cudaGetLastError();
 }
 

@@ -72,9 +72,10 @@ __global__ void __launch_bounds__(kThreads) pn_gemv_simt_kernel(const uint8_t* _
     }
 }
 
+// g multiplies each output, or divides it (div: the divisor reading of the global field).
 __global__ void __launch_bounds__(kThreads) nvfp4_gemv_simt_kernel(const uint8_t* __restrict__ codes,
                                                                      const uint8_t* __restrict__ scales, float g,
-                                                                     int64_t N, int64_t K,
+                                                                     bool div, int64_t N, int64_t K,
                                                                      const uint16_t* __restrict__ X, int M,
                                                                      float* __restrict__ Y) {
     const int lane = threadIdx.x & 31;
@@ -112,7 +113,7 @@ __global__ void __launch_bounds__(kThreads) nvfp4_gemv_simt_kernel(const uint8_t
         for (int m = 0; m < kMaxM; ++m) {
             if (m < M) {
                 const float v = warp_sum(acc[m]);
-                if (lane == 0) Y[m * N + row] = v * g;
+                if (lane == 0) Y[m * N + row] = div ? v / g : v * g;
             }
         }
     }
@@ -138,7 +139,7 @@ cudaError_t launch_pn_gemv_simt(int type, const uint8_t* W, int64_t N, int64_t K
 cudaError_t launch_nvfp4_gemv_simt(const Nvfp4View& w, int64_t N, int64_t K, const uint16_t* X, int M,
                                    float* Y, cudaStream_t stream) {
     if (N == 0) return cudaSuccess;
-    nvfp4_gemv_simt_kernel<<<rows_grid(N), kThreads, 0, stream>>>(w.codes, w.scales, w.g, N, K, X, M, Y);
+    nvfp4_gemv_simt_kernel<<<rows_grid(N), kThreads, 0, stream>>>(w.codes, w.scales, w.g, w.div, N, K, X, M, Y);
     return cudaGetLastError();
 }
 

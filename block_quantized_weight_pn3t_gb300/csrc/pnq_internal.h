@@ -10,7 +10,8 @@ namespace pnq {
 struct Nvfp4View {
     const uint8_t* codes;   // device [N][K/2], low nibble = even k
     const uint8_t* scales;  // device [N][K/16] E4M3FN
-    float g;                // global multiplier
+    float g;                // global multiplier (div: the global divisor d_w)
+    bool div = false;       // the weight is e2m1 * e4m3 / g
 };
 
 int device_sm_count();

@@ -31,6 +31,9 @@
  *     packed two per byte, low nibble = even k, [N][K/2] row-major, and scales one
  *     E4M3FN byte per 16 weights along K, [N][K/16] row-major. global_scale is a
  *     multiplier (the TandemLLM reading).
+ *   PNQ_NVFP4_DIV (1005, a library id): the same codes and scales with the global field read
+ *     as a divisor d_w ("tensor-formats.md" section 3.3): w = e2m1 * e4m3fn / d_w. The
+ *     pnq_nvfp4_weights descriptor carries d_w in global_scale.
  *
  * Fast paths (taken automatically, never required)
  *   PN: W and X 16-byte aligned and (K/BLK) % 8 == 0.  NVFP4: codes, scales and X 16-byte
@@ -48,7 +51,7 @@
 extern "C" {
 #endif
 
-enum pnq_type { PNQ_PN3T = 124, PNQ_PN4T = 125, PNQ_NVFP4 = 1004 };
+enum pnq_type { PNQ_PN3T = 124, PNQ_PN4T = 125, PNQ_NVFP4 = 1004, PNQ_NVFP4_DIV = 1005 };
 
 enum pnq_status {
     PNQ_OK = 0,
@@ -76,7 +79,8 @@ enum pnq_gemv_flags {
 typedef struct pnq_nvfp4_weights {
     const uint8_t* codes;   /* device, [N][K/2] E2M1 pairs, low nibble = even k */
     const uint8_t* scales;  /* device, [N][K/16] E4M3FN */
-    float global_scale;     /* host value, multiplies every weight */
+    float global_scale;     /* host value: multiplies every weight (PNQ_NVFP4), or the
+                               divisor d_w of every weight (PNQ_NVFP4_DIV) */
 } pnq_nvfp4_weights;
 
 /*
@@ -84,9 +88,9 @@ typedef struct pnq_nvfp4_weights {
  * The decode-step product of the pages ("PN weight format", section "Where PN runs":
  * PN tensors use their own GEMV kernels; TandemLLM "Quantisation and profiles",
  * section NVFP4: the W4A16 kernel unpacks codes in registers before the multiply).
- *   type  PNQ_PN3T, PNQ_PN4T or PNQ_NVFP4.
+ *   type  PNQ_PN3T, PNQ_PN4T, PNQ_NVFP4 or PNQ_NVFP4_DIV.
  *   W     PN: device pointer to N*(K/BLK)*34 bytes, >= 2-byte aligned (else PNQ_ERR_ALIGN).
- *         NVFP4: host pointer to a pnq_nvfp4_weights.
+ *         NVFP4, NVFP4_DIV: host pointer to a pnq_nvfp4_weights.
  *   N     output rows (>= 0; N == 0 launches nothing).  K: inner dimension.
  *   X     device, [M][K] row-major: fp32 for PN (4-byte aligned), bf16 for NVFP4
  *         (2-byte aligned). Finite values; any magnitude is accepted.
@@ -128,7 +132,8 @@ int pnq_gemv_noalloc(int type, const void* W, int64_t N, int64_t K, const void* 
  * pnq_dequantize_row -- out[r][k] = the fp32 weight, bit-exact:
  *   PN: fp32(d) * fp32(n - z), exact ("PN weight format", section Value: both steps exact
  *   in fp32; code z with negative d gives -0.0). NVFP4: e2m1 * e4m3 (exact) times the
- *   global scale, rounded once to nearest-even fp32. A non-finite d or a NaN scale gives
+ *   global scale, rounded once to nearest-even fp32. NVFP4_DIV: e2m1 * e4m3 (exact)
+ *   divided by d_w, rounded once to nearest-even fp32. A non-finite d or a NaN scale gives
  *   NaN/inf of the IEEE product (bit patterns of NaNs are not specified).
  *   W      as for pnq_gemv (n_rows rows).   out: device fp32 [n_rows][K], 4-byte aligned.
  */
@@ -139,8 +144,9 @@ int pnq_dequantize_row(int type, const void* W, int64_t n_rows, int64_t K, float
  * pnq_validate_row -- flags[r] = 1 if row r is invalid, else 0.
  *   PN ("PN weight format", section Validation): any block's d is an fp16 NaN or infinity,
  *   or (pn3t) bit 15 or bit 31 of any word is set.
- *   NVFP4 ("tensor-formats.md" section 3.3): any scale byte has its sign bit set (negative
- *   or -0) or is NaN (0x7F / 0xFF), or global_scale is not finite and > 0 (then every row).
+ *   NVFP4 and NVFP4_DIV ("tensor-formats.md" section 3.3): any scale byte has its sign bit
+ *   set (negative or -0) or is NaN (0x7F / 0xFF), or global_scale is not finite and > 0
+ *   (then every row).
  *   W as for pnq_gemv.   flags: device int32 [n_rows], 4-byte aligned.
  */
 int pnq_validate_row(int type, const void* W, int64_t n_rows, int64_t K, int32_t* flags,

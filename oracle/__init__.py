@@ -19,6 +19,8 @@ _SRC = os.path.join(_HERE, "pnq_oracle.c")
 LIB_PATH = os.path.join(_HERE, "libpnq_oracle.so")
 
 PN3T, PN4T, NVFP4 = 124, 125, 1004
+Q4G64, Q5G64, Q6G64, W8G32 = 1104, 1105, 1106, 1108
+GROUPED = {Q4G64: (4, 64, -8, 7), Q5G64: (5, 64, -16, 15), Q6G64: (6, 64, -32, 31), W8G32: (8, 32, -127, 127)}
 BLOCK_WEIGHTS = {PN3T: 80, PN4T: 64}
 OK = 0
 
@@ -62,6 +64,13 @@ def lib() -> ctypes.CDLL:
             "pnq_ref_validate_row_nvfp4": (I32, [P, F, I64, I64, P]),
             "pnq_ref_gemv": (I32, [I32, P, I64, I64, P, I32, P, P]),
             "pnq_ref_gemv_nvfp4": (I32, [P, P, F, I64, I64, P, I32, P, P]),
+            "pnq_ref_dequantize_row_nvfp4_div": (I32, [P, P, F, I64, I64, P]),
+            "pnq_ref_grouped_plane_bytes": (I32, [I32, I64, P, P, P]),
+            "pnq_ref_dequantize_grouped": (I32, [I32, P, P, P, I64, I64, P]),
+            "pnq_ref_validate_grouped": (I32, [I32, P, P, P, I64, I64, P]),
+            "pnq_ref_quantize_grouped": (I32, [I32, P, I64, I64, P, P, P, P]),
+            "pnq_ref_gemv_grouped": (I32, [I32, P, P, P, I64, I64, P, I32, P, P]),
+            "pnq_ref_gemv_nvfp4_div": (I32, [P, P, F, I64, I64, P, I32, P, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -191,4 +200,91 @@ def gemv_nvfp4(codes: np.ndarray, scales: np.ndarray, g: float, N: int, K: int, 
     A = np.empty((M, N), dtype=np.float64)
     _check(lib().pnq_ref_gemv_nvfp4(_ptr(codes), _ptr(scales), g, N, K, _ptr(X), M, _ptr(Y), _ptr(A)),
            "gemv_nvfp4")
+    return Y, A
+
+
+def dequantize_nvfp4_div(codes: np.ndarray, scales: np.ndarray, dw: float, n_rows: int, K: int) -> np.ndarray:
+    """NVFP4 with the global field as a divisor: fp32(e2m1 * e4m3) / d_w."""
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    scales = np.ascontiguousarray(scales, dtype=np.uint8)
+    out = np.empty((n_rows, K), dtype=np.float32)
+    _check(lib().pnq_ref_dequantize_row_nvfp4_div(_ptr(codes), _ptr(scales), dw, n_rows, K, _ptr(out)),
+           "dequantize_nvfp4_div")
+    return out
+
+
+def gemv_nvfp4_div(codes: np.ndarray, scales: np.ndarray, dw: float, N: int, K: int, X_bf16: np.ndarray):
+    """X_bf16: uint16 [M][K] raw bf16 words; the weight is e2m1 * e4m3 / d_w."""
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    scales = np.ascontiguousarray(scales, dtype=np.uint8)
+    X = np.ascontiguousarray(X_bf16, dtype=np.uint16)
+    if X.ndim == 1:
+        X = X[None, :]
+    M = X.shape[0]
+    Y = np.empty((M, N), dtype=np.float64)
+    A = np.empty((M, N), dtype=np.float64)
+    _check(lib().pnq_ref_gemv_nvfp4_div(_ptr(codes), _ptr(scales), dw, N, K, _ptr(X), M, _ptr(Y), _ptr(A)),
+           "gemv_nvfp4_div")
+    return Y, A
+
+
+# ---- grouped signed-integer formats ("tensor-formats.md" sections 4 to 7) ----
+
+def grouped_plane_bytes(type_: int, K: int):
+    """(lo bytes, hi bytes, scales) per row of the library's plane layout."""
+    lo, hi, ns = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
+    _check(lib().pnq_ref_grouped_plane_bytes(type_, K, ctypes.byref(lo), ctypes.byref(hi), ctypes.byref(ns)),
+           "grouped_plane_bytes")
+    return lo.value, hi.value, ns.value
+
+
+def _planes(type_, lo, hi, sc):
+    lo = np.ascontiguousarray(lo, dtype=np.uint8)
+    hi = None if hi is None else np.ascontiguousarray(hi, dtype=np.uint8)
+    sc = np.ascontiguousarray(sc, dtype=np.uint16)
+    return lo, hi, sc
+
+
+def dequantize_grouped(type_: int, lo, hi, sc, n_rows: int, K: int) -> np.ndarray:
+    lo, hi, sc = _planes(type_, lo, hi, sc)
+    out = np.empty((n_rows, K), dtype=np.float32)
+    _check(lib().pnq_ref_dequantize_grouped(type_, _ptr(lo), None if hi is None else _ptr(hi), _ptr(sc), n_rows, K,
+                                            _ptr(out)), "dequantize_grouped")
+    return out
+
+
+def validate_grouped(type_: int, lo, hi, sc, n_rows: int, K: int) -> np.ndarray:
+    lo, hi, sc = _planes(type_, lo, hi, sc)
+    flags = np.empty(n_rows, dtype=np.int32)
+    _check(lib().pnq_ref_validate_grouped(type_, _ptr(lo), None if hi is None else _ptr(hi), _ptr(sc), n_rows, K,
+                                          _ptr(flags)), "validate_grouped")
+    return flags
+
+
+def quantize_grouped(type_: int, w: np.ndarray):
+    """Canonical encoder MAXABS_F16_RECIP_RNE_V1 on a [n_rows][K] float32 matrix. Returns
+    (lo, hi or None, scales); ValueError for a group the profile rejects (non-finite value or
+    an overflowing scale)."""
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    n_rows, K = w.shape
+    lb, hb, ns = grouped_plane_bytes(type_, K)
+    lo = np.zeros((n_rows, lb), dtype=np.uint8)
+    hi = np.zeros((n_rows, hb), dtype=np.uint8) if hb else None
+    sc = np.zeros((n_rows, ns), dtype=np.uint16)
+    fail = ctypes.c_int64(-1)
+    _check(lib().pnq_ref_quantize_grouped(type_, _ptr(w), n_rows, K, _ptr(lo), None if hi is None else _ptr(hi),
+                                          _ptr(sc), ctypes.byref(fail)), "quantize_grouped")
+    return lo, hi, sc
+
+
+def gemv_grouped(type_: int, lo, hi, sc, N: int, K: int, X: np.ndarray):
+    lo, hi, sc = _planes(type_, lo, hi, sc)
+    X = np.ascontiguousarray(X, dtype=np.float32)
+    if X.ndim == 1:
+        X = X[None, :]
+    M = X.shape[0]
+    Y = np.empty((M, N), dtype=np.float64)
+    A = np.empty((M, N), dtype=np.float64)
+    _check(lib().pnq_ref_gemv_grouped(type_, _ptr(lo), None if hi is None else _ptr(hi), _ptr(sc), N, K, _ptr(X), M,
+                                      _ptr(Y), _ptr(A)), "gemv_grouped")
     return Y, A

@@ -376,6 +376,46 @@ int pnq_ref_gemv(int type, const uint8_t* W, int64_t N, int64_t K, const float* 
     return PNQ_REF_OK;
 }
 
+/* GEMV over the divisor reading: the weight is e2m1 * e4m3 (exact) divided by d_w in fp64, which
+ * is within 2^-53 of the exact quotient (far inside the GEMV tolerance). */
+int pnq_ref_gemv_nvfp4_div(const uint8_t* codes, const uint8_t* scales, float dw, int64_t N,
+                           int64_t K, const uint16_t* X, int M, double* Y, double* A) {
+    if (N < 0 || K <= 0 || K % 16 != 0 || M < 1) return PNQ_REF_ERR_SHAPE;
+    if (!codes || !scales || !X || !Y) return PNQ_REF_ERR_NULL;
+    double* xd = (double*)malloc((size_t)K * (size_t)M * sizeof(double));
+    if (!xd) return PNQ_REF_ERR_VALUE;
+    for (int64_t i = 0; i < (int64_t)M * K; ++i) xd[i] = pnq_ref_bf16_to_double(X[i]);
+    for (int64_t n = 0; n < N; ++n)
+        for (int m = 0; m < M; ++m) {
+            double s = 0.0, a = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                double w = nvfp4_weight(codes + n * (K / 2), scales + n * (K / 16), 1.0f, k) / (double)dw;
+                double t = w * xd[(int64_t)m * K + k];
+                s += t;
+                a += fabs(t);
+            }
+            Y[(int64_t)m * N + n] = s;
+            if (A) A[(int64_t)m * N + n] = a;
+        }
+    free(xd);
+    return PNQ_REF_OK;
+}
+
+/* "tensor-formats.md" section 3.3 reads the global field as a divisor d_w:
+ * W = e2m1(code) * e4m3fn(scale) / d_w. e2m1 * e4m3 is exact in fp32 (at most 7 significant bits,
+ * magnitudes 2^-10 .. 2688), so the fp32 quotient is the exact weight rounded once. */
+int pnq_ref_dequantize_row_nvfp4_div(const uint8_t* codes, const uint8_t* scales, float dw,
+                                     int64_t n_rows, int64_t K, float* out) {
+    if (n_rows < 0 || K <= 0 || K % 16 != 0) return PNQ_REF_ERR_SHAPE;
+    if ((!codes || !scales || !out) && n_rows > 0) return PNQ_REF_ERR_NULL;
+    for (int64_t r = 0; r < n_rows; ++r)
+        for (int64_t k = 0; k < K; ++k) {
+            float prod = (float)nvfp4_weight(codes + r * (K / 2), scales + r * (K / 16), 1.0f, k);
+            out[r * K + k] = prod / dw;
+        }
+    return PNQ_REF_OK;
+}
+
 int pnq_ref_gemv_nvfp4(const uint8_t* codes, const uint8_t* scales, float g, int64_t N,
                        int64_t K, const uint16_t* X, int M, double* Y, double* A) {
     if (N < 0 || K <= 0 || K % 16 != 0 || M < 1) return PNQ_REF_ERR_SHAPE;
@@ -395,6 +435,183 @@ int pnq_ref_gemv_nvfp4(const uint8_t* codes, const uint8_t* scales, float g, int
             Y[(int64_t)m * N + n] = s;
             if (A) A[(int64_t)m * N + n] = a;
         }
+    free(xd);
+    return PNQ_REF_OK;
+}
+
+/* ---- grouped signed-integer formats ("tensor-formats.md", sections 4 to 7) ----------------
+ * Q4G64_F16S, Q5G64_F16S, Q6G64_F16S (b = 4, 5, 6 bits, groups of G = 64) and W8G32_F16S
+ * (b = 8, G = 32): one two's-complement code per weight, one binary16 scale per group of G along
+ * K (the last group of a row may be partial), reconstruction w = binary32(s32 * binary32(q)).
+ *
+ * Physical layout (the pages leave it to a layout registry; this is the library's own, a
+ * reading): K % 8 == 0; the low 4 bits of each logical word u in a nibble plane lo[N][K/2]
+ * (even k in the low nibble); the bits above in a second plane hi: Q5 one bit per weight,
+ * hi[N][K/8], bit k % 8 of byte k / 8; Q6 two bits per weight, hi[N][K/4], bits
+ * 2 (k % 4) .. 2 (k % 4) + 1 of byte k / 4; W8 stores u as one byte per weight in lo[N][K]
+ * and has no hi plane. Scales sc[N][ceil(K / G)], binary16 words. */
+
+typedef struct {
+    int bits, G, qmin, qmax;
+} grp_params;
+
+static int grp_lookup(int type, grp_params* p) {
+    switch (type) {
+        case PNQ_REF_Q4G64: p->bits = 4; p->G = 64; p->qmin = -8; p->qmax = 7; return 1;
+        case PNQ_REF_Q5G64: p->bits = 5; p->G = 64; p->qmin = -16; p->qmax = 15; return 1;
+        case PNQ_REF_Q6G64: p->bits = 6; p->G = 64; p->qmin = -32; p->qmax = 31; return 1;
+        case PNQ_REF_W8G32: p->bits = 8; p->G = 32; p->qmin = -127; p->qmax = 127; return 1;
+        default: return 0;
+    }
+}
+
+/* Logical word u of weight k of a row (planes of that row). */
+static uint32_t grp_word(const grp_params* p, const uint8_t* lo, const uint8_t* hi, int64_t k) {
+    if (p->bits == 8) return lo[k];
+    uint32_t u = (k & 1) ? (uint32_t)(lo[k / 2] >> 4) : (uint32_t)(lo[k / 2] & 15);
+    if (p->bits == 5) u |= (uint32_t)((hi[k / 8] >> (k % 8)) & 1) << 4;
+    if (p->bits == 6) u |= (uint32_t)((hi[k / 4] >> (2 * (k % 4))) & 3) << 4;
+    return u;
+}
+
+static void grp_put(const grp_params* p, uint8_t* lo, uint8_t* hi, int64_t k, uint32_t u) {
+    if (p->bits == 8) { lo[k] = (uint8_t)u; return; }
+    if (k & 1) lo[k / 2] = (uint8_t)((lo[k / 2] & 0x0F) | ((u & 15) << 4));
+    else lo[k / 2] = (uint8_t)((lo[k / 2] & 0xF0) | (u & 15));
+    if (p->bits == 5) hi[k / 8] = (uint8_t)((hi[k / 8] & ~(1u << (k % 8))) | (((u >> 4) & 1) << (k % 8)));
+    if (p->bits == 6)
+        hi[k / 4] = (uint8_t)((hi[k / 4] & ~(3u << (2 * (k % 4)))) | (((u >> 4) & 3) << (2 * (k % 4))));
+}
+
+/* Section 5: q = u for u < 2^(b-1), else u - 2^b. */
+static int grp_signed(const grp_params* p, uint32_t u) {
+    return (u < (1u << (p->bits - 1))) ? (int)u : (int)u - (1 << p->bits);
+}
+
+int pnq_ref_grouped_plane_bytes(int type, int64_t K, int64_t* lo_bytes, int64_t* hi_bytes, int64_t* n_scales) {
+    grp_params p;
+    if (!grp_lookup(type, &p)) return PNQ_REF_ERR_TYPE;
+    if (K <= 0 || K % 8 != 0) return PNQ_REF_ERR_SHAPE;
+    *lo_bytes = (p.bits == 8) ? K : K / 2;
+    *hi_bytes = (p.bits == 5) ? K / 8 : (p.bits == 6) ? K / 4 : 0;
+    *n_scales = (K + p.G - 1) / p.G;
+    return PNQ_REF_OK;
+}
+
+static float f16_bits_to_float(uint16_t h) { return (float)pnq_ref_fp16_to_double(h); } /* exact */
+
+/* Section 6.2: w_hat = binary32(s32 * binary32(q)). */
+int pnq_ref_dequantize_grouped(int type, const uint8_t* lo, const uint8_t* hi, const uint16_t* sc,
+                               int64_t n_rows, int64_t K, float* out) {
+    grp_params p;
+    int64_t lb, hb, ns;
+    int rc = pnq_ref_grouped_plane_bytes(type, K, &lb, &hb, &ns);
+    if (rc != PNQ_REF_OK) return rc;
+    grp_lookup(type, &p);
+    if (n_rows < 0) return PNQ_REF_ERR_SHAPE;
+    if (n_rows > 0 && (!lo || !sc || !out || (hb > 0 && !hi))) return PNQ_REF_ERR_NULL;
+    for (int64_t r = 0; r < n_rows; ++r)
+        for (int64_t k = 0; k < K; ++k) {
+            int q = grp_signed(&p, grp_word(&p, lo + r * lb, hi ? hi + r * hb : NULL, k));
+            float s32 = f16_bits_to_float(sc[r * ns + k / p.G]);
+            out[r * K + k] = s32 * (float)q;
+        }
+    return PNQ_REF_OK;
+}
+
+/* Section 6 validity: a scale is +0 or a finite positive binary16 (sign clear, exponent not all
+ * ones); a group whose scale is +0 holds only zero codes; W8 never holds the word 0x80. */
+int pnq_ref_validate_grouped(int type, const uint8_t* lo, const uint8_t* hi, const uint16_t* sc,
+                             int64_t n_rows, int64_t K, int32_t* flags) {
+    grp_params p;
+    int64_t lb, hb, ns;
+    int rc = pnq_ref_grouped_plane_bytes(type, K, &lb, &hb, &ns);
+    if (rc != PNQ_REF_OK) return rc;
+    grp_lookup(type, &p);
+    if (n_rows < 0) return PNQ_REF_ERR_SHAPE;
+    if (n_rows > 0 && (!lo || !sc || !flags || (hb > 0 && !hi))) return PNQ_REF_ERR_NULL;
+    for (int64_t r = 0; r < n_rows; ++r) {
+        int bad = 0;
+        for (int64_t k = 0; k < K; ++k) {
+            uint16_t s = sc[r * ns + k / p.G];
+            uint32_t u = grp_word(&p, lo + r * lb, hi ? hi + r * hb : NULL, k);
+            if ((s & 0x8000) || (s & 0x7C00) == 0x7C00) bad = 1;
+            if (s == 0 && u != 0) bad = 1;
+            if (p.bits == 8 && u == 0x80) bad = 1;
+        }
+        flags[r] = bad;
+    }
+    return PNQ_REF_OK;
+}
+
+/* Section 7, MAXABS_F16_RECIP_RNE_V1, per group of binary32 values, every step rounded to
+ * nearest even in binary32 (or binary16 for the scale):
+ *   amax = max |x|; amax == +0 -> scale +0, codes 0;
+ *   raw = amax / qmax; scale16 = binary16(raw), +0 -> 0x0001; not finite -> fail;
+ *   inv = 1 / scale32; code = clamp(rint(x * inv), qmin, qmax).
+ * A non-finite source value fails. On failure the call returns PNQ_REF_ERR_VALUE and
+ * fail_row (if given) receives the row. */
+int pnq_ref_quantize_grouped(int type, const float* w, int64_t n_rows, int64_t K, uint8_t* lo,
+                             uint8_t* hi, uint16_t* sc, int64_t* fail_row) {
+    grp_params p;
+    int64_t lb, hb, ns;
+    int rc = pnq_ref_grouped_plane_bytes(type, K, &lb, &hb, &ns);
+    if (rc != PNQ_REF_OK) return rc;
+    grp_lookup(type, &p);
+    if (n_rows < 0) return PNQ_REF_ERR_SHAPE;
+    if (n_rows > 0 && (!w || !lo || !sc || (hb > 0 && !hi))) return PNQ_REF_ERR_NULL;
+    for (int64_t r = 0; r < n_rows; ++r) {
+        uint8_t* lr = lo + r * lb;
+        uint8_t* hr = hi ? hi + r * hb : NULL;
+        for (int64_t g = 0; g < ns; ++g) {
+            int64_t k0 = g * p.G, k1 = (k0 + p.G < K) ? k0 + p.G : K;
+            float amax = 0.0f;
+            for (int64_t k = k0; k < k1; ++k) {
+                float v = w[r * K + k];
+                if (!isfinite(v)) { if (fail_row) *fail_row = r; return PNQ_REF_ERR_VALUE; }
+                if (fabsf(v) > amax) amax = fabsf(v);
+            }
+            if (amax == 0.0f) {
+                sc[r * ns + g] = 0x0000;
+                for (int64_t k = k0; k < k1; ++k) grp_put(&p, lr, hr, k, 0);
+                continue;
+            }
+            float raw = amax / (float)p.qmax;
+            uint16_t s16 = pnq_ref_double_to_fp16((double)raw);  /* one rounding: raw is exact in fp64 */
+            if (s16 == 0x0000) s16 = 0x0001;
+            if ((s16 & 0x7C00) == 0x7C00) { if (fail_row) *fail_row = r; return PNQ_REF_ERR_VALUE; }
+            sc[r * ns + g] = s16;
+            float inv = 1.0f / f16_bits_to_float(s16);
+            for (int64_t k = k0; k < k1; ++k) {
+                float nrm = w[r * K + k] * inv;
+                float q = rintf(nrm);  /* ties to even in the default rounding mode */
+                if (q < (float)p.qmin) q = (float)p.qmin;
+                if (q > (float)p.qmax) q = (float)p.qmax;
+                int qi = (int)q;
+                grp_put(&p, lr, hr, k, (uint32_t)qi & ((1u << p.bits) - 1u));
+            }
+        }
+    }
+    return PNQ_REF_OK;
+}
+
+/* Y[m][n] = sum_k w_hat[n][k] x[m][k] in fp64 over the reconstructed binary32 weights, x fp32. */
+int pnq_ref_gemv_grouped(int type, const uint8_t* lo, const uint8_t* hi, const uint16_t* sc, int64_t N,
+                         int64_t K, const float* X, int M, double* Y, double* A) {
+    int64_t lb, hb, ns;
+    int rc = pnq_ref_grouped_plane_bytes(type, K, &lb, &hb, &ns);
+    if (rc != PNQ_REF_OK) return rc;
+    if (N < 0 || M < 1) return PNQ_REF_ERR_SHAPE;
+    if (!lo || !sc || !X || !Y || (hb > 0 && !hi)) return PNQ_REF_ERR_NULL;
+    float* row = (float*)malloc((size_t)K * sizeof(float));
+    double* xd = (double*)malloc((size_t)K * (size_t)M * sizeof(double));
+    if (!row || !xd) { free(row); free(xd); return PNQ_REF_ERR_VALUE; }
+    for (int64_t i = 0; i < (int64_t)M * K; ++i) xd[i] = (double)X[i];
+    for (int64_t n = 0; n < N; ++n) {
+        pnq_ref_dequantize_grouped(type, lo + n * lb, hi ? hi + n * hb : NULL, sc + n * ns, 1, K, row);
+        dot_rows(row, K, xd, M, N, n, Y, A);
+    }
+    free(row);
     free(xd);
     return PNQ_REF_OK;
 }

@@ -27,6 +27,8 @@ extern "C" {
 #endif
 
 enum { PNQ_REF_PN3T = 124, PNQ_REF_PN4T = 125, PNQ_REF_NVFP4 = 1004 };
+/* grouped signed-integer formats ("tensor-formats.md" sections 4-7; the ids are this library's) */
+enum { PNQ_REF_Q4G64 = 1104, PNQ_REF_Q5G64 = 1105, PNQ_REF_Q6G64 = 1106, PNQ_REF_W8G32 = 1108 };
 enum { PNQ_REF_OK = 0, PNQ_REF_ERR_TYPE = -1, PNQ_REF_ERR_SHAPE = -2,
        PNQ_REF_ERR_NULL = -3, PNQ_REF_ERR_VALUE = -6 };
 
@@ -62,8 +64,27 @@ int pnq_ref_validate_row_nvfp4(const uint8_t* scales, float g, int64_t n_rows, i
  * Y and A are fp64 [M][N]; A may be NULL. */
 int pnq_ref_gemv(int type, const uint8_t* W, int64_t N, int64_t K, const float* X, int M,
                  double* Y, double* A);
+/* NVFP4 with the global field read as a divisor d_w ("tensor-formats.md" section 3.3):
+ * out = fp32(e2m1 * e4m3) / d_w (one rounding); the GEMV divides the exact product in fp64. */
+int pnq_ref_dequantize_row_nvfp4_div(const uint8_t* codes, const uint8_t* scales, float dw,
+                                     int64_t n_rows, int64_t K, float* out);
+int pnq_ref_gemv_nvfp4_div(const uint8_t* codes, const uint8_t* scales, float dw, int64_t N,
+                           int64_t K, const uint16_t* X, int M, double* Y, double* A);
 int pnq_ref_gemv_nvfp4(const uint8_t* codes, const uint8_t* scales, float g, int64_t N,
                        int64_t K, const uint16_t* X, int M, double* Y, double* A);
+
+/* Grouped signed-integer formats ("tensor-formats.md" sections 4 to 7), in the library's plane
+ * layout (pnq_oracle.c states it): plane sizes per row, decode, validity, the canonical encoder
+ * MAXABS_F16_RECIP_RNE_V1 (section 7) and the GEMV over the reconstructed binary32 weights. */
+int pnq_ref_grouped_plane_bytes(int type, int64_t K, int64_t* lo_bytes, int64_t* hi_bytes, int64_t* n_scales);
+int pnq_ref_dequantize_grouped(int type, const uint8_t* lo, const uint8_t* hi, const uint16_t* sc,
+                               int64_t n_rows, int64_t K, float* out);
+int pnq_ref_validate_grouped(int type, const uint8_t* lo, const uint8_t* hi, const uint16_t* sc,
+                             int64_t n_rows, int64_t K, int32_t* flags);
+int pnq_ref_quantize_grouped(int type, const float* w, int64_t n_rows, int64_t K, uint8_t* lo,
+                             uint8_t* hi, uint16_t* sc, int64_t* fail_row);
+int pnq_ref_gemv_grouped(int type, const uint8_t* lo, const uint8_t* hi, const uint16_t* sc, int64_t N,
+                         int64_t K, const float* X, int M, double* Y, double* A);
 
 #ifdef __cplusplus
 }

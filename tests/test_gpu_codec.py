@@ -69,6 +69,38 @@ def test_nvfp4_dequantize_random(oracle, offset):
     assert same_bits_or_nan(out.cpu().numpy(), oracle.dequantize_nvfp4(codes.numpy(), scales.numpy(), g, N, K))
 
 
+def test_nvfp4_div_dequantize_every_code_and_scale(oracle):
+    codes = np.zeros((256, 8), dtype=np.uint8)
+    scales = np.arange(256, dtype=np.uint8).reshape(256, 1)
+    codes[:] = [(2 * i) | ((2 * i + 1) << 4) for i in range(8)]
+    for dw in (1.0, 0.37, 3.0e-5, 7.5e30, 1.0e-40):
+        out = pnq.dequantize_row(pnq.NVFP4_DIV, (torch.from_numpy(codes).cuda(), torch.from_numpy(scales).cuda(), dw),
+                                 256, 16)
+        assert same_bits_or_nan(out.cpu().numpy(), oracle.dequantize_nvfp4_div(codes, scales, dw, 256, 16))
+
+
+@pytest.mark.parametrize("offset", [0, 1, 3])
+def test_nvfp4_div_dequantize_random(oracle, offset):
+    N, K = 50, 272
+    codes, scales, _ = synth.nvfp4_random(N, K, seed=7)
+    cd, _ = device_bytes(codes.numpy(), offset)
+    sd, _ = device_bytes(scales.numpy(), offset)
+    out = pnq.dequantize_row(pnq.NVFP4_DIV, (cd, sd, 0.37), N, K)
+    assert same_bits_or_nan(out.cpu().numpy(), oracle.dequantize_nvfp4_div(codes.numpy(), scales.numpy(), 0.37, N, K))
+
+
+def test_validate_nvfp4_div(oracle):
+    """Same validity rule as the multiplier reading: the divisor must be finite and > 0."""
+    N, K = 40, 64
+    codes, scales, _ = synth.nvfp4_random(N, K, seed=8)
+    s = scales.numpy().copy()
+    s[3, 1] = 0x80
+    s[7, 0] = 0x7F
+    for dw in (0.37, 1.0e-45, 0.0, -1.0, float("inf"), float("nan")):
+        flags = pnq.validate_row(pnq.NVFP4_DIV, (codes.cuda(), torch.from_numpy(s).cuda(), dw), N, K).cpu().numpy()
+        assert np.array_equal(flags, oracle.validate_nvfp4(s, dw, N, K))
+
+
 def inject_bad_rows(type_, W, K, rng):
     """Rows with non-finite d (0x7C00, 0xFC00, 0x7E00, 0x7C01) and, for pn3t, set reserved bits."""
     nb = K // BLK[type_]

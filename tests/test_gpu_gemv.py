@@ -88,6 +88,50 @@ def test_nvfp4_shapes(oracle, K, N, M):
         assert_within_tolerance(Y, Yr, Ar, f"nvfp4 K={K} N={N} M={M} off={offset}")
 
 
+def run_nv_div(codes, scales, dw, N, K, Xb, offset=0):
+    cd, _b1 = device_bytes(codes, offset)
+    sd, _b2 = device_bytes(scales, offset)
+    M = Xb.shape[0]
+    buf, Y = f32_with_canary(M, N)
+    pnq.gemv(pnq.NVFP4_DIV, (cd, sd, dw), torch.from_numpy(Xb.view(np.int16)).cuda(), N, K, Y=Y)
+    torch.cuda.synchronize()
+    assert canary_intact(buf, M * N)
+    return Y.cpu().numpy()
+
+
+@pytest.mark.parametrize("K", [256, 768, 528])
+@pytest.mark.parametrize("N", [1, 33, 130])
+@pytest.mark.parametrize("M", [1, 4, 16])
+@pytest.mark.parametrize("dw", [0.37, 2.0e38])
+def test_nvfp4_div_shapes(oracle, K, N, M, dw):
+    """NVFP4 with the global field as a divisor d_w ("tensor-formats.md" section 3.3). d_w = 2e38:
+    1 / d_w is not a normal fp32 number, so every path divides each output by d_w (x is scaled
+    by 2^100 to keep the products away from the bound's absolute term)."""
+    seed = hash((K, N, M, dw)) % 1000
+    codes, scales, _ = synth.nvfp4_random(N, K, seed=seed)
+    codes, scales = codes.numpy(), scales.numpy()
+    Xb = synth.activations_bf16(M, K, seed=seed)
+    if dw > 1e30:
+        Xb = (Xb.astype(np.uint32) + (100 << 7)).astype(np.uint16)  # x * 2^100 (exponent field + 100)
+    Yr, Ar = oracle.gemv_nvfp4_div(codes, scales, dw, N, K, Xb)
+    for offset in (0, 1):  # 1: unaligned codes/scales -> generic path
+        Y = run_nv_div(codes, scales, dw, N, K, Xb, offset)
+        assert_within_tolerance(Y, Yr, Ar, f"nvfp4/dw K={K} N={N} M={M} dw={dw} off={offset}")
+
+
+@pytest.mark.parametrize("N,K", [(17408, 5120), (5120, 17408)])
+@pytest.mark.parametrize("M", [1, 4])
+def test_nvfp4_div_workload_sampled(oracle, N, K, M):
+    codes, scales, _ = synth.nvfp4_random(N, K, seed=79, device="cuda")
+    dw = 0.0123
+    Xb = synth.activations_bf16(M, K, seed=80)
+    Y = pnq.gemv(pnq.NVFP4_DIV, (codes, scales, dw), torch.from_numpy(Xb.view(np.int16)).cuda(), N, K).cpu().numpy()
+    rows = sampled_rows(N)
+    cr, sr, _ = synth.nvfp4_random(N, K, seed=79, rows=torch.from_numpy(rows))
+    Yr, Ar = oracle.gemv_nvfp4_div(cr.numpy(), sr.numpy(), dw, len(rows), K, Xb)
+    assert_within_tolerance(Y[:, rows], Yr, Ar, f"nvfp4/dw {N}x{K} M={M}")
+
+
 @pytest.mark.parametrize("type_", [pnq.PN3T, pnq.PN4T])
 @pytest.mark.parametrize("offset", [0, 2])
 def test_one_hot_x_gives_exact_column(oracle, type_, offset):
