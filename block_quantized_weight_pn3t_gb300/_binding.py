@@ -10,8 +10,19 @@ import enum
 import os
 
 PN3T, PN4T, NVFP4, NVFP4_DIV = 124, 125, 1004, 1005
+Q4G64_F16S, Q5G64_F16S, Q6G64_F16S, W8G32_F16S = 1104, 1105, 1106, 1108
 NVFP4_TYPES = (NVFP4, NVFP4_DIV)
 BLOCK_WEIGHTS = {PN3T: 80, PN4T: 64}
+# grouped signed-integer formats: (code bits, group size)
+GROUPED = {Q4G64_F16S: (4, 64), Q5G64_F16S: (5, 64), Q6G64_F16S: (6, 64), W8G32_F16S: (8, 32)}
+
+
+def grouped_plane_shapes(type_: int, n_rows: int, K: int):
+    """Shapes of the (lo, hi, scales) planes of an [n_rows][K] grouped matrix (hi None for Q4, W8)."""
+    bits, G = GROUPED[type_]
+    lo = (n_rows, K if bits == 8 else K // 2)
+    hi = {5: (n_rows, K // 8), 6: (n_rows, K // 4)}.get(bits)
+    return lo, hi, (n_rows, (K + G - 1) // G)
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "libpnq.so")
@@ -27,6 +38,7 @@ class Status(enum.IntEnum):
     ERR_DEVICE = -6
     ERR_FLAGS = -7
     ERR_SCRATCH = -8
+    ERR_VALUE = -9
 
 
 GEMV_STATIC_WEIGHTS = 1
@@ -40,6 +52,10 @@ class PnqError(RuntimeError):
 
 class pnq_nvfp4_weights(ctypes.Structure):
     _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p), ("global_scale", ctypes.c_float)]
+
+
+class pnq_grouped_weights(ctypes.Structure):
+    _fields_ = [("lo", ctypes.c_void_p), ("hi", ctypes.c_void_p), ("scales", ctypes.c_void_p)]
 
 
 _lib = None
@@ -70,6 +86,10 @@ def lib() -> ctypes.CDLL:
         L.pnq_dequantize_row.argtypes = [I, P, I64, I64, P, P]
         L.pnq_validate_row.restype = I
         L.pnq_validate_row.argtypes = [I, P, I64, I64, P, P]
+        L.pnq_quantize_row.restype = I
+        L.pnq_quantize_row.argtypes = [I, P, I64, I64, P, P, P]
+        L.pnq_quantize_nvfp4_clip.restype = I
+        L.pnq_quantize_nvfp4_clip.argtypes = [P, P, I64, I64, ctypes.c_float, P, P, P, P]
         L.pnq_device_error.restype = I
         L.pnq_device_error.argtypes = [ctypes.POINTER(ctypes.c_int32)]
         L.pnq_version.restype = ctypes.c_char_p
@@ -92,6 +112,10 @@ def _w_arg(type_: int, W):
     if type_ in NVFP4_TYPES:
         if not isinstance(W, pnq_nvfp4_weights):
             raise TypeError("NVFP4 weights must be a pnq_nvfp4_weights descriptor")
+        return ctypes.byref(W)
+    if type_ in GROUPED:
+        if not isinstance(W, pnq_grouped_weights):
+            raise TypeError("grouped weights must be a pnq_grouped_weights descriptor")
         return ctypes.byref(W)
     return ctypes.c_void_p(W)
 
@@ -120,6 +144,13 @@ def dequantize_row_ptr(type_: int, W, n_rows: int, K: int, out: int, stream: int
 
 def validate_row_ptr(type_: int, W, n_rows: int, K: int, flags: int, stream: int = 0) -> int:
     return lib().pnq_validate_row(type_, _w_arg(type_, W), n_rows, K, ctypes.c_void_p(flags),
+                                  ctypes.c_void_p(stream))
+
+
+def quantize_row_ptr(type_: int, w: int, n_rows: int, K: int, out, status: int, stream: int = 0) -> int:
+    """out: a device address (PN) or a pnq_grouped_weights holding the output planes (grouped)."""
+    o = ctypes.byref(out) if type_ in GROUPED else ctypes.c_void_p(out)
+    return lib().pnq_quantize_row(type_, ctypes.c_void_p(w), n_rows, K, o, ctypes.c_void_p(status),
                                   ctypes.c_void_p(stream))
 
 
@@ -166,13 +197,21 @@ def _check_weights(type_: int, W, n_rows: int, K: int) -> None:
     elif type_ in BLOCK_WEIGHTS:
         blk = BLOCK_WEIGHTS[type_]
         _require(W, "W", (torch.uint8,), n_rows * (K // blk) * 34 if K > 0 and K % blk == 0 else None)
+    elif type_ in GROUPED:
+        lo, hi, sc = W
+        shapes = grouped_plane_shapes(type_, n_rows, K) if K > 0 and K % 8 == 0 else (None, None, None)
+        _require(lo, "grouped lo plane", (torch.uint8, torch.int8), None if shapes[0] is None else shapes[0][0] * shapes[0][1])
+        if shapes[1] is not None:
+            _require(hi, "grouped hi plane", (torch.uint8,), shapes[1][0] * shapes[1][1])
+        _require(sc, "grouped scales", (torch.uint16, torch.int16, torch.float16),
+                 None if shapes[2] is None else shapes[2][0] * shapes[2][1])
     # an unknown type is left to the library (PNQ_ERR_TYPE)
 
 
 def _check_x(type_: int, X, K: int) -> int:
     """The activation rows M of X ([M][K], or [K] for M = 1), after checking X."""
     import torch
-    dtypes = (torch.bfloat16, torch.int16) if type_ in NVFP4_TYPES else (torch.float32,)
+    dtypes = (torch.bfloat16, torch.int16) if type_ in NVFP4_TYPES else (torch.float32,)  # PN, grouped: fp32
     M = X.shape[0] if X.dim() == 2 else 1
     _require(X, "X", dtypes)
     if X.numel() != M * K:
@@ -184,6 +223,9 @@ def _weights(type_: int, W):
     if type_ in NVFP4_TYPES:
         codes, scales, g = W
         return nvfp4_weights(codes.data_ptr(), scales.data_ptr(), g)
+    if type_ in GROUPED:
+        lo, hi, sc = W
+        return pnq_grouped_weights(lo.data_ptr(), 0 if hi is None else hi.data_ptr(), sc.data_ptr())
     return W.data_ptr()
 
 
@@ -219,7 +261,7 @@ def dequantize_row(type_: int, W, n_rows: int, K: int, out=None, stream=None):
     import torch
     _check_weights(type_, W, n_rows, K)
     if out is None:
-        dev = W[0].device if type_ in NVFP4_TYPES else W.device
+        dev = W[0].device if isinstance(W, tuple) else W.device
         out = torch.empty((n_rows, K), dtype=torch.float32, device=dev)
     _require(out, "out", (torch.float32,), n_rows * K)
     _check(dequantize_row_ptr(type_, _weights(type_, W), n_rows, K, out.data_ptr(), _stream_handle(stream)),
@@ -231,9 +273,59 @@ def validate_row(type_: int, W, n_rows: int, K: int, flags=None, stream=None):
     import torch
     _check_weights(type_, W, n_rows, K)
     if flags is None:
-        dev = W[0].device if type_ in NVFP4_TYPES else W.device
+        dev = W[0].device if isinstance(W, tuple) else W.device
         flags = torch.empty((n_rows,), dtype=torch.int32, device=dev)
     _require(flags, "flags", (torch.int32,), n_rows)
     _check(validate_row_ptr(type_, _weights(type_, W), n_rows, K, flags.data_ptr(), _stream_handle(stream)),
            "pnq_validate_row")
     return flags
+
+
+def quantize_row(type_: int, w, out=None, status=None, stream=None):
+    """Encode a CUDA fp32 [n_rows][K] matrix on the GPU: the PN reference quantizer (returns the
+    uint8 blocks) or the grouped canonical encoder (returns (lo, hi or None, scales)); also
+    returns the per-row status (int32, 1 = row rejected)."""
+    import torch
+    _require(w, "w", (torch.float32,))
+    if w.dim() != 2:
+        raise PnqError(f"w has shape {tuple(w.shape)}; expected [n_rows][K]")
+    n_rows, K = w.shape
+    if status is None:
+        status = torch.empty((n_rows,), dtype=torch.int32, device=w.device)
+    _require(status, "status", (torch.int32,), n_rows)
+    if type_ in GROUPED:
+        if out is None:
+            slo, shi, ssc = grouped_plane_shapes(type_, n_rows, K)
+            out = (torch.empty(slo, dtype=torch.uint8, device=w.device),
+                   None if shi is None else torch.empty(shi, dtype=torch.uint8, device=w.device),
+                   torch.empty(ssc, dtype=torch.int16, device=w.device))
+        desc = pnq_grouped_weights(out[0].data_ptr(), 0 if out[1] is None else out[1].data_ptr(), out[2].data_ptr())
+        _check(quantize_row_ptr(type_, w.data_ptr(), n_rows, K, desc, status.data_ptr(), _stream_handle(stream)),
+               "pnq_quantize_row")
+        return out, status
+    if out is None:
+        blk = BLOCK_WEIGHTS.get(type_, 1)
+        out = torch.empty((n_rows * (K // blk) * 34,), dtype=torch.uint8, device=w.device)
+    _require(out, "out", (torch.uint8,))
+    _check(quantize_row_ptr(type_, w.data_ptr(), n_rows, K, out.data_ptr(), status.data_ptr(), _stream_handle(stream)),
+           "pnq_quantize_row")
+    return out, status
+
+
+def quantize_nvfp4_clip(w, act_ms, global_scale: float, stream=None):
+    """NVFP4 clip search on the GPU: w CUDA fp32 [n_rows][K], act_ms CUDA fp32 [K]. Returns
+    (codes uint8 [n_rows][K/2], scales uint8 [n_rows][K/16], row status int32 [n_rows])."""
+    import torch
+    _require(w, "w", (torch.float32,))
+    if w.dim() != 2:
+        raise PnqError(f"w has shape {tuple(w.shape)}; expected [n_rows][K]")
+    n_rows, K = w.shape
+    _require(act_ms, "act_ms", (torch.float32,), K)
+    codes = torch.empty((n_rows, K // 2), dtype=torch.uint8, device=w.device)
+    scales = torch.empty((n_rows, max(K // 16, 0)), dtype=torch.uint8, device=w.device)
+    status = torch.empty((n_rows,), dtype=torch.int32, device=w.device)
+    _check(lib().pnq_quantize_nvfp4_clip(ctypes.c_void_p(w.data_ptr()), ctypes.c_void_p(act_ms.data_ptr()), n_rows, K,
+                                         float(global_scale), ctypes.c_void_p(codes.data_ptr()),
+                                         ctypes.c_void_p(scales.data_ptr()), ctypes.c_void_p(status.data_ptr()),
+                                         ctypes.c_void_p(_stream_handle(stream))), "pnq_quantize_nvfp4_clip")
+    return codes, scales, status

@@ -71,6 +71,34 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 int map_cuda(cudaError_t e) { return e == cudaSuccess ? PNQ_OK : PNQ_ERR_CUDA; }
 
+bool is_grouped(int type) {
+    return type == PNQ_Q4G64_F16S || type == PNQ_Q5G64_F16S || type == PNQ_Q6G64_F16S || type == PNQ_W8G32_F16S;
+}
+
+int grouped_bits(int type) {
+    return type == PNQ_Q4G64_F16S ? 4 : type == PNQ_Q5G64_F16S ? 5 : type == PNQ_Q6G64_F16S ? 6 : 8;
+}
+
+// Grouped planes: K % 8 == 0 (whole octets per row), the planes present and aligned for the
+// kernels' loads (row strides keep the base alignment because K % 8 == 0).
+int check_grouped_planes(int type, int64_t rows, const uint8_t* lo, const uint8_t* hi, const uint16_t* scales) {
+    const int bits = grouped_bits(type);
+    if (rows > 0 && (!lo || !scales || ((bits == 5 || bits == 6) && !hi))) return PNQ_ERR_NULL;
+    if (!aligned(lo, bits == 8 ? 8 : 4) || !aligned(scales, 2) || (bits == 6 && !aligned(hi, 2)))
+        return PNQ_ERR_ALIGN;
+    return PNQ_OK;
+}
+
+int check_grouped(int type, const void* W, int64_t rows, int64_t K, GroupedView* v) {
+    if (rows < 0 || K <= 0 || K % 8 != 0 || rows > INT64_MAX / K) return PNQ_ERR_SHAPE;
+    if (!W) return PNQ_ERR_NULL;
+    const pnq_grouped_weights* d = static_cast<const pnq_grouped_weights*>(W);
+    v->lo = d->lo;
+    v->hi = d->hi;
+    v->scales = d->scales;
+    return check_grouped_planes(type, rows, d->lo, d->hi, d->scales);
+}
+
 // Shared shape / pointer checks. On success fills the NVFP4 view (when type is NVFP4).
 int check_common(int type, const void* W, int64_t rows, int64_t K, Nvfp4View* nv) {
     if (type != PNQ_PN3T && type != PNQ_PN4T && type != PNQ_NVFP4 && type != PNQ_NVFP4_DIV) return PNQ_ERR_TYPE;
@@ -151,6 +179,17 @@ namespace {
 
 int gemv_impl(int type, const void* W, int64_t N, int64_t K, const void* X, int M, float* Y, unsigned int flags,
               cudaStream_t stream) {
+    if (is_grouped(type)) {
+        GroupedView v{};
+        const int rc = check_grouped(type, W, N, K, &v);
+        if (rc != PNQ_OK) return rc;
+        if (M < 1 || M > 16 || static_cast<int64_t>(M) > INT64_MAX / K) return PNQ_ERR_SHAPE;
+        if ((flags & ~static_cast<unsigned int>(PNQ_GEMV_STATIC_WEIGHTS)) != 0) return PNQ_ERR_FLAGS;
+        if (N == 0) return PNQ_OK;
+        if (!X || !Y) return PNQ_ERR_NULL;
+        if (!aligned(X, 16) || !aligned(Y, 4)) return PNQ_ERR_ALIGN;
+        return map_cuda(launch_grouped_gemv(type, v, N, K, static_cast<const float*>(X), M, Y, stream));
+    }
     Nvfp4View nv{};
     int rc = check_common(type, W, N, K, &nv);
     if (rc != PNQ_OK) return rc;
@@ -210,6 +249,15 @@ extern "C" int pnq_gemv(int type, const void* W, int64_t N, int64_t K, const voi
 
 extern "C" int pnq_dequantize_row(int type, const void* W, int64_t n_rows, int64_t K, float* out,
                                   cudaStream_t stream) {
+    if (is_grouped(type)) {
+        GroupedView v{};
+        const int rc = check_grouped(type, W, n_rows, K, &v);
+        if (rc != PNQ_OK) return rc;
+        if (n_rows == 0) return PNQ_OK;
+        if (!out) return PNQ_ERR_NULL;
+        if (!aligned(out, 16)) return PNQ_ERR_ALIGN;
+        return map_cuda(launch_grouped_dequant(type, v, n_rows, K, out, stream));
+    }
     Nvfp4View nv{};
     int rc = check_common(type, W, n_rows, K, &nv);
     if (rc != PNQ_OK) return rc;
@@ -222,6 +270,15 @@ extern "C" int pnq_dequantize_row(int type, const void* W, int64_t n_rows, int64
 
 extern "C" int pnq_validate_row(int type, const void* W, int64_t n_rows, int64_t K, int32_t* flags,
                                 cudaStream_t stream) {
+    if (is_grouped(type)) {
+        GroupedView v{};
+        const int rc = check_grouped(type, W, n_rows, K, &v);
+        if (rc != PNQ_OK) return rc;
+        if (n_rows == 0) return PNQ_OK;
+        if (!flags) return PNQ_ERR_NULL;
+        if (!aligned(flags, 4)) return PNQ_ERR_ALIGN;
+        return map_cuda(launch_grouped_validate(type, v, n_rows, K, flags, stream));
+    }
     Nvfp4View nv{};
     int rc = check_common(type, W, n_rows, K, &nv);
     if (rc != PNQ_OK) return rc;
@@ -230,6 +287,41 @@ extern "C" int pnq_validate_row(int type, const void* W, int64_t n_rows, int64_t
     if (!aligned(flags, 4)) return PNQ_ERR_ALIGN;
     if (type == PNQ_NVFP4 || type == PNQ_NVFP4_DIV) return map_cuda(launch_nvfp4_validate(nv, n_rows, K, flags, stream));
     return map_cuda(launch_pn_validate(type, static_cast<const uint8_t*>(W), n_rows, K, flags, stream));
+}
+
+extern "C" int pnq_quantize_row(int type, const float* w, int64_t n_rows, int64_t K, void* out, int32_t* row_status,
+                                cudaStream_t stream) {
+    if (type != PNQ_PN3T && type != PNQ_PN4T && !is_grouped(type)) return PNQ_ERR_TYPE;
+    if (n_rows < 0 || K <= 0 || n_rows > INT64_MAX / K) return PNQ_ERR_SHAPE;
+    if (is_grouped(type)) {
+        if (K % 8 != 0) return PNQ_ERR_SHAPE;
+        if (!out) return PNQ_ERR_NULL;
+        const pnq_grouped_planes* p = static_cast<const pnq_grouped_planes*>(out);
+        int rc = check_grouped_planes(type, n_rows, p->lo, p->hi, p->scales);
+        if (rc != PNQ_OK) return rc;
+        if (n_rows == 0) return PNQ_OK;
+        if (!w || !row_status) return PNQ_ERR_NULL;
+        if (!aligned(w, 4) || !aligned(row_status, 4)) return PNQ_ERR_ALIGN;
+        return map_cuda(launch_grouped_quantize(type, w, n_rows, K, GroupedOut{p->lo, p->hi, p->scales}, row_status,
+                                                stream));
+    }
+    const int blk = block_weights(type);
+    if (K % blk != 0 || n_rows > INT64_MAX / (K / blk * 34)) return PNQ_ERR_SHAPE;
+    if (n_rows == 0) return PNQ_OK;
+    if (!w || !out || !row_status) return PNQ_ERR_NULL;
+    if (!aligned(w, 4) || !aligned(out, 2) || !aligned(row_status, 4)) return PNQ_ERR_ALIGN;
+    return map_cuda(launch_pn_quantize(type, w, n_rows, K, static_cast<uint8_t*>(out), row_status, stream));
+}
+
+extern "C" int pnq_quantize_nvfp4_clip(const float* w, const float* act_ms, int64_t n_rows, int64_t K,
+                                       float global_scale, uint8_t* codes, uint8_t* scales, int32_t* row_status,
+                                       cudaStream_t stream) {
+    if (n_rows < 0 || K <= 0 || K % 16 != 0 || n_rows > INT64_MAX / K) return PNQ_ERR_SHAPE;
+    if (!(global_scale > 0.0f && global_scale <= 3.4028234663852886e38f)) return PNQ_ERR_VALUE;
+    if (n_rows == 0) return PNQ_OK;
+    if (!w || !act_ms || !codes || !scales || !row_status) return PNQ_ERR_NULL;
+    if (!aligned(w, 4) || !aligned(act_ms, 4) || !aligned(row_status, 4)) return PNQ_ERR_ALIGN;
+    return map_cuda(launch_nvfp4_clip(w, act_ms, global_scale, n_rows, K, codes, scales, row_status, stream));
 }
 
 extern "C" int pnq_device_error(int32_t* code) {

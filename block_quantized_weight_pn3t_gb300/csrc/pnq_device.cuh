@@ -17,6 +17,11 @@ constexpr int kBlockBytes = 34;
 constexpr int kTypePn3t = 124;
 constexpr int kTypePn4t = 125;
 constexpr int kTypeNvfp4 = 1004;
+// grouped signed-integer formats of NInfer "tensor-formats.md" (library ids)
+constexpr int kTypeQ4G64 = 1104;
+constexpr int kTypeQ5G64 = 1105;
+constexpr int kTypeQ6G64 = 1106;
+constexpr int kTypeW8G32 = 1108;
 
 template <int TYPE> struct PnFmt;
 template <> struct PnFmt<kTypePn3t> {

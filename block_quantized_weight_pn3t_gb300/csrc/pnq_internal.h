@@ -14,6 +14,18 @@ struct Nvfp4View {
     bool div = false;       // the weight is e2m1 * e4m3 / g
 };
 
+// Planes of a grouped signed-integer matrix (pnq_grouped.cu states the layout).
+struct GroupedView {
+    const uint8_t* lo;
+    const uint8_t* hi;
+    const uint16_t* scales;
+};
+struct GroupedOut {
+    uint8_t* lo;
+    uint8_t* hi;
+    uint16_t* scales;
+};
+
 int device_sm_count();
 
 // 2-D tensor map over a row-major u32 matrix [rows][row_u32] (row pitch a multiple of 16
@@ -32,6 +44,28 @@ cudaError_t launch_pn_validate(int type, const uint8_t* W, int64_t n_rows, int64
                                cudaStream_t stream);
 cudaError_t launch_nvfp4_validate(const Nvfp4View& w, int64_t n_rows, int64_t K, int32_t* flags,
                                   cudaStream_t stream);
+
+// Grouped signed-integer formats (type = kTypeQ4G64 ..): bit-exact dequantize, validate, GEMV on
+// the CUDA cores (X fp32), and the canonical encoder MAXABS_F16_RECIP_RNE_V1 (status[r] = 1 for
+// a row with a non-finite weight or a scale that overflows binary16; zeroed first).
+cudaError_t launch_grouped_dequant(int type, const GroupedView& v, int64_t n_rows, int64_t K, float* out,
+                                   cudaStream_t stream);
+cudaError_t launch_grouped_validate(int type, const GroupedView& v, int64_t n_rows, int64_t K, int32_t* flags,
+                                    cudaStream_t stream);
+cudaError_t launch_grouped_gemv(int type, const GroupedView& v, int64_t N, int64_t K, const float* X, int M,
+                                float* Y, cudaStream_t stream);
+cudaError_t launch_grouped_quantize(int type, const float* w, int64_t n_rows, int64_t K, const GroupedOut& out,
+                                    int32_t* status, cudaStream_t stream);
+
+// PN reference quantizer, bit-exact with the CPU reference (status[r] = 1 for a row with a
+// non-finite weight; zeroed first).
+cudaError_t launch_pn_quantize(int type, const float* w, int64_t n_rows, int64_t K, uint8_t* out, int32_t* status,
+                               cudaStream_t stream);
+
+// NVFP4 clip search (TandemLLM "Quantisation and profiles"), bit-exact with the CPU reference;
+// status[r] = 1 for a row with a non-finite weight (zeroed first).
+cudaError_t launch_nvfp4_clip(const float* w, const float* act_ms, float g, int64_t n_rows, int64_t K, uint8_t* codes,
+                              uint8_t* scales, int32_t* status, cudaStream_t stream);
 
 // Generic path: any 2-byte aligned PN buffer / any NVFP4 layout, CUDA-core FMA.
 cudaError_t launch_pn_gemv_simt(int type, const uint8_t* W, int64_t N, int64_t K, const float* X, int M,

@@ -34,6 +34,19 @@
  *   PNQ_NVFP4_DIV (1005, a library id): the same codes and scales with the global field read
  *     as a divisor d_w ("tensor-formats.md" section 3.3): w = e2m1 * e4m3fn / d_w. The
  *     pnq_nvfp4_weights descriptor carries d_w in global_scale.
+ *   PNQ_Q4G64_F16S, PNQ_Q5G64_F16S, PNQ_Q6G64_F16S, PNQ_W8G32_F16S (1104, 1105, 1106, 1108,
+ *     library ids): the grouped signed-integer formats of NInfer "tensor-formats.md" (sections 4
+ *     to 7). One two's-complement code per weight (4, 5, 6 or 8 bits; W8 in -127..127) and one
+ *     binary16 scale per group of 64 (32 for W8) along K, the last group of a row possibly
+ *     partial; w = binary32(scale * code). K % 8 == 0. Planes (a layout of this library; the
+ *     pages leave layouts to a registry), passed in a pnq_grouped_weights descriptor:
+ *       lo      [N][K/2] bytes: low 4 bits of each code's word, even k in the low nibble
+ *               (W8: [N][K], the code's byte);
+ *       hi      Q5: [N][K/8], bit 4 of weight k at bit k % 8 of byte k / 8;
+ *               Q6: [N][K/4], bits 4..5 of weight k at bits 2 (k % 4) .. of byte k / 4;
+ *               Q4, W8: unused (may be NULL);
+ *       scales  [N][ceil(K / G)] binary16 words.
+ *     Alignment: lo 8 bytes (W8) or 4 bytes, hi 2 bytes, scales 2 bytes (else PNQ_ERR_ALIGN).
  *
  * Fast paths (taken automatically, never required)
  *   PN: W and X 16-byte aligned and (K/BLK) % 8 == 0.  NVFP4: codes, scales and X 16-byte
@@ -51,7 +64,16 @@
 extern "C" {
 #endif
 
-enum pnq_type { PNQ_PN3T = 124, PNQ_PN4T = 125, PNQ_NVFP4 = 1004, PNQ_NVFP4_DIV = 1005 };
+enum pnq_type {
+    PNQ_PN3T = 124,
+    PNQ_PN4T = 125,
+    PNQ_NVFP4 = 1004,
+    PNQ_NVFP4_DIV = 1005,
+    PNQ_Q4G64_F16S = 1104,
+    PNQ_Q5G64_F16S = 1105,
+    PNQ_Q6G64_F16S = 1106,
+    PNQ_W8G32_F16S = 1108
+};
 
 enum pnq_status {
     PNQ_OK = 0,
@@ -63,7 +85,9 @@ enum pnq_status {
     PNQ_ERR_CUDA = -5,   /* a CUDA call failed (launch error, no device, bad stream) */
     PNQ_ERR_DEVICE = -6, /* a kernel gave up on an internal wait (see pnq_device_error) */
     PNQ_ERR_FLAGS = -7,  /* unknown bit in a flags argument */
-    PNQ_ERR_SCRATCH = -8 /* reserved (no entry point of this version returns it) */
+    PNQ_ERR_SCRATCH = -8, /* reserved (no entry point of this version returns it) */
+    PNQ_ERR_VALUE = -9    /* an argument value outside its domain (a global scale that is not finite
+                             and > 0) */
 };
 
 /* Flags of pnq_gemv_ex. */
@@ -83,14 +107,31 @@ typedef struct pnq_nvfp4_weights {
                                divisor d_w of every weight (PNQ_NVFP4_DIV) */
 } pnq_nvfp4_weights;
 
+/* Grouped signed-integer weight descriptor, passed by HOST pointer as the W argument for the
+ * PNQ_Q*G64_F16S / PNQ_W8G32_F16S types; the planes are device pointers. */
+typedef struct pnq_grouped_weights {
+    const uint8_t* lo;       /* device, low-4-bit plane (W8: the code bytes) */
+    const uint8_t* hi;       /* device, high-bit plane (Q5, Q6), else unused */
+    const uint16_t* scales;  /* device, binary16 scale per group */
+} pnq_grouped_weights;
+
+/* The same planes as outputs of pnq_quantize_row. */
+typedef struct pnq_grouped_planes {
+    uint8_t* lo;
+    uint8_t* hi;
+    uint16_t* scales;
+} pnq_grouped_planes;
+
 /*
  * pnq_gemv -- Y[m][n] = sum_k W[n][k] * X[m][k] for m < M, n < N, fp32 accumulation.
  * The decode-step product of the pages ("PN weight format", section "Where PN runs":
  * PN tensors use their own GEMV kernels; TandemLLM "Quantisation and profiles",
  * section NVFP4: the W4A16 kernel unpacks codes in registers before the multiply).
- *   type  PNQ_PN3T, PNQ_PN4T, PNQ_NVFP4 or PNQ_NVFP4_DIV.
+ *   type  PNQ_PN3T, PNQ_PN4T, PNQ_NVFP4, PNQ_NVFP4_DIV or a grouped signed-integer type.
  *   W     PN: device pointer to N*(K/BLK)*34 bytes, >= 2-byte aligned (else PNQ_ERR_ALIGN).
  *         NVFP4, NVFP4_DIV: host pointer to a pnq_nvfp4_weights.
+ *         Grouped: host pointer to a pnq_grouped_weights (the GEMV runs on the CUDA cores; X
+ *         fp32, 16-byte aligned).
  *   N     output rows (>= 0; N == 0 launches nothing).  K: inner dimension.
  *   X     device, [M][K] row-major: fp32 for PN (4-byte aligned), bf16 for NVFP4
  *         (2-byte aligned). Finite values; any magnitude is accepted.
@@ -142,6 +183,9 @@ int pnq_dequantize_row(int type, const void* W, int64_t n_rows, int64_t K, float
 
 /*
  * pnq_validate_row -- flags[r] = 1 if row r is invalid, else 0.
+ *   Grouped ("tensor-formats.md" section 6): a scale with its sign bit set or an all-ones
+ *   exponent (negative, -0, infinity, NaN), a +0 scale over a nonzero code, or (W8) the word
+ *   0x80.
  *   PN ("PN weight format", section Validation): any block's d is an fp16 NaN or infinity,
  *   or (pn3t) bit 15 or bit 31 of any word is set.
  *   NVFP4 and NVFP4_DIV ("tensor-formats.md" section 3.3): any scale byte has its sign bit
@@ -151,6 +195,44 @@ int pnq_dequantize_row(int type, const void* W, int64_t n_rows, int64_t K, float
  */
 int pnq_validate_row(int type, const void* W, int64_t n_rows, int64_t K, int32_t* flags,
                      cudaStream_t stream);
+
+/*
+ * pnq_quantize_row -- encode n_rows rows of K fp32 weights (device w, [n_rows][K], 4-byte
+ * aligned) on the GPU; row_status (device int32 [n_rows], 4-byte aligned) is set to 0 for each
+ * row encoded and 1 for a row the encoder rejects (its output bytes are then unspecified).
+ *   PN3T / PN4T: the reference quantizer of "PN weight format" (section Reference quantizer),
+ *     bit for bit the CPU reference's d and codes: per block, 36 multipliers 0.50 .. 1.20 of
+ *     amax / z with the sign that favours the larger tail, each scale rounded to fp16, codes
+ *     rint(w / s) + z clamped, the least squared error kept (a tie to the larger multiplier),
+ *     all in IEEE double in that order. out: device pointer to n_rows*(K/BLK)*34 bytes, 2-byte
+ *     aligned. A row with a non-finite weight is rejected.
+ *   Grouped: the canonical encoder MAXABS_F16_RECIP_RNE_V1 ("tensor-formats.md" section 7):
+ *     per group amax, scale16 = binary16(amax / qmax) (+0 becomes 0x0001), inv = 1 / scale,
+ *     code = clamp(rint(w * inv)), each step one binary32 (binary16) rounding to nearest even;
+ *     an all-zero group gets scale +0. out: host pointer to a pnq_grouped_planes. A row with a
+ *     non-finite weight or a scale that overflows binary16 is rejected.
+ *   Errors: PNQ_ERR_TYPE (NVFP4 types have no encoder here), PNQ_ERR_SHAPE, PNQ_ERR_NULL,
+ *   PNQ_ERR_ALIGN, PNQ_ERR_CUDA. (Library call; the pages define the algorithms, not the call.)
+ */
+int pnq_quantize_row(int type, const float* w, int64_t n_rows, int64_t K, void* out, int32_t* row_status,
+                     cudaStream_t stream);
+
+/*
+ * pnq_quantize_nvfp4_clip -- encode n_rows rows of K fp32 weights (device w, [n_rows][K]) as NVFP4
+ * (codes [n_rows][K/2], scales [n_rows][K/16], device) for the global multiplier global_scale
+ * with the clip search of TandemLLM "Quantisation and profiles" (section "The clip search"): per
+ * group of 16, the scale multiplier among 1.00, 0.95, 0.90, 0.85, 0.80 of amax / (6 g) whose
+ * act_ms-weighted squared error is smallest; act_ms (device fp32 [K]) is the mean square of each
+ * input channel over calibration data. Bit for bit the CPU reference's choice. Readings where the
+ * page is silent: scales round to the nearest E4M3FN value (ties to the even word, saturating at
+ * 448), weights to the nearest E2M1 magnitude (ties to the even word, saturating at 6) with the
+ * sign of w, the error is summed in k order in double, a tie keeps the earlier multiplier.
+ * row_status (device int32 [n_rows]): 0, or 1 for a row with a non-finite weight (its bytes are
+ * then unspecified). w, act_ms and row_status 4-byte aligned. Errors: PNQ_ERR_SHAPE (K % 16),
+ * PNQ_ERR_VALUE (global_scale not finite and > 0), PNQ_ERR_NULL, PNQ_ERR_ALIGN, PNQ_ERR_CUDA.
+ */
+int pnq_quantize_nvfp4_clip(const float* w, const float* act_ms, int64_t n_rows, int64_t K, float global_scale,
+                            uint8_t* codes, uint8_t* scales, int32_t* row_status, cudaStream_t stream);
 
 /*
  * pnq_device_error -- reads and clears the library's device error word on the current

@@ -70,6 +70,7 @@ def lib() -> ctypes.CDLL:
             "pnq_ref_validate_grouped": (I32, [I32, P, P, P, I64, I64, P]),
             "pnq_ref_quantize_grouped": (I32, [I32, P, I64, I64, P, P, P, P]),
             "pnq_ref_gemv_grouped": (I32, [I32, P, P, P, I64, I64, P, I32, P, P]),
+            "pnq_ref_quantize_nvfp4_clip": (I32, [P, P, F, I64, I64, P, P, P]),
             "pnq_ref_gemv_nvfp4_div": (I32, [P, P, F, I64, I64, P, I32, P, P]),
         }
         for name, (res, args) in sig.items():
@@ -288,3 +289,17 @@ def gemv_grouped(type_: int, lo, hi, sc, N: int, K: int, X: np.ndarray):
     _check(lib().pnq_ref_gemv_grouped(type_, _ptr(lo), None if hi is None else _ptr(hi), _ptr(sc), N, K, _ptr(X), M,
                                       _ptr(Y), _ptr(A)), "gemv_grouped")
     return Y, A
+
+
+def quantize_nvfp4_clip(w: np.ndarray, act_ms: np.ndarray, g: float):
+    """NVFP4 clip search on a [N][K] fp32 matrix with per-channel act_ms [K]; returns
+    (codes [N][K/2], scales [N][K/16], chosen multiplier index [N][K/16])."""
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    act_ms = np.ascontiguousarray(act_ms, dtype=np.float32)
+    N, K = w.shape
+    codes = np.empty((N, K // 2), dtype=np.uint8)
+    scales = np.empty((N, K // 16), dtype=np.uint8)
+    chosen = np.empty((N, K // 16), dtype=np.int32)
+    _check(lib().pnq_ref_quantize_nvfp4_clip(_ptr(w), _ptr(act_ms), g, N, K, _ptr(codes), _ptr(scales), _ptr(chosen)),
+           "quantize_nvfp4_clip")
+    return codes, scales, chosen

@@ -615,3 +615,88 @@ int pnq_ref_gemv_grouped(int type, const uint8_t* lo, const uint8_t* hi, const u
     free(xd);
     return PNQ_REF_OK;
 }
+
+/* ---- NVFP4 clip search (TandemLLM "Quantisation and profiles", section "The clip search") ------
+ * Per group of 16 weights of a row, five scale multipliers 1.00, 0.95, 0.90, 0.85, 0.80 are
+ * tried and the one with the smallest error  sum_k act_ms[k] (w[k] - dequant(quant(w[k])))^2
+ * is kept. Readings where the page is silent (the page's tool is not printed): the weight is
+ * e2m1 * e4m3 * g with a given global multiplier g (the TandemLLM reading); the multiplier
+ * scales the group's base scale amax / (6 g) (6: the largest e2m1 magnitude), computed in
+ * double as ((mu * amax) / 6) / g; the scale is the nearest E4M3FN value, ties to the even code
+ * word, saturating at 448; each weight takes the nearest E2M1 magnitude of |w| / (scale * g),
+ * ties to the even code word, saturating at 6, with the sign of w (a negative weight that rounds
+ * to zero keeps the negative-zero word); a zero scale gives every weight the zero word of its
+ * sign; the error is summed in k order in double; a tie in error keeps the earlier multiplier.
+ * Every step is one IEEE double operation in that order. */
+
+static const double kClipMultipliers[5] = {1.00, 0.95, 0.90, 0.85, 0.80};
+
+/* Nearest positive E4M3FN code word to t >= 0 (0x00 .. 0x7E), ties to the even word. */
+static uint8_t e4m3_nearest(double t) {
+    uint8_t best = 0;
+    double bd = INFINITY;
+    for (int c = 0; c <= 0x7E; ++c) {
+        double d = fabs(pnq_ref_e4m3fn_to_double((uint8_t)c) - t);
+        if (d < bd || (d == bd && (c & 1) == 0)) { bd = d; best = (uint8_t)c; }
+    }
+    return best;
+}
+
+/* Nearest E2M1 magnitude word (0..7) to a >= 0, ties to the even word. */
+static uint8_t e2m1_nearest(double a) {
+    uint8_t best = 0;
+    double bd = INFINITY;
+    for (int c = 0; c <= 7; ++c) {
+        double d = fabs(pnq_ref_e2m1_to_double((uint8_t)c) - a);
+        if (d < bd || (d == bd && (c & 1) == 0)) { bd = d; best = (uint8_t)c; }
+    }
+    return best;
+}
+
+int pnq_ref_quantize_nvfp4_clip(const float* w, const float* act_ms, float g, int64_t n_rows, int64_t K,
+                                uint8_t* codes, uint8_t* scales, int32_t* chosen) {
+    if (n_rows < 0 || K <= 0 || K % 16 != 0) return PNQ_REF_ERR_SHAPE;
+    if (n_rows > 0 && (!w || !act_ms || !codes || !scales)) return PNQ_REF_ERR_NULL;
+    if (!(isfinite(g) && g > 0.0f)) return PNQ_REF_ERR_VALUE;
+    const double gd = (double)g;
+    for (int64_t r = 0; r < n_rows; ++r)
+        for (int64_t grp = 0; grp < K / 16; ++grp) {
+            const float* x = w + r * K + grp * 16;
+            const float* a = act_ms + grp * 16;
+            double amax = 0.0;
+            for (int k = 0; k < 16; ++k) {
+                if (!isfinite(x[k])) return PNQ_REF_ERR_VALUE;
+                if (fabs((double)x[k]) > amax) amax = fabs((double)x[k]);
+            }
+            double best = INFINITY;
+            int best_i = 0;
+            uint8_t best_sc = 0, best_c[16];
+            for (int i = 0; i < 5; ++i) {
+                double t = ((kClipMultipliers[i] * amax) / 6.0) / gd;
+                uint8_t sc = e4m3_nearest(t);
+                double sv = pnq_ref_e4m3fn_to_double(sc);
+                uint8_t cw[16];
+                double err = 0.0;
+                for (int k = 0; k < 16; ++k) {
+                    uint8_t sign = (x[k] < 0.0f || (x[k] == 0.0f && signbit(x[k]))) ? 8 : 0;
+                    uint8_t mag = 0;
+                    if (sv != 0.0) mag = e2m1_nearest(fabs((double)x[k]) / (sv * gd));
+                    cw[k] = (uint8_t)(sign | mag);
+                    double dq = (pnq_ref_e2m1_to_double(cw[k]) * sv) * gd;
+                    double diff = (double)x[k] - dq;
+                    err = err + (double)a[k] * (diff * diff);
+                }
+                if (i == 0 || err < best) {
+                    best = err;
+                    best_i = i;
+                    best_sc = sc;
+                    memcpy(best_c, cw, sizeof cw);
+                }
+            }
+            scales[r * (K / 16) + grp] = best_sc;
+            for (int k = 0; k < 16; k += 2)
+                codes[r * (K / 2) + grp * 8 + k / 2] = (uint8_t)(best_c[k] | (best_c[k + 1] << 4));
+            if (chosen) chosen[r * (K / 16) + grp] = best_i;
+        }
+    return PNQ_REF_OK;
+}

@@ -86,6 +86,13 @@ int pnq_ref_quantize_grouped(int type, const float* w, int64_t n_rows, int64_t K
 int pnq_ref_gemv_grouped(int type, const uint8_t* lo, const uint8_t* hi, const uint16_t* sc, int64_t N,
                          int64_t K, const float* X, int M, double* Y, double* A);
 
+/* NVFP4 clip search (TandemLLM "Quantisation and profiles", section "The clip search"): per group
+ * of 16, the multiplier of 1.00, 0.95, 0.90, 0.85, 0.80 on the base scale amax / (6 g) with the
+ * least act_ms-weighted squared error; codes [N][K/2], scales [N][K/16] E4M3FN; chosen (may be
+ * NULL) receives the index of the multiplier kept per group. pnq_oracle.c states the readings. */
+int pnq_ref_quantize_nvfp4_clip(const float* w, const float* act_ms, float g, int64_t n_rows, int64_t K,
+                                uint8_t* codes, uint8_t* scales, int32_t* chosen);
+
 #ifdef __cplusplus
 }
 #endif
