@@ -366,6 +366,12 @@ struct PnMma {
 //
 // Either way the slices are summed in warp order at the end.
 //
+// FMA = true replaces the tensor-core decode with a CUDA-core one (the plain design the measurement
+// compares against; it takes the row-segment code path, all of x staged, no B operands): lane l
+// of a warp takes row l / 2 of the group and words 4 (l % 2) .. 4 (l % 2) + 3 of each block; a code
+// c becomes the exact float c - z by one AND-OR into the mantissa of 1.5 * 2^23 and one
+// subtraction, and M fp32 FMAs with x from shared memory follow; d scales each block's sums.
+//
 // The SM takes in bulk copies at about the HBM rate per SM, in issue order, so x requested after
 // the producer has filled the ring would land only behind all of it. The producer therefore issues
 // one stage, then waits until every consumer warp has requested its x, and fills the ring behind.
@@ -397,7 +403,48 @@ struct RsArgs {
     uint32_t off_rec, off_zb, off_x, off_part, off_stage, stage_bytes;
 };
 
-template <int TYPE, int LR, bool SEG>
+// CUDA-core decode of one (row group, unit) task: the lane's row (srow: the row at the unit's
+// first byte) and half hf of every block's words; tot[m] += sum over its weights of w * x[m].
+template <int TYPE>
+__device__ __forceinline__ void fma_task(uint32_t srow, int hf, const float* xu, int K, int M, float (&tot)[kRsZs]) {
+    using F = PnFmt<TYPE>;
+    constexpr uint32_t MASK = (1u << F::BITS) - 1u;
+    constexpr float BIAS = 12582912.0f + static_cast<float>(F::Z);  // 1.5 * 2^23 + z
+    static_for<kUnitBlocks>([&](auto Bc) {
+        constexpr int B = decltype(Bc)::value, OFF = kBlockBytes * B;
+        const float d = (B & 1) ? half_hi(ld_shared_u32<OFF - 2>(srow)) : half_lo(ld_shared_u32<OFF>(srow));
+        float blk[kRsZs] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+        for (int iw = 0; iw < 4; ++iw) {
+            const int wi = 4 * hf + iw;
+            const uint32_t wa = srow + static_cast<uint32_t>(OFF + 4 * wi);
+            uint32_t wd;
+            if constexpr (B & 1) {
+                wd = ld_shared_u32<2>(wa);
+            } else {
+                wd = prmt(ld_shared_u32<0>(wa), ld_shared_u32<4>(wa), 0x5432u);  // bytes 2..5 of the pair
+            }
+            const float* xw = xu + B * F::BLK + F::CPW * wi;
+#pragma unroll
+            for (int t = 0; t < F::CPW; t += 2) {
+                const int sh = F::BITS * (t >> 1);
+                const float v0 = __uint_as_float(((wd >> sh) & MASK) | 0x4B400000u) - BIAS;
+                const float v1 = __uint_as_float(((wd >> (sh + 16)) & MASK) | 0x4B400000u) - BIAS;
+#pragma unroll
+                for (int m = 0; m < kRsZs; ++m) {
+                    if (m < M) {
+                        const float2 xv = *reinterpret_cast<const float2*>(xw + static_cast<size_t>(m) * K + t);
+                        blk[m] = fmaf(v1, xv.y, fmaf(v0, xv.x, blk[m]));
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int m = 0; m < kRsZs; ++m) tot[m] = fmaf(d, blk[m], tot[m]);
+    });
+}
+
+template <int TYPE, int LR, bool SEG, bool FMA = false>
 __global__ void __launch_bounds__(kRsThreads, 1) pn_rows_kernel(const __grid_constant__ RsArgs a) {
     using C = Cfg<TYPE, 1, LR>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -561,7 +608,7 @@ __global__ void __launch_bounds__(kRsThreads, 1) pn_rows_kernel(const __grid_con
             }
             if (lane == 0) mbar_arrive(xreq);
             ok = mbar_wait_warp(xfull, 0);
-            if (ok)
+            if (ok && !FMA)
                 for (int p = warp; p < U * M; p += kRsWarps) {
                     const int u = p / M, m = p - u * M;
                     build_row<TYPE, 1, LR, kRsZs>(rec(u), zbu(u), zbu(u) + kUnitBlocks * kRsZs,
@@ -578,7 +625,17 @@ __global__ void __launch_bounds__(kRsThreads, 1) pn_rows_kernel(const __grid_con
                 const int u0 = seg_tab[j], n = seg_tab[j + 1] - u0;
                 const uint32_t pitch = static_cast<uint32_t>(rs_pitch(n * kUnitBytes));
                 const uint32_t s0 = smem_addr(stage(slot)) + g * pitch, s8 = s0 + 8u * pitch;
-                if (k0 < n) {
+                if (FMA && k0 < n) {
+                    float tot[kRsZs] = {0.0f, 0.0f, 0.0f, 0.0f};
+                    const uint32_t srow = smem_addr(stage(slot)) + static_cast<uint32_t>(lane >> 1) * pitch;
+                    for (int k = k0; k < n; k += kRsWarps)
+                        fma_task<TYPE>(srow + static_cast<uint32_t>(k * kUnitBytes), lane & 1, xs + (u0 + k) * C::UK,
+                                       a.K, M, tot);
+#pragma unroll
+                    for (int m = 0; m < kRsZs; ++m) tot[m] += __shfl_xor_sync(0xffffffffu, tot[m], 1);
+                    if ((lane & 1) == 0)
+                        for (int m = 0; m < M; ++m) mine[m * a.rows_pad + i * kGroupRows + (lane >> 1)] += tot[m];
+                } else if (!FMA && k0 < n) {
                     float tot0 = 0.0f, tot1 = 0.0f;
                     for (int k = k0; k < n; k += kRsWarps) task(s0, s8, static_cast<uint32_t>(k * kUnitBytes), u0 + k, tot0, tot1);
                     if (c < M) {
@@ -618,19 +675,22 @@ struct RsPlan {
 // Grid (one CTA per SM, or one per row when there are fewer rows), segments per row and the ring
 // of stages. Rows of at most 16 units stay whole (per-warp x buffers), with the deepest ring of
 // 8..2 stages that fits. Longer rows are cut into segments of at most 8, 6 then 4 units (all of x
-// staged), the first with a ring of 8..3 stages, then 2 as a last resort. False when nothing fits.
+// staged), the first with a ring of 8..3 stages, then 2 as a last resort. The CUDA-core decode
+// (fma) keeps no B operands and stages all of x. False when nothing fits.
 template <int TYPE, int LR>
-bool rs_plan(int64_t N, int U, int M, int sms, int s_req, RsPlan& p) {
+bool rs_plan(int64_t N, int U, int M, int sms, int s_req, RsPlan& p, bool fma = false) {
     using C = Cfg<TYPE, 1, LR>;
     if (U < 1 || M < 1 || M > kRsZs || (U + 3) / 4 > kRsMaxSeg) return false;
     p.G = static_cast<int>(std::min<int64_t>(sms, N));
     const int64_t rows_max = (N + p.G - 1) / p.G;
     p.rows_pad = static_cast<int>((rows_max + kGroupRows - 1) / kGroupRows * kGroupRows);
     const bool whole = U <= kRsWholeUnits;
+    const uint32_t nrec = fma ? 0u : static_cast<uint32_t>(U);
     p.off_rec = align_up(8u * (2u * kMaxStages + 2), 128);
-    p.off_zb = align_up(p.off_rec + static_cast<uint32_t>(U) * C::REC, 16);
-    p.off_x = align_up(p.off_zb + static_cast<uint32_t>(U) * kRsZb * 4u, 16);
-    const uint32_t xbytes = whole ? kRsWarps * 2u * C::UK * 4u : static_cast<uint32_t>(M) * U * C::UK * 4u;
+    p.off_zb = align_up(p.off_rec + nrec * C::REC, 16);
+    p.off_x = align_up(p.off_zb + nrec * kRsZb * 4u, 16);
+    const uint32_t xbytes =
+        (whole && !fma) ? kRsWarps * 2u * C::UK * 4u : static_cast<uint32_t>(M) * U * C::UK * 4u;
     p.off_part = align_up(p.off_x + xbytes, 16);
     p.off_stage = align_up(p.off_part + kRsWarps * static_cast<uint32_t>(M * p.rows_pad) * 4u, 128);
     const int cap[3] = {8, 6, 4};
@@ -649,9 +709,9 @@ bool rs_plan(int64_t N, int U, int M, int sms, int s_req, RsPlan& p) {
     return false;
 }
 
-template <int TYPE, int LR, bool SEG>
+template <int TYPE, int LR, bool SEG, bool FMA = false>
 cudaError_t launch_rows_kernel(const RsArgs& a, const RsPlan& p, cudaStream_t stream) {
-    auto kern = pn_rows_kernel<TYPE, LR, SEG>;
+    auto kern = pn_rows_kernel<TYPE, LR, SEG, FMA>;
     static std::atomic<bool> opted[64];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -677,9 +737,9 @@ cudaError_t launch_rows_kernel(const RsArgs& a, const RsPlan& p, cudaStream_t st
 
 template <int TYPE, int LR>
 cudaError_t launch_rows(const uint8_t* W, const float* X, float* Y, int* err, int64_t N, int64_t K, int M, int U,
-                        int row_bytes, int s_req, bool static_weights, cudaStream_t stream) {
+                        int row_bytes, int s_req, bool static_weights, bool fma, cudaStream_t stream) {
     RsPlan p;
-    if (!rs_plan<TYPE, LR>(N, U, M, device_sm_count(), s_req, p)) return cudaErrorNotSupported;
+    if (!rs_plan<TYPE, LR>(N, U, M, device_sm_count(), s_req, p, fma)) return cudaErrorNotSupported;
     RsArgs a{};
     a.W = W;
     a.X = X;
@@ -702,17 +762,18 @@ cudaError_t launch_rows(const uint8_t* W, const float* X, float* Y, int* err, in
     a.off_part = p.off_part;
     a.off_stage = p.off_stage;
     a.stage_bytes = p.stage_bytes;
+    if (fma) return launch_rows_kernel<TYPE, LR, true, true>(a, p, stream);
     return p.nseg > 1 ? launch_rows_kernel<TYPE, LR, true>(a, p, stream) : launch_rows_kernel<TYPE, LR, false>(a, p, stream);
 }
 
 template <int TYPE>
 cudaError_t launch_rows_typed(const uint8_t* W, const float* X, float* Y, int* err, int64_t N, int64_t K, int M,
-                              int U, int row_bytes, int s_req, bool static_weights, cudaStream_t stream) {
+                              int U, int row_bytes, int s_req, bool static_weights, bool fma, cudaStream_t stream) {
     switch (M) {
-        case 1: return launch_rows<TYPE, 8>(W, X, Y, err, N, K, M, U, row_bytes, s_req, static_weights, stream);
-        case 2: return launch_rows<TYPE, 16>(W, X, Y, err, N, K, M, U, row_bytes, s_req, static_weights, stream);
-        case 3: return launch_rows<TYPE, 24>(W, X, Y, err, N, K, M, U, row_bytes, s_req, static_weights, stream);
-        case 4: return launch_rows<TYPE, 32>(W, X, Y, err, N, K, M, U, row_bytes, s_req, static_weights, stream);
+        case 1: return launch_rows<TYPE, 8>(W, X, Y, err, N, K, M, U, row_bytes, s_req, static_weights, fma, stream);
+        case 2: return launch_rows<TYPE, 16>(W, X, Y, err, N, K, M, U, row_bytes, s_req, static_weights, fma, stream);
+        case 3: return launch_rows<TYPE, 24>(W, X, Y, err, N, K, M, U, row_bytes, s_req, static_weights, fma, stream);
+        case 4: return launch_rows<TYPE, 32>(W, X, Y, err, N, K, M, U, row_bytes, s_req, static_weights, fma, stream);
         default: return cudaErrorNotSupported;
     }
 }
@@ -757,19 +818,21 @@ cudaError_t launch_pn_gemv_mma(int type, const uint8_t* W, int64_t N, int64_t K,
     if (!encode_u32_map(&map[0], W, N, nb * kBlockBytes / 4, kUnitU32, kPieceRows) ||
         !encode_u32_map(&map[1], W, N, nb * kBlockBytes / 4, kUnitU32, kStageRows))
         return cudaErrorNotSupported;
-    static int env[4];  // PNQ_PN_CFG = "CTAs per cluster, stages, CTAs per SM, path (1 rows, 2 strips)"
+    // PNQ_PN_CFG = "CTAs per cluster, stages, CTAs per SM, path (1 rows, 2 strips), decode (1 CUDA-core FMA)"
+    static int env[5];
     static std::once_flag once;
     std::call_once(once, [] { env_cluster_config("PNQ_PN_CFG", env); });
     const int req[3] = {c_req > 0 ? c_req : env[0], s_req > 0 ? s_req : env[1], env[2]};
     // whole rows per CTA when the B operands of every unit fit beside the stages (M <= 4)
     const int row_bytes = static_cast<int>(nb * kBlockBytes);
+    const bool fma = env[4] == 1;
     if (env[3] != 2 && M <= 4 && c_req <= 0) {
         const cudaError_t e = (type == kTypePn3t)
                                   ? launch_rows_typed<kTypePn3t>(W, X, Y, err, N, K, M, static_cast<int>(U), row_bytes,
-                                                                 req[1], static_weights, stream)
+                                                                 req[1], static_weights, fma, stream)
                                   : launch_rows_typed<kTypePn4t>(W, X, Y, err, N, K, M, static_cast<int>(U), row_bytes,
-                                                                 req[1], static_weights, stream);
-        if (e != cudaErrorNotSupported || env[3] == 1) return e;
+                                                                 req[1], static_weights, fma, stream);
+        if (e != cudaErrorNotSupported || env[3] == 1 || fma) return e;
     }
     return (type == kTypePn3t)
                ? launch_typed<kTypePn3t>(map, X, Y, err, N, K, M, static_cast<int>(U), req, static_weights, stream)

@@ -162,13 +162,13 @@ void run_type() {
 }
 
 template <int TYPE, int LR>
-void check_rs_plan(int64_t N, int U, int M, int s_req) {
+void check_rs_plan(int64_t N, int U, int M, int s_req, bool fma = false) {
     using C = pnq::Cfg<TYPE, 1, LR>;
     char what[128];
     std::snprintf(what, sizeof what, "rows %s N %lld U %d M %d s %d", TYPE == pnq::kTypePn3t ? "pn3t" : "pn4t",
                   (long long)N, U, M, s_req);
     pnq::RsPlan p;
-    if (!pnq::rs_plan<TYPE, LR>(N, U, M, 152, s_req, p)) return;
+    if (!pnq::rs_plan<TYPE, LR>(N, U, M, 152, s_req, p, fma)) return;
     ++plans;
     if (s_req > 0 && p.S != s_req) FAIL("forced %d stages, planned %d", s_req, p.S);
     if (p.S < 2 || p.S > 8) FAIL("%d stages", p.S);
@@ -183,10 +183,11 @@ void check_rs_plan(int64_t N, int U, int M, int s_req) {
     const bool whole = U <= pnq::kRsWholeUnits;
     if (whole != (p.nseg == 1)) FAIL("%d segments for %d units", p.nseg, U);
     if (whole && p.pitch != pnq::rs_pitch(U * pnq::kUnitBytes)) FAIL("whole-row pitch %d", p.pitch);
-    const uint64_t xbytes = whole ? 4ull * pnq::kRsWarps * 2 * C::UK : 4ull * M * U * C::UK;
+    const uint64_t xbytes = (whole && !fma) ? 4ull * pnq::kRsWarps * 2 * C::UK : 4ull * M * U * C::UK;
+    const uint64_t nrec = fma ? 0 : U;
     std::vector<R> r = {{0, 8ull * (2 * p.S + 2), "barriers"},
-                        {p.off_rec, p.off_rec + 1ull * U * C::REC, "B operands"},
-                        {p.off_zb, p.off_zb + 4ull * U * pnq::kRsZb, "zero-point terms"},
+                        {p.off_rec, p.off_rec + nrec * C::REC, "B operands"},
+                        {p.off_zb, p.off_zb + 4ull * nrec * pnq::kRsZb, "zero-point terms"},
                         {p.off_x, p.off_x + xbytes, "x rows"},
                         {p.off_part, p.off_part + 4ull * pnq::kRsWarps * M * p.rows_pad, "row partials"},
                         {p.off_stage, p.off_stage + 1ull * p.S * p.stage_bytes, "stages"}};
@@ -244,10 +245,12 @@ void run_rows() {
         for (int U : {1, 2, 7, 8, 9, 12, 16, 17, 25, 33, 34, 48, 68})
             for (int s : {0, 2, 3, 5})
                 for (int M = 1; M <= 4 && !failures; ++M) {
-                    if (M == 1) check_rs_plan<TYPE, 8>(N, U, M, s);
-                    if (M == 2) check_rs_plan<TYPE, 16>(N, U, M, s);
-                    if (M == 3) check_rs_plan<TYPE, 24>(N, U, M, s);
-                    if (M == 4) check_rs_plan<TYPE, 32>(N, U, M, s);
+                    for (bool fma : {false, true}) {
+                        if (M == 1) check_rs_plan<TYPE, 8>(N, U, M, s, fma);
+                        if (M == 2) check_rs_plan<TYPE, 16>(N, U, M, s, fma);
+                        if (M == 3) check_rs_plan<TYPE, 24>(N, U, M, s, fma);
+                        if (M == 4) check_rs_plan<TYPE, 32>(N, U, M, s, fma);
+                    }
                 }
     // the decode-step projections at M = 1 take the row-stream path
     for (int64_t N : {1024, 5120, 12288, 17408})
