@@ -614,9 +614,9 @@ CODEC_SHAPES = [(PN4T, 5120, 17408), (PN3T, 17408, 5120), (NVFP4, 17408, 5120)]
 def run_codec(args):
     """Dequantize and validate on full-size shapes (pn4t 5120 x 17408, pn3t 17408 x 5120, NVFP4
     17408 x 5120; weights generated on the device from the seed). Each call's time is the mean of
-    CUDA events around back-to-back calls on the current stream (`--steps`, at least one per weight
-    copy) after `--warmup` calls, rotating through weight copies that together exceed the L2
-    twice, so the weights come from HBM.
+    CUDA events around one replay of a CUDA graph of back-to-back calls (`--steps`, at least one
+    per weight copy; captured after `--warmup` calls), rotating through weight copies that
+    together exceed the L2 twice, so the weights come from HBM.
     Algorithmic bytes per call: the weights read plus the fp32 weights written (dequantize); for
     validate, the int32 row flags written plus the PN tensor (its d fields sit at a 34-byte stride,
     so every 32-byte sector holds one and the whole tensor crosses the bus) or the NVFP4 scales
@@ -653,17 +653,28 @@ def run_codec(args):
                ("validate_row", lambda W: pnq.validate_row(t, W, N, K, flags=flags),
                 (N * K // 16 if t == NVFP4 else wbytes) + 4 * N)]
         for op, call, nbytes in ops:
-            for i in range(args.warmup):
-                call(copies[i % n_copies])
+            reps = max(args.steps, n_copies)  # every copy at least once, none reused while in L2
+            # the calls are captured once into a CUDA graph and replayed, so the time is the
+            # device's (a Python call costs more than a small kernel)
+            side = torch.cuda.Stream()
+            side.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(side):
+                for i in range(args.warmup):
+                    call(copies[i % n_copies])
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=side):
+                for i in range(args.warmup, args.warmup + reps):
+                    call(copies[i % n_copies])
+            g.replay()
             torch.cuda.synchronize()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            reps = max(args.steps, n_copies)  # every copy at least once, none reused while in L2
             e0.record()
-            for i in range(args.warmup, args.warmup + reps):
-                call(copies[i % n_copies])
+            g.replay()
             e1.record()
             torch.cuda.synchronize()
             us = e0.elapsed_time(e1) * 1e3 / reps
+            del g
             gbs = nbytes / (us * 1e-6) / 1e9
             print(json.dumps({"op": op, "type": name, "N": N, "K": K, "calls": reps, "us_per_call": round(us, 3),
                               "algorithmic_bytes": nbytes, "weight_copies": n_copies, "achieved": round(gbs, 1),

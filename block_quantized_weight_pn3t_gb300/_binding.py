@@ -90,6 +90,8 @@ def lib() -> ctypes.CDLL:
         L.pnq_quantize_row.argtypes = [I, P, I64, I64, P, P, P]
         L.pnq_quantize_nvfp4_clip.restype = I
         L.pnq_quantize_nvfp4_clip.argtypes = [P, P, I64, I64, ctypes.c_float, P, P, P, P]
+        L.pnq_selftest_wait.restype = I
+        L.pnq_selftest_wait.argtypes = [ctypes.c_uint32, P]
         L.pnq_device_error.restype = I
         L.pnq_device_error.argtypes = [ctypes.POINTER(ctypes.c_int32)]
         L.pnq_version.restype = ctypes.c_char_p
@@ -152,6 +154,12 @@ def quantize_row_ptr(type_: int, w: int, n_rows: int, K: int, out, status: int, 
     o = ctypes.byref(out) if type_ in GROUPED else ctypes.c_void_p(out)
     return lib().pnq_quantize_row(type_, ctypes.c_void_p(w), n_rows, K, o, ctypes.c_void_p(status),
                                   ctypes.c_void_p(stream))
+
+
+def selftest_wait(limit_us: int, stream=None) -> None:
+    """Run the bounded-wait self-test (a wait nothing completes, giving up after limit_us)."""
+    _check(lib().pnq_selftest_wait(int(limit_us), ctypes.c_void_p(_stream_handle(stream) if stream is not None else 0)),
+           "pnq_selftest_wait")
 
 
 def device_error() -> int:

@@ -1,5 +1,6 @@
 // pnq_api.cu -- the C ABI declared in include/pnq.h: argument checks, kernel choice, status codes.
 #include "pnq.h"
+#include "pnq_device.cuh"
 #include "pnq_internal.h"
 
 #include <algorithm>
@@ -322,6 +323,30 @@ extern "C" int pnq_quantize_nvfp4_clip(const float* w, const float* act_ms, int6
     if (!w || !act_ms || !codes || !scales || !row_status) return PNQ_ERR_NULL;
     if (!aligned(w, 4) || !aligned(act_ms, 4) || !aligned(row_status, 4)) return PNQ_ERR_ALIGN;
     return map_cuda(launch_nvfp4_clip(w, act_ms, global_scale, n_rows, K, codes, scales, row_status, stream));
+}
+
+namespace pnq {
+
+// One thread waits, bounded by limit_ns, on a shared-memory barrier nothing arrives at, with the
+// kernels' own bounded wait, and records the self-test site code when the wait runs out.
+__global__ void wait_selftest_kernel(int* err, uint64_t limit_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_addr(&bar), 1);
+        mbar_fence_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && !mbar_wait_bounded(smem_addr(&bar), 0, limit_ns)) record_error(err, kErrSelfTest);
+}
+
+}  // namespace pnq
+
+extern "C" int pnq_selftest_wait(uint32_t limit_us, cudaStream_t stream) {
+    if (limit_us == 0 || limit_us > 2000000u) return PNQ_ERR_VALUE;
+    int* err = error_word();
+    if (!err) return PNQ_ERR_CUDA;
+    wait_selftest_kernel<<<1, 32, 0, stream>>>(err, static_cast<uint64_t>(limit_us) * 1000ull);
+    return map_cuda(cudaGetLastError());
 }
 
 extern "C" int pnq_device_error(int32_t* code) {

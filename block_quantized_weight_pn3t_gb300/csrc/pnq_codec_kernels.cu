@@ -8,6 +8,7 @@
 #include "pnq_internal.h"
 
 #include <algorithm>
+#include <cstdint>
 
 namespace pnq {
 namespace {
@@ -20,93 +21,161 @@ int grid_for(int64_t work_items, int per_thread) {
     return static_cast<int>(std::max<int64_t>(1, std::min(blocks, cap)));
 }
 
-// One thread per (block, 16-bit half): the half holds the codes of CPW/2 elements, all
-// even t (low half of a word) or all odd t (high half); only 16-bit loads are used, so
-// the 2-byte alignment of odd blocks is never an issue. Output row-major order equals
-// block order, so block gb writes out[gb * BLK + e].
-template <int TYPE>
+// A warp takes 32 consecutive blocks at a time (1088 bytes in, 32 * BLK floats out). It stages
+// the blocks in shared memory, with 16-byte loads when W is 16-byte aligned (16-bit loads
+// otherwise: odd blocks start on a 2-byte boundary), then lane l writes float4 j = l, l + 32, ..
+// of the chunk's output: elements 4j .. 4j + 3 lie in one block (BLK is a multiple of 4), each a
+// code read from its 16-bit half (word e / CPW, half t & 1, shift BITS * (t >> 1), t = e mod CPW)
+// times d, exact in fp32. The writes, 9.4 of every 10 bytes moved, are whole 512-byte warp stores.
+constexpr int kChunkBlocks = 32;
+constexpr int kChunkBytes = kChunkBlocks * kBlockBytes;  // 1088 = 68 * 16
+
+template <int TYPE, bool VEC>
 __global__ void __launch_bounds__(kThreads) pn_dequant_kernel(const uint8_t* __restrict__ W, int64_t nblocks,
                                                                 float* __restrict__ out) {
     using F = PnFmt<TYPE>;
-    const int64_t total = nblocks * 16;
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total; i += stride) {
-        const int64_t gb = i >> 4;
-        const int h = static_cast<int>(i & 15);
-        const uint8_t* blk = W + gb * kBlockBytes;
-        const float d = __half2float(__ushort_as_half(__ldg(reinterpret_cast<const unsigned short*>(blk))));
-        const uint32_t half = __ldg(reinterpret_cast<const unsigned short*>(blk + 2 + 2 * h));
-        float* o = out + gb * F::BLK + (h >> 1) * F::CPW + (h & 1);
-#pragma unroll
-        for (int j = 0; j < F::PAIRS; ++j) {
-            const int n = static_cast<int>((half >> (F::BITS * j)) & ((1u << F::BITS) - 1u));
-            o[2 * j] = d * static_cast<float>(n - F::Z);
+    __shared__ __align__(16) uint8_t stage[kThreads / 32][kChunkBytes];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    uint8_t* sb = stage[warp];
+    const int64_t nchunks = (nblocks + kChunkBlocks - 1) / kChunkBlocks;
+    const int64_t wstride = static_cast<int64_t>(gridDim.x) * (kThreads / 32);
+    for (int64_t ch = static_cast<int64_t>(blockIdx.x) * (kThreads / 32) + warp; ch < nchunks; ch += wstride) {
+        const int64_t left = nblocks - ch * kChunkBlocks;
+        const int nblk = left < kChunkBlocks ? static_cast<int>(left) : kChunkBlocks;
+        const uint8_t* src = W + ch * kChunkBytes;
+        if (VEC && nblk == kChunkBlocks) {
+            for (int q = lane; q < kChunkBytes / 16; q += 32)
+                reinterpret_cast<uint4*>(sb)[q] = __ldg(reinterpret_cast<const uint4*>(src) + q);
+        } else {
+            for (int q = lane; q < nblk * kBlockBytes / 2; q += 32)
+                reinterpret_cast<unsigned short*>(sb)[q] = __ldg(reinterpret_cast<const unsigned short*>(src) + q);
         }
+        __syncwarp();
+        const int nvec = nblk * F::BLK / 4;
+        float4* o = reinterpret_cast<float4*>(out + ch * kChunkBlocks * F::BLK);
+        for (int j = lane; j < nvec; j += 32) {
+            const int blk = (4 * j) / F::BLK, e0 = 4 * j - blk * F::BLK;
+            const uint8_t* bp = sb + blk * kBlockBytes;
+            const float d = __half2float(__ushort_as_half(*reinterpret_cast<const unsigned short*>(bp)));
+            float v[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int e = e0 + q, w = e / F::CPW, t = e - w * F::CPW;
+                const uint32_t half = *reinterpret_cast<const unsigned short*>(bp + 2 + 4 * w + 2 * (t & 1));
+                const int n = static_cast<int>((half >> (F::BITS * (t >> 1))) & ((1u << F::BITS) - 1u));
+                v[q] = __fmul_rn(d, static_cast<float>(n - F::Z));
+            }
+            if (VEC) {
+                o[j] = make_float4(v[0], v[1], v[2], v[3]);
+            } else {
+                float* os = reinterpret_cast<float*>(o) + 4 * j;
+                os[0] = v[0];
+                os[1] = v[1];
+                os[2] = v[2];
+                os[3] = v[3];
+            }
+        }
+        __syncwarp();
     }
 }
 
-// One thread per code byte (two weights); code byte c of the flat [N][K/2] array belongs
-// to scale c / 8 of the flat [N][K/16] array.
-template <bool DIV>
+// One thread per two code bytes (four weights, one float4): code byte c of the flat [N][K/2]
+// array belongs to scale c / 8 of the flat [N][K/16] array; a warp writes 512 contiguous bytes.
+template <bool DIV, bool VEC>
 __global__ void __launch_bounds__(kThreads) nvfp4_dequant_kernel(const uint8_t* __restrict__ codes,
                                                                    const uint8_t* __restrict__ scales, float g,
-                                                                   int64_t nbytes, float* __restrict__ out) {
+                                                                   int64_t npairs, float* __restrict__ out) {
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < nbytes; i += stride) {
-        const uint32_t c = __ldg(codes + i);
-        const float s = e4m3_to_f32(__ldg(scales + (i >> 3)));
-        // e2m1 * e4m3 is exact in fp32; the product with (quotient by) g is the single rounding.
-        const float lo = e2m1_to_f32(c & 15u) * s;
-        const float hi = e2m1_to_f32(c >> 4) * s;
-        out[2 * i] = DIV ? __fdiv_rn(lo, g) : __fmul_rn(lo, g);
-        out[2 * i + 1] = DIV ? __fdiv_rn(hi, g) : __fmul_rn(hi, g);
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < npairs; i += stride) {
+        const uint32_t c = VEC ? __ldg(reinterpret_cast<const unsigned short*>(codes) + i)
+                               : (static_cast<uint32_t>(__ldg(codes + 2 * i)) |
+                                  (static_cast<uint32_t>(__ldg(codes + 2 * i + 1)) << 8));
+        const float s = e4m3_to_f32(__ldg(scales + (i >> 2)));
+        float v[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            // e2m1 * e4m3 is exact in fp32; the product with (quotient by) g is the single rounding
+            const float p = e2m1_to_f32((c >> (4 * q)) & 15u) * s;
+            v[q] = DIV ? __fdiv_rn(p, g) : __fmul_rn(p, g);
+        }
+        if (VEC) {
+            reinterpret_cast<float4*>(out)[i] = make_float4(v[0], v[1], v[2], v[3]);
+        } else {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) out[4 * i + q] = v[q];
+        }
     }
 }
 
-// One warp per row over the row's 16-bit halves: half 0 of each 17-half block is d
-// (invalid if its exponent field is all ones), the other 16 are word halves whose bit 15
-// (word bits 15 and 31) is reserved in pn3t.
-template <int TYPE>
+// One warp per row. Half h of a row is half h mod 17 of its block (half 0: d, invalid if its
+// exponent field is all ones; halves 1..16: word halves, whose bit 15 — word bits 15 and 31 — is
+// reserved in pn3t). With 16-byte aligned rows (W aligned, row length a multiple of 16 bytes) a
+// lane reads 8 halves per 16-byte load; otherwise 16-bit loads. Positions mod 17 stay in 32 bits.
+template <int TYPE, bool VEC>
 __global__ void __launch_bounds__(kThreads) pn_validate_kernel(const uint8_t* __restrict__ W, int64_t n_rows,
-                                                                 int64_t nb, int32_t* __restrict__ flags) {
+                                                                 int row_halves, int32_t* __restrict__ flags) {
     const int lane = threadIdx.x & 31;
     const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
-    const int64_t nh = nb * 17;
+    auto bad_half = [](int pos, uint32_t v) {
+        return pos == 0 ? (v & 0x7C00u) == 0x7C00u : (TYPE == kTypePn3t && (v & 0x8000u) != 0);
+    };
     for (int64_t row = warp0; row < n_rows; row += nwarps) {
-        const unsigned short* h = reinterpret_cast<const unsigned short*>(W + row * nb * kBlockBytes);
+        const unsigned short* h = reinterpret_cast<const unsigned short*>(W) + row * row_halves;
         bool bad = false;
-        int pos = lane % 17;
-        for (int64_t i = lane; i < nh; i += 32) {
-            const uint32_t v = __ldg(h + i);
-            if (pos == 0)
-                bad |= (v & 0x7C00u) == 0x7C00u;
-            else if (TYPE == kTypePn3t)
-                bad |= (v & 0x8000u) != 0;
-            pos += 15;  // (i + 32) mod 17
-            if (pos >= 17) pos -= 17;
+        if (VEC) {
+            const uint4* v = reinterpret_cast<const uint4*>(h);
+            for (int q = lane; q < row_halves / 8; q += 32) {
+                const uint4 u = __ldg(v + q);
+                const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+                int pos = (8 * q) % 17;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    bad |= bad_half(pos, w[k] & 0xFFFFu);
+                    pos = (pos == 16) ? 0 : pos + 1;
+                    bad |= bad_half(pos, w[k] >> 16);
+                    pos = (pos == 16) ? 0 : pos + 1;
+                }
+            }
+        } else {
+            for (int i = lane; i < row_halves; i += 32) bad |= bad_half(i % 17, __ldg(h + i));
         }
         bad = __any_sync(0xffffffffu, bad);
         if (lane == 0) flags[row] = bad ? 1 : 0;
     }
 }
 
-__global__ void __launch_bounds__(kThreads) nvfp4_validate_kernel(const uint8_t* __restrict__ scales,
-                                                                    int64_t n_rows, int64_t ns, int g_ok,
-                                                                    int32_t* __restrict__ flags) {
+// One warp per row of scale bytes: a byte with its sign bit set or the NaN pattern 0x7F / 0xFF
+// makes the row invalid, and so does a global field that is not finite and > 0 (g_ok == 0, every
+// row). 16 bytes per lane-load when the rows are 16-byte aligned.
+template <bool VEC>
+__global__ void __launch_bounds__(kThreads) nvfp4_validate_kernel(const uint8_t* __restrict__ scales, int64_t n_rows,
+                                                                    int ns, int g_ok, int32_t* __restrict__ flags) {
     const int lane = threadIdx.x & 31;
     const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    auto bad_byte = [](uint32_t b) { return (b & 0x80u) != 0 || (b & 0x7Fu) == 0x7Fu; };
     for (int64_t row = warp0; row < n_rows; row += nwarps) {
+        const uint8_t* r = scales + row * ns;
         bool bad = !g_ok;
-        for (int64_t i = lane; i < ns; i += 32) {
-            const uint32_t s = __ldg(scales + row * ns + i);
-            bad |= (s & 0x80u) != 0 || (s & 0x7Fu) == 0x7Fu;
+        if (g_ok) {
+            if (VEC) {
+                for (int q = lane; q < ns / 16; q += 32) {
+                    const uint4 u = __ldg(reinterpret_cast<const uint4*>(r) + q);
+                    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) bad |= bad_byte((w[k >> 2] >> (8 * (k & 3))) & 0xFFu);
+                }
+            } else {
+                for (int i = lane; i < ns; i += 32) bad |= bad_byte(__ldg(r + i));
+            }
         }
         bad = __any_sync(0xffffffffu, bad);
         if (lane == 0) flags[row] = bad ? 1 : 0;
     }
 }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace
 
@@ -115,22 +184,31 @@ cudaError_t launch_pn_dequant(int type, const uint8_t* W, int64_t n_rows, int64_
     const int blk = (type == kTypePn3t) ? PnFmt<kTypePn3t>::BLK : PnFmt<kTypePn4t>::BLK;
     const int64_t nblocks = n_rows * (K / blk);
     if (nblocks == 0) return cudaSuccess;
-    const int grid = grid_for(nblocks * 16, 1);
-    if (type == kTypePn3t)
-        pn_dequant_kernel<kTypePn3t><<<grid, kThreads, 0, stream>>>(W, nblocks, out);
-    else
-        pn_dequant_kernel<kTypePn4t><<<grid, kThreads, 0, stream>>>(W, nblocks, out);
+    const int grid = grid_for((nblocks + kChunkBlocks - 1) / kChunkBlocks * 32, 1);
+    const bool vec = aligned16(W) && aligned16(out);
+    if (type == kTypePn3t) {
+        if (vec) pn_dequant_kernel<kTypePn3t, true><<<grid, kThreads, 0, stream>>>(W, nblocks, out);
+        else pn_dequant_kernel<kTypePn3t, false><<<grid, kThreads, 0, stream>>>(W, nblocks, out);
+    } else {
+        if (vec) pn_dequant_kernel<kTypePn4t, true><<<grid, kThreads, 0, stream>>>(W, nblocks, out);
+        else pn_dequant_kernel<kTypePn4t, false><<<grid, kThreads, 0, stream>>>(W, nblocks, out);
+    }
     return cudaGetLastError();
 }
 
 cudaError_t launch_nvfp4_dequant(const Nvfp4View& w, int64_t n_rows, int64_t K, float* out,
                                  cudaStream_t stream) {
-    const int64_t nbytes = n_rows * (K / 2);
-    if (nbytes == 0) return cudaSuccess;
-    if (w.div)
-        nvfp4_dequant_kernel<true><<<grid_for(nbytes, 1), kThreads, 0, stream>>>(w.codes, w.scales, w.g, nbytes, out);
-    else
-        nvfp4_dequant_kernel<false><<<grid_for(nbytes, 1), kThreads, 0, stream>>>(w.codes, w.scales, w.g, nbytes, out);
+    const int64_t npairs = n_rows * (K / 4);
+    if (npairs == 0) return cudaSuccess;
+    const int grid = grid_for(npairs, 1);
+    const bool vec = (reinterpret_cast<uintptr_t>(w.codes) & 1u) == 0 && aligned16(out);
+    if (w.div) {
+        if (vec) nvfp4_dequant_kernel<true, true><<<grid, kThreads, 0, stream>>>(w.codes, w.scales, w.g, npairs, out);
+        else nvfp4_dequant_kernel<true, false><<<grid, kThreads, 0, stream>>>(w.codes, w.scales, w.g, npairs, out);
+    } else {
+        if (vec) nvfp4_dequant_kernel<false, true><<<grid, kThreads, 0, stream>>>(w.codes, w.scales, w.g, npairs, out);
+        else nvfp4_dequant_kernel<false, false><<<grid, kThreads, 0, stream>>>(w.codes, w.scales, w.g, npairs, out);
+    }
     return cudaGetLastError();
 }
 
@@ -138,11 +216,18 @@ cudaError_t launch_pn_validate(int type, const uint8_t* W, int64_t n_rows, int64
                                cudaStream_t stream) {
     if (n_rows == 0) return cudaSuccess;
     const int blk = (type == kTypePn3t) ? PnFmt<kTypePn3t>::BLK : PnFmt<kTypePn4t>::BLK;
+    const int64_t nb = K / blk;
+    if (nb * 17 > INT32_MAX) return cudaErrorInvalidValue;  // rows of over 2^31 halves
+    const int row_halves = static_cast<int>(nb * 17);
+    const bool vec = aligned16(W) && (nb * kBlockBytes) % 16 == 0;
     const int grid = grid_for(n_rows * 32, 1);
-    if (type == kTypePn3t)
-        pn_validate_kernel<kTypePn3t><<<grid, kThreads, 0, stream>>>(W, n_rows, K / blk, flags);
-    else
-        pn_validate_kernel<kTypePn4t><<<grid, kThreads, 0, stream>>>(W, n_rows, K / blk, flags);
+    if (type == kTypePn3t) {
+        if (vec) pn_validate_kernel<kTypePn3t, true><<<grid, kThreads, 0, stream>>>(W, n_rows, row_halves, flags);
+        else pn_validate_kernel<kTypePn3t, false><<<grid, kThreads, 0, stream>>>(W, n_rows, row_halves, flags);
+    } else {
+        if (vec) pn_validate_kernel<kTypePn4t, true><<<grid, kThreads, 0, stream>>>(W, n_rows, row_halves, flags);
+        else pn_validate_kernel<kTypePn4t, false><<<grid, kThreads, 0, stream>>>(W, n_rows, row_halves, flags);
+    }
     return cudaGetLastError();
 }
 
@@ -150,8 +235,12 @@ cudaError_t launch_nvfp4_validate(const Nvfp4View& w, int64_t n_rows, int64_t K,
                                   cudaStream_t stream) {
     if (n_rows == 0) return cudaSuccess;
     const int g_ok = (w.g > 0.0f && w.g <= 3.4028234663852886e38f) ? 1 : 0;  // finite and > 0
-    nvfp4_validate_kernel<<<grid_for(n_rows * 32, 1), kThreads, 0, stream>>>(w.scales, n_rows, K / 16, g_ok,
-                                                                              flags);
+    if (K / 16 > INT32_MAX) return cudaErrorInvalidValue;  // rows of over 2^31 scales
+    const int ns = static_cast<int>(K / 16);
+    const bool vec = aligned16(w.scales) && ns % 16 == 0;
+    const int grid = grid_for(n_rows * 32, 1);
+    if (vec) nvfp4_validate_kernel<true><<<grid, kThreads, 0, stream>>>(w.scales, n_rows, ns, g_ok, flags);
+    else nvfp4_validate_kernel<false><<<grid, kThreads, 0, stream>>>(w.scales, n_rows, ns, g_ok, flags);
     return cudaGetLastError();
 }
 

@@ -32,7 +32,7 @@ template <> struct PnFmt<kTypePn4t> {
 };
 
 // Site codes written to the device error word when a bounded wait gives up.
-enum ErrSite : int { kErrFullWait = 1, kErrEmptyWait = 2, kErrDrainWait = 3, kErrOperandWait = 5 };
+enum ErrSite : int { kErrFullWait = 1, kErrEmptyWait = 2, kErrDrainWait = 3, kErrOperandWait = 5, kErrSelfTest = 6 };
 
 // The device error word lives in pnq_api.cu; kernels receive its address. It holds 0, or the
 // site code of the first bounded wait that gave up.
@@ -77,20 +77,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
         : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// Same test, but the thread may sleep until the phase completes or about hint_ns pass (so a
-// waiting warp does not take issue slots from the others).
-__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity), "r"(hint_ns)
         : "memory");
     return ok != 0;
 }
@@ -154,12 +140,6 @@ __device__ __forceinline__ void griddep_launch_dependents() {
 
 // ---- cluster ------------------------------------------------------------------
 
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
                      : "memory");
@@ -171,50 +151,6 @@ __device__ __forceinline__ float ld_dsmem_f32(uint32_t local_addr, uint32_t rank
     float v;
     asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
     return v;
-}
-
-// Address of the same shared-memory location in CTA `rank` of the cluster.
-__device__ __forceinline__ uint32_t mapa_shared(uint32_t local_addr, uint32_t rank) {
-    uint32_t remote;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_addr), "r"(rank));
-    return remote;
-}
-
-__device__ __forceinline__ float ld_dsmem_f32_at(uint32_t cluster_addr) {
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(cluster_addr) : "memory");
-    return v;
-}
-
-// Arrive (release, cluster scope) on an mbarrier of another CTA of the cluster.
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_bar_addr) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar_addr) : "memory");
-}
-
-__device__ __forceinline__ void fence_acq_rel_cluster() { asm volatile("fence.acq_rel.cluster;" ::: "memory"); }
-
-// try_wait with acquire at cluster scope: writes released by other CTAs of the cluster before
-// their arrive become visible to this thread.
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-__device__ __forceinline__ bool mbar_wait_cluster_bounded(uint32_t bar, uint32_t parity,
-                                                          uint64_t limit_ns = 2000000000ull) {
-    if (mbar_try_wait_cluster(bar, parity)) return true;
-    const uint64_t t0 = global_timer_ns();
-    while (true) {
-        if (mbar_try_wait_cluster(bar, parity)) return true;
-        if (global_timer_ns() - t0 > limit_ns) return false;
-    }
 }
 
 // Named barrier over the first `threads` threads of the CTA (id 1; id 0 is __syncthreads).
@@ -337,28 +273,6 @@ __device__ __forceinline__ void cp_async_wait_dyn(int n) {
     }
 }
 
-// atomicAdd with acquire-release semantics at GPU scope: the writes that happen before it (in
-// this thread, or in threads ordered before it by a barrier) are visible to whoever observes the
-// new value, and this thread's later reads see what the earlier incrementers wrote before theirs.
-__device__ __forceinline__ uint32_t atomic_add_acq_rel(uint32_t* p, uint32_t v) {
-    uint32_t old;
-    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
-    return old;
-}
-
-// Named barrier that also ANDs a predicate over the participating threads: every thread gets
-// the same answer, so all of them take the same branch afterwards.
-__device__ __forceinline__ bool named_sync_and(uint32_t id, uint32_t threads, bool pred) {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
-        "bar.red.and.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
-        : "=r"(r)
-        : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(threads)
-        : "memory");
-    return r != 0;
-}
-
 // Bounded mbarrier wait by a whole warp; the result is the same in every lane.
 __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity) {
     return __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity));
@@ -366,28 +280,9 @@ __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity) {
 
 // ---- integer / half helpers ----------------------------------------------------
 
-// (a & b) | c in one instruction.
-__device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t b, uint32_t c) {
-    uint32_t d;
-    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-    return d;
-}
-
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
     uint32_t d;
     asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
-    return d;
-}
-
-__device__ __forceinline__ uint32_t hadd2_u32(uint32_t a, uint32_t b) {
-    uint32_t d;
-    asm("add.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-    return d;
-}
-
-__device__ __forceinline__ uint32_t hfma2_u32(uint32_t a, uint32_t b, uint32_t c) {
-    uint32_t d;
-    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
     return d;
 }
 
@@ -395,12 +290,6 @@ __device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
     uint32_t d;
     asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
     return d;
-}
-
-// Two fp16 halves packed low | high << 16.
-__device__ __forceinline__ uint32_t pack_half2(__half lo, __half hi) {
-    return static_cast<uint32_t>(__half_as_ushort(lo)) |
-           (static_cast<uint32_t>(__half_as_ushort(hi)) << 16);
 }
 
 // Two floats -> f16x2 (low half = a), rounded to nearest even, in one conversion instruction.
@@ -430,12 +319,6 @@ __device__ __forceinline__ uint64_t f32x2_sub(uint64_t a, uint64_t b) {
     asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
     return d;
 }
-__device__ __forceinline__ uint64_t f32x2_add(uint64_t a, uint64_t b) {
-    uint64_t d;
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
-
 // v = hi + lo exactly on both lanes of a pair: hi = v truncated to its leading 11 significant bits
 // (the low 13 mantissa bits cleared; exact in fp16 for 2^-14 <= |hi| < 65520), lo = v - hi
 // (exact, |lo| < 2^-10 |v|). Integer masking, so no compiler rewriting of the floating-point

@@ -2,9 +2,14 @@
 //
 // Computes Y[m][n] = sum_k w[n][k] x[m][k] for 1 <= M <= 16, with w = d * (n - z) decoded in
 // registers from the 34-byte blocks of the "PN weight format" page (sections Block layout and
-// Value) just before the multiply. The pipeline (cluster work split, weight stream, operand
-// builders, on-chip reduction) is pnq_cluster.cuh; this file is the PN format policy: a K unit is
-// 8 blocks (272 bytes of a row), one 8-row piece is one tensor-map copy.
+// Value) just before the multiply. A K unit is 8 blocks (272 bytes of a row). Two pipelines:
+//   - the row stream (M <= 4; below): each CTA owns whole rows, stages of 16 rows (or of a K
+//     segment of 16 rows) arrive by one 1-D bulk copy per row, B operands of every unit stay in
+//     shared memory;
+//   - the cluster strip pipeline (pnq_cluster.cuh, with this file's PnMma policy): 2-D tensor-map
+//     copies of 8- and 64-row strips of a unit, clusters of one or two CTAs sharing row tiles and
+//     summing through distributed shared memory; it takes M = 5..16 and the M <= 4 shapes whose B
+//     operands do not fit beside a row-stream ring.
 //
 // Decode and multiply. A 32-bit word of a block holds two codes at the same shift in its two
 // 16-bit halves; masking out one such pair leaves in each half the exact fp16 subnormal
@@ -15,16 +20,14 @@
 // 16-byte aligned row; even blocks are read as the aligned words that pair the high half of word
 // i with the low half of word i + 1 (the k order inside a block is free as long as B follows it),
 // and the one pair that straddles the block end (word 7 high, word 0 low) is joined with a PRMT.
-// Two blocks' mma chains are interleaved step by step (two accumulations in flight per warp).
+// Four blocks' mma chains are interleaved step by step (four accumulations in flight per warp).
 //
 // B operand (per K unit and activation row m): x * 2^sigma * 2^-(shift of the pair), sigma so that
 // max |x| * 2^sigma over the unit lies in [2^14, 2^15), split into fp16 hi (the leading 11 bits)
-// and lo (the remainder, rounded) in mma columns 2m and 2m + 1. Z = z * 2^(sigma - 24) * (sum of
-// the block's x) starts the accumulator of column 2m, so one block gives (c - Z) and the row sum
-// gains d * (c - Z); each unit's sums are scaled by 2^(24 - sigma) into the row partials.
-//
-// At M <= 4 (one n8 tile) a CTA uses at most ~112 KB of shared memory and 32 K registers, so the
-// next launch's CTA is resident beside it and streams its first stages meanwhile.
+// and lo (the remainder, rounded) in mma columns 2m and 2m + 1. A block's two column sums added
+// give sum_k c_k x_k * 2^(sigma - 24); minus Z = z * 2^(sigma - 24) * (sum of the block's x) and
+// times d that is the block's share of the row sum, and each unit's sums are scaled by
+// 2^(24 - sigma) into the row partials.
 #include <cuda.h>
 #include <cuda_runtime.h>
 

@@ -240,12 +240,24 @@ int pnq_quantize_nvfp4_clip(const float* w, const float* act_ms, int64_t n_rows,
  * *code = 0 when no kernel has given up on a bounded internal wait since the last call;
  * otherwise the nonzero site code of the first one (1: a consumer's wait for a weight stage or
  * for the operands of a K unit, 2: the producer's wait for a free stage, 3: the producer's final
- * wait for copies in flight, 5: a builder's wait for a free operand slot), and the call returns
+ * wait for copies in flight, 5: a builder's wait for a free operand slot, 6: pnq_selftest_wait),
+ * and the call returns
  * PNQ_ERR_DEVICE. The Y of a GEMV that gave up is unspecified; later GEMVs are unaffected (no
  * state outlives a launch). Other returns: PNQ_OK, PNQ_ERR_NULL, PNQ_ERR_CUDA. (Library
  * plumbing; the pages define no such call.)
  */
 int pnq_device_error(int32_t* code);
+
+/*
+ * pnq_selftest_wait -- exercises the failure path of the bounded waits: one thread waits, with the
+ * GEMV kernels' own bounded wait limited to limit_us microseconds (1 .. 2,000,000), on a
+ * shared-memory barrier that nothing arrives at, gives up and records site code 6 in the device
+ * error word, as a GEMV kernel records a wait that gave up. Nothing faults or hangs: the kernel
+ * returns and the context stays usable; read the code with pnq_device_error. Returns PNQ_OK,
+ * PNQ_ERR_VALUE (limit out of range) or PNQ_ERR_CUDA. (Library plumbing; the pages define no such
+ * call.)
+ */
+int pnq_selftest_wait(uint32_t limit_us, cudaStream_t stream);
 
 /* Library version string (static storage). */
 const char* pnq_version(void);

@@ -6,16 +6,25 @@ TOL_REL = 1e-5
 TOL_ABS = 1e-6
 
 
+# worst |y - y_ref| / bound seen per check (printed in the session summary by conftest)
+WORST_RATIO = {}
+
+
 def assert_within_tolerance(y, y_ref, a_ref, what=""):
-    """|y - y_ref| <= 1e-5 * sum|w x| + 1e-6, element by element (the stated GEMV bound)."""
+    """|y - y_ref| <= 1e-5 * sum|w x| + 1e-6, element by element (the stated GEMV bound).
+    Returns the worst ratio of error to bound (recorded under `what`)."""
     y = np.asarray(y, dtype=np.float64)
     err = np.abs(y - y_ref)
     bound = TOL_REL * a_ref + TOL_ABS
+    ratio = float(np.max(err / bound)) if err.size else 0.0
+    if what:
+        WORST_RATIO[what] = max(ratio, WORST_RATIO.get(what, 0.0))
     bad = ~(err <= bound)
     if bad.any():
         i = np.argwhere(bad)[0]
         raise AssertionError(f"{what}: {bad.sum()} of {bad.size} outside tolerance; first at {tuple(i)}: "
                              f"y={y[tuple(i)]!r} ref={y_ref[tuple(i)]!r} bound={bound[tuple(i)]!r}")
+    return ratio
 
 
 def device_bytes(arr: np.ndarray, offset: int = 0, device="cuda"):

@@ -195,6 +195,45 @@ def test_pn_row_segments(oracle, type_, N, U, M):
     assert_within_tolerance(run_pn(type_, W, N, K, X), Yr, Ar, f"type={type_} N={N} U={U} M={M}")
 
 
+def d_extremes(type_, N, seed):
+    """PN blocks whose d runs over every fp16 exponent field 0..30 with both signs (so subnormals,
+    the smallest and largest normals and 65504 = 0x7BFF appear), +0 and -0 over codes that are not
+    z, and random fractions; codes random."""
+    K_blocks = 8 * 4
+    W = synth.pn_random_blocks(type_, N, BLK[type_] * K_blocks, seed=seed).numpy().reshape(N, K_blocks, 34).copy()
+    rng = np.random.default_rng(seed)
+    d = np.empty((N, K_blocks), dtype=np.uint16)
+    vals = [(s << 15) | (e << 10) | f for e in range(31) for s in (0, 1) for f in (0, 1, 0x3FF, 0x155)]
+    vals += [0x0000, 0x8000, 0x0001, 0x8001, 0x03FF, 0x7BFF, 0xFBFF, 0x0400]
+    flat = d.reshape(-1)
+    for i in range(flat.size):
+        flat[i] = vals[i % len(vals)] if i < 3 * len(vals) else vals[rng.integers(len(vals))]
+    W[:, :, 0] = d & 0xFF
+    W[:, :, 1] = d >> 8
+    if type_ == pnq.PN3T:  # keep the reserved bits clear
+        W[:, :, 3] &= 0x7F
+        W[:, :, 5] &= 0x7F
+        for w in range(8):
+            W[:, :, 2 + 4 * w + 1] &= 0x7F
+            W[:, :, 2 + 4 * w + 3] &= 0x7F
+    return W.reshape(N, -1), BLK[type_] * K_blocks
+
+
+@pytest.mark.parametrize("type_", [pnq.PN3T, pnq.PN4T])
+@pytest.mark.parametrize("M", [1, 4, 16])
+def test_d_extremes(oracle, type_, M):
+    """d over the whole fp16 range ("PN weight format", section Value: w = d * (n - z) is exact in
+    fp32, a zero d gives a signed zero), on the fast path (aligned) and the generic path."""
+    N = 160
+    W, K = d_extremes(type_, N, seed=M)
+    X = synth.activations(M, K, seed=M + 10)
+    Yr, Ar = oracle.gemv(type_, W, N, K, X)
+    assert np.all(np.isfinite(Yr))
+    for offset in (0, 6):
+        Y = run_pn(type_, W, N, K, X, offset)
+        assert_within_tolerance(Y, Yr, Ar, f"d extremes type={type_} M={M} off={offset}")
+
+
 LAYER = [("gate", pnq.PN3T, 17408, 5120), ("up", pnq.PN3T, 17408, 5120), ("q", pnq.PN3T, 12288, 5120),
          ("k", pnq.PN4T, 1024, 5120), ("v", pnq.PN4T, 1024, 5120), ("o", pnq.PN4T, 5120, 6144),
          ("down", pnq.PN4T, 5120, 17408)]
