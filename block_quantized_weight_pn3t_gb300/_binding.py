@@ -92,6 +92,10 @@ def lib() -> ctypes.CDLL:
         L.pnq_quantize_nvfp4_clip.argtypes = [P, P, I64, I64, ctypes.c_float, P, P, P, P]
         L.pnq_selftest_wait.restype = I
         L.pnq_selftest_wait.argtypes = [ctypes.c_uint32, P]
+        L.pnq_gemm.restype = I
+        L.pnq_gemm.argtypes = [I, P, I64, I64, P, I64, P, P, ctypes.c_uint64, P]
+        L.pnq_gemm_scratch_bytes.restype = I
+        L.pnq_gemm_scratch_bytes.argtypes = [I, I64, I64, I64, I64, ctypes.POINTER(ctypes.c_uint64)]
         L.pnq_device_error.restype = I
         L.pnq_device_error.argtypes = [ctypes.POINTER(ctypes.c_int32)]
         L.pnq_version.restype = ctypes.c_char_p
@@ -337,3 +341,31 @@ def quantize_nvfp4_clip(w, act_ms, global_scale: float, stream=None):
                                          ctypes.c_void_p(scales.data_ptr()), ctypes.c_void_p(status.data_ptr()),
                                          ctypes.c_void_p(_stream_handle(stream))), "pnq_quantize_nvfp4_clip")
     return codes, scales, status
+
+
+def gemm_scratch_bytes(type_: int, N: int, K: int, M: int, slice_rows: int = 0) -> int:
+    out = ctypes.c_uint64(0)
+    _check(lib().pnq_gemm_scratch_bytes(type_, N, K, M, slice_rows, ctypes.byref(out)), "pnq_gemm_scratch_bytes")
+    return int(out.value)
+
+
+def gemm(type_: int, W, X, N: int, K: int, Y=None, scratch=None, slice_rows: int = 0, stream=None):
+    """Y[m][n] = sum_k W[n][k] X[m][k] for any M (prefill path, PN types). W: uint8 CUDA tensor of PN
+    blocks; X: CUDA fp32 [M][K]. scratch: a CUDA uint8 tensor of at least
+    gemm_scratch_bytes(type_, N, K, M, slice_rows) bytes (made here when None)."""
+    import torch
+    _check_weights(type_, W, N, K)
+    _require(X, "X", (torch.float32,))
+    M = X.shape[0] if X.dim() == 2 else 1
+    if X.numel() != M * K:
+        raise PnqError(f"X has shape {tuple(X.shape)}; expected [M][{K}]")
+    if Y is None:
+        Y = torch.empty((M, N), dtype=torch.float32, device=X.device)
+    _require(Y, "Y", (torch.float32,), M * N)
+    if scratch is None:
+        scratch = torch.empty((gemm_scratch_bytes(type_, N, K, M, slice_rows),), dtype=torch.uint8, device=X.device)
+    _require(scratch, "scratch", (torch.uint8,))
+    _check(lib().pnq_gemm(type_, ctypes.c_void_p(W.data_ptr()), N, K, ctypes.c_void_p(X.data_ptr()), M,
+                          ctypes.c_void_p(Y.data_ptr()), ctypes.c_void_p(scratch.data_ptr()), scratch.numel(),
+                          ctypes.c_void_p(_stream_handle(stream))), "pnq_gemm")
+    return Y

@@ -13,7 +13,7 @@ INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libpnq.so")
 BUILD_DIR = os.path.join(ROOT, "_build")
 SOURCES = ["pnq_api.cu", "pnq_codec_kernels.cu", "pnq_gemv_simt.cu", "pnq_gemv_pn.cu", "pnq_gemv_nvfp4.cu",
-           "pnq_grouped.cu", "pnq_quantize.cu"]
+           "pnq_grouped.cu", "pnq_quantize.cu", "pnq_prefill.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

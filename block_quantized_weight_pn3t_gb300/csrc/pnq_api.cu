@@ -243,6 +243,35 @@ extern "C" int pnq_gemv_noalloc(int type, const void* W, int64_t N, int64_t K, c
     return gemv_impl(type, W, N, K, X, M, Y, flags, stream);
 }
 
+extern "C" int pnq_gemm_scratch_bytes(int type, int64_t N, int64_t K, int64_t M, int64_t slice_rows,
+                                      uint64_t* bytes) {
+    if (type != PNQ_PN3T && type != PNQ_PN4T) return PNQ_ERR_TYPE;
+    if (!bytes) return PNQ_ERR_NULL;
+    const int blk = block_weights(type);
+    if (N < 0 || K <= 0 || K % blk != 0 || M < 1 || slice_rows < 0) return PNQ_ERR_SHAPE;
+    int64_t rows = slice_rows > 0 ? slice_rows : N;
+    rows = (rows + 127) / 128 * 128;
+    if (rows == 0) rows = 128;
+    if (M > INT64_MAX / 8 / K || rows > INT64_MAX / 8 / K - M) return PNQ_ERR_SHAPE;
+    *bytes = static_cast<uint64_t>(8 * K * (M + rows));
+    return PNQ_OK;
+}
+
+extern "C" int pnq_gemm(int type, const void* W, int64_t N, int64_t K, const float* X, int64_t M, float* Y,
+                        void* scratch, uint64_t scratch_bytes, cudaStream_t stream) {
+    if (type != PNQ_PN3T && type != PNQ_PN4T) return PNQ_ERR_TYPE;
+    Nvfp4View nv{};
+    const int rc = check_common(type, W, N, K, &nv);
+    if (rc != PNQ_OK) return rc;
+    if (M < 1 || M > INT32_MAX / 2 || K > INT32_MAX || N > INT32_MAX || M > INT64_MAX / 8 / K) return PNQ_ERR_SHAPE;
+    if (N == 0) return PNQ_OK;
+    if (!X || !Y || !scratch) return PNQ_ERR_NULL;
+    if (!aligned(X, 16) || !aligned(Y, 4) || !aligned(scratch, 16)) return PNQ_ERR_ALIGN;
+    if (prefill_slice_rows(N, K, M, static_cast<size_t>(scratch_bytes)) < 128) return PNQ_ERR_SCRATCH;
+    return map_cuda(launch_pn_prefill(type, static_cast<const uint8_t*>(W), N, K, X, M, Y, error_word(), scratch,
+                                      static_cast<size_t>(scratch_bytes), stream));
+}
+
 extern "C" int pnq_gemv(int type, const void* W, int64_t N, int64_t K, const void* X, int M, float* Y,
                         cudaStream_t stream) {
     return pnq_gemv_ex(type, W, N, K, X, M, Y, 0u, stream);

@@ -124,17 +124,24 @@ __global__ void __launch_bounds__(kThreads) pn_validate_kernel(const uint8_t* __
         const unsigned short* h = reinterpret_cast<const unsigned short*>(W) + row * row_halves;
         bool bad = false;
         if (VEC) {
+            // four 16-byte loads in flight per lane before any is checked
             const uint4* v = reinterpret_cast<const uint4*>(h);
-            for (int q = lane; q < row_halves / 8; q += 32) {
-                const uint4 u = __ldg(v + q);
-                const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-                int pos = (8 * q) % 17;
+            const int nq = row_halves / 8;
+            for (int q0 = lane; q0 < nq; q0 += 4 * 32) {
+                uint4 u[4];
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    bad |= bad_half(pos, w[k] & 0xFFFFu);
-                    pos = (pos == 16) ? 0 : pos + 1;
-                    bad |= bad_half(pos, w[k] >> 16);
-                    pos = (pos == 16) ? 0 : pos + 1;
+                for (int j = 0; j < 4; ++j) u[j] = (q0 + 32 * j < nq) ? __ldg(v + q0 + 32 * j) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint32_t w[4] = {u[j].x, u[j].y, u[j].z, u[j].w};
+                    int pos = (8 * (q0 + 32 * j)) % 17;  // zero words past the row are valid halves
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        bad |= bad_half(pos, w[k] & 0xFFFFu);
+                        pos = (pos == 16) ? 0 : pos + 1;
+                        bad |= bad_half(pos, w[k] >> 16);
+                        pos = (pos == 16) ? 0 : pos + 1;
+                    }
                 }
             }
         } else {

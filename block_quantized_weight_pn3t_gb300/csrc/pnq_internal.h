@@ -67,6 +67,14 @@ cudaError_t launch_pn_quantize(int type, const float* w, int64_t n_rows, int64_t
 cudaError_t launch_nvfp4_clip(const float* w, const float* act_ms, float g, int64_t n_rows, int64_t K, uint8_t* codes,
                               uint8_t* scales, int32_t* status, cudaStream_t stream);
 
+// PN products for any M on the tcgen05 tensor cores (prefill): x split into two tf32 planes, the
+// weights decoded slice by slice into two tf32 planes, three tf32 MMAs per K step (pnq_prefill.cu).
+// scratch: 8 * M * K bytes for x plus 8 * K bytes per weight row of a slice (slices of a multiple
+// of 128 rows); cudaErrorMemoryAllocation when it holds less than one 128-row slice.
+int64_t prefill_slice_rows(int64_t N, int64_t K, int64_t M, size_t scratch_bytes);
+cudaError_t launch_pn_prefill(int type, const uint8_t* W, int64_t N, int64_t K, const float* X, int64_t M, float* Y,
+                              int* err, void* scratch, size_t scratch_bytes, cudaStream_t stream);
+
 // Generic path: any 2-byte aligned PN buffer / any NVFP4 layout, CUDA-core FMA.
 cudaError_t launch_pn_gemv_simt(int type, const uint8_t* W, int64_t N, int64_t K, const float* X, int M,
                                 float* Y, cudaStream_t stream);

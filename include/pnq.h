@@ -85,7 +85,7 @@ enum pnq_status {
     PNQ_ERR_CUDA = -5,   /* a CUDA call failed (launch error, no device, bad stream) */
     PNQ_ERR_DEVICE = -6, /* a kernel gave up on an internal wait (see pnq_device_error) */
     PNQ_ERR_FLAGS = -7,  /* unknown bit in a flags argument */
-    PNQ_ERR_SCRATCH = -8, /* reserved (no entry point of this version returns it) */
+    PNQ_ERR_SCRATCH = -8, /* the caller's scratch holds less than the call needs (pnq_gemm) */
     PNQ_ERR_VALUE = -9    /* an argument value outside its domain (a global scale that is not finite
                              and > 0) */
 };
@@ -168,6 +168,29 @@ int pnq_gemv_ex(int type, const void* W, int64_t N, int64_t K, const void* X, in
  */
 int pnq_gemv_noalloc(int type, const void* W, int64_t N, int64_t K, const void* X, int M, float* Y,
                      unsigned int flags, cudaStream_t stream);
+
+/*
+ * pnq_gemm -- Y[m][n] = sum_k W[n][k] * X[m][k] for any number M >= 1 of activation rows
+ * (prefill), PN3T and PN4T, on the tcgen05 tensor cores. The prefill route of the pages (feedman.me
+ * post on BF16_P12, section "How the engine uses it": with more than 16 tokens a cache-sized piece
+ * of the weights is unpacked, then multiplied densely): the weights are decoded slice by slice into
+ * the caller's scratch as two tf32 planes (the exact decoded weight is their sum) and multiplied,
+ * with x split into two tf32 planes the same way, by three tf32 MMAs per K step accumulated in fp32.
+ *   W        device, as for pnq_gemv (>= 2-byte aligned).
+ *   X        device fp32 [M][K], 16-byte aligned.   Y: device fp32 [M][N], 4-byte aligned.
+ *   scratch  device, 16-byte aligned, scratch_bytes long: 8*M*K bytes for x plus 8*K bytes per
+ *            weight row of a slice; slices are the largest multiple of 128 rows that fits (at least
+ *            128, else PNQ_ERR_SCRATCH). pnq_gemm_scratch_bytes gives the size for a slice length.
+ *            The library allocates nothing; scratch contents are overwritten.
+ * Accuracy: the pnq_gemv bound. Errors: PNQ_ERR_TYPE (NVFP4 and grouped types have no prefill
+ * path here), PNQ_ERR_SHAPE, PNQ_ERR_NULL, PNQ_ERR_ALIGN, PNQ_ERR_SCRATCH, PNQ_ERR_CUDA.
+ */
+int pnq_gemm(int type, const void* W, int64_t N, int64_t K, const float* X, int64_t M, float* Y, void* scratch,
+             uint64_t scratch_bytes, cudaStream_t stream);
+
+/* Scratch bytes pnq_gemm needs for slices of slice_rows weight rows (rounded up to a multiple of
+ * 128; 0 = all N rows in one slice). Returns PNQ_OK, PNQ_ERR_TYPE, PNQ_ERR_SHAPE or PNQ_ERR_NULL. */
+int pnq_gemm_scratch_bytes(int type, int64_t N, int64_t K, int64_t M, int64_t slice_rows, uint64_t* bytes);
 
 /*
  * pnq_dequantize_row -- out[r][k] = the fp32 weight, bit-exact:
