@@ -25,6 +25,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
+#include <atomic>
 #include <cstdint>
 #include <mutex>
 
@@ -202,6 +204,336 @@ struct NvMma {
     }
 };
 
+// ---- row-stream path (M <= 4) ------------------------------------------------------------------
+//
+// The structure of the PN row stream (pnq_gemv_pn.cu): each CTA owns whole rows; a stage is a
+// 16-row group of one K segment (all units of a short row, or a near-equal share of a long one),
+// brought in by two 1-D bulk copies per row (its code bytes and its scale bytes), issued by two
+// producer warps; rows are `pitch` bytes apart in each region, padded so that pitch / 16 is odd
+// (the eight rows a warp reads at once then fall in different banks; no swizzle is needed). All
+// of x (bf16 [M][K]) comes in with one bulk copy per activation row; the consumer warps build the
+// B operands of every unit between them (records of the 4M lanes whose columns are live) and the
+// (row group, unit) tasks of the stages are dealt to them in turn.
+
+constexpr int kNrWarps = 8;
+constexpr int kNrProducers = 2;
+constexpr int kNrThreads = 32 * (kNrWarps + kNrProducers);
+constexpr int kNrMaxSeg = 32;
+constexpr int kNrMaxStages = 8;
+constexpr uint32_t kNrSmem = 226u * 1024u;
+constexpr int nr_pitch(int bytes) { return ((bytes / 16) & 1) ? bytes : bytes + 16; }
+
+// B operands of activation row m (m < LR / 4) for one unit, in the compact layout: slice pair P
+// at P * LR * 16, lane record (4 (m) + c) * 16 within it.
+template <int LR>
+__device__ __forceinline__ void nv_build_row_compact(uint8_t* rec, float* so, const uint16_t* xr, int m, float g,
+                                                     int lane) {
+    const uint4 xv = reinterpret_cast<const uint4*>(xr)[lane];
+    const uint32_t w[4] = {xv.x, xv.y, xv.z, xv.w};
+    uint32_t mx = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) mx = max(mx, max(w[i] & 0x7FFFu, (w[i] >> 16) & 0x7FFFu));
+    const uint32_t bits = __reduce_max_sync(0xffffffffu, mx) << 16;
+    const int E = static_cast<int>(bits >> 23);
+    int sg = (bits == 0 || E >= 255) ? 0 : 141 - E;
+    sg = min(100, max(-100, sg));
+    const float si = exp2i(sg);
+    const int P = lane >> 2, c = lane & 3;
+    const uint32_t* x32 = reinterpret_cast<const uint32_t*>(xr);
+    uint32_t v[4];
+#pragma unroll
+    for (int q4 = 0; q4 < 4; ++q4) {
+        const int S = 2 * P + (q4 >> 1), r = q4 & 1;
+        const int half = S >> 3, q = (S >> 2) & 1, b = S & 3;
+        const uint32_t pair = x32[4 * (16 * half + c + 8 * q + 4 * r) + b];
+        v[q4] = f32x2_to_f16x2(__uint_as_float(pair << 16) * si, __uint_as_float(pair & 0xFFFF0000u) * si);
+    }
+    *reinterpret_cast<uint4*>(rec + P * (LR * 16) + ((m << 2) | c) * 16) = make_uint4(v[0], v[1], v[2], v[3]);
+    if (lane == 0) so[m] = exp2i(-sg) * g;
+}
+
+// One (row group, unit) task: rows g (h = 0) and g + 8 (h = 1) at scode[h] (code bytes of the
+// unit) and sscl[h] (its 16 scale bytes); srec = the lane's B record. acc: the four accumulators
+// of the lane (rows g, g + 8 x columns 2c, 2c + 1), already summed over the unit's slices.
+template <int LR>
+__device__ __forceinline__ void nv_task(const uint32_t (&scode)[2], const uint32_t (&sscl)[2], uint32_t srec, int c,
+                                        uint32_t sel0, uint32_t sel1, float (&acc)[4]) {
+    uint32_t w[2][2][4], sc[2][2][4];
+    static_for<2>([&](auto Hh) {
+        constexpr int h = decltype(Hh)::value;
+        const uint4 s4 = ld_shared_v4<0>(sscl[h]);
+        static_for<2>([&](auto HH) {
+            constexpr int H = decltype(HH)::value;
+            static_for<4>([&](auto Jj) {
+                constexpr int j = decltype(Jj)::value;
+                w[H][h][j] = ld_shared_u32<(4 * H + j) * 16>(scode[h]);  // word c + 4j of half H (scode has + 4c)
+            });
+            const uint32_t sw0 = H ? s4.z : s4.x, sw1 = H ? s4.w : s4.y;
+            sc[H][h][0] = e4m3x2_to_f16x2(prmt(sw0, 0u, sel0));
+            sc[H][h][1] = e4m3x2_to_f16x2(prmt(sw0, 0u, sel1));
+            sc[H][h][2] = e4m3x2_to_f16x2(prmt(sw1, 0u, sel0));
+            sc[H][h][3] = e4m3x2_to_f16x2(prmt(sw1, 0u, sel1));
+        });
+    });
+    float c2[2][2][4];
+    uint4 bq[2];
+    static_for<8>([&](auto Sc) {
+        constexpr int S = decltype(Sc)::value, q = S >> 2, bt = S & 3;
+        static_for<2>([&](auto HH) {
+            constexpr int H = decltype(HH)::value;
+            if constexpr ((S & 1) == 0) bq[H] = ld_shared_v4<(4 * H + (S >> 1)) * LR * 16>(srec);
+            const uint32_t a0 = hmul2_u32(e2m1x2_to_f16x2<bt>(w[H][0][2 * q]), sc[H][0][2 * q]);
+            const uint32_t a1 = hmul2_u32(e2m1x2_to_f16x2<bt>(w[H][1][2 * q]), sc[H][1][2 * q]);
+            const uint32_t a2 = hmul2_u32(e2m1x2_to_f16x2<bt>(w[H][0][2 * q + 1]), sc[H][0][2 * q + 1]);
+            const uint32_t a3 = hmul2_u32(e2m1x2_to_f16x2<bt>(w[H][1][2 * q + 1]), sc[H][1][2 * q + 1]);
+            const uint32_t b0 = (S & 1) ? bq[H].z : bq[H].x, b1 = (S & 1) ? bq[H].w : bq[H].y;
+            if constexpr (S < 2)
+                mma_f16_16816_z(c2[H][S & 1], a0, a1, a2, a3, b0, b1);
+            else
+                mma_f16_16816(c2[H][S & 1], a0, a1, a2, a3, b0, b1);
+        });
+    });
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[i] = (c2[0][0][i] + c2[0][1][i]) + (c2[1][0][i] + c2[1][1][i]);
+}
+
+struct NrArgs {
+    const uint8_t* codes;
+    const uint8_t* scales;
+    const uint16_t* X;
+    float* Y;
+    int* err;
+    float g;
+    int N, K, M, U, G, S, nseg, rows_pad;
+    unsigned flags;
+    uint32_t off_rec, off_so, off_x, off_part, off_stage, stage_bytes, scale_region;  // scale region offset in a stage
+};
+
+template <int LR>
+__global__ void __launch_bounds__(kNrThreads, 1) nv_rows_kernel(const __grid_constant__ NrArgs a) {
+    constexpr int REC = 8 * LR * 16;  // bytes of one unit's B records
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* base = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+    const uint32_t bar0 = smem_addr(base);
+    const int S = a.S, M = a.M, U = a.U, nseg = a.nseg;
+    auto full = [&](int s) { return bar0 + 8u * s; };
+    auto empty = [&](int s) { return bar0 + 8u * (S + s); };
+    const uint32_t xfull = bar0 + 8u * (2 * S), xreq = bar0 + 8u * (2 * S + 1);
+    auto stage = [&](int s) { return base + a.off_stage + static_cast<uint32_t>(s) * a.stage_bytes; };
+    auto rec = [&](int u) { return base + a.off_rec + static_cast<uint32_t>(u) * REC; };
+    auto so = [&](int u) { return reinterpret_cast<float*>(base + a.off_so) + u * 4; };
+    __shared__ int seg_tab[kNrMaxSeg + 1];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t r0 = static_cast<int64_t>(blockIdx.x) * a.N / a.G, r1 = static_cast<int64_t>(blockIdx.x + 1) * a.N / a.G;
+    const int nrows = static_cast<int>(r1 - r0);
+    const int nstages = (nrows + kGroupRows - 1) / kGroupRows * nseg;
+    float* part = reinterpret_cast<float*>(base + a.off_part);  // [warp][m][rows_pad]
+    const int64_t crow = a.K / 2, srow_b = a.K / 16;             // code / scale bytes per row
+
+    if (threadIdx.x == 0) {
+        griddep_launch_dependents();
+        for (int s = 0; s < S; ++s) {
+            mbar_init(full(s), kNrProducers);
+            mbar_init(empty(s), kNrWarps);
+        }
+        for (int j = 0; j <= nseg; ++j) seg_tab[j] = j * U / nseg;
+        mbar_init(xfull, 1);
+        mbar_init(xreq, kNrWarps);
+        mbar_fence_init();
+    }
+    __syncthreads();
+
+    if (warp >= kNrWarps) {
+        const int pr = (warp - kNrWarps) * 8;
+        const uint64_t pol = l2_policy_evict_first();
+        if (!(a.flags & kStaticWeights)) griddep_wait();
+        bool ok = true;
+        int s = 0;
+        for (int i = 0, j = 0; s < nstages; ++s) {
+            const int slot = s % S;
+            if (s == 1 && !mbar_wait_warp(xreq, 0)) {  // x is requested before the ring fills
+                ok = false;
+                break;
+            }
+            if (s >= S && !mbar_wait_warp(empty(slot), ((s / S) - 1) & 1)) {
+                ok = false;
+                break;
+            }
+            const int mine = min(8, max(0, nrows - i * kGroupRows - pr));
+            const int u0 = seg_tab[j], n = seg_tab[j + 1] - u0;
+            const int cb = n * 128, sb = n * 16, pc = nr_pitch(cb), ps = nr_pitch(sb);
+            if (lane == 0) mbar_arrive_expect_tx(full(slot), static_cast<uint32_t>(mine * (cb + sb)));
+            __syncwarp();
+            if (lane < mine) {
+                const int64_t row = r0 + i * kGroupRows + pr + lane;
+                const uint32_t dst = smem_addr(stage(slot));
+                bulk_g2s(dst + static_cast<uint32_t>((pr + lane) * pc), a.codes + row * crow + u0 * 128,
+                         static_cast<uint32_t>(cb), full(slot), pol);
+                bulk_g2s(dst + a.scale_region + static_cast<uint32_t>((pr + lane) * ps), a.scales + row * srow_b + u0 * 16,
+                         static_cast<uint32_t>(sb), full(slot), pol);
+            }
+            if (++j == nseg) {
+                j = 0;
+                ++i;
+            }
+        }
+        if (!ok && lane == 0) record_error(a.err, kErrEmptyWait);
+        bool drained = mbar_wait_warp(xfull, 0);
+        for (int gg = max(0, s - S); drained && gg < s; ++gg) drained = mbar_wait_warp(full(gg % S), (gg / S) & 1);
+        if (!drained && lane == 0) record_error(a.err, kErrDrainWait);
+    } else {
+        const int g = lane >> 2, c = lane & 3;
+        const uint32_t sel0 = ((lane & 3) >> 1) * 0x11u, sel1 = (2 + ((lane & 3) >> 1)) * 0x11u;
+        const uint32_t boff = static_cast<uint32_t>((4 * min(g, M - 1) + c) * 16);
+        float* mine = part + warp * M * a.rows_pad;
+        for (int e = lane; e < M * a.rows_pad; e += 32) mine[e] = 0.0f;
+        const uint16_t* xs = reinterpret_cast<const uint16_t*>(base + a.off_x);  // [M][K] bf16
+        if (warp == 0) {
+            griddep_wait();  // X belongs to the previous grid until now
+            if (lane == 0) {
+                const uint32_t row = static_cast<uint32_t>(a.K) * 2u;
+                mbar_arrive_expect_tx(xfull, row * static_cast<uint32_t>(M));
+                for (int m = 0; m < M; ++m)
+                    bulk_g2s_plain(smem_addr(xs) + m * row, a.X + static_cast<size_t>(m) * a.K, row, xfull);
+            }
+            __syncwarp();
+        }
+        if (lane == 0) mbar_arrive(xreq);
+        bool ok = mbar_wait_warp(xfull, 0);
+        if (ok)
+            for (int p = warp; p < U * M; p += kNrWarps) {
+                const int u = p / M, m = p - u * M;
+                nv_build_row_compact<LR>(rec(u), so(u), xs + static_cast<size_t>(m) * a.K + u * kUnitK, m, a.g, lane);
+            }
+        named_sync(1, 32 * kNrWarps);
+        int k0 = warp;
+        for (int s = 0, i = 0, j = 0; ok && s < nstages; ++s) {
+            const int slot = s % S;
+            if (!mbar_wait_warp(full(slot), (s / S) & 1)) {
+                ok = false;
+                break;
+            }
+            const int u0 = seg_tab[j], n = seg_tab[j + 1] - u0;
+            const uint32_t pc = static_cast<uint32_t>(nr_pitch(n * 128)), ps = static_cast<uint32_t>(nr_pitch(n * 16));
+            const uint32_t st = smem_addr(stage(slot));
+            const uint32_t c0 = st + g * pc + 4u * c, s0 = st + a.scale_region + g * ps;
+            if (k0 < n) {
+                float t0 = 0.0f, t1 = 0.0f;  // rows g, g + 8 of activation row c (c < M)
+                for (int k = k0; k < n; k += kNrWarps) {
+                    const int u = u0 + k;
+                    const uint32_t scode[2] = {c0 + 128u * k, c0 + 8u * pc + 128u * k};
+                    const uint32_t sscl[2] = {s0 + 16u * k, s0 + 8u * ps + 16u * k};
+                    float acc[4];
+                    nv_task<LR>(scode, sscl, smem_addr(rec(u)) + boff, c, sel0, sel1, acc);
+                    // column 2c' + i of the mma is activation row m = ... : the live columns are m < M
+                    // (one column per row); lane c holds columns 2c and 2c + 1
+                    const float* f = so(u);
+                    if (2 * c < M) {
+                        t0 = fmaf(acc[0], f[2 * c], t0);
+                        t1 = fmaf(acc[2], f[2 * c], t1);
+                    }
+                    if (2 * c + 1 < M) {
+                        mine[(2 * c + 1) * a.rows_pad + i * kGroupRows + g] += acc[1] * f[2 * c + 1];
+                        mine[(2 * c + 1) * a.rows_pad + i * kGroupRows + g + 8] += acc[3] * f[2 * c + 1];
+                    }
+                }
+                if (2 * c < M) {
+                    mine[(2 * c) * a.rows_pad + i * kGroupRows + g] += t0;
+                    mine[(2 * c) * a.rows_pad + i * kGroupRows + g + 8] += t1;
+                }
+            }
+            k0 = (k0 - n) & (kNrWarps - 1);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty(slot));
+            if (++j == nseg) {
+                j = 0;
+                ++i;
+            }
+        }
+        if (!ok && lane == 0) record_error(a.err, kErrFullWait);
+    }
+
+    __syncthreads();
+    griddep_wait();  // Y may still be read by the previous grid
+    for (int e = threadIdx.x; e < M * nrows; e += kNrThreads) {
+        const int m = e / nrows, r = e - m * nrows;
+        float v = 0.0f;
+        for (int w = 0; w < kNrWarps; ++w) v += part[(w * M + m) * a.rows_pad + r];
+        a.Y[static_cast<size_t>(m) * a.N + r0 + r] = v;
+    }
+}
+
+// Plan: grid (one CTA per SM), segments (whole rows of at most 20 units, else segments of at most
+// 8, 6, 4 units), the deepest ring of 8..3 stages (2 as a last resort); false when nothing fits.
+template <int LR>
+bool nr_plan(int64_t N, int U, int M, int sms, NrArgs& a, uint32_t& total) {
+    constexpr int REC = 8 * LR * 16;
+    if (U < 1 || M < 1 || 4 * M > LR || (U + 3) / 4 > kNrMaxSeg) return false;
+    a.G = static_cast<int>(std::min<int64_t>(sms, N));
+    const int64_t rows_max = (N + a.G - 1) / a.G;
+    a.rows_pad = static_cast<int>((rows_max + kGroupRows - 1) / kGroupRows * kGroupRows);
+    a.off_rec = align_up(8u * (2u * kNrMaxStages + 2), 128);
+    a.off_so = align_up(a.off_rec + static_cast<uint32_t>(U) * REC, 16);
+    a.off_x = align_up(a.off_so + static_cast<uint32_t>(U) * 16u, 16);
+    a.off_part = align_up(a.off_x + static_cast<uint32_t>(M) * U * kUnitK * 2u, 16);
+    a.off_stage = align_up(a.off_part + kNrWarps * static_cast<uint32_t>(M * a.rows_pad) * 4u, 128);
+    const int cap[4] = {20, 8, 6, 4};
+    for (int s_lo : {3, 2})
+        for (int t = 0; t < 4; ++t) {
+            a.nseg = (U + cap[t] - 1) / cap[t];
+            const int longest = (U + a.nseg - 1) / a.nseg;
+            a.scale_region = align_up(static_cast<uint32_t>(kGroupRows * nr_pitch(longest * 128)), 16);
+            a.stage_bytes = align_up(a.scale_region + static_cast<uint32_t>(kGroupRows * nr_pitch(longest * 16)), 128);
+            for (int S = kNrMaxStages; S >= s_lo; --S) {
+                a.S = S;
+                total = a.off_stage + static_cast<uint32_t>(S) * a.stage_bytes;
+                if (total + 1024u <= kNrSmem) return true;
+            }
+        }
+    return false;
+}
+
+template <int LR>
+cudaError_t launch_nv_rows(const Nvfp4View& w, int64_t N, int64_t K, const uint16_t* X, int M, float* Y, int* err,
+                           bool static_weights, cudaStream_t stream) {
+    NrArgs a{};
+    uint32_t total = 0;
+    if (!nr_plan<LR>(N, static_cast<int>(K / kUnitK), M, device_sm_count(), a, total)) return cudaErrorNotSupported;
+    a.codes = w.codes;
+    a.scales = w.scales;
+    a.X = X;
+    a.Y = Y;
+    a.err = err;
+    a.g = w.g;
+    a.N = static_cast<int>(N);
+    a.K = static_cast<int>(K);
+    a.M = M;
+    a.U = static_cast<int>(K / kUnitK);
+    a.flags = static_weights ? kStaticWeights : 0u;
+    auto kern = nv_rows_kernel<LR>;
+    static std::atomic<bool> opted[64];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!opted[dev].load(std::memory_order_relaxed)) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kNrSmem));
+        if (e != cudaSuccess) return e;
+        opted[dev].store(true, std::memory_order_relaxed);
+    }
+    cudaLaunchConfig_t lc{};
+    lc.gridDim = dim3(a.G, 1, 1);
+    lc.blockDim = dim3(kNrThreads, 1, 1);
+    lc.dynamicSmemBytes = total + 1024u;
+    lc.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+    return cudaLaunchKernelEx(&lc, kern, a);
+}
+
 template <int NT>
 cudaError_t launch_nt(const CUtensorMap (&maps)[4], float g, const uint16_t* X, float* Y, int* err, int64_t N,
                       int64_t K, int M, int U, const int (&req)[3], bool static_weights, cudaStream_t stream) {
@@ -238,6 +570,14 @@ cudaError_t launch_nvfp4_gemv_mma(const Nvfp4View& w, int64_t N, int64_t K, cons
     std::call_once(once, [] { env_cluster_config("PNQ_NV_CFG", env); });
     const int req[3] = {c_req > 0 ? c_req : env[0], s_req > 0 ? s_req : env[1], env[2]};
     const int U = static_cast<int>(K / kUnitK);
+    // whole rows per CTA when every unit's B records and all of x fit beside the ring (M <= 4)
+    if (M <= 4 && c_req <= 0 && env[0] == 0 && env[1] == 0) {
+        const cudaError_t e = (M == 1)   ? launch_nv_rows<4>(w, N, K, X, M, Y, err, static_weights, stream)
+                              : (M == 2) ? launch_nv_rows<8>(w, N, K, X, M, Y, err, static_weights, stream)
+                              : (M == 3) ? launch_nv_rows<12>(w, N, K, X, M, Y, err, static_weights, stream)
+                                         : launch_nv_rows<16>(w, N, K, X, M, Y, err, static_weights, stream);
+        if (e != cudaErrorNotSupported) return e;
+    }
     if (M <= 8) return launch_nt<1>(maps, w.g, X, Y, err, N, K, M, U, req, static_weights, stream);
     return launch_nt<2>(maps, w.g, X, Y, err, N, K, M, U, req, static_weights, stream);
 }

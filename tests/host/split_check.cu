@@ -239,6 +239,52 @@ void check_rs_plan(int64_t N, int U, int M, int s_req, bool fma = false) {
     }
 }
 
+template <int LR>
+void check_nr_plan(int64_t N, int U, int M) {
+    char what[128];
+    std::snprintf(what, sizeof what, "nvfp4 rows N %lld U %d M %d", (long long)N, U, M);
+    pnq::NrArgs a{};
+    uint32_t total = 0;
+    if (!pnq::nr_plan<LR>(N, U, M, 152, a, total)) return;
+    ++plans;
+    constexpr int REC = 8 * LR * 16;
+    if (a.S < 2 || a.S > pnq::kNrMaxStages) FAIL("%d stages", a.S);
+    if (total + 1024u > pnq::kNrSmem) FAIL("total %u", total);
+    if (a.nseg < 1 || a.nseg > pnq::kNrMaxSeg) FAIL("%d segments", a.nseg);
+    struct R {
+        uint64_t lo, hi;
+        const char* name;
+    };
+    std::vector<R> r = {{0, 8ull * (2 * a.S + 2), "barriers"},
+                        {a.off_rec, a.off_rec + 1ull * U * REC, "B records"},
+                        {a.off_so, a.off_so + 16ull * U, "unit scales"},
+                        {a.off_x, a.off_x + 2ull * M * U * 256, "x"},
+                        {a.off_part, a.off_part + 4ull * pnq::kNrWarps * M * a.rows_pad, "row partials"},
+                        {a.off_stage, a.off_stage + 1ull * a.S * a.stage_bytes, "stages"}};
+    if (a.off_rec % 16 || a.off_so % 16 || a.off_x % 16 || a.off_part % 16 || a.off_stage % 128 ||
+        a.stage_bytes % 128 || a.scale_region % 16)
+        FAIL("misaligned region");
+    if (r.back().hi != total) FAIL("stages end at %llu, total %u", (unsigned long long)r.back().hi, total);
+    std::sort(r.begin(), r.end(), [](const R& x, const R& y) { return x.lo < y.lo; });
+    for (size_t k = 1; k < r.size(); ++k)
+        if (r[k].lo < r[k - 1].hi) FAIL("%s overlaps %s", r[k].name, r[k - 1].name);
+    int prev = 0;
+    for (int j = 0; j < a.nseg; ++j) {
+        const int u0 = j * U / a.nseg, u1 = (j + 1) * U / a.nseg, n = u1 - u0;
+        if (u0 != prev || n < 1) FAIL("segment %d", j);
+        prev = u1;
+        const int pc = pnq::nr_pitch(128 * n), ps = pnq::nr_pitch(16 * n);
+        if ((pc / 16) % 2 == 0 || (ps / 16) % 2 == 0) FAIL("pitch %d / %d", pc, ps);
+        if (15u * pc + 128u * n > a.scale_region) FAIL("codes of segment %d overflow", j);
+        if (a.scale_region + 15u * ps + 16u * n > a.stage_bytes) FAIL("scales of segment %d overflow", j);
+    }
+    if (prev != U) FAIL("segments end at %d", prev);
+    for (int b = 0; b < a.G; ++b) {
+        const int64_t r0 = static_cast<int64_t>(b) * N / a.G, r1 = static_cast<int64_t>(b + 1) * N / a.G;
+        if (r1 - r0 < 1 || r1 - r0 > a.rows_pad) FAIL("CTA %d rows", b);
+    }
+}
+
 template <int TYPE>
 void run_rows() {
     for (int64_t N : {1, 7, 16, 17, 151, 152, 153, 777, 1024, 5120, 12288, 17408, 151936})
@@ -280,6 +326,13 @@ int main() {
     run_type<pnq::kTypePn4t>();
     run_rows<pnq::kTypePn3t>();
     run_rows<pnq::kTypePn4t>();
+    for (int64_t N : {1, 9, 151, 152, 1000, 5120, 17408, 151936})
+        for (int U : {1, 2, 4, 20, 21, 40, 68, 100}) {
+            check_nr_plan<4>(N, U, 1);
+            check_nr_plan<8>(N, U, 2);
+            check_nr_plan<12>(N, U, 3);
+            check_nr_plan<16>(N, U, 4);
+        }
     if (failures) return 1;
     std::printf("ok %ld plans, %ld splits\n", plans, splits);
     return 0;
