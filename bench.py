@@ -120,7 +120,7 @@ class ClockSampler:
 
 def kernel_source_digest():
     h = hashlib.sha256()
-    for fn in ("pnq_gemv_pn.cu", "pnq_split.cuh", "pnq_device.cuh"):
+    for fn in ("pnq_gemv_pn.cu", "pnq_cluster.cuh", "pnq_split.cuh", "pnq_device.cuh"):
         with open(os.path.join(ROOT, "block_quantized_weight_pn3t_gb300", "csrc", fn), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -535,7 +535,9 @@ def run_ours(args):
                            hbm_fraction=round(value / world / peak, 4)),
             "roofline": {"bound": "hbm", "achieved": round(dom_gbs, 2), "peak": peak, "unit": "GB/s",
                          "frac": round(dom_gbs / peak, 4), "traffic": traffic,
-                         "kernel": f"pn_gemv_kernel<pn3t, NT={min(4, 1 << ((2 * M + 7) // 8 - 1).bit_length())}>", "launches": len(dom),
+                         "kernel": ("pn_rows_kernel<pn3t> (row stream, mma.sync decode)" if M <= 4 else
+                                    f"cluster_gemv_kernel<PnMma<pn3t, NT={min(4, 1 << ((2 * M + 7) // 8 - 1).bit_length())}>> "
+                                    "(strip pipeline)"), "launches": len(dom),
                          "algorithmic_bytes_per_launch": round(dom_bytes / len(dom)),
                          "avg_launch_us": round(sum(dur_ms) / len(dur_ms) * 1e3, 3),
                          "timing": f"graph of the step's {len(dom)} pn3t launches replayed back to back, "
@@ -606,6 +608,65 @@ def run_single(args):
                       "weight_bytes": N * row_bytes(t, K), "device_error": err}))
     if err:
         raise SystemExit(1)
+
+
+PREFILL_SHAPES = [("ffn_gate", PN3T, 17408, 5120), ("ffn_down", PN4T, 5120, 17408)]
+
+
+def run_prefill(args):
+    """The prefill path (pnq_gemm, any M, tcgen05 tf32 splits) on the gate and down shapes at M = 64
+    and 512: one JSON line each. Time = mean of CUDA events around one replay of a graph of
+    `--steps` back-to-back calls (scratch sized for the whole matrix, allocated once, outside the
+    timed region), after `--warmup` calls. useful TFLOP/s counts 2 M N K; the MMAs execute three
+    times that (hi x hi, hi x lo, lo x hi), against tf32 tensor throughput = the measured bf16
+    peak x the nominal tf32 / bf16 ratio (1.1 / 2.25)."""
+    import block_quantized_weight_pn3t_gb300 as pnq
+    from block_quantized_weight_pn3t_gb300 import synth
+    torch.cuda.set_device(0)
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            bf16 = float(json.load(f)["bf16_tflops"])
+        bf16_kind = "measured"
+    except Exception:
+        bf16, bf16_kind = 1900.0, "fallback"
+    tf32 = bf16 * 1.1 / 2.25
+    for name, t, N, K in PREFILL_SHAPES:
+        W = synth.pn_random_blocks(t, N, K, seed=SEED, device="cuda")
+        for M in (64, 512):
+            X = torch.from_numpy(synth.activations(M, K, seed=1)).cuda()
+            Y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+            scratch = torch.empty((pnq.gemm_scratch_bytes(t, N, K, M),), dtype=torch.uint8, device="cuda")
+            side = torch.cuda.Stream()
+            side.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(side):
+                for _ in range(args.warmup):
+                    pnq.gemm(t, W, X, N, K, Y=Y, scratch=scratch)
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=side):
+                for _ in range(args.steps):
+                    pnq.gemm(t, W, X, N, K, Y=Y, scratch=scratch)
+            g.replay()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            g.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            err = pnq.device_error()
+            us = e0.elapsed_time(e1) * 1e3 / args.steps
+            useful = 2.0 * M * N * K / (us * 1e-6) / 1e12
+            print(json.dumps({"op": "prefill_gemm", "projection": name, "type": "pn3t" if t == PN3T else "pn4t",
+                              "N": N, "K": K, "M": M, "calls": args.steps, "us_per_call": round(us, 2),
+                              "useful_tflops": round(useful, 1), "mma_tflops": round(3 * useful, 1),
+                              "bound": "tensor", "peak": round(tf32, 1), "unit": "TFLOP/s",
+                              "frac": round(3 * useful / tf32, 4),
+                              "peak_source": f"MEASURED_PEAKS.json bf16_tflops x 1.1/2.25 ({bf16_kind})",
+                              "includes": "x split, slice decode to two tf32 planes, GEMM", "device_error": err}),
+                  flush=True)
+            del g, scratch
+        del W
+        torch.cuda.empty_cache()
 
 
 CODEC_SHAPES = [(PN4T, 5120, 17408), (PN3T, 17408, 5120), (NVFP4, 17408, 5120)]
@@ -697,6 +758,8 @@ def main():
     ap.add_argument("--layers", type=int, default=64)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-singles", action="store_true", help="skip the single-GEMV lines of the JSON line")
+    ap.add_argument("--prefill", action="store_true",
+                    help="time the prefill path (pnq_gemm) on the gate and down shapes at M = 64 and 512")
     ap.add_argument("--codec", action="store_true",
                     help="time dequantize and validate on the full-size shapes and exit")
     ap.add_argument("--single", default=None,
@@ -706,6 +769,8 @@ def main():
         raise SystemExit("--warmup must be >= 3")
     if args.codec:
         run_codec(args)
+    elif args.prefill:
+        run_prefill(args)
     elif args.single:
         run_single(args)
     elif args.impl == "reference":
