@@ -408,12 +408,15 @@ def run_ours(args):
     # the previous one finishes (x is still read only after it completes)
     flags = pnq.GEMV_STATIC_WEIGHTS
 
-    def step(s):
-        h = s.cuda_stream
-        for t, w, N, K, x, y in calls:
+    def issue(seq, h):
+        """The GEMVs of seq, in order, on stream handle h."""
+        for t, w, N, K, x, y in seq:
             rc = pnq.gemv_ex_ptr(t, w, N, K, x, M, y, flags, h)
             if rc != 0:
                 raise pnq.PnqError("pnq_gemv", rc)
+
+    def step(s):
+        issue(calls, s.cuda_stream)
 
     # eager warm-up (sets kernel attributes once), then capture one step in a graph
     with torch.cuda.stream(stream):
@@ -478,10 +481,7 @@ def run_ours(args):
     dom = [(t, w, N, K, x, y) for (t, w, N, K, x, y) in calls if t == PN3T]
 
     def dom_launches(h):
-        for t, w, N, K, x, y in dom:
-            rc = pnq.gemv_ex_ptr(t, w, N, K, x, M, y, flags, h)
-            if rc != 0:
-                raise pnq.PnqError("pnq_gemv", rc)
+        issue(dom, h)
 
     gdom = torch.cuda.CUDAGraph()
     with torch.cuda.graph(gdom, stream=stream):
@@ -509,10 +509,7 @@ def run_ours(args):
         sub = calls[p::len(PROJECTIONS)]
 
         def launch(h, sub=sub):
-            for t_, w, N_, K_, x, y in sub:
-                rc = pnq.gemv_ex_ptr(t_, w, N_, K_, x, M, y, flags, h)
-                if rc != 0:
-                    raise pnq.PnqError("pnq_gemv", rc)
+            issue(sub, h)
 
         us = graph_us_per_launch(launch, len(sub), stream, reps=max(3, args.steps // 20), warmup=args.warmup)
         gbs = N * row_bytes(t, K) / (us * 1e-6) / 1e9

@@ -387,7 +387,6 @@ constexpr int kRsMaxSeg = 32;      // segments of a row at most
 constexpr int kRsZs = 4;           // activation rows of the zero-point table (M <= 4)
 constexpr int kRsZb = kUnitBlocks * kRsZs + kRsZs;  // floats per unit: terms [block][m], then 2^(24 - sigma) [m]
 constexpr uint32_t kRsConsumerBar = 1;              // named barrier of the consumer warps
-constexpr int kRsXAhead = 1;                        // weight stages issued before x is requested
 
 // Stage pitch of a row (segment) of `bytes` (a multiple of 16): the least multiple of 16 >= bytes
 // whose quotient by 16 is odd.
@@ -404,6 +403,8 @@ struct RsArgs {
     int rows_pad;          // partial rows per (warp, activation row), >= any CTA's rows
     unsigned flags;
     uint32_t off_rec, off_zb, off_x, off_part, off_stage, stage_bytes;
+    int x_slot0;  // first ring slot that holds x until the operands are built (S: x has its own region)
+    int x_ahead;  // weight stages issued before the producer waits for every warp's x request
 };
 
 // CUDA-core decode of one (row group, unit) task: the lane's row (srow: the row at the unit's
@@ -458,6 +459,7 @@ __global__ void __launch_bounds__(kRsThreads, 1) pn_rows_kernel(const __grid_con
     auto empty = [&](int s) { return bar0 + 8u * (S + s); };
     const uint32_t xfull = bar0 + 8u * (2 * S);      // all of x has landed (SEG)
     const uint32_t xreq = bar0 + 8u * (2 * S + 1);   // every consumer warp has requested its x
+    const uint32_t xdone = bar0 + 8u * (2 * S + 2);  // every consumer warp has built its operands (x is dead)
     auto stage = [&](int s) { return base + a.off_stage + static_cast<uint32_t>(s) * a.stage_bytes; };
     auto rec = [&](int u) { return base + a.off_rec + static_cast<uint32_t>(u) * C::REC; };
     auto zbu = [&](int u) { return reinterpret_cast<float*>(base + a.off_zb) + u * kRsZb; };
@@ -480,6 +482,7 @@ __global__ void __launch_bounds__(kRsThreads, 1) pn_rows_kernel(const __grid_con
             mbar_init(xfull, 1);
         }
         mbar_init(xreq, active);
+        mbar_init(xdone, active);
         mbar_fence_init();
     }
     __syncthreads();
@@ -493,11 +496,15 @@ __global__ void __launch_bounds__(kRsThreads, 1) pn_rows_kernel(const __grid_con
         int s = 0;
         for (int i = 0, j = 0; s < nstages; ++s) {
             const int slot = s % S;
-            if (s == kRsXAhead && !mbar_wait_warp(xreq, 0)) {
+            if (s == a.x_ahead && !mbar_wait_warp(xreq, 0)) {
                 ok = false;
                 break;
             }
             if (s >= S && !mbar_wait_warp(empty(slot), ((s / S) - 1) & 1)) {
+                ok = false;
+                break;
+            }
+            if (s == a.x_slot0 && s < S && !mbar_wait_warp(xdone, 0)) {  // x lives in this slot until then
                 ok = false;
                 break;
             }
@@ -578,6 +585,7 @@ __global__ void __launch_bounds__(kRsThreads, 1) pn_rows_kernel(const __grid_con
             }
             cp_async_wait<0>();
             __syncwarp();
+            if (lane == 0) mbar_arrive(xdone);
             for (int i = 0; i < nstages; ++i) {
                 const int slot = i % S;
                 if (!mbar_wait_warp(full(slot), (i / S) & 1)) {
@@ -617,6 +625,8 @@ __global__ void __launch_bounds__(kRsThreads, 1) pn_rows_kernel(const __grid_con
                     build_row<TYPE, 1, LR, kRsZs>(rec(u), zbu(u), zbu(u) + kUnitBlocks * kRsZs,
                                                   xs + static_cast<size_t>(m) * a.K + u * C::UK, m, lane);
                 }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(xdone);
             named_sync(kRsConsumerBar, 32 * kRsWarps);  // every unit's operands are built
             int k0 = warp;  // the warp's first task of the next stage (tasks of a stage: its units in order)
             for (int s = 0, i = 0, j = 0; ok && s < nstages; ++s) {
@@ -671,17 +681,19 @@ __global__ void __launch_bounds__(kRsThreads, 1) pn_rows_kernel(const __grid_con
 }
 
 struct RsPlan {
-    int G = 0, S = 0, nseg = 0, rows_pad = 0, pitch = 0;
+    int G = 0, S = 0, nseg = 0, rows_pad = 0, pitch = 0, x_slot0 = 0;
     uint32_t off_rec = 0, off_zb = 0, off_x = 0, off_part = 0, off_stage = 0, stage_bytes = 0, total = 0;
 };
 
 // Grid (one CTA per SM, or one per row when there are fewer rows), segments per row and the ring
-// of stages. Rows of at most 16 units stay whole (per-warp x buffers), with the deepest ring of
-// 8..2 stages that fits. Longer rows are cut into segments of at most 8, 6 then 4 units (all of x
-// staged), the first with a ring of 8..3 stages, then 2 as a last resort. The CUDA-core decode
-// (fma) keeps no B operands and stages all of x. False when nothing fits.
+// of stages. Rows of at most 16 units stay whole (per-warp x buffers); longer rows are cut into
+// segments of at most 8, 6 then 4 units (all of x staged). x is read only while the operands are
+// built, so it may sit in the ring's last slots (slot 2 or later), which the producer fills only
+// once every warp has built: of the two layouts, x apart or x in the ring, the one with the deeper
+// ring is taken (8..3 stages, then 2 as a last resort). The CUDA-core decode (fma) keeps no B
+// operands and reads x throughout, so its x has a region of its own. False when nothing fits.
 template <int TYPE, int LR>
-bool rs_plan(int64_t N, int U, int M, int sms, int s_req, RsPlan& p, bool fma = false) {
+bool rs_plan(int64_t N, int U, int M, int sms, int s_req, RsPlan& p, bool fma = false, bool x_in_ring = true) {
     using C = Cfg<TYPE, 1, LR>;
     if (U < 1 || M < 1 || M > kRsZs || (U + 3) / 4 > kRsMaxSeg) return false;
     p.G = static_cast<int>(std::min<int64_t>(sms, N));
@@ -689,25 +701,37 @@ bool rs_plan(int64_t N, int U, int M, int sms, int s_req, RsPlan& p, bool fma = 
     p.rows_pad = static_cast<int>((rows_max + kGroupRows - 1) / kGroupRows * kGroupRows);
     const bool whole = U <= kRsWholeUnits;
     const uint32_t nrec = fma ? 0u : static_cast<uint32_t>(U);
-    p.off_rec = align_up(8u * (2u * kMaxStages + 2), 128);
+    p.off_rec = align_up(8u * (2u * kMaxStages + 3), 128);
     p.off_zb = align_up(p.off_rec + nrec * C::REC, 16);
-    p.off_x = align_up(p.off_zb + nrec * kRsZb * 4u, 16);
+    p.off_part = align_up(p.off_zb + nrec * kRsZb * 4u, 16);
+    const uint32_t part_end = p.off_part + kRsWarps * static_cast<uint32_t>(M * p.rows_pad) * 4u;
     const uint32_t xbytes =
         (whole && !fma) ? kRsWarps * 2u * C::UK * 4u : static_cast<uint32_t>(M) * U * C::UK * 4u;
-    p.off_part = align_up(p.off_x + xbytes, 16);
-    p.off_stage = align_up(p.off_part + kRsWarps * static_cast<uint32_t>(M * p.rows_pad) * 4u, 128);
+    const uint32_t sep_x = align_up(part_end, 16), sep_stage = align_up(sep_x + xbytes, 128);
+    const uint32_t ovl_stage = align_up(part_end, 128);
     const int cap[3] = {8, 6, 4};
+    const int s_hi = s_req > 0 ? s_req : 8;
     for (int s_lo : {3, 2})
         for (int t = 0; t < (whole ? 1 : 3); ++t) {
             p.nseg = whole ? 1 : (U + cap[t] - 1) / cap[t];
             const int longest = (U + p.nseg - 1) / p.nseg;
             p.pitch = rs_pitch(longest * kUnitBytes);
             p.stage_bytes = align_up(static_cast<uint32_t>(kGroupRows * p.pitch), 128);
-            for (int S = (s_req > 0 ? s_req : 8); S >= (s_req > 0 ? s_req : s_lo); --S) {
-                p.S = S;
-                p.total = p.off_stage + static_cast<uint32_t>(S) * p.stage_bytes;
-                if (S <= kMaxStages && p.total + 1024u <= kSmemOne) return true;
-            }
+            const int nx = static_cast<int>((xbytes + p.stage_bytes - 1) / p.stage_bytes);
+            const int lo = s_req > 0 ? s_req : s_lo;
+            int s_sep = 0, s_ovl = 0;
+            for (int S = std::min(s_hi, kMaxStages); S >= lo && s_sep == 0; --S)
+                if (sep_stage + static_cast<uint32_t>(S) * p.stage_bytes + 1024u <= kSmemOne) s_sep = S;
+            for (int S = std::min(s_hi, kMaxStages); S >= lo && s_ovl == 0 && !fma && x_in_ring; --S)
+                if (S - nx >= 2 && ovl_stage + static_cast<uint32_t>(S) * p.stage_bytes + 1024u <= kSmemOne) s_ovl = S;
+            if (s_sep == 0 && s_ovl == 0) continue;
+            const bool ovl = s_ovl > s_sep;
+            p.S = ovl ? s_ovl : s_sep;
+            p.off_stage = ovl ? ovl_stage : sep_stage;
+            p.x_slot0 = ovl ? p.S - nx : p.S;
+            p.off_x = ovl ? p.off_stage + static_cast<uint32_t>(p.x_slot0) * p.stage_bytes : sep_x;
+            p.total = p.off_stage + static_cast<uint32_t>(p.S) * p.stage_bytes;
+            return true;
         }
     return false;
 }
@@ -740,9 +764,10 @@ cudaError_t launch_rows_kernel(const RsArgs& a, const RsPlan& p, cudaStream_t st
 
 template <int TYPE, int LR>
 cudaError_t launch_rows(const uint8_t* W, const float* X, float* Y, int* err, int64_t N, int64_t K, int M, int U,
-                        int row_bytes, int s_req, bool static_weights, bool fma, cudaStream_t stream) {
+                        int row_bytes, int s_req, bool static_weights, bool fma, int x_ahead, bool x_in_ring,
+                        cudaStream_t stream) {
     RsPlan p;
-    if (!rs_plan<TYPE, LR>(N, U, M, device_sm_count(), s_req, p, fma)) return cudaErrorNotSupported;
+    if (!rs_plan<TYPE, LR>(N, U, M, device_sm_count(), s_req, p, fma, x_in_ring)) return cudaErrorNotSupported;
     RsArgs a{};
     a.W = W;
     a.X = X;
@@ -765,18 +790,21 @@ cudaError_t launch_rows(const uint8_t* W, const float* X, float* Y, int* err, in
     a.off_part = p.off_part;
     a.off_stage = p.off_stage;
     a.stage_bytes = p.stage_bytes;
+    a.x_slot0 = p.x_slot0;
+    a.x_ahead = x_ahead;
     if (fma) return launch_rows_kernel<TYPE, LR, true, true>(a, p, stream);
     return p.nseg > 1 ? launch_rows_kernel<TYPE, LR, true>(a, p, stream) : launch_rows_kernel<TYPE, LR, false>(a, p, stream);
 }
 
 template <int TYPE>
 cudaError_t launch_rows_typed(const uint8_t* W, const float* X, float* Y, int* err, int64_t N, int64_t K, int M,
-                              int U, int row_bytes, int s_req, bool static_weights, bool fma, cudaStream_t stream) {
+                              int U, int row_bytes, int s_req, bool static_weights, bool fma, int xa, bool xr,
+                              cudaStream_t stream) {
     switch (M) {
-        case 1: return launch_rows<TYPE, 8>(W, X, Y, err, N, K, M, U, row_bytes, s_req, static_weights, fma, stream);
-        case 2: return launch_rows<TYPE, 16>(W, X, Y, err, N, K, M, U, row_bytes, s_req, static_weights, fma, stream);
-        case 3: return launch_rows<TYPE, 24>(W, X, Y, err, N, K, M, U, row_bytes, s_req, static_weights, fma, stream);
-        case 4: return launch_rows<TYPE, 32>(W, X, Y, err, N, K, M, U, row_bytes, s_req, static_weights, fma, stream);
+        case 1: return launch_rows<TYPE, 8>(W, X, Y, err, N, K, M, U, row_bytes, s_req, static_weights, fma, xa, xr, stream);
+        case 2: return launch_rows<TYPE, 16>(W, X, Y, err, N, K, M, U, row_bytes, s_req, static_weights, fma, xa, xr, stream);
+        case 3: return launch_rows<TYPE, 24>(W, X, Y, err, N, K, M, U, row_bytes, s_req, static_weights, fma, xa, xr, stream);
+        case 4: return launch_rows<TYPE, 32>(W, X, Y, err, N, K, M, U, row_bytes, s_req, static_weights, fma, xa, xr, stream);
         default: return cudaErrorNotSupported;
     }
 }
@@ -821,20 +849,23 @@ cudaError_t launch_pn_gemv_mma(int type, const uint8_t* W, int64_t N, int64_t K,
     if (!encode_u32_map(&map[0], W, N, nb * kBlockBytes / 4, kUnitU32, kPieceRows) ||
         !encode_u32_map(&map[1], W, N, nb * kBlockBytes / 4, kUnitU32, kStageRows))
         return cudaErrorNotSupported;
-    // PNQ_PN_CFG = "CTAs per cluster, stages, CTAs per SM, path (1 rows, 2 strips), decode (1 CUDA-core FMA)"
-    static int env[5];
+    // PNQ_PN_CFG = "CTAs per cluster, stages, CTAs per SM, path (1 rows, 2 strips), decode (1 CUDA-core FMA),
+    // row stream: weight stages issued before x is requested (0: 1), x apart from the ring (1)"
+    static int env[7];
     static std::once_flag once;
     std::call_once(once, [] { env_cluster_config("PNQ_PN_CFG", env); });
     const int req[3] = {c_req > 0 ? c_req : env[0], s_req > 0 ? s_req : env[1], env[2]};
     // whole rows per CTA when the B operands of every unit fit beside the stages (M <= 4)
     const int row_bytes = static_cast<int>(nb * kBlockBytes);
     const bool fma = env[4] == 1;
+    const int x_ahead = env[5] > 0 ? env[5] : 1;
+    const bool x_in_ring = env[6] != 1;
     if (env[3] != 2 && M <= 4 && c_req <= 0) {
         const cudaError_t e = (type == kTypePn3t)
                                   ? launch_rows_typed<kTypePn3t>(W, X, Y, err, N, K, M, static_cast<int>(U), row_bytes,
-                                                                 req[1], static_weights, fma, stream)
+                                                                 req[1], static_weights, fma, x_ahead, x_in_ring, stream)
                                   : launch_rows_typed<kTypePn4t>(W, X, Y, err, N, K, M, static_cast<int>(U), row_bytes,
-                                                                 req[1], static_weights, fma, stream);
+                                                                 req[1], static_weights, fma, x_ahead, x_in_ring, stream);
         if (e != cudaErrorNotSupported || env[3] == 1 || fma) return e;
     }
     return (type == kTypePn3t)

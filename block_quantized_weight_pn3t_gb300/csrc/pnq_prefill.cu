@@ -60,37 +60,66 @@ __global__ void __launch_bounds__(256) split_x_kernel(const float4* __restrict__
     }
 }
 
-// Rows [r0, r0 + rows) of the PN matrix -> w_hi, w_lo planes [rows][K]; one thread per block,
-// 16-bit loads (a block may start on any even byte), float4 stores (BLK is a multiple of 4).
-template <int TYPE>
-__global__ void __launch_bounds__(256) decode_slice_kernel(const uint8_t* __restrict__ W, int64_t r0, int64_t rows,
-                                                           int64_t nb, float* __restrict__ hi, float* __restrict__ lo) {
+// A slice of consecutive PN blocks (whole rows) -> w_hi, w_lo planes in the same element order.
+// A warp takes 32 blocks at a time (1088 bytes): it stages them in shared memory (16-byte loads
+// when the chunk is 16-byte aligned, 16-bit loads otherwise), then lane l decodes elements
+// 4j .. 4j + 3 (one block: BLK is a multiple of 4) for j = l, l + 32, .. and writes one float4 to
+// each plane, so every warp store covers 512 contiguous bytes.
+constexpr int kSliceChunk = 32;
+constexpr int kSliceChunkBytes = kSliceChunk * kBlockBytes;  // 1088 = 68 * 16
+
+template <int TYPE, bool VEC>
+__global__ void __launch_bounds__(256) decode_slice_kernel(const uint8_t* __restrict__ W, int64_t nblocks,
+                                                           float* __restrict__ hi, float* __restrict__ lo) {
     using F = PnFmt<TYPE>;
-    const int64_t total = rows * nb;
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total; i += stride) {
-        const int64_t r = i / nb, b = i - r * nb;
-        const unsigned short* h = reinterpret_cast<const unsigned short*>(W + ((r0 + r) * nb + b) * kBlockBytes);
-        const float d = __half2float(__ushort_as_half(__ldg(h)));
-        float* oh = hi + r * nb * F::BLK + b * F::BLK;
-        float* ol = lo + r * nb * F::BLK + b * F::BLK;
-#pragma unroll
-        for (int w = 0; w < 8; ++w) {
-            const uint32_t word = __ldg(h + 1 + 2 * w) | (static_cast<uint32_t>(__ldg(h + 2 + 2 * w)) << 16);
-            float v[F::CPW];
-#pragma unroll
-            for (int t = 0; t < F::CPW; ++t) {
-                const int n = static_cast<int>((word >> (F::BITS * (t >> 1) + 16 * (t & 1))) & ((1u << F::BITS) - 1u));
-                v[t] = d * static_cast<float>(n - F::Z);  // exact in fp32
-            }
-#pragma unroll
-            for (int t = 0; t < F::CPW; t += 2) {
-                const float2 wh = make_float2(tf32_hi(v[t]), tf32_hi(v[t + 1]));
-                reinterpret_cast<float2*>(oh + w * F::CPW)[t / 2] = wh;
-                reinterpret_cast<float2*>(ol + w * F::CPW)[t / 2] = make_float2(v[t] - wh.x, v[t + 1] - wh.y);
-            }
+    __shared__ __align__(16) uint8_t stage[8][kSliceChunkBytes];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    uint8_t* sb = stage[warp];
+    const int64_t nchunks = (nblocks + kSliceChunk - 1) / kSliceChunk;
+    const int64_t wstride = static_cast<int64_t>(gridDim.x) * 8;
+    for (int64_t ch = static_cast<int64_t>(blockIdx.x) * 8 + warp; ch < nchunks; ch += wstride) {
+        const int64_t left = nblocks - ch * kSliceChunk;
+        const int nblk = left < kSliceChunk ? static_cast<int>(left) : kSliceChunk;
+        const uint8_t* src = W + ch * kSliceChunkBytes;
+        if (VEC && nblk == kSliceChunk) {
+            for (int q = lane; q < kSliceChunkBytes / 16; q += 32)
+                reinterpret_cast<uint4*>(sb)[q] = __ldg(reinterpret_cast<const uint4*>(src) + q);
+        } else {
+            for (int q = lane; q < nblk * kBlockBytes / 2; q += 32)
+                reinterpret_cast<unsigned short*>(sb)[q] = __ldg(reinterpret_cast<const unsigned short*>(src) + q);
         }
+        __syncwarp();
+        const int nvec = nblk * F::BLK / 4;
+        float4* oh = reinterpret_cast<float4*>(hi + ch * kSliceChunk * F::BLK);
+        float4* ol = reinterpret_cast<float4*>(lo + ch * kSliceChunk * F::BLK);
+        for (int j = lane; j < nvec; j += 32) {
+            const int blk = (4 * j) / F::BLK, e0 = 4 * j - blk * F::BLK;
+            const uint8_t* bp = sb + blk * kBlockBytes;
+            const float d = __half2float(__ushort_as_half(*reinterpret_cast<const unsigned short*>(bp)));
+            float v[4], h[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int e = e0 + q, w = e / F::CPW, t = e - w * F::CPW;
+                const uint32_t half = *reinterpret_cast<const unsigned short*>(bp + 2 + 4 * w + 2 * (t & 1));
+                const int n = static_cast<int>((half >> (F::BITS * (t >> 1))) & ((1u << F::BITS) - 1u));
+                v[q] = d * static_cast<float>(n - F::Z);  // exact in fp32
+                h[q] = tf32_hi(v[q]);
+            }
+            oh[j] = make_float4(h[0], h[1], h[2], h[3]);
+            ol[j] = make_float4(v[0] - h[0], v[1] - h[1], v[2] - h[2], v[3] - h[3]);
+        }
+        __syncwarp();
     }
+}
+
+template <int TYPE>
+void launch_decode_slice(const uint8_t* W, int64_t nblocks, float* hi, float* lo, int sms, cudaStream_t stream) {
+    const int64_t chunks = (nblocks + kSliceChunk - 1) / kSliceChunk;
+    const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>((chunks + 7) / 8, int64_t(sms) * 8)));
+    if (reinterpret_cast<uintptr_t>(W) % 16 == 0)
+        decode_slice_kernel<TYPE, true><<<grid, 256, 0, stream>>>(W, nblocks, hi, lo);
+    else
+        decode_slice_kernel<TYPE, false><<<grid, 256, 0, stream>>>(W, nblocks, hi, lo);
 }
 
 // Shared-memory matrix descriptor, K-major with the 128-byte swizzle (rows of 128 bytes, 8-row
@@ -297,12 +326,11 @@ cudaError_t launch_pn_prefill(int type, const uint8_t* W, int64_t N, int64_t K, 
         return cudaErrorInvalidValue;
     for (int64_t n0 = 0; n0 < N; n0 += rows) {
         const int64_t rr = std::min(rows, N - n0);
-        const int64_t nblocks = rr * nb;
-        const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>((nblocks + 255) / 256, int64_t(sms) * 16)));
+        const uint8_t* ws = W + n0 * nb * kBlockBytes;  // the slice's first block
         if (type == kTypePn3t)
-            decode_slice_kernel<kTypePn3t><<<grid, 256, 0, stream>>>(W, n0, rr, nb, wh, wl);
+            launch_decode_slice<kTypePn3t>(ws, rr * nb, wh, wl, sms, stream);
         else
-            decode_slice_kernel<kTypePn4t><<<grid, 256, 0, stream>>>(W, n0, rr, nb, wh, wl);
+            launch_decode_slice<kTypePn4t>(ws, rr * nb, wh, wl, sms, stream);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
         if (!encode_u32_map(&maps[0], wh, rr, K, kTK, kTM, true) || !encode_u32_map(&maps[1], wl, rr, K, kTK, kTM, true))

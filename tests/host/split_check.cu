@@ -185,16 +185,28 @@ void check_rs_plan(int64_t N, int U, int M, int s_req, bool fma = false) {
     if (whole && p.pitch != pnq::rs_pitch(U * pnq::kUnitBytes)) FAIL("whole-row pitch %d", p.pitch);
     const uint64_t xbytes = (whole && !fma) ? 4ull * pnq::kRsWarps * 2 * C::UK : 4ull * M * U * C::UK;
     const uint64_t nrec = fma ? 0 : U;
-    std::vector<R> r = {{0, 8ull * (2 * p.S + 2), "barriers"},
+    // x either has a region of its own or lies in the ring's slots [x_slot0, S), slot 2 or later
+    // (the producer fills those only after every warp has built its operands)
+    const bool x_in_ring = p.x_slot0 < p.S;
+    if (x_in_ring) {
+        if (fma) FAIL("x in the ring with the CUDA-core decode");
+        if (p.x_slot0 < 2) FAIL("x in slot %d", p.x_slot0);
+        if (p.off_x != p.off_stage + 1ull * p.x_slot0 * p.stage_bytes ||
+            p.off_x + xbytes > p.off_stage + 1ull * p.S * p.stage_bytes)
+            FAIL("x [%u, +%llu) outside slots %d..%d", p.off_x, (unsigned long long)xbytes, p.x_slot0, p.S);
+    } else if (p.x_slot0 != p.S) {
+        FAIL("x slot %d of %d stages", p.x_slot0, p.S);
+    }
+    std::vector<R> r = {{0, 8ull * (2 * p.S + 3), "barriers"},
                         {p.off_rec, p.off_rec + nrec * C::REC, "B operands"},
                         {p.off_zb, p.off_zb + 4ull * nrec * pnq::kRsZb, "zero-point terms"},
-                        {p.off_x, p.off_x + xbytes, "x rows"},
                         {p.off_part, p.off_part + 4ull * pnq::kRsWarps * M * p.rows_pad, "row partials"},
                         {p.off_stage, p.off_stage + 1ull * p.S * p.stage_bytes, "stages"}};
+    if (!x_in_ring) r.push_back({p.off_x, p.off_x + xbytes, "x rows"});
     if (p.off_rec % 16 || p.off_zb % 16 || p.off_x % 16 || p.off_part % 16 || p.off_stage % 128 ||
         p.stage_bytes % 128)
         FAIL("misaligned region");
-    if (r.back().hi != p.total) FAIL("stages end at %llu, total %u", (unsigned long long)r.back().hi, p.total);
+    if (p.off_stage + 1ull * p.S * p.stage_bytes != p.total) FAIL("stages end before the total %u", p.total);
     std::sort(r.begin(), r.end(), [](const R& a, const R& b) { return a.lo < b.lo; });
     for (size_t k = 1; k < r.size(); ++k)
         if (r[k].lo < r[k - 1].hi) FAIL("%s overlaps %s", r[k].name, r[k - 1].name);
