@@ -397,7 +397,8 @@ struct RsArgs {
     const float* X;
     float* Y;
     int* err;
-    int N, K, M, U, G, S;  // G CTAs, S stages
+    int N, K, M, U, G, S;  // G clusters of CL CTAs, S stages
+    int CL;                // CTAs of a cluster: CTA r of a cluster takes K units [r U / CL, (r + 1) U / CL) of its rows
     int nseg;              // segments of a row (units [j U / nseg, (j + 1) U / nseg) for segment j)
     int row_bytes, pitch;  // a weight row in HBM; a whole row's stride in a stage
     int rows_pad;          // partial rows per (warp, activation row), >= any CTA's rows
@@ -454,7 +455,11 @@ __global__ void __launch_bounds__(kRsThreads, 1) pn_rows_kernel(const __grid_con
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* base = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     const uint32_t bar0 = smem_addr(base);
-    const int S = a.S, M = a.M, U = a.U, nseg = SEG ? a.nseg : 1;
+    const int S = a.S, M = a.M, nseg = SEG ? a.nseg : 1;
+    const int CL = a.CL, cr = static_cast<int>(blockIdx.x) % CL, cid = static_cast<int>(blockIdx.x) / CL;
+    const int ua = cr * a.U / CL, U = (cr + 1) * a.U / CL - ua;  // this CTA's K units [ua, ua + U)
+    const int xk = U * C::UK;                                   // floats of an activation row it reads
+    const int wpitch = rs_pitch(U * kUnitBytes);                // stage pitch of whole (CTA) rows
     auto full = [&](int s) { return bar0 + 8u * s; };
     auto empty = [&](int s) { return bar0 + 8u * (S + s); };
     const uint32_t xfull = bar0 + 8u * (2 * S);      // all of x has landed (SEG)
@@ -466,7 +471,7 @@ __global__ void __launch_bounds__(kRsThreads, 1) pn_rows_kernel(const __grid_con
     __shared__ int seg_tab[kRsMaxSeg + 1];  // first unit of segment j (seg_tab[nseg] = U)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int active = SEG ? kRsWarps : min(kRsWarps, U);  // consumer warps with work
-    const int64_t r0 = static_cast<int64_t>(blockIdx.x) * a.N / a.G, r1 = static_cast<int64_t>(blockIdx.x + 1) * a.N / a.G;
+    const int64_t r0 = static_cast<int64_t>(cid) * a.N / a.G, r1 = static_cast<int64_t>(cid + 1) * a.N / a.G;
     const int nrows = static_cast<int>(r1 - r0);
     const int nstages = (nrows + kGroupRows - 1) / kGroupRows * nseg;  // (row group, segment), segment fastest
     float* part = reinterpret_cast<float*>(base + a.off_part);  // [warp][m][rows_pad]
@@ -511,7 +516,7 @@ __global__ void __launch_bounds__(kRsThreads, 1) pn_rows_kernel(const __grid_con
             // rows of the last group past the CTA's range are not copied: a row's products depend
             // on that row alone, and those rows' sums are never stored
             const int mine = min(8, max(0, nrows - i * kGroupRows - pr));
-            int u0 = 0, bytes = a.row_bytes, pitch = a.pitch;
+            int u0 = 0, bytes = U * kUnitBytes, pitch = wpitch;
             if (SEG) {
                 u0 = seg_tab[j];
                 bytes = (seg_tab[j + 1] - u0) * kUnitBytes;
@@ -521,7 +526,7 @@ __global__ void __launch_bounds__(kRsThreads, 1) pn_rows_kernel(const __grid_con
             __syncwarp();
             if (lane < mine)
                 bulk_g2s(smem_addr(stage(slot)) + static_cast<uint32_t>((pr + lane) * pitch),
-                         a.W + (r0 + i * kGroupRows + pr + lane) * a.row_bytes + u0 * kUnitBytes,
+                         a.W + (r0 + i * kGroupRows + pr + lane) * a.row_bytes + (ua + u0) * kUnitBytes,
                          static_cast<uint32_t>(bytes), full(slot), pol);
             if (++j == nseg) {
                 j = 0;
@@ -564,7 +569,7 @@ __global__ void __launch_bounds__(kRsThreads, 1) pn_rows_kernel(const __grid_con
             auto load = [&](int q) {
                 if (q < npair) {
                     const int u = warp + (q / M) * kRsWarps, m = q % M;
-                    const float* src = a.X + static_cast<size_t>(m) * a.K + static_cast<size_t>(u) * C::UK;
+                    const float* src = a.X + static_cast<size_t>(m) * a.K + static_cast<size_t>(ua + u) * C::UK;
                     const uint32_t dst = smem_addr(xb + (q & 1) * C::UK);
                     for (int v = lane; v < C::UK / 4; v += 32) cp_async16(dst + 16u * v, src + 4 * v);
                 }
@@ -592,8 +597,8 @@ __global__ void __launch_bounds__(kRsThreads, 1) pn_rows_kernel(const __grid_con
                     ok = false;
                     break;
                 }
-                const uint32_t s0 = smem_addr(stage(slot)) + static_cast<uint32_t>(g * a.pitch);
-                const uint32_t s8 = s0 + static_cast<uint32_t>(8 * a.pitch);
+                const uint32_t s0 = smem_addr(stage(slot)) + static_cast<uint32_t>(g * wpitch);
+                const uint32_t s8 = s0 + static_cast<uint32_t>(8 * wpitch);
                 float tot0 = 0.0f, tot1 = 0.0f;
                 for (int u = warp; u < U; u += kRsWarps) task(s0, s8, static_cast<uint32_t>(u * kUnitBytes), u, tot0, tot1);
                 if (c < M) {
@@ -606,14 +611,15 @@ __global__ void __launch_bounds__(kRsThreads, 1) pn_rows_kernel(const __grid_con
             }
         } else {
             for (int e = lane; e < M * a.rows_pad; e += 32) mine[e] = 0.0f;
-            const float* xs = reinterpret_cast<const float*>(base + a.off_x);  // [M][K]
+            const float* xs = reinterpret_cast<const float*>(base + a.off_x);  // [M][xk]: the CTA's units of x
             if (warp == 0) {
                 griddep_wait();  // X belongs to the previous grid until now
                 if (lane == 0) {
-                    const uint32_t row = static_cast<uint32_t>(a.K) * 4u;
+                    const uint32_t row = static_cast<uint32_t>(xk) * 4u;
                     mbar_arrive_expect_tx(xfull, row * static_cast<uint32_t>(M));
                     for (int m = 0; m < M; ++m)
-                        bulk_g2s_plain(smem_addr(xs) + m * row, a.X + static_cast<size_t>(m) * a.K, row, xfull);
+                        bulk_g2s_plain(smem_addr(xs) + m * row, a.X + static_cast<size_t>(m) * a.K + ua * C::UK, row,
+                                       xfull);
                 }
                 __syncwarp();
             }
@@ -623,7 +629,7 @@ __global__ void __launch_bounds__(kRsThreads, 1) pn_rows_kernel(const __grid_con
                 for (int p = warp; p < U * M; p += kRsWarps) {
                     const int u = p / M, m = p - u * M;
                     build_row<TYPE, 1, LR, kRsZs>(rec(u), zbu(u), zbu(u) + kUnitBlocks * kRsZs,
-                                                  xs + static_cast<size_t>(m) * a.K + u * C::UK, m, lane);
+                                                  xs + static_cast<size_t>(m) * xk + u * C::UK, m, lane);
                 }
             __syncwarp();
             if (lane == 0) mbar_arrive(xdone);
@@ -643,7 +649,7 @@ __global__ void __launch_bounds__(kRsThreads, 1) pn_rows_kernel(const __grid_con
                     const uint32_t srow = smem_addr(stage(slot)) + static_cast<uint32_t>(lane >> 1) * pitch;
                     for (int k = k0; k < n; k += kRsWarps)
                         fma_task<TYPE>(srow + static_cast<uint32_t>(k * kUnitBytes), lane & 1, xs + (u0 + k) * C::UK,
-                                       a.K, M, tot);
+                                       xk, M, tot);
 #pragma unroll
                     for (int m = 0; m < kRsZs; ++m) tot[m] += __shfl_xor_sync(0xffffffffu, tot[m], 1);
                     if ((lane & 1) == 0)
@@ -669,34 +675,66 @@ __global__ void __launch_bounds__(kRsThreads, 1) pn_rows_kernel(const __grid_con
         if (!ok && lane == 0) record_error(a.err, kErrFullWait);
     }
 
-    // ---------------- the warps' row sums -> Y ----------------
+    // ---------------- the warps' row sums (and the cluster's, in CTA order) -> Y ----------------
     __syncthreads();
-    griddep_wait();  // Y may still be read by the previous grid
+    if (CL == 1) {
+        griddep_wait();  // Y may still be read by the previous grid
+        for (int e = threadIdx.x; e < M * nrows; e += kRsThreads) {
+            const int m = e / nrows, r = e - m * nrows;
+            float v = 0.0f;
+            for (int w = 0; w < active; ++w) v += part[(w * M + m) * a.rows_pad + r];
+            a.Y[static_cast<size_t>(m) * a.N + r0 + r] = v;
+        }
+        return;
+    }
+    // this CTA's sum over its warps, in warp 0's slice; then CTA cr writes a share of the rows
+    // from the sums of every CTA of the cluster (distributed shared memory)
     for (int e = threadIdx.x; e < M * nrows; e += kRsThreads) {
         const int m = e / nrows, r = e - m * nrows;
         float v = 0.0f;
         for (int w = 0; w < active; ++w) v += part[(w * M + m) * a.rows_pad + r];
-        a.Y[static_cast<size_t>(m) * a.N + r0 + r] = v;
+        part[m * a.rows_pad + r] = v;
     }
+    cluster_sync();
+    griddep_wait();  // Y may still be read by the previous grid
+    {
+        const int E = M * nrows, e0 = cr * E / CL, e1 = (cr + 1) * E / CL;
+        const uint32_t pbase = smem_addr(part);
+        for (int e = e0 + static_cast<int>(threadIdx.x); e < e1; e += kRsThreads) {
+            const int m = e / nrows, r = e - m * nrows;
+            const uint32_t off = 4u * static_cast<uint32_t>(m * a.rows_pad + r);
+            float v = 0.0f;
+            for (int q = 0; q < CL; ++q) v += ld_dsmem_f32(pbase + off, static_cast<uint32_t>(q));
+            a.Y[static_cast<size_t>(m) * a.N + r0 + r] = v;
+        }
+    }
+    cluster_sync();  // no CTA leaves while another still reads its sums
 }
 
 struct RsPlan {
-    int G = 0, S = 0, nseg = 0, rows_pad = 0, pitch = 0, x_slot0 = 0;
+    int G = 0, CL = 1, S = 0, nseg = 0, rows_pad = 0, pitch = 0, x_slot0 = 0;
     uint32_t off_rec = 0, off_zb = 0, off_x = 0, off_part = 0, off_stage = 0, stage_bytes = 0, total = 0;
 };
 
-// Grid (one CTA per SM, or one per row when there are fewer rows), segments per row and the ring
-// of stages. Rows of at most 16 units stay whole (per-warp x buffers); longer rows are cut into
-// segments of at most 8, 6 then 4 units (all of x staged). x is read only while the operands are
+// Grid (clusters of CL CTAs, one CTA per SM, or one cluster per row when there are fewer rows),
+// segments per row and the ring of stages, for the K units of one CTA (at most ceil(U / CL)).
+// Rows of at most 16 units stay whole (per-warp x buffers); longer rows are cut into segments of
+// at most 8, 6 then 4 units (all of the CTA's x staged). x is read only while the operands are
 // built, so it may sit in the ring's last slots (slot 2 or later), which the producer fills only
 // once every warp has built: of the two layouts, x apart or x in the ring, the one with the deeper
 // ring is taken (8..3 stages, then 2 as a last resort). The CUDA-core decode (fma) keeps no B
 // operands and reads x throughout, so its x has a region of its own. False when nothing fits.
 template <int TYPE, int LR>
-bool rs_plan(int64_t N, int U, int M, int sms, int s_req, RsPlan& p, bool fma = false, bool x_in_ring = true) {
+bool rs_plan(int64_t N, int Ut, int M, int sms, int s_req, RsPlan& p, bool fma = false, bool x_in_ring = true,
+             int CL = 1, int max_clusters = 0) {
     using C = Cfg<TYPE, 1, LR>;
+    if (CL < 1 || CL > 8 || sms / CL < 1 || Ut < CL) return false;
+    const int U = (Ut + CL - 1) / CL;  // the most units of a CTA
     if (U < 1 || M < 1 || M > kRsZs || (U + 3) / 4 > kRsMaxSeg) return false;
-    p.G = static_cast<int>(std::min<int64_t>(sms, N));
+    p.CL = CL;
+    // clusters: one CTA per SM, no more than can be resident at once (max_clusters > 0)
+    const int ncl = max_clusters > 0 ? std::min(sms / CL, max_clusters) : sms / CL;
+    p.G = static_cast<int>(std::min<int64_t>(ncl, N));
     const int64_t rows_max = (N + p.G - 1) / p.G;
     p.rows_pad = static_cast<int>((rows_max + kGroupRows - 1) / kGroupRows * kGroupRows);
     const bool whole = U <= kRsWholeUnits;
@@ -750,24 +788,128 @@ cudaError_t launch_rows_kernel(const RsArgs& a, const RsPlan& p, cudaStream_t st
         opted[dev].store(true, std::memory_order_relaxed);
     }
     cudaLaunchConfig_t lc{};
-    lc.gridDim = dim3(p.G, 1, 1);
+    lc.gridDim = dim3(p.G * p.CL, 1, 1);
     lc.blockDim = dim3(kRsThreads, 1, 1);
     lc.dynamicSmemBytes = p.total + 1024u;
     lc.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = static_cast<unsigned>(p.CL);
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    lc.attrs = attr;
+    lc.numAttrs = 2;
+    return cudaLaunchKernelEx(&lc, kern, a);
+}
+
+// Estimated time (us) of a row-stream plan, fitted to the decode-step projections on this GPU at
+// M = 1, 2, 4 with every cluster size forced: ~2.5 us until the first stage is multiplied; 0.35 us
+// per further (unit, activation row) operand build of the busiest warp (whole rows: warp w builds
+// units w, w + 8, ..; segments: the builds are dealt evenly); then the longer of the busiest
+// consumer warp's tasks (0.65 us per 16 rows x one unit) and the CTA's weight stream (35 GB/s per
+// SM); plus 1.5 us for a cluster's final sum and 4 us for segments (all builds before any task).
+inline double rs_cost(const RsPlan& p, int64_t N, int Ut, int M) {
+    const int U = (Ut + p.CL - 1) / p.CL;
+    const int64_t rows = (N + p.G - 1) / p.G;
+    const int64_t groups = (rows + kGroupRows - 1) / kGroupRows;
+    const bool seg = p.nseg > 1;
+    const int per_warp = (U + kRsWarps - 1) / kRsWarps;
+    const double tasks = seg ? static_cast<double>((groups * U + kRsWarps - 1) / kRsWarps)
+                             : static_cast<double>(groups * per_warp);
+    const double builds = seg ? static_cast<double>((U * M + kRsWarps - 1) / kRsWarps) : static_cast<double>(per_warp * M);
+    const double stream = static_cast<double>(rows) * U * kUnitBytes / 35e3;
+    return 2.5 + 0.35 * (builds - 1.0) + std::max(0.65 * tasks, stream) + (p.CL > 1 ? 1.5 : 0.0) + (seg ? 4.0 : 0.0);
+}
+
+// The cheapest plan over clusters of 1, 2, 4 and 8 CTAs (cl_req > 0: that size only).
+// resident(CL, plan) = clusters of CL CTAs of that plan's kernel that fit on the GPU at once
+// (clusters of 4 or 8 need that many SMs of one GPC, which does not divide every GPC).
+template <int TYPE, int LR, class Resident>
+bool rs_best_plan(int64_t N, int U, int M, int sms, int s_req, bool fma, bool x_in_ring, int cl_req, RsPlan& p,
+                  Resident&& resident) {
+    bool found = false;
+    double best = 0.0;
+    for (int CL : {1, 2, 4, 8}) {
+        if (cl_req > 0 && CL != cl_req) continue;
+        RsPlan q;
+        if (!rs_plan<TYPE, LR>(N, U, M, sms, s_req, q, fma, x_in_ring, CL)) continue;
+        if (CL > 1) {
+            const int most = resident(CL, q);
+            if (most < 1) continue;
+            if (most < q.G && !rs_plan<TYPE, LR>(N, U, M, sms, s_req, q, fma, x_in_ring, CL, most)) continue;
+        }
+        const double cost = rs_cost(q, N, U, M);
+        if (!found || cost < best) {
+            p = q;
+            best = cost;
+            found = true;
+        }
+    }
+    return found;
+}
+
+// Clusters of CL CTAs of the plan's kernel that can be resident at once on this device (0 when the
+// query fails).
+template <int TYPE, int LR>
+int rows_resident_clusters(int CL, const RsPlan& q, bool fma) {
+    void (*kern)(RsArgs) = fma ? pn_rows_kernel<TYPE, LR, true, true>
+                               : (q.nseg > 1 ? pn_rows_kernel<TYPE, LR, true> : pn_rows_kernel<TYPE, LR, false>);
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmemOne)) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    cudaLaunchConfig_t lc{};
+    lc.gridDim = dim3(q.G * CL, 1, 1);
+    lc.blockDim = dim3(kRsThreads, 1, 1);
+    lc.dynamicSmemBytes = q.total + 1024u;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(CL);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
     lc.attrs = attr;
     lc.numAttrs = 1;
-    return cudaLaunchKernelEx(&lc, kern, a);
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &lc) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return n;
+}
+
+// rs_best_plan with the device's SM count and resident clusters, cached per device and shape.
+template <int TYPE, int LR>
+bool rs_cached_plan(int64_t N, int U, int M, int s_req, bool fma, bool x_in_ring, int cl_req, RsPlan& p) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    using Key = std::tuple<int, int64_t, int, int, int, bool, bool, int>;
+    static std::mutex mu;
+    static std::map<Key, RsPlan> cache;
+    const Key key{dev, N, U, M, s_req, fma, x_in_ring, cl_req};
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        auto it = cache.find(key);
+        if (it != cache.end()) {
+            p = it->second;
+            return true;
+        }
+    }
+    auto resident = [fma](int CL, const RsPlan& q) { return rows_resident_clusters<TYPE, LR>(CL, q, fma); };
+    if (!rs_best_plan<TYPE, LR>(N, U, M, device_sm_count(), s_req, fma, x_in_ring, cl_req, p, resident)) return false;
+    std::lock_guard<std::mutex> lock(mu);
+    if (cache.size() < 4096) cache.emplace(key, p);
+    return true;
 }
 
 template <int TYPE, int LR>
 cudaError_t launch_rows(const uint8_t* W, const float* X, float* Y, int* err, int64_t N, int64_t K, int M, int U,
                         int row_bytes, int s_req, bool static_weights, bool fma, int x_ahead, bool x_in_ring,
-                        cudaStream_t stream) {
+                        int cl_req, cudaStream_t stream) {
     RsPlan p;
-    if (!rs_plan<TYPE, LR>(N, U, M, device_sm_count(), s_req, p, fma, x_in_ring)) return cudaErrorNotSupported;
+    if (!rs_cached_plan<TYPE, LR>(N, U, M, s_req, fma, x_in_ring, cl_req, p)) return cudaErrorNotSupported;
     RsArgs a{};
     a.W = W;
     a.X = X;
@@ -778,6 +920,7 @@ cudaError_t launch_rows(const uint8_t* W, const float* X, float* Y, int* err, in
     a.M = M;
     a.U = U;
     a.G = p.G;
+    a.CL = p.CL;
     a.S = p.S;
     a.nseg = p.nseg;
     a.row_bytes = row_bytes;
@@ -799,12 +942,12 @@ cudaError_t launch_rows(const uint8_t* W, const float* X, float* Y, int* err, in
 template <int TYPE>
 cudaError_t launch_rows_typed(const uint8_t* W, const float* X, float* Y, int* err, int64_t N, int64_t K, int M,
                               int U, int row_bytes, int s_req, bool static_weights, bool fma, int xa, bool xr,
-                              cudaStream_t stream) {
+                              int cl, cudaStream_t stream) {
     switch (M) {
-        case 1: return launch_rows<TYPE, 8>(W, X, Y, err, N, K, M, U, row_bytes, s_req, static_weights, fma, xa, xr, stream);
-        case 2: return launch_rows<TYPE, 16>(W, X, Y, err, N, K, M, U, row_bytes, s_req, static_weights, fma, xa, xr, stream);
-        case 3: return launch_rows<TYPE, 24>(W, X, Y, err, N, K, M, U, row_bytes, s_req, static_weights, fma, xa, xr, stream);
-        case 4: return launch_rows<TYPE, 32>(W, X, Y, err, N, K, M, U, row_bytes, s_req, static_weights, fma, xa, xr, stream);
+        case 1: return launch_rows<TYPE, 8>(W, X, Y, err, N, K, M, U, row_bytes, s_req, static_weights, fma, xa, xr, cl, stream);
+        case 2: return launch_rows<TYPE, 16>(W, X, Y, err, N, K, M, U, row_bytes, s_req, static_weights, fma, xa, xr, cl, stream);
+        case 3: return launch_rows<TYPE, 24>(W, X, Y, err, N, K, M, U, row_bytes, s_req, static_weights, fma, xa, xr, cl, stream);
+        case 4: return launch_rows<TYPE, 32>(W, X, Y, err, N, K, M, U, row_bytes, s_req, static_weights, fma, xa, xr, cl, stream);
         default: return cudaErrorNotSupported;
     }
 }
@@ -850,8 +993,9 @@ cudaError_t launch_pn_gemv_mma(int type, const uint8_t* W, int64_t N, int64_t K,
         !encode_u32_map(&map[1], W, N, nb * kBlockBytes / 4, kUnitU32, kStageRows))
         return cudaErrorNotSupported;
     // PNQ_PN_CFG = "CTAs per cluster, stages, CTAs per SM, path (1 rows, 2 strips), decode (1 CUDA-core FMA),
-    // row stream: weight stages issued before x is requested (0: 1), x apart from the ring (1)"
-    static int env[7];
+    // row stream: weight stages issued before x is requested (0: 1), x apart from the ring (1), CTAs per
+    // cluster splitting K (1, 2, 4, 8; 0: cheapest)"
+    static int env[8];
     static std::once_flag once;
     std::call_once(once, [] { env_cluster_config("PNQ_PN_CFG", env); });
     const int req[3] = {c_req > 0 ? c_req : env[0], s_req > 0 ? s_req : env[1], env[2]};
@@ -860,12 +1004,13 @@ cudaError_t launch_pn_gemv_mma(int type, const uint8_t* W, int64_t N, int64_t K,
     const bool fma = env[4] == 1;
     const int x_ahead = env[5] > 0 ? env[5] : 1;
     const bool x_in_ring = env[6] != 1;
+    const int rows_cl = env[7];
     if (env[3] != 2 && M <= 4 && c_req <= 0) {
         const cudaError_t e = (type == kTypePn3t)
                                   ? launch_rows_typed<kTypePn3t>(W, X, Y, err, N, K, M, static_cast<int>(U), row_bytes,
-                                                                 req[1], static_weights, fma, x_ahead, x_in_ring, stream)
+                                                                 req[1], static_weights, fma, x_ahead, x_in_ring, rows_cl, stream)
                                   : launch_rows_typed<kTypePn4t>(W, X, Y, err, N, K, M, static_cast<int>(U), row_bytes,
-                                                                 req[1], static_weights, fma, x_ahead, x_in_ring, stream);
+                                                                 req[1], static_weights, fma, x_ahead, x_in_ring, rows_cl, stream);
         if (e != cudaErrorNotSupported || env[3] == 1 || fma) return e;
     }
     return (type == kTypePn3t)

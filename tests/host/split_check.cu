@@ -162,19 +162,23 @@ void run_type() {
 }
 
 template <int TYPE, int LR>
-void check_rs_plan(int64_t N, int U, int M, int s_req, bool fma = false) {
+void check_rs_plan(int64_t N, int Ut, int M, int s_req, bool fma = false, int CL = 1, int max_cl = 0) {
     using C = pnq::Cfg<TYPE, 1, LR>;
-    char what[128];
-    std::snprintf(what, sizeof what, "rows %s N %lld U %d M %d s %d", TYPE == pnq::kTypePn3t ? "pn3t" : "pn4t",
-                  (long long)N, U, M, s_req);
+    char what[160];
+    std::snprintf(what, sizeof what, "rows %s N %lld U %d M %d s %d CL %d max %d", TYPE == pnq::kTypePn3t ? "pn3t" : "pn4t",
+                  (long long)N, Ut, M, s_req, CL, max_cl);
     pnq::RsPlan p;
-    if (!pnq::rs_plan<TYPE, LR>(N, U, M, 152, s_req, p, fma)) return;
+    if (!pnq::rs_plan<TYPE, LR>(N, Ut, M, 152, s_req, p, fma, true, CL, max_cl)) return;
     ++plans;
+    if (p.CL != CL) FAIL("cluster of %d, asked %d", p.CL, CL);
+    if (max_cl > 0 && p.G > max_cl) FAIL("%d clusters, %d resident", p.G, max_cl);
+    if (1ll * p.G * CL > 152) FAIL("%d CTAs", p.G * CL);
+    const int U = (Ut + CL - 1) / CL;  // the most units of a CTA
     if (s_req > 0 && p.S != s_req) FAIL("forced %d stages, planned %d", s_req, p.S);
     if (p.S < 2 || p.S > 8) FAIL("%d stages", p.S);
     if (p.nseg < 1 || p.nseg > U) FAIL("%d segments", p.nseg);
     if (p.total + 1024u > pnq::kSmemOne) FAIL("total %u", p.total);
-    if (p.G < 1 || p.G > 152 || p.G > N) FAIL("grid %d", p.G);
+    if (p.G < 1 || p.G > 152 / CL || p.G > N) FAIL("grid %d", p.G);
     struct R {
         uint64_t lo, hi;
         const char* name;
@@ -183,6 +187,15 @@ void check_rs_plan(int64_t N, int U, int M, int s_req, bool fma = false) {
     const bool whole = U <= pnq::kRsWholeUnits;
     if (whole != (p.nseg == 1)) FAIL("%d segments for %d units", p.nseg, U);
     if (whole && p.pitch != pnq::rs_pitch(U * pnq::kUnitBytes)) FAIL("whole-row pitch %d", p.pitch);
+    // every CTA of a cluster: its units [r Ut / CL, (r + 1) Ut / CL) tile [0, Ut); its whole rows fit a stage
+    for (int r = 0, prev_u = 0; r < CL; ++r) {
+        const int ua = r * Ut / CL, ub = (r + 1) * Ut / CL;
+        if (ua != prev_u || ub <= ua || ub - ua > U) FAIL("CTA %d of the cluster has units [%d, %d)", r, ua, ub);
+        prev_u = ub;
+        const int bytes = (ub - ua) * pnq::kUnitBytes, pitch = pnq::rs_pitch(bytes);
+        if (whole && 15u * pitch + bytes > p.stage_bytes) FAIL("rows of cluster CTA %d overflow their stage", r);
+        if (r == CL - 1 && ub != Ut) FAIL("cluster units end at %d", ub);
+    }
     const uint64_t xbytes = (whole && !fma) ? 4ull * pnq::kRsWarps * 2 * C::UK : 4ull * M * U * C::UK;
     const uint64_t nrec = fma ? 0 : U;
     // x either has a region of its own or lies in the ring's slots [x_slot0, S), slot 2 or later
@@ -222,7 +235,7 @@ void check_rs_plan(int64_t N, int U, int M, int s_req, bool fma = false) {
         if ((u0 * pnq::kUnitBytes) % 16) FAIL("segment %d source misaligned", j);
     }
     if (prev != U) FAIL("segments end at %d", prev);
-    // rows of every CTA, and the task dealing of its stages
+    // rows of every cluster, and the task dealing of its stages (a CTA with the most units)
     for (int b = 0; b < p.G; ++b) {
         const int64_t r0 = static_cast<int64_t>(b) * N / p.G, r1 = static_cast<int64_t>(b + 1) * N / p.G;
         const int nrows = static_cast<int>(r1 - r0);
@@ -304,10 +317,14 @@ void run_rows() {
             for (int s : {0, 2, 3, 5})
                 for (int M = 1; M <= 4 && !failures; ++M) {
                     for (bool fma : {false, true}) {
-                        if (M == 1) check_rs_plan<TYPE, 8>(N, U, M, s, fma);
-                        if (M == 2) check_rs_plan<TYPE, 16>(N, U, M, s, fma);
-                        if (M == 3) check_rs_plan<TYPE, 24>(N, U, M, s, fma);
-                        if (M == 4) check_rs_plan<TYPE, 32>(N, U, M, s, fma);
+                        for (int CL : {1, 2, 4, 8})
+                            for (int mc : {0, 17, 36}) {
+                                if (CL == 1 && mc) continue;
+                                if (M == 1) check_rs_plan<TYPE, 8>(N, U, M, s, fma, CL, mc);
+                                if (M == 2) check_rs_plan<TYPE, 16>(N, U, M, s, fma, CL, mc);
+                                if (M == 3) check_rs_plan<TYPE, 24>(N, U, M, s, fma, CL, mc);
+                                if (M == 4) check_rs_plan<TYPE, 32>(N, U, M, s, fma, CL, mc);
+                            }
                     }
                 }
     // the decode-step projections at M = 1 take the row-stream path

@@ -299,13 +299,17 @@ print(json.dumps({{"ok": True, "device_error": pnq.device_error()}}))
 @pytest.mark.parametrize("pn_cfg,nv_cfg", [("1,0,0,2", "2,0"), ("2,0,0,2", "1,0"), ("1,3,0,2", "1,6"),
                                             ("2,3,2,2", "2,3,2"), ("0,0,0,1", "2,4"), ("0,2,0,1", "1,3,1"),
                                             ("0,3,0,1", "0,5,2"), ("0,8,0,1", "0,3"), ("0,3,0,0", "1,4"),
-                                            ("0,6,1,2", "2,6,1"), ("0,0,0,1,1", "0,0"), ("0,2,0,1,1", "0,0")])
+                                            ("0,6,1,2", "2,6,1"), ("0,0,0,1,1", "0,0"), ("0,2,0,1,1", "0,0"),
+                                            ("0,0,0,1,0,0,0,2", "0,0"), ("0,3,0,1,0,0,0,4", "0,0"),
+                                            ("0,0,0,1,0,8,1,8", "0,0"), ("0,0,0,1,1,0,0,2", "0,0")])
 def test_tile_and_grid_configs(pn_cfg, nv_cfg):
     """Forced configurations, read once per process (so each runs in a child): the PN path through
-    PNQ_PN_CFG = "CTAs per cluster, weight stages, CTAs per SM, path, decode" (path 1 = whole rows
-    per CTA, 2 = K-unit strips over clusters; decode 1 = the CUDA-core FMA decode of the row path,
-    which shapes outside its plan leave to the generic path) and the NVFP4 path through
-    PNQ_NV_CFG = "CTAs per cluster, weight stages, CTAs per SM" (0 = automatic)."""
+    PNQ_PN_CFG = "CTAs per cluster, weight stages, CTAs per SM, path, decode, x ahead, x apart, row
+    clusters" (path 1 = the row stream, 2 = K-unit strips over clusters; decode 1 = the CUDA-core
+    FMA decode of the row path, which shapes outside its plan leave to the generic path; x ahead =
+    weight stages issued before x is requested; x apart 1 = x outside the weight ring; row clusters
+    = CTAs splitting K in the row stream) and the NVFP4 path through PNQ_NV_CFG = "CTAs per
+    cluster, weight stages, CTAs per SM" (0 = automatic)."""
     env = dict(os.environ, PNQ_PN_CFG=pn_cfg, PNQ_NV_CFG=nv_cfg, PNQ_FORCE_KERNEL="mma")
     r = subprocess.run([sys.executable, "-c", CHILD.format(root=ROOT)], env=env, capture_output=True, text=True,
                        timeout=600)
