@@ -384,8 +384,11 @@ constexpr int kRsProducers = 2;  // producer warps, rows 0..7 and 8..15 of each 
 constexpr int kRsThreads = 32 * (kRsWarps + kRsProducers);
 constexpr int kRsWholeUnits = 16;  // longest whole row (units); longer rows are cut into segments
 constexpr int kRsMaxSeg = 32;      // segments of a row at most
-constexpr int kRsZs = 4;           // activation rows of the zero-point table (M <= 4)
-constexpr int kRsZb = kUnitBlocks * kRsZs + kRsZs;  // floats per unit: terms [block][m], then 2^(24 - sigma) [m]
+constexpr int kRsZs = 4;           // activation rows of the CUDA-core decode (M <= 4)
+// zero-point table of NT n8 tiles (4 NT activation rows): floats per unit, terms [block][m], then
+// 2^(24 - sigma) [m]
+constexpr int rs_zs(int NT) { return 4 * NT; }
+constexpr int rs_zb(int NT) { return kUnitBlocks * rs_zs(NT) + rs_zs(NT); }
 constexpr uint32_t kRsConsumerBar = 1;              // named barrier of the consumer warps
 
 // Stage pitch of a row (segment) of `bytes` (a multiple of 16): the least multiple of 16 >= bytes
@@ -449,9 +452,11 @@ __device__ __forceinline__ void fma_task(uint32_t srow, int hf, const float* xu,
     });
 }
 
-template <int TYPE, int LR, bool SEG, bool FMA = false>
+template <int TYPE, int LR, bool SEG, bool FMA = false, int NT = 1>
 __global__ void __launch_bounds__(kRsThreads, 1) pn_rows_kernel(const __grid_constant__ RsArgs a) {
-    using C = Cfg<TYPE, 1, LR>;
+    using C = Cfg<TYPE, NT, LR>;
+    constexpr int ZS = rs_zs(NT);
+    static_assert(!FMA || NT == 1, "the CUDA-core decode covers M <= 4");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* base = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     const uint32_t bar0 = smem_addr(base);
@@ -467,7 +472,7 @@ __global__ void __launch_bounds__(kRsThreads, 1) pn_rows_kernel(const __grid_con
     const uint32_t xdone = bar0 + 8u * (2 * S + 2);  // every consumer warp has built its operands (x is dead)
     auto stage = [&](int s) { return base + a.off_stage + static_cast<uint32_t>(s) * a.stage_bytes; };
     auto rec = [&](int u) { return base + a.off_rec + static_cast<uint32_t>(u) * C::REC; };
-    auto zbu = [&](int u) { return reinterpret_cast<float*>(base + a.off_zb) + u * kRsZb; };
+    auto zbu = [&](int u) { return reinterpret_cast<float*>(base + a.off_zb) + u * rs_zb(NT); };
     __shared__ int seg_tab[kRsMaxSeg + 1];  // first unit of segment j (seg_tab[nseg] = U)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int active = SEG ? kRsWarps : min(kRsWarps, U);  // consumer warps with work
@@ -541,23 +546,50 @@ __global__ void __launch_bounds__(kRsThreads, 1) pn_rows_kernel(const __grid_con
         // ---------------- consumer warps ----------------
         const int g = lane >> 2, c = lane & 3;
         const uint32_t sel = (c == 3) ? 0x7610u : 0x3210u;
-        // the lane's B record and zero-point offsets (columns past 2M read a live column's)
-        const uint32_t boff = static_cast<uint32_t>((4 * min(g, 2 * M - 1) + c) * 16);
-        const int mz = min(c, M - 1);
+        // the lane's B record and zero-point offsets per n8 tile (columns past 2M read a live
+        // column's; their sums are never stored)
+        uint32_t boff[NT];
+        int mz[NT];
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+            boff[t] = static_cast<uint32_t>((4 * min(g, max(0, 2 * M - 1 - 8 * t)) + c) * 16);
+            mz[t] = min(4 * t + c, M - 1);
+        }
         float* mine = part + warp * M * a.rows_pad;
-        // one (row group, unit) task: rows g, g + 8 of the stage rows s0 / s8, at byte uo of them
-        auto task = [&](uint32_t s0, uint32_t s8, uint32_t uo, int u, float& tot0, float& tot1) {
+        // one (row group, unit) task: rows g, g + 8 of the stage rows s0 / s8, at byte uo of them;
+        // tot[t][h] += the row's sum for activation row 4t + c
+        auto task = [&](uint32_t s0, uint32_t s8, uint32_t uo, int u, float (&tot)[NT][2]) {
             const uint32_t srow[2] = {s0 + uo, s8 + uo};
             const uint32_t srow_c[2] = {s0 + uo + 4u * c, s8 + uo + 4u * c};
             const uint32_t rs = smem_addr(rec(u));
-            const uint32_t srec[1] = {rs + boff}, srec_h[1] = {rs + boff / 2};
-            const uint32_t szb[1] = {smem_addr(zbu(u)) + 4u * mz};
-            float acc[1][2] = {{0.0f, 0.0f}};
-            pn_blocks<TYPE, 1, 0, 4, LR, kRsZs>(srow, srow_c, sel, srec, srec_h, szb, acc);
-            pn_blocks<TYPE, 1, 4, 4, LR, kRsZs>(srow, srow_c, sel, srec, srec_h, szb, acc);
-            const float f = zbu(u)[kUnitBlocks * kRsZs + mz];  // 2^(24 - sigma) of the unit
-            tot0 = fmaf(acc[0][0], f, tot0);
-            tot1 = fmaf(acc[0][1], f, tot1);
+            uint32_t srec[NT], srec_h[NT], szb[NT];
+#pragma unroll
+            for (int t = 0; t < NT; ++t) {
+                srec[t] = rs + boff[t];
+                srec_h[t] = rs + boff[t] / 2;
+                szb[t] = smem_addr(zbu(u)) + 4u * mz[t];
+            }
+            float acc[NT][2];
+#pragma unroll
+            for (int t = 0; t < NT; ++t) acc[t][0] = acc[t][1] = 0.0f;
+            pn_blocks<TYPE, NT, 0, 4, LR, ZS>(srow, srow_c, sel, srec, srec_h, szb, acc);
+            pn_blocks<TYPE, NT, 4, 4, LR, ZS>(srow, srow_c, sel, srec, srec_h, szb, acc);
+#pragma unroll
+            for (int t = 0; t < NT; ++t) {
+                const float f = zbu(u)[kUnitBlocks * ZS + mz[t]];  // 2^(24 - sigma) of the unit
+                tot[t][0] = fmaf(acc[t][0], f, tot[t][0]);
+                tot[t][1] = fmaf(acc[t][1], f, tot[t][1]);
+            }
+        };
+        // a task total of rows g, g + 8 of row group i into the warp's partials (+= in segments)
+        auto store = [&](int i, const float (&tot)[NT][2], bool add) {
+#pragma unroll
+            for (int t = 0; t < NT; ++t)
+                if (4 * t + c < M) {
+                    float* pr = mine + (4 * t + c) * a.rows_pad + i * kGroupRows + g;
+                    pr[0] = add ? pr[0] + tot[t][0] : tot[t][0];
+                    pr[8] = add ? pr[8] + tot[t][1] : tot[t][1];
+                }
         };
         bool ok = true;
         if constexpr (!SEG) {
@@ -583,8 +615,7 @@ __global__ void __launch_bounds__(kRsThreads, 1) pn_rows_kernel(const __grid_con
                 const int u = warp + (q / M) * kRsWarps, m = q % M;
                 cp_async_wait<1>();  // pair q's x has landed (pair q + 1's may still be in flight)
                 __syncwarp();
-                build_row<TYPE, 1, LR, kRsZs>(rec(u), zbu(u), zbu(u) + kUnitBlocks * kRsZs, xb + (q & 1) * C::UK, m,
-                                              lane);
+                build_row<TYPE, NT, LR, ZS>(rec(u), zbu(u), zbu(u) + kUnitBlocks * ZS, xb + (q & 1) * C::UK, m, lane);
                 __syncwarp();
                 load(q + 2);
             }
@@ -599,13 +630,11 @@ __global__ void __launch_bounds__(kRsThreads, 1) pn_rows_kernel(const __grid_con
                 }
                 const uint32_t s0 = smem_addr(stage(slot)) + static_cast<uint32_t>(g * wpitch);
                 const uint32_t s8 = s0 + static_cast<uint32_t>(8 * wpitch);
-                float tot0 = 0.0f, tot1 = 0.0f;
-                for (int u = warp; u < U; u += kRsWarps) task(s0, s8, static_cast<uint32_t>(u * kUnitBytes), u, tot0, tot1);
-                if (c < M) {
-                    float* pr = mine + c * a.rows_pad + i * kGroupRows + g;
-                    pr[0] = tot0;
-                    pr[8] = tot1;
-                }
+                float tot[NT][2];
+#pragma unroll
+                for (int t = 0; t < NT; ++t) tot[t][0] = tot[t][1] = 0.0f;
+                for (int u = warp; u < U; u += kRsWarps) task(s0, s8, static_cast<uint32_t>(u * kUnitBytes), u, tot);
+                store(i, tot, false);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(empty(slot));
             }
@@ -628,8 +657,8 @@ __global__ void __launch_bounds__(kRsThreads, 1) pn_rows_kernel(const __grid_con
             if (ok && !FMA)
                 for (int p = warp; p < U * M; p += kRsWarps) {
                     const int u = p / M, m = p - u * M;
-                    build_row<TYPE, 1, LR, kRsZs>(rec(u), zbu(u), zbu(u) + kUnitBlocks * kRsZs,
-                                                  xs + static_cast<size_t>(m) * xk + u * C::UK, m, lane);
+                    build_row<TYPE, NT, LR, ZS>(rec(u), zbu(u), zbu(u) + kUnitBlocks * ZS,
+                                                xs + static_cast<size_t>(m) * xk + u * C::UK, m, lane);
                 }
             __syncwarp();
             if (lane == 0) mbar_arrive(xdone);
@@ -644,7 +673,8 @@ __global__ void __launch_bounds__(kRsThreads, 1) pn_rows_kernel(const __grid_con
                 const int u0 = seg_tab[j], n = seg_tab[j + 1] - u0;
                 const uint32_t pitch = static_cast<uint32_t>(rs_pitch(n * kUnitBytes));
                 const uint32_t s0 = smem_addr(stage(slot)) + g * pitch, s8 = s0 + 8u * pitch;
-                if (FMA && k0 < n) {
+                if constexpr (FMA) {
+                  if (k0 < n) {
                     float tot[kRsZs] = {0.0f, 0.0f, 0.0f, 0.0f};
                     const uint32_t srow = smem_addr(stage(slot)) + static_cast<uint32_t>(lane >> 1) * pitch;
                     for (int k = k0; k < n; k += kRsWarps)
@@ -654,14 +684,13 @@ __global__ void __launch_bounds__(kRsThreads, 1) pn_rows_kernel(const __grid_con
                     for (int m = 0; m < kRsZs; ++m) tot[m] += __shfl_xor_sync(0xffffffffu, tot[m], 1);
                     if ((lane & 1) == 0)
                         for (int m = 0; m < M; ++m) mine[m * a.rows_pad + i * kGroupRows + (lane >> 1)] += tot[m];
-                } else if (!FMA && k0 < n) {
-                    float tot0 = 0.0f, tot1 = 0.0f;
-                    for (int k = k0; k < n; k += kRsWarps) task(s0, s8, static_cast<uint32_t>(k * kUnitBytes), u0 + k, tot0, tot1);
-                    if (c < M) {
-                        float* pr = mine + c * a.rows_pad + i * kGroupRows + g;
-                        pr[0] += tot0;
-                        pr[8] += tot1;
-                    }
+                  }
+                } else if (k0 < n) {
+                    float tot[NT][2];
+#pragma unroll
+                    for (int t = 0; t < NT; ++t) tot[t][0] = tot[t][1] = 0.0f;
+                    for (int k = k0; k < n; k += kRsWarps) task(s0, s8, static_cast<uint32_t>(k * kUnitBytes), u0 + k, tot);
+                    store(i, tot, true);
                 }
                 k0 = (k0 - n) & (kRsWarps - 1);
                 __syncwarp();
@@ -724,13 +753,13 @@ struct RsPlan {
 // once every warp has built: of the two layouts, x apart or x in the ring, the one with the deeper
 // ring is taken (8..3 stages, then 2 as a last resort). The CUDA-core decode (fma) keeps no B
 // operands and reads x throughout, so its x has a region of its own. False when nothing fits.
-template <int TYPE, int LR>
+template <int TYPE, int LR, int NT = 1>
 bool rs_plan(int64_t N, int Ut, int M, int sms, int s_req, RsPlan& p, bool fma = false, bool x_in_ring = true,
              int CL = 1, int max_clusters = 0) {
-    using C = Cfg<TYPE, 1, LR>;
-    if (CL < 1 || CL > 8 || sms / CL < 1 || Ut < CL) return false;
+    using C = Cfg<TYPE, NT, LR>;
+    if (CL < 1 || CL > 8 || sms / CL < 1 || Ut < CL || (fma && NT > 1)) return false;
     const int U = (Ut + CL - 1) / CL;  // the most units of a CTA
-    if (U < 1 || M < 1 || M > kRsZs || (U + 3) / 4 > kRsMaxSeg) return false;
+    if (U < 1 || M < 1 || M > rs_zs(NT) || (U + 3) / 4 > kRsMaxSeg) return false;
     p.CL = CL;
     // clusters: one CTA per SM, no more than can be resident at once (max_clusters > 0)
     const int ncl = max_clusters > 0 ? std::min(sms / CL, max_clusters) : sms / CL;
@@ -741,7 +770,7 @@ bool rs_plan(int64_t N, int Ut, int M, int sms, int s_req, RsPlan& p, bool fma =
     const uint32_t nrec = fma ? 0u : static_cast<uint32_t>(U);
     p.off_rec = align_up(8u * (2u * kMaxStages + 3), 128);
     p.off_zb = align_up(p.off_rec + nrec * C::REC, 16);
-    p.off_part = align_up(p.off_zb + nrec * kRsZb * 4u, 16);
+    p.off_part = align_up(p.off_zb + nrec * rs_zb(NT) * 4u, 16);
     const uint32_t part_end = p.off_part + kRsWarps * static_cast<uint32_t>(M * p.rows_pad) * 4u;
     const uint32_t xbytes =
         (whole && !fma) ? kRsWarps * 2u * C::UK * 4u : static_cast<uint32_t>(M) * U * C::UK * 4u;
@@ -774,9 +803,9 @@ bool rs_plan(int64_t N, int Ut, int M, int sms, int s_req, RsPlan& p, bool fma =
     return false;
 }
 
-template <int TYPE, int LR, bool SEG, bool FMA = false>
+template <int TYPE, int LR, bool SEG, bool FMA = false, int NT = 1>
 cudaError_t launch_rows_kernel(const RsArgs& a, const RsPlan& p, cudaStream_t stream) {
-    auto kern = pn_rows_kernel<TYPE, LR, SEG, FMA>;
+    auto kern = pn_rows_kernel<TYPE, LR, SEG, FMA, NT>;
     static std::atomic<bool> opted[64];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -810,7 +839,7 @@ cudaError_t launch_rows_kernel(const RsArgs& a, const RsPlan& p, cudaStream_t st
 // units w, w + 8, ..; segments: the builds are dealt evenly); then the longer of the busiest
 // consumer warp's tasks (0.65 us per 16 rows x one unit) and the CTA's weight stream (35 GB/s per
 // SM); plus 1.5 us for a cluster's final sum and 4 us for segments (all builds before any task).
-inline double rs_cost(const RsPlan& p, int64_t N, int Ut, int M) {
+inline double rs_cost(const RsPlan& p, int64_t N, int Ut, int M, int NT = 1) {
     const int U = (Ut + p.CL - 1) / p.CL;
     const int64_t rows = (N + p.G - 1) / p.G;
     const int64_t groups = (rows + kGroupRows - 1) / kGroupRows;
@@ -820,13 +849,15 @@ inline double rs_cost(const RsPlan& p, int64_t N, int Ut, int M) {
                              : static_cast<double>(groups * per_warp);
     const double builds = seg ? static_cast<double>((U * M + kRsWarps - 1) / kRsWarps) : static_cast<double>(per_warp * M);
     const double stream = static_cast<double>(rows) * U * kUnitBytes / 35e3;
-    return 2.5 + 0.35 * (builds - 1.0) + std::max(0.65 * tasks, stream) + (p.CL > 1 ? 1.5 : 0.0) + (seg ? 4.0 : 0.0);
+    const double per_task = NT == 1 ? 0.65 : 0.65 * 1.4;  // a second n8 tile shares the decode
+    return 2.5 + 0.35 * (builds - 1.0) + std::max(per_task * tasks, stream) + (p.CL > 1 ? 1.5 : 0.0) +
+           (seg ? 4.0 : 0.0);
 }
 
 // The cheapest plan over clusters of 1, 2, 4 and 8 CTAs (cl_req > 0: that size only).
 // resident(CL, plan) = clusters of CL CTAs of that plan's kernel that fit on the GPU at once
 // (clusters of 4 or 8 need that many SMs of one GPC, which does not divide every GPC).
-template <int TYPE, int LR, class Resident>
+template <int TYPE, int LR, int NT, class Resident>
 bool rs_best_plan(int64_t N, int U, int M, int sms, int s_req, bool fma, bool x_in_ring, int cl_req, RsPlan& p,
                   Resident&& resident) {
     bool found = false;
@@ -834,13 +865,13 @@ bool rs_best_plan(int64_t N, int U, int M, int sms, int s_req, bool fma, bool x_
     for (int CL : {1, 2, 4, 8}) {
         if (cl_req > 0 && CL != cl_req) continue;
         RsPlan q;
-        if (!rs_plan<TYPE, LR>(N, U, M, sms, s_req, q, fma, x_in_ring, CL)) continue;
+        if (!rs_plan<TYPE, LR, NT>(N, U, M, sms, s_req, q, fma, x_in_ring, CL)) continue;
         if (CL > 1) {
             const int most = resident(CL, q);
             if (most < 1) continue;
-            if (most < q.G && !rs_plan<TYPE, LR>(N, U, M, sms, s_req, q, fma, x_in_ring, CL, most)) continue;
+            if (most < q.G && !rs_plan<TYPE, LR, NT>(N, U, M, sms, s_req, q, fma, x_in_ring, CL, most)) continue;
         }
-        const double cost = rs_cost(q, N, U, M);
+        const double cost = rs_cost(q, N, U, M, NT);
         if (!found || cost < best) {
             p = q;
             best = cost;
@@ -852,10 +883,10 @@ bool rs_best_plan(int64_t N, int U, int M, int sms, int s_req, bool fma, bool x_
 
 // Clusters of CL CTAs of the plan's kernel that can be resident at once on this device (0 when the
 // query fails).
-template <int TYPE, int LR>
+template <int TYPE, int LR, int NT>
 int rows_resident_clusters(int CL, const RsPlan& q, bool fma) {
-    void (*kern)(RsArgs) = fma ? pn_rows_kernel<TYPE, LR, true, true>
-                               : (q.nseg > 1 ? pn_rows_kernel<TYPE, LR, true> : pn_rows_kernel<TYPE, LR, false>);
+    void (*kern)(RsArgs) = (fma && NT == 1) ? pn_rows_kernel<TYPE, LR, true, NT == 1, NT>
+                           : (q.nseg > 1 ? pn_rows_kernel<TYPE, LR, true, false, NT> : pn_rows_kernel<TYPE, LR, false, false, NT>);
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmemOne)) !=
         cudaSuccess) {
         cudaGetLastError();
@@ -881,7 +912,7 @@ int rows_resident_clusters(int CL, const RsPlan& q, bool fma) {
 }
 
 // rs_best_plan with the device's SM count and resident clusters, cached per device and shape.
-template <int TYPE, int LR>
+template <int TYPE, int LR, int NT>
 bool rs_cached_plan(int64_t N, int U, int M, int s_req, bool fma, bool x_in_ring, int cl_req, RsPlan& p) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return false;
@@ -897,19 +928,20 @@ bool rs_cached_plan(int64_t N, int U, int M, int s_req, bool fma, bool x_in_ring
             return true;
         }
     }
-    auto resident = [fma](int CL, const RsPlan& q) { return rows_resident_clusters<TYPE, LR>(CL, q, fma); };
-    if (!rs_best_plan<TYPE, LR>(N, U, M, device_sm_count(), s_req, fma, x_in_ring, cl_req, p, resident)) return false;
+    auto resident = [fma](int CL, const RsPlan& q) { return rows_resident_clusters<TYPE, LR, NT>(CL, q, fma); };
+    if (!rs_best_plan<TYPE, LR, NT>(N, U, M, device_sm_count(), s_req, fma, x_in_ring, cl_req, p, resident)) return false;
     std::lock_guard<std::mutex> lock(mu);
     if (cache.size() < 4096) cache.emplace(key, p);
     return true;
 }
 
-template <int TYPE, int LR>
+template <int TYPE, int LR, int NT = 1>
 cudaError_t launch_rows(const uint8_t* W, const float* X, float* Y, int* err, int64_t N, int64_t K, int M, int U,
                         int row_bytes, int s_req, bool static_weights, bool fma, int x_ahead, bool x_in_ring,
                         int cl_req, cudaStream_t stream) {
     RsPlan p;
-    if (!rs_cached_plan<TYPE, LR>(N, U, M, s_req, fma, x_in_ring, cl_req, p)) return cudaErrorNotSupported;
+    if ((fma && NT > 1) || !rs_cached_plan<TYPE, LR, NT>(N, U, M, s_req, fma, x_in_ring, cl_req, p))
+        return cudaErrorNotSupported;
     RsArgs a{};
     a.W = W;
     a.X = X;
@@ -935,8 +967,10 @@ cudaError_t launch_rows(const uint8_t* W, const float* X, float* Y, int* err, in
     a.stage_bytes = p.stage_bytes;
     a.x_slot0 = p.x_slot0;
     a.x_ahead = x_ahead;
-    if (fma) return launch_rows_kernel<TYPE, LR, true, true>(a, p, stream);
-    return p.nseg > 1 ? launch_rows_kernel<TYPE, LR, true>(a, p, stream) : launch_rows_kernel<TYPE, LR, false>(a, p, stream);
+    if constexpr (NT == 1)
+        if (fma) return launch_rows_kernel<TYPE, LR, true, true>(a, p, stream);
+    return p.nseg > 1 ? launch_rows_kernel<TYPE, LR, true, false, NT>(a, p, stream)
+                      : launch_rows_kernel<TYPE, LR, false, false, NT>(a, p, stream);
 }
 
 template <int TYPE>
@@ -948,6 +982,12 @@ cudaError_t launch_rows_typed(const uint8_t* W, const float* X, float* Y, int* e
         case 2: return launch_rows<TYPE, 16>(W, X, Y, err, N, K, M, U, row_bytes, s_req, static_weights, fma, xa, xr, cl, stream);
         case 3: return launch_rows<TYPE, 24>(W, X, Y, err, N, K, M, U, row_bytes, s_req, static_weights, fma, xa, xr, cl, stream);
         case 4: return launch_rows<TYPE, 32>(W, X, Y, err, N, K, M, U, row_bytes, s_req, static_weights, fma, xa, xr, cl, stream);
+        case 5:
+        case 6:
+        case 7:
+        case 8:
+            return launch_rows<TYPE, 32, 2>(W, X, Y, err, N, K, M, U, row_bytes, s_req, static_weights, fma, xa, xr, cl,
+                                            stream);
         default: return cudaErrorNotSupported;
     }
 }
@@ -999,13 +1039,13 @@ cudaError_t launch_pn_gemv_mma(int type, const uint8_t* W, int64_t N, int64_t K,
     static std::once_flag once;
     std::call_once(once, [] { env_cluster_config("PNQ_PN_CFG", env); });
     const int req[3] = {c_req > 0 ? c_req : env[0], s_req > 0 ? s_req : env[1], env[2]};
-    // whole rows per CTA when the B operands of every unit fit beside the stages (M <= 4)
+    // the row stream (M <= 8) when its plan fits, else the strip pipeline
     const int row_bytes = static_cast<int>(nb * kBlockBytes);
     const bool fma = env[4] == 1;
     const int x_ahead = env[5] > 0 ? env[5] : 1;
     const bool x_in_ring = env[6] != 1;
     const int rows_cl = env[7];
-    if (env[3] != 2 && M <= 4 && c_req <= 0) {
+    if (env[3] != 2 && M <= 8 && c_req <= 0) {
         const cudaError_t e = (type == kTypePn3t)
                                   ? launch_rows_typed<kTypePn3t>(W, X, Y, err, N, K, M, static_cast<int>(U), row_bytes,
                                                                  req[1], static_weights, fma, x_ahead, x_in_ring, rows_cl, stream)

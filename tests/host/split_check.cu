@@ -161,14 +161,15 @@ void run_type() {
                     }
 }
 
-template <int TYPE, int LR>
+template <int TYPE, int LR, int NT = 1>
 void check_rs_plan(int64_t N, int Ut, int M, int s_req, bool fma = false, int CL = 1, int max_cl = 0) {
-    using C = pnq::Cfg<TYPE, 1, LR>;
+    using C = pnq::Cfg<TYPE, NT, LR>;
     char what[160];
     std::snprintf(what, sizeof what, "rows %s N %lld U %d M %d s %d CL %d max %d", TYPE == pnq::kTypePn3t ? "pn3t" : "pn4t",
                   (long long)N, Ut, M, s_req, CL, max_cl);
     pnq::RsPlan p;
-    if (!pnq::rs_plan<TYPE, LR>(N, Ut, M, 152, s_req, p, fma, true, CL, max_cl)) return;
+    if (!pnq::rs_plan<TYPE, LR, NT>(N, Ut, M, 152, s_req, p, fma, true, CL, max_cl)) return;
+    if (fma && NT > 1) FAIL("CUDA-core decode planned for %d tiles", NT);
     ++plans;
     if (p.CL != CL) FAIL("cluster of %d, asked %d", p.CL, CL);
     if (max_cl > 0 && p.G > max_cl) FAIL("%d clusters, %d resident", p.G, max_cl);
@@ -212,7 +213,7 @@ void check_rs_plan(int64_t N, int Ut, int M, int s_req, bool fma = false, int CL
     }
     std::vector<R> r = {{0, 8ull * (2 * p.S + 3), "barriers"},
                         {p.off_rec, p.off_rec + nrec * C::REC, "B operands"},
-                        {p.off_zb, p.off_zb + 4ull * nrec * pnq::kRsZb, "zero-point terms"},
+                        {p.off_zb, p.off_zb + 4ull * nrec * pnq::rs_zb(NT), "zero-point terms"},
                         {p.off_part, p.off_part + 4ull * pnq::kRsWarps * M * p.rows_pad, "row partials"},
                         {p.off_stage, p.off_stage + 1ull * p.S * p.stage_bytes, "stages"}};
     if (!x_in_ring) r.push_back({p.off_x, p.off_x + xbytes, "x rows"});
@@ -315,7 +316,7 @@ void run_rows() {
     for (int64_t N : {1, 7, 16, 17, 151, 152, 153, 777, 1024, 5120, 12288, 17408, 151936})
         for (int U : {1, 2, 7, 8, 9, 12, 16, 17, 25, 33, 34, 48, 68})
             for (int s : {0, 2, 3, 5})
-                for (int M = 1; M <= 4 && !failures; ++M) {
+                for (int M = 1; M <= 8 && !failures; ++M) {
                     for (bool fma : {false, true}) {
                         for (int CL : {1, 2, 4, 8})
                             for (int mc : {0, 17, 36}) {
@@ -324,6 +325,7 @@ void run_rows() {
                                 if (M == 2) check_rs_plan<TYPE, 16>(N, U, M, s, fma, CL, mc);
                                 if (M == 3) check_rs_plan<TYPE, 24>(N, U, M, s, fma, CL, mc);
                                 if (M == 4) check_rs_plan<TYPE, 32>(N, U, M, s, fma, CL, mc);
+                                if (M > 4) check_rs_plan<TYPE, 32, 2>(N, U, M, s, fma, CL, mc);
                             }
                     }
                 }

@@ -62,7 +62,7 @@ def test_config1_quantizer_packed(oracle):
 @pytest.mark.parametrize("type_", [pnq.PN3T, pnq.PN4T])
 @pytest.mark.parametrize("nblk", [8, 24, 40, 3])
 @pytest.mark.parametrize("N", [1, 33, 130])
-@pytest.mark.parametrize("M", [1, 2, 4, 5, 8, 16])
+@pytest.mark.parametrize("M", [1, 2, 4, 5, 7, 8, 16])
 def test_pn_shapes(oracle, type_, nblk, N, M):
     K = BLK[type_] * nblk
     seed = hash((type_, nblk, N, M)) % 1000
@@ -183,10 +183,12 @@ def sampled_rows(N, n=48, seed=0):
 
 @pytest.mark.parametrize("type_,N,U,M", [(pnq.PN4T, 777, 34, 1), (pnq.PN3T, 300, 17, 1), (pnq.PN4T, 40, 33, 1),
                                          (pnq.PN3T, 2000, 25, 1), (pnq.PN4T, 161, 20, 2), (pnq.PN3T, 999, 12, 3),
-                                         (pnq.PN4T, 153, 16, 4)])
+                                         (pnq.PN4T, 153, 16, 4), (pnq.PN4T, 1500, 34, 6), (pnq.PN3T, 700, 12, 7),
+                                         (pnq.PN4T, 4000, 20, 5), (pnq.PN3T, 2900, 9, 8), (pnq.PN4T, 5000, 34, 2)])
 def test_pn_row_segments(oracle, type_, N, U, M):
     """Rows long enough to be cut into K segments (U = K units of 8 blocks), with segments of unequal
-    length and CTAs whose last 16-row group is ragged."""
+    length and CTAs whose last 16-row group is ragged; at M = 5..8 two n8 tiles per task; rows
+    whose plan splits K over a cluster (unequal unit counts per CTA)."""
     K = BLK[type_] * 8 * U
     seed = 31 * U + N
     W = synth.pn_random_blocks(type_, N, K, seed=seed).numpy()
