@@ -305,6 +305,7 @@ struct NrArgs {
     int* err;
     float g;
     int N, K, M, U, G, S, nseg, rows_pad;
+    int CL;  // CTAs of a cluster: CTA r of a cluster takes K units [r U / CL, (r + 1) U / CL) of its rows
     unsigned flags;
     uint32_t off_rec, off_so, off_x, off_part, off_stage, stage_bytes, scale_region;  // scale region offset in a stage
 };
@@ -315,7 +316,10 @@ __global__ void __launch_bounds__(kNrThreads, 1) nv_rows_kernel(const __grid_con
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* base = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     const uint32_t bar0 = smem_addr(base);
-    const int S = a.S, M = a.M, U = a.U, nseg = a.nseg;
+    const int S = a.S, M = a.M, nseg = a.nseg;
+    const int CL = a.CL, cr = static_cast<int>(blockIdx.x) % CL, cid = static_cast<int>(blockIdx.x) / CL;
+    const int ua = cr * a.U / CL, U = (cr + 1) * a.U / CL - ua;  // this CTA's K units [ua, ua + U)
+    const int xk = U * kUnitK;                                   // bf16 of an activation row it reads
     auto full = [&](int s) { return bar0 + 8u * s; };
     auto empty = [&](int s) { return bar0 + 8u * (S + s); };
     const uint32_t xfull = bar0 + 8u * (2 * S), xreq = bar0 + 8u * (2 * S + 1);
@@ -324,7 +328,7 @@ __global__ void __launch_bounds__(kNrThreads, 1) nv_rows_kernel(const __grid_con
     auto so = [&](int u) { return reinterpret_cast<float*>(base + a.off_so) + u * 4; };
     __shared__ int seg_tab[kNrMaxSeg + 1];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t r0 = static_cast<int64_t>(blockIdx.x) * a.N / a.G, r1 = static_cast<int64_t>(blockIdx.x + 1) * a.N / a.G;
+    const int64_t r0 = static_cast<int64_t>(cid) * a.N / a.G, r1 = static_cast<int64_t>(cid + 1) * a.N / a.G;
     const int nrows = static_cast<int>(r1 - r0);
     const int nstages = (nrows + kGroupRows - 1) / kGroupRows * nseg;
     float* part = reinterpret_cast<float*>(base + a.off_part);  // [warp][m][rows_pad]
@@ -367,10 +371,10 @@ __global__ void __launch_bounds__(kNrThreads, 1) nv_rows_kernel(const __grid_con
             if (lane < mine) {
                 const int64_t row = r0 + i * kGroupRows + pr + lane;
                 const uint32_t dst = smem_addr(stage(slot));
-                bulk_g2s(dst + static_cast<uint32_t>((pr + lane) * pc), a.codes + row * crow + u0 * 128,
+                bulk_g2s(dst + static_cast<uint32_t>((pr + lane) * pc), a.codes + row * crow + (ua + u0) * 128,
                          static_cast<uint32_t>(cb), full(slot), pol);
-                bulk_g2s(dst + a.scale_region + static_cast<uint32_t>((pr + lane) * ps), a.scales + row * srow_b + u0 * 16,
-                         static_cast<uint32_t>(sb), full(slot), pol);
+                bulk_g2s(dst + a.scale_region + static_cast<uint32_t>((pr + lane) * ps),
+                         a.scales + row * srow_b + (ua + u0) * 16, static_cast<uint32_t>(sb), full(slot), pol);
             }
             if (++j == nseg) {
                 j = 0;
@@ -387,14 +391,14 @@ __global__ void __launch_bounds__(kNrThreads, 1) nv_rows_kernel(const __grid_con
         const uint32_t boff = static_cast<uint32_t>((4 * min(g, M - 1) + c) * 16);
         float* mine = part + warp * M * a.rows_pad;
         for (int e = lane; e < M * a.rows_pad; e += 32) mine[e] = 0.0f;
-        const uint16_t* xs = reinterpret_cast<const uint16_t*>(base + a.off_x);  // [M][K] bf16
+        const uint16_t* xs = reinterpret_cast<const uint16_t*>(base + a.off_x);  // [M][xk] bf16: the CTA's units
         if (warp == 0) {
             griddep_wait();  // X belongs to the previous grid until now
             if (lane == 0) {
-                const uint32_t row = static_cast<uint32_t>(a.K) * 2u;
+                const uint32_t row = static_cast<uint32_t>(xk) * 2u;
                 mbar_arrive_expect_tx(xfull, row * static_cast<uint32_t>(M));
                 for (int m = 0; m < M; ++m)
-                    bulk_g2s_plain(smem_addr(xs) + m * row, a.X + static_cast<size_t>(m) * a.K, row, xfull);
+                    bulk_g2s_plain(smem_addr(xs) + m * row, a.X + static_cast<size_t>(m) * a.K + ua * kUnitK, row, xfull);
             }
             __syncwarp();
         }
@@ -403,7 +407,7 @@ __global__ void __launch_bounds__(kNrThreads, 1) nv_rows_kernel(const __grid_con
         if (ok)
             for (int p = warp; p < U * M; p += kNrWarps) {
                 const int u = p / M, m = p - u * M;
-                nv_build_row_compact<LR>(rec(u), so(u), xs + static_cast<size_t>(m) * a.K + u * kUnitK, m, a.g, lane);
+                nv_build_row_compact<LR>(rec(u), so(u), xs + static_cast<size_t>(m) * xk + u * kUnitK, m, a.g, lane);
             }
         named_sync(1, 32 * kNrWarps);
         int k0 = warp;
@@ -454,22 +458,53 @@ __global__ void __launch_bounds__(kNrThreads, 1) nv_rows_kernel(const __grid_con
     }
 
     __syncthreads();
-    griddep_wait();  // Y may still be read by the previous grid
+    if (CL == 1) {
+        griddep_wait();  // Y may still be read by the previous grid
+        for (int e = threadIdx.x; e < M * nrows; e += kNrThreads) {
+            const int m = e / nrows, r = e - m * nrows;
+            float v = 0.0f;
+            for (int w = 0; w < kNrWarps; ++w) v += part[(w * M + m) * a.rows_pad + r];
+            a.Y[static_cast<size_t>(m) * a.N + r0 + r] = v;
+        }
+        return;
+    }
+    // this CTA's sum over its warps, in warp 0's slice; then CTA cr writes a share of the rows
+    // from the sums of every CTA of the cluster (distributed shared memory, CTA order)
     for (int e = threadIdx.x; e < M * nrows; e += kNrThreads) {
         const int m = e / nrows, r = e - m * nrows;
         float v = 0.0f;
         for (int w = 0; w < kNrWarps; ++w) v += part[(w * M + m) * a.rows_pad + r];
-        a.Y[static_cast<size_t>(m) * a.N + r0 + r] = v;
+        part[m * a.rows_pad + r] = v;
     }
+    cluster_sync();
+    griddep_wait();  // Y may still be read by the previous grid
+    {
+        const int E = M * nrows, e0 = cr * E / CL, e1 = (cr + 1) * E / CL;
+        const uint32_t pbase = smem_addr(part);
+        for (int e = e0 + static_cast<int>(threadIdx.x); e < e1; e += kNrThreads) {
+            const int m = e / nrows, r = e - m * nrows;
+            const uint32_t off = 4u * static_cast<uint32_t>(m * a.rows_pad + r);
+            float v = 0.0f;
+            for (int q = 0; q < CL; ++q) v += ld_dsmem_f32(pbase + off, static_cast<uint32_t>(q));
+            a.Y[static_cast<size_t>(m) * a.N + r0 + r] = v;
+        }
+    }
+    cluster_sync();  // no CTA leaves while another still reads its sums
 }
 
-// Plan: grid (one CTA per SM), segments (whole rows of at most 20 units, else segments of at most
-// 8, 6, 4 units), the deepest ring of 8..3 stages (2 as a last resort); false when nothing fits.
+// Plan: grid (clusters of CL CTAs splitting K, one CTA per SM, no more clusters than can be
+// resident when max_clusters > 0), segments of one CTA's units (whole rows of at most 20 units,
+// else segments of at most 8, 6, 4 units), the deepest ring of 8..3 stages (2 as a last resort);
+// false when nothing fits.
 template <int LR>
-bool nr_plan(int64_t N, int U, int M, int sms, NrArgs& a, uint32_t& total) {
+bool nr_plan(int64_t N, int Ut, int M, int sms, NrArgs& a, uint32_t& total, int CL = 1, int max_clusters = 0) {
     constexpr int REC = 8 * LR * 16;
+    if (CL < 1 || CL > 8 || sms / CL < 1 || Ut < CL) return false;
+    const int U = (Ut + CL - 1) / CL;  // the most units of a CTA
     if (U < 1 || M < 1 || 4 * M > LR || (U + 3) / 4 > kNrMaxSeg) return false;
-    a.G = static_cast<int>(std::min<int64_t>(sms, N));
+    a.CL = CL;
+    const int ncl = max_clusters > 0 ? std::min(sms / CL, max_clusters) : sms / CL;
+    a.G = static_cast<int>(std::min<int64_t>(ncl, N));
     const int64_t rows_max = (N + a.G - 1) / a.G;
     a.rows_pad = static_cast<int>((rows_max + kGroupRows - 1) / kGroupRows * kGroupRows);
     a.off_rec = align_up(8u * (2u * kNrMaxStages + 2), 128);
@@ -493,12 +528,99 @@ bool nr_plan(int64_t N, int U, int M, int sms, NrArgs& a, uint32_t& total) {
     return false;
 }
 
+// Estimated time (us) of an NVFP4 row-stream plan, fitted like the PN one: ~2.5 us until the
+// first stage is multiplied, 0.2 us per further round of operand builds, the longer of the dealt
+// tasks (0.5 us per 16 rows x one 256-weight unit) and the weight stream (35 GB/s per SM), and
+// 1.5 us for a cluster's final sum.
+inline double nr_cost(const NrArgs& a, int64_t N, int Ut, int M) {
+    const int U = (Ut + a.CL - 1) / a.CL;
+    const int64_t rows = (N + a.G - 1) / a.G;
+    const int64_t groups = (rows + kGroupRows - 1) / kGroupRows;
+    const double tasks = static_cast<double>((groups * U + kNrWarps - 1) / kNrWarps);
+    const double builds = static_cast<double>((U * M + kNrWarps - 1) / kNrWarps);
+    const double stream = static_cast<double>(rows) * U * 144.0 / 35e3;
+    return 2.5 + 0.2 * (builds - 1.0) + std::max(0.5 * tasks, stream) + (a.CL > 1 ? 1.5 : 0.0);
+}
+
+// Clusters of CL CTAs of the row kernel that can be resident at once (0 when the query fails).
+template <int LR>
+int nv_rows_resident_clusters(int CL, int ncl, uint32_t total) {
+    if (cudaFuncSetAttribute(nv_rows_kernel<LR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kNrSmem)) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    cudaLaunchConfig_t lc{};
+    lc.gridDim = dim3(ncl * CL, 1, 1);
+    lc.blockDim = dim3(kNrThreads, 1, 1);
+    lc.dynamicSmemBytes = total + 1024u;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(CL);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, nv_rows_kernel<LR>, &lc) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return n;
+}
+
+// The cheapest plan over clusters of 1, 2, 4 and 8 CTAs (cl_req > 0: that size only), cached per
+// device and shape.
+template <int LR>
+bool nr_best_plan(int64_t N, int U, int M, int cl_req, NrArgs& a, uint32_t& total) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    using Key = std::tuple<int, int64_t, int, int, int>;
+    static std::mutex mu;
+    static std::map<Key, std::pair<NrArgs, uint32_t>> cache;
+    const Key key{dev, N, U, M, cl_req};
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        auto it = cache.find(key);
+        if (it != cache.end()) {
+            a = it->second.first;
+            total = it->second.second;
+            return true;
+        }
+    }
+    const int sms = device_sm_count();
+    bool found = false;
+    double best = 0.0;
+    for (int CL : {1, 2, 4, 8}) {
+        if (cl_req > 0 && CL != cl_req) continue;
+        NrArgs q{};
+        uint32_t t = 0;
+        if (!nr_plan<LR>(N, U, M, sms, q, t, CL)) continue;
+        if (CL > 1) {
+            const int most = nv_rows_resident_clusters<LR>(CL, q.G, t);
+            if (most < 1) continue;
+            if (most < q.G && !nr_plan<LR>(N, U, M, sms, q, t, CL, most)) continue;
+        }
+        const double cost = nr_cost(q, N, U, M);
+        if (!found || cost < best) {
+            a = q;
+            total = t;
+            best = cost;
+            found = true;
+        }
+    }
+    if (!found) return false;
+    std::lock_guard<std::mutex> lock(mu);
+    if (cache.size() < 4096) cache.emplace(key, std::make_pair(a, total));
+    return true;
+}
+
 template <int LR>
 cudaError_t launch_nv_rows(const Nvfp4View& w, int64_t N, int64_t K, const uint16_t* X, int M, float* Y, int* err,
-                           bool static_weights, cudaStream_t stream) {
+                           bool static_weights, int cl_req, cudaStream_t stream) {
     NrArgs a{};
     uint32_t total = 0;
-    if (!nr_plan<LR>(N, static_cast<int>(K / kUnitK), M, device_sm_count(), a, total)) return cudaErrorNotSupported;
+    if (!nr_best_plan<LR>(N, static_cast<int>(K / kUnitK), M, cl_req, a, total)) return cudaErrorNotSupported;
     a.codes = w.codes;
     a.scales = w.scales;
     a.X = X;
@@ -522,15 +644,19 @@ cudaError_t launch_nv_rows(const Nvfp4View& w, int64_t N, int64_t K, const uint1
         opted[dev].store(true, std::memory_order_relaxed);
     }
     cudaLaunchConfig_t lc{};
-    lc.gridDim = dim3(a.G, 1, 1);
+    lc.gridDim = dim3(a.G * a.CL, 1, 1);
     lc.blockDim = dim3(kNrThreads, 1, 1);
     lc.dynamicSmemBytes = total + 1024u;
     lc.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = static_cast<unsigned>(a.CL);
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
     lc.attrs = attr;
-    lc.numAttrs = 1;
+    lc.numAttrs = 2;
     return cudaLaunchKernelEx(&lc, kern, a);
 }
 
@@ -565,17 +691,20 @@ cudaError_t launch_nvfp4_gemv_mma(const Nvfp4View& w, int64_t N, int64_t K, cons
         !encode_u32_map(&maps[2], w.codes, N, K / 8, kCodeRow / 4, kStageRows, true) ||
         !encode_u32_map(&maps[3], w.scales, N, K / 64, kScaleRow / 4, kStageRows, false))
         return cudaErrorNotSupported;
-    static int env[3];  // PNQ_NV_CFG = "CTAs per cluster, stages, CTAs per SM", read once
+    // PNQ_NV_CFG = "CTAs per cluster, stages, CTAs per SM (strip pipeline), CTAs per cluster splitting K
+    // (row stream; 0: cheapest)", read once
+    static int env[4];
     static std::once_flag once;
     std::call_once(once, [] { env_cluster_config("PNQ_NV_CFG", env); });
     const int req[3] = {c_req > 0 ? c_req : env[0], s_req > 0 ? s_req : env[1], env[2]};
     const int U = static_cast<int>(K / kUnitK);
-    // whole rows per CTA when every unit's B records and all of x fit beside the ring (M <= 4)
+    // the row stream when a CTA's units' B records and x fit beside the ring (M <= 4)
     if (M <= 4 && c_req <= 0 && env[0] == 0 && env[1] == 0) {
-        const cudaError_t e = (M == 1)   ? launch_nv_rows<4>(w, N, K, X, M, Y, err, static_weights, stream)
-                              : (M == 2) ? launch_nv_rows<8>(w, N, K, X, M, Y, err, static_weights, stream)
-                              : (M == 3) ? launch_nv_rows<12>(w, N, K, X, M, Y, err, static_weights, stream)
-                                         : launch_nv_rows<16>(w, N, K, X, M, Y, err, static_weights, stream);
+        const int cl = env[3];
+        const cudaError_t e = (M == 1)   ? launch_nv_rows<4>(w, N, K, X, M, Y, err, static_weights, cl, stream)
+                              : (M == 2) ? launch_nv_rows<8>(w, N, K, X, M, Y, err, static_weights, cl, stream)
+                              : (M == 3) ? launch_nv_rows<12>(w, N, K, X, M, Y, err, static_weights, cl, stream)
+                                         : launch_nv_rows<16>(w, N, K, X, M, Y, err, static_weights, cl, stream);
         if (e != cudaErrorNotSupported) return e;
     }
     if (M <= 8) return launch_nt<1>(maps, w.g, X, Y, err, N, K, M, U, req, static_weights, stream);

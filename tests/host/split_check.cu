@@ -266,13 +266,23 @@ void check_rs_plan(int64_t N, int Ut, int M, int s_req, bool fma = false, int CL
 }
 
 template <int LR>
-void check_nr_plan(int64_t N, int U, int M) {
+void check_nr_plan(int64_t N, int Ut, int M, int CL = 1, int max_cl = 0) {
     char what[128];
-    std::snprintf(what, sizeof what, "nvfp4 rows N %lld U %d M %d", (long long)N, U, M);
+    std::snprintf(what, sizeof what, "nvfp4 rows N %lld U %d M %d CL %d max %d", (long long)N, Ut, M, CL, max_cl);
     pnq::NrArgs a{};
     uint32_t total = 0;
-    if (!pnq::nr_plan<LR>(N, U, M, 152, a, total)) return;
+    if (!pnq::nr_plan<LR>(N, Ut, M, 152, a, total, CL, max_cl)) return;
     ++plans;
+    const int U = (Ut + CL - 1) / CL;  // the most units of a CTA
+    if (a.CL != CL) FAIL("cluster of %d, asked %d", a.CL, CL);
+    if (max_cl > 0 && a.G > max_cl) FAIL("%d clusters, %d resident", a.G, max_cl);
+    if (1ll * a.G * CL > 152) FAIL("%d CTAs", a.G * CL);
+    for (int r = 0, prev_u = 0; r < CL; ++r) {
+        const int ua = r * Ut / CL, ub = (r + 1) * Ut / CL;
+        if (ua != prev_u || ub <= ua || ub - ua > U) FAIL("CTA %d of the cluster has units [%d, %d)", r, ua, ub);
+        prev_u = ub;
+        if (r == CL - 1 && ub != Ut) FAIL("cluster units end at %d", ub);
+    }
     constexpr int REC = 8 * LR * 16;
     if (a.S < 2 || a.S > pnq::kNrMaxStages) FAIL("%d stages", a.S);
     if (total + 1024u > pnq::kNrSmem) FAIL("total %u", total);
@@ -358,12 +368,15 @@ int main() {
     run_rows<pnq::kTypePn3t>();
     run_rows<pnq::kTypePn4t>();
     for (int64_t N : {1, 9, 151, 152, 1000, 5120, 17408, 151936})
-        for (int U : {1, 2, 4, 20, 21, 40, 68, 100}) {
-            check_nr_plan<4>(N, U, 1);
-            check_nr_plan<8>(N, U, 2);
-            check_nr_plan<12>(N, U, 3);
-            check_nr_plan<16>(N, U, 4);
-        }
+        for (int U : {1, 2, 4, 20, 21, 40, 68, 100})
+            for (int CL : {1, 2, 4, 8})
+                for (int mc : {0, 15, 36}) {
+                    if (CL == 1 && mc) continue;
+                    check_nr_plan<4>(N, U, 1, CL, mc);
+                    check_nr_plan<8>(N, U, 2, CL, mc);
+                    check_nr_plan<12>(N, U, 3, CL, mc);
+                    check_nr_plan<16>(N, U, 4, CL, mc);
+                }
     if (failures) return 1;
     std::printf("ok %ld plans, %ld splits\n", plans, splits);
     return 0;

@@ -287,7 +287,8 @@ for type_, N, K, M in [(124, 200, 80*48, 1), (125, 130, 64*80, 3), (125, 64, 64*
         Y = pnq.gemv(type_, W.cuda(), torch.from_numpy(X).cuda(), N, K, flags=flags).cpu().numpy()
         Yr, Ar = oracle.gemv(type_, W.numpy(), N, K, X)
         assert_within_tolerance(Y, Yr, Ar, str((type_, N, K, M, flags)))
-for N, K, M in [(130, 256*6, 1), (33, 256*9, 5), (64, 256*2, 16), (300, 256*10, 12)]:
+for N, K, M in [(130, 256*6, 1), (33, 256*9, 5), (64, 256*2, 16), (300, 256*10, 12), (777, 256*68, 2),
+                (151, 256*21, 4)]:
     c, s, g = synth.nvfp4_random(N, K, seed=K)
     Xb = synth.activations_bf16(M, K, seed=K)
     Y = pnq.gemv(1004, (c.cuda(), s.cuda(), g), torch.from_numpy(Xb.view(np.int16)).cuda(), N, K).cpu().numpy()
@@ -303,7 +304,8 @@ print(json.dumps({{"ok": True, "device_error": pnq.device_error()}}))
                                             ("0,3,0,1", "0,5,2"), ("0,8,0,1", "0,3"), ("0,3,0,0", "1,4"),
                                             ("0,6,1,2", "2,6,1"), ("0,0,0,1,1", "0,0"), ("0,2,0,1,1", "0,0"),
                                             ("0,0,0,1,0,0,0,2", "0,0"), ("0,3,0,1,0,0,0,4", "0,0"),
-                                            ("0,0,0,1,0,8,1,8", "0,0"), ("0,0,0,1,1,0,0,2", "0,0")])
+                                            ("0,0,0,1,0,8,1,8", "0,0"), ("0,0,0,1,1,0,0,2", "0,0"),
+                                            ("0,0,0,1", "0,0,0,2"), ("0,0,0,1", "0,0,0,4"), ("0,0,0,1", "0,0,0,8")])
 def test_tile_and_grid_configs(pn_cfg, nv_cfg):
     """Forced configurations, read once per process (so each runs in a child): the PN path through
     PNQ_PN_CFG = "CTAs per cluster, weight stages, CTAs per SM, path, decode, x ahead, x apart, row
@@ -311,7 +313,7 @@ def test_tile_and_grid_configs(pn_cfg, nv_cfg):
     FMA decode of the row path, which shapes outside its plan leave to the generic path; x ahead =
     weight stages issued before x is requested; x apart 1 = x outside the weight ring; row clusters
     = CTAs splitting K in the row stream) and the NVFP4 path through PNQ_NV_CFG = "CTAs per
-    cluster, weight stages, CTAs per SM" (0 = automatic)."""
+    cluster, weight stages, CTAs per SM, row clusters" (0 = automatic)."""
     env = dict(os.environ, PNQ_PN_CFG=pn_cfg, PNQ_NV_CFG=nv_cfg, PNQ_FORCE_KERNEL="mma")
     r = subprocess.run([sys.executable, "-c", CHILD.format(root=ROOT)], env=env, capture_output=True, text=True,
                        timeout=600)
