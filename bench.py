@@ -532,9 +532,9 @@ def run_ours(args):
                            hbm_fraction=round(value / world / peak, 4)),
             "roofline": {"bound": "hbm", "achieved": round(dom_gbs, 2), "peak": peak, "unit": "GB/s",
                          "frac": round(dom_gbs / peak, 4), "traffic": traffic,
-                         "kernel": ("pn_rows_kernel<pn3t> (row stream, mma.sync decode)" if M <= 4 else
-                                    f"cluster_gemv_kernel<PnMma<pn3t, NT={min(4, 1 << ((2 * M + 7) // 8 - 1).bit_length())}>> "
-                                    "(strip pipeline)"), "launches": len(dom),
+                         "kernel": (f"pn_rows_kernel<pn3t, NT={1 if M <= 4 else 2}> (row stream, mma.sync decode)"
+                                    if M <= 8 else "cluster_gemv_kernel<PnMma<pn3t, NT=4>> (strip pipeline)"),
+                         "launches": len(dom),
                          "algorithmic_bytes_per_launch": round(dom_bytes / len(dom)),
                          "avg_launch_us": round(sum(dur_ms) / len(dur_ms) * 1e3, 3),
                          "timing": f"graph of the step's {len(dom)} pn3t launches replayed back to back, "

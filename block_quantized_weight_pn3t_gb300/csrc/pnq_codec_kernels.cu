@@ -81,28 +81,48 @@ __global__ void __launch_bounds__(kThreads) pn_dequant_kernel(const uint8_t* __r
 
 // One thread per two code bytes (four weights, one float4): code byte c of the flat [N][K/2]
 // array belongs to scale c / 8 of the flat [N][K/16] array; a warp writes 512 contiguous bytes.
+// A thread takes UNR such pairs a grid stride apart per round, all loads first, so that UNR code
+// and scale loads per thread are in flight at once.
+constexpr int kNvUnroll = 4;
+
 template <bool DIV, bool VEC>
 __global__ void __launch_bounds__(kThreads) nvfp4_dequant_kernel(const uint8_t* __restrict__ codes,
                                                                    const uint8_t* __restrict__ scales, float g,
                                                                    int64_t npairs, float* __restrict__ out) {
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < npairs; i += stride) {
-        const uint32_t c = VEC ? __ldg(reinterpret_cast<const unsigned short*>(codes) + i)
-                               : (static_cast<uint32_t>(__ldg(codes + 2 * i)) |
-                                  (static_cast<uint32_t>(__ldg(codes + 2 * i + 1)) << 8));
-        const float s = e4m3_to_f32(__ldg(scales + (i >> 2)));
-        float v[4];
+    for (int64_t i0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i0 < npairs;
+         i0 += kNvUnroll * stride) {
+        uint32_t c[kNvUnroll], sb[kNvUnroll];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            // e2m1 * e4m3 is exact in fp32; the product with (quotient by) g is the single rounding
-            const float p = e2m1_to_f32((c >> (4 * q)) & 15u) * s;
-            v[q] = DIV ? __fdiv_rn(p, g) : __fmul_rn(p, g);
+        for (int u = 0; u < kNvUnroll; ++u) {
+            const int64_t i = i0 + u * stride;
+            c[u] = 0u;
+            sb[u] = 0u;
+            if (i < npairs) {
+                c[u] = VEC ? __ldg(reinterpret_cast<const unsigned short*>(codes) + i)
+                           : (static_cast<uint32_t>(__ldg(codes + 2 * i)) |
+                              (static_cast<uint32_t>(__ldg(codes + 2 * i + 1)) << 8));
+                sb[u] = __ldg(scales + (i >> 2));
+            }
         }
-        if (VEC) {
-            reinterpret_cast<float4*>(out)[i] = make_float4(v[0], v[1], v[2], v[3]);
-        } else {
 #pragma unroll
-            for (int q = 0; q < 4; ++q) out[4 * i + q] = v[q];
+        for (int u = 0; u < kNvUnroll; ++u) {
+            const int64_t i = i0 + u * stride;
+            if (i >= npairs) break;
+            const float s = e4m3_to_f32(sb[u]);
+            float v[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                // e2m1 * e4m3 is exact in fp32; the product with (quotient by) g is the single rounding
+                const float p = e2m1_to_f32((c[u] >> (4 * q)) & 15u) * s;
+                v[q] = DIV ? __fdiv_rn(p, g) : __fmul_rn(p, g);
+            }
+            if (VEC) {
+                reinterpret_cast<float4*>(out)[i] = make_float4(v[0], v[1], v[2], v[3]);
+            } else {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) out[4 * i + q] = v[q];
+            }
         }
     }
 }
@@ -110,42 +130,52 @@ __global__ void __launch_bounds__(kThreads) nvfp4_dequant_kernel(const uint8_t* 
 // One warp per row. Half h of a row is half h mod 17 of its block (half 0: d, invalid if its
 // exponent field is all ones; halves 1..16: word halves, whose bit 15 — word bits 15 and 31 — is
 // reserved in pn3t). With 16-byte aligned rows (W aligned, row length a multiple of 16 bytes) a
-// lane reads 8 halves per 16-byte load; otherwise 16-bit loads. Positions mod 17 stay in 32 bits.
+// lane reads 8 halves per 16-byte load, five loads in flight (a 2,176-byte pn3t row in one round
+// trip of the warp), and checks a chunk's halves as four
+// 32-bit words: the chunk starting at half 8q holds at most one d, half (17 - 8q mod 17) mod 17
+// of the chunk when that is below 8; every other half of a pn3t chunk must have bit 15 clear.
+// Otherwise 16-bit loads. Positions mod 17 stay in 32 bits.
+constexpr int kValLoads = 5;
+
 template <int TYPE, bool VEC>
 __global__ void __launch_bounds__(kThreads) pn_validate_kernel(const uint8_t* __restrict__ W, int64_t n_rows,
                                                                  int row_halves, int32_t* __restrict__ flags) {
     const int lane = threadIdx.x & 31;
     const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
-    auto bad_half = [](int pos, uint32_t v) {
-        return pos == 0 ? (v & 0x7C00u) == 0x7C00u : (TYPE == kTypePn3t && (v & 0x8000u) != 0);
-    };
     for (int64_t row = warp0; row < n_rows; row += nwarps) {
         const unsigned short* h = reinterpret_cast<const unsigned short*>(W) + row * row_halves;
         bool bad = false;
         if (VEC) {
-            // four 16-byte loads in flight per lane before any is checked
             const uint4* v = reinterpret_cast<const uint4*>(h);
             const int nq = row_halves / 8;
-            for (int q0 = lane; q0 < nq; q0 += 4 * 32) {
-                uint4 u[4];
+            for (int q0 = lane; q0 < nq; q0 += kValLoads * 32) {
+                uint4 u[kValLoads];
 #pragma unroll
-                for (int j = 0; j < 4; ++j) u[j] = (q0 + 32 * j < nq) ? __ldg(v + q0 + 32 * j) : make_uint4(0, 0, 0, 0);
+                for (int j = 0; j < kValLoads; ++j) u[j] = (q0 + 32 * j < nq) ? __ldg(v + q0 + 32 * j) : make_uint4(0, 0, 0, 0);
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const uint32_t w[4] = {u[j].x, u[j].y, u[j].z, u[j].w};
-                    int pos = (8 * (q0 + 32 * j)) % 17;  // zero words past the row are valid halves
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        bad |= bad_half(pos, w[k] & 0xFFFFu);
-                        pos = (pos == 16) ? 0 : pos + 1;
-                        bad |= bad_half(pos, w[k] >> 16);
-                        pos = (pos == 16) ? 0 : pos + 1;
+                for (int j = 0; j < kValLoads; ++j) {
+                    const int p0 = (8 * (q0 + 32 * j)) % 17;  // position of the chunk's first half
+                    const int hd = p0 == 0 ? 0 : 17 - p0;       // the chunk's d half, if below 8
+                    const int wd = hd >> 1;
+                    const uint32_t w = wd == 0 ? u[j].x : wd == 1 ? u[j].y : wd == 2 ? u[j].z : u[j].w;
+                    // zero chunks past the row are valid halves
+                    bad |= hd < 8 && ((w >> (16 * (hd & 1))) & 0x7C00u) == 0x7C00u;
+                    if (TYPE == kTypePn3t) {
+                        const uint32_t dm = hd < 8 ? ((hd & 1) ? 0x80000000u : 0x00008000u) : 0u;
+                        const uint32_t r = (u[j].x & (0x80008000u ^ (wd == 0 ? dm : 0u))) |
+                                           (u[j].y & (0x80008000u ^ (wd == 1 ? dm : 0u))) |
+                                           (u[j].z & (0x80008000u ^ (wd == 2 ? dm : 0u))) |
+                                           (u[j].w & (0x80008000u ^ (wd == 3 ? dm : 0u)));
+                        bad |= r != 0u;
                     }
                 }
             }
         } else {
-            for (int i = lane; i < row_halves; i += 32) bad |= bad_half(i % 17, __ldg(h + i));
+            for (int i = lane; i < row_halves; i += 32) {
+                const uint32_t x = __ldg(h + i);
+                bad |= (i % 17 == 0) ? (x & 0x7C00u) == 0x7C00u : (TYPE == kTypePn3t && (x & 0x8000u) != 0);
+            }
         }
         bad = __any_sync(0xffffffffu, bad);
         if (lane == 0) flags[row] = bad ? 1 : 0;
@@ -207,7 +237,7 @@ cudaError_t launch_nvfp4_dequant(const Nvfp4View& w, int64_t n_rows, int64_t K, 
                                  cudaStream_t stream) {
     const int64_t npairs = n_rows * (K / 4);
     if (npairs == 0) return cudaSuccess;
-    const int grid = grid_for(npairs, 1);
+    const int grid = grid_for(npairs, kNvUnroll);
     const bool vec = (reinterpret_cast<uintptr_t>(w.codes) & 1u) == 0 && aligned16(out);
     if (w.div) {
         if (vec) nvfp4_dequant_kernel<true, true><<<grid, kThreads, 0, stream>>>(w.codes, w.scales, w.g, npairs, out);
