@@ -334,10 +334,10 @@ SINGLE_SHAPES = [("pn4t 5120x17408 M=1 (down-projection shape)", PN4T, 5120, 174
                  ("nvfp4 17408x5120 M=1", NVFP4, 17408, 5120), ("nvfp4 5120x17408 M=1", NVFP4, 5120, 17408)]
 
 
-def single_call_lines(dev, stream, flags, peak, warmup):
-    """One GEMV shape at a time (M = 1, the same flags as the step), called back to back in a
-    graph that rotates through weight copies whose total exceeds the L2 twice (so every call
-    reads HBM): us per call, weight GB/s and the fraction of the measured HBM rate."""
+def single_call_lines(dev, stream, flags, peak, warmup, M=1):
+    """One GEMV shape at a time (M activation rows, the same flags as the step), called back to
+    back in a graph that rotates through weight copies whose total exceeds the L2 twice (so every
+    call reads HBM): us per call, weight GB/s and the fraction of the measured HBM rate."""
     import block_quantized_weight_pn3t_gb300 as pnq
     from block_quantized_weight_pn3t_gb300 import synth
     out = []
@@ -347,23 +347,23 @@ def single_call_lines(dev, stream, flags, peak, warmup):
         if t == NVFP4:
             ws = [synth.nvfp4_random(N, K, seed=SEED, stream=c, device=dev) for c in range(n_copies)]
             descs = [pnq.nvfp4_weights(c.data_ptr(), sc.data_ptr(), g) for c, sc, g in ws]
-            X = torch.from_numpy(synth.activations_bf16(1, K, seed=SEED).view(np.int16)).to(dev)
+            X = torch.from_numpy(synth.activations_bf16(M, K, seed=SEED).view(np.int16)).to(dev)
         else:
             ws = [synth.pn_random_blocks(t, N, K, seed=SEED, stream=c, device=dev) for c in range(n_copies)]
             descs = [w.data_ptr() for w in ws]
-            X = torch.from_numpy(synth.activations(1, K, seed=SEED)).to(dev)
-        Y = torch.empty((1, N), dtype=torch.float32, device=dev)
+            X = torch.from_numpy(synth.activations(M, K, seed=SEED)).to(dev)
+        Y = torch.empty((M, N), dtype=torch.float32, device=dev)
         n = n_copies * max(1, 60 // n_copies)
 
         def launch(h):
             for i in range(n):
-                rc = pnq.gemv_ex_ptr(t, descs[i % n_copies], N, K, X.data_ptr(), 1, Y.data_ptr(), flags, h)
+                rc = pnq.gemv_ex_ptr(t, descs[i % n_copies], N, K, X.data_ptr(), M, Y.data_ptr(), flags, h)
                 if rc != 0:
                     raise pnq.PnqError("pnq_gemv", rc)
 
         us = graph_us_per_launch(launch, n, stream, reps=5, warmup=warmup)
         gbs = wbytes / (us * 1e-6) / 1e9
-        out.append({"shape": label, "us_per_call": round(us, 3), "weight_bytes": wbytes, "achieved": round(gbs, 1),
+        out.append({"shape": label.replace("M=1", f"M={M}"), "us_per_call": round(us, 3), "weight_bytes": wbytes, "achieved": round(gbs, 1),
                     "frac": round(gbs / peak, 4), "weight_copies": n_copies, "launches": n})
         del ws
         torch.cuda.empty_cache()
@@ -514,7 +514,7 @@ def run_ours(args):
         us = graph_us_per_launch(launch, len(sub), stream, reps=max(3, args.steps // 20), warmup=args.warmup)
         gbs = N * row_bytes(t, K) / (us * 1e-6) / 1e9
         per_proj[name] = {"us_per_call": round(us, 3), "achieved": round(gbs, 1), "frac": round(gbs / peak, 4)}
-    singles = single_call_lines(dev, stream, flags, peak, args.warmup) if M == 1 and not args.no_singles else None
+    singles = single_call_lines(dev, stream, flags, peak, args.warmup, M) if not args.no_singles else None
 
     err = pnq.device_error()
     if err:

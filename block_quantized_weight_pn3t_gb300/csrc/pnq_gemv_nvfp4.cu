@@ -204,7 +204,7 @@ struct NvMma {
     }
 };
 
-// ---- row-stream path (M <= 4) ------------------------------------------------------------------
+// ---- row-stream path (M <= 8) ------------------------------------------------------------------
 //
 // The structure of the PN row stream (pnq_gemv_pn.cu): each CTA owns whole rows; a stage is a
 // 16-row group of one K segment (all units of a short row, or a near-equal share of a long one),
@@ -220,6 +220,7 @@ constexpr int kNrProducers = 2;
 constexpr int kNrThreads = 32 * (kNrWarps + kNrProducers);
 constexpr int kNrMaxSeg = 32;
 constexpr int kNrMaxStages = 8;
+constexpr int kNrMaxM = 8;  // activation rows (one n8 tile: a column per row)
 constexpr uint32_t kNrSmem = 226u * 1024u;
 constexpr int nr_pitch(int bytes) { return ((bytes / 16) & 1) ? bytes : bytes + 16; }
 
@@ -325,7 +326,7 @@ __global__ void __launch_bounds__(kNrThreads, 1) nv_rows_kernel(const __grid_con
     const uint32_t xfull = bar0 + 8u * (2 * S), xreq = bar0 + 8u * (2 * S + 1);
     auto stage = [&](int s) { return base + a.off_stage + static_cast<uint32_t>(s) * a.stage_bytes; };
     auto rec = [&](int u) { return base + a.off_rec + static_cast<uint32_t>(u) * REC; };
-    auto so = [&](int u) { return reinterpret_cast<float*>(base + a.off_so) + u * 4; };
+    auto so = [&](int u) { return reinterpret_cast<float*>(base + a.off_so) + u * kNrMaxM; };
     __shared__ int seg_tab[kNrMaxSeg + 1];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t r0 = static_cast<int64_t>(cid) * a.N / a.G, r1 = static_cast<int64_t>(cid + 1) * a.N / a.G;
@@ -509,7 +510,7 @@ bool nr_plan(int64_t N, int Ut, int M, int sms, NrArgs& a, uint32_t& total, int 
     a.rows_pad = static_cast<int>((rows_max + kGroupRows - 1) / kGroupRows * kGroupRows);
     a.off_rec = align_up(8u * (2u * kNrMaxStages + 2), 128);
     a.off_so = align_up(a.off_rec + static_cast<uint32_t>(U) * REC, 16);
-    a.off_x = align_up(a.off_so + static_cast<uint32_t>(U) * 16u, 16);
+    a.off_x = align_up(a.off_so + static_cast<uint32_t>(U) * kNrMaxM * 4u, 16);
     a.off_part = align_up(a.off_x + static_cast<uint32_t>(M) * U * kUnitK * 2u, 16);
     a.off_stage = align_up(a.off_part + kNrWarps * static_cast<uint32_t>(M * a.rows_pad) * 4u, 128);
     const int cap[4] = {20, 8, 6, 4};
@@ -698,13 +699,15 @@ cudaError_t launch_nvfp4_gemv_mma(const Nvfp4View& w, int64_t N, int64_t K, cons
     std::call_once(once, [] { env_cluster_config("PNQ_NV_CFG", env); });
     const int req[3] = {c_req > 0 ? c_req : env[0], s_req > 0 ? s_req : env[1], env[2]};
     const int U = static_cast<int>(K / kUnitK);
-    // the row stream when a CTA's units' B records and x fit beside the ring (M <= 4)
-    if (M <= 4 && c_req <= 0 && env[0] == 0 && env[1] == 0) {
+    // the row stream when a CTA's units' B records and x fit beside the ring (M <= 8: one column
+    // per activation row, so one n8 tile)
+    if (M <= 8 && c_req <= 0 && env[0] == 0 && env[1] == 0) {
         const int cl = env[3];
         const cudaError_t e = (M == 1)   ? launch_nv_rows<4>(w, N, K, X, M, Y, err, static_weights, cl, stream)
                               : (M == 2) ? launch_nv_rows<8>(w, N, K, X, M, Y, err, static_weights, cl, stream)
                               : (M == 3) ? launch_nv_rows<12>(w, N, K, X, M, Y, err, static_weights, cl, stream)
-                                         : launch_nv_rows<16>(w, N, K, X, M, Y, err, static_weights, cl, stream);
+                              : (M == 4) ? launch_nv_rows<16>(w, N, K, X, M, Y, err, static_weights, cl, stream)
+                                         : launch_nv_rows<32>(w, N, K, X, M, Y, err, static_weights, cl, stream);
         if (e != cudaErrorNotSupported) return e;
     }
     if (M <= 8) return launch_nt<1>(maps, w.g, X, Y, err, N, K, M, U, req, static_weights, stream);

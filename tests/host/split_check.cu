@@ -293,7 +293,7 @@ void check_nr_plan(int64_t N, int Ut, int M, int CL = 1, int max_cl = 0) {
     };
     std::vector<R> r = {{0, 8ull * (2 * a.S + 2), "barriers"},
                         {a.off_rec, a.off_rec + 1ull * U * REC, "B records"},
-                        {a.off_so, a.off_so + 16ull * U, "unit scales"},
+                        {a.off_so, a.off_so + 4ull * pnq::kNrMaxM * U, "unit scales"},
                         {a.off_x, a.off_x + 2ull * M * U * 256, "x"},
                         {a.off_part, a.off_part + 4ull * pnq::kNrWarps * M * a.rows_pad, "row partials"},
                         {a.off_stage, a.off_stage + 1ull * a.S * a.stage_bytes, "stages"}};
@@ -376,6 +376,7 @@ int main() {
                     check_nr_plan<8>(N, U, 2, CL, mc);
                     check_nr_plan<12>(N, U, 3, CL, mc);
                     check_nr_plan<16>(N, U, 4, CL, mc);
+                    for (int M = 5; M <= 8; ++M) check_nr_plan<32>(N, U, M, CL, mc);
                 }
     if (failures) return 1;
     std::printf("ok %ld plans, %ld splits\n", plans, splits);
