@@ -529,17 +529,21 @@ bool nr_plan(int64_t N, int Ut, int M, int sms, NrArgs& a, uint32_t& total, int 
     return false;
 }
 
-// Estimated time (us) of an NVFP4 row-stream plan, fitted like the PN one: ~2.5 us until the
-// first stage is multiplied, 0.2 us per further round of operand builds, the longer of the dealt
-// tasks (0.5 us per 16 rows x one 256-weight unit) and the weight stream (35 GB/s per SM), and
-// 1.5 us for a cluster's final sum.
+// Estimated time (us) of an NVFP4 row-stream plan, fitted like the PN one to both NVFP4 shapes
+// at M = 1, 2, 4, 8 with every cluster size forced: ~2.5 us until the first stage is multiplied,
+// 0.2 us per further round of operand builds, the longer of the dealt tasks (0.5 us per 16 rows
+// x one 256-weight unit) and the weight stream, and 1.5 us for a cluster's final sum. The stream
+// takes at least ~0.8 us per stage however small its copies (each stage is 32 of them), and
+// runs at 35 GB/s per SM or at the ring's pace when that is slower: the S - 1 stages in flight
+// over a ~1.8 us round trip.
 inline double nr_cost(const NrArgs& a, int64_t N, int Ut, int M) {
     const int U = (Ut + a.CL - 1) / a.CL;
     const int64_t rows = (N + a.G - 1) / a.G;
     const int64_t groups = (rows + kGroupRows - 1) / kGroupRows;
     const double tasks = static_cast<double>((groups * U + kNrWarps - 1) / kNrWarps);
     const double builds = static_cast<double>((U * M + kNrWarps - 1) / kNrWarps);
-    const double stream = static_cast<double>(rows) * U * 144.0 / 35e3;
+    const double rate = std::min(35e3, std::max(1, a.S - 1) * static_cast<double>(a.stage_bytes) / 1.8);  // bytes / us
+    const double stream = std::max(static_cast<double>(rows) * U * 144.0 / rate, 0.8 * static_cast<double>(groups * a.nseg));
     return 2.5 + 0.2 * (builds - 1.0) + std::max(0.5 * tasks, stream) + (a.CL > 1 ? 1.5 : 0.0);
 }
 

@@ -838,7 +838,8 @@ cudaError_t launch_rows_kernel(const RsArgs& a, const RsPlan& p, cudaStream_t st
 // per further (unit, activation row) operand build of the busiest warp (whole rows: warp w builds
 // units w, w + 8, ..; segments: the builds are dealt evenly); then the longer of the busiest
 // consumer warp's tasks (0.65 us per 16 rows x one unit) and the CTA's weight stream (35 GB/s per
-// SM); plus 1.5 us for a cluster's final sum and 4 us for segments (all builds before any task).
+// SM, and at least ~0.8 us per stage of 16 copies however small they are); plus 1.5 us for a
+// cluster's final sum and 4 us for segments (all builds before any task).
 inline double rs_cost(const RsPlan& p, int64_t N, int Ut, int M, int NT = 1) {
     const int U = (Ut + p.CL - 1) / p.CL;
     const int64_t rows = (N + p.G - 1) / p.G;
@@ -848,7 +849,7 @@ inline double rs_cost(const RsPlan& p, int64_t N, int Ut, int M, int NT = 1) {
     const double tasks = seg ? static_cast<double>((groups * U + kRsWarps - 1) / kRsWarps)
                              : static_cast<double>(groups * per_warp);
     const double builds = seg ? static_cast<double>((U * M + kRsWarps - 1) / kRsWarps) : static_cast<double>(per_warp * M);
-    const double stream = static_cast<double>(rows) * U * kUnitBytes / 35e3;
+    const double stream = std::max(static_cast<double>(rows) * U * kUnitBytes / 35e3, 0.8 * static_cast<double>(groups * p.nseg));
     const double per_task = NT == 1 ? 0.65 : 0.65 * 1.4;  // a second n8 tile shares the decode
     return 2.5 + 0.35 * (builds - 1.0) + std::max(per_task * tasks, stream) + (p.CL > 1 ? 1.5 : 0.0) +
            (seg ? 4.0 : 0.0);
