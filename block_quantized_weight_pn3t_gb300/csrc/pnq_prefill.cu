@@ -144,6 +144,7 @@ struct GemmArgs {
     float* Y;
     int* err;
     int M, rows, K, S;  // activation rows, weight rows of the slice, K, stages
+    int ks;             // K split over a cluster of ks CTAs along z (1: none)
     int64_t ldy, n0;    // Y row stride (N) and the slice's first weight row
 };
 
@@ -171,7 +172,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tf32_gemm_kernel(const __grid
     auto stage = [&](int s) { return smem_addr(base) + static_cast<uint32_t>(s * kStage); };
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int row0 = blockIdx.x * kTM, col0 = blockIdx.y * BN;
-    const int nk = (a.K + kTK - 1) / kTK;
+    // this CTA's K tiles [kt0, kt0 + nk): share blockIdx.z of a.ks (every share holds at least one)
+    const int nk_all = (a.K + kTK - 1) / kTK, kz = static_cast<int>(blockIdx.z);
+    const int kt0 = kz * nk_all / a.ks, nk = (kz + 1) * nk_all / a.ks - kt0;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -199,11 +202,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tf32_gemm_kernel(const __grid
                     break;
                 }
                 const uint32_t st = stage(s);
+                const int kx = (kt0 + kt) * kTK;
                 mbar_arrive_expect_tx(full(s), static_cast<uint32_t>(kStage));
-                tma_load_2d(st, &mwh, kt * kTK, row0, full(s), pol_w);
-                tma_load_2d(st + kATile, &mwl, kt * kTK, row0, full(s), pol_w);
-                tma_load_2d(st + 2 * kATile, &mxh, kt * kTK, col0, full(s), pol_x);
-                tma_load_2d(st + 2 * kATile + kBTile, &mxl, kt * kTK, col0, full(s), pol_x);
+                tma_load_2d(st, &mwh, kx, row0, full(s), pol_w);
+                tma_load_2d(st + kATile, &mwl, kx, row0, full(s), pol_w);
+                tma_load_2d(st + 2 * kATile, &mxh, kx, col0, full(s), pol_x);
+                tma_load_2d(st + 2 * kATile + kBTile, &mxl, kx, col0, full(s), pol_x);
             }
             if (!ok) record_error(a.err, kErrEmptyWait);
             bool drained = true;  // every copy issued has landed before the CTA may exit
@@ -243,7 +247,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tf32_gemm_kernel(const __grid
         tc_fence_after();
         if (!ok) {
             if (lane == 0) record_error(a.err, kErrFullWait);
-        } else {
+        } else if (a.ks == 1) {
 #pragma unroll 1
             for (int c0 = 0; c0 < BN; c0 += 16) {
                 uint32_t v[16];
@@ -257,10 +261,42 @@ __global__ void __launch_bounds__(kGemmThreads, 1) tf32_gemm_kernel(const __grid
                     }
                 }
             }
+        } else {
+            // the partial tile to shared memory (the stages are free: every MMA has completed),
+            // rows kRedPitch floats apart
+            float* red = reinterpret_cast<float*>(base);
+#pragma unroll 1
+            for (int c0 = 0; c0 < BN; c0 += 16) {
+                uint32_t v[16];
+                tmem_ld<16>(tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(c0), v);
+                tmem_wait_ld();
+                float4* dst = reinterpret_cast<float4*>(red + (32 * q + lane) * (BN + 4) + c0);
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    dst[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                         __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+            }
         }
         tc_fence_before();
     }
     __syncthreads();
+    if (a.ks > 1) {
+        // CTA kz of the cluster sums its share of the tile's rows over the ks partial tiles, in
+        // CTA order (distributed shared memory), and writes Y
+        cluster_sync();
+        const int share = kTM / a.ks + (kTM % a.ks ? 1 : 0);
+        const int rl0 = kz * share, rl1 = min(kTM, rl0 + share);
+        const uint32_t rbase = smem_addr(base);
+        for (int e = static_cast<int>(threadIdx.x); e < (rl1 - rl0) * BN; e += kGemmThreads) {
+            const int rl = rl0 + e % (rl1 - rl0), c = e / (rl1 - rl0);
+            const uint32_t off = 4u * static_cast<uint32_t>(rl * (BN + 4) + c);
+            float v = 0.0f;
+            for (int z = 0; z < a.ks; ++z) v += ld_dsmem_f32(rbase + off, static_cast<uint32_t>(z));
+            const int r = row0 + rl, m = col0 + c;
+            if (r < a.rows && m < a.M) a.Y[static_cast<int64_t>(m) * a.ldy + a.n0 + r] = v;
+        }
+        cluster_sync();  // no CTA leaves while another still reads its tile
+    }
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, kCols);
@@ -273,6 +309,8 @@ cudaError_t launch_gemm_bn(const CUtensorMap (&maps)[4], const GemmArgs& a0, cud
     GemmArgs a = a0;
     a.S = static_cast<int>(std::min<size_t>(8, (kGemmSmemLimit - 1024 - 1024) / kStage));
     if (a.S < 2) return cudaErrorNotSupported;
+    // the stages also hold a K-split cluster's partial tile (128 rows of BN + 4 floats)
+    if (a.ks > 1 && static_cast<size_t>(a.S) * kStage < static_cast<size_t>(kTM) * (BN + 4) * 4) return cudaErrorNotSupported;
     const int smem = a.S * kStage + 1024;
     auto kern = tf32_gemm_kernel<BN>;
     static std::atomic<bool> opted[64];
@@ -285,9 +323,19 @@ cudaError_t launch_gemm_bn(const CUtensorMap (&maps)[4], const GemmArgs& a0, cud
         if (e != cudaSuccess) return e;
         opted[dev].store(true, std::memory_order_relaxed);
     }
-    const dim3 grid((a.rows + kTM - 1) / kTM, (a.M + BN - 1) / BN);
-    kern<<<grid, kGemmThreads, smem, stream>>>(maps[0], maps[1], maps[2], maps[3], a);
-    return cudaGetLastError();
+    cudaLaunchConfig_t lc{};
+    lc.gridDim = dim3((a.rows + kTM - 1) / kTM, (a.M + BN - 1) / BN, a.ks);
+    lc.blockDim = dim3(kGemmThreads, 1, 1);
+    lc.dynamicSmemBytes = smem;
+    lc.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = static_cast<unsigned>(a.ks);
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+    return cudaLaunchKernelEx(&lc, kern, maps[0], maps[1], maps[2], maps[3], a);
 }
 
 }  // namespace
@@ -343,6 +391,14 @@ cudaError_t launch_pn_prefill(int type, const uint8_t* W, int64_t N, int64_t K, 
         a.K = static_cast<int>(K);
         a.ldy = N;
         a.n0 = n0;
+        // K split over a cluster while the slice's tiles would fill fewer SMs than they could
+        // (every share keeps at least 8 K tiles)
+        {
+            const int64_t tiles = (rr + kTM - 1) / kTM * ((M + bn - 1) / bn);
+            const int64_t nk = (K + kTK - 1) / kTK;
+            a.ks = 1;
+            while (a.ks < 8 && tiles * (a.ks + 1) <= sms && nk >= 8 * (a.ks + 1)) ++a.ks;
+        }
         e = (bn == 32) ? launch_gemm_bn<32>(maps, a, stream)
             : (bn == 64) ? launch_gemm_bn<64>(maps, a, stream)
                          : launch_gemm_bn<128>(maps, a, stream);
