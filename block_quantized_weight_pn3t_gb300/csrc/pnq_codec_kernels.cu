@@ -127,6 +127,45 @@ __global__ void __launch_bounds__(kThreads) nvfp4_dequant_kernel(const uint8_t* 
     }
 }
 
+// Staged NVFP4 dequantize for 16-byte aligned codes, scales and output: a warp takes 1024
+// consecutive weights at a time (512 code bytes, 64 scale bytes), copies them to shared memory
+// with 16-byte loads, then lane l writes float4 j = l, l + 32, .. of the chunk's output: weights
+// 4j .. 4j + 3, code bytes 2j and 2j + 1, scale byte j / 4. Every warp load and store covers
+// 512 contiguous bytes. Whole chunks only (the caller runs the rest through the kernel above).
+constexpr int kNvChunk = 1024;  // weights per warp chunk
+
+template <bool DIV>
+__global__ void __launch_bounds__(kThreads) nvfp4_dequant_staged_kernel(const uint8_t* __restrict__ codes,
+                                                                          const uint8_t* __restrict__ scales, float g,
+                                                                          int64_t nchunks, float* __restrict__ out) {
+    __shared__ __align__(16) uint8_t stage[kThreads / 32][kNvChunk / 2 + kNvChunk / 16];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    uint8_t* sb = stage[warp];
+    const int64_t wstride = static_cast<int64_t>(gridDim.x) * (kThreads / 32);
+    for (int64_t ch = static_cast<int64_t>(blockIdx.x) * (kThreads / 32) + warp; ch < nchunks; ch += wstride) {
+        reinterpret_cast<uint4*>(sb)[lane] = __ldg(reinterpret_cast<const uint4*>(codes) + ch * 32 + lane);
+        if (lane < 4)
+            reinterpret_cast<uint4*>(sb + kNvChunk / 2)[lane] = __ldg(reinterpret_cast<const uint4*>(scales) + ch * 4 + lane);
+        __syncwarp();
+        float4* o = reinterpret_cast<float4*>(out) + ch * (kNvChunk / 4);
+#pragma unroll
+        for (int k = 0; k < kNvChunk / 4 / 32; ++k) {
+            const int j = lane + 32 * k;
+            const uint32_t c = *reinterpret_cast<const unsigned short*>(sb + 2 * j);
+            const float s = e4m3_to_f32(sb[kNvChunk / 2 + (j >> 2)]);
+            float v[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                // e2m1 * e4m3 is exact in fp32; the product with (quotient by) g is the single rounding
+                const float p = e2m1_to_f32((c >> (4 * q)) & 15u) * s;
+                v[q] = DIV ? __fdiv_rn(p, g) : __fmul_rn(p, g);
+            }
+            o[j] = make_float4(v[0], v[1], v[2], v[3]);
+        }
+        __syncwarp();
+    }
+}
+
 // One warp per row. Half h of a row is half h mod 17 of its block (half 0: d, invalid if its
 // exponent field is all ones; halves 1..16: word halves, whose bit 15 — word bits 15 and 31 — is
 // reserved in pn3t). With 16-byte aligned rows (W aligned, row length a multiple of 16 bytes) a
@@ -233,10 +272,37 @@ cudaError_t launch_pn_dequant(int type, const uint8_t* W, int64_t n_rows, int64_
     return cudaGetLastError();
 }
 
+// NVFP4 dequantize of npairs code-byte pairs from w's pointers, by the pair-per-thread kernel.
+cudaError_t launch_nvfp4_dequant_pairs(const Nvfp4View& w, int64_t npairs, float* out, cudaStream_t stream);
+
 cudaError_t launch_nvfp4_dequant(const Nvfp4View& w, int64_t n_rows, int64_t K, float* out,
                                  cudaStream_t stream) {
     const int64_t npairs = n_rows * (K / 4);
     if (npairs == 0) return cudaSuccess;
+    // whole 1024-weight chunks through the staged kernel when everything is 16-byte aligned
+    if (aligned16(w.codes) && aligned16(w.scales) && aligned16(out)) {
+        const int64_t nchunks = npairs * 4 / kNvChunk;
+        if (nchunks > 0) {
+            const int g2 = grid_for(nchunks * 32, 1);
+            if (w.div)
+                nvfp4_dequant_staged_kernel<true><<<g2, kThreads, 0, stream>>>(w.codes, w.scales, w.g, nchunks, out);
+            else
+                nvfp4_dequant_staged_kernel<false><<<g2, kThreads, 0, stream>>>(w.codes, w.scales, w.g, nchunks, out);
+            const cudaError_t e = cudaGetLastError();
+            if (e != cudaSuccess) return e;
+        }
+        const int64_t done = nchunks * kNvChunk;  // weights written
+        const int64_t rest = npairs - done / 4;
+        if (rest == 0) return cudaSuccess;
+        Nvfp4View tail = w;
+        tail.codes = w.codes + done / 2;
+        tail.scales = w.scales + done / 16;
+        return launch_nvfp4_dequant_pairs(tail, rest, out + done, stream);
+    }
+    return launch_nvfp4_dequant_pairs(w, npairs, out, stream);
+}
+
+cudaError_t launch_nvfp4_dequant_pairs(const Nvfp4View& w, int64_t npairs, float* out, cudaStream_t stream) {
     const int grid = grid_for(npairs, kNvUnroll);
     const bool vec = (reinterpret_cast<uintptr_t>(w.codes) & 1u) == 0 && aligned16(out);
     if (w.div) {
