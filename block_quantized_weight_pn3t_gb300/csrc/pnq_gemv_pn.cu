@@ -3,12 +3,12 @@
 // Computes Y[m][n] = sum_k w[n][k] x[m][k] for 1 <= M <= 16, with w = d * (n - z) decoded in
 // registers from the 34-byte blocks of the "PN weight format" page (sections Block layout and
 // Value) just before the multiply. A K unit is 8 blocks (272 bytes of a row). Two pipelines:
-//   - the row stream (M <= 4; below): each CTA owns whole rows, stages of 16 rows (or of a K
-//     segment of 16 rows) arrive by one 1-D bulk copy per row, B operands of every unit stay in
-//     shared memory;
+//   - the row stream (M <= 8; below): clusters of 1..8 CTAs own rows, each CTA a share of their
+//     K units; stages of 16 rows (or of a K segment of 16 rows) arrive by one 1-D bulk copy per
+//     row, and the B operands of the CTA's units stay in shared memory;
 //   - the cluster strip pipeline (pnq_cluster.cuh, with this file's PnMma policy): 2-D tensor-map
 //     copies of 8- and 64-row strips of a unit, clusters of one or two CTAs sharing row tiles and
-//     summing through distributed shared memory; it takes M = 5..16 and the M <= 4 shapes whose B
+//     summing through distributed shared memory; it takes M = 9..16 and the M <= 8 shapes whose B
 //     operands do not fit beside a row-stream ring.
 //
 // Decode and multiply. A 32-bit word of a block holds two codes at the same shift in its two
@@ -343,10 +343,15 @@ struct PnMma {
     }
 };
 
-// ---- row-stream path (M <= 4) ----------------------------------------------------------------------
+// ---- row-stream path (M <= 8) ----------------------------------------------------------------------
 //
-// Each CTA owns a contiguous range of whole rows, so nothing is summed across CTAs. A stage holds
-// 16 rows of the CTA (a row group): sixteen 1-D bulk copies, one per row, issued by the lanes of two
+// A cluster of CL CTAs (CL = 1, 2, 4 or 8, chosen by rs_cost below) owns a contiguous range of
+// rows; CTA r of the cluster takes K units [r U / CL, (r + 1) U / CL) of those rows: it streams
+// only those bytes of each row, builds only those units' operands from only that slice of x, and
+// at the end the cluster sums the CTAs' partial rows through distributed shared memory in CTA
+// order (CL = 1: nothing is summed across CTAs). M <= 4 uses one n8 tile per task (columns 2m,
+// 2m + 1), M = 5..8 two (one decoded A fragment, two MMAs). A stage holds 16 rows of the CTA's
+// units (a row group): sixteen 1-D bulk copies, one per row, issued by the lanes of two
 // producer warps, eight rows each (copies issued from two warps stream at the full HBM rate, one
 // warp's at about two thirds of it; 2-D boxes of 272-byte strips stream far slower). A stage row
 // is `pitch` bytes apart: its length, padded by 16 bytes where needed so that pitch / 16 is odd,
@@ -378,6 +383,9 @@ struct PnMma {
 // The SM takes in bulk copies at about the HBM rate per SM, in issue order, so x requested after
 // the producer has filled the ring would land only behind all of it. The producer therefore issues
 // one stage, then waits until every consumer warp has requested its x, and fills the ring behind.
+// x is read only while the operands are built, so the plan may place it in the ring's last slots
+// (slot 2 or later): the producer fills those only after every consumer warp has arrived on the
+// "operands built" barrier.
 
 constexpr int kRsWarps = 8;      // consumer warps
 constexpr int kRsProducers = 2;  // producer warps, rows 0..7 and 8..15 of each group
