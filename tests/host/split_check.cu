@@ -13,7 +13,9 @@
 //   - the row-stream plan (rs_plan): its regions are disjoint, aligned and inside one CTA's budget,
 //     every row segment's bulk copies are 16-byte aligned and land inside their stage, the
 //     segments of a row tile its units in order, and the dealing of (row group, unit) tasks to the
-//     consumer warps gives every task to exactly one warp, each warp the same count to within one.
+//     consumer warps gives every task to exactly one warp, each warp the same count to within one;
+//   - the row streams' cost estimates pick, for the decode-step projections and both NVFP4 shapes,
+//     the K-splitting cluster size that timed fastest on a GB300 with every size forced.
 // Host code only: the kernels are compiled but never launched.
 #include "pnq_gemv_pn.cu"
 #include "pnq_gemv_nvfp4.cu"
@@ -352,7 +354,74 @@ void run_rows() {
 
 }  // namespace
 
+// The planner's choice of K-splitting cluster size for the decode-step projections and both NVFP4
+// shapes, with the resident-cluster counts of a GB300 at ~210 KB per CTA (76 / 36 / 15 clusters
+// of 2 / 4 / 8): the sizes that timed fastest with every size forced.
+void check_cluster_choices() {
+    auto resident = [](int CL, const pnq::RsPlan&) { return CL == 2 ? 76 : CL == 4 ? 36 : 15; };
+    struct Pn {
+        int type, M, U;
+        int64_t N;
+        int want;
+    };
+    const Pn pn[] = {{pnq::kTypePn3t, 1, 8, 12288, 1},  {pnq::kTypePn4t, 1, 10, 1024, 1},
+                     {pnq::kTypePn4t, 1, 12, 5120, 1},  {pnq::kTypePn3t, 1, 8, 17408, 1},
+                     {pnq::kTypePn4t, 1, 34, 5120, 4},  {pnq::kTypePn4t, 2, 34, 5120, 4},
+                     {pnq::kTypePn3t, 4, 8, 17408, 1},  {pnq::kTypePn4t, 4, 12, 5120, 2},
+                     {pnq::kTypePn4t, 4, 10, 1024, 2},  {pnq::kTypePn4t, 4, 34, 5120, 4}};
+    for (const Pn& c : pn) {
+        char what[96];
+        std::snprintf(what, sizeof what, "cluster choice type %d M %d N %lld U %d", c.type, c.M, (long long)c.N, c.U);
+        pnq::RsPlan p;
+        bool ok = false;
+        if (c.type == pnq::kTypePn3t) {
+            ok = c.M == 1   ? pnq::rs_best_plan<pnq::kTypePn3t, 8, 1>(c.N, c.U, c.M, 152, 0, false, true, 0, p, resident)
+                 : c.M == 2 ? pnq::rs_best_plan<pnq::kTypePn3t, 16, 1>(c.N, c.U, c.M, 152, 0, false, true, 0, p, resident)
+                            : pnq::rs_best_plan<pnq::kTypePn3t, 32, 1>(c.N, c.U, c.M, 152, 0, false, true, 0, p, resident);
+        } else {
+            ok = c.M == 1   ? pnq::rs_best_plan<pnq::kTypePn4t, 8, 1>(c.N, c.U, c.M, 152, 0, false, true, 0, p, resident)
+                 : c.M == 2 ? pnq::rs_best_plan<pnq::kTypePn4t, 16, 1>(c.N, c.U, c.M, 152, 0, false, true, 0, p, resident)
+                            : pnq::rs_best_plan<pnq::kTypePn4t, 32, 1>(c.N, c.U, c.M, 152, 0, false, true, 0, p, resident);
+        }
+        ++plans;
+        if (!ok) FAIL("no plan");
+        else if (p.CL != c.want) FAIL("clusters of %d, the fastest measured were %d", p.CL, c.want);
+    }
+    struct Nv {
+        int M;
+        int64_t N;
+        int K, want;
+    };
+    const Nv nv[] = {{1, 17408, 5120, 1}, {1, 5120, 17408, 4}, {2, 17408, 5120, 1}, {2, 5120, 17408, 4},
+                     {4, 17408, 5120, 2}, {4, 5120, 17408, 4}, {8, 17408, 5120, 2}, {8, 5120, 17408, 8}};
+    for (const Nv& c : nv) {
+        char what[96];
+        std::snprintf(what, sizeof what, "nvfp4 cluster choice M %d N %lld K %d", c.M, (long long)c.N, c.K);
+        const int U = c.K / 256;
+        double best = 0.0;
+        int pick = 0;
+        for (int CL : {1, 2, 4, 8}) {
+            pnq::NrArgs a{};
+            uint32_t t = 0;
+            const int mc = CL == 2 ? 76 : CL == 4 ? 36 : CL == 8 ? 15 : 0;
+            const bool ok = c.M == 1   ? pnq::nr_plan<4>(c.N, U, c.M, 152, a, t, CL, mc)
+                            : c.M == 2 ? pnq::nr_plan<8>(c.N, U, c.M, 152, a, t, CL, mc)
+                            : c.M == 4 ? pnq::nr_plan<16>(c.N, U, c.M, 152, a, t, CL, mc)
+                                       : pnq::nr_plan<32>(c.N, U, c.M, 152, a, t, CL, mc);
+            if (!ok) continue;
+            const double cost = pnq::nr_cost(a, c.N, U, c.M);
+            if (pick == 0 || cost < best) {
+                best = cost;
+                pick = CL;
+            }
+        }
+        ++plans;
+        if (pick != c.want) FAIL("clusters of %d, the fastest measured were %d", pick, c.want);
+    }
+}
+
 int main() {
+    check_cluster_choices();
     // the split alone, over grids the planner does not pick
     for (int64_t N : {1, 8, 9, 63, 64, 65, 1000, 5120, 17408})
         for (int U : {1, 3, 34})
