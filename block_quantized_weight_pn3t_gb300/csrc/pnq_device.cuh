@@ -16,7 +16,6 @@ namespace pnq {
 constexpr int kBlockBytes = 34;
 constexpr int kTypePn3t = 124;
 constexpr int kTypePn4t = 125;
-constexpr int kTypeNvfp4 = 1004;
 // grouped signed-integer formats of NInfer "tensor-formats.md" (library ids)
 constexpr int kTypeQ4G64 = 1104;
 constexpr int kTypeQ5G64 = 1105;

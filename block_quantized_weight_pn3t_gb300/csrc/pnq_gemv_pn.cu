@@ -61,8 +61,6 @@ struct Cfg {
     static constexpr int JS = (TYPE == kTypePn3t) ? 3 : 2;  // pairs below the shift
 };
 
-__device__ __forceinline__ uint32_t lds32(const uint8_t* p) { return *reinterpret_cast<const uint32_t*>(p); }
-
 // fp16 in the low / high half of a word -> fp32
 __device__ __forceinline__ float half_lo(uint32_t w) { return __half2float(__ushort_as_half(static_cast<unsigned short>(w))); }
 __device__ __forceinline__ float half_hi(uint32_t w) {
