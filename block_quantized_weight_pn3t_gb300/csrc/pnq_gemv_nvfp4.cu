@@ -3,9 +3,11 @@
 // Computes Y[m][n] = sum_k w[n][k] x[m][k] for 1 <= M <= 16 with w = e2m1(code) * e4m3(scale) * g
 // ("Quantisation and profiles", NVFP4; tensor-formats page, NVFP4 / E2M1 / E4M3FN): codes two per
 // byte, low nibble = even k, one E4M3FN scale per 16 weights along K, one fp32 global multiplier;
-// x is bf16. The weights are decoded in registers just before the multiply. The pipeline (cluster
-// work split, weight stream, operand builders, on-chip reduction) is pnq_cluster.cuh; this file is
-// the NVFP4 format policy.
+// x is bf16. The weights are decoded in registers just before the multiply. Two paths:
+//   - M <= 8: the row stream of this file (nv_rows_kernel, below);
+//   - M = 9..16, and M <= 8 shapes whose row plan does not fit in shared memory: the strip
+//     pipeline (cluster work split, weight stream, operand builders, on-chip reduction) of
+//     pnq_cluster.cuh, with this file's NVFP4 format policy, described next.
 //
 // Unit and stage. A K unit is 256 weights of a row: 128 code bytes and 16 scale bytes. An 8-row
 // piece is two tensor-map copies: the codes (8 rows x 128 bytes, with the 128-byte swizzle:
@@ -213,7 +215,10 @@ struct NvMma {
 // (the eight rows a warp reads at once then fall in different banks; no swizzle is needed). All
 // of x (bf16 [M][K]) comes in with one bulk copy per activation row; the consumer warps build the
 // B operands of every unit between them (records of the 4M lanes whose columns are live) and the
-// (row group, unit) tasks of the stages are dealt to them in turn.
+// (row group, unit) tasks of the stages are dealt to them in turn. Clusters of CL = 1, 2, 4 or 8
+// CTAs may split K: CTA r of a cluster streams, builds and multiplies only units
+// [r U / CL, (r + 1) U / CL) of the cluster's rows, and CTA r writes a share of the rows, adding
+// every CTA's row sums in CTA order through distributed shared memory (deterministic).
 
 constexpr int kNrWarps = 8;
 constexpr int kNrProducers = 2;
